@@ -1,0 +1,63 @@
+"""Oracle of the VRAM expert-slot cache's replacement policy (plain Python).
+
+TEST INFRASTRUCTURE ONLY.
+
+The page "8GB 笔记本 39.3 tok/s、单卡跑 753B：FreeToken 把 frontier MoE 拉回本地"
+(section 设计核心, second principle) keeps a global LRU cache of experts in
+VRAM: adjacent tokens route to overlapping experts, so most routed accesses
+hit and only misses are filled from host memory.  It does not fix the
+details, so this oracle states them:
+
+* one cache per layer with ``slots`` slots, initially empty;
+* a token's k experts are visited in ascending expert id;
+* a hit sets the expert's last-use stamp to the current step;
+* a miss takes the lowest-index free slot if there is one, otherwise evicts
+  the slot with the oldest stamp among experts the current token does not
+  select, the lower slot index winning a tie; the new expert's stamp is the
+  current step.
+"""
+from __future__ import annotations
+
+
+class LayerLRU:
+    def __init__(self, slots: int):
+        if slots <= 0:
+            raise ValueError("slots must be positive")
+        self.slots = slots
+        self.expert_of = [-1] * slots   # slot -> expert, -1 when free
+        self.stamp = [-1] * slots       # slot -> step of last use
+        self.slot_of = {}               # expert -> slot
+
+    def access(self, step: int, ids):
+        """Process one token's expert ids; returns (slots, misses) in the order of ``ids``.
+
+        ``misses`` is the list of (expert, slot) pairs the caller must fill,
+        in ascending expert order.
+        """
+        ids = [int(e) for e in ids]
+        if len(set(ids)) != len(ids):
+            raise ValueError("a token selects each expert at most once")
+        if len(ids) > self.slots:
+            raise ValueError("more experts per token than slots")
+        current = set(ids)
+        result = {}
+        misses = []
+        for e in sorted(ids):
+            if e in self.slot_of:
+                s = self.slot_of[e]
+                self.stamp[s] = step
+                result[e] = s
+                continue
+            free = [s for s in range(self.slots) if self.expert_of[s] < 0]
+            if free:
+                s = free[0]
+            else:
+                cands = [s for s in range(self.slots) if self.expert_of[s] not in current]
+                s = min(cands, key=lambda q: (self.stamp[q], q))
+                del self.slot_of[self.expert_of[s]]
+            self.expert_of[s] = e
+            self.stamp[s] = step
+            self.slot_of[e] = s
+            result[e] = s
+            misses.append((e, s))
+        return [result[e] for e in ids], misses
