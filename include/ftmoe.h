@@ -1,0 +1,232 @@
+/*
+ * ftmoe.h -- C ABI of the sparse Mixture-of-Experts layer step over NVFP4
+ * expert weights, for NVIDIA B300 (sm_103a).
+ *
+ * The step, as the FreeToken pages state the problem:
+ *   router softmax + top-k  ->  token-to-expert permutation  ->  expert SwiGLU
+ *   FFN over 4-bit block-quantised weights  ->  routing-weighted combine,
+ * plus a VRAM expert-slot cache filled from pinned host memory.
+ * Sources (cited per function below):
+ *   [P4] page "FreeToken：753B大模型塞进单卡的本地部署硬件账该怎么算", paragraph
+ *        on the MoE core mechanism (MoE的核心机制): router = linear + softmax,
+ *        top-K experts, weighted outputs; each expert an independent FFN;
+ *        paragraph on bandwidth-aware storage: hot experts stay in VRAM,
+ *        asynchronous cudaMemcpyAsync overlaps transfer with compute.
+ *   [P5] page "8GB 笔记本 39.3 tok/s、单卡跑 753B：FreeToken 把 frontier MoE
+ *        拉回本地": section 设计核心 (global LRU expert cache in VRAM, misses
+ *        filled from host memory), sections 实测六款消费级硬件 and 局限 (NVFP4
+ *        weights read directly).
+ *   [P3] page xxmr.cn/news/175150, section 2.2 (tokens are dispatched to the
+ *        few selected experts) and section 2.1 (dequantisation at compute time).
+ *
+ * NVFP4 (bit level): element codes E2M1 (OCP MX v1.0 FP4: values 0, .5, 1,
+ * 1.5, 2, 3, 4, 6 and their negatives), one unsigned E4M3 scale per 16
+ * consecutive elements along the reduction dimension, one fp32 scale per
+ * tensor.  Packed codes: byte j of a row holds element 2j in its low nibble
+ * and element 2j+1 in its high nibble.
+ *
+ * Conventions for every function:
+ *  - Returns ft_status; FT_OK is 0.  ft_last_error() gives a thread-local
+ *    message for the last failure.  No C++ exception crosses the ABI and no
+ *    kernel traps: data errors found on the device (NaN logits, invalid
+ *    scales, a bounded wait that ran out) set bits in a per-device error word
+ *    read by ft_device_status().
+ *  - Pointers marked (device) are device memory owned by the caller; (host)
+ *    is host memory owned by the caller.  The library allocates no device
+ *    memory on the hot path: scratch comes from a caller workspace whose size
+ *    the matching *_workspace_size() function returns.  Workspaces need
+ *    256-byte alignment.
+ *  - All device work is enqueued asynchronously on the caller's stream; the
+ *    functions do not synchronise unless stated.
+ *  - Argument errors (sizes <= 0 where a count is required, k > E, E > 1024,
+ *    k > 32, null required pointers, misaligned pointers, too-small
+ *    workspace) return FT_ERR_INVALID_ARG before anything is enqueued.
+ */
+#ifndef FTMOE_H_
+#define FTMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FT_API __attribute__((visibility("default")))
+#else
+#define FT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ft_stream_t; /* a cudaStream_t; NULL is the legacy default stream */
+typedef struct CUevent_st* ft_event_t;   /* a cudaEvent_t */
+
+typedef enum ft_status {
+    FT_OK = 0,
+    FT_ERR_INVALID_ARG = 1,
+    FT_ERR_CUDA = 2,
+    FT_ERR_UNSUPPORTED = 3,
+    FT_ERR_TIMEOUT = 4,
+    FT_ERR_NO_SLOT = 5,
+    FT_ERR_OOM = 6,
+    FT_ERR_DEVICE = 7
+} ft_status;
+
+/* Device error-word bits (ft_device_status). */
+#define FT_DEVERR_NAN_LOGIT 0x1u     /* a router logit was NaN or +inf */
+#define FT_DEVERR_BAD_SCALE 0x2u     /* an E4M3 scale byte was NaN or had its sign bit set */
+#define FT_DEVERR_TIMEOUT 0x4u       /* a bounded device wait gave up */
+#define FT_DEVERR_BAD_INDEX 0x8u     /* an expert id / slot / offset was out of range */
+
+FT_API const char* ft_status_string(ft_status s);
+/* Message for the last failure on this thread ("" if none).  The pointer stays
+ * valid until the next ft_* call on the same thread. */
+FT_API const char* ft_last_error(void);
+/* Library ABI version, (major << 16) | minor. */
+FT_API int ft_version(void);
+
+/* Waits for `stream`, then reads and clears the current device's error word.
+ * *err_word receives the FT_DEVERR_* bits; returns FT_ERR_DEVICE if any bit was
+ * set, FT_ERR_CUDA if the stream reported a CUDA error, FT_OK otherwise. */
+FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
+
+/* ------------------------------------------------------------------------ */
+/* Weights of one MoE layer                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Expert weights of one layer in device memory, in the layout the kernels read.
+ * For weight index w (the expert id, or its cache slot when expert_to_slot is
+ * given):
+ *   gate/up  codes  gu_codes  + w*gu_codes_stride  : [2I][H/2] bytes; row 2i is
+ *                   gate row i, row 2i+1 is up row i (interleaved so that one
+ *                   tile holds both halves of each SwiGLU pair)
+ *            scales gu_scales + w*gu_scales_stride : [2I][H/16] E4M3 bytes
+ *   down     codes  d_codes   + w*d_codes_stride   : [H][I/2]
+ *            scales d_scales  + w*d_scales_stride  : [H][I/16]
+ *   tensor scales  tscale + w*tscale_stride       : float {gate, up, down}
+ *   gu_sf_tiled / d_sf_tiled (optional, prefill only): the same scales
+ *            rearranged by ft_nvfp4_tile_scales(), strides gu_sf_tiled_stride /
+ *            d_sf_tiled_stride.
+ * Strides are in bytes (tscale_stride in floats).  Every base address and
+ * stride must be a multiple of 16.  expert_to_slot (device, optional, [E]
+ * int32) maps an expert id to its weight index; ids mapping to a negative or
+ * out-of-range index set FT_DEVERR_BAD_INDEX and produce zeros.
+ * Sizes: 1 <= E <= 1024 experts; H a multiple of 256; I a multiple of 128. */
+typedef struct ft_moe_layer_weights {
+    int32_t E, H, I, n_weights; /* n_weights: number of weight indices (E, or cache slots) */
+    const uint8_t* gu_codes;
+    int64_t gu_codes_stride;
+    const uint8_t* gu_scales;
+    int64_t gu_scales_stride;
+    const uint8_t* d_codes;
+    int64_t d_codes_stride;
+    const uint8_t* d_scales;
+    int64_t d_scales_stride;
+    const float* tscale;
+    int64_t tscale_stride;
+    const int32_t* expert_to_slot;
+    const uint8_t* gu_sf_tiled;
+    int64_t gu_sf_tiled_stride;
+    const uint8_t* d_sf_tiled;
+    int64_t d_sf_tiled_stride;
+} ft_moe_layer_weights;
+
+/* ------------------------------------------------------------------------ */
+/* Router                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* [P4 MoE core mechanism] Softmax over E router logits and top-k selection.
+ *   logits (device) fp32 [T][E], row-major.
+ *   ids    (device) int32 [T][k]: expert ids by decreasing logit; equal logits
+ *          go to the lower expert index.  Selection compares the fp32 logits.
+ *   w      (device) fp32 [T][k]: exp(l_j - max) / sum over the k selected,
+ *          i.e. the softmax restricted to the selected experts and
+ *          renormalised to sum to 1.  A row whose logits are all -inf gets 1/k.
+ * NaN or +inf logits set FT_DEVERR_NAN_LOGIT (outputs of that row are then
+ * unspecified).  1 <= k <= min(E, 32), E <= 1024, T >= 0. */
+FT_API ft_status ft_moe_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, ft_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Permutation                                                                */
+/* ------------------------------------------------------------------------ */
+
+FT_API size_t ft_moe_permute_workspace_size(int T, int E, int k);
+
+/* [P3 §2.2, P4] Groups the T*k (token, slot) pairs by expert: a stable
+ * counting sort of f = t*k + j by ids[f].
+ *   offsets (device) int32 [E+1]: exclusive prefix sum of the per-expert
+ *           counts; expert e owns permuted rows [offsets[e], offsets[e+1]).
+ *   perm    (device) int32 [T*k]: perm[p] = f of the p-th permuted row; rows of
+ *           one expert are in increasing f.
+ *   inv     (device) int32 [T*k]: inv[f] = p.
+ *   active  (device, optional) int32 [E+1]: active[0] = number of experts with
+ *           at least one row, active[1..] their ids ascending.
+ * Result is bit-identical to the sequential definition for any launch.
+ * ids out of [0, E) set FT_DEVERR_BAD_INDEX. */
+FT_API ft_status ft_moe_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets, int32_t* perm, int32_t* inv,
+                         int32_t* active, void* ws, size_t ws_bytes, ft_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Expert FFN                                                                 */
+/* ------------------------------------------------------------------------ */
+
+FT_API size_t ft_moe_decode_workspace_size(int T, int k, int H, int I);
+
+/* [P4 MoE core mechanism; P3 §2.1; P5 NVFP4] Decode expert FFN, bf16
+ * activations, NVFP4 weights dequantised in registers, fp32 accumulation:
+ * for each permuted row p of expert e (token t = perm[p] / k):
+ *   g = Wg x_t, u = Wu x_t, h = bf16(silu(g) * u), y_p = Wd h.
+ *   x       (device) bf16 [T][H].
+ *   offsets, perm, active: from ft_moe_permute.
+ *   y       (device, optional) fp32 [T*k][H]: per-row expert outputs.
+ *   out     (device, optional) bf16 [T][H]: if given (with inv and w), the
+ *           combine is applied: out[t] = bf16(sum_j w[t][j] * y[inv[t*k+j]]).
+ * At least one of y, out.  Intended for small T (up to a few dozen tokens);
+ * works for any T. */
+FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
+                                         const int32_t* offsets, const int32_t* perm, const int32_t* active,
+                                         const int32_t* inv, const float* w, float* y, uint16_t* out, void* ws,
+                                         size_t ws_bytes, ft_stream_t stream);
+
+/* [P4 MoE core mechanism] Routing-weighted combine:
+ * out[t][n] = bf16( sum_{j<k} w[t][j] * y[inv[t*k+j]][n] ), fp32, j order.
+ *   y (device) fp32 [T*k][H]; inv, w as above; out (device) bf16 [T][H]. */
+FT_API ft_status ft_moe_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H, uint16_t* out,
+                         ft_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Quantisation and synthetic weights                                         */
+/* ------------------------------------------------------------------------ */
+
+FT_API size_t ft_nvfp4_quantize_workspace_size(int64_t N, int64_t K);
+
+/* NVFP4 weight quantiser, fp32 arithmetic with IEEE division:
+ *   s_t = amax / 2688 (1 if that is 0); per 16-block: sb = E4M3_rn_sat(amax_b /
+ *   6 / s_t), eff = e4m3(sb) * s_t, code = E2M1_rn_sat(w / eff) (0 when eff is
+ *   0; a negative value that rounds to 0 is code 0).
+ *   w (device) fp32 [N][K]; codes (device) rows of K/2 bytes at byte stride
+ *   codes_ld; scales (device) rows of K/16 bytes at stride scales_ld;
+ *   tensor_scale (device) one float.  K a multiple of 32. */
+FT_API ft_status ft_nvfp4_quantize_weight(const float* w, int64_t N, int64_t K, uint8_t* codes, int64_t codes_ld,
+                                   uint8_t* scales, int64_t scales_ld, float* tensor_scale, void* ws,
+                                   size_t ws_bytes, ft_stream_t stream);
+
+/* NVFP4 activation quantiser with unit tensor scale (bf16 input): per
+ * 16-block sb = E4M3_rn_sat(amax_b / 6), code = E2M1_rn_sat(x / e4m3(sb)).
+ *   x (device) bf16 [T][K]; codes (device) [T][K/2]; scales (device) [T][K/16]
+ *   row-major.  K a multiple of 32. */
+FT_API ft_status ft_nvfp4_quantize_act(const uint16_t* x, int64_t T, int64_t K, uint8_t* codes, uint8_t* scales,
+                                ft_stream_t stream);
+
+/* Synthetic weights: out[j] = (float)(sigma * Z_{first+j}) where Z is the
+ * Box-Muller normal of Philox4x32-10 block (first+j)/2 with counter
+ * (q_lo, q_hi, stream_lo, stream_hi) and key (seed_lo, seed_hi), evaluated in
+ * fp64 (cosine branch for even index, sine branch for odd).  out (device). */
+FT_API ft_status ft_gen_normal_f32(uint64_t seed, uint64_t stream_id, uint64_t first, int64_t n, double sigma, float* out,
+                            ft_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FTMOE_H_ */

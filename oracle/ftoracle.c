@@ -145,20 +145,29 @@ ORA_API int ora_quantize_weight(const float* w, int64_t N, int64_t K, uint8_t* c
                                 float* tensor_scale) {
     if (N <= 0 || K <= 0 || K % 16 != 0) return ORA_ERR_ARG;
     float amax = 0.0f;
+    int bad = 0;
+#pragma omp parallel for reduction(max : amax) reduction(| : bad)
     for (int64_t i = 0; i < N * K; ++i) {
-        if (!isfinite(w[i])) return ORA_ERR_ARG;
+        if (!isfinite(w[i])) bad = 1;
         const float a = fabsf(w[i]);
         if (a > amax) amax = a;
     }
+    if (bad) return ORA_ERR_ARG;
     float st = amax / 2688.0f;
     if (st == 0.0f) st = 1.0f;
     *tensor_scale = st;
-    uint8_t* tmp = (uint8_t*)malloc((size_t)K);
-    for (int64_t n = 0; n < N; ++n) {
-        for (int64_t b = 0; b < K / 16; ++b) quant_block16(w + n * K + b * 16, st, tmp + b * 16, scales + n * (K / 16) + b);
-        pack_row(tmp, K, codes + n * (K / 2));
+    /* rows are independent: the row loop may run on several threads */
+#pragma omp parallel
+    {
+        uint8_t* tmp = (uint8_t*)malloc((size_t)K);
+#pragma omp for schedule(static)
+        for (int64_t n = 0; n < N; ++n) {
+            for (int64_t b = 0; b < K / 16; ++b)
+                quant_block16(w + n * K + b * 16, st, tmp + b * 16, scales + n * (K / 16) + b);
+            pack_row(tmp, K, codes + n * (K / 2));
+        }
+        free(tmp);
     }
-    free(tmp);
     return ORA_OK;
 }
 
@@ -179,15 +188,17 @@ ORA_API int ora_quantize_act(const float* x, int64_t T, int64_t K, uint8_t* code
 ORA_API int ora_dequantize(const uint8_t* codes, const uint8_t* scales, double tensor_scale, int64_t N, int64_t K,
                            double* out) {
     if (N <= 0 || K <= 0 || K % 16 != 0) return ORA_ERR_ARG;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k) {
             const uint8_t byte = codes[n * (K / 2) + k / 2];
             const uint8_t c = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
             const double s = ora_e4m3_value(scales[n * (K / 16) + k / 16]);
-            if (isnan(s) || s < 0) return ORA_ERR_ARG;
+            if (isnan(s) || s < 0) bad = 1;
             out[n * K + k] = ora_e2m1_value(c) * s * tensor_scale;
         }
-    return ORA_OK;
+    return bad ? ORA_ERR_ARG : ORA_OK;
 }
 
 /* ------------------------------------------------------------------------- */

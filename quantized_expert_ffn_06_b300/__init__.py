@@ -1,0 +1,210 @@
+"""Thin Python binding of libftmoe.so (the C ABI declared in include/ftmoe.h).
+
+Argument marshalling only: every step of the MoE layer runs in the library's
+CUDA kernels.  PyTorch provides device memory and streams.  If the compiled
+library is missing this module raises at import -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libftmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libftmoe.so not found at {LIB_PATH}; build it with "
+                      "`python -m quantized_expert_ffn_06_b300.build`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_UNSUPPORTED, FT_ERR_TIMEOUT, FT_ERR_NO_SLOT, FT_ERR_OOM, \
+    FT_ERR_DEVICE = range(8)
+FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX = 1, 2, 4, 8
+
+_vp, _i32, _i64, _u64, _sz, _dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t,
+                                    ctypes.c_double)
+
+
+class FtError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_lib.ft_status_string(status).decode()}: {msg}")
+        self.status = status
+
+
+class ft_moe_layer_weights(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("n_weights", ctypes.c_int32),
+                ("gu_codes", _vp), ("gu_codes_stride", _i64),
+                ("gu_scales", _vp), ("gu_scales_stride", _i64),
+                ("d_codes", _vp), ("d_codes_stride", _i64),
+                ("d_scales", _vp), ("d_scales_stride", _i64),
+                ("tscale", _vp), ("tscale_stride", _i64),
+                ("expert_to_slot", _vp),
+                ("gu_sf_tiled", _vp), ("gu_sf_tiled_stride", _i64),
+                ("d_sf_tiled", _vp), ("d_sf_tiled_stride", _i64)]
+
+
+def _sig(name, args, res=ctypes.c_int):
+    f = getattr(_lib, name)
+    f.argtypes = args
+    f.restype = res
+    return f
+
+
+_sig("ft_status_string", [_i32], ctypes.c_char_p)
+_sig("ft_last_error", [], ctypes.c_char_p)
+_sig("ft_version", [], _i32)
+_sig("ft_device_status", [_vp, ctypes.POINTER(ctypes.c_uint32)])
+_sig("ft_moe_route", [_vp, _i32, _i32, _i32, _vp, _vp, _vp])
+_sig("ft_moe_permute_workspace_size", [_i32, _i32, _i32], _sz)
+_sig("ft_moe_permute", [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp])
+_sig("ft_moe_decode_workspace_size", [_i32, _i32, _i32, _i32], _sz)
+_sig("ft_moe_expert_ffn_nvfp4_decode", [ctypes.POINTER(ft_moe_layer_weights), _vp, _i32, _i32, _vp, _vp, _vp, _vp,
+                                        _vp, _vp, _vp, _vp, _sz, _vp])
+_sig("ft_moe_combine", [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp])
+_sig("ft_nvfp4_quantize_workspace_size", [_i64, _i64], _sz)
+_sig("ft_nvfp4_quantize_weight", [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _sz, _vp])
+_sig("ft_nvfp4_quantize_act", [_vp, _i64, _i64, _vp, _vp, _vp])
+_sig("ft_gen_normal_f32", [_u64, _u64, _u64, _i64, _dbl, _vp, _vp])
+
+EXPORTED = [n for n in dir(_lib) if n.startswith("ft_")]
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != FT_OK:
+        raise FtError(rc, _lib.ft_last_error().decode())
+
+
+def _p(t) -> int | None:
+    if t is None or isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _s(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _req(t: torch.Tensor, dtype, name: str) -> None:
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor of {dtype}, got {t.dtype} on {t.device}")
+
+
+def _ws(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+# --------------------------------------------------------------------------- status
+
+def ft_version() -> int:
+    return _lib.ft_version()
+
+
+def ft_device_status(stream=None) -> int:
+    """Waits for the stream, returns and clears the device error word (raises on CUDA errors only)."""
+    word = ctypes.c_uint32(0)
+    rc = _lib.ft_device_status(_s(stream), ctypes.byref(word))
+    if rc not in (FT_OK, FT_ERR_DEVICE):
+        _check(rc)
+    return word.value
+
+
+# --------------------------------------------------------------------------- router / permute / combine
+
+def ft_moe_route(logits: torch.Tensor, k: int, ids=None, w=None, stream=None):
+    _req(logits, torch.float32, "logits")
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device) if ids is None else ids
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device) if w is None else w
+    _check(_lib.ft_moe_route(_p(logits), T, E, k, _p(ids), _p(w), _s(stream)))
+    return ids, w
+
+
+def ft_moe_permute_workspace_size(T: int, E: int, k: int) -> int:
+    return _lib.ft_moe_permute_workspace_size(T, E, k)
+
+
+def ft_moe_permute(ids: torch.Tensor, E: int, offsets=None, perm=None, inv=None, active=None, ws=None, stream=None):
+    _req(ids, torch.int32, "ids")
+    T, k = ids.shape
+    dev = ids.device
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev) if perm is None else perm
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev) if inv is None else inv
+    active = torch.empty(E + 1, dtype=torch.int32, device=dev) if active is None else active
+    need = ft_moe_permute_workspace_size(T, E, k)
+    ws = _ws(need, dev) if ws is None else ws
+    _check(_lib.ft_moe_permute(_p(ids), T, E, k, _p(offsets), _p(perm), _p(inv), _p(active), _p(ws),
+                               0 if ws is None else ws.numel() * ws.element_size(), _s(stream)))
+    return offsets, perm, inv, active
+
+
+def ft_moe_combine(y: torch.Tensor, inv: torch.Tensor, w: torch.Tensor, T: int, k: int, out=None, stream=None):
+    _req(y, torch.float32, "y")
+    H = y.shape[1]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device) if out is None else out
+    _check(_lib.ft_moe_combine(_p(y), _p(inv), _p(w), T, k, H, _p(out), _s(stream)))
+    return out
+
+
+# --------------------------------------------------------------------------- expert FFN
+
+def ft_moe_decode_workspace_size(T: int, k: int, H: int, I: int) -> int:
+    return _lib.ft_moe_decode_workspace_size(T, k, H, I)
+
+
+def ft_moe_expert_ffn_nvfp4_decode(W, x: torch.Tensor, k: int, offsets, perm, active, inv=None, w=None, y=None,
+                                   out=None, ws=None, stream=None):
+    """W: a LayerWeights (or anything with .desc()).  Returns (y, out)."""
+    _req(x, torch.bfloat16, "x")
+    T, H = x.shape
+    desc = W.desc()
+    need = ft_moe_decode_workspace_size(T, k, desc.H, desc.I)
+    ws = _ws(need, x.device) if ws is None else ws
+    _check(_lib.ft_moe_expert_ffn_nvfp4_decode(ctypes.byref(desc), _p(x), T, k, _p(offsets), _p(perm), _p(active),
+                                               _p(inv), _p(w), _p(y), _p(out), _p(ws),
+                                               0 if ws is None else ws.numel() * ws.element_size(), _s(stream)))
+    return y, out
+
+
+# --------------------------------------------------------------------------- quantisers / generator
+
+def ft_nvfp4_quantize_weight(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, tensor_scale: torch.Tensor,
+                             codes_ld: int | None = None, scales_ld: int | None = None, ws=None, stream=None):
+    _req(w, torch.float32, "w")
+    N, K = w.shape
+    codes_ld = K // 2 if codes_ld is None else codes_ld
+    scales_ld = K // 16 if scales_ld is None else scales_ld
+    need = _lib.ft_nvfp4_quantize_workspace_size(N, K)
+    ws = _ws(need, w.device) if ws is None else ws
+    _check(_lib.ft_nvfp4_quantize_weight(_p(w), N, K, _p(codes), codes_ld, _p(scales), scales_ld, _p(tensor_scale),
+                                         _p(ws), ws.numel() * ws.element_size(), _s(stream)))
+
+
+def ft_nvfp4_quantize_act(x: torch.Tensor, codes=None, scales=None, stream=None):
+    _req(x, torch.bfloat16, "x")
+    T, K = x.shape
+    codes = torch.empty((T, K // 2), dtype=torch.uint8, device=x.device) if codes is None else codes
+    scales = torch.empty((T, K // 16), dtype=torch.uint8, device=x.device) if scales is None else scales
+    _check(_lib.ft_nvfp4_quantize_act(_p(x), T, K, _p(codes), _p(scales), _s(stream)))
+    return codes, scales
+
+
+def ft_gen_normal_f32(seed: int, stream_id: int, n: int, sigma: float, out: torch.Tensor, first: int = 0,
+                      stream=None):
+    _req(out, torch.float32, "out")
+    _check(_lib.ft_gen_normal_f32(seed, stream_id, first, n, sigma, _p(out), _s(stream)))
+    return out
+
+
+from .layer import LayerWeights, MoEDecodeLayer  # noqa: E402,F401

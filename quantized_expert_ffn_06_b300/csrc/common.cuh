@@ -1,0 +1,109 @@
+// common.cuh -- shared plumbing of the sm_103a MoE kernels: status handling,
+// the per-device error word, and small PTX helpers for the NVFP4 formats.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/ftmoe.h"
+
+namespace ft {
+
+// ----------------------------------------------------------------------------
+// host-side status plumbing
+// ----------------------------------------------------------------------------
+void set_error(const std::string& msg);
+ft_status fail(ft_status s, const std::string& msg);
+ft_status check_launch(const char* what);
+inline cudaStream_t cu(ft_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ----------------------------------------------------------------------------
+// device error word (one per device; read and cleared by ft_device_status)
+// ----------------------------------------------------------------------------
+extern __device__ unsigned int g_err_word;
+
+__device__ __forceinline__ void raise_dev_error(unsigned int bits) { atomicOr(&g_err_word, bits); }
+
+// ----------------------------------------------------------------------------
+// NVFP4 helpers
+// ----------------------------------------------------------------------------
+
+// Two E2M1 codes (low nibble = first element) -> f16x2 (first element in the
+// low half).  Exact: every E2M1 value is an f16 value.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(out) : "r"(byte));
+    return out;
+}
+
+// E4M3 scale byte -> f16x2 with the value in both halves (exact: E4M3 values
+// are f16 normals).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t b) {
+    uint32_t out;
+    const uint32_t pair = (b & 0xFFu) | ((b & 0xFFu) << 8);
+    asm("{\n\t.reg .b16 p;\n\tcvt.u16.u32 p, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, p;\n\t}" : "=r"(out) : "r"(pair));
+    return out;
+}
+
+// Unsigned E4M3 byte -> float (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const uint32_t h2 = e4m3_to_f16x2_bcast(b);
+    return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
+}
+
+// fp32 -> E4M3 byte, round to nearest even, saturating to 448 (input >= 0).
+__device__ __forceinline__ uint32_t f32_to_e4m3_rn_sat(float r) {
+    uint16_t out;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(0.0f), "f"(r));
+    return out & 0xFFu;  // second source lands in the low byte
+}
+
+// two fp32 -> packed E2M1 byte (lo -> low nibble), round to nearest even,
+// saturating to +-6; a code of -0 is replaced by +0.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2_rn_sat(float lo, float hi) {
+    uint16_t out;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(out) : "f"(hi), "f"(lo));
+    uint32_t v = out & 0xFFu;
+    if ((v & 0x0Fu) == 0x08u) v &= 0xF0u;
+    if ((v & 0xF0u) == 0x80u) v &= 0x0Fu;
+    return v;
+}
+
+// acc += a(f16) * b(f16), fp32 accumulate.
+__device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float acc) {
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(acc));
+    return d;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ uint16_t bf16_bits(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// weight index of an expert (identity, or through a slot table)
+__device__ __forceinline__ int weight_index(const ft_moe_layer_weights& W, int e) {
+    if (W.expert_to_slot == nullptr) return e;
+    const int s = W.expert_to_slot[e];
+    if (s < 0 || s >= W.n_weights) {
+        raise_dev_error(FT_DEVERR_BAD_INDEX);
+        return -1;
+    }
+    return s;
+}
+
+}  // namespace ft
