@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse-MoE NVFP4 layer step on B300.
+
+Default workload: 35B-A3B-shaped decode -- 48 MoE layers, hidden 2048, 256
+experts, top-8, expert intermediate 512, batch 1, NVFP4 weights of all experts
+resident in HBM, 256 distinct decode steps of synthetic inputs (cycled).  One
+bench step = one token through all 48 layers, each layer one fused launch
+(router top-k, grouping, NVFP4 SwiGLU expert FFN, weighted combine), replayed
+from a CUDA graph per step.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "MoE decode tok/s and % of HBM roofline; prefill NVFP4 TFLOP/s vs peak"
+UNIT = "tok/s"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons while the timed region runs (NVML, else nvidia-smi)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str | None, period_s: float = 0.02):
+        self.samples, self.reasons, self.period = [], set(), period_s
+        self.max_mhz, self.how, self.err = None, None, None
+        self._stop = threading.Event()
+        self._t = None
+        self._proc = None
+        self.bus = pci_bus_id
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = (pynvml.nvmlDeviceGetHandleByPciBusId(pci_bus_id) if pci_bus_id
+                      else pynvml.nvmlDeviceGetHandleByIndex(0))
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.how = "nvml"
+        except Exception as e:  # fall back to polling nvidia-smi
+            self.err = f"{type(e).__name__}: {e}"
+            self.how = "nvidia-smi"
+
+    def _run_nvml(self):
+        nv = self.nv
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                mask = fn(self.h)
+                self.reasons |= {name for bit, name in self.REASONS.items() if mask & bit}
+            except Exception as e:
+                self.err = f"{type(e).__name__}: {e}"
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.how == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
+            self._t.start()
+        else:
+            cmd = ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                   "--format=csv,noheader,nounits", "-lms", "50"]
+            if self.bus:
+                cmd += ["-i", self.bus]
+            try:
+                self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception as e:
+                self.err = f"{type(e).__name__}: {e}"
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+        if self._proc:
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append(float(parts[0]))
+                    self.max_mhz = float(parts[1])
+                    mask = int(parts[2], 16)
+                    self.reasons |= {name for bit, name in self.REASONS.items() if mask & bit}
+                except (ValueError, IndexError):
+                    pass
+
+    def report(self):
+        r = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+             "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.how}
+        if self.err and not self.samples:
+            r["error"] = self.err
+        return r
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------- oracle (CPU baseline)
+
+class OracleDecode:
+    """The CPU oracle on decode steps of one layer of the workload.
+
+    The layer's experts are quantised by the oracle on first use (its inputs,
+    untimed); each timed step routes a fresh token, dequantises the selected
+    experts, runs their FFN in fp64 and combines -- one layer of one token.
+    """
+
+    def __init__(self, cfg: W.MoEConfig, layer: int = 0):
+        import oracle as O
+        self.O, self.cfg, self.layer = O, cfg, layer
+        self.q = {}
+
+    def step(self, s: int) -> float:
+        O, cfg = self.O, self.cfg
+        logits = W.router_logits(cfg, self.layer, s)
+        x_bits = W.activations_bf16(cfg, self.layer, s)
+        ids, _ = O.route(logits, cfg.k)
+        for e in sorted(set(ids.ravel().tolist())):
+            if e not in self.q:
+                self.q[e] = [O.quantize_weight(W.weights_fp32(cfg, self.layer, e, p)) for p in range(3)]
+        q = self.q
+
+        class _Deq:
+            def __init__(self, t):
+                self.Wg, self.Wu, self.Wd = (O.dequantize(*a) for a in t)
+
+        t0 = time.perf_counter()
+        O.moe_layer(logits, x_bits, cfg.k, lambda e: _Deq(q[e]), O.MODE_A16)
+        return time.perf_counter() - t0
+
+    def threads(self) -> int:
+        return self.O.lib().ora_max_threads()
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode_fused.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "quantized_expert_ffn_06_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, src_hash: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", f"k_moe_decode_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != src_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def run_gpu(args, ws, rank, local):
+    import torch
+    import quantized_expert_ffn_06_b300 as Q
+    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = W.CONFIGS[args.config]
+    L, S, T, H, E, k = cfg.layers, min(cfg.steps, args.distinct_steps), cfg.T, cfg.H, cfg.E, cfg.k
+    if args.layers:
+        L = args.layers
+
+    # ---- weights (device generator + device quantiser), all experts resident, decode tile layout
+    weights = []
+    for layer in range(L):
+        lw = LayerWeights(E, H, cfg.I, dev, layout=Q.FT_LAYOUT_DECODE_TILES)
+        lw.fill_synthetic(lambda e, p, layer=layer: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
+        weights.append(lw)
+    torch.cuda.synchronize()
+
+    # ---- inputs of S distinct steps, resident in HBM (rank r draws steps offset by r*S)
+    step0 = rank * S
+    x_host = np.stack([np.stack([W.activations_bf16(cfg, l, step0 + s) for l in range(L)]) for s in range(S)])
+    lg_host = np.stack([np.stack([W.router_logits(cfg, l, step0 + s) for l in range(L)]) for s in range(S)])
+    x_dev = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).to(dev)     # [S, L, T, H]
+    lg_dev = torch.from_numpy(lg_host).to(dev)                                         # [S, L, T, E]
+    out_dev = torch.empty((S, L, T, H), dtype=torch.bfloat16, device=dev)
+
+    layer_mods = [FusedDecodeLayer(E, H, cfg.I, k, T, dev) for _ in range(L)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step_body(xs, ls, os_):
+        for l in range(L):
+            layer_mods[l](weights[l], ls[l], xs[l], os_[l], routing=False, stream=stream)
+
+    # ---- one CUDA graph per distinct step
+    with torch.cuda.stream(stream):
+        step_body(x_dev[0], lg_dev[0], out_dev[0])   # warm the code paths before capture
+    stream.synchronize()
+    graphs = []
+    for s in range(S):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step_body(x_dev[s], lg_dev[s], out_dev[s])
+        graphs.append(g)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status(stream) == 0
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % S].replay()
+    stream.synchronize()
+
+    # ---- timed region: K steps, inputs resident; each step streams ~680 MB of weights (> L2)
+    props = torch.cuda.get_device_properties(dev)
+    bus = None
+    if hasattr(props, "pci_bus_id"):
+        bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(bus) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(args.steps):
+                graphs[i % S].replay()
+            ev1.record(stream)
+        ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    value = args.steps * T * ws / (ms / 1e3)
+    assert Q.ft_device_status(stream) == 0
+
+    # ---- dominant kernel, timed live: CUDA events around each fused layer launch on its stream
+    evs = []
+    n_k = min(args.steps, S)
+    with torch.cuda.stream(stream):
+        for i in range(n_k):
+            for l in range(L):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                layer_mods[l](weights[l], lg_dev[i][l], x_dev[i][l], out_dev[i][l], routing=False, stream=stream)
+                b.record(stream)
+                evs.append((a, b))
+    stream.synchronize()
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    unique = [len(set(np.argsort(-lg_host[i][l], axis=1, kind="stable")[:, :k].ravel().tolist()))
+              for i in range(n_k) for l in range(L)]
+    # algorithmic bytes of one layer launch: the selected experts' NVFP4 weights (three matrices at
+    # 0.5625 B/param plus three fp32 tensor scales) plus logits, activations and output
+    bytes_per_launch = float(np.mean(unique)) * (cfg.expert_bytes + 12) + T * (E * 4 + H * 2 * 2)
+    avg_launch_s = float(np.mean(launch_ms)) / 1e3
+    peak, peak_kind = load_peaks()
+    achieved = bytes_per_launch / avg_launch_s / 1e9
+
+    # ---- e2e through the public API with pinned host buffers: H2D inputs, layer launches, D2H outputs
+    e2e = None
+    if not args.no_e2e:
+        xb = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
+        lb = torch.empty((L, T, E), dtype=torch.float32, device=dev)
+        ob = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step_body(xb, lb, ob)
+        x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+        l_pin = torch.from_numpy(lg_host).pin_memory()
+        o_pin = torch.empty((S, L, T, H), dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step(i):
+            xb.copy_(x_pin[i % S], non_blocking=True)
+            lb.copy_(l_pin[i % S], non_blocking=True)
+            g.replay()
+            o_pin[i % S].copy_(ob, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                e2e_step(i)
+        stream.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                e2e_step(i)
+            e1.record(stream)
+        e1.synchronize()
+        ems = e0.elapsed_time(e1)
+        if ws > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = t.item()
+        e2e = {"value": args.steps * T * ws / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": L * T * (H * 2 + E * 4), "d2h_bytes_per_step": L * T * H * 2}
+
+    src_hash = kernel_source_hash()
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 weights x bf16 activations, fp32 accumulate", "data": "synthetic (seeded Philox4x32-10)",
+        "config": {"workload": f"{cfg.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, intermediate {cfg.I}, "
+                               f"batch {T}, NVFP4 (E2M1 + E4M3/16 + fp32 tensor scale), all experts resident",
+                   "global_batch": T * ws, "distinct_steps": S,
+                   "l2": "inputs larger than L2: each step streams ~%.0f MB of expert weights" %
+                         (L * float(np.mean(unique)) * cfg.expert_bytes / 1e6),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "kernel": "k_moe_decode (ft_moe_layer_decode), one launch per layer",
+                     "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_launch_s * 1e6,
+                     "traffic": profiled_traffic(cfg.name, src_hash), "source_hash": src_hash},
+        "e2e": e2e,
+        "gpu_launches": L * args.steps,
+        "clocks": clk.report(),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode_35b")
+    ap.add_argument("--distinct-steps", type=int, default=256)
+    ap.add_argument("--layers", type=int, default=0, help="(debug) fewer layers; the result is then not the workload")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-steps", type=int, default=48)
+    args = ap.parse_args()
+
+    ws, rank, local = dist_env()
+    cfg = W.CONFIGS[args.config]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # the oracle as it stands on the host cores; one bench step = one token through one layer of
+        # the workload (layer 0, a fresh token each step), scaled to a full token of all layers
+        ref = OracleDecode(cfg)
+        for s in range(args.warmup):
+            ref.step(10_000 + s)
+        secs = sum(ref.step(s) for s in range(args.steps))
+        per_token = secs / args.steps * cfg.layers
+        val = cfg.T / per_token
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": per_token * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox4x32-10)",
+                "config": {"workload": cfg.name},
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": ref.threads(), "kind": "oracle",
+                                 "sample": f"each step: one token through one of the {cfg.layers} layers (route, "
+                                           f"permute, fp64 dequantisation, FFN, combine), scaled to all layers"},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if ws > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            ref = OracleDecode(cfg)
+            secs = sum(ref.step(s) for s in range(args.cpu_steps))
+            per_token = secs / args.cpu_steps * cfg.layers
+            res["cpu_baseline"] = {"value": cfg.T / per_token, "unit": UNIT, "cores": ref.threads(), "kind": "oracle",
+                                   "sample": f"{args.cpu_steps} single-token steps of layer 0 (route, permute, fp64 "
+                                             f"dequantisation, FFN, combine), scaled to {cfg.layers} layers; "
+                                             f"weight generation and quantisation untimed"}
+        print(json.dumps(res))
+    if ws > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -94,26 +94,36 @@ FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
 /* Weights of one MoE layer                                                   */
 /* ------------------------------------------------------------------------ */
 
-/* Expert weights of one layer in device memory, in the layout the kernels read.
- * For weight index w (the expert id, or its cache slot when expert_to_slot is
- * given):
+/* Layouts of expert weights in device memory (ft_moe_layer_weights.layout). */
+#define FT_LAYOUT_ROWS 0         /* row-major codes [N][K/2] + row-major scales [N][K/16] */
+#define FT_LAYOUT_DECODE_TILES 1 /* 16-row tiles for the decode kernels, see ft_nvfp4_pack_tiles() */
+
+/* Expert weights of one layer in device memory.  For weight index w (the
+ * expert id, or its cache slot when expert_to_slot is given):
+ *  layout FT_LAYOUT_ROWS
  *   gate/up  codes  gu_codes  + w*gu_codes_stride  : [2I][H/2] bytes; row 2i is
  *                   gate row i, row 2i+1 is up row i (interleaved so that one
  *                   tile holds both halves of each SwiGLU pair)
  *            scales gu_scales + w*gu_scales_stride : [2I][H/16] E4M3 bytes
  *   down     codes  d_codes   + w*d_codes_stride   : [H][I/2]
  *            scales d_scales  + w*d_scales_stride  : [H][I/16]
- *   tensor scales  tscale + w*tscale_stride       : float {gate, up, down}
- *   gu_sf_tiled / d_sf_tiled (optional, prefill only): the same scales
- *            rearranged by ft_nvfp4_tile_scales(), strides gu_sf_tiled_stride /
- *            d_sf_tiled_stride.
+ *  layout FT_LAYOUT_DECODE_TILES (codes and scales together; scale pointers unused)
+ *   gate/up  gu_codes + w*gu_codes_stride : the [2I][H] matrix above packed by
+ *            ft_nvfp4_pack_tiles() (2I*H*9/16 bytes)
+ *   down     d_codes  + w*d_codes_stride  : the [H][I] matrix packed likewise
+ *  both layouts
+ *   tensor scales  tscale + w*tscale_stride : float {gate, up, down}
+ *   gu_sf_tiled / d_sf_tiled (optional, prefill only): scales rearranged for the
+ *            block-scaled tensor cores, strides gu_sf_tiled_stride / d_sf_tiled_stride.
  * Strides are in bytes (tscale_stride in floats).  Every base address and
  * stride must be a multiple of 16.  expert_to_slot (device, optional, [E]
  * int32) maps an expert id to its weight index; ids mapping to a negative or
- * out-of-range index set FT_DEVERR_BAD_INDEX and produce zeros.
+ * out-of-range index set FT_DEVERR_BAD_INDEX and contribute zeros.
  * Sizes: 1 <= E <= 1024 experts; H a multiple of 256; I a multiple of 128. */
 typedef struct ft_moe_layer_weights {
     int32_t E, H, I, n_weights; /* n_weights: number of weight indices (E, or cache slots) */
+    int32_t layout;             /* FT_LAYOUT_* */
+    int32_t reserved0;
     const uint8_t* gu_codes;
     int64_t gu_codes_stride;
     const uint8_t* gu_scales;
@@ -188,6 +198,26 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
                                          const int32_t* inv, const float* w, float* y, uint16_t* out, void* ws,
                                          size_t ws_bytes, ft_stream_t stream);
 
+/* Fused decode layer step for up to 16 tokens, weights in FT_LAYOUT_DECODE_TILES:
+ * router top-k (same selection and weights as ft_moe_route), grouping by
+ * expert (same order as ft_moe_permute), the NVFP4 SwiGLU expert FFN and the
+ * weighted combine, in one launch of one CTA per SM.
+ * [P4 MoE core mechanism; P3 §2.1; P5 NVFP4]
+ *   logits (device) fp32 [T][E]; x (device) bf16 [T][H], 16-byte aligned.
+ *   out    (device) bf16 [T][H]: out[t] = bf16(sum_j w[t][j] * y_{t,j}), the
+ *          sum over a token's experts taken in ascending expert id, fp32.
+ *   ids, w (device, optional, both or neither) [T][k]: the routing result.
+ *   ws: ft_moe_layer_decode_workspace_size(T, k, H, I) bytes, 256-byte
+ *       aligned, ZERO-FILLED before its first use.  Its first 256 bytes hold a
+ *       grid-barrier counter that the kernel keeps consistent across calls;
+ *       calls sharing a workspace must not overlap on the device.  After a
+ *       FT_DEVERR_TIMEOUT zero it again.
+ * 0 <= T <= 16, 1 <= k <= min(E, 32). */
+FT_API size_t ft_moe_layer_decode_workspace_size(int T, int k, int H, int I);
+FT_API ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x, int T,
+                                     int k, uint16_t* out, int32_t* ids, float* w, void* ws, size_t ws_bytes,
+                                     ft_stream_t stream);
+
 /* [P4 MoE core mechanism] Routing-weighted combine:
  * out[t][n] = bf16( sum_{j<k} w[t][j] * y[inv[t*k+j]][n] ), fp32, j order.
  *   y (device) fp32 [T*k][H]; inv, w as above; out (device) bf16 [T][H]. */
@@ -217,6 +247,19 @@ FT_API ft_status ft_nvfp4_quantize_weight(const float* w, int64_t N, int64_t K, 
  *   row-major.  K a multiple of 32. */
 FT_API ft_status ft_nvfp4_quantize_act(const uint16_t* x, int64_t T, int64_t K, uint8_t* codes, uint8_t* scales,
                                 ft_stream_t stream);
+
+/* Packs a row-major NVFP4 matrix [N][K] (codes [N][K/2] at byte stride
+ * codes_ld, scales [N][K/16] at stride scales_ld) into FT_LAYOUT_DECODE_TILES:
+ * N/16 tiles of 16*K*9/16 bytes.  Within a tile, per 128-element K-block kb
+ * (K/128 of them): 1024 code bytes, byte i of piece q (bytes 16q..16q+15 of the
+ * row's 64 bytes in that block) of row 8h+g at kb*1024 + h*512 + (q*8+g)*16 + i;
+ * then, after all code blocks, 128 scale bytes per K-block: scale 2q+b of the
+ * block's eight for row 8h+g at (K/128)*1024 + kb*128 + (q*8+g)*4 + 2h + b.
+ * One warp lane thus reads 16 contiguous code bytes of rows g and g+8 and one
+ * 4-byte scale word, conflict-free.  N a multiple of 16, K a multiple of 128.
+ * All pointers (device). */
+FT_API ft_status ft_nvfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
+                                     int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
 
 /* Synthetic weights: out[j] = (float)(sigma * Z_{first+j}) where Z is the
  * Box-Muller normal of Philox4x32-10 block (first+j)/2 with counter

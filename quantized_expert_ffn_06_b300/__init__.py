@@ -16,12 +16,13 @@ LIB_PATH = os.path.join(_HERE, "libftmoe.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libftmoe.so not found at {LIB_PATH}; build it with "
-                      "`python -m quantized_expert_ffn_06_b300.build`")
+                      "`python quantized_expert_ffn_06_b300/build.py`")
 
 _lib = ctypes.CDLL(LIB_PATH)
 
 FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_UNSUPPORTED, FT_ERR_TIMEOUT, FT_ERR_NO_SLOT, FT_ERR_OOM, \
     FT_ERR_DEVICE = range(8)
+FT_LAYOUT_ROWS, FT_LAYOUT_DECODE_TILES = 0, 1
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX = 1, 2, 4, 8
 
 _vp, _i32, _i64, _u64, _sz, _dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t,
@@ -36,6 +37,7 @@ class FtError(RuntimeError):
 
 class ft_moe_layer_weights(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("n_weights", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("reserved0", ctypes.c_int32),
                 ("gu_codes", _vp), ("gu_codes_stride", _i64),
                 ("gu_scales", _vp), ("gu_scales_stride", _i64),
                 ("d_codes", _vp), ("d_codes_stride", _i64),
@@ -68,6 +70,10 @@ _sig("ft_nvfp4_quantize_workspace_size", [_i64, _i64], _sz)
 _sig("ft_nvfp4_quantize_weight", [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _sz, _vp])
 _sig("ft_nvfp4_quantize_act", [_vp, _i64, _i64, _vp, _vp, _vp])
 _sig("ft_gen_normal_f32", [_u64, _u64, _u64, _i64, _dbl, _vp, _vp])
+_sig("ft_nvfp4_pack_tiles", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
+_sig("ft_moe_layer_decode_workspace_size", [_i32, _i32, _i32, _i32], _sz)
+_sig("ft_moe_layer_decode", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
+                             _vp])
 
 EXPORTED = [n for n in dir(_lib) if n.startswith("ft_")]
 
@@ -207,4 +213,22 @@ def ft_gen_normal_f32(seed: int, stream_id: int, n: int, sigma: float, out: torc
     return out
 
 
-from .layer import LayerWeights, MoEDecodeLayer  # noqa: E402,F401
+def ft_nvfp4_pack_tiles(codes, codes_ld: int, scales, scales_ld: int, N: int, K: int, tiles, stream=None):
+    _check(_lib.ft_nvfp4_pack_tiles(_p(codes), codes_ld, _p(scales), scales_ld, N, K, _p(tiles), _s(stream)))
+
+
+def ft_moe_layer_decode_workspace_size(T: int, k: int, H: int, I: int) -> int:
+    return _lib.ft_moe_layer_decode_workspace_size(T, k, H, I)
+
+
+def ft_moe_layer_decode(W, logits: torch.Tensor, x: torch.Tensor, k: int, out: torch.Tensor, ws: torch.Tensor,
+                        ids=None, w=None, stream=None):
+    """Fused decode layer step (route + group + NVFP4 SwiGLU FFN + combine).  ws must start zero-filled."""
+    T = x.shape[0]
+    desc = W.desc()
+    _check(_lib.ft_moe_layer_decode(ctypes.byref(desc), _p(logits), _p(x), T, k, _p(out), _p(ids), _p(w), _p(ws),
+                                    ws.numel() * ws.element_size(), _s(stream)))
+    return out
+
+
+from .layer import FusedDecodeLayer, LayerWeights, MoEDecodeLayer  # noqa: E402,F401

@@ -1,6 +1,6 @@
 """Build libftmoe.so in-tree for sm_103a with nvcc (parallel per-file compile, device link).
 
-Usage: python -m quantized_expert_ffn_06_b300.build [--force]
+Usage: python quantized_expert_ffn_06_b300/build.py [--force]
 """
 from __future__ import annotations
 
@@ -15,7 +15,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libftmoe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "route_permute.cu", "quant.cu", "decode.cu"]
+SOURCES = ["api.cu", "route_permute.cu", "quant.cu", "decode.cu", "decode_fused.cu"]
 HOST_SOURCES = []
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

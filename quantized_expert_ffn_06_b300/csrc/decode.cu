@@ -237,17 +237,22 @@ __global__ void __launch_bounds__(kDnWarps * 32) k_decode_down(ft_moe_layer_weig
     }
 }
 
+ft_status decode_tiles_grouped(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k, const int32_t* offsets,
+                               const int32_t* perm, const float* w, float* y, uint16_t* out, void* ws, size_t ws_bytes,
+                               ft_stream_t stream);
+
 ft_status validate_weights(const ft_moe_layer_weights* W, const char* fn) {
     if (!W) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights descriptor is null");
     if (W->E <= 0 || W->E > 1024 || W->H <= 0 || W->H % 256 || W->I <= 0 || W->I % 128 || W->n_weights <= 0)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 1 <= E <= 1024, H a multiple of 256, I a multiple of 128");
-    if (!W->gu_codes || !W->gu_scales || !W->d_codes || !W->d_scales || !W->tscale)
+    const bool rows = W->layout == FT_LAYOUT_ROWS;
+    if (!W->gu_codes || !W->d_codes || !W->tscale || (rows && (!W->gu_scales || !W->d_scales)))
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null weight pointer");
     if (!W->expert_to_slot && W->n_weights < W->E)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": n_weights < E without a slot table");
     const void* ptrs[4] = {W->gu_codes, W->gu_scales, W->d_codes, W->d_scales};
     for (const void* p : ptrs)
-        if (!aligned(p, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weight pointers need 16-byte alignment");
+        if (p && !aligned(p, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weight pointers need 16-byte alignment");
     if (W->gu_codes_stride % 16 || W->gu_scales_stride % 16 || W->d_codes_stride % 16 || W->d_scales_stride % 16)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weight strides need to be multiples of 16 bytes");
     if (W->tscale_stride < 3) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": tscale_stride < 3");
@@ -267,7 +272,8 @@ extern "C" {
 size_t ft_moe_decode_workspace_size(int T, int k, int H, int I) {
     if (T <= 0 || k <= 0 || H <= 0 || I <= 0) return 0;
     const size_t rows = (size_t)T * k;
-    return align256(rows * I * sizeof(uint16_t)) + align256(rows * H * sizeof(float));
+    // [0, 256): grid-barrier counter of the tiled kernel; then h; then y for the row kernels
+    return 256 + align256(rows * I * sizeof(uint16_t)) + align256(rows * H * sizeof(float));
 }
 
 ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
@@ -286,10 +292,13 @@ ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, const ui
     if (!ws || ws_bytes < need || !aligned(ws, 256))
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": workspace missing, too small or not 256-byte aligned");
     if (y && !aligned(y, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": y needs 16-byte alignment");
+    if (W->layout == FT_LAYOUT_DECODE_TILES)
+        return decode_tiles_grouped(W, x, T, k, offsets, perm, w, y, out, ws, ws_bytes, stream);
+    if (W->layout != FT_LAYOUT_ROWS) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": unknown weight layout");
     const int H = W->H, I = W->I;
     const int rows = T * k;
-    uint16_t* hbuf = static_cast<uint16_t*>(ws);
-    float* ybuf = y ? y : reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)rows * I * 2));
+    uint16_t* hbuf = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + 256);
+    float* ybuf = y ? y : reinterpret_cast<float*>(static_cast<char*>(ws) + 256 + align256((size_t)rows * I * 2));
     const int max_active = std::min(W->E, rows);
     cudaStream_t s = cu(stream);
 
