@@ -165,6 +165,24 @@ class OracleDecode:
         O.moe_layer(logits, x_bits, cfg.k, lambda e: _Deq(q[e]), O.MODE_A16)
         return time.perf_counter() - t0
 
+    def expert_step(self, s: int) -> float:
+        """One routed expert of one token: route, permute, dequantise that expert, its FFN (timed)."""
+        O, cfg = self.O, self.cfg
+        logits = W.router_logits(cfg, self.layer, s)
+        x_bits = W.activations_bf16(cfg, self.layer, s)
+        t0 = time.perf_counter()
+        ids, w = O.route(logits, cfg.k)
+        O.permute(ids, cfg.E)
+        t_route = time.perf_counter() - t0
+        e = int(ids[0, s % cfg.k])
+        if e not in self.q:
+            self.q[e] = [O.quantize_weight(W.weights_fp32(cfg, self.layer, e, p)) for p in range(3)]
+        x = (x_bits[:1].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        t0 = time.perf_counter()
+        Wg, Wu, Wd = (O.dequantize(*a) for a in self.q[e])
+        O.expert_ffn(Wg, Wu, Wd, x, O.MODE_A16)
+        return t_route + (time.perf_counter() - t0) * cfg.k
+
     def threads(self) -> int:
         return self.O.lib().ora_max_threads()
 
@@ -375,12 +393,13 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        # the oracle as it stands on the host cores; one bench step = one token through one layer of
-        # the workload (layer 0, a fresh token each step), scaled to a full token of all layers
+        # the oracle as it stands on the host cores; one bench step = one routed expert of one token in
+        # layer 0 (route + permute + that expert's dequantisation and FFN, scaled by k), so that a full
+        # token is k x layers of them
         ref = OracleDecode(cfg)
         for s in range(args.warmup):
-            ref.step(10_000 + s)
-        secs = sum(ref.step(s) for s in range(args.steps))
+            ref.expert_step(10_000 + s)
+        secs = sum(ref.expert_step(s) for s in range(args.steps))
         per_token = secs / args.steps * cfg.layers
         val = cfg.T / per_token
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
@@ -388,8 +407,9 @@ def main():
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox4x32-10)",
                 "config": {"workload": cfg.name},
                 "cpu_baseline": {"value": val, "unit": UNIT, "cores": ref.threads(), "kind": "oracle",
-                                 "sample": f"each step: one token through one of the {cfg.layers} layers (route, "
-                                           f"permute, fp64 dequantisation, FFN, combine), scaled to all layers"},
+                                 "sample": f"each step: one routed expert of one token in layer 0 (route, permute, "
+                                           f"fp64 dequantisation and FFN of that expert x {cfg.k}), scaled to "
+                                           f"{cfg.layers} layers"},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
