@@ -65,7 +65,7 @@ struct DecodeArgs {
     unsigned int* bar;        // grid barrier counter (monotonic, starts at 0)
     int T, k;
     int stage_bytes, nstages;
-    int xs_stride;            // halves per staged row
+    int xs_stride;            // halves per staged row (general path; both phases)
     int xs_bytes;             // bytes of the staging area
     int tge;                  // token columns per mma pass (<= 8)
     int fast;                 // all x rows and all h rows fit in the staging area
@@ -301,6 +301,10 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const int nf = T * k;
     const int tge = a.tge;          // token columns per pass (<= 8)
     const bool fast = a.fast != 0;  // all x rows and all h rows fit in xs
+    // staged-row strides in halves: the fast path holds T rows of H, then nf rows of I; the
+    // general path holds tge rows of either, at the wider stride
+    const int xstride = fast ? H + 8 : a.xs_stride;
+    const int hstride = fast ? I + 8 : a.xs_stride;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
     auto all_sync = [] { __syncthreads(); };
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         }
     }
     if (fast)  // all T activation rows, once (its barriers also publish the loads above)
-        stage_rows(sm.xexp, &sm.flag, xs, a.xs_stride, a.x, T, H, [&](int r) { return (int64_t)r * H; }, tid,
+        stage_rows(sm.xexp, &sm.flag, xs, xstride, a.x, T, H, [&](int r) { return (int64_t)r * H; }, tid,
                    dk::THREADS, all_sync);
     else
         __syncthreads();
@@ -489,7 +493,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             const int g0 = gi * tge, nt = min(tge, tu - g0);
             if (!fast && (staged_u != u || staged_g != gi)) {
                 csync();  // earlier readers of xs / xexp are done
-                stage_rows(sm.xexp, &sm.flag, xs, a.xs_stride, a.x, nt, H,
+                stage_rows(sm.xexp, &sm.flag, xs, xstride, a.x, nt, H,
                            [&](int r) { return (int64_t)(sm.plist[pb + g0 + r] / k) * H; }, tid, dk::NCW * 32, csync);
                 staged_u = u;
                 staged_g = gi;
@@ -497,7 +501,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             const int col = min(g8, nt - 1);
             const int xr = fast ? sm.plist[pb + g0 + col] / k : col;
             float d[4] = {0.f, 0.f, 0.f, 0.f};
-            if (wi >= 0) tile_partial(tile, KB1, warp, dk::NCW, xs + xr * a.xs_stride, d);
+            if (wi >= 0) tile_partial(tile, KB1, warp, dk::NCW, xs + xr * xstride, d);
             float* rb = red + buf * dk::NCW * 16 * tge;
             store_partial(rb, tge, warp, d, nt);
             consumer_sync();
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
 
     // ---------------- phase 2: down projection and combine over this CTA's output rows
     if (fast && n_ot > 0)  // all h rows in plist order, once
-        stage_rows(sm.rexp, &sm.flag, xs, a.xs_stride, a.hbuf, nf, I,
+        stage_rows(sm.rexp, &sm.flag, xs, hstride, a.hbuf, nf, I,
                    [&](int r) { return (int64_t)sm.plist[r] * I; }, tid, dk::NCW * 32, csync);
     staged_u = -1;
     staged_g = -1;
@@ -566,7 +570,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 const int pb = sm.ubeg[u], tu = sm.ubeg[u + 1] - pb;
                 nt = tu;
                 const int xr = pb + min(g8, tu - 1);
-                if (sm.uwi[u] >= 0) tile_partial(slot + jj * bytes2, KB2, warp % wpe, wpe, xs + xr * a.xs_stride, d);
+                if (sm.uwi[u] >= 0) tile_partial(slot + jj * bytes2, KB2, warp % wpe, wpe, xs + xr * hstride, d);
             }
             float* rb = red + buf * dk::NCW * 16 * tge;
             store_partial(rb, tge, warp, d, min(nt, tge));
@@ -602,13 +606,13 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 const int g0 = gi * tge, nt = min(tge, tu - g0);
                 if (staged_u != u || staged_g != gi) {
                     csync();
-                    stage_rows(sm.xexp, &sm.flag, xs, a.xs_stride, a.hbuf, nt, I,
+                    stage_rows(sm.xexp, &sm.flag, xs, hstride, a.hbuf, nt, I,
                                [&](int r) { return (int64_t)sm.plist[pb + g0 + r] * I; }, tid, dk::NCW * 32, csync);
                     staged_u = u;
                     staged_g = gi;
                 }
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
-                if (wi >= 0) tile_partial(slot, KB2, warp, dk::NCW, xs + min(g8, nt - 1) * a.xs_stride, d);
+                if (wi >= 0) tile_partial(slot, KB2, warp, dk::NCW, xs + min(g8, nt - 1) * hstride, d);
                 float* rb = red + buf * dk::NCW * 16 * tge;
                 store_partial(rb, tge, warp, d, nt);
                 consumer_sync();
