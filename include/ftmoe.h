@@ -209,10 +209,14 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
  *   ids, w (device, optional, both or neither) [T][k]: the routing result.
  *   ws: ft_moe_layer_decode_workspace_size(T, k, H, I) bytes, 256-byte
  *       aligned, ZERO-FILLED before its first use.  Its first 256 bytes hold a
- *       grid-barrier counter that the kernel keeps consistent across calls;
- *       calls sharing a workspace must not overlap on the device.  After a
- *       FT_DEVERR_TIMEOUT zero it again.
- * 0 <= T <= 16, 1 <= k <= min(E, 32). */
+ *       call counter (each call adds one per CTA) that tags the h values the
+ *       gate/up phase hands to the down phase; calls sharing a workspace must
+ *       not overlap on the device.  After a FT_DEVERR_TIMEOUT zero it again.
+ * 0 <= T <= 16, 1 <= k <= min(E, 32).  The activations are staged in shared
+ * memory as f16: T*(H+32) + T*k*(I+32) halves must fit 120 KB, otherwise
+ * FT_ERR_UNSUPPORTED is returned (use the separate calls with FT_LAYOUT_ROWS).
+ * The launch allows programmatic dependent launch: the kernel reads no input
+ * before the preceding kernel in the stream has completed. */
 FT_API size_t ft_moe_layer_decode_workspace_size(int T, int k, int H, int I);
 FT_API ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x, int T,
                                      int k, uint16_t* out, int32_t* ids, float* w, void* ws, size_t ws_bytes,
@@ -252,11 +256,12 @@ FT_API ft_status ft_nvfp4_quantize_act(const uint16_t* x, int64_t T, int64_t K, 
  * codes_ld, scales [N][K/16] at stride scales_ld) into FT_LAYOUT_DECODE_TILES:
  * N/16 tiles of 16*K*9/16 bytes.  Within a tile, per 128-element K-block kb
  * (K/128 of them): 1024 code bytes, byte i of piece q (bytes 16q..16q+15 of the
- * row's 64 bytes in that block) of row 8h+g at kb*1024 + h*512 + (q*8+g)*16 + i;
+ * row's 64 bytes in that block) of row 8h+g at kb*1024 + h*512 + (g*4+q)*16 + i;
  * then, after all code blocks, 128 scale bytes per K-block: scale 2q+b of the
- * block's eight for row 8h+g at (K/128)*1024 + kb*128 + (q*8+g)*4 + 2h + b.
- * One warp lane thus reads 16 contiguous code bytes of rows g and g+8 and one
- * 4-byte scale word, conflict-free.  N a multiple of 16, K a multiple of 128.
+ * block's eight for row 8h+g at (K/128)*1024 + kb*128 + (g*4+q)*4 + 2h + b.
+ * Warp lane L = 4g+q thus reads the 16 code bytes at L*16 and 512 + L*16 (rows
+ * g and g+8) and the scale word at L*4: consecutive lanes, consecutive
+ * addresses, no bank conflicts.  N a multiple of 16, K a multiple of 128.
  * All pointers (device). */
 FT_API ft_status ft_nvfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
                                      int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);

@@ -272,8 +272,10 @@ extern "C" {
 size_t ft_moe_decode_workspace_size(int T, int k, int H, int I) {
     if (T <= 0 || k <= 0 || H <= 0 || I <= 0) return 0;
     const size_t rows = (size_t)T * k;
-    // [0, 256): grid-barrier counter of the tiled kernel; then h; then y for the row kernels
-    return 256 + align256(rows * I * sizeof(uint16_t)) + align256(rows * H * sizeof(float));
+    // [0, 256): call counter of the tiled kernel; then its h words (4 bytes per value), or
+    // h (bf16) and y (fp32) of the row kernels
+    const size_t row_path = align256(rows * I * sizeof(uint16_t)) + align256(rows * H * sizeof(float));
+    return 256 + std::max(row_path, align256(rows * I * 4));
 }
 
 ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,

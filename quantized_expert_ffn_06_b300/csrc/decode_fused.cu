@@ -4,32 +4,42 @@
 //
 // The step follows the page "FreeToken：753B大模型塞进单卡的本地部署硬件账该怎么算"
 // (MoE core mechanism: linear + softmax router, top-K experts, weighted sum of
-// independent expert FFNs).  Decode is bound by streaming the selected
-// experts' weights from HBM, so the kernel is organised around that stream:
+// independent expert FFNs).  Decode is bound by streaming the selected experts'
+// weights from HBM, and at batch 1 a layer moves only ~14 MB (a few
+// microseconds), so the kernel is built around the latency of that stream:
 //
-//  * Weights sit in HBM in 16-row tiles (ft_nvfp4_pack_tiles): a tile of a
-//    [N][K] matrix holds, per 128-element K-block, 1 KB of codes arranged so
-//    that the 32 lanes of a warp read 16 conflict-free bytes each, then 128 B
-//    of E4M3 scales (4 per lane).  One tile is one contiguous bulk copy.
-//  * One producer warp streams tiles with cp.async.bulk into a ring of shared
-//    memory stages guarded by mbarriers; 16 consumer warps decode E2M1 pairs to
-//    f16 in registers (exact), multiply by the block scale in f16 (exact: at
+//  * Weights sit in HBM in 16-row tiles (ft_nvfp4_pack_tiles): per 128-element
+//    K-block 1 KB of codes in which lane L of a warp owns the 16-byte pieces at
+//    L*16 and 512 + L*16 (its mma A fragment for rows L/4 and L/4 + 8), then
+//    128 B of E4M3 scales, one 4-byte word per lane.  One tile is one bulk copy
+//    and every shared-memory read of it is conflict-free.
+//  * Prologue: each token's top-k is found by one warp (k rounds of a warp-wide
+//    integer max on order-preserving keys, ties to the lower expert id) while the
+//    other threads stage the activations as f16.  Every CTA does this
+//    redundantly, so the weight stream starts without any inter-CTA traffic.
+//  * One producer warp issues every tile the CTA needs with cp.async.bulk into
+//    a ring of shared-memory stages guarded by mbarriers; the down-projection
+//    tiles are prefetched while the gate/up tiles are consumed.
+//  * Sixteen consumer warps form four groups.  A group owns whole tiles: its
+//    four warps split a tile's K-blocks, decode each E2M1 pair exactly to f16
+//    (cvt.rn.f16x2.e2m1x2), multiply by the E4M3 block scale in f16 (exact: at
 //    most 6 significant bits, magnitudes in [2^-10, 2688]) and feed mma.sync
-//    m16n8k16 with fp32 accumulation.  The tensor cores only take over the
-//    multiply-adds of this HBM-bound GEMV; tokens are the mma's N.
-//  * Prologue: every CTA routes redundantly (top-k by rank, so all threads
-//    work at once), groups the (token, slot) pairs by expert and stages the
-//    activations as f16, all before the first weight byte is needed.
-//  * Phase 1 (gate/up) splits the selected experts' gate/up tiles evenly over
-//    the CTAs; each CTA writes h = bf16(silu(g) * u) for its pairs.  A bounded
-//    grid barrier follows.  Phase 2 (down + combine) gives each CTA a range of
-//    output rows for all selected experts, so the weighted sum over experts is
-//    accumulated in a fixed order in shared memory.  Phase-2 tiles are
-//    prefetched into the ring while phase 1 runs; several experts' tiles share
-//    one ring slot.
-//  * Grid = one CTA per SM, all co-resident, which the barrier relies on.
-//    Every wait is bounded by a %globaltimer budget; on expiry the kernel
-//    sets FT_DEVERR_TIMEOUT and finishes without trapping.
+//    m16n8k16 with fp32 accumulation (tokens are the mma's N).  The tensor cores
+//    only take over the multiply-adds of this HBM-bound GEMV.  The group then
+//    reduces its four partial tiles and writes h = bf16(silu(g) * u).
+//  * The gate/up phase writes h as 64-bit words {bf16, bf16, call epoch}; the
+//    down phase of every CTA waits (bounded) for exactly the words it reads, so
+//    no grid-wide barrier separates the phases.
+//    In the down phase each CTA owns a range of 16-row output tiles for all
+//    selected experts; a warp computes one expert's down tile over the full K,
+//    so no cross-warp reduction is needed, and the weighted sum over a token's
+//    k experts is taken in slot order j from shared memory.
+//  * Grid = one CTA per SM, all co-resident, which those waits rely on.  Every
+//    wait is bounded by a %globaltimer budget; on expiry the kernel sets
+//    FT_DEVERR_TIMEOUT, stops waiting and finishes without trapping.
+//  * The launch allows programmatic dependent launch: the kernel waits for its
+//    predecessor's results (griddepcontrol.wait) before reading any input, and
+//    lets its successor be scheduled once all of its own CTAs have started.
 #include "common.cuh"
 
 #include <algorithm>
@@ -39,16 +49,29 @@ namespace ft {
 
 namespace dk {
 constexpr int NCW = 16;                  // consumer warps
+constexpr int NG = 4;                    // consumer groups
+constexpr int WPG = NCW / NG;            // warps per group
 constexpr int THREADS = 32 * (NCW + 1);  // + one producer warp
 constexpr int MAXT = 16;                 // tokens per launch
 constexpr int MAXK = 32;                 // experts per token
-constexpr int MAXF = MAXT * MAXK;        // (token, slot) pairs
-constexpr int TG = 8;                    // tokens per mma pass (mma N)
-constexpr int MAXNS = 8;                 // ring stages
-constexpr int MAXU = MAXF;               // selected experts per launch
-constexpr int MAX_OUT_TILES = 4;         // 16-row output tiles per CTA in phase 2
+constexpr int MAXNS = 16;                // ring stages
+constexpr int XPAD = 32;                 // halves of padding per staged f16 row (bank spread between rows)
+constexpr size_t SMEM_BUDGET = 227 * 1024;
+constexpr size_t XS_BUDGET = 120 * 1024;  // staged activations: x and h, separate buffers
 constexpr unsigned long long WAIT_NS = 2000000000ull;  // bound on any single wait
 }  // namespace dk
+
+// Shared-memory plan, computed on the host (byte offsets into dynamic shared memory).
+struct DecodePlan {
+    int nstages, stage_bytes;  // ring
+    int J;                     // down tiles (experts) per phase-2 stage
+    int tcol;                  // token columns of a partial tile (T)
+    int max_ot;                // phase-2 output tiles per CTA, at most
+    int xs_stride, hs_stride;  // halves per staged x / h row
+    int off_bars, off_ids, off_wts, off_plist, off_pexp, off_hexp, off_ulist, off_ubeg, off_uwi, off_misc;
+    int off_xs, off_hs, off_red, off_ybuf, off_ring;
+    int smem;
+};
 
 struct DecodeArgs {
     ft_moe_layer_weights W;
@@ -61,34 +84,14 @@ struct DecodeArgs {
     float* y;                 // [T*k][H] fp32 per permuted row, optional (grouped mode)
     int32_t* ids_out;         // route mode, optional
     float* w_out;             // route mode, optional
-    uint16_t* hbuf;           // [T*k][I] bf16
-    unsigned int* bar;        // grid barrier counter (monotonic, starts at 0)
+    void* hbuf;               // [T*k][I/2] h words {bf16, bf16, epoch}, by permuted row
+    unsigned int* bar;        // call counter (monotonic, starts at 0): G per call
     int T, k;
-    int stage_bytes, nstages;
-    int xs_stride;            // halves per staged row (general path; both phases)
-    int xs_bytes;             // bytes of the staging area
-    int tge;                  // token columns per mma pass (<= 8)
-    int fast;                 // all x rows and all h rows fit in the staging area
+    DecodePlan P;
 };
 
-struct DecodeSmem {
-    unsigned long long full[dk::MAXNS];
-    unsigned long long empty[dk::MAXNS];
-    int ids[dk::MAXF];         // route mode: expert of slot f = t*k + j
-    float wts[dk::MAXF];       // routing weight of slot f
-    float selv[dk::MAXF];      // route mode: selected logit of slot f
-    int plist[dk::MAXF];       // slots grouped by expert ascending, increasing f within an expert
-    int pexp[dk::MAXF];        // expert of plist position p
-    int rexp[dk::MAXF];        // power-of-two pre-scale of staged h row p (fast path)
-    int ulist[dk::MAXU];       // selected experts, ascending
-    int ubeg[dk::MAXU + 1];    // plist range of each selected expert
-    int uwi[dk::MAXU];         // weight index of each selected expert (-1: invalid slot)
-    float uts[dk::MAXU][3];    // tensor scales (gate, up, down) of each selected expert
-    int U;
-    int flag;
-    int xexp[dk::MAXT];        // power-of-two pre-scale of staged x rows
-    float oacc[dk::MAX_OUT_TILES][16][dk::MAXT];
-};
+// misc ints in shared memory
+enum { M_U = 0, M_FLAG = 1, M_ABORT = 2, M_EPOCH = 3, M_XEXP = 4, M_TAGS = 4 + 16 };  // xexp: MAXT entries, tags: MAXNS
 
 // ---------------------------------------------------------------------------- PTX helpers
 
@@ -122,12 +125,15 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* b, uint32_t pa
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase; false (and the device error bit) on expiry.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* b, uint32_t parity) {
+// Bounded wait on an mbarrier phase.  On expiry (or if the CTA already gave up)
+// returns false; the first expiry sets FT_DEVERR_TIMEOUT and the CTA's abort flag.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(b, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait(b, parity)) {
+        if (*abort_flag) return false;
         if (globaltimer() - t0 > dk::WAIT_NS) {
+            *abort_flag = 1;
             raise_dev_error(FT_DEVERR_TIMEOUT);
             return false;
         }
@@ -142,7 +148,44 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  : "memory");
 }
 
+// Stage tags: the producer publishes, after arming a stage's full barrier for
+// chunk n, tag[stage] = n (release); a consumer of chunk n first waits for that
+// tag (acquire) and only then tests the barrier's phase parity.  Without the tag
+// a consumer group running ahead could test the parity of a use whose previous
+// use has not landed yet, and parity alone cannot tell the two apart.
+__device__ __forceinline__ void tag_publish(int* tag, int n) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tag)), "r"(n) : "memory");
+}
+__device__ __forceinline__ int tag_read(const int* tag) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(tag)) : "memory");
+    return v;
+}
+
+// Bounded wait for chunk n in stage s: its tag, then its full-barrier phase.
+__device__ __forceinline__ bool chunk_wait(unsigned long long* full, int* tags, int n, int NS, volatile int* abort_flag) {
+    const int s = n % NS;
+    if (tag_read(&tags[s]) != n) {
+        const unsigned long long t0 = globaltimer();
+        while (tag_read(&tags[s]) != n) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > dk::WAIT_NS) {
+                *abort_flag = 1;
+                raise_dev_error(FT_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    return mbar_wait(&full[s], (n / NS) & 1, abort_flag);
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(dk::NCW * 32) : "memory"); }
+__device__ __forceinline__ void group_sync(int gi) {
+    asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "n"(dk::WPG * 32) : "memory");
+}
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -158,485 +201,679 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t byte_of(const uint4& v, int b) {
-    const uint32_t w = (b < 4) ? v.x : (b < 8) ? v.y : (b < 12) ? v.z : v.w;
-    return (w >> (8 * (b & 3))) & 0xFFu;
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
     return (i == 0) ? v.x : (i == 1) ? v.y : (i == 2) ? v.z : v.w;
 }
 
+// ---------------------------------------------------------------------------- staged activation rows
+
+// Position (in halves) of element e of a row in the staged f16 layout: within
+// each 128-element K-block, the 8-element piece i (0..3) of lane-quarter q
+// (elements 32q + 8i .. +7) sits at piece (4i + q), so the four lanes of an mma
+// row group read distinct banks for every i.
+__device__ __forceinline__ int staged_pos(int e) {
+    const int kb = e >> 7, w = e & 127;
+    const int q = w >> 5, i = (w >> 3) & 3, r = w & 7;
+    return (kb << 7) + (((i << 2) + q) << 3) + r;
+}
+
+// 2^e for the small exponents of the staging pre-scale (|e| < 126): exact.
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& big) {
+    const float lo = bf16_to_f32((uint16_t)(w & 0xFFFFu)), hi = bf16_to_f32((uint16_t)(w >> 16));
+    big |= !(fabsf(lo) < 60000.0f) || !(fabsf(hi) < 60000.0f);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Rare path of the staging: rows holding a value of magnitude >= 60000 are
+// rescaled by a power of two so that they fit f16; exps[r] records it.  The
+// caller synchronises before and after.  Source: bf16 rows (x), or h words.
+__device__ __noinline__ void restage_scaled(int* exps, __half* dst, int stride, int n, int K, const uint16_t* xsrc,
+                                            const unsigned long long* hw, int ti, int nthr, bool cta_wide) {
+    auto val = [&](int r, int c) {
+        if (xsrc) return bf16_to_f32(__ldcg(xsrc + (int64_t)r * K + c));
+        const uint32_t w = (uint32_t)__ldcg(hw + (int64_t)r * (K / 2) + c / 2);
+        return bf16_to_f32((uint16_t)((c & 1) ? (w >> 16) : (w & 0xFFFFu)));
+    };
+    const int w = ti >> 5, lane = ti & 31, nw = nthr >> 5;
+    for (int r = w; r < n; r += nw) {
+        float m = 0.0f;
+        for (int i = lane; i < K; i += 32) m = fmaxf(m, fabsf(val(r, i)));
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) exps[r] = (m >= 16384.0f) ? ilogbf(m) - 14 : 0;
+    }
+    if (cta_wide) __syncthreads();
+    else consumer_sync();
+    for (int idx = ti; idx < n * K; idx += nthr) {
+        const int r = idx / K, c = idx - r * K;
+        dst[r * stride + staged_pos(c)] = __float2half_rn(val(r, c) * pow2i(-exps[r]));
+    }
+}
+
+// Stage the T activation rows x[T][K] (bf16) as f16 into dst (row stride
+// `stride` halves, staged_pos order) with every thread of the CTA.  The first
+// round of loads is issued before `mid()` runs, so the router's work overlaps
+// their latency.
+template <typename Mid>
+__device__ void stage_x(int* exps, volatile int* flag, __half* dst, int stride, const uint16_t* src, int n, int K,
+                        Mid mid) {
+    const int ti = threadIdx.x, nthr = blockDim.x;
+    const int per_row = K / 8, total = n * per_row;
+    constexpr int B = 4;  // 16-byte loads in flight per thread
+    bool big = false;
+    bool first = true;
+    for (int base = ti; first || base < total; base += B * nthr) {
+        uint4 v[B];
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int idx = base + u * nthr;
+            if (idx < total) v[u] = __ldcg(reinterpret_cast<const uint4*>(src) + idx);
+        }
+        if (first) {
+            mid();
+            first = false;
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int idx = base + u * nthr;
+            if (idx < total) {
+                const int r = idx / per_row, c = idx - r * per_row;
+                const uint4 o = make_uint4(bf16x2_to_f16x2(v[u].x, big), bf16x2_to_f16x2(v[u].y, big),
+                                           bf16x2_to_f16x2(v[u].z, big), bf16x2_to_f16x2(v[u].w, big));
+                *reinterpret_cast<uint4*>(dst + r * stride + staged_pos(c * 8)) = o;
+            }
+        }
+    }
+    if (big) *flag = 1;
+    __syncthreads();
+    if (*flag) {
+        restage_scaled(exps, dst, stride, n, K, src, nullptr, ti, nthr, true);
+        __syncthreads();
+    }
+}
+
+// h words: the gate/up phase writes h as 64-bit words {bf16 h[2j], bf16 h[2j+1],
+// uint32 epoch} (one single-copy-atomic store each), so the down phase can wait
+// for exactly the words it reads instead of for a grid-wide barrier.
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Stage all n h rows (I values each, nw = I/2 words per row) as f16 into dst,
+// waiting (bounded) for each word to carry `epoch`; consumer threads only.
+// Returns false if a wait gave up.
+__device__ bool stage_h(int* exps, volatile int* flag, __half* dst, int stride, const unsigned long long* hw, int n, int I,
+                        unsigned int epoch, volatile int* abort_flag) {
+    const int ti = threadIdx.x, nthr = dk::NCW * 32;
+    const int nw = I / 2, total = n * nw;
+    constexpr int B = 4;
+    bool big = false, ok = true;
+    for (int base = ti; base < total; base += B * nthr) {
+        unsigned long long v[B];
+        uint32_t pending = 0;
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int idx = base + u * nthr;
+            if (idx < total) {
+                v[u] = ld_relaxed_u64(hw + idx);
+                if ((uint32_t)(v[u] >> 32) != epoch) pending |= 1u << u;
+            }
+        }
+        if (pending) {
+            const unsigned long long t0 = globaltimer();
+            while (pending) {
+#pragma unroll
+                for (int u = 0; u < B; ++u)
+                    if (pending & (1u << u)) {
+                        v[u] = ld_relaxed_u64(hw + base + u * nthr);
+                        if ((uint32_t)(v[u] >> 32) == epoch) pending &= ~(1u << u);
+                    }
+                if (pending && (*abort_flag || globaltimer() - t0 > dk::WAIT_NS)) {
+                    if (!*abort_flag) raise_dev_error(FT_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int idx = base + u * nthr;
+            if (idx < total) {
+                const int r = idx / nw, c = idx - r * nw;
+                *reinterpret_cast<uint32_t*>(dst + r * stride + staged_pos(2 * c)) = bf16x2_to_f16x2((uint32_t)v[u], big);
+            }
+        }
+        if (!ok) break;
+    }
+    if (big) *flag = 1;
+    consumer_sync();
+    if (*flag) {
+        restage_scaled(exps, dst, stride, n, I, nullptr, hw, ti, nthr, false);
+        consumer_sync();
+    }
+    return ok;
+}
+
 // ---------------------------------------------------------------------------- tile math
 
-// Partial products of one 16-row tile over K-blocks kb0, kb0+step, ... (K = 128*KB)
-// against staged f16 activation rows into the mma accumulator d (rows g, g+8;
-// token columns 2q, 2q+1).  `xrow` is this lane's activation row (column g).
+// Partial products of one 16-row tile over K-blocks kb0, kb0+kstep, ... (K =
+// 128*KB) against one staged f16 row per lane column (`xrow`, staged_pos
+// order): the mma accumulator (rows g, g+8; token columns 2q, 2q+1) as
+// {d0, d1, d2, d3}.  Out of line: one copy serves both phases.
 //
-// Lane (g, q) owns the 16 code bytes q of rows g and g+8 of each K-block, i.e.
-// 32 consecutive elements per row.  mma s (of 8 per K-block) takes elements
-// 4s..4s+3 of them: the pair 4s, 4s+1 as the fragment's k = 2q, 2q+1 and the
-// pair 4s+2, 4s+3 as k = 2q+8, 2q+9.  The activations are read at the same
-// element positions, so the dot product is unchanged by this K order.
-__device__ __forceinline__ void tile_partial(const uint8_t* tile, int KB, int kb0, int step, const __half* xrow,
-                                             float (&d)[4]) {
+// Lane L = 4g + q owns code bytes [16q, 16q+16) of rows g and g+8 in each
+// K-block, i.e. elements 32q .. 32q+31.  mma s (of 8 per K-block) takes
+// elements 32q + 4s .. +3 of them: the pair 4s, 4s+1 as the fragment's
+// k = 2q, 2q+1 and the pair 4s+2, 4s+3 as k = 2q+8, 2q+9.  The activations are
+// read at the same element positions, so the dot product is unchanged by this
+// K order.  Two accumulators shorten the dependent mma chain.
+__device__ __noinline__ float4 tile_partial(const uint8_t* tile, int KB, int kb0, int kstep, const __half* xrow) {
     const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, q = lane & 3;
+    const int q = lane & 3;
     const uint8_t* scl = tile + KB * 1024;
-    const __half* xr0 = xrow + 32 * q;
-    for (int kb = kb0; kb < KB; kb += step) {
-        const uint4 c0 = *reinterpret_cast<const uint4*>(tile + kb * 1024 + (q * 8 + g) * 16);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(tile + kb * 1024 + 512 + (q * 8 + g) * 16);
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(scl + kb * 128 + (q * 8 + g) * 4);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kb = kb0; kb < KB; kb += kstep) {
+        const uint4 c0 = *reinterpret_cast<const uint4*>(tile + kb * 1024 + lane * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(tile + kb * 1024 + 512 + lane * 16);
+        const uint32_t sc = *reinterpret_cast<const uint32_t*>(scl + kb * 128 + lane * 4);
         const uint32_t sg0 = e4m3_to_f16x2_bcast(sc & 0xFFu), sg1 = e4m3_to_f16x2_bcast((sc >> 8) & 0xFFu);
         const uint32_t sh0 = e4m3_to_f16x2_bcast((sc >> 16) & 0xFFu), sh1 = e4m3_to_f16x2_bcast(sc >> 24);
-        const __half* xr = xr0 + kb * 128;
+        const __half* xr = xrow + kb * 128 + q * 8;
         uint4 xv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) xv[i] = *reinterpret_cast<const uint4*>(xr + 8 * i);
+        for (int i = 0; i < 4; ++i) xv[i] = *reinterpret_cast<const uint4*>(xr + 32 * i);
+        const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w};
+        const uint32_t cw1[4] = {c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             const uint32_t sa = (s < 4) ? sg0 : sg1, sb = (s < 4) ? sh0 : sh1;
-            const uint32_t a0 = hmul2(e2m1x2_to_f16x2(byte_of(c0, 2 * s)), sa);
-            const uint32_t a2 = hmul2(e2m1x2_to_f16x2(byte_of(c0, 2 * s + 1)), sa);
-            const uint32_t a1 = hmul2(e2m1x2_to_f16x2(byte_of(c1, 2 * s)), sb);
-            const uint32_t a3 = hmul2(e2m1x2_to_f16x2(byte_of(c1, 2 * s + 1)), sb);
+            const uint32_t w0 = cw0[s >> 1], w1 = cw1[s >> 1];
+            const int sh = (s & 1) * 16;
+            const uint32_t a0 = hmul2(e2m1x2_to_f16x2((w0 >> sh) & 0xFFu), sa);
+            const uint32_t a2 = hmul2(e2m1x2_to_f16x2((w0 >> (sh + 8)) & 0xFFu), sa);
+            const uint32_t a1 = hmul2(e2m1x2_to_f16x2((w1 >> sh) & 0xFFu), sb);
+            const uint32_t a3 = hmul2(e2m1x2_to_f16x2((w1 >> (sh + 8)) & 0xFFu), sb);
             const uint32_t b0 = word_of(xv[s >> 1], (2 * s) & 3);
             const uint32_t b1 = word_of(xv[s >> 1], (2 * s + 1) & 3);
-            mma16816(d, a0, a1, a2, a3, b0, b1);
+            if (s & 1)
+                mma16816(e, a0, a1, a2, a3, b0, b1);
+            else
+                mma16816(d, a0, a1, a2, a3, b0, b1);
         }
     }
+    return make_float4(d[0] + e[0], d[1] + e[1], d[2] + e[2], d[3] + e[3]);
 }
 
-// red layout: [NCW][16 rows][tge token columns]
-__device__ __forceinline__ void store_partial(float* red, int tge, int warp, const float (&d)[4], int ntok) {
+// ---------------------------------------------------------------------------- routing
+
+// Order-preserving key of an fp32 logit: larger value -> larger key; -0 and +0
+// map to the same key; NaN to 1 (below every number); 0 is never produced.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    if (v != v) return 1u;
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-k of one token's E logits by one warp.  Lane l holds experts
+// l*EPL .. l*EPL+EPL-1, so among equal keys the lowest lane, and within it the
+// lowest slot, is the lowest expert id.  Round j takes the warp-wide maximum key
+// (redux.sync), the lowest lane holding it, and that lane's lowest slot with it.
+// The weights are exp(l_j - l_0) / sum over the k selected, with the same
+// butterfly sum as ft_moe_route.  Lane j < k returns expert j and its weight.
+template <int EPL>
+__device__ __forceinline__ void route_token(const float* row, int E, int k, int& my_e, float& my_w, bool& bad) {
     const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, q = lane & 3;
-    float* r = red + warp * 16 * tge;
-    if (2 * q < ntok) {
-        r[g * tge + 2 * q] = d[0];
-        r[(g + 8) * tge + 2 * q] = d[2];
+    float v[EPL];
+    uint32_t key[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane * EPL + i;
+        v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+        key[i] = (e < E) ? logit_key(v[i]) : 0u;
+        bad |= (e < E) && ((v[i] != v[i]) || (v[i] == INFINITY));
     }
-    if (2 * q + 1 < ntok) {
-        r[g * tge + 2 * q + 1] = d[1];
-        r[(g + 8) * tge + 2 * q + 1] = d[3];
+    my_e = 0;
+    float my_v = -INFINITY;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        uint32_t lk = 0;
+        int li = 0;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            if (key[i] > lk) {
+                lk = key[i];
+                li = i;
+            }
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, lk);
+        const uint32_t ball = __ballot_sync(0xffffffffu, lk == gk);
+        const int wl = __ffs(ball) - 1;
+        float wv = -INFINITY;
+        if (lane == wl) {
+            wv = v[0];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (i == li) {
+                    wv = v[i];
+                    key[i] = 0u;
+                }
+        }
+        const int we = __shfl_sync(0xffffffffu, wl * EPL + li, wl);
+        wv = __shfl_sync(0xffffffffu, wv, wl);
+        if (lane == j) {
+            my_e = we;
+            my_v = wv;
+        }
+    }
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    if (m == -INFINITY || m != m) {
+        my_w = 1.0f / (float)k;
+    } else {
+        const float ej = (lane < k) ? expf(my_v - m) : 0.0f;
+        const float s = warp_sum(ej);
+        my_w = ej / s;
     }
 }
 
-// Stage `n` rows of `K` bf16 values as f16 into xs (row stride `stride`
-// halves), row r from src + row_off(r), by `nthr` threads with index `ti`;
-// `sync` is the barrier of those threads.  Rows whose values would not fit
-// f16 are pre-scaled by a power of two recorded in exps[r] (0 normally).
-template <typename RowOff, typename Sync>
-__device__ void stage_rows(int* exps, int* flag, __half* xs, int stride, const uint16_t* src, int n, int K,
-                           RowOff row_off, int ti, int nthr, Sync sync) {
-    const int per_row = K / 8;
-    for (int r = ti; r < n; r += nthr) exps[r] = 0;
-    if (ti == 0) *flag = 0;
-    sync();
-    bool big = false;
-    for (int idx = ti; idx < n * per_row; idx += nthr) {
-        const int r = idx / per_row, c = idx - r * per_row;
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(src + row_off(r) + (int64_t)c * 8));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = bf16_to_f32((uint16_t)(w[i] & 0xFFFFu)), hi = bf16_to_f32((uint16_t)(w[i] >> 16));
-            big |= !(fabsf(lo) < 60000.0f) || !(fabsf(hi) < 60000.0f);
-            const __half2 h = __floats2half2_rn(lo, hi);
-            o[i] = *reinterpret_cast<const uint32_t*>(&h);
+// The same selection for 256 < E <= 1024 with few registers: each round every
+// lane rescans its (up to 32) logits through the L1 cache; `taken` marks the
+// slots already selected.
+__device__ __noinline__ void route_token_wide(const float* row, int E, int k, int& my_e, float& my_w, bool& bad) {
+    const int lane = threadIdx.x & 31;
+    const int EPL = (E + 31) / 32;
+    uint32_t taken = 0;
+#pragma unroll 1
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane * EPL + i;
+        if (e < E) {
+            const float v = __ldg(row + e);
+            bad |= (v != v) || (v == INFINITY);
         }
-        *reinterpret_cast<uint4*>(xs + r * stride + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    if (big) *flag = 1;
-    sync();
-    if (*flag) {  // rare: rescale rows by a power of two so that they fit f16
-        const int w = ti >> 5, lane = ti & 31, nw = nthr >> 5;
-        for (int r = w; r < n; r += nw) {
-            float m = 0.0f;
-            for (int i = lane; i < K; i += 32) m = fmaxf(m, fabsf(bf16_to_f32(__ldcg(src + row_off(r) + i))));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) exps[r] = (m >= 16384.0f) ? ilogbf(m) - 14 : 0;
+    my_e = 0;
+    float my_v = -INFINITY;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        uint32_t lk = 0;
+        int li = 0;
+        float lv = -INFINITY;
+#pragma unroll 1
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane * EPL + i;
+            if (e < E && !((taken >> i) & 1u)) {
+                const float v = __ldg(row + e);
+                const uint32_t key = logit_key(v);
+                if (key > lk) {
+                    lk = key;
+                    li = i;
+                    lv = v;
+                }
+            }
         }
-        sync();
-        for (int idx = ti; idx < n * K; idx += nthr) {
-            const int r = idx / K, c = idx - r * K;
-            xs[r * stride + c] = __float2half_rn(ldexpf(bf16_to_f32(__ldcg(src + row_off(r) + c)), -exps[r]));
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, lk);
+        const uint32_t ball = __ballot_sync(0xffffffffu, lk == gk);
+        const int wl = __ffs(ball) - 1;
+        if (lane == wl) taken |= 1u << li;
+        const int we = __shfl_sync(0xffffffffu, wl * EPL + li, wl);
+        const float wv = __shfl_sync(0xffffffffu, lv, wl);
+        if (lane == j) {
+            my_e = we;
+            my_v = wv;
         }
-        sync();
+    }
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    if (m == -INFINITY || m != m) {
+        my_w = 1.0f / (float)k;
+    } else {
+        const float ej = (lane < k) ? expf(my_v - m) : 0.0f;
+        const float s = warp_sum(ej);
+        my_w = ej / s;
     }
 }
 
-// ---------------------------------------------------------------------------- work split
-
-struct Split {
-    int64_t p1_beg, p1_end;  // phase-1 tiles (over all selected experts' gate/up tiles)
-    int o_beg, o_end;        // phase-2 output tiles (16 rows of H)
-};
-
-__device__ __forceinline__ Split split_work(int U, int I, int H, int G, int c) {
-    Split s;
-    const int64_t n1 = (int64_t)U * (2 * I / 16);
-    s.p1_beg = n1 * c / G;
-    s.p1_end = n1 * (c + 1) / G;
-    const int n2 = H / 16;
-    s.o_beg = (int)((int64_t)n2 * c / G);
-    s.o_end = (int)((int64_t)n2 * (c + 1) / G);
-    return s;
+__device__ __forceinline__ void route_token_any(const float* row, int E, int k, int& my_e, float& my_w, bool& bad) {
+    if (E <= 256) route_token<8>(row, E, k, my_e, my_w, bad);
+    else route_token_wide(row, E, k, my_e, my_w, bad);
 }
 
 // ---------------------------------------------------------------------------- kernel
 
 __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
-    DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(dsm);
-    uint8_t* ring = dsm + ((sizeof(DecodeSmem) + 127) / 128) * 128;
-    __half* xs = reinterpret_cast<__half*>(ring + (size_t)a.nstages * a.stage_bytes);
-    float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + a.xs_bytes);
+    const DecodePlan& P = a.P;
+    unsigned long long* full = reinterpret_cast<unsigned long long*>(dsm + P.off_bars);
+    unsigned long long* empty = full + dk::MAXNS;
+    int* s_ids = reinterpret_cast<int*>(dsm + P.off_ids);      // [nf] expert of slot f (route mode)
+    float* s_wts = reinterpret_cast<float*>(dsm + P.off_wts);  // [nf] weight of slot f
+    int* s_plist = reinterpret_cast<int*>(dsm + P.off_plist);  // [nf] slot f of permuted row p
+    int* s_pexp = reinterpret_cast<int*>(dsm + P.off_pexp);    // [nf] expert of permuted row p
+    int* s_hexp = reinterpret_cast<int*>(dsm + P.off_hexp);    // [nf] pre-scale of staged h row p
+    int* s_ulist = reinterpret_cast<int*>(dsm + P.off_ulist);  // [nf] selected experts, ascending
+    int* s_ubeg = reinterpret_cast<int*>(dsm + P.off_ubeg);    // [nf+1] permuted-row range of each
+    int* s_uwi = reinterpret_cast<int*>(dsm + P.off_uwi);      // [nf] weight index (-1: invalid slot)
+    int* misc = reinterpret_cast<int*>(dsm + P.off_misc);
+    volatile int* abort_flag = misc + M_ABORT;
+    __half* xs = reinterpret_cast<__half*>(dsm + P.off_xs);  // x rows (phase 1)
+    __half* hs = reinterpret_cast<__half*>(dsm + P.off_hs);  // h rows (phase 2); separate, so no CTA-wide sync between
+    float* red = reinterpret_cast<float*>(dsm + P.off_red);
+    float* ybuf = reinterpret_cast<float*>(dsm + P.off_ybuf);  // [max_ot][nf][16]
+    uint8_t* ring = dsm + P.off_ring;
 
     const ft_moe_layer_weights& W = a.W;
     const int H = W.H, I = W.I, E = W.E, T = a.T, k = a.k;
     const int nf = T * k;
-    const int tge = a.tge;          // token columns per pass (<= 8)
-    const bool fast = a.fast != 0;  // all x rows and all h rows fit in xs
-    // staged-row strides in halves: the fast path holds T rows of H, then nf rows of I; the
-    // general path holds tge rows of either, at the wider stride
-    const int xstride = fast ? H + 8 : a.xs_stride;
-    const int hstride = fast ? I + 8 : a.xs_stride;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    auto all_sync = [] { __syncthreads(); };
+    const int NS = P.nstages;
 
-    // ---------------- prologue (all warps): barriers, x, routing, grouping
-    if (tid < dk::MAXNS) {
-        mbar_init(&sm.full[tid], 1);
-        mbar_init(&sm.empty[tid], 1);
+    if (tid == 0) {
+#pragma unroll 1
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], dk::WPG);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        misc[M_FLAG] = 0;
+        misc[M_ABORT] = 0;
     }
-    for (int i = tid; i < dk::MAX_OUT_TILES * 16 * dk::MAXT; i += dk::THREADS) (&sm.oacc[0][0][0])[i] = 0.0f;
-    float* scratch = reinterpret_cast<float*>(ring);  // the ring is free until the producer starts
-    if (a.logits) {
-        for (int i = tid; i < T * E; i += dk::THREADS) scratch[i] = a.logits[i];
-        for (int f = tid; f < nf; f += dk::THREADS) sm.ids[f] = f % k;  // stays in range if logits are NaN
-    } else {
-        for (int i = tid; i <= E; i += dk::THREADS) reinterpret_cast<int*>(scratch)[i] = a.offsets[i];
+    if (tid < dk::MAXT) misc[M_XEXP + tid] = 0;
+    if (tid < dk::MAXNS) misc[M_TAGS + tid] = -1;
+    for (int i = tid; i < nf; i += dk::THREADS) s_hexp[i] = 0;
+    __syncthreads();
+    // inputs (and the workspace) may be written by the preceding kernel in the stream
+    griddep_wait();
+    // this call's epoch: calls sharing a workspace each add G to its counter.  The producer
+    // lane takes it (off the router's path) and publishes it at the end of the prologue.
+    unsigned int old_count = 0;
+    if (tid == dk::NCW * 32) old_count = atomicAdd(a.bar, 1u);
+
+    // ---------------- prologue: every thread stages x; warps < T route their token meanwhile
+    int my_e = 0;
+    float my_w = 0.0f;
+    bool bad = false;
+    const bool route_mode = a.logits != nullptr;
+    stage_x(misc + M_XEXP, misc + M_FLAG, xs, P.xs_stride, a.x, T, H, [&] {
+        if (route_mode && warp < T) route_token_any(a.logits + (int64_t)warp * E, E, k, my_e, my_w, bad);
+    });
+    if (route_mode) {
+        if (warp < T) {
+            if (__any_sync(0xffffffffu, bad) && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
+            if (lane < k) {
+                s_ids[warp * k + lane] = my_e;
+                s_wts[warp * k + lane] = my_w;
+                if (c == 0 && a.ids_out) {
+                    a.ids_out[warp * k + lane] = my_e;
+                    a.w_out[warp * k + lane] = my_w;
+                }
+            }
+        }
+        __syncthreads();
+        // grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}
         for (int f = tid; f < nf; f += dk::THREADS) {
-            int pf = a.perm[f];
+            const int e = s_ids[f];
+            int pos = 0;
+#pragma unroll 1
+            for (int f2 = 0; f2 < nf; ++f2) {
+                const int e2 = s_ids[f2];
+                pos += (e2 < e) || (e2 == e && f2 < f);
+            }
+            s_plist[pos] = f;
+            s_pexp[pos] = e;
+        }
+    } else {
+        for (int p = tid; p < nf; p += dk::THREADS) {
+            int pf = a.perm[p];
             if (pf < 0 || pf >= nf) {
                 raise_dev_error(FT_DEVERR_BAD_INDEX);
                 pf = 0;
             }
-            sm.plist[f] = pf;
-            sm.wts[f] = a.w_in[f];
-        }
-    }
-    if (fast)  // all T activation rows, once (its barriers also publish the loads above)
-        stage_rows(sm.xexp, &sm.flag, xs, xstride, a.x, T, H, [&](int r) { return (int64_t)r * H; }, tid,
-                   dk::THREADS, all_sync);
-    else
-        __syncthreads();
-
-    if (a.logits) {
-        // top-k by rank: candidate e of token t has rank #{e2 : l2 > l or (l2 == l and e2 < e)};
-        // equal logits go to the lower expert id, as in ft_moe_route
-        bool bad = false;
-        for (int cand = tid; cand < T * E; cand += dk::THREADS) {
-            const int t = cand / E, e = cand - t * E;
-            const float* row = scratch + t * E;
-            const float v = row[e];
-            bad |= (v != v) || (v == INFINITY);
-            int r = 0;
-            for (int e2 = 0; e2 < E; ++e2) {
-                const float v2 = row[e2];
-                r += (v2 > v) || (v2 == v && e2 < e);
-            }
-            if (r < k) {
-                sm.ids[t * k + r] = e;
-                sm.selv[t * k + r] = v;
-            }
-        }
-        if (bad) raise_dev_error(FT_DEVERR_NAN_LOGIT);
-        __syncthreads();
-        if (warp < T) {  // weights as the router computes them: exp(l_j - l_0) / sum, same butterfly sum
-            const float vj = (lane < k) ? sm.selv[warp * k + lane] : -INFINITY;
-            const float m = __shfl_sync(0xffffffffu, vj, 0);
-            float wj;
-            if (m == -INFINITY || m != m) {
-                wj = 1.0f / (float)k;
-            } else {
-                const float ej = (lane < k) ? expf(vj - m) : 0.0f;
-                const float sum = warp_sum(ej);
-                wj = ej / sum;
-            }
-            if (lane < k) {
-                sm.wts[warp * k + lane] = wj;
-                if (c == 0 && a.ids_out) {
-                    a.ids_out[warp * k + lane] = sm.ids[warp * k + lane];
-                    a.w_out[warp * k + lane] = wj;
-                }
-            }
-        }
-        // grouping: plist position of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}
-        for (int f = tid; f < nf; f += dk::THREADS) {
-            const int e = sm.ids[f];
-            int pos = 0;
-            for (int f2 = 0; f2 < nf; ++f2) {
-                const int e2 = sm.ids[f2];
-                pos += (e2 < e) || (e2 == e && f2 < f);
-            }
-            sm.plist[pos] = f;
-            sm.pexp[pos] = e;
-        }
-    } else {
-        const int* offs = reinterpret_cast<const int*>(scratch);
-        for (int p = tid; p < nf; p += dk::THREADS) {  // expert owning position p: last e with offs[e] <= p
+            s_plist[p] = pf;
+            s_wts[p] = a.w_in ? a.w_in[p] : 0.0f;  // indexed by slot f: w_in is [T][k]
+            // expert owning row p: last e with offsets[e] <= p
             int lo = 0, hi = E - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
-                if (offs[mid] <= p) lo = mid;
+                if (__ldg(a.offsets + mid) <= p) lo = mid;
                 else hi = mid - 1;
             }
-            if (offs[lo] > p || offs[lo + 1] <= p || offs[E] != nf) raise_dev_error(FT_DEVERR_BAD_INDEX);
-            sm.pexp[p] = lo;
+            if (__ldg(a.offsets + lo) > p || __ldg(a.offsets + lo + 1) <= p || __ldg(a.offsets + E) != nf)
+                raise_dev_error(FT_DEVERR_BAD_INDEX);
+            s_pexp[p] = lo;
         }
     }
     __syncthreads();
-    // selected experts = segment starts of pexp
-    for (int p = tid; p < nf; p += dk::THREADS) {
-        if (p == 0 || sm.pexp[p] != sm.pexp[p - 1]) {
-            int u = 0;
-            for (int p2 = 1; p2 <= p; ++p2) u += (sm.pexp[p2] != sm.pexp[p2 - 1]);
-            sm.ulist[u] = sm.pexp[p];
-            sm.ubeg[u] = p;
+    // every thread has read the x-staging flag: reset it for the h staging (published below)
+    if (tid == 32) misc[M_FLAG] = 0;
+    // selected experts = segment starts of pexp (warp 0, ballot scan)
+    if (warp == 0) {
+        int run = 0;
+#pragma unroll 1
+        for (int p0 = 0; p0 < nf; p0 += 32) {
+            const int p = p0 + lane;
+            const bool start = p < nf && (p == 0 || s_pexp[p] != s_pexp[p - 1]);
+            const uint32_t b = __ballot_sync(0xffffffffu, start);
+            if (start) {
+                const int u = run + __popc(b & ((1u << lane) - 1u));
+                s_ulist[u] = s_pexp[p];
+                s_ubeg[u] = p;
+                s_uwi[u] = weight_index(W, s_pexp[p]);
+            }
+            run += __popc(b);
+        }
+        if (lane == 0) {
+            misc[M_U] = run;
+            s_ubeg[run] = nf;
         }
     }
-    if (tid == 0) {
-        int u = (nf > 0) ? 1 : 0;
-        for (int p2 = 1; p2 < nf; ++p2) u += (sm.pexp[p2] != sm.pexp[p2 - 1]);
-        sm.U = u;
-        sm.ubeg[u] = nf;
-    }
+    if (tid == dk::NCW * 32) misc[M_EPOCH] = (int)(old_count / (unsigned)G + 1u);
     __syncthreads();
-    const int U = sm.U;
-    for (int u = tid; u < U; u += dk::THREADS) {
-        const int wi = weight_index(W, sm.ulist[u]);
-        sm.uwi[u] = wi;
-        for (int j = 0; j < 3; ++j) sm.uts[u][j] = (wi >= 0) ? W.tscale[(int64_t)wi * W.tscale_stride + j] : 0.0f;
-    }
-    __syncthreads();
+    const int U = misc[M_U];
+    const unsigned int epoch = (unsigned int)misc[M_EPOCH];
 
-    const Split sp = split_work(U, I, H, G, c);
+    // ---------------- work split
     const int tiles_gu = 2 * I / 16;
     const int KB1 = H / 128, KB2 = I / 128;
     const int bytes1 = 9 * H, bytes2 = 9 * I;  // one 16-row tile of [.][H] or [.][I]
-    const int J = fast ? max(1, min(a.stage_bytes / bytes2, dk::NCW)) : 1;  // experts per phase-2 slot
-    const int n_p1 = (int)(sp.p1_end - sp.p1_beg);
-    const int n_ot = sp.o_end - sp.o_beg;
+    const int n1 = U * tiles_gu;  // <= 512 * 256
+    const int p1_beg = (int)((long long)n1 * c / G), p1_end = (int)((long long)n1 * (c + 1) / G);
+    const int n2 = H / 16;
+    const int o_beg = n2 * c / G, o_end = n2 * (c + 1) / G;  // n2 * G <= 64 K
+    const int J = P.J;
+    const int n_p1 = p1_end - p1_beg;
+    const int n_ot = o_end - o_beg;
     const int n_jg = (U + J - 1) / J;  // expert groups per output tile
     const int n_chunks = n_p1 + n_ot * n_jg;
 
     if (warp == dk::NCW) {
         // ---------------- producer: stream tiles into the ring
         if (lane == 0) {
-            for (int n = 0; n < n_chunks; ++n) {
-                const int s = n % a.nstages, use = n / a.nstages;
-                if (use > 0 && !mbar_wait(&sm.empty[s], (use - 1) & 1)) break;
-                uint8_t* dst = ring + (size_t)s * a.stage_bytes;
+            int issued = 0;
+            for (int n = 0; n < n_chunks; ++n, ++issued) {
+                const int s = n % NS, use = n / NS;
+                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag)) break;
+                uint8_t* dst = ring + (size_t)s * P.stage_bytes;
                 if (n < n_p1) {
-                    const int64_t t = sp.p1_beg + n;
-                    const int u = (int)(t / tiles_gu), lt = (int)(t % tiles_gu);
-                    const int wi = sm.uwi[u];
+                    const int t = p1_beg + n;
+                    const int u = t / tiles_gu, lt = t - u * tiles_gu;
+                    const int wi = s_uwi[u];
                     if (wi < 0) {
-                        mbar_arrive(&sm.full[s]);
+                        mbar_arrive(&full[s]);
                     } else {
-                        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)bytes1);
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)bytes1);
                         bulk_g2s(dst, W.gu_codes + (int64_t)wi * W.gu_codes_stride + (int64_t)lt * bytes1,
-                                 (uint32_t)bytes1, &sm.full[s]);
+                                 (uint32_t)bytes1, &full[s]);
                     }
+                    tag_publish(&misc[M_TAGS + s], n);
                 } else {
                     const int m = n - n_p1;
-                    const int jg = m / n_ot, ot = sp.o_beg + m % n_ot;
+                    const int otl = m / n_jg, jg = m % n_jg, ot = o_beg + otl;
                     const int u0 = jg * J, nj = min(J, U - u0);
                     uint32_t tx = 0;
-                    for (int jj = 0; jj < nj; ++jj) tx += (sm.uwi[u0 + jj] >= 0) ? (uint32_t)bytes2 : 0u;
-                    mbar_arrive_expect_tx(&sm.full[s], tx);
+                    for (int jj = 0; jj < nj; ++jj) tx += (s_uwi[u0 + jj] >= 0) ? (uint32_t)bytes2 : 0u;
+                    mbar_arrive_expect_tx(&full[s], tx);
                     for (int jj = 0; jj < nj; ++jj) {
-                        const int wi = sm.uwi[u0 + jj];
+                        const int wi = s_uwi[u0 + jj];
                         if (wi >= 0)
-                            bulk_g2s(dst + jj * bytes2,
-                                     W.d_codes + (int64_t)wi * W.d_codes_stride + (int64_t)ot * bytes2,
-                                     (uint32_t)bytes2, &sm.full[s]);
+                            bulk_g2s(dst + jj * bytes2, W.d_codes + (int64_t)wi * W.d_codes_stride + (int64_t)ot * bytes2,
+                                     (uint32_t)bytes2, &full[s]);
                     }
+                    tag_publish(&misc[M_TAGS + s], n);
                 }
             }
+            // the CTA must not exit with copies still landing in its shared memory: wait
+            // (bounded, even after an abort) for the last use of every stage issued
+            const unsigned long long t0 = globaltimer();
+            for (int n = max(0, issued - NS); n < issued; ++n)
+                while (!mbar_try_wait(&full[n % NS], (n / NS) & 1) && globaltimer() - t0 < dk::WAIT_NS) {
+                }
         }
         return;
     }
 
-    // ---------------- consumers (warps 0 .. NCW-1)
-    auto csync = [] { consumer_sync(); };
-    const int g8 = lane >> 2;  // this lane's mma column
+    // ---------------- consumers (warps 0 .. NCW-1), phase 1: gate/up tiles -> h words
+    const int gi = warp / dk::WPG, wig = warp % dk::WPG, gtid = tid % (dk::WPG * 32);
+    const int g8 = lane >> 2, q4 = lane & 3;
+    const int TC = P.tcol;
+    const int hw_row = I / 2;  // h words per permuted row
+    unsigned long long* hw = reinterpret_cast<unsigned long long*>(a.hbuf);
+    float* gred = red + gi * 2 * dk::WPG * 16 * TC;  // this group's two partial buffers [WPG][16][TC]
     int buf = 0;
-    int staged_u = -1, staged_g = -1;
-    for (int n = 0; n < n_p1; ++n) {
-        const int s = n % a.nstages, use = n / a.nstages;
-        const int64_t t = sp.p1_beg + n;
-        const int u = (int)(t / tiles_gu), lt = (int)(t % tiles_gu);
-        const int wi = sm.uwi[u];
-        const int pb = sm.ubeg[u], tu = sm.ubeg[u + 1] - pb;
-        mbar_wait(&sm.full[s], use & 1);
-        const uint8_t* tile = ring + (size_t)s * a.stage_bytes;
-        const int ngroups = (tu + tge - 1) / tge;
-        for (int gi = 0; gi < ngroups; ++gi) {
-            const int g0 = gi * tge, nt = min(tge, tu - g0);
-            if (!fast && (staged_u != u || staged_g != gi)) {
-                csync();  // earlier readers of xs / xexp are done
-                stage_rows(sm.xexp, &sm.flag, xs, xstride, a.x, nt, H,
-                           [&](int r) { return (int64_t)(sm.plist[pb + g0 + r] / k) * H; }, tid, dk::NCW * 32, csync);
-                staged_u = u;
-                staged_g = gi;
-            }
+    for (int n = gi; n < n_p1; n += dk::NG) {
+        const int s = n % NS;
+        const int t = p1_beg + n;
+        const int u = t / tiles_gu, lt = t - u * tiles_gu;
+        const int wi = s_uwi[u];
+        const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
+        // tensor scales, in flight while the tile lands
+        const float tsg = (wi >= 0) ? W.tscale[(int64_t)wi * W.tscale_stride + 0] : 0.0f;
+        const float tsu = (wi >= 0) ? W.tscale[(int64_t)wi * W.tscale_stride + 1] : 0.0f;
+        chunk_wait(full, misc + M_TAGS, n, NS, abort_flag);
+        const uint8_t* tile = ring + (size_t)s * P.stage_bytes;
+        float* rb = gred + buf * dk::WPG * 16 * TC;
+        for (int c0 = 0; c0 < tu; c0 += 8) {
+            const int nt = min(8, tu - c0);
             const int col = min(g8, nt - 1);
-            const int xr = fast ? sm.plist[pb + g0 + col] / k : col;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            if (wi >= 0) tile_partial(tile, KB1, warp, dk::NCW, xs + xr * xstride, d);
-            float* rb = red + buf * dk::NCW * 16 * tge;
-            store_partial(rb, tge, warp, d, nt);
-            consumer_sync();
-            if (gi == ngroups - 1 && tid == 0) mbar_arrive(&sm.empty[s]);
-            if (tid < 8 * nt) {
-                const int p = tid / nt, tt = tid - p * nt;
-                const int nw = min(dk::NCW, KB1);
-                float gs = 0.f, us = 0.f;
-                for (int w = 0; w < nw; ++w) {
-                    gs += rb[(w * 16 + 2 * p) * tge + tt];
-                    us += rb[(w * 16 + 2 * p + 1) * tge + tt];
-                }
-                const int f = sm.plist[pb + g0 + tt];
-                float hv = 0.0f;
-                if (wi >= 0) {
-                    const float sc = ldexpf(1.0f, sm.xexp[fast ? f / k : tt]);
-                    hv = silu_f32(gs * sm.uts[u][0] * sc) * (us * sm.uts[u][1] * sc);
-                }
-                a.hbuf[(int64_t)f * I + lt * 8 + p] = bf16_bits(hv);
+            const int xr = s_plist[pb + c0 + col] / k;  // token of this lane's column
+            float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (wi >= 0) dv = tile_partial(tile, KB1, wig, dk::WPG, xs + xr * P.xs_stride);
+            const float d[4] = {dv.x, dv.y, dv.z, dv.w};
+            float* r = rb + wig * 16 * TC;
+            if (2 * q4 < nt) {
+                r[g8 * TC + c0 + 2 * q4] = d[0];
+                r[(g8 + 8) * TC + c0 + 2 * q4] = d[2];
             }
-            buf ^= 1;
+            if (2 * q4 + 1 < nt) {
+                r[g8 * TC + c0 + 2 * q4 + 1] = d[1];
+                r[(g8 + 8) * TC + c0 + 2 * q4 + 1] = d[3];
+            }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        group_sync(gi);
+        // h = silu(g) * u for the tile's 8 (gate, up) row pairs: word j holds pairs 2j, 2j+1
+        for (int idx = gtid; idx < 4 * tu; idx += dk::WPG * 32) {
+            const int j = idx / tu, tt = idx - j * tu;
+            float hv[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int p = 2 * j + h2;
+                float gs = 0.f, us = 0.f;
+#pragma unroll
+                for (int w = 0; w < dk::WPG; ++w) {
+                    gs += rb[(w * 16 + 2 * p) * TC + tt];
+                    us += rb[(w * 16 + 2 * p + 1) * TC + tt];
+                }
+                if (wi >= 0) {
+                    const float sc = pow2i(misc[M_XEXP + s_plist[pb + tt] / k]);
+                    hv[h2] = silu_f32(gs * tsg * sc) * (us * tsu * sc);
+                }
+            }
+            const unsigned long long word = (unsigned long long)bf16_bits(hv[0]) |
+                                            ((unsigned long long)bf16_bits(hv[1]) << 16) | ((unsigned long long)epoch << 32);
+            st_relaxed_u64(hw + (int64_t)(pb + tt) * hw_row + lt * 4 + j, word);
+        }
+        buf ^= 1;
     }
 
-    // ---------------- grid barrier: every CTA's h is written
-    __threadfence();
-    consumer_sync();
-    if (tid == 0) {
-        const unsigned int old = atomicAdd(a.bar, 1u);
-        const unsigned int target = (old / (unsigned)G + 1u) * (unsigned)G;
-        const unsigned long long t0 = globaltimer();
-        while (true) {
+    // ---------------- phase 2: down projection over this CTA's output rows
+    if (n_ot > 0) {  // all h rows (permuted order), as each becomes available
+        stage_h(s_hexp, misc + M_FLAG, hs, P.hs_stride, hw, nf, I, epoch, abort_flag);
+        // once every CTA of this grid has started (the call counter says so), the next
+        // kernel in the stream may be scheduled: it cannot take an SM one of ours still
+        // needs, and it waits for our completion itself before reading anything
+        if (tid == 0) {
             unsigned int v;
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.bar) : "memory");
-            if ((int)(v - target) >= 0) break;
-            if (globaltimer() - t0 > dk::WAIT_NS) {
-                raise_dev_error(FT_DEVERR_TIMEOUT);
-                break;
-            }
-            __nanosleep(32);
+            if ((int)(v - epoch * (unsigned)G) >= 0) griddep_launch_dependents();
         }
     }
-    consumer_sync();
-
-    // ---------------- phase 2: down projection and combine over this CTA's output rows
-    if (fast && n_ot > 0)  // all h rows in plist order, once
-        stage_rows(sm.rexp, &sm.flag, xs, hstride, a.hbuf, nf, I,
-                   [&](int r) { return (int64_t)sm.plist[r] * I; }, tid, dk::NCW * 32, csync);
-    staged_u = -1;
-    staged_g = -1;
-    const int wpe = dk::NCW / J;  // warps per expert of a slot
-    for (int m = 0; m < n_ot * n_jg; ++m) {
-        const int n = n_p1 + m;
-        const int s = n % a.nstages, use = n / a.nstages;
-        const int jg = m / n_ot, otl = m % n_ot, ot = sp.o_beg + otl;
-        const int u0 = jg * J, nj = min(J, U - u0);
-        mbar_wait(&sm.full[s], use & 1);
-        const uint8_t* slot = ring + (size_t)s * a.stage_bytes;
-        if (fast) {
-            // warp w works on expert jj = w / wpe of the slot, K-blocks w % wpe, w % wpe + wpe, ...
-            const int jj = warp / wpe;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            int nt = 1;
-            if (jj < nj) {
+    {
+        // chunks n_p1 .. n_chunks-1, round robin over the groups continuing phase 1's order
+        int n = n_p1 + ((gi - n_p1) % dk::NG + dk::NG) % dk::NG;
+        for (; n < n_chunks; n += dk::NG) {
+            const int s = n % NS;
+            const int m = n - n_p1;
+            const int otl = m / n_jg, jg = m % n_jg, ot = o_beg + otl;
+            const int u0 = jg * J, nj = min(J, U - u0);
+            const int wi0 = (wig < nj) ? s_uwi[u0 + wig] : -1;
+            const float tsd0 = (wi0 >= 0) ? W.tscale[(int64_t)wi0 * W.tscale_stride + 2] : 0.0f;
+            chunk_wait(full, misc + M_TAGS, n, NS, abort_flag);
+            const uint8_t* slot = ring + (size_t)s * P.stage_bytes;
+            for (int jj = wig; jj < nj; jj += dk::WPG) {
                 const int u = u0 + jj;
-                const int pb = sm.ubeg[u], tu = sm.ubeg[u + 1] - pb;
-                nt = tu;
-                const int xr = pb + min(g8, tu - 1);
-                if (sm.uwi[u] >= 0) tile_partial(slot + jj * bytes2, KB2, warp % wpe, wpe, xs + xr * hstride, d);
-            }
-            float* rb = red + buf * dk::NCW * 16 * tge;
-            store_partial(rb, tge, warp, d, min(nt, tge));
-            consumer_sync();
-            if (tid == 0) mbar_arrive(&sm.empty[s]);
-            if (tid < 16 * T) {  // (row r, token tok): add this slot's experts in ascending order
-                const int r = tid / T, tok = tid - r * T;
-                const int nw = min(wpe, KB2);
-                float acc = sm.oacc[otl][r][tok];
-                for (int j2 = 0; j2 < nj; ++j2) {
-                    const int u = u0 + j2;
-                    const int pb = sm.ubeg[u], tu = sm.ubeg[u + 1] - pb;
-                    for (int tt = 0; tt < tu; ++tt) {
-                        const int f = sm.plist[pb + tt];
-                        if (f / k != tok) continue;
-                        float ys = 0.f;
-                        for (int w = 0; w < nw; ++w) ys += rb[((j2 * wpe + w) * 16 + r) * tge + tt];
-                        ys = (sm.uwi[u] >= 0) ? ys * sm.uts[u][2] * ldexpf(1.0f, sm.rexp[pb + tt]) : 0.0f;
-                        acc += sm.wts[f] * ys;
-                        if (a.y) a.y[(int64_t)(pb + tt) * H + ot * 16 + r] = ys;
+                const int wi = s_uwi[u];
+                const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
+                const float tsd = (jj == wig) ? tsd0 : ((wi >= 0) ? W.tscale[(int64_t)wi * W.tscale_stride + 2] : 0.0f);
+                for (int c0 = 0; c0 < tu; c0 += 8) {
+                    const int nt = min(8, tu - c0);
+                    const int col = min(g8, nt - 1);
+                    float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (wi >= 0) dv = tile_partial(slot + jj * bytes2, KB2, 0, 1, hs + (pb + c0 + col) * P.hs_stride);
+                    const float d[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int cc = c0 + 2 * q4 + h2;  // column of d[h2] (row g8) and d[2 + h2] (row g8 + 8)
+                        if (2 * q4 + h2 < nt) {
+                            const int p = pb + cc;
+                            const float sc = (wi >= 0) ? tsd * pow2i(s_hexp[p]) : 0.0f;
+                            const int f = s_plist[p];
+                            const float y0 = d[h2] * sc, y1 = d[2 + h2] * sc;
+                            ybuf[(otl * nf + f) * 16 + g8] = y0;
+                            ybuf[(otl * nf + f) * 16 + g8 + 8] = y1;
+                            if (a.y) {
+                                a.y[(int64_t)p * H + ot * 16 + g8] = y0;
+                                a.y[(int64_t)p * H + ot * 16 + g8 + 8] = y1;
+                            }
+                        }
                     }
                 }
-                sm.oacc[otl][r][tok] = acc;
             }
-            buf ^= 1;
-        } else {
-            // one expert per slot; its tokens in groups of tge, restaged when they change
-            const int u = u0;
-            const int wi = sm.uwi[u];
-            const int pb = sm.ubeg[u], tu = sm.ubeg[u + 1] - pb;
-            const int ngroups = (tu + tge - 1) / tge;
-            for (int gi = 0; gi < ngroups; ++gi) {
-                const int g0 = gi * tge, nt = min(tge, tu - g0);
-                if (staged_u != u || staged_g != gi) {
-                    csync();
-                    stage_rows(sm.xexp, &sm.flag, xs, hstride, a.hbuf, nt, I,
-                               [&](int r) { return (int64_t)sm.plist[pb + g0 + r] * I; }, tid, dk::NCW * 32, csync);
-                    staged_u = u;
-                    staged_g = gi;
-                }
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                if (wi >= 0) tile_partial(slot, KB2, warp, dk::NCW, xs + min(g8, nt - 1) * hstride, d);
-                float* rb = red + buf * dk::NCW * 16 * tge;
-                store_partial(rb, tge, warp, d, nt);
-                consumer_sync();
-                if (gi == ngroups - 1 && tid == 0) mbar_arrive(&sm.empty[s]);
-                if (tid < 16 * nt) {
-                    const int r = tid / nt, tt = tid - r * nt;
-                    const int nw = min(dk::NCW, KB2);
-                    float ys = 0.f;
-                    for (int w = 0; w < nw; ++w) ys += rb[(w * 16 + r) * tge + tt];
-                    const int f = sm.plist[pb + g0 + tt];
-                    ys = (wi >= 0) ? ys * sm.uts[u][2] * ldexpf(1.0f, sm.xexp[tt]) : 0.0f;
-                    sm.oacc[otl][r][f / k] += sm.wts[f] * ys;
-                    if (a.y) a.y[(int64_t)(pb + g0 + tt) * H + ot * 16 + r] = ys;
-                }
-                buf ^= 1;
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
     }
     consumer_sync();
+    // combine: out[t][row] = bf16(sum_j w[t][j] * y[t*k + j][row]) in slot order j
     if (a.out) {
         for (int i = tid; i < n_ot * 16 * T; i += dk::NCW * 32) {
             const int tok = i / (n_ot * 16), rr = i - tok * n_ot * 16;
-            const int otl = rr / 16, r = rr % 16;
-            a.out[(int64_t)tok * H + (sp.o_beg + otl) * 16 + r] = bf16_bits(sm.oacc[otl][r][tok]);
+            const int otl = rr >> 4, r = rr & 15;
+            float acc = 0.0f;
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) {
+                const int f = tok * k + j;
+                acc += s_wts[f] * ybuf[(otl * nf + f) * 16 + r];
+            }
+            a.out[(int64_t)tok * H + (o_beg + otl) * 16 + r] = bf16_bits(acc);
         }
     }
 }
@@ -655,22 +892,22 @@ __global__ void __launch_bounds__(256) k_pack_tiles(const uint8_t* __restrict__ 
         const int64_t tile = i / per_tile;
         int64_t r = i % per_tile;
         uint8_t* dst = tiles + tile * tile_bytes;
-        if (r < KB * 64) {  // code piece: (kb, h, q, g)
+        if (r < KB * 64) {  // code piece (kb, h, g, q): bytes 16q..16q+15 of row 8h+g's 64 bytes in block kb
             const int64_t kb = r / 64;
             const int rem = (int)(r % 64);
-            const int h = rem / 32, q = (rem / 8) & 3, g = rem & 7;
+            const int h = rem / 32, g = (rem / 4) & 7, q = rem & 3;
             const int64_t row = tile * 16 + 8 * h + g;
             const uint4 v = *reinterpret_cast<const uint4*>(codes + row * codes_ld + kb * 64 + 16 * q);
-            *reinterpret_cast<uint4*>(dst + kb * 1024 + h * 512 + (q * 8 + g) * 16) = v;
-        } else {  // scale word: (kb, q, g)
+            *reinterpret_cast<uint4*>(dst + kb * 1024 + h * 512 + (g * 4 + q) * 16) = v;
+        } else {  // scale word (kb, g, q): blocks 2q, 2q+1 of rows g and g+8
             r -= KB * 64;
             const int64_t kb = r / 32;
             const int rem = (int)(r % 32);
-            const int q = rem / 8, g = rem & 7;
+            const int g = rem / 4, q = rem & 3;
             const uint8_t* s0 = scales + (tile * 16 + g) * scales_ld + kb * 8 + 2 * q;
             const uint8_t* s1 = scales + (tile * 16 + 8 + g) * scales_ld + kb * 8 + 2 * q;
             const uint32_t w = (uint32_t)s0[0] | ((uint32_t)s0[1] << 8) | ((uint32_t)s1[0] << 16) | ((uint32_t)s1[1] << 24);
-            *reinterpret_cast<uint32_t*>(dst + KB * 1024 + kb * 128 + (q * 8 + g) * 4) = w;
+            *reinterpret_cast<uint32_t*>(dst + KB * 1024 + kb * 128 + (g * 4 + q) * 4) = w;
         }
     }
 }
@@ -692,67 +929,84 @@ static int sm_count() {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-struct DecodeLaunch {
-    int nstages, stage_bytes, xs_stride, xs_bytes, tge, fast;
-    size_t smem;
-};
-
-// Shared memory: static part, ring of stages (one 16-row tile of the wider
-// matrix each), staging area for f16 activation / h rows, partial tiles.
-static bool plan_decode(int T, int k, int H, int I, DecodeLaunch& p) {
-    const size_t budget = 227 * 1024;
-    const size_t fixed = align_up(sizeof(DecodeSmem), 128);
-    p.stage_bytes = (int)align_up((size_t)9 * std::max(H, I), 128);
-    p.xs_stride = std::max(H, I) + 8;
-    auto try_plan = [&](bool fast, int tge) {
-        const size_t red = align_up((size_t)2 * dk::NCW * 16 * tge * sizeof(float), 128);
-        const size_t xs = fast ? align_up((size_t)std::max(T * (H + 8), T * k * (I + 8)) * 2, 128)
-                               : align_up((size_t)tge * p.xs_stride * 2, 128);
-        if (fixed + xs + red + 2 * (size_t)p.stage_bytes > budget) return false;
-        p.fast = fast ? 1 : 0;
-        p.tge = tge;
-        p.xs_bytes = (int)xs;
-        p.nstages = (int)std::min<size_t>(dk::MAXNS, (budget - fixed - xs - red) / p.stage_bytes);
-        p.smem = fixed + (size_t)p.nstages * p.stage_bytes + xs + red;
-        return true;
+// Shared memory: barriers and routing tables, staged activations (x in phase
+// 1, h in phase 2, same area), the groups' partial tiles, the per-slot down
+// outputs, and the ring (one 16-row tile of the wider matrix per stage).
+static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::string& why) {
+    const int nf = T * k;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 128);
+        return (int)o;
     };
-    // fast path: every x row and every h row staged at once (T <= 8, one mma pass per expert)
-    if (T <= dk::TG && try_plan(true, T)) return true;
-    for (int tge = std::min(T, dk::TG); tge >= 1; tge /= 2)
-        if (try_plan(false, tge)) return true;
-    return false;
+    p.off_bars = take(2 * dk::MAXNS * 8);
+    p.off_ids = take((size_t)nf * 4);
+    p.off_wts = take((size_t)nf * 4);
+    p.off_plist = take((size_t)nf * 4);
+    p.off_pexp = take((size_t)nf * 4);
+    p.off_hexp = take((size_t)nf * 4);
+    p.off_ulist = take((size_t)nf * 4);
+    p.off_ubeg = take((size_t)(nf + 1) * 4);
+    p.off_uwi = take((size_t)nf * 4);
+    p.off_misc = take((4 + dk::MAXT + dk::MAXNS) * 4);
+    p.xs_stride = H + dk::XPAD;
+    p.hs_stride = I + dk::XPAD;
+    const size_t xs = (size_t)T * p.xs_stride * 2, hs = (size_t)nf * p.hs_stride * 2;
+    if (xs + hs > dk::XS_BUDGET) {
+        why = "activations of " + std::to_string(T) + " tokens and their " + std::to_string(nf) +
+              " expert rows do not fit the fused kernel's staging area";
+        return false;
+    }
+    p.off_xs = take(xs);
+    p.off_hs = take(hs);
+    p.tcol = T;
+    p.off_red = take((size_t)dk::NG * 2 * dk::WPG * 16 * T * 4);
+    const int n2 = H / 16;
+    p.max_ot = (n2 + G - 1) / G;
+    p.off_ybuf = take((size_t)p.max_ot * nf * 16 * 4);
+    p.stage_bytes = (int)align_up((size_t)9 * std::max(H, I), 128);
+    p.off_ring = (int)off;
+    if (off + 2 * (size_t)p.stage_bytes > dk::SMEM_BUDGET) {
+        why = "layer too large for the fused kernel's shared memory";
+        return false;
+    }
+    p.nstages = (int)std::min<size_t>(dk::MAXNS, (dk::SMEM_BUDGET - off) / p.stage_bytes);
+    p.smem = (int)(off + (size_t)p.nstages * p.stage_bytes);
+    p.J = std::max(1, std::min(p.stage_bytes / (9 * I), 16));
+    return true;
 }
 
 static ft_status launch_decode(const DecodeArgs& args0, ft_stream_t stream, const char* fn) {
-    DecodeLaunch p;
     const ft_moe_layer_weights& W = args0.W;
-    if (!plan_decode(args0.T, args0.k, W.H, W.I, p))
-        return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": layer too large for the decode kernel's shared memory");
     const int G = sm_count();
-    if (W.H / 16 > dk::MAX_OUT_TILES * G)
-        return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": H too large for one output tile range per SM");
-    const size_t ring = (size_t)p.nstages * p.stage_bytes;
-    if ((size_t)args0.T * W.E * 4 > ring || (size_t)(W.E + 1) * 4 > ring)
-        return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": router logits do not fit the prologue scratch");
     DecodeArgs a = args0;
-    a.nstages = p.nstages;
-    a.stage_bytes = p.stage_bytes;
-    a.xs_stride = p.xs_stride;
-    a.xs_bytes = p.xs_bytes;
-    a.tge = p.tge;
-    a.fast = p.fast;
+    std::string why;
+    if (!plan_decode(a.T, a.k, W.H, W.I, G, a.P, why)) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
     static std::once_flag once;
     std::call_once(once, [] {
-        cudaFuncSetAttribute(k_moe_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(k_moe_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET);
     });
-    k_moe_decode<<<G, dk::THREADS, p.smem, cu(stream)>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(dk::THREADS);
+    cfg.dynamicSmemBytes = a.P.smem;
+    cfg.stream = cu(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_moe_decode, a);
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
     return check_launch(fn);
 }
 
 ft_status validate_weights(const ft_moe_layer_weights* W, const char* fn);
 
-// Workspace: [0, 256) grid-barrier counter (zero before first use), then h.
-static size_t fused_workspace_size(int T, int k, int I) { return 256 + align_up((size_t)T * k * I * 2, 256); }
+// Workspace: [0, 256) call counter (zero before first use), then the h words
+// (8 bytes per two h values).
+static size_t fused_workspace_size(int T, int k, int I) { return 256 + align_up((size_t)T * k * I * 4, 256); }
 
 // grouped-mode launch used by ft_moe_expert_ffn_nvfp4_decode for tiled weights
 ft_status decode_tiles_grouped(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k, const int32_t* offsets,
@@ -765,6 +1019,7 @@ ft_status decode_tiles_grouped(const ft_moe_layer_weights* W, const uint16_t* x,
     const size_t need = fused_workspace_size(T, k, W->I);
     if (!ws || ws_bytes < need || !aligned(ws, 256))
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": workspace missing, too small or not 256-byte aligned");
+    if (out && !w) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": out needs w");
     DecodeArgs a{};
     a.W = *W;
     a.offsets = offsets;
@@ -774,7 +1029,7 @@ ft_status decode_tiles_grouped(const ft_moe_layer_weights* W, const uint16_t* x,
     a.out = out;
     a.y = y;
     a.bar = static_cast<unsigned int*>(ws);
-    a.hbuf = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + 256);
+    a.hbuf = static_cast<char*>(ws) + 256;
     a.T = T;
     a.k = k;
     return launch_decode(a, stream, fn);
@@ -830,7 +1085,7 @@ ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits
     a.ids_out = ids;
     a.w_out = w;
     a.bar = static_cast<unsigned int*>(ws);
-    a.hbuf = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + 256);
+    a.hbuf = static_cast<char*>(ws) + 256;
     a.T = T;
     a.k = k;
     return launch_decode(a, stream, fn);

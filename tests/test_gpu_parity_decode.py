@@ -135,11 +135,11 @@ def test_tile_packing_is_a_permutation_of_row_bytes():
         for b in range(0, K // 2, 3):
             kb, within = divmod(b, 64)
             q, i = divmod(within, 16)
-            assert tb[base + kb * 1024 + h * 512 + (q * 8 + g) * 16 + i] == codes[n, b]
+            assert tb[base + kb * 1024 + h * 512 + (g * 4 + q) * 16 + i] == codes[n, b]
         for blk in range(K // 16):
             kb, j = divmod(blk, 8)
             q, bb = divmod(j, 2)
-            assert tb[base + KB * 1024 + kb * 128 + (q * 8 + g) * 4 + 2 * h + bb] == scales[n, blk]
+            assert tb[base + KB * 1024 + kb * 128 + (g * 4 + q) * 4 + 2 * h + bb] == scales[n, blk]
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -163,15 +163,24 @@ def test_decode_753b_batch1_layer(path):
     assert_layer_close(out.float().cpu().numpy(), ref["out"], "753B b1")
 
 
-@pytest.mark.parametrize("path", PATHS)
-def test_decode_753b_batch16_sampled_tokens(path):
+def test_decode_753b_batch16_sampled_tokens():
     cfg = W.CONFIGS["decode_753b_b16"]
-    lw = device_weights_generated(cfg, 1, layout=layout_of(path))
-    logits, x_bits, mod, out, _ = run_layer(cfg, lw, 1, 2, path=path)
+    lw = device_weights_generated(cfg, 1, layout=Q.FT_LAYOUT_ROWS)
+    logits, x_bits, mod, out, _ = run_layer(cfg, lw, 1, 2, path="rows")
     rows = [0, 9]
     ref = oracle_layer(cfg, 1, logits, x_bits, rows=rows)
     check_routing(mod, ref)
     assert_layer_close(out.float().cpu().numpy()[rows], ref["out"], "753B b16 sampled")
+
+
+@pytest.mark.parametrize("path", ["tiles", "fused"])
+def test_tiled_kernel_reports_unsupported_staging_size(path):
+    """16 tokens of hidden 6144 do not fit the tiled kernel's f16 staging area: a clear error, nothing launched."""
+    cfg = W.CONFIGS["decode_753b_b16"]
+    lw = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_DECODE_TILES, n_weights=cfg.E)
+    with pytest.raises(Q.FtError) as ei:
+        run_layer(cfg, lw, 1, 2, path=path)
+    assert ei.value.status == Q.FT_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("path", PATHS)
