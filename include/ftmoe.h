@@ -222,6 +222,34 @@ FT_API ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float*
                                      int k, uint16_t* out, int32_t* ids, float* w, void* ws, size_t ws_bytes,
                                      ft_stream_t stream);
 
+/* The fused decode layer step above, for callers that cannot allocate device
+ * memory.  (No counterpart in the pages: this is a deployment convenience.)
+ * Typical such callers are:
+ *  - a plugin that its host hands only input and output buffers, with no way
+ *    to ask for a workspace;
+ *  - an application whose own pool allocator owns all device memory and
+ *    forbids other components from calling cudaMalloc;
+ *  - a latency-critical decode loop that must not take the allocator's locks
+ *    and implicit synchronisation.
+ * Arguments as ft_moe_layer_decode, without ws: the scratch (the call counter
+ * and the h hand-off words, 256 + 4*T*k*I bytes) lives in a device array
+ * inside the library of FT_NOALLOC_DECODE_MAX_SCRATCH bytes.  Every GPU that
+ * loads the library holds it until the process exits.
+ *  - T*k*I > 262144 returns FT_ERR_INVALID_ARG before anything is enqueued.
+ *  - The function allocates nothing: no cudaMalloc, no cudaFree, no
+ *    allocating library call.  Each call first clears the part of the array it
+ *    uses with cudaMemsetAsync on `stream`, so it never depends on what
+ *    earlier calls left there.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current.  Make that first call
+ *    before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (other
+ *    streams, other threads, or two in flight on different streams) race and
+ *    give wrong results.  Serialise them. */
+#define FT_NOALLOC_DECODE_MAX_SCRATCH ((1u << 20) + 256u)
+FT_API ft_status ft_moe_layer_decode_noalloc(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x,
+                                             int T, int k, uint16_t* out, int32_t* ids, float* w, ft_stream_t stream);
+
 /* [P4 MoE core mechanism] Routing-weighted combine:
  * out[t][n] = bf16( sum_{j<k} w[t][j] * y[inv[t*k+j]][n] ), fp32, j order.
  *   y (device) fp32 [T*k][H]; inv, w as above; out (device) bf16 [T][H]. */

@@ -74,6 +74,7 @@ _sig("ft_nvfp4_pack_tiles", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_moe_layer_decode_workspace_size", [_i32, _i32, _i32, _i32], _sz)
 _sig("ft_moe_layer_decode", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
                              _vp])
+_sig("ft_moe_layer_decode_noalloc", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp])
 
 EXPORTED = [n for n in dir(_lib) if n.startswith("ft_")]
 
@@ -228,6 +229,16 @@ def ft_moe_layer_decode(W, logits: torch.Tensor, x: torch.Tensor, k: int, out: t
     desc = W.desc()
     _check(_lib.ft_moe_layer_decode(ctypes.byref(desc), _p(logits), _p(x), T, k, _p(out), _p(ids), _p(w), _p(ws),
                                     ws.numel() * ws.element_size(), _s(stream)))
+    return out
+
+
+def ft_moe_layer_decode_noalloc(W, logits: torch.Tensor, x: torch.Tensor, k: int, out: torch.Tensor, ids=None, w=None,
+                                stream=None):
+    """Fused decode layer step with the library's built-in scratch (no workspace, nothing allocated)."""
+    T = x.shape[0]
+    desc = W.desc()
+    _check(_lib.ft_moe_layer_decode_noalloc(ctypes.byref(desc), _p(logits), _p(x), T, k, _p(out), _p(ids), _p(w),
+                                            _s(stream)))
     return out
 
 

@@ -1054,6 +1054,66 @@ ft_status ft_nvfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint
     return check_launch("ft_nvfp4_pack_tiles");
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------- variant without allocation
+
+namespace ft {
+
+// Scratch of ft_moe_layer_decode_noalloc: the call counter and the h words of
+// one call, in a file-scope device array (every device that loads the library
+// holds it until the process exits).  In host code the name is only a stand-in:
+// the device address comes from cudaGetSymbolAddress, resolved once per device.
+constexpr size_t kNoAllocScratchBytes = FT_NOALLOC_DECODE_MAX_SCRATCH;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device (resolved on the first call there).
+static ft_status noalloc_scratch(void** out, const char* fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": device ordinal beyond 63");
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(FT_ERR_CUDA, std::string(fn) + ": cudaGetSymbolAddress failed: " + cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FT_OK;
+}
+
+}  // namespace ft
+
+extern "C" {
+
+ft_status ft_moe_layer_decode_noalloc(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x, int T,
+                                      int k, uint16_t* out, int32_t* ids, float* w, ft_stream_t stream) {
+    const char* fn = "ft_moe_layer_decode_noalloc";
+    ft_status st = validate_weights(W, fn);
+    if (st != FT_OK) return st;
+    if (T < 0 || T > dk::MAXT || k <= 0 || k > W->E || k > dk::MAXK)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 0 <= T <= 16 and 1 <= k <= min(E, 32)");
+    if (T == 0) return FT_OK;
+    const size_t need = fused_workspace_size(T, k, W->I);
+    if (need > kNoAllocScratchBytes)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": T*k*I = " + std::to_string((size_t)T * k * W->I) +
+                                            " needs " + std::to_string(need) + " bytes of scratch; the built-in scratch holds " +
+                                            std::to_string(kNoAllocScratchBytes) + " (T*k*I <= 262144)");
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch, fn);
+    if (st != FT_OK) return st;
+    // every call starts from a zeroed counter and zeroed h words, whatever earlier calls left there
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, need, cu(stream));
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": clearing the scratch: " + cudaGetErrorString(e));
+    return ft_moe_layer_decode(W, logits, x, T, k, out, ids, w, scratch, need, stream);
+}
+
 size_t ft_moe_layer_decode_workspace_size(int T, int k, int H, int I) {
     (void)H;
     if (T <= 0 || k <= 0 || I <= 0) return 0;
