@@ -257,6 +257,55 @@ FT_API ft_status ft_moe_combine(const float* y, const int32_t* inv, const float*
                          ft_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Expert-slot cache                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* [P5 设计核心, second principle; P4 bandwidth-aware storage] A VRAM cache of
+ * experts per layer with LRU replacement, filled from pinned host memory by
+ * cudaMemcpyAsync on a side stream.  Adjacent tokens route to overlapping
+ * experts, so most routed accesses hit and only misses cross PCIe.
+ * Policy (the pages say only "global LRU"): one cache of S slots per layer,
+ * initially empty; a token's experts are visited in ascending id; a hit
+ * refreshes the expert's stamp to `step`; a miss takes the lowest free slot,
+ * else evicts the slot with the oldest stamp among experts the token does not
+ * select (lower slot on a tie).
+ * Memory is the caller's:
+ *   host_experts (host) [L*E] pointers, expert e of layer l at [l*E + e]:
+ *       expert_bytes each, in pinned host memory, laid out exactly as a slot.
+ *   slots (device) the slot pool: slot s of layer l at slots + (l*S + s)*slot_stride
+ *       (slot_stride >= expert_bytes, slot_stride and slots 256-byte aligned).
+ *   tables (device) int32 [L][E]: expert -> slot or -1, written by _publish; give
+ *       tables + l*E as expert_to_slot of layer l's ft_moe_layer_weights.
+ * The handle is host memory, freed by ft_expert_cache_destroy.  The first
+ * _publish makes a small pinned staging area; create and lookup touch no device.
+ * Calls on one handle are serialised by an internal lock. */
+typedef struct ft_expert_cache ft_expert_cache;
+FT_API ft_status ft_expert_cache_create(int L, int E, int S, size_t expert_bytes, const void* const* host_experts,
+                                        void* slots, size_t slot_stride, int32_t* tables, ft_expert_cache** out);
+FT_API ft_status ft_expert_cache_destroy(ft_expert_cache* cache);
+/* One token's expert ids (host, n <= S, distinct, in [0, E)).  slots_out[i]
+ * (host) receives the slot of ids[i]; the misses, which the caller must fill
+ * before the layer reads them, are miss_experts[0..*n_miss) / miss_slots
+ * (host, room for n), ascending expert id.  Pure host bookkeeping. */
+FT_API ft_status ft_expert_cache_lookup(ft_expert_cache* cache, int layer, int64_t step, const int32_t* ids, int n,
+                                        int32_t* slots_out, int32_t* miss_experts, int32_t* miss_slots, int* n_miss);
+/* Enqueues the copy of expert `expert` of `layer` from its pinned host source
+ * into `slot` on copy_stream, then records `done` (optional) there.  A copy
+ * that cannot be enqueued returns FT_ERR_CUDA (nothing recorded). */
+FT_API ft_status ft_expert_cache_fill(ft_expert_cache* cache, int layer, int expert, int slot, ft_stream_t copy_stream,
+                                      ft_event_t done);
+/* Enqueues on `stream` the copy of layer `layer`'s expert -> slot table into
+ * tables + layer*E (from a pinned ring of 4 staging copies per layer; a ring
+ * entry still in flight is waited for on the host). */
+FT_API ft_status ft_expert_cache_publish(ft_expert_cache* cache, int layer, ft_stream_t stream);
+/* Counters since creation: hit and miss accesses, bytes enqueued by fills. */
+FT_API ft_status ft_expert_cache_stats(ft_expert_cache* cache, int64_t* hits, int64_t* misses, int64_t* bytes_filled);
+/* Test hook: the fill with 0-based index `fill_index` (counting every fill
+ * call on this handle) returns FT_ERR_CUDA without enqueuing a copy; -1 turns
+ * the hook off. */
+FT_API ft_status ft_expert_cache_inject_fill_failure(ft_expert_cache* cache, int64_t fill_index);
+
+/* ------------------------------------------------------------------------ */
 /* Quantisation and synthetic weights                                         */
 /* ------------------------------------------------------------------------ */
 

@@ -75,6 +75,15 @@ _sig("ft_moe_layer_decode_workspace_size", [_i32, _i32, _i32, _i32], _sz)
 _sig("ft_moe_layer_decode", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
                              _vp])
 _sig("ft_moe_layer_decode_noalloc", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp])
+_sig("ft_expert_cache_create", [_i32, _i32, _i32, _sz, ctypes.POINTER(ctypes.c_void_p), _vp, _sz, _vp,
+                                ctypes.POINTER(ctypes.c_void_p)])
+_sig("ft_expert_cache_destroy", [_vp])
+_sig("ft_expert_cache_lookup", [_vp, _i32, _i64, ctypes.POINTER(ctypes.c_int32), _i32, ctypes.POINTER(ctypes.c_int32),
+                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(_i32)])
+_sig("ft_expert_cache_fill", [_vp, _i32, _i32, _i32, _vp, _vp])
+_sig("ft_expert_cache_publish", [_vp, _i32, _vp])
+_sig("ft_expert_cache_stats", [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64)])
+_sig("ft_expert_cache_inject_fill_failure", [_vp, _i64])
 
 EXPORTED = [n for n in dir(_lib) if n.startswith("ft_")]
 
@@ -240,6 +249,57 @@ def ft_moe_layer_decode_noalloc(W, logits: torch.Tensor, x: torch.Tensor, k: int
     _check(_lib.ft_moe_layer_decode_noalloc(ctypes.byref(desc), _p(logits), _p(x), T, k, _p(out), _p(ids), _p(w),
                                             _s(stream)))
     return out
+
+
+# --------------------------------------------------------------------------- expert-slot cache
+
+class ExpertCacheHandle:
+    """Owns an ft_expert_cache handle (host bookkeeping); the pools stay the caller's."""
+
+    def __init__(self, L: int, E: int, S: int, expert_bytes: int, host_ptrs, slots_ptr: int, slot_stride: int,
+                 tables_ptr: int):
+        arr = (ctypes.c_void_p * (L * E))(*host_ptrs)
+        h = ctypes.c_void_p()
+        _check(_lib.ft_expert_cache_create(L, E, S, expert_bytes, arr, slots_ptr, slot_stride, tables_ptr,
+                                           ctypes.byref(h)))
+        self.h, self.L, self.E, self.S = h, L, E, S
+
+    def close(self):
+        if self.h:
+            _lib.ft_expert_cache_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def lookup(self, layer: int, step: int, ids):
+        """Returns (slots, [(expert, slot) misses]) for one token's expert ids (host ints)."""
+        n = len(ids)
+        c_ids = (ctypes.c_int32 * max(n, 1))(*ids)
+        slots = (ctypes.c_int32 * max(n, 1))()
+        me = (ctypes.c_int32 * max(n, 1))()
+        ms = (ctypes.c_int32 * max(n, 1))()
+        nm = ctypes.c_int(0)
+        _check(_lib.ft_expert_cache_lookup(self.h, layer, step, c_ids, n, slots, me, ms, ctypes.byref(nm)))
+        return [slots[i] for i in range(n)], [(me[i], ms[i]) for i in range(nm.value)]
+
+    def fill(self, layer: int, expert: int, slot: int, stream=None, event=None):
+        _check(_lib.ft_expert_cache_fill(self.h, layer, expert, slot, _s(stream),
+                                         None if event is None else event.cuda_event))
+
+    def publish(self, layer: int, stream=None):
+        _check(_lib.ft_expert_cache_publish(self.h, layer, _s(stream)))
+
+    def stats(self):
+        h, m, b = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.ft_expert_cache_stats(self.h, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b)))
+        return h.value, m.value, b.value
+
+    def inject_fill_failure(self, fill_index: int):
+        _check(_lib.ft_expert_cache_inject_fill_failure(self.h, fill_index))
 
 
 from .layer import FusedDecodeLayer, LayerWeights, MoEDecodeLayer  # noqa: E402,F401

@@ -140,3 +140,107 @@ class FusedDecodeLayer:
         ft_moe_layer_decode(weights, logits, x, self.k, out, self.ws, ids=self.ids if routing else None,
                             w=self.w if routing else None, stream=stream)
         return out
+
+
+class ExpertSlotPool:
+    """Expert weights of L layers in pinned host memory, a VRAM pool of S slots per layer, and the LRU cache
+    (ft_expert_cache_*) that maps experts to slots.
+
+    Each expert occupies one contiguous block, in the host pool and in its slot alike:
+        [gate/up tiles: 2I*H*9/16 bytes][down tiles: H*I*9/16 bytes][tensor scales: 4 floats]
+    so that a miss is filled by one cudaMemcpyAsync.  layer_weights(l) describes layer l's slots for the FFN
+    kernels (weight index = slot, expert_to_slot = the layer's device table).
+    """
+
+    def __init__(self, L: int, E: int, H: int, I: int, S: int, device):
+        import ctypes
+
+        from . import ExpertCacheHandle
+        self.L, self.E, self.H, self.I, self.S = L, E, H, I, S
+        self.device = torch.device(device)
+        self.gu_bytes = 2 * I * H * 9 // 16
+        self.d_bytes = H * I * 9 // 16
+        self.expert_bytes = self.gu_bytes + self.d_bytes + 16
+        self.slot_stride = (self.expert_bytes + 255) // 256 * 256
+        self.host = torch.empty(L * E * self.slot_stride, dtype=torch.uint8).pin_memory()
+        self.slots = torch.empty(L * S * self.slot_stride, dtype=torch.uint8, device=self.device)
+        self.tables = torch.full((L, E), -1, dtype=torch.int32, device=self.device)
+        base = self.host.data_ptr()
+        ptrs = [base + i * self.slot_stride for i in range(L * E)]
+        self.cache = ExpertCacheHandle(L, E, S, self.expert_bytes, ptrs, self.slots.data_ptr(), self.slot_stride,
+                                       self.tables.data_ptr())
+        self._ctypes = ctypes
+
+    def host_expert(self, layer: int, e: int) -> torch.Tensor:
+        off = (layer * self.E + e) * self.slot_stride
+        return self.host[off:off + self.expert_bytes]
+
+    def load_layer(self, layer: int, lw: LayerWeights) -> None:
+        """Copy the E experts of a device LayerWeights (decode-tile layout) into the host pool."""
+        assert lw.layout == FT_LAYOUT_DECODE_TILES and lw.n >= self.E
+        torch.cuda.synchronize(lw.device)
+        for e in range(self.E):
+            blk = torch.cat([lw.gu_codes[e], lw.d_codes[e], lw.tscale[e].view(torch.uint8)]).cpu()
+            self.host_expert(layer, e).copy_(blk)
+
+    def layer_weights(self, layer: int) -> "SlotLayerWeights":
+        return SlotLayerWeights(self, layer)
+
+
+class SlotLayerWeights:
+    """Descriptor of one layer's cache slots for the FFN kernels (decode-tile layout)."""
+
+    def __init__(self, pool: ExpertSlotPool, layer: int):
+        self.pool, self.layer = pool, layer
+        self.E, self.H, self.I = pool.E, pool.H, pool.I
+        self.n = pool.S
+        self.layout = FT_LAYOUT_DECODE_TILES
+        self.device = pool.device
+
+    def desc(self) -> ft_moe_layer_weights:
+        p = self.pool
+        d = ft_moe_layer_weights()
+        d.E, d.H, d.I, d.n_weights, d.layout = p.E, p.H, p.I, p.S, FT_LAYOUT_DECODE_TILES
+        base = p.slots.data_ptr() + self.layer * p.S * p.slot_stride
+        d.gu_codes, d.gu_codes_stride = base, p.slot_stride
+        d.d_codes, d.d_codes_stride = base + p.gu_bytes, p.slot_stride
+        d.tscale, d.tscale_stride = base + p.gu_bytes + p.d_bytes, p.slot_stride // 4
+        d.expert_to_slot = p.tables[self.layer].data_ptr()
+        return d
+
+
+class CachedDecodeLayer:
+    """Decode step of one layer whose experts come from an ExpertSlotPool.
+
+    route (device) -> expert ids to the host -> LRU lookup -> fills of the misses on the copy stream -> publish the
+    slot table -> the fused layer kernel (which routes again, identically, and reads weights through the table).
+    """
+
+    def __init__(self, pool: ExpertSlotPool, layer: int, k: int, T: int, copy_stream=None):
+        self.pool, self.layer, self.k, self.T = pool, layer, k, T
+        dev = pool.device
+        self.weights = pool.layer_weights(layer)
+        self.ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.ids_host = torch.empty((T, k), dtype=torch.int32).pin_memory()
+        self.fused = FusedDecodeLayer(pool.E, pool.H, pool.I, k, T, dev)
+        self.copy_stream = copy_stream if copy_stream is not None else torch.cuda.Stream(device=dev)
+        self.filled = torch.cuda.Event()
+        self.routed = torch.cuda.Event()
+
+    def __call__(self, logits: torch.Tensor, x: torch.Tensor, out: torch.Tensor, step: int, stream=None):
+        stream = torch.cuda.current_stream(self.pool.device) if stream is None else stream
+        ft_moe_route(logits, self.k, self.ids, self.w, stream=stream)
+        with torch.cuda.stream(stream):
+            self.ids_host.copy_(self.ids, non_blocking=True)
+            self.routed.record(stream)
+        self.routed.synchronize()
+        needed = sorted(set(int(e) for e in self.ids_host.view(-1).tolist()))
+        _, misses = self.pool.cache.lookup(self.layer, step, needed)
+        for e, s in misses:
+            self.pool.cache.fill(self.layer, e, s, stream=self.copy_stream)
+        self.filled.record(self.copy_stream)
+        self.pool.cache.publish(self.layer, stream=stream)
+        stream.wait_event(self.filled)
+        self.fused(self.weights, logits, x, out, routing=False, stream=stream)
+        return misses
