@@ -97,6 +97,7 @@ FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
 /* Layouts of expert weights in device memory (ft_moe_layer_weights.layout). */
 #define FT_LAYOUT_ROWS 0         /* row-major codes [N][K/2] + row-major scales [N][K/16] */
 #define FT_LAYOUT_DECODE_TILES 1 /* 16-row tiles for the decode kernels, see ft_nvfp4_pack_tiles() */
+#define FT_LAYOUT_UMMA_TILES 2   /* 128x128 blocks for the tensor-core prefill, see ft_nvfp4_pack_umma() */
 
 /* Expert weights of one layer in device memory.  For weight index w (the
  * expert id, or its cache slot when expert_to_slot is given):
@@ -107,6 +108,10 @@ FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
  *            scales gu_scales + w*gu_scales_stride : [2I][H/16] E4M3 bytes
  *   down     codes  d_codes   + w*d_codes_stride   : [H][I/2]
  *            scales d_scales  + w*d_scales_stride  : [H][I/16]
+ *  layout FT_LAYOUT_UMMA_TILES (codes and scales together; scale pointers unused)
+ *   gate/up  gu_codes + w*gu_codes_stride : the [2I][H] matrix above packed by
+ *            ft_nvfp4_pack_umma() ((2I/128)*(H/128) blocks of 9216 bytes)
+ *   down     d_codes  + w*d_codes_stride  : the [H][I] matrix packed likewise
  *  layout FT_LAYOUT_DECODE_TILES (codes and scales together; scale pointers unused)
  *   gate/up  gu_codes + w*gu_codes_stride : the [2I][H] matrix above packed by
  *            ft_nvfp4_pack_tiles() (2I*H*9/16 bytes)
@@ -250,6 +255,29 @@ FT_API ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float*
 FT_API ft_status ft_moe_layer_decode_noalloc(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x,
                                              int T, int k, uint16_t* out, int32_t* ids, float* w, ft_stream_t stream);
 
+FT_API size_t ft_moe_prefill_workspace_size(int T, int k, int E, int H, int I);
+
+/* [P4 MoE core mechanism; P5 NVFP4; P3 §2.1] Prefill expert FFN and combine on
+ * the block-scaled FP4 tensor cores (tcgen05.mma kind::mxf4nvf4, TMEM
+ * accumulators).  The FP4 MMA needs FP4 on both sides, so activations are
+ * NVFP4 too ("A4"): x rows and h rows are quantised with unit tensor scale,
+ * per 16 elements along the reduction dimension:
+ *   g = Wg q(x_t), u = Wu q(x_t), h = bf16(silu(g) * u), y_p = Wd q(h),
+ *   out[t] = bf16( sum_j w[t][j] * y_{inv[t*k+j]} ), fp32 (order of the
+ *   additions not fixed: fp32 atomics).
+ *   W (device) weights in FT_LAYOUT_UMMA_TILES, no slot table; H a multiple
+ *          of 128, I a multiple of 128.
+ *   x (device) bf16 [T][H]; offsets, perm (device) from ft_moe_permute;
+ *   w (device) fp32 [T][k] routing weights; out (device) bf16 [T][H].
+ *   ws: ft_moe_prefill_workspace_size(T, k, E, H, I) bytes, 256-byte aligned
+ *       (per-expert tile offsets, quantised x and h tiles, an fp32 output
+ *       accumulator); no initial content needed.
+ * Each expert's rows are padded to whole 128-row tiles; padding rows are zero
+ * and ignored. */
+FT_API ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
+                                                 const int32_t* offsets, const int32_t* perm, const float* w,
+                                                 uint16_t* out, void* ws, size_t ws_bytes, ft_stream_t stream);
+
 /* [P4 MoE core mechanism] Routing-weighted combine:
  * out[t][n] = bf16( sum_{j<k} w[t][j] * y[inv[t*k+j]][n] ), fp32, j order.
  *   y (device) fp32 [T*k][H]; inv, w as above; out (device) bf16 [T][H]. */
@@ -342,6 +370,18 @@ FT_API ft_status ft_nvfp4_quantize_act(const uint16_t* x, int64_t T, int64_t K, 
  * All pointers (device). */
 FT_API ft_status ft_nvfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
                                      int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
+
+/* Packs a row-major NVFP4 matrix [N][K] (codes [N][K/2] at byte stride
+ * codes_ld, scales [N][K/16] at stride scales_ld) into FT_LAYOUT_UMMA_TILES:
+ * (N/128)*(K/128) blocks of 9216 bytes, block (rt, ks) of rows 128*rt.. and
+ * K 128*ks.. at (rt*(K/128) + ks)*9216.  Within a block, code byte b (0..63) of
+ * row r at (b/16)*2048 + (r/8)*128 + (r%8)*16 + b%16 (the tensor core's
+ * K-major no-swizzle layout: 8-row x 16-byte core matrices) and scale j (0..7)
+ * of row r at 8192 + (j/4)*512 + (r%32)*16 + (r/32)*4 + j%4 (the scale-factor
+ * layout moved to TMEM by tcgen05.cp .32x128b.warpx4).  N and K multiples of
+ * 128.  All pointers (device). */
+FT_API ft_status ft_nvfp4_pack_umma(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
+                                    int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
 
 /* Synthetic weights: out[j] = (float)(sigma * Z_{first+j}) where Z is the
  * Box-Muller normal of Philox4x32-10 block (first+j)/2 with counter

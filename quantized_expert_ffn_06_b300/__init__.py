@@ -22,7 +22,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_UNSUPPORTED, FT_ERR_TIMEOUT, FT_ERR_NO_SLOT, FT_ERR_OOM, \
     FT_ERR_DEVICE = range(8)
-FT_LAYOUT_ROWS, FT_LAYOUT_DECODE_TILES = 0, 1
+FT_LAYOUT_ROWS, FT_LAYOUT_DECODE_TILES, FT_LAYOUT_UMMA_TILES = 0, 1, 2
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX = 1, 2, 4, 8
 
 _vp, _i32, _i64, _u64, _sz, _dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t,
@@ -75,6 +75,10 @@ _sig("ft_moe_layer_decode_workspace_size", [_i32, _i32, _i32, _i32], _sz)
 _sig("ft_moe_layer_decode", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
                              _vp])
 _sig("ft_moe_layer_decode_noalloc", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp])
+_sig("ft_nvfp4_pack_umma", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
+_sig("ft_moe_prefill_workspace_size", [_i32, _i32, _i32, _i32, _i32], _sz)
+_sig("ft_moe_expert_ffn_nvfp4_prefill", [ctypes.POINTER(ft_moe_layer_weights), _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                         _sz, _vp])
 _sig("ft_expert_cache_create", [_i32, _i32, _i32, _sz, ctypes.POINTER(ctypes.c_void_p), _vp, _sz, _vp,
                                 ctypes.POINTER(ctypes.c_void_p)])
 _sig("ft_expert_cache_destroy", [_vp])
@@ -248,6 +252,24 @@ def ft_moe_layer_decode_noalloc(W, logits: torch.Tensor, x: torch.Tensor, k: int
     desc = W.desc()
     _check(_lib.ft_moe_layer_decode_noalloc(ctypes.byref(desc), _p(logits), _p(x), T, k, _p(out), _p(ids), _p(w),
                                             _s(stream)))
+    return out
+
+
+def ft_nvfp4_pack_umma(codes, codes_ld: int, scales, scales_ld: int, N: int, K: int, tiles, stream=None):
+    _check(_lib.ft_nvfp4_pack_umma(_p(codes), codes_ld, _p(scales), scales_ld, N, K, _p(tiles), _s(stream)))
+
+
+def ft_moe_prefill_workspace_size(T: int, k: int, E: int, H: int, I: int) -> int:
+    return _lib.ft_moe_prefill_workspace_size(T, k, E, H, I)
+
+
+def ft_moe_expert_ffn_nvfp4_prefill(W, x: torch.Tensor, k: int, offsets, perm, w, out, ws, stream=None):
+    """Prefill expert FFN + combine on the FP4 tensor cores (weights in FT_LAYOUT_UMMA_TILES)."""
+    _req(x, torch.bfloat16, "x")
+    T = x.shape[0]
+    desc = W.desc()
+    _check(_lib.ft_moe_expert_ffn_nvfp4_prefill(ctypes.byref(desc), _p(x), T, k, _p(offsets), _p(perm), _p(w), _p(out),
+                                                _p(ws), ws.numel() * ws.element_size(), _s(stream)))
     return out
 
 

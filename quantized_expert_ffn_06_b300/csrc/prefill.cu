@@ -1,0 +1,625 @@
+// prefill.cu -- grouped expert FFN for many tokens (prefill) on the 5th-
+// generation tensor cores: block-scaled FP4 MMA (tcgen05.mma kind::mxf4nvf4,
+// E2M1 operands, one UE4M3 scale per 16 elements), fp32 accumulators in TMEM.
+//
+// Each expert is an independent FFN applied to the tokens routed to it (page
+// "FreeToken：753B大模型塞进单卡的本地部署硬件账该怎么算", MoE core mechanism);
+// the weights are NVFP4 (page "8GB 笔记本 39.3 tok/s、单卡跑 753B：FreeToken 把
+// frontier MoE 拉回本地", sections on the evaluation and the limits).  The FP4
+// MMA takes FP4 on both sides, so the activations x and h are quantised to
+// NVFP4 with unit tensor scale (E4M3 scale per 16 along the reduction
+// dimension); the weights' fp32 tensor scales are applied in the epilogues.
+//
+// Steps (one stream):
+//  1. k_pf_plan: every expert's permuted rows are padded to whole 128-row
+//     tiles; tile_off[e] = first tile of expert e (exclusive scan).
+//  2. k_pf_quant_x: x rows, gathered in permuted order, quantised into
+//     operand tiles.
+//  3. k_pf_gemm<1>: h = silu(Wg x) * (Wu x) per (expert, 128 gate/up rows,
+//     128 tokens) tile, rounded to bf16 and quantised into operand tiles.
+//  4. k_pf_gemm<2>: y = Wd h per (expert, 128 output rows, 128 tokens) tile;
+//     the epilogue adds w[t][j] * y into an fp32 accumulator of the output
+//     (red.global.add), i.e. the routing-weighted combine.
+//  5. k_pf_out: the accumulator rounded to bf16.
+//
+// Operand tiles ("UMMA tiles"): an [R][K] NVFP4 matrix (R a multiple of 128,
+// K of 128) is stored as blocks of 128 rows x 128 K, 9216 bytes each, block
+// (rt, ks) at (rt*(K/128) + ks)*9216.  In a block, code byte b (0..63) of row r
+// sits at (b/16)*2048 + (r/8)*128 + (r%8)*16 + b%16 -- the tensor core's
+// K-major layout without swizzle: 8-row x 16-byte core matrices, 128 bytes
+// apart along the rows and 2048 bytes apart along K -- and scale j (0..7) of
+// row r at 8192 + (j/4)*512 + (r%32)*16 + (r/32)*4 + j%4, the layout that
+// tcgen05.cp .32x128b.warpx4 moves into TMEM (4 columns per 64 K).  A block is
+// one contiguous bulk copy.
+//
+// The GEMM kernel is persistent (one CTA per SM): warp 0 streams A and B
+// blocks into an 8-stage shared-memory ring (cp.async.bulk + mbarriers),
+// warp 1 allocates TMEM and one of its threads issues the MMAs (two per stage,
+// K = 64 each, scales copied to TMEM with tcgen05.cp) into one of two 128-column
+// accumulators, and warps 2-5 drain the other accumulator (tcgen05.ld) through
+// the epilogue, so MMA and epilogue overlap.  Every wait is bounded; on expiry
+// the kernel sets FT_DEVERR_TIMEOUT and finishes, freeing its TMEM.
+#include "common.cuh"
+
+#include <algorithm>
+#include <mutex>
+
+namespace ft {
+
+namespace pf {
+constexpr int BLK = 9216;           // one 128 x 128 operand block
+constexpr int NS = 8;               // ring stages (A block + B block each)
+constexpr int STAGE = 2 * BLK;
+constexpr int THREADS = 192;        // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr uint32_t TMEM_COLS = 512; // 2 x 128 accumulator columns + scale-factor columns
+constexpr uint32_t SF_COL0 = 256;   // 16 scale-factor columns per ring stage
+constexpr unsigned long long WAIT_NS = 2000000000ull;
+constexpr size_t SMEM = (size_t)NS * STAGE + 1024;
+}  // namespace pf
+
+struct PfGemmArgs {
+    const uint8_t* A;        // weights in UMMA tiles, expert e at A + e*a_stride
+    int64_t a_stride;
+    const float* tscale;     // per expert {gate, up, down}
+    int64_t ts_stride;
+    const uint8_t* B;        // activation tiles [tiles][KSN] blocks
+    int MT, KSN;             // M tiles per expert, K blocks
+    int E;
+    const int32_t* offsets;  // [E+1] permuted rows per expert
+    const int32_t* tile_off; // [E+1] padded tiles per expert (exclusive scan)
+    // SwiGLU epilogue: h tiles [tiles][KSN2] blocks
+    uint8_t* hq;
+    int KSN2;
+    // combine epilogue
+    const int32_t* perm;
+    const float* w;
+    int k;
+    float* out32;            // [T][H]
+    int H;
+};
+
+// ---------------------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t pf_su(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long pf_gt() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool pf_try_wait(unsigned long long* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(pf_su(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool pf_wait(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
+    if (pf_try_wait(b, parity)) return true;
+    const unsigned long long t0 = pf_gt();
+    while (!pf_try_wait(b, parity)) {
+        if (*abort_flag) return false;
+        if (pf_gt() - t0 > pf::WAIT_NS) {
+            *abort_flag = 1;
+            raise_dev_error(FT_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Shared-memory operand descriptor of the 5th-generation tensor core, no swizzle:
+// start address, leading (K-direction) and stride (row-direction) core-matrix offsets.
+__device__ __forceinline__ uint64_t umma_desc(const void* p, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((pf_su(p) & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor: kind::mxf4nvf4, E2M1 x E2M1, UE4M3 scales, M = 128, N = 128, both K-major.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ int pf_find_expert(const int32_t* tile_off, int E, int v) {
+    // largest e in [0, E) with tile_off[e] <= v
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(tile_off + mid) <= v) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Offset of code byte b (0..63) / scale j (0..7) of row r within a 128 x 128 block.
+__host__ __device__ __forceinline__ int blk_code_off(int r, int b) {
+    return (b >> 4) * 2048 + (r >> 3) * 128 + (r & 7) * 16 + (b & 15);
+}
+__host__ __device__ __forceinline__ int blk_scale_off(int r, int j) {
+    return 8192 + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
+}
+
+// ---------------------------------------------------------------------------- plan and activation tiles
+
+__global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ tile_off) {
+    __shared__ int part[1024];
+    __shared__ int wsum[33];
+    const int tid = threadIdx.x;
+    // experts per thread: E <= 1024, so one each
+    const int n = (tid < E) ? (offsets[tid + 1] - offsets[tid]) : 0;
+    const int nt = (n + 127) / 128;
+    int incl = nt;
+    const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int s = wsum[lane], si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += v;
+        }
+        wsum[lane] = si - s;
+        if (lane == 31) wsum[32] = si;
+    }
+    __syncthreads();
+    part[tid] = wsum[wid] + incl - nt;
+    if (tid < E) tile_off[tid] = part[tid];
+    if (tid == 0) tile_off[E] = wsum[32];
+}
+
+// One warp per padded row q: x of the row's token, quantised with unit tensor
+// scale, into the operand tiles (zeros for padding rows).
+__global__ void __launch_bounds__(256) k_pf_quant_x(const uint16_t* __restrict__ x, int H, int k, int E,
+                                                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
+                                                    const int32_t* __restrict__ tile_off, int max_rows,
+                                                    uint8_t* __restrict__ xq) {
+    const int q = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (q >= max_rows || q >= 128 * __ldg(tile_off + E)) return;
+    const int e = pf_find_expert(tile_off, E, q >> 7);
+    const int local = q - 128 * __ldg(tile_off + e);
+    const int ne = __ldg(offsets + e + 1) - __ldg(offsets + e);
+    const bool valid = local < ne;
+    int t = 0;
+    if (valid) {
+        const int f = __ldg(perm + __ldg(offsets + e) + local);
+        t = f / k;
+    }
+    const int KSN = H / 128, rt = q >> 7, r = q & 127;
+    for (int e0 = lane * 64; e0 < H; e0 += 32 * 64) {
+        uint8_t* blk = xq + ((int64_t)rt * KSN + e0 / 128) * pf::BLK;
+        const int b0 = (e0 & 127) / 2;  // 0 or 32
+        uint32_t cw[8], sw = 0;
+        if (valid) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H + e0);
+#pragma unroll
+            for (int bl = 0; bl < 4; ++bl) {
+                float v[16];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint4 u = __ldg(src + 2 * bl + hh);
+                    const uint32_t words[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        v[8 * hh + 2 * i] = __uint_as_float(words[i] << 16);
+                        v[8 * hh + 2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
+                    }
+                }
+                uint2 c;
+                uint32_t sb;
+                quant_block16(v, 1.0f, c, sb);
+                cw[2 * bl] = c.x;
+                cw[2 * bl + 1] = c.y;
+                sw |= sb << (8 * bl);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cw[i] = 0;
+        }
+        *reinterpret_cast<uint4*>(blk + blk_code_off(r, b0)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint4*>(blk + blk_code_off(r, b0 + 16)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        *reinterpret_cast<uint32_t*>(blk + blk_scale_off(r, (e0 & 127) / 16)) = sw;
+    }
+}
+
+__global__ void __launch_bounds__(256) k_pf_out(const float* __restrict__ out32, int64_t n, uint16_t* __restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = bf16_bits(out32[i]);
+}
+
+// ---------------------------------------------------------------------------- epilogues
+
+// SwiGLU + h quantisation.  Thread of TMEM lane r (gate row r even, up row r odd
+// of the tile's 64 pairs) holds 32 token columns.  Pair p = r/2 is feature
+// m*64 + p of h; the 16 features of one quantisation block are the 32 lanes of
+// one warp.
+__device__ __forceinline__ void epi_swiglu(const PfGemmArgs& a, const uint32_t (&v)[32], int e, int m, int ntg, int c0,
+                                           int qd, int lane, float tsg, float tsu) {
+    const int f0 = m * 64 + 16 * qd;  // first feature of this warp's block
+    const int ks2 = f0 / 128, b0 = (f0 & 127) / 2, jblk = (f0 & 127) / 16;
+    uint8_t* blk_base = a.hq + (int64_t)ntg * a.KSN2 * pf::BLK + (int64_t)ks2 * pf::BLK;
+    const bool gate = (lane & 1) == 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float mine = __uint_as_float(v[j]);
+        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+        const float g = (gate ? mine : other) * tsg, u = (gate ? other : mine) * tsu;
+        const float hb = bf16_to_f32(bf16_bits(silu_f32(g) * u));
+        float am = fabsf(hb);
+#pragma unroll
+        for (int o = 2; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const uint32_t sb = f32_to_e4m3_rn_sat(__fdiv_rn(am, 6.0f));
+        const float eff = e4m3_to_f32(sb);
+        // this lane's code (lanes 4u and 4u+2 hold features 2u and 2u+1 of the block)
+        const uint32_t pair = (eff == 0.0f) ? 0u : f32x2_to_e2m1x2_rn_sat(__fdiv_rn(hb, eff), 0.0f);
+        const uint32_t code = pair & 0xFu;
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 2);
+        uint32_t word = ((lane & 3) == 0) ? ((code | (hi << 4)) << (8 * ((lane >> 2) & 3))) : 0u;
+        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+        word |= __shfl_xor_sync(0xffffffffu, word, 8);
+        const uint32_t w1 = __shfl_sync(0xffffffffu, word, 16);
+        if (lane == 0) {
+            const int r = c0 + j;  // token row within the tile
+            *reinterpret_cast<uint2*>(blk_base + blk_code_off(r, b0)) = make_uint2(word, w1);
+            blk_base[blk_scale_off(r, jblk)] = (uint8_t)sb;
+        }
+    }
+    (void)e;
+}
+
+// Down projection + combine: out32[t][m*128 + r] += w[f] * tsd * y for each real token column.
+__device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t (&v)[32], int e, int m, int ntg, int c0,
+                                            int qd, int lane, float tsd) {
+    const int n_e = __ldg(a.offsets + e + 1) - __ldg(a.offsets + e);
+    const int local0 = (ntg - __ldg(a.tile_off + e)) * 128 + c0;
+    // column metadata: lane j looks up column c0 + j
+    int tj = -1;
+    float wj = 0.0f;
+    if (local0 + lane < n_e) {
+        const int f = __ldg(a.perm + __ldg(a.offsets + e) + local0 + lane);
+        tj = f / a.k;
+        wj = __ldg(a.w + f) * tsd;
+    }
+    const int row = m * 128 + 32 * qd + lane;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int t = __shfl_sync(0xffffffffu, tj, j);
+        const float wt = __shfl_sync(0xffffffffu, wj, j);
+        if (t >= 0) atomicAdd(a.out32 + (int64_t)t * a.H + row, __uint_as_float(v[j]) * wt);
+    }
+}
+
+// ---------------------------------------------------------------------------- grouped GEMM
+
+template <int EPI>
+__global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) {
+    extern __shared__ __align__(1024) uint8_t pf_smem[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_smem) + 1023) & ~(uintptr_t)1023);
+    __shared__ __align__(8) unsigned long long full[pf::NS], empty[pf::NS], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_s;
+    volatile int* abort_flag = &abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < pf::NS; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&full[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&empty[s])));
+        }
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&acc_full[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(pf_su(&acc_empty[b])));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_s = 0;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(pf_su(&tmem_base)),
+                     "n"(pf::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tbase = tmem_base;
+    const int n_items = a.MT * __ldg(a.tile_off + a.E);
+
+    // decode item i -> (expert, m tile, global token tile)
+    auto item = [&](int i, int& e, int& m, int& ntg) {
+        const int v = i / a.MT;
+        e = pf_find_expert(a.tile_off, a.E, v);
+        const int t0 = __ldg(a.tile_off + e), nt = __ldg(a.tile_off + e + 1) - t0;
+        const int local = i - a.MT * t0;
+        m = local / nt;
+        ntg = t0 + (local - m * nt);
+    };
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            int sc = 0;
+            for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
+                int e, m, ntg;
+                item(i, e, m, ntg);
+                const uint8_t* ab = a.A + (int64_t)e * a.a_stride + (int64_t)m * a.KSN * pf::BLK;
+                const uint8_t* bb = a.B + (int64_t)ntg * a.KSN * pf::BLK;
+                for (int ks = 0; ks < a.KSN; ++ks, ++sc) {
+                    const int s = sc % pf::NS, use = sc / pf::NS;
+                    if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag)) break;
+                    uint8_t* dst = ring + (size_t)s * pf::STAGE;
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&full[s])),
+                                 "r"((uint32_t)pf::STAGE) : "memory");
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            pf_su(dst)), "l"(ab + (int64_t)ks * pf::BLK), "r"((uint32_t)pf::BLK), "r"(pf_su(&full[s]))
+                        : "memory");
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            pf_su(dst + pf::BLK)), "l"(bb + (int64_t)ks * pf::BLK), "r"((uint32_t)pf::BLK), "r"(pf_su(&full[s]))
+                        : "memory");
+                }
+            }
+            // do not leave copies landing after exit: wait (bounded) for the last stages issued
+            const unsigned long long t0 = pf_gt();
+            for (int n = max(0, sc - pf::NS); n < sc; ++n)
+                while (!pf_try_wait(&full[n % pf::NS], (n / pf::NS) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            int sc = 0, it = 0;
+            for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x, ++it) {
+                const int buf = it & 1, useb = it >> 1;
+                if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t dcol = tbase + (uint32_t)(buf * 128);
+                for (int ks = 0; ks < a.KSN; ++ks, ++sc) {
+                    const int s = sc % pf::NS;
+                    if (!pf_wait(&full[s], (sc / pf::NS) & 1, abort_flag)) break;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint8_t* sa = ring + (size_t)s * pf::STAGE;
+                    const uint8_t* sbp = sa + pf::BLK;
+#pragma unroll
+                    for (int kb = 0; kb < 2; ++kb) {
+                        const uint32_t tsfa = tbase + pf::SF_COL0 + (uint32_t)(s * 16 + kb * 8), tsfb = tsfa + 4;
+                        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsfa),
+                                     "l"(umma_desc(sa + 8192 + kb * 512, 0, 128)));
+                        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsfb),
+                                     "l"(umma_desc(sbp + 8192 + kb * 512, 0, 128)));
+                        const uint64_t da = umma_desc(sa + kb * 4096, 2048, 128), db = umma_desc(sbp + kb * 4096, 2048, 128);
+                        const uint32_t acc = (ks | kb) ? 1u : 0u;
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                                dcol), "l"(da), "l"(db), "r"(kIdesc), "r"(tsfa), "r"(tsfb), "r"(acc));
+                    }
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     pf_su(&empty[s])) : "memory");
+                }
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 pf_su(&acc_full[buf])) : "memory");
+            }
+        }
+    } else {
+        // ---------------- epilogue warps 2..5: TMEM lane quadrant qd = warp % 4
+        const int qd = warp & 3;
+        int it = 0;
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
+            const int buf = it & 1;
+            if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            int e, m, ntg;
+            item(i, e, m, ntg);
+            const float* ts = a.tscale + (int64_t)e * a.ts_stride;
+            const float t0s = __ldg(ts + 0), t1s = __ldg(ts + 1), t2s = __ldg(ts + 2);
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
+                if (EPI == 1) epi_swiglu(a, v, e, m, ntg, c0, qd, lane, t0s, t1s);
+                else epi_combine(a, v, e, m, ntg, c0, qd, lane, t2s);
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pf_su(&acc_empty[buf])) : "memory");
+        }
+    }
+    // all MMAs have completed once the epilogue has consumed every accumulator; on an abort
+    // wait (bounded) for the last commit before the TMEM is released
+    if (warp == 1 && lane == 0 && *abort_flag) {
+        const unsigned long long t0 = pf_gt();
+        int it = 0;
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x) ++it;
+        if (it > 0)
+            while (!pf_try_wait(&acc_full[(it - 1) & 1], ((it - 1) >> 1) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
+            }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(pf::TMEM_COLS));
+    }
+}
+
+// ---------------------------------------------------------------------------- weight packing
+
+// [N][K] row-major codes/scales -> UMMA tiles (N, K multiples of 128).
+__global__ void __launch_bounds__(256) k_pack_umma(const uint8_t* __restrict__ codes, int64_t codes_ld,
+                                                   const uint8_t* __restrict__ scales, int64_t scales_ld, int64_t N,
+                                                   int64_t K, uint8_t* __restrict__ out) {
+    const int64_t KSN = K / 128;
+    const int64_t per_row = 4 + 1;  // four 16-byte code pieces and one 8-byte scale group per 128 K
+    const int64_t total = N * KSN * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / (KSN * per_row);
+        const int64_t rem = i % (KSN * per_row);
+        const int64_t ks = rem / per_row;
+        const int piece = (int)(rem % per_row);
+        uint8_t* blk = out + ((row / 128) * KSN + ks) * pf::BLK;
+        const int r = (int)(row % 128);
+        if (piece < 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(codes + row * codes_ld + ks * 64 + piece * 16);
+            *reinterpret_cast<uint4*>(blk + blk_code_off(r, piece * 16)) = v;
+        } else {
+            const uint8_t* s = scales + row * scales_ld + ks * 8;
+            for (int j = 0; j < 8; ++j) blk[blk_scale_off(r, j)] = s[j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------- host side
+
+static int pf_sm_count() {
+    static int cached = 0;
+    if (!cached) {
+        int dev = 0, n = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached = n > 0 ? n : 148;
+    }
+    return cached;
+}
+
+static size_t a256(size_t v) { return (v + 255) / 256 * 256; }
+
+struct PfWs {
+    size_t tile_off, xq, hq, out32, total;
+    int max_tiles;
+};
+
+static PfWs pf_ws_layout(int T, int k, int E, int H, int I) {
+    PfWs w;
+    const int64_t P = (int64_t)T * k;
+    w.max_tiles = (int)((P + 127) / 128 + std::min<int64_t>(E, P));
+    size_t off = 0;
+    w.tile_off = off;
+    off += a256((size_t)(E + 1) * 4);
+    w.xq = off;
+    off += a256((size_t)w.max_tiles * (H / 128) * pf::BLK);
+    w.hq = off;
+    off += a256((size_t)w.max_tiles * (I / 128) * pf::BLK);
+    w.out32 = off;
+    off += a256((size_t)T * H * 4);
+    w.total = off;
+    return w;
+}
+
+ft_status validate_weights(const ft_moe_layer_weights* W, const char* fn);
+
+}  // namespace ft
+
+using namespace ft;
+
+extern "C" {
+
+ft_status ft_nvfp4_pack_umma(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
+                             int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream) {
+    if (N <= 0 || K <= 0 || N % 128 || K % 128)
+        return fail(FT_ERR_INVALID_ARG, "ft_nvfp4_pack_umma: need N and K multiples of 128");
+    if (!codes || !scales || !tiles) return fail(FT_ERR_INVALID_ARG, "ft_nvfp4_pack_umma: null pointer");
+    if (!aligned(codes, 16) || codes_ld % 16 || !aligned(tiles, 16) || codes_ld < K / 2 || scales_ld < K / 16)
+        return fail(FT_ERR_INVALID_ARG, "ft_nvfp4_pack_umma: codes/tiles need 16-byte alignment and row strides");
+    const int64_t total = N * (K / 128) * 5;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 64);
+    k_pack_umma<<<(unsigned)blocks, 256, 0, cu(stream)>>>(codes, codes_ld, scales, scales_ld, N, K, tiles);
+    return check_launch("ft_nvfp4_pack_umma");
+}
+
+size_t ft_moe_prefill_workspace_size(int T, int k, int E, int H, int I) {
+    if (T <= 0 || k <= 0 || E <= 0 || H <= 0 || I <= 0) return 0;
+    return pf_ws_layout(T, k, E, H, I).total;
+}
+
+ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
+                                          const int32_t* offsets, const int32_t* perm, const float* w, uint16_t* out,
+                                          void* ws, size_t ws_bytes, ft_stream_t stream) {
+    const char* fn = "ft_moe_expert_ffn_nvfp4_prefill";
+    ft_status st = validate_weights(W, fn);
+    if (st != FT_OK) return st;
+    if (W->layout != FT_LAYOUT_UMMA_TILES)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights must use FT_LAYOUT_UMMA_TILES");
+    if (W->expert_to_slot) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": slot tables are not supported");
+    if (W->H % 128 || W->I % 64 || (2 * W->I) % 128)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need H a multiple of 128 and I of 64");
+    if (W->I % 128) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": I must be a multiple of 128");
+    if (T < 0 || k <= 0 || k > W->E || k > 32) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need T >= 0, 1 <= k <= min(E, 32)");
+    if (T == 0) return FT_OK;
+    if (!x || !offsets || !perm || !w || !out) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if (!aligned(x, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": x needs 16-byte alignment");
+    const int E = W->E, H = W->H, I = W->I;
+    const PfWs L = pf_ws_layout(T, k, E, H, I);
+    if (!ws || ws_bytes < L.total || !aligned(ws, 256))
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": workspace missing, too small or not 256-byte aligned");
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int32_t* tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
+    uint8_t* xq = base + L.xq;
+    uint8_t* hq = base + L.hq;
+    float* out32 = reinterpret_cast<float*>(base + L.out32);
+    cudaStream_t s = cu(stream);
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(k_pf_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM);
+        cudaFuncSetAttribute(k_pf_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM);
+    });
+    cudaError_t e = cudaMemsetAsync(out32, 0, (size_t)T * H * 4, s);
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+    k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, tile_off);
+    const int max_rows = 128 * L.max_tiles;
+    k_pf_quant_x<<<(unsigned)((max_rows + 7) / 8), 256, 0, s>>>(x, H, k, E, offsets, perm, tile_off, max_rows, xq);
+    PfGemmArgs g{};
+    g.tscale = W->tscale;
+    g.ts_stride = W->tscale_stride;
+    g.E = E;
+    g.offsets = offsets;
+    g.tile_off = tile_off;
+    g.hq = hq;
+    g.KSN2 = I / 128;
+    g.perm = perm;
+    g.w = w;
+    g.k = k;
+    g.out32 = out32;
+    g.H = H;
+    const int G = pf_sm_count();
+    // gate/up + SwiGLU
+    g.A = W->gu_codes;
+    g.a_stride = W->gu_codes_stride;
+    g.B = xq;
+    g.MT = 2 * I / 128;
+    g.KSN = H / 128;
+    k_pf_gemm<1><<<G, pf::THREADS, pf::SMEM, s>>>(g);
+    // down + combine
+    g.A = W->d_codes;
+    g.a_stride = W->d_codes_stride;
+    g.B = hq;
+    g.MT = H / 128;
+    g.KSN = I / 128;
+    k_pf_gemm<2><<<G, pf::THREADS, pf::SMEM, s>>>(g);
+    const int64_t n = (int64_t)T * H;
+    k_pf_out<<<(unsigned)std::min<int64_t>((n + 255) / 256, 148 * 32), 256, 0, s>>>(out32, n, out);
+    return check_launch(fn);
+}
+
+}  // extern "C"

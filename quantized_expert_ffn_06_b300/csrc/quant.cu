@@ -12,25 +12,6 @@
 
 namespace ft {
 
-// ----------------------------------------------------------------------------
-// shared block quantiser: 16 fp32 values -> 8 code bytes + 1 scale byte
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ void quant_block16(const float (&v)[16], float st, uint2& codes, uint32_t& sb) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const float d = __fdiv_rn(amax, 6.0f);
-    const float r = __fdiv_rn(d, st);
-    sb = f32_to_e4m3_rn_sat(r);
-    const float eff = __fmul_rn(e4m3_to_f32(sb), st);
-    uint32_t b[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        b[i] = (eff == 0.0f) ? 0u : f32x2_to_e2m1x2_rn_sat(__fdiv_rn(v[2 * i], eff), __fdiv_rn(v[2 * i + 1], eff));
-    codes.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-    codes.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-}
-
 // amax over a tensor; non-negative floats order like their bit patterns.
 __global__ void __launch_bounds__(256) k_amax(const float* __restrict__ w, int64_t n, unsigned int* amax_bits) {
     float m = 0.0f;

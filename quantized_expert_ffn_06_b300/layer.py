@@ -7,10 +7,11 @@ from __future__ import annotations
 
 import torch
 
-from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_ROWS, ft_gen_normal_f32, ft_moe_decode_workspace_size,
-               ft_moe_expert_ffn_nvfp4_decode, ft_moe_layer_decode, ft_moe_layer_decode_workspace_size,
-               ft_moe_layer_weights, ft_moe_permute, ft_moe_permute_workspace_size, ft_moe_route, ft_nvfp4_pack_tiles,
-               ft_nvfp4_quantize_weight)
+from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_ROWS, FT_LAYOUT_UMMA_TILES, ft_gen_normal_f32,
+               ft_moe_decode_workspace_size, ft_moe_expert_ffn_nvfp4_decode, ft_moe_expert_ffn_nvfp4_prefill,
+               ft_moe_layer_decode, ft_moe_layer_decode_workspace_size, ft_moe_layer_weights, ft_moe_permute,
+               ft_moe_permute_workspace_size, ft_moe_prefill_workspace_size, ft_moe_route, ft_nvfp4_pack_tiles,
+               ft_nvfp4_pack_umma, ft_nvfp4_quantize_weight)
 
 PROJ_GATE, PROJ_UP, PROJ_DOWN = 0, 1, 2
 
@@ -21,6 +22,7 @@ class LayerWeights:
     layout ROWS:   gu_codes [n, 2I, H/2], gu_scales [n, 2I, H/16] (rows 2i / 2i+1 = gate / up row i),
                    d_codes [n, H, I/2], d_scales [n, H, I/16]
     layout TILES:  gu_codes [n, 2I*H*9/16], d_codes [n, H*I*9/16] (16-row tiles, see ft_nvfp4_pack_tiles)
+    layout UMMA:   the same sizes in 128x128 blocks for the tensor-core prefill (see ft_nvfp4_pack_umma)
     tscale [n, 4] fp32 (gate, up, down, pad)
     """
 
@@ -87,6 +89,9 @@ class LayerWeights:
         if self.layout == FT_LAYOUT_DECODE_TILES:
             ft_nvfp4_pack_tiles(guc, H // 2, gus, H // 16, 2 * I, H, self.gu_codes[wi], stream=stream)
             ft_nvfp4_pack_tiles(dc, I // 2, ds, I // 16, H, I, self.d_codes[wi], stream=stream)
+        elif self.layout == FT_LAYOUT_UMMA_TILES:
+            ft_nvfp4_pack_umma(guc, H // 2, gus, H // 16, 2 * I, H, self.gu_codes[wi], stream=stream)
+            ft_nvfp4_pack_umma(dc, I // 2, ds, I // 16, H, I, self.d_codes[wi], stream=stream)
 
     def fill_synthetic(self, stream_of, seed: int = 0, sigma: float = 0.02, experts=None, stream=None) -> None:
         """Draw each expert's fp32 weights on the device (Philox4x32-10 + Box-Muller) and quantise them.
@@ -99,6 +104,30 @@ class LayerWeights:
             for proj in (PROJ_GATE, PROJ_UP, PROJ_DOWN):
                 ft_gen_normal_f32(seed, stream_of(e, proj), H * I, sigma, tmp[proj], stream=stream)
             self.set_expert(e, tmp[0].view(I, H), tmp[1].view(I, H), tmp[2].view(H, I), stream=stream)
+
+
+class PrefillLayer:
+    """route -> permute -> tensor-core NVFP4 expert FFN with the combine, buffers allocated once."""
+
+    def __init__(self, E: int, H: int, I: int, k: int, T: int, device):
+        self.E, self.H, self.I, self.k, self.T = E, H, I, k, T
+        i32 = torch.int32
+        self.ids = torch.empty((T, k), dtype=i32, device=device)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.offsets = torch.empty(E + 1, dtype=i32, device=device)
+        self.perm = torch.empty(T * k, dtype=i32, device=device)
+        self.inv = torch.empty(T * k, dtype=i32, device=device)
+        self.active = torch.empty(E + 1, dtype=i32, device=device)
+        self.ws_perm = torch.empty(max(ft_moe_permute_workspace_size(T, E, k), 256), dtype=torch.uint8, device=device)
+        self.ws = torch.empty(ft_moe_prefill_workspace_size(T, k, E, H, I), dtype=torch.uint8, device=device)
+
+    def __call__(self, weights: LayerWeights, logits: torch.Tensor, x: torch.Tensor, out: torch.Tensor,
+                 stream=None) -> torch.Tensor:
+        ft_moe_route(logits, self.k, self.ids, self.w, stream=stream)
+        ft_moe_permute(self.ids, self.E, self.offsets, self.perm, self.inv, self.active, self.ws_perm, stream=stream)
+        ft_moe_expert_ffn_nvfp4_prefill(weights, x, self.k, self.offsets, self.perm, self.w, out, self.ws,
+                                        stream=stream)
+        return out
 
 
 class MoEDecodeLayer:

@@ -1,0 +1,123 @@
+"""GPU parity of the prefill expert FFN on the block-scaled FP4 tensor cores.
+
+The tensor-core path quantises the activations (x, and h after its bf16
+rounding) to NVFP4 with unit tensor scale; the oracle's A4 mode states the same
+arithmetic in fp64.  Routing and grouping are bit-exact; outputs within relative
+L2 5e-3 and max |err| 2e-2 * RMS per layer output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from helpers import assert_layer_close, oracle_expert
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+if torch.cuda.is_available():
+    import quantized_expert_ffn_06_b300 as Q
+    from quantized_expert_ffn_06_b300.layer import LayerWeights, PrefillLayer
+
+
+def to_dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(DEV)
+
+
+def weights(cfg, layer, generated=True):
+    lw = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_UMMA_TILES)
+    if generated:
+        lw.fill_synthetic(lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
+    else:
+        for e in range(cfg.E):
+            lw.set_expert(e, *(to_dev(W.weights_fp32(cfg, layer, e, p)) for p in range(3)))
+    return lw
+
+
+def run(cfg, lw, logits, x_bits):
+    T = logits.shape[0]
+    mod = PrefillLayer(cfg.E, cfg.H, cfg.I, cfg.k, T, DEV)
+    out = torch.empty((T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    mod(lw, to_dev(logits), to_dev(x_bits.view(np.int16), torch.bfloat16), out)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    return mod, out
+
+
+def check(cfg, layer, mod, out, logits, x_bits, rows=None):
+    ref = O.moe_layer(logits, x_bits, cfg.k, lambda e: oracle_expert(cfg, layer, e), O.MODE_A4, rows=rows)
+    assert np.array_equal(mod.ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(mod.offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(mod.perm.cpu().numpy(), ref["perm"])
+    got = out.float().cpu().numpy()
+    if rows is not None:
+        got = got[rows]
+    return assert_layer_close(got, ref["out"], f"prefill {cfg.name}")
+
+
+def test_tiny_layer_every_output():
+    cfg = W.CONFIGS["tiny"]
+    lw = weights(cfg, 0, generated=False)
+    logits, x_bits = W.router_logits(cfg, 0, 0), W.activations_bf16(cfg, 0, 0)
+    mod, out = run(cfg, lw, logits, x_bits)
+    check(cfg, 0, mod, out, logits, x_bits)
+
+
+@pytest.mark.parametrize("T", [1, 13, 37, 200])
+def test_ragged_token_counts(T):
+    cfg = W.scaled(W.CONFIGS["tiny"], T=T)
+    lw = weights(cfg, 0, generated=False)
+    logits, x_bits = W.router_logits(cfg, 0, 1), W.activations_bf16(cfg, 0, 1)
+    mod, out = run(cfg, lw, logits, x_bits)
+    check(cfg, 0, mod, out, logits, x_bits)
+
+
+def test_one_expert_spanning_several_tiles():
+    """k = 1 and every token routed to expert 5: 300 rows = three 128-row tiles, the last one partial."""
+    cfg = W.scaled(W.CONFIGS["tiny"], T=300, k=1)
+    lw = weights(cfg, 0, generated=False)
+    logits = W.router_logits(cfg, 0, 2).copy()
+    logits[:, 5] = 50.0
+    x_bits = W.activations_bf16(cfg, 0, 2)
+    mod, out = run(cfg, lw, logits, x_bits)
+    assert (mod.ids.cpu().numpy() == 5).all()
+    check(cfg, 0, mod, out, logits, x_bits)
+
+
+def test_prefill_35b_zipf_sampled_tokens():
+    cfg = W.CONFIGS["prefill_35b"]
+    lw = weights(cfg, 0)
+    logits, x_bits = W.router_logits(cfg, 0, 0), W.activations_bf16(cfg, 0, 0)
+    mod, out = run(cfg, lw, logits, x_bits)
+    counts = np.diff(mod.offsets.cpu().numpy())
+    assert counts.max() > 1000 and counts.min() < 100   # skewed groups, as Zipf(1.1) popularity gives
+    rows = [0, 1, 777, 2048, 4095]
+    check(cfg, 0, mod, out, logits, x_bits, rows=rows)
+
+
+def test_umma_packing_places_every_byte_where_the_layout_says():
+    cfg = W.CONFIGS["tiny"]
+    rows = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_ROWS)
+    umma = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_UMMA_TILES)
+    for lw in (rows, umma):
+        lw.set_expert(2, *(to_dev(W.weights_fp32(cfg, 0, 2, p)) for p in range(3)))
+    torch.cuda.synchronize()
+    codes = rows.gu_codes[2].cpu().numpy()    # [2I][H/2]
+    scales = rows.gu_scales[2].cpu().numpy()  # [2I][H/16]
+    blob = umma.gu_codes[2].cpu().numpy()
+    N, K = 2 * cfg.I, cfg.H
+    KSN = K // 128
+    for n in range(0, N, 7):
+        rt, r = divmod(n, 128)
+        for kk in range(0, K // 2, 5):
+            ks, b = divmod(kk, 64)
+            base = (rt * KSN + ks) * 9216
+            assert blob[base + (b // 16) * 2048 + (r // 8) * 128 + (r % 8) * 16 + b % 16] == codes[n, kk]
+        for j in range(K // 16):
+            ks, jj = divmod(j, 8)
+            base = (rt * KSN + ks) * 9216
+            assert blob[base + 8192 + (jj // 4) * 512 + (r % 32) * 16 + (r // 32) * 4 + jj % 4] == scales[n, j]
