@@ -34,6 +34,15 @@ METRIC = "MoE decode tok/s and % of HBM roofline; prefill NVFP4 TFLOP/s vs peak"
 UNIT = "tok/s"
 
 
+def load_bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    return 1800.0, "fallback"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -185,6 +194,31 @@ class OracleDecode:
 
     def threads(self) -> int:
         return self.O.lib().ora_max_threads()
+
+
+def oracle_prefill_baseline(cfg, n_rows: int = 16):
+    """The oracle (A4 mode) on a bounded sample of the prefill layer: route and permute all tokens, the expert FFN
+    and combine for n_rows tokens; reported as tokens/s and the FLOP rate of that sample."""
+    import oracle as O
+    logits = W.router_logits(cfg, 0, 0)
+    x_bits = W.activations_bf16(cfg, 0, 0)
+    q = {}
+
+    class _Deq:
+        def __init__(self, t):
+            self.Wg, self.Wu, self.Wd = (O.dequantize(*a) for a in t)
+
+    ids, _ = O.route(logits, cfg.k)
+    rows = list(range(n_rows))
+    for e in sorted(set(ids[rows].ravel().tolist())):
+        q[e] = [O.quantize_weight(W.weights_fp32(cfg, 0, e, p)) for p in range(3)]
+    t0 = time.perf_counter()
+    O.moe_layer(logits, x_bits, cfg.k, lambda e: _Deq(q[e]), O.MODE_A4, rows=np.array(rows))
+    secs = time.perf_counter() - t0
+    return {"value": n_rows / secs, "unit": "tok/s", "tflops": 6.0 * cfg.H * cfg.I * cfg.k * n_rows / secs / 1e12,
+            "cores": O.lib().ora_max_threads(), "kind": "oracle",
+            "sample": f"route and permute of all {cfg.T} tokens, then fp64 dequantisation, A4-mode FFN and combine "
+                      f"of {n_rows} tokens (weight quantisation untimed)"}
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -363,6 +397,152 @@ def run_gpu(args, ws, rank, local):
     }
 
 
+def run_gpu_prefill(args, ws, rank, local):
+    """Prefill layer step: T tokens through route -> permute -> tensor-core NVFP4 expert FFN + combine."""
+    import torch
+    import quantized_expert_ffn_06_b300 as Q
+    from quantized_expert_ffn_06_b300.layer import LayerWeights, PrefillLayer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = W.CONFIGS[args.config]
+    T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    NW = 4  # weight sets rotated between steps: 4 x the layer's weights, far beyond L2
+    S = min(args.distinct_steps, 4)
+    weights = []
+    for l in range(NW):
+        lw = LayerWeights(E, H, I, dev, layout=Q.FT_LAYOUT_UMMA_TILES)
+        lw.fill_synthetic(lambda e, p, l=l: W.w_stream(cfg.weight_cfg, l, e, p), sigma=cfg.w_sigma)
+        weights.append(lw)
+    step0 = rank * S
+    lg_host = np.stack([W.router_logits(cfg, s % NW, step0 + s) for s in range(S)])
+    x_host = np.stack([W.activations_bf16(cfg, s % NW, step0 + s) for s in range(S)])
+    lg_dev = torch.from_numpy(lg_host).to(dev)
+    x_dev = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    mod = PrefillLayer(E, H, I, k, T, dev)
+    stream = torch.cuda.Stream(device=dev)
+    n_cfg = NW * S  # (weight set, input) pairs cycled by the steps
+    with torch.cuda.stream(stream):
+        mod(weights[0], lg_dev[0], x_dev[0], out, stream=stream)
+    stream.synchronize()
+    graphs = []
+    for i in range(n_cfg):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            mod(weights[i % NW], lg_dev[i % S], x_dev[i % S], out, stream=stream)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status(stream) == 0
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_cfg].replay()
+    stream.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    bus = None
+    if hasattr(props, "pci_bus_id"):
+        bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(bus) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(args.steps):
+                graphs[i % n_cfg].replay()
+            ev1.record(stream)
+        ev1.synchronize()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    assert Q.ft_device_status(stream) == 0
+    step_s = ms / 1e3 / args.steps
+    # the expert FFN call alone (its kernels: plan, x quantisation, two grouped GEMMs, output), live, same stream
+    fe0, fe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_ffn = max(8, min(args.steps, 64))
+    with torch.cuda.stream(stream):
+        for i in range(n_cfg):
+            mod(weights[i % NW], lg_dev[i % S], x_dev[i % S], out, stream=stream)
+        fe0.record(stream)
+        for i in range(n_ffn):
+            Q.ft_moe_expert_ffn_nvfp4_prefill(weights[i % NW], x_dev[0], k, mod.offsets, mod.perm, mod.w, out, mod.ws,
+                                              stream=stream)
+        fe1.record(stream)
+    stream.synchronize()
+    ffn_s = fe0.elapsed_time(fe1) / 1e3 / n_ffn
+    # algorithmic work: real (unpadded) FLOPs 2*3*H*I per routed row; bytes = weights of the experts that
+    # received rows + x + logits + output
+    P = T * k
+    flops = 6.0 * H * I * P
+    touched = np.mean([len(set(np.argsort(-lg_host[s], axis=1, kind="stable")[:, :k].ravel().tolist()))
+                       for s in range(S)])
+    bytes_ffn = touched * (cfg.expert_bytes + 12) + T * H * 2 * 2
+    hbm_peak, hbm_kind = load_peaks()
+    bf16_peak, bf16_kind = load_bf16_peak()
+    fp4_peak = bf16_peak * 6.0  # nominal dense FP4 : BF16 ratio of 13.5 : 2.25
+    e2e = None
+    if not args.no_e2e:
+        x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+        l_pin = torch.from_numpy(lg_host).pin_memory()
+        o_pin = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        xb, lb = torch.empty_like(x_dev[0]), torch.empty_like(lg_dev[0])
+        eg = []
+        for i in range(NW):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                mod(weights[i], lb, xb, out, stream=stream)
+            eg.append(g)
+
+        def e2e_step(i):
+            xb.copy_(x_pin[i % S], non_blocking=True)
+            lb.copy_(l_pin[i % S], non_blocking=True)
+            eg[i % NW].replay()
+            o_pin.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                e2e_step(i)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                e2e_step(i)
+            e1.record(stream)
+        e1.synchronize()
+        ems = e0.elapsed_time(e1) / 1e3 / args.steps
+        e2e = {"value": flops / ems / 1e12, "unit": "TFLOP/s", "tok_per_s": T / ems,
+               "h2d_bytes_per_step": T * (H * 2 + E * 4), "d2h_bytes_per_step": T * H * 2}
+    return {
+        "metric": METRIC, "value": flops * ws / step_s / 1e12, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 x nvfp4 (E2M1, UE4M3 per 16), fp32 accumulate",
+        "data": "synthetic (seeded Philox4x32-10, Zipf(1.1) expert popularity)",
+        "tok_per_s": T * ws / step_s,
+        "config": {"workload": f"{cfg.name}: one MoE layer, hidden {H}, {E} experts, top-{k}, intermediate {I}, "
+                               f"{T} prompt tokens, NVFP4 weights and activations",
+                   "global_batch": T * ws,
+                   "l2": f"inputs larger than L2: {NW} weight sets of {touched * cfg.expert_bytes / 1e6:.0f} MB "
+                         f"rotated between steps",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": bytes_ffn / ffn_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": bytes_ffn / ffn_s / 1e9 / hbm_peak, "peak_kind": hbm_kind,
+                     "kernel": "ft_moe_expert_ffn_nvfp4_prefill (plan, x quantisation, gate/up and down grouped "
+                               "GEMMs, output), timed as one call",
+                     "bytes_per_launch": bytes_ffn, "avg_launch_us": ffn_s * 1e6, "traffic": None},
+        "tensor": {"achieved": flops / ffn_s / 1e12, "peak": fp4_peak, "unit": "TFLOP/s",
+                   "frac": flops / ffn_s / 1e12 / fp4_peak,
+                   "peak_kind": f"{bf16_kind} bf16 x 6 (nominal FP4:BF16 dense ratio)", "flops_per_launch": flops},
+        "e2e": e2e,
+        "gpu_launches": None,
+        "clocks": clk.report(),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,6 +587,16 @@ def main():
     if ws > 1:
         import torch
         torch.distributed.init_process_group("nccl")
+    if cfg.routing == "zipf":
+        res = run_gpu_prefill(args, ws, rank, local)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                res["cpu_baseline"] = oracle_prefill_baseline(cfg)
+            print(json.dumps(res))
+        if ws > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
     res = run_gpu(args, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:

@@ -13,8 +13,9 @@
 // Steps (one stream):
 //  1. k_pf_plan: every expert's permuted rows are padded to whole 128-row
 //     tiles; tile_off[e] = first tile of expert e (exclusive scan).
-//  2. k_pf_quant_x: x rows, gathered in permuted order, quantised into
-//     operand tiles.
+//  2. k_pf_quant_tokens + k_pf_gather_x: each token's x quantised once, then
+//     copied in permuted order into operand tiles, with a (token, weight) table
+//     of the padded rows.
 //  3. k_pf_gemm<1>: h = silu(Wg x) * (Wu x) per (expert, 128 gate/up rows,
 //     128 tokens) tile, rounded to bf16 and quantised into operand tiles.
 //  4. k_pf_gemm<2>: y = Wd h per (expert, 128 output rows, 128 tokens) tile;
@@ -36,8 +37,9 @@
 // blocks into an 8-stage shared-memory ring (cp.async.bulk + mbarriers),
 // warp 1 allocates TMEM and one of its threads issues the MMAs (two per stage,
 // K = 64 each, scales copied to TMEM with tcgen05.cp) into one of two 128-column
-// accumulators, and warps 2-5 drain the other accumulator (tcgen05.ld) through
-// the epilogue, so MMA and epilogue overlap.  Every wait is bounded; on expiry
+// accumulators, and warps 2-17 (four per TMEM lane quadrant, 32 columns each)
+// drain the other accumulator (tcgen05.ld) through the epilogue, so MMA and
+// epilogue overlap.  Every wait is bounded; on expiry
 // the kernel sets FT_DEVERR_TIMEOUT and finishes, freeing its TMEM.
 #include "common.cuh"
 
@@ -50,7 +52,8 @@ namespace pf {
 constexpr int BLK = 9216;           // one 128 x 128 operand block
 constexpr int NS = 8;               // ring stages (A block + B block each)
 constexpr int STAGE = 2 * BLK;
-constexpr int THREADS = 192;        // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int EPI_WARPS = 16;       // four per TMEM lane quadrant, each draining 32 of the 128 columns
+constexpr int THREADS = 32 * (2 + EPI_WARPS);  // warp 0 producer, warp 1 MMA, warps 2.. epilogue
 constexpr uint32_t TMEM_COLS = 512; // 2 x 128 accumulator columns + scale-factor columns
 constexpr uint32_t SF_COL0 = 256;   // 16 scale-factor columns per ring stage
 constexpr unsigned long long WAIT_NS = 2000000000ull;
@@ -71,9 +74,7 @@ struct PfGemmArgs {
     uint8_t* hq;
     int KSN2;
     // combine epilogue
-    const int32_t* perm;
-    const float* w;
-    int k;
+    const int2* rowmeta;     // [tiles*128] (token, routing weight bits) per padded row, token -1 for padding
     float* out32;            // [T][H]
     int H;
 };
@@ -88,12 +89,14 @@ __device__ __forceinline__ unsigned long long pf_gt() {
     return t;
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps (up to ~1 us) instead of
+// spinning, leaving issue slots to the epilogue warps; it wakes when the phase completes.
 __device__ __forceinline__ bool pf_try_wait(unsigned long long* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(pf_su(b)), "r"(parity)
+        : "r"(pf_su(b)), "r"(parity), "n"(1000)
         : "memory");
     return ok != 0;
 }
@@ -190,58 +193,76 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ of
     if (tid == 0) tile_off[E] = wsum[32];
 }
 
-// One warp per padded row q: x of the row's token, quantised with unit tensor
-// scale, into the operand tiles (zeros for padding rows).
-__global__ void __launch_bounds__(256) k_pf_quant_x(const uint16_t* __restrict__ x, int H, int k, int E,
-                                                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
-                                                    const int32_t* __restrict__ tile_off, int max_rows,
-                                                    uint8_t* __restrict__ xq) {
+// One warp per token: x[t] quantised once (unit tensor scale) into a compact
+// row of H/2 code bytes followed by H/16 scale bytes.
+__global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restrict__ x, int T, int H,
+                                                         uint8_t* __restrict__ xc) {
+    const int t = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    uint8_t* row = xc + (int64_t)t * (H / 2 + H / 16);
+    for (int e0 = lane * 64; e0 < H; e0 += 32 * 64) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H + e0);
+        uint32_t cw[8], sw = 0;
+#pragma unroll
+        for (int bl = 0; bl < 4; ++bl) {
+            float v[16];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint4 u = __ldg(src + 2 * bl + hh);
+                const uint32_t words[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[8 * hh + 2 * i] = __uint_as_float(words[i] << 16);
+                    v[8 * hh + 2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
+                }
+            }
+            uint2 c;
+            uint32_t sb;
+            quant_block16(v, 1.0f, c, sb);
+            cw[2 * bl] = c.x;
+            cw[2 * bl + 1] = c.y;
+            sw |= sb << (8 * bl);
+        }
+        *reinterpret_cast<uint4*>(row + e0 / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint4*>(row + e0 / 2 + 16) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        *reinterpret_cast<uint32_t*>(row + H / 2 + e0 / 16) = sw;
+    }
+}
+
+// One warp per padded row q: the compact quantised row of its token copied into
+// the operand tiles, and the row's (token, routing weight) for the combine
+// (token -1 for padding rows, whose tile rows keep whatever they held: every
+// output column depends only on its own row, and padding columns are skipped).
+__global__ void __launch_bounds__(256) k_pf_gather_x(const uint8_t* __restrict__ xc, int H, int k, int E,
+                                                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
+                                                     const float* __restrict__ w, const int32_t* __restrict__ tile_off,
+                                                     int max_rows, uint8_t* __restrict__ xq, int2* __restrict__ rowmeta) {
     const int q = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (q >= max_rows || q >= 128 * __ldg(tile_off + E)) return;
     const int e = pf_find_expert(tile_off, E, q >> 7);
     const int local = q - 128 * __ldg(tile_off + e);
     const int ne = __ldg(offsets + e + 1) - __ldg(offsets + e);
-    const bool valid = local < ne;
-    int t = 0;
-    if (valid) {
-        const int f = __ldg(perm + __ldg(offsets + e) + local);
-        t = f / k;
+    if (local >= ne) {
+        if (lane == 0) rowmeta[q] = make_int2(-1, 0);
+        return;
     }
+    const int f = __ldg(perm + __ldg(offsets + e) + local);
+    const int t = f / k;
+    if (lane == 0) rowmeta[q] = make_int2(t, __float_as_int(__ldg(w + f)));
+    const uint8_t* row = xc + (int64_t)t * (H / 2 + H / 16);
     const int KSN = H / 128, rt = q >> 7, r = q & 127;
-    for (int e0 = lane * 64; e0 < H; e0 += 32 * 64) {
-        uint8_t* blk = xq + ((int64_t)rt * KSN + e0 / 128) * pf::BLK;
-        const int b0 = (e0 & 127) / 2;  // 0 or 32
-        uint32_t cw[8], sw = 0;
-        if (valid) {
-            const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H + e0);
-#pragma unroll
-            for (int bl = 0; bl < 4; ++bl) {
-                float v[16];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint4 u = __ldg(src + 2 * bl + hh);
-                    const uint32_t words[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        v[8 * hh + 2 * i] = __uint_as_float(words[i] << 16);
-                        v[8 * hh + 2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
-                    }
-                }
-                uint2 c;
-                uint32_t sb;
-                quant_block16(v, 1.0f, c, sb);
-                cw[2 * bl] = c.x;
-                cw[2 * bl + 1] = c.y;
-                sw |= sb << (8 * bl);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) cw[i] = 0;
-        }
-        *reinterpret_cast<uint4*>(blk + blk_code_off(r, b0)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        *reinterpret_cast<uint4*>(blk + blk_code_off(r, b0 + 16)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        *reinterpret_cast<uint32_t*>(blk + blk_scale_off(r, (e0 & 127) / 16)) = sw;
+    // codes: 16-byte pieces (4 per 128-K block), then scale words (2 per block)
+    for (int i = lane; i < H / 32; i += 32) {
+        const int ks = i >> 2, piece = i & 3;
+        const uint4 v = *reinterpret_cast<const uint4*>(row + i * 16);
+        *reinterpret_cast<uint4*>(xq + ((int64_t)rt * KSN + ks) * pf::BLK + blk_code_off(r, piece * 16)) = v;
+    }
+    for (int i = lane; i < H / 64; i += 32) {
+        const int ks = i >> 1, half = i & 1;
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(row + H / 2 + i * 4);
+        *reinterpret_cast<uint32_t*>(xq + ((int64_t)rt * KSN + ks) * pf::BLK + blk_scale_off(r, half * 4)) = v;
     }
 }
 
@@ -255,60 +276,76 @@ __global__ void __launch_bounds__(256) k_pf_out(const float* __restrict__ out32,
 // SwiGLU + h quantisation.  Thread of TMEM lane r (gate row r even, up row r odd
 // of the tile's 64 pairs) holds 32 token columns.  Pair p = r/2 is feature
 // m*64 + p of h; the 16 features of one quantisation block are the 32 lanes of
-// one warp.
-__device__ __forceinline__ void epi_swiglu(const PfGemmArgs& a, const uint32_t (&v)[32], int e, int m, int ntg, int c0,
-                                           int qd, int lane, float tsg, float tsu) {
+// one warp.  The two lanes of a pair split the tokens: the even lane takes the
+// even tokens and the odd lane the odd ones, after one exchange, so every lane
+// computes distinct h values.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+__device__ __forceinline__ void epi_swiglu(const PfGemmArgs& a, const uint32_t (&v)[32], int m, int ntg, int c0, int qd,
+                                           int lane, float tsg, float tsu) {
     const int f0 = m * 64 + 16 * qd;  // first feature of this warp's block
     const int ks2 = f0 / 128, b0 = (f0 & 127) / 2, jblk = (f0 & 127) / 16;
     uint8_t* blk_base = a.hq + (int64_t)ntg * a.KSN2 * pf::BLK + (int64_t)ks2 * pf::BLK;
-    const bool gate = (lane & 1) == 0;
+    const int par = lane & 1;  // 0: gate lane, computes even tokens; 1: up lane, odd tokens
+    // phase 1: h of token 2q+par for this lane's feature (the even lane sends g of token 2q+1,
+    // the odd lane sends u of token 2q)
+    float hb[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float mine = __uint_as_float(v[j]);
-        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-        const float g = (gate ? mine : other) * tsg, u = (gate ? other : mine) * tsu;
-        const float hb = bf16_to_f32(bf16_bits(silu_f32(g) * u));
-        float am = fabsf(hb);
+    for (int q = 0; q < 16; ++q) {
+        const float ve = __uint_as_float(v[2 * q]), vo = __uint_as_float(v[2 * q + 1]);
+        const float recv = __shfl_xor_sync(0xffffffffu, par ? ve : vo, 1);
+        const float g = (par ? recv : ve) * tsg, u = (par ? vo : recv) * tsu;
+        hb[q] = bf16_to_f32(bf16_bits(silu_fast(g) * u));
+    }
+    // phase 2: block amax over the 16 lanes of the same parity
+    float am[16];
 #pragma unroll
-        for (int o = 2; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        const uint32_t sb = f32_to_e4m3_rn_sat(__fdiv_rn(am, 6.0f));
-        const float eff = e4m3_to_f32(sb);
-        // this lane's code (lanes 4u and 4u+2 hold features 2u and 2u+1 of the block)
-        const uint32_t pair = (eff == 0.0f) ? 0u : f32x2_to_e2m1x2_rn_sat(__fdiv_rn(hb, eff), 0.0f);
-        const uint32_t code = pair & 0xFu;
-        const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 2);
-        uint32_t word = ((lane & 3) == 0) ? ((code | (hi << 4)) << (8 * ((lane >> 2) & 3))) : 0u;
-        word |= __shfl_xor_sync(0xffffffffu, word, 4);
-        word |= __shfl_xor_sync(0xffffffffu, word, 8);
-        const uint32_t w1 = __shfl_sync(0xffffffffu, word, 16);
-        if (lane == 0) {
-            const int r = c0 + j;  // token row within the tile
-            *reinterpret_cast<uint2*>(blk_base + blk_code_off(r, b0)) = make_uint2(word, w1);
-            blk_base[blk_scale_off(r, jblk)] = (uint8_t)sb;
+    for (int q = 0; q < 16; ++q) am[q] = fabsf(hb[q]);
+#pragma unroll
+    for (int o = 2; o < 32; o <<= 1)
+#pragma unroll
+        for (int q = 0; q < 16; ++q) am[q] = fmaxf(am[q], __shfl_xor_sync(0xffffffffu, am[q], o));
+    // phase 3: scale and code (fp32, IEEE division, as the quantiser defines them)
+    uint32_t sbv[16], word[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        sbv[q] = f32_to_e4m3_rn_sat(__fdiv_rn(am[q], 6.0f));
+        const float eff = e4m3_to_f32(sbv[q]);
+        word[q] = (eff == 0.0f) ? 0u : (f32x2_to_e2m1x2_rn_sat(__fdiv_rn(hb[q], eff), 0.0f) & 0xFu);
+    }
+    // phase 4: bytes of features (2u, 2u+1) in lane 4u+par, then 8 bytes per token in lanes 0/1 and 16/17
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, word[q], 2);
+        word[q] = ((lane & 2) == 0) ? ((word[q] | (hi << 4)) << (8 * ((lane >> 2) & 3))) : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) word[q] |= __shfl_xor_sync(0xffffffffu, word[q], 4);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) word[q] |= __shfl_xor_sync(0xffffffffu, word[q], 8);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const uint32_t w1 = __shfl_sync(0xffffffffu, word[q], 16 + par);
+        if (lane < 2) {
+            const int r = c0 + 2 * q + par;  // token row within the tile
+            *reinterpret_cast<uint2*>(blk_base + blk_code_off(r, b0)) = make_uint2(word[q], w1);
+            blk_base[blk_scale_off(r, jblk)] = (uint8_t)sbv[q];
         }
     }
-    (void)e;
 }
 
-// Down projection + combine: out32[t][m*128 + r] += w[f] * tsd * y for each real token column.
-__device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t (&v)[32], int e, int m, int ntg, int c0,
-                                            int qd, int lane, float tsd) {
-    const int n_e = __ldg(a.offsets + e + 1) - __ldg(a.offsets + e);
-    const int local0 = (ntg - __ldg(a.tile_off + e)) * 128 + c0;
-    // column metadata: lane j looks up column c0 + j
-    int tj = -1;
-    float wj = 0.0f;
-    if (local0 + lane < n_e) {
-        const int f = __ldg(a.perm + __ldg(a.offsets + e) + local0 + lane);
-        tj = f / a.k;
-        wj = __ldg(a.w + f) * tsd;
-    }
-    const int row = m * 128 + 32 * qd + lane;
+// Down projection + combine: out32[t][m*128 + r] += w * tsd * y for each real token
+// column (row table entry: token, routing weight; token -1 for padding).
+__device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t (&v)[32], int2 meta, int m, int qd,
+                                            int lane, float tsd) {
+    const int tj = meta.x;
+    const float wj = __int_as_float(meta.y) * tsd;
+    float* dst = a.out32 + m * 128 + 32 * qd + lane;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const int t = __shfl_sync(0xffffffffu, tj, j);
         const float wt = __shfl_sync(0xffffffffu, wj, j);
-        if (t >= 0) atomicAdd(a.out32 + (int64_t)t * a.H + row, __uint_as_float(v[j]) * wt);
+        if (t >= 0) atomicAdd(dst + (int64_t)t * a.H, __uint_as_float(v[j]) * wt);
     }
 }
 
@@ -330,7 +367,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) 
         }
         for (int b = 0; b < 2; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&acc_full[b])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(pf_su(&acc_empty[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(pf_su(&acc_empty[b])), "n"(pf::EPI_WARPS));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_s = 0;
@@ -424,22 +461,25 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) 
             }
         }
     } else {
-        // ---------------- epilogue warps 2..5: TMEM lane quadrant qd = warp % 4
-        const int qd = warp & 3;
+        // ---------------- epilogue warps 2..17: TMEM lane quadrant qd = warp % 4, 32 columns each
+        const int qd = warp & 3, c0 = 32 * ((warp - 2) >> 2);
         int it = 0;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
             const int buf = it & 1;
-            if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // everything that does not depend on the accumulator is loaded before waiting for it
             int e, m, ntg;
             item(i, e, m, ntg);
             const float* ts = a.tscale + (int64_t)e * a.ts_stride;
             const float t0s = __ldg(ts + 0), t1s = __ldg(ts + 1), t2s = __ldg(ts + 2);
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            int2 meta = make_int2(-1, 0);
+            if (EPI == 2) meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + c0 + lane);
+            if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            {
                 uint32_t v[32];
                 tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
-                if (EPI == 1) epi_swiglu(a, v, e, m, ntg, c0, qd, lane, t0s, t1s);
-                else epi_combine(a, v, e, m, ntg, c0, qd, lane, t2s);
+                if (EPI == 1) epi_swiglu(a, v, m, ntg, c0, qd, lane, t0s, t1s);
+                else epi_combine(a, v, meta, m, qd, lane, t2s);
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
@@ -506,7 +546,7 @@ static int pf_sm_count() {
 static size_t a256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct PfWs {
-    size_t tile_off, xq, hq, out32, total;
+    size_t tile_off, xc, xq, hq, rowmeta, out32, total;
     int max_tiles;
 };
 
@@ -517,8 +557,12 @@ static PfWs pf_ws_layout(int T, int k, int E, int H, int I) {
     size_t off = 0;
     w.tile_off = off;
     off += a256((size_t)(E + 1) * 4);
+    w.xc = off;
+    off += a256((size_t)T * (H / 2 + H / 16));
     w.xq = off;
     off += a256((size_t)w.max_tiles * (H / 128) * pf::BLK);
+    w.rowmeta = off;
+    off += a256((size_t)w.max_tiles * 128 * 8);
     w.hq = off;
     off += a256((size_t)w.max_tiles * (I / 128) * pf::BLK);
     w.out32 = off;
@@ -576,6 +620,8 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     uint8_t* base = static_cast<uint8_t*>(ws);
     int32_t* tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
     uint8_t* xq = base + L.xq;
+    uint8_t* xc = base + L.xc;
+    int2* rowmeta = reinterpret_cast<int2*>(base + L.rowmeta);
     uint8_t* hq = base + L.hq;
     float* out32 = reinterpret_cast<float*>(base + L.out32);
     cudaStream_t s = cu(stream);
@@ -588,7 +634,9 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
     k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, tile_off);
     const int max_rows = 128 * L.max_tiles;
-    k_pf_quant_x<<<(unsigned)((max_rows + 7) / 8), 256, 0, s>>>(x, H, k, E, offsets, perm, tile_off, max_rows, xq);
+    k_pf_quant_tokens<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(x, T, H, xc);
+    k_pf_gather_x<<<(unsigned)((max_rows + 7) / 8), 256, 0, s>>>(xc, H, k, E, offsets, perm, w, tile_off, max_rows, xq,
+                                                                   rowmeta);
     PfGemmArgs g{};
     g.tscale = W->tscale;
     g.ts_stride = W->tscale_stride;
@@ -597,9 +645,7 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     g.tile_off = tile_off;
     g.hq = hq;
     g.KSN2 = I / 128;
-    g.perm = perm;
-    g.w = w;
-    g.k = k;
+    g.rowmeta = rowmeta;
     g.out32 = out32;
     g.H = H;
     const int G = pf_sm_count();
