@@ -246,7 +246,7 @@ def profiled_traffic(workload: str, src_hash: str):
 def run_gpu(args, ws, rank, local):
     import torch
     import quantized_expert_ffn_06_b300 as Q
-    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights
+    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights, MoEDecodeLayer
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -254,11 +254,15 @@ def run_gpu(args, ws, rank, local):
     L, S, T, H, E, k = cfg.layers, min(cfg.steps, args.distinct_steps), cfg.T, cfg.H, cfg.E, cfg.k
     if args.layers:
         L = args.layers
+    # the fused launch stages x and the h rows as f16 in shared memory (120 KB); larger shapes take the
+    # separate calls (route, permute, row-layout expert FFN, combine)
+    fused = T <= 16 and (T * (H + 32) + T * k * (cfg.I + 32)) * 2 <= 120 * 1024
+    layout = Q.FT_LAYOUT_DECODE_TILES if fused else Q.FT_LAYOUT_ROWS
 
-    # ---- weights (device generator + device quantiser), all experts resident, decode tile layout
+    # ---- weights (device generator + device quantiser), all experts resident
     weights = []
     for layer in range(L):
-        lw = LayerWeights(E, H, cfg.I, dev, layout=Q.FT_LAYOUT_DECODE_TILES)
+        lw = LayerWeights(E, H, cfg.I, dev, layout=layout)
         lw.fill_synthetic(lambda e, p, layer=layer: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
         weights.append(lw)
     torch.cuda.synchronize()
@@ -271,12 +275,19 @@ def run_gpu(args, ws, rank, local):
     lg_dev = torch.from_numpy(lg_host).to(dev)                                         # [S, L, T, E]
     out_dev = torch.empty((S, L, T, H), dtype=torch.bfloat16, device=dev)
 
-    layer_mods = [FusedDecodeLayer(E, H, cfg.I, k, T, dev) for _ in range(L)]
+    if fused:
+        layer_mods = [FusedDecodeLayer(E, H, cfg.I, k, T, dev) for _ in range(L)]
+    else:
+        layer_mods = [MoEDecodeLayer(E, H, cfg.I, k, T, dev) for _ in range(L)]
+    launches_per_layer = 1 if fused else 5  # route, permute, gate/up, down, combine
     stream = torch.cuda.Stream(device=dev)
 
     def step_body(xs, ls, os_):
         for l in range(L):
-            layer_mods[l](weights[l], ls[l], xs[l], os_[l], routing=False, stream=stream)
+            if fused:
+                layer_mods[l](weights[l], ls[l], xs[l], os_[l], routing=False, stream=stream)
+            else:
+                layer_mods[l](weights[l], ls[l], xs[l], os_[l], stream=stream)
 
     # ---- one CUDA graph per distinct step
     with torch.cuda.stream(stream):
@@ -388,11 +399,13 @@ def run_gpu(args, ws, rank, local):
                          (L * float(np.mean(unique)) * cfg.expert_bytes / 1e6),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "kernel": "k_moe_decode (ft_moe_layer_decode), one launch per layer",
+                     "peak_kind": peak_kind,
+                     "kernel": ("k_moe_decode (ft_moe_layer_decode), one launch per layer" if fused else
+                                "route + permute + k_decode_gateup + k_decode_down + combine per layer, timed together"),
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_launch_s * 1e6,
-                     "traffic": profiled_traffic(cfg.name, src_hash), "source_hash": src_hash},
+                     "traffic": profiled_traffic(cfg.name, src_hash) if fused else None, "source_hash": src_hash},
         "e2e": e2e,
-        "gpu_launches": L * args.steps,
+        "gpu_launches": L * args.steps * launches_per_layer,
         "clocks": clk.report(),
     }
 
@@ -543,6 +556,113 @@ def run_gpu_prefill(args, ws, rank, local):
     }
 
 
+def run_gpu_cache(args, ws, rank, local):
+    """Expert-cache decode stream: batch-1 tokens through L layers whose experts live in pinned host memory, with a
+    VRAM LRU cache of S slots per layer (misses filled by cudaMemcpyAsync on a side stream)."""
+    import torch
+    import quantized_expert_ffn_06_b300 as Q
+    from quantized_expert_ffn_06_b300.layer import CachedDecodeLayer, ExpertSlotPool, LayerWeights
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = W.CONFIGS[args.config]
+    L, T, H, E, k, I = cfg.layers, cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    if args.layers:
+        L = args.layers
+    n_steps = args.warmup + args.steps
+    pool = ExpertSlotPool(L, E, H, I, cfg.slots, dev)
+    scratch = LayerWeights(E, H, I, dev, layout=Q.FT_LAYOUT_DECODE_TILES)
+    for l in range(L):
+        scratch.fill_synthetic(lambda e, p, l=l: W.w_stream(cfg.weight_cfg, l, e, p), sigma=cfg.w_sigma)
+        pool.load_layer(l, scratch)
+    del scratch
+    torch.cuda.synchronize()
+    # routing of every (layer, step); activations cycle over 16 distinct draws (they do not affect the routing)
+    rank_off = rank * n_steps
+    lg_dev = torch.stack([torch.from_numpy(W.cache_stream_logits(cfg, l, rank_off + n_steps)[rank_off:])
+                          for l in range(L)]).to(dev)                                   # [L, steps, E]
+    NX = 16
+    x_dev = torch.from_numpy(np.stack([np.stack([W.activations_bf16(cfg, l, s) for l in range(L)])
+                                       for s in range(NX)]).view(np.int16)).view(torch.bfloat16).to(dev)  # [NX, L, T, H]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    copy_stream = torch.cuda.Stream(device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    layers = [CachedDecodeLayer(pool, l, k, T, copy_stream=copy_stream) for l in range(L)]
+    # pinned host -> device copy bandwidth on this box (the bound of the misses)
+    probe_h = torch.empty(512 << 20, dtype=torch.uint8, pin_memory=True)
+    probe_d = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    probe_d.copy_(probe_h, non_blocking=True)
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record()
+    for _ in range(4):
+        probe_d.copy_(probe_h, non_blocking=True)
+    p1.record()
+    torch.cuda.synchronize()
+    h2d_gbs = 4 * (512 << 20) / (p0.elapsed_time(p1) / 1e3) / 1e9
+    del probe_h, probe_d
+
+    def token(s):
+        for l in range(L):
+            layers[l](lg_dev[l, s][None, :], x_dev[s % NX, l], out, rank_off + s, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            token(s)
+    torch.cuda.synchronize()
+    h0, m0, b0 = pool.cache.stats()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    bus = None
+    if hasattr(props, "pci_bus_id"):
+        bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(bus) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for s in range(args.warmup, n_steps):
+                token(s)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    assert Q.ft_device_status(stream) == 0
+    h1, m1, b1 = pool.cache.stats()
+    hits, misses, filled = h1 - h0, m1 - m0, b1 - b0
+    step_s = ms / 1e3 / args.steps
+    hbm_peak, hbm_kind = load_peaks()
+    # per-token bound: every layer must bring its misses over PCIe and stream its k experts from HBM
+    miss_bytes_tok = filled / args.steps
+    hbm_bytes_tok = L * k * pool.expert_bytes
+    bound_s = miss_bytes_tok / (h2d_gbs * 1e9) + hbm_bytes_tok / (hbm_peak * 1e9)
+    return {
+        "metric": METRIC, "value": T * ws / step_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 weights x bf16 activations, fp32 accumulate",
+        "data": "synthetic (seeded Philox4x32-10; Zipf(1.1) popularity, 60 % of experts shared between tokens)",
+        "config": {"workload": f"{cfg.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, intermediate {I}, "
+                               f"batch {T}, VRAM LRU cache of {cfg.slots} slots per layer over a "
+                               f"{L * E * pool.slot_stride / 1e9:.1f} GB pinned host pool",
+                   "global_batch": T * ws, "l2": "inputs larger than L2: misses come from host memory",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "cache": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
+                  "h2d_bytes_per_token": miss_bytes_tok, "h2d_gbs_achieved": filled / (ms / 1e3) / 1e9,
+                  "h2d_gbs_measured_peak": h2d_gbs},
+        "roofline": {"bound": "pcie+hbm", "achieved": 1.0 / step_s, "peak": 1.0 / bound_s, "unit": "tok/s",
+                     "frac": bound_s / step_s, "peak_kind": f"measured pinned H2D {h2d_gbs:.1f} GB/s and {hbm_kind} HBM",
+                     "kernel": "whole token (route, host lookup, fills, slot-table publish, fused layer kernel) x layers",
+                     "traffic": None},
+        "e2e": None,
+        "gpu_launches": L * args.steps * 2,
+        "clocks": clk.report(),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,6 +707,14 @@ def main():
     if ws > 1:
         import torch
         torch.distributed.init_process_group("nccl")
+    if cfg.routing == "stream":
+        res = run_gpu_cache(args, ws, rank, local)
+        if rank == 0:
+            print(json.dumps(res))
+        if ws > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
     if cfg.routing == "zipf":
         res = run_gpu_prefill(args, ws, rank, local)
         if rank == 0:

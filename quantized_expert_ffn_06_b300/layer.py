@@ -191,7 +191,7 @@ class ExpertSlotPool:
         self.d_bytes = H * I * 9 // 16
         self.expert_bytes = self.gu_bytes + self.d_bytes + 16
         self.slot_stride = (self.expert_bytes + 255) // 256 * 256
-        self.host = torch.empty(L * E * self.slot_stride, dtype=torch.uint8).pin_memory()
+        self.host = torch.empty(L * E * self.slot_stride, dtype=torch.uint8, pin_memory=True)
         self.slots = torch.empty(L * S * self.slot_stride, dtype=torch.uint8, device=self.device)
         self.tables = torch.full((L, E), -1, dtype=torch.int32, device=self.device)
         base = self.host.data_ptr()
@@ -207,10 +207,13 @@ class ExpertSlotPool:
     def load_layer(self, layer: int, lw: LayerWeights) -> None:
         """Copy the E experts of a device LayerWeights (decode-tile layout) into the host pool."""
         assert lw.layout == FT_LAYOUT_DECODE_TILES and lw.n >= self.E
+        stage = torch.empty((self.E, self.slot_stride), dtype=torch.uint8, device=lw.device)
+        stage[:, :self.gu_bytes].copy_(lw.gu_codes[:self.E])
+        stage[:, self.gu_bytes:self.gu_bytes + self.d_bytes].copy_(lw.d_codes[:self.E])
+        stage[:, self.gu_bytes + self.d_bytes:self.expert_bytes].copy_(lw.tscale[:self.E].view(torch.uint8))
+        off = layer * self.E * self.slot_stride
+        self.host[off:off + self.E * self.slot_stride].view(self.E, self.slot_stride).copy_(stage)  # device -> pinned
         torch.cuda.synchronize(lw.device)
-        for e in range(self.E):
-            blk = torch.cat([lw.gu_codes[e], lw.d_codes[e], lw.tscale[e].view(torch.uint8)]).cpu()
-            self.host_expert(layer, e).copy_(blk)
 
     def layer_weights(self, layer: int) -> "SlotLayerWeights":
         return SlotLayerWeights(self, layer)
