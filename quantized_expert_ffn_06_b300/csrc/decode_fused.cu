@@ -61,6 +61,25 @@ constexpr size_t XS_BUDGET = 120 * 1024;  // staged activations: x and h, separa
 constexpr unsigned long long WAIT_NS = 2000000000ull;  // bound on any single wait
 }  // namespace dk
 
+// Division by a divisor fixed at launch: q = x / d as one multiply-high with
+// m = ceil(2^32 / d), exact whenever x * d < 2^32 (every use below stays far
+// inside that).  Runtime integer division is a long instruction sequence, and
+// this kernel's control code runs once per launch, so its size is its latency.
+struct FastDiv {
+    uint32_t d, m;  // m == 0 encodes d == 1
+};
+
+static FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.m = (d <= 1) ? 0u : (uint32_t)((0x100000000ull + d - 1) / d);
+    return f;
+}
+
+__device__ __forceinline__ int fdiv(int x, const FastDiv& f) {
+    return f.m ? (int)__umulhi((uint32_t)x, f.m) : x;
+}
+
 // Shared-memory plan, computed on the host (byte offsets into dynamic shared memory).
 struct DecodePlan {
     int nstages, stage_bytes;  // ring
@@ -69,8 +88,18 @@ struct DecodePlan {
     int max_ot;                // phase-2 output tiles per CTA, at most
     int xs_stride, hs_stride;  // halves per staged x / h row
     int off_bars, off_ids, off_wts, off_plist, off_pexp, off_hexp, off_ulist, off_ubeg, off_uwi, off_misc;
-    int off_xs, off_hs, off_red, off_ybuf, off_ring;
+    int off_xs, off_hs, off_red, off_ybuf, off_ring, off_ptok, off_ts;
     int smem;
+    FastDiv dv_ns;    // ring stages
+    FastDiv dv_tgu;   // gate/up tiles per expert (2I/16)
+    FastDiv dv_k;     // slots per token
+    FastDiv dv_xrow;  // 16-byte pieces per x row (H/8)
+    FastDiv dv_hrow;  // h words per row (I/2)
+    FastDiv dv_g;     // CTAs in the grid
+    FastDiv dv_t;     // tokens
+    FastDiv dv_j;     // down tiles per stage (J)
+    int logits_bulk;  // the logits are copied into the ring by one bulk copy
+    float inv_k;      // 1/k, rounded to nearest (the weight of every slot of a -inf row)
 };
 
 struct DecodeArgs {
@@ -91,7 +120,7 @@ struct DecodeArgs {
 };
 
 // misc ints in shared memory
-enum { M_U = 0, M_FLAG = 1, M_ABORT = 2, M_EPOCH = 3, M_XEXP = 4, M_TAGS = 4 + 16 };  // xexp: MAXT entries, tags: MAXNS
+enum { M_U = 0, M_FLAG = 1, M_ABORT = 2, M_EPOCH = 3, M_XEXP = 4, M_TAGS = 4 + 16, M_TS = 4 + 16 + 16 };  // xexp: MAXT entries, tags: MAXNS
 
 // ---------------------------------------------------------------------------- PTX helpers
 
@@ -125,20 +154,29 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* b, uint32_t pa
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase.  On expiry (or if the CTA already gave up)
-// returns false; the first expiry sets FT_DEVERR_TIMEOUT and the CTA's abort flag.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(b, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(b, parity)) {
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > dk::WAIT_NS) {
-            *abort_flag = 1;
-            raise_dev_error(FT_DEVERR_TIMEOUT);
-            return false;
-        }
+// Gives up a bounded wait: the first expiry in a CTA sets FT_DEVERR_TIMEOUT and
+// the CTA's abort flag; returns whether the wait may go on.
+__device__ __forceinline__ bool wait_budget_left(unsigned long long t0, volatile int* abort_flag) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > dk::WAIT_NS) {
+        *abort_flag = 1;
+        raise_dev_error(FT_DEVERR_TIMEOUT);
+        return false;
     }
     return true;
+}
+
+// Bounded wait on an mbarrier phase (slow path, out of line).  On expiry, or
+// if the CTA already gave up, returns false.
+__device__ __noinline__ bool mbar_wait_slow(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(b, parity))
+        if (!wait_budget_left(t0, abort_flag)) return false;
+    return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
+    return mbar_try_wait(b, parity) || mbar_wait_slow(b, parity, abort_flag);
 }
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* b) {
@@ -162,21 +200,26 @@ __device__ __forceinline__ int tag_read(const int* tag) {
     return v;
 }
 
-// Bounded wait for chunk n in stage s: its tag, then its full-barrier phase.
-__device__ __forceinline__ bool chunk_wait(unsigned long long* full, int* tags, int n, int NS, volatile int* abort_flag) {
-    const int s = n % NS;
-    if (tag_read(&tags[s]) != n) {
-        const unsigned long long t0 = globaltimer();
-        while (tag_read(&tags[s]) != n) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > dk::WAIT_NS) {
-                *abort_flag = 1;
-                raise_dev_error(FT_DEVERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-    return mbar_wait(&full[s], (n / NS) & 1, abort_flag);
+// Bounded wait for chunk n (stage n mod NS, use n / NS): its tag, then its
+// full-barrier phase.  Out of line: both consumer loops share one copy.
+// Bounded wait (slow path, out of line) for a shared-memory tag to read `want`.
+__device__ __noinline__ void tag_wait_slow(int* tag, int want, volatile int* abort_flag) {
+    const unsigned long long t0 = globaltimer();
+    while (tag_read(tag) != want)
+        if (!wait_budget_left(t0, abort_flag)) return;
+}
+
+__device__ __forceinline__ void tag_wait(int* tag, int want, volatile int* abort_flag) {
+    if (tag_read(tag) != want) tag_wait_slow(tag, want, abort_flag);
+}
+
+// Returns the stage; after an expired wait the CTA's abort flag is set and the
+// stage's contents are not to be trusted (the caller finishes without waiting).
+__device__ __noinline__ int chunk_wait(unsigned long long* full, int* tags, int n, FastDiv dv_ns, volatile int* abort_flag) {
+    const int q = fdiv(n, dv_ns), s = n - q * (int)dv_ns.d;
+    tag_wait(&tags[s], n, abort_flag);
+    mbar_wait(&full[s], q & 1, abort_flag);
+    return s;
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -238,53 +281,39 @@ __device__ __noinline__ void restage_scaled(int* exps, __half* dst, int stride, 
         return bf16_to_f32((uint16_t)((c & 1) ? (w >> 16) : (w & 0xFFFFu)));
     };
     const int w = ti >> 5, lane = ti & 31, nw = nthr >> 5;
+#pragma unroll 1
     for (int r = w; r < n; r += nw) {
         float m = 0.0f;
+#pragma unroll 1
         for (int i = lane; i < K; i += 32) m = fmaxf(m, fabsf(val(r, i)));
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) exps[r] = (m >= 16384.0f) ? ilogbf(m) - 14 : 0;
     }
     if (cta_wide) __syncthreads();
     else consumer_sync();
+#pragma unroll 1
     for (int idx = ti; idx < n * K; idx += nthr) {
         const int r = idx / K, c = idx - r * K;
         dst[r * stride + staged_pos(c)] = __float2half_rn(val(r, c) * pow2i(-exps[r]));
     }
 }
 
-// Stage the T activation rows x[T][K] (bf16) as f16 into dst (row stride
-// `stride` halves, staged_pos order) with every thread of the CTA.  The first
-// round of loads is issued before `mid()` runs, so the router's work overlaps
-// their latency.
-template <typename Mid>
-__device__ void stage_x(int* exps, volatile int* flag, __half* dst, int stride, const uint16_t* src, int n, int K,
-                        Mid mid) {
+// Convert the n activation rows that landed as bf16 [n][K] in `raw` (shared
+// memory, by one bulk copy) to f16 in dst (row stride `stride` halves,
+// staged_pos order), with every thread of the CTA; `src` is the same rows in
+// global memory, read again only on the rare rescaling path.
+__device__ void stage_x(int* exps, volatile int* flag, __half* dst, int stride, const uint16_t* raw, const uint16_t* src,
+                        int n, int K, FastDiv dv_row) {
     const int ti = threadIdx.x, nthr = blockDim.x;
-    const int per_row = K / 8, total = n * per_row;
-    constexpr int B = 4;  // 16-byte loads in flight per thread
+    const int per_row = K >> 3, total = n * per_row;
     bool big = false;
-    bool first = true;
-    for (int base = ti; first || base < total; base += B * nthr) {
-        uint4 v[B];
-#pragma unroll
-        for (int u = 0; u < B; ++u) {
-            const int idx = base + u * nthr;
-            if (idx < total) v[u] = __ldcg(reinterpret_cast<const uint4*>(src) + idx);
-        }
-        if (first) {
-            mid();
-            first = false;
-        }
-#pragma unroll
-        for (int u = 0; u < B; ++u) {
-            const int idx = base + u * nthr;
-            if (idx < total) {
-                const int r = idx / per_row, c = idx - r * per_row;
-                const uint4 o = make_uint4(bf16x2_to_f16x2(v[u].x, big), bf16x2_to_f16x2(v[u].y, big),
-                                           bf16x2_to_f16x2(v[u].z, big), bf16x2_to_f16x2(v[u].w, big));
-                *reinterpret_cast<uint4*>(dst + r * stride + staged_pos(c * 8)) = o;
-            }
-        }
+#pragma unroll 1
+    for (int idx = ti; idx < total; idx += nthr) {
+        const int r = fdiv(idx, dv_row), c = idx - r * per_row;
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + (size_t)idx * 8);
+        const uint4 o = make_uint4(bf16x2_to_f16x2(v.x, big), bf16x2_to_f16x2(v.y, big), bf16x2_to_f16x2(v.z, big),
+                                   bf16x2_to_f16x2(v.w, big));
+        *reinterpret_cast<uint4*>(dst + r * stride + staged_pos(c * 8)) = o;
     }
     if (big) *flag = 1;
     __syncthreads();
@@ -310,11 +339,12 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 // waiting (bounded) for each word to carry `epoch`; consumer threads only.
 // Returns false if a wait gave up.
 __device__ bool stage_h(int* exps, volatile int* flag, __half* dst, int stride, const unsigned long long* hw, int n, int I,
-                        unsigned int epoch, volatile int* abort_flag) {
+                        FastDiv dv_row, unsigned int epoch, volatile int* abort_flag) {
     const int ti = threadIdx.x, nthr = dk::NCW * 32;
     const int nw = I / 2, total = n * nw;
-    constexpr int B = 4;
+    constexpr int B = 8;  // 8-byte loads in flight per thread
     bool big = false, ok = true;
+#pragma unroll 1
     for (int base = ti; base < total; base += B * nthr) {
         unsigned long long v[B];
         uint32_t pending = 0;
@@ -335,9 +365,7 @@ __device__ bool stage_h(int* exps, volatile int* flag, __half* dst, int stride, 
                         v[u] = ld_relaxed_u64(hw + base + u * nthr);
                         if ((uint32_t)(v[u] >> 32) == epoch) pending &= ~(1u << u);
                     }
-                if (pending && (*abort_flag || globaltimer() - t0 > dk::WAIT_NS)) {
-                    if (!*abort_flag) raise_dev_error(FT_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
+                if (pending && !wait_budget_left(t0, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -347,7 +375,7 @@ __device__ bool stage_h(int* exps, volatile int* flag, __half* dst, int stride, 
         for (int u = 0; u < B; ++u) {
             const int idx = base + u * nthr;
             if (idx < total) {
-                const int r = idx / nw, c = idx - r * nw;
+                const int r = fdiv(idx, dv_row), c = idx - r * nw;
                 *reinterpret_cast<uint32_t*>(dst + r * stride + staged_pos(2 * c)) = bf16x2_to_f16x2((uint32_t)v[u], big);
             }
         }
@@ -418,131 +446,134 @@ __device__ __noinline__ float4 tile_partial(const uint8_t* tile, int KB, int kb0
 // Order-preserving key of an fp32 logit: larger value -> larger key; -0 and +0
 // map to the same key; NaN to 1 (below every number); 0 is never produced.
 __device__ __forceinline__ uint32_t logit_key(float v) {
-    if (v != v) return 1u;
-    if (v == 0.0f) v = 0.0f;
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (v != v) ? 1u : key;
 }
 
-// Top-k of one token's E logits by one warp.  Lane l holds experts
-// l*EPL .. l*EPL+EPL-1, so among equal keys the lowest lane, and within it the
-// lowest slot, is the lowest expert id.  Round j takes the warp-wide maximum key
-// (redux.sync), the lowest lane holding it, and that lane's lowest slot with it.
-// The weights are exp(l_j - l_0) / sum over the k selected, with the same
-// butterfly sum as ft_moe_route.  Lane j < k returns expert j and its weight.
-template <int EPL>
-__device__ __forceinline__ void route_token(const float* row, int E, int k, int& my_e, float& my_w, bool& bad) {
+// Top-k selection of one token's E logits by one warp.  Lane l holds experts
+// l*EPL .. l*EPL+EPL-1 (EPL = ceil(E/32)), so among equal keys the lowest lane,
+// and within it the lowest slot, is the lowest expert id.  Round j takes the
+// warp-wide maximum of the lanes' best keys (redux.sync) and the lowest lane
+// holding it; that lane clears the key it gave.  `row` may point to shared or
+// global memory.  Lane j < k gets expert j.
+//
+// E <= 256: eight keys per lane in registers, best of them by a 3-level tree.
+__device__ __forceinline__ int select_topk8(const float* row, int E, int k, bool& bad) {
     const int lane = threadIdx.x & 31;
-    float v[EPL];
-    uint32_t key[EPL];
+    const int EPL = (E + 31) >> 5;  // <= 8
+    uint32_t key[8];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const int e = lane * EPL + i;
-        v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
-        key[i] = (e < E) ? logit_key(v[i]) : 0u;
-        bad |= (e < E) && ((v[i] != v[i]) || (v[i] == INFINITY));
+        const bool in = i < EPL && e < E;
+        const float v = in ? row[e] : 0.0f;
+        key[i] = in ? logit_key(v) : 0u;
+        bad |= in && ((v != v) || (v == INFINITY));
     }
-    my_e = 0;
-    float my_v = -INFINITY;
+    int my_e = 0;
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
-        uint32_t lk = 0;
-        int li = 0;
+        // best key and its slot, ties to the lower slot
+        uint32_t k2[4], k1[2];
+        int i2[4], i1[2];
 #pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (key[i] > lk) {
-                lk = key[i];
-                li = i;
-            }
-        const uint32_t gk = __reduce_max_sync(0xffffffffu, lk);
-        const uint32_t ball = __ballot_sync(0xffffffffu, lk == gk);
-        const int wl = __ffs(ball) - 1;
-        float wv = -INFINITY;
+        for (int p = 0; p < 4; ++p) {
+            const bool hi = key[2 * p + 1] > key[2 * p];
+            k2[p] = hi ? key[2 * p + 1] : key[2 * p];
+            i2[p] = 2 * p + (hi ? 1 : 0);
+        }
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const bool hi = k2[2 * p + 1] > k2[2 * p];
+            k1[p] = hi ? k2[2 * p + 1] : k2[2 * p];
+            i1[p] = hi ? i2[2 * p + 1] : i2[2 * p];
+        }
+        const bool hi = k1[1] > k1[0];
+        const uint32_t bk = hi ? k1[1] : k1[0];
+        const int bi = hi ? i1[1] : i1[0];
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
+        const int wl = __ffs(__ballot_sync(0xffffffffu, bk == gk)) - 1;
+        const int we = __shfl_sync(0xffffffffu, lane * EPL + bi, wl);
         if (lane == wl) {
-            wv = v[0];
 #pragma unroll
-            for (int i = 0; i < EPL; ++i)
-                if (i == li) {
-                    wv = v[i];
-                    key[i] = 0u;
-                }
+            for (int i = 0; i < 8; ++i)
+                if (i == bi) key[i] = 0u;
         }
-        const int we = __shfl_sync(0xffffffffu, wl * EPL + li, wl);
-        wv = __shfl_sync(0xffffffffu, wv, wl);
-        if (lane == j) {
-            my_e = we;
-            my_v = wv;
-        }
+        if (lane == j) my_e = we;
     }
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    if (m == -INFINITY || m != m) {
-        my_w = 1.0f / (float)k;
-    } else {
-        const float ej = (lane < k) ? expf(my_v - m) : 0.0f;
-        const float s = warp_sum(ej);
-        my_w = ej / s;
-    }
+    return my_e;
 }
 
-// The same selection for 256 < E <= 1024 with few registers: each round every
-// lane rescans its (up to 32) logits through the L1 cache; `taken` marks the
-// slots already selected.
-__device__ __noinline__ void route_token_wide(const float* row, int E, int k, int& my_e, float& my_w, bool& bad) {
+// 256 < E <= 1024: a lane rescans its (up to 32) logits, skipping the slots in
+// `taken`.  Returns {expert of lane j < k, bad}.
+__device__ __noinline__ uint2 select_topk_wide(const float* row, int E, int k) {
     const int lane = threadIdx.x & 31;
-    const int EPL = (E + 31) / 32;
-    uint32_t taken = 0;
-#pragma unroll 1
-    for (int i = 0; i < EPL; ++i) {
-        const int e = lane * EPL + i;
-        if (e < E) {
-            const float v = __ldg(row + e);
-            bad |= (v != v) || (v == INFINITY);
-        }
-    }
-    my_e = 0;
-    float my_v = -INFINITY;
+    const int EPL = (E + 31) >> 5;
+    const int n = max(0, min(EPL, E - lane * EPL));
+    const float* mine = row + lane * EPL;
+    uint32_t taken = 0, bad = 0;
+    int my_e = 0;
+    uint32_t bk = 0;
+    int bi = 0;
+    bool dirty = true;
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
-        uint32_t lk = 0;
-        int li = 0;
-        float lv = -INFINITY;
+        if (dirty) {
+            bk = 0;
 #pragma unroll 1
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane * EPL + i;
-            if (e < E && !((taken >> i) & 1u)) {
-                const float v = __ldg(row + e);
-                const uint32_t key = logit_key(v);
-                if (key > lk) {
-                    lk = key;
-                    li = i;
-                    lv = v;
+            for (int i0 = 0; i0 < n; i0 += 4) {
+                float x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) x[u] = (i0 + u < n) ? mine[i0 + u] : 0.0f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u;
+                    bad |= (i < n) && ((x[u] != x[u]) || (x[u] == INFINITY));
+                    const uint32_t key = (i < n && !((taken >> i) & 1u)) ? logit_key(x[u]) : 0u;
+                    if (key > bk) {
+                        bk = key;
+                        bi = i;
+                    }
                 }
             }
+            dirty = false;
         }
-        const uint32_t gk = __reduce_max_sync(0xffffffffu, lk);
-        const uint32_t ball = __ballot_sync(0xffffffffu, lk == gk);
-        const int wl = __ffs(ball) - 1;
-        if (lane == wl) taken |= 1u << li;
-        const int we = __shfl_sync(0xffffffffu, wl * EPL + li, wl);
-        const float wv = __shfl_sync(0xffffffffu, lv, wl);
-        if (lane == j) {
-            my_e = we;
-            my_v = wv;
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
+        const int wl = __ffs(__ballot_sync(0xffffffffu, bk == gk)) - 1;
+        const int we = __shfl_sync(0xffffffffu, lane * EPL + bi, wl);
+        if (lane == wl) {
+            taken |= 1u << bi;
+            dirty = true;
         }
+        if (lane == j) my_e = we;
     }
+    return make_uint2((uint32_t)my_e, bad);
+}
+
+// Router of one token by one warp: top-k selection, then the weights
+// exp(l_j - l_0) / sum over the k selected, with the same butterfly sum as
+// ft_moe_route (every weight inv_k = 1/k when the largest logit is -inf).
+__device__ __forceinline__ void route_token(const float* row, int E, int k, float inv_k, int& my_e, float& my_w, bool& bad) {
+    const int lane = threadIdx.x & 31;
+    bool b = false;
+    if (E <= 256) {
+        my_e = select_topk8(row, E, k, b);
+    } else {
+        const uint2 r = select_topk_wide(row, E, k);
+        my_e = (int)r.x;
+        b = r.y != 0u;
+    }
+    bad = __any_sync(0xffffffffu, b);
+    const float my_v = (lane < k) ? row[my_e] : -INFINITY;
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
     if (m == -INFINITY || m != m) {
-        my_w = 1.0f / (float)k;
+        my_w = inv_k;
     } else {
         const float ej = (lane < k) ? expf(my_v - m) : 0.0f;
         const float s = warp_sum(ej);
         my_w = ej / s;
     }
-}
-
-__device__ __forceinline__ void route_token_any(const float* row, int E, int k, int& my_e, float& my_w, bool& bad) {
-    if (E <= 256) route_token<8>(row, E, k, my_e, my_w, bad);
-    else route_token_wide(row, E, k, my_e, my_w, bad);
 }
 
 // ---------------------------------------------------------------------------- kernel
@@ -552,14 +583,17 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const DecodePlan& P = a.P;
     unsigned long long* full = reinterpret_cast<unsigned long long*>(dsm + P.off_bars);
     unsigned long long* empty = full + dk::MAXNS;
+    unsigned long long* xbar = full + 2 * dk::MAXNS;  // the bulk copy of x
     int* s_ids = reinterpret_cast<int*>(dsm + P.off_ids);      // [nf] expert of slot f (route mode)
     float* s_wts = reinterpret_cast<float*>(dsm + P.off_wts);  // [nf] weight of slot f
     int* s_plist = reinterpret_cast<int*>(dsm + P.off_plist);  // [nf] slot f of permuted row p
+    int* s_ptok = reinterpret_cast<int*>(dsm + P.off_ptok);    // [nf] token of permuted row p
     int* s_pexp = reinterpret_cast<int*>(dsm + P.off_pexp);    // [nf] expert of permuted row p
     int* s_hexp = reinterpret_cast<int*>(dsm + P.off_hexp);    // [nf] pre-scale of staged h row p
     int* s_ulist = reinterpret_cast<int*>(dsm + P.off_ulist);  // [nf] selected experts, ascending
     int* s_ubeg = reinterpret_cast<int*>(dsm + P.off_ubeg);    // [nf+1] permuted-row range of each
     int* s_uwi = reinterpret_cast<int*>(dsm + P.off_uwi);      // [nf] weight index (-1: invalid slot)
+    float* s_ts = reinterpret_cast<float*>(dsm + P.off_ts);   // [nf][4] tensor scales (gate, up, down) of each
     int* misc = reinterpret_cast<int*>(dsm + P.off_misc);
     volatile int* abort_flag = misc + M_ABORT;
     __half* xs = reinterpret_cast<__half*>(dsm + P.off_xs);  // x rows (phase 1)
@@ -581,43 +615,60 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], dk::WPG);
         }
+        mbar_init(xbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         misc[M_FLAG] = 0;
         misc[M_ABORT] = 0;
+        misc[M_TS] = 0;
     }
     if (tid < dk::MAXT) misc[M_XEXP + tid] = 0;
     if (tid < dk::MAXNS) misc[M_TAGS + tid] = -1;
+#pragma unroll 1
     for (int i = tid; i < nf; i += dk::THREADS) s_hexp[i] = 0;
     __syncthreads();
     // inputs (and the workspace) may be written by the preceding kernel in the stream
     griddep_wait();
-    // this call's epoch: calls sharing a workspace each add G to its counter.  The producer
+    // x lands as bf16 in the h staging area (unused until the down phase) by one bulk copy.
+    // This call's epoch: calls sharing a workspace each add G to its counter.  The producer
     // lane takes it (off the router's path) and publishes it at the end of the prologue.
-    unsigned int old_count = 0;
-    if (tid == dk::NCW * 32) old_count = atomicAdd(a.bar, 1u);
-
-    // ---------------- prologue: every thread stages x; warps < T route their token meanwhile
-    int my_e = 0;
-    float my_w = 0.0f;
-    bool bad = false;
+    // The logits, where the plan allows, land the same way in the ring (unused until the weights
+    // stream); the router then reads them through a generic pointer either way.
     const bool route_mode = a.logits != nullptr;
-    stage_x(misc + M_XEXP, misc + M_FLAG, xs, P.xs_stride, a.x, T, H, [&] {
-        if (route_mode && warp < T) route_token_any(a.logits + (int64_t)warp * E, E, k, my_e, my_w, bad);
-    });
-    if (route_mode) {
-        if (warp < T) {
-            if (__any_sync(0xffffffffu, bad) && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
-            if (lane < k) {
-                s_ids[warp * k + lane] = my_e;
-                s_wts[warp * k + lane] = my_w;
-                if (c == 0 && a.ids_out) {
-                    a.ids_out[warp * k + lane] = my_e;
-                    a.w_out[warp * k + lane] = my_w;
-                }
+    const uint16_t* xraw = reinterpret_cast<const uint16_t*>(hs);
+    const float* lsrc = P.logits_bulk ? reinterpret_cast<const float*>(ring) : a.logits;
+    unsigned int old_count = 0;
+    if (tid == dk::NCW * 32) {
+        const uint32_t xbytes = (uint32_t)(T * H * 2), lbytes = route_mode && P.logits_bulk ? (uint32_t)(T * E * 4) : 0u;
+        mbar_arrive_expect_tx(xbar, xbytes + lbytes);
+        bulk_g2s(hs, a.x, xbytes, xbar);
+        if (lbytes) bulk_g2s(ring, a.logits, lbytes, xbar);
+        old_count = atomicAdd(a.bar, 1u);
+    }
+
+    // ---------------- prologue: warps < T route their token once the inputs have landed, then all
+    // threads stage x
+    mbar_wait(xbar, 0, abort_flag);
+    if (route_mode && warp < T) {
+        int my_e = 0;
+        float my_w = 0.0f;
+        bool bad = false;
+        route_token(lsrc + warp * E, E, k, P.inv_k, my_e, my_w, bad);
+        if (bad && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
+        if (lane < k) {
+            s_ids[warp * k + lane] = my_e;
+            s_wts[warp * k + lane] = my_w;
+            if (c == 0 && a.ids_out) {
+                a.ids_out[warp * k + lane] = my_e;
+                a.w_out[warp * k + lane] = my_w;
             }
         }
-        __syncthreads();
+    }
+    // the ring is next written by the async proxy (the weight stream): order the reads before it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    stage_x(misc + M_XEXP, misc + M_FLAG, xs, P.xs_stride, xraw, a.x, T, H, P.dv_xrow);  // ends with __syncthreads
+    if (route_mode) {
         // grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}
+#pragma unroll 1
         for (int f = tid; f < nf; f += dk::THREADS) {
             const int e = s_ids[f];
             int pos = 0;
@@ -627,9 +678,11 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 pos += (e2 < e) || (e2 == e && f2 < f);
             }
             s_plist[pos] = f;
+            s_ptok[pos] = fdiv(f, P.dv_k);
             s_pexp[pos] = e;
         }
     } else {
+#pragma unroll 1
         for (int p = tid; p < nf; p += dk::THREADS) {
             int pf = a.perm[p];
             if (pf < 0 || pf >= nf) {
@@ -637,6 +690,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 pf = 0;
             }
             s_plist[p] = pf;
+            s_ptok[p] = fdiv(pf, P.dv_k);
             s_wts[p] = a.w_in ? a.w_in[p] : 0.0f;  // indexed by slot f: w_in is [T][k]
             // expert owning row p: last e with offsets[e] <= p
             int lo = 0, hi = E - 1;
@@ -680,30 +734,34 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const unsigned int epoch = (unsigned int)misc[M_EPOCH];
 
     // ---------------- work split
-    const int tiles_gu = 2 * I / 16;
-    const int KB1 = H / 128, KB2 = I / 128;
+    const int tiles_gu = I >> 3;  // 16-row tiles of an expert's [2I][H] gate/up matrix
+    const int KB1 = H >> 7, KB2 = I >> 7;
     const int bytes1 = 9 * H, bytes2 = 9 * I;  // one 16-row tile of [.][H] or [.][I]
-    const int n1 = U * tiles_gu;  // <= 512 * 256
-    const int p1_beg = (int)((long long)n1 * c / G), p1_end = (int)((long long)n1 * (c + 1) / G);
-    const int n2 = H / 16;
-    const int o_beg = n2 * c / G, o_end = n2 * (c + 1) / G;  // n2 * G <= 64 K
+    const int n1 = U * tiles_gu;                // <= 512 * 2048
+    const int p1_beg = (int)((unsigned)(n1 * c) / (unsigned)G), p1_end = (int)((unsigned)(n1 * (c + 1)) / (unsigned)G);
+    const int n2 = H >> 4;
+    const int o_beg = fdiv(n2 * c, P.dv_g), o_end = fdiv(n2 * (c + 1), P.dv_g);
     const int J = P.J;
     const int n_p1 = p1_end - p1_beg;
     const int n_ot = o_end - o_beg;
-    const int n_jg = (U + J - 1) / J;  // expert groups per output tile
+    const int n_jg = fdiv(U + J - 1, P.dv_j);  // expert groups per output tile
     const int n_chunks = n_p1 + n_ot * n_jg;
 
     if (warp == dk::NCW) {
         // ---------------- producer: stream tiles into the ring
         if (lane == 0) {
-            int issued = 0;
-            for (int n = 0; n < n_chunks; ++n, ++issued) {
-                const int s = n % NS, use = n / NS;
+            int n = 0, s = 0, use = 0;  // chunk, its stage and the stage's use
+            int u = 0, lt = 0;          // gate/up chunk: expert and tile within it
+            if (n_p1 > 0) {
+                u = fdiv(p1_beg, P.dv_tgu);
+                lt = p1_beg - u * tiles_gu;
+            }
+            int otl = 0, jg = 0;  // down chunk: output tile and expert group
+#pragma unroll 1
+            for (; n < n_chunks; ++n) {
                 if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag)) break;
                 uint8_t* dst = ring + (size_t)s * P.stage_bytes;
                 if (n < n_p1) {
-                    const int t = p1_beg + n;
-                    const int u = t / tiles_gu, lt = t - u * tiles_gu;
                     const int wi = s_uwi[u];
                     if (wi < 0) {
                         mbar_arrive(&full[s]);
@@ -712,29 +770,75 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                         bulk_g2s(dst, W.gu_codes + (int64_t)wi * W.gu_codes_stride + (int64_t)lt * bytes1,
                                  (uint32_t)bytes1, &full[s]);
                     }
-                    tag_publish(&misc[M_TAGS + s], n);
+                    if (++lt == tiles_gu) {
+                        lt = 0;
+                        ++u;
+                    }
                 } else {
-                    const int m = n - n_p1;
-                    const int otl = m / n_jg, jg = m % n_jg, ot = o_beg + otl;
+                    const int ot = o_beg + otl;
                     const int u0 = jg * J, nj = min(J, U - u0);
                     uint32_t tx = 0;
+#pragma unroll 1
                     for (int jj = 0; jj < nj; ++jj) tx += (s_uwi[u0 + jj] >= 0) ? (uint32_t)bytes2 : 0u;
                     mbar_arrive_expect_tx(&full[s], tx);
+#pragma unroll 1
                     for (int jj = 0; jj < nj; ++jj) {
                         const int wi = s_uwi[u0 + jj];
                         if (wi >= 0)
                             bulk_g2s(dst + jj * bytes2, W.d_codes + (int64_t)wi * W.d_codes_stride + (int64_t)ot * bytes2,
                                      (uint32_t)bytes2, &full[s]);
                     }
-                    tag_publish(&misc[M_TAGS + s], n);
+                    if (++jg == n_jg) {
+                        jg = 0;
+                        ++otl;
+                    }
                 }
+                tag_publish(&misc[M_TAGS + s], n);
+                if (++s == NS) {
+                    s = 0;
+                    ++use;
+                }
+            }
+            // Once every CTA of this grid has started (the call counter reaches epoch * G), the
+            // next kernel in the stream may be scheduled: it cannot take an SM one of ours still
+            // needs, and it waits for our completion itself before reading anything.
+            {
+                const unsigned long long t0 = globaltimer();
+                unsigned int v;
+                do {
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.bar) : "memory");
+                } while ((int)(v - epoch * (unsigned)G) < 0 && globaltimer() - t0 < 100000ull);
+                if ((int)(v - epoch * (unsigned)G) >= 0) griddep_launch_dependents();
             }
             // the CTA must not exit with copies still landing in its shared memory: wait
             // (bounded, even after an abort) for the last use of every stage issued
             const unsigned long long t0 = globaltimer();
-            for (int n = max(0, issued - NS); n < issued; ++n)
-                while (!mbar_try_wait(&full[n % NS], (n / NS) & 1) && globaltimer() - t0 < dk::WAIT_NS) {
+            int q = max(0, n - NS);
+            const int uq = fdiv(q, P.dv_ns);
+            int sq = q - uq * NS, pq = uq & 1;
+#pragma unroll 1
+            for (; q < n; ++q) {
+                while (!mbar_try_wait(&full[sq], pq) && globaltimer() - t0 < dk::WAIT_NS) {
                 }
+                if (++sq == NS) {
+                    sq = 0;
+                    pq ^= 1;
+                }
+            }
+        } else {
+            // lanes 1..31: the tensor scales (gate, up, down) of the selected experts into shared
+            // memory, published once all are there
+#pragma unroll 1
+            for (int u = lane - 1; u < U; u += 31) {
+                const int wi = s_uwi[u];
+                const float* ts = W.tscale + (int64_t)(wi >= 0 ? wi : 0) * W.tscale_stride;
+                const float t0 = ts[0], t1 = ts[1], t2 = ts[2];
+                s_ts[4 * u + 0] = (wi >= 0) ? t0 : 0.0f;
+                s_ts[4 * u + 1] = (wi >= 0) ? t1 : 0.0f;
+                s_ts[4 * u + 2] = (wi >= 0) ? t2 : 0.0f;
+            }
+            __syncwarp(0xfffffffeu);
+            if (lane == 1) tag_publish(&misc[M_TS], 1);
         }
         return;
     }
@@ -747,22 +851,20 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     unsigned long long* hw = reinterpret_cast<unsigned long long*>(a.hbuf);
     float* gred = red + gi * 2 * dk::WPG * 16 * TC;  // this group's two partial buffers [WPG][16][TC]
     int buf = 0;
+#pragma unroll 1
     for (int n = gi; n < n_p1; n += dk::NG) {
-        const int s = n % NS;
         const int t = p1_beg + n;
-        const int u = t / tiles_gu, lt = t - u * tiles_gu;
+        const int u = fdiv(t, P.dv_tgu), lt = t - u * tiles_gu;
         const int wi = s_uwi[u];
         const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
-        // tensor scales, in flight while the tile lands
-        const float tsg = (wi >= 0) ? W.tscale[(int64_t)wi * W.tscale_stride + 0] : 0.0f;
-        const float tsu = (wi >= 0) ? W.tscale[(int64_t)wi * W.tscale_stride + 1] : 0.0f;
-        chunk_wait(full, misc + M_TAGS, n, NS, abort_flag);
+        const int s = chunk_wait(full, misc + M_TAGS, n, P.dv_ns, abort_flag);
         const uint8_t* tile = ring + (size_t)s * P.stage_bytes;
         float* rb = gred + buf * dk::WPG * 16 * TC;
+#pragma unroll 1
         for (int c0 = 0; c0 < tu; c0 += 8) {
             const int nt = min(8, tu - c0);
             const int col = min(g8, nt - 1);
-            const int xr = s_plist[pb + c0 + col] / k;  // token of this lane's column
+            const int xr = s_ptok[pb + c0 + col];  // token of this lane's column
             float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
             if (wi >= 0) dv = tile_partial(tile, KB1, wig, dk::WPG, xs + xr * P.xs_stride);
             const float d[4] = {dv.x, dv.y, dv.z, dv.w};
@@ -780,8 +882,11 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         if (lane == 0) mbar_arrive(&empty[s]);
         group_sync(gi);
         // h = silu(g) * u for the tile's 8 (gate, up) row pairs: word j holds pairs 2j, 2j+1
+        tag_wait(&misc[M_TS], 1, abort_flag);
+        const float tsg = s_ts[4 * u + 0], tsu = s_ts[4 * u + 1];
+#pragma unroll 1
         for (int idx = gtid; idx < 4 * tu; idx += dk::WPG * 32) {
-            const int j = idx / tu, tt = idx - j * tu;
+            const int j = idx & 3, tt = idx >> 2;
             float hv[2] = {0.0f, 0.0f};
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -793,7 +898,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                     us += rb[(w * 16 + 2 * p + 1) * TC + tt];
                 }
                 if (wi >= 0) {
-                    const float sc = pow2i(misc[M_XEXP + s_plist[pb + tt] / k]);
+                    const float sc = pow2i(misc[M_XEXP + s_ptok[pb + tt]]);
                     hv[h2] = silu_f32(gs * tsg * sc) * (us * tsu * sc);
                 }
             }
@@ -805,34 +910,31 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     }
 
     // ---------------- phase 2: down projection over this CTA's output rows
-    if (n_ot > 0) {  // all h rows (permuted order), as each becomes available
-        stage_h(s_hexp, misc + M_FLAG, hs, P.hs_stride, hw, nf, I, epoch, abort_flag);
-        // once every CTA of this grid has started (the call counter says so), the next
-        // kernel in the stream may be scheduled: it cannot take an SM one of ours still
-        // needs, and it waits for our completion itself before reading anything
-        if (tid == 0) {
-            unsigned int v;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.bar) : "memory");
-            if ((int)(v - epoch * (unsigned)G) >= 0) griddep_launch_dependents();
-        }
-    }
+    if (n_ot > 0)  // all h rows (permuted order), as each becomes available
+        stage_h(s_hexp, misc + M_FLAG, hs, P.hs_stride, hw, nf, I, P.dv_hrow, epoch, abort_flag);
+    tag_wait(&misc[M_TS], 1, abort_flag);
     {
-        // chunks n_p1 .. n_chunks-1, round robin over the groups continuing phase 1's order
+        // chunks n_p1 .. n_chunks-1, round robin over the groups continuing phase 1's order;
+        // chunk n_p1 + m is (output tile m / n_jg, expert group m mod n_jg)
         int n = n_p1 + ((gi - n_p1) % dk::NG + dk::NG) % dk::NG;
+        int otl = 0, jg = n - n_p1;
+        while (n_jg > 0 && jg >= n_jg) {
+            jg -= n_jg;
+            ++otl;
+        }
+#pragma unroll 1
         for (; n < n_chunks; n += dk::NG) {
-            const int s = n % NS;
-            const int m = n - n_p1;
-            const int otl = m / n_jg, jg = m % n_jg, ot = o_beg + otl;
+            const int ot = o_beg + otl;
             const int u0 = jg * J, nj = min(J, U - u0);
-            const int wi0 = (wig < nj) ? s_uwi[u0 + wig] : -1;
-            const float tsd0 = (wi0 >= 0) ? W.tscale[(int64_t)wi0 * W.tscale_stride + 2] : 0.0f;
-            chunk_wait(full, misc + M_TAGS, n, NS, abort_flag);
+            const int s = chunk_wait(full, misc + M_TAGS, n, P.dv_ns, abort_flag);
             const uint8_t* slot = ring + (size_t)s * P.stage_bytes;
+#pragma unroll 1
             for (int jj = wig; jj < nj; jj += dk::WPG) {
                 const int u = u0 + jj;
                 const int wi = s_uwi[u];
                 const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
-                const float tsd = (jj == wig) ? tsd0 : ((wi >= 0) ? W.tscale[(int64_t)wi * W.tscale_stride + 2] : 0.0f);
+                const float tsd = s_ts[4 * u + 2];
+#pragma unroll 1
                 for (int c0 = 0; c0 < tu; c0 += 8) {
                     const int nt = min(8, tu - c0);
                     const int col = min(g8, nt - 1);
@@ -859,14 +961,21 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            jg += dk::NG;
+            while (jg >= n_jg) {
+                jg -= n_jg;
+                ++otl;
+            }
         }
     }
     consumer_sync();
-    // combine: out[t][row] = bf16(sum_j w[t][j] * y[t*k + j][row]) in slot order j
+    // combine: out[t][row] = bf16(sum_j w[t][j] * y[t*k + j][row]) in slot order j;
+    // item i = (otl * T + tok) * 16 + row
     if (a.out) {
+#pragma unroll 1
         for (int i = tid; i < n_ot * 16 * T; i += dk::NCW * 32) {
-            const int tok = i / (n_ot * 16), rr = i - tok * n_ot * 16;
-            const int otl = rr >> 4, r = rr & 15;
+            const int q = i >> 4, r = i & 15;
+            const int otl = fdiv(q, P.dv_t), tok = q - otl * T;
             float acc = 0.0f;
 #pragma unroll 1
             for (int j = 0; j < k; ++j) {
@@ -940,19 +1049,22 @@ static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::s
         off = align_up(off + bytes, 128);
         return (int)o;
     };
-    p.off_bars = take(2 * dk::MAXNS * 8);
+    p.off_bars = take((2 * dk::MAXNS + 1) * 8);
     p.off_ids = take((size_t)nf * 4);
     p.off_wts = take((size_t)nf * 4);
     p.off_plist = take((size_t)nf * 4);
+    p.off_ptok = take((size_t)nf * 4);
     p.off_pexp = take((size_t)nf * 4);
     p.off_hexp = take((size_t)nf * 4);
     p.off_ulist = take((size_t)nf * 4);
     p.off_ubeg = take((size_t)(nf + 1) * 4);
     p.off_uwi = take((size_t)nf * 4);
-    p.off_misc = take((4 + dk::MAXT + dk::MAXNS) * 4);
+    p.off_misc = take((4 + dk::MAXT + dk::MAXNS + 1) * 4);
+    p.off_ts = take((size_t)nf * 16);
     p.xs_stride = H + dk::XPAD;
     p.hs_stride = I + dk::XPAD;
-    const size_t xs = (size_t)T * p.xs_stride * 2, hs = (size_t)nf * p.hs_stride * 2;
+    // the h staging area first receives x as bf16 [T][H] (the prologue's bulk copy)
+    const size_t xs = (size_t)T * p.xs_stride * 2, hs = std::max((size_t)nf * p.hs_stride * 2, (size_t)T * H * 2);
     if (xs + hs > dk::XS_BUDGET) {
         why = "activations of " + std::to_string(T) + " tokens and their " + std::to_string(nf) +
               " expert rows do not fit the fused kernel's staging area";
@@ -974,6 +1086,15 @@ static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::s
     p.nstages = (int)std::min<size_t>(dk::MAXNS, (dk::SMEM_BUDGET - off) / p.stage_bytes);
     p.smem = (int)(off + (size_t)p.nstages * p.stage_bytes);
     p.J = std::max(1, std::min(p.stage_bytes / (9 * I), 16));
+    p.dv_ns = make_fastdiv((uint32_t)p.nstages);
+    p.dv_tgu = make_fastdiv((uint32_t)(I / 8));
+    p.dv_k = make_fastdiv((uint32_t)k);
+    p.dv_xrow = make_fastdiv((uint32_t)(H / 8));
+    p.dv_hrow = make_fastdiv((uint32_t)(I / 2));
+    p.dv_g = make_fastdiv((uint32_t)G);
+    p.dv_t = make_fastdiv((uint32_t)T);
+    p.dv_j = make_fastdiv((uint32_t)p.J);
+    p.inv_k = 1.0f / (float)k;
     return true;
 }
 
@@ -983,6 +1104,10 @@ static ft_status launch_decode(const DecodeArgs& args0, ft_stream_t stream, cons
     DecodeArgs a = args0;
     std::string why;
     if (!plan_decode(a.T, a.k, W.H, W.I, G, a.P, why)) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
+    // the router's logits come in by one bulk copy when their address and size allow it
+    const size_t lbytes = (size_t)a.T * W.E * 4;
+    a.P.logits_bulk = a.logits && aligned(a.logits, 16) && lbytes % 16 == 0 &&
+                      lbytes <= (size_t)a.P.nstages * a.P.stage_bytes;
     static std::once_flag once;
     std::call_once(once, [] {
         cudaFuncSetAttribute(k_moe_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET);

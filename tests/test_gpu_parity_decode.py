@@ -264,3 +264,63 @@ def test_fused_nan_logits_flag_and_stay_in_bounds():
     assert Q.ft_device_status() & Q.FT_DEVERR_NAN_LOGIT
     ids = mod.ids.cpu().numpy()
     assert ids.min() >= 0 and ids.max() < cfg.E
+
+
+def fused_run(cfg, lw, logits_dev, x_bits):
+    mod = FusedDecodeLayer(cfg.E, cfg.H, cfg.I, cfg.k, logits_dev.shape[0], DEV)
+    out = torch.empty((logits_dev.shape[0], cfg.H), dtype=torch.bfloat16, device=DEV)
+    mod(lw, logits_dev, to_dev(x_bits.view(np.int16), torch.bfloat16), out)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    return mod, out
+
+
+@pytest.mark.parametrize("E,k,T", [(8, 2, 4), (10, 3, 3), (512, 8, 3)])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_fused_router_on_wide_odd_and_unaligned_logits(E, k, T, offset):
+    """E = 512 takes more than eight logits per lane; T*E*4 not a multiple of 16 bytes, or logits
+    not 16-byte aligned (offset 1), make the router read global memory instead of a staged copy."""
+    cfg = W.scaled(W.CONFIGS["tiny"], E=E, k=k, T=T)
+    lw = device_weights_generated(cfg, 0, layout=Q.FT_LAYOUT_DECODE_TILES)
+    logits = W.router_logits(cfg, 0, 1)
+    x_bits = W.activations_bf16(cfg, 0, 1)
+    buf = torch.zeros(T * E + 4, dtype=torch.float32, device=DEV)
+    lg = buf[offset:offset + T * E].view(T, E)
+    lg.copy_(to_dev(logits))
+    mod, out = fused_run(cfg, lw, lg, x_bits)
+    ref = oracle_layer(cfg, 0, logits, x_bits)
+    check_routing(mod, ref)
+    assert_layer_close(out.float().cpu().numpy(), ref["out"], f"E={E} offset={offset}")
+
+
+def test_fused_router_ties_and_infinities():
+    """Equal logits go to the lower expert id; a row of -inf gives every slot weight 1/k."""
+    cfg = W.scaled(W.CONFIGS["tiny"], E=16, k=3)
+    lw = device_weights_generated(cfg, 0, layout=Q.FT_LAYOUT_DECODE_TILES)
+    logits = np.zeros((4, 16), np.float32)
+    logits[1, [9, 3, 12]] = 2.0
+    logits[2] = -np.inf
+    logits[3, :] = -np.inf
+    logits[3, [5, 7]] = [0.0, -0.0]
+    x_bits = W.activations_bf16(cfg, 0, 3)
+    mod, out = fused_run(cfg, lw, to_dev(logits), x_bits)
+    ref = oracle_layer(cfg, 0, logits, x_bits)
+    check_routing(mod, ref)
+    assert_layer_close(out.float().cpu().numpy(), ref["out"], "ties")
+
+
+def test_fused_activations_beyond_f16_range_are_rescaled():
+    """A token row scaled by 2^20 overflows f16 staging: x and its h rows take the exact
+    power-of-two rescaling path.  Each token row is checked on its own scale."""
+    cfg = W.CONFIGS["tiny"]
+    lw = device_weights_from_host(cfg, 0, layout=Q.FT_LAYOUT_DECODE_TILES)
+    logits = W.router_logits(cfg, 0, 2)
+    x32 = W.bf16_bits_to_f32(W.activations_bf16(cfg, 0, 2)).copy()
+    x32[1] *= 2.0 ** 20
+    x_bits = (x32.view(np.uint32) >> 16).astype(np.uint16)   # exact: only exponents changed
+    mod, out = fused_run(cfg, lw, to_dev(logits), x_bits)
+    ref = oracle_layer(cfg, 0, logits, x_bits)
+    check_routing(mod, ref)
+    got = out.float().cpu().numpy()
+    for t in range(cfg.T):
+        assert_layer_close(got[t:t + 1], ref["out"][t:t + 1], f"token {t}")
