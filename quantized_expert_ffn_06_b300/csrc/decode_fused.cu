@@ -120,7 +120,8 @@ struct DecodeArgs {
 };
 
 // misc ints in shared memory
-enum { M_U = 0, M_FLAG = 1, M_ABORT = 2, M_EPOCH = 3, M_XEXP = 4, M_TAGS = 4 + 16, M_TS = 4 + 16 + 16 };  // xexp: MAXT entries, tags: MAXNS
+// (xexp: MAXT entries, tags: MAXNS; FLAG / HFLAG: x / h rows needed rescaling)
+enum { M_U = 0, M_FLAG = 1, M_ABORT = 2, M_EPOCH = 3, M_XEXP = 4, M_TAGS = 4 + 16, M_TS = 4 + 16 + 16, M_HFLAG = M_TS + 1 };
 
 // ---------------------------------------------------------------------------- PTX helpers
 
@@ -455,52 +456,53 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
 // l*EPL .. l*EPL+EPL-1 (EPL = ceil(E/32)), so among equal keys the lowest lane,
 // and within it the lowest slot, is the lowest expert id.  Round j takes the
 // warp-wide maximum of the lanes' best keys (redux.sync) and the lowest lane
-// holding it; that lane clears the key it gave.  `row` may point to shared or
-// global memory.  Lane j < k gets expert j.
+// holding it.  `row` may point to shared or global memory.  Lane j < k gets
+// expert j.
 //
-// E <= 256: eight keys per lane in registers, best of them by a 3-level tree.
+// E <= 256: each lane sorts its (up to) eight keys once, descending, by a
+// stable odd-even transposition network (equal keys keep their slot order), so
+// a round reads only the head of every lane's list and the winner pops it:
+// the rounds' dependent chain is the warp reduction alone.
 __device__ __forceinline__ int select_topk8(const float* row, int E, int k, bool& bad) {
     const int lane = threadIdx.x & 31;
     const int EPL = (E + 31) >> 5;  // <= 8
-    uint32_t key[8];
+    uint32_t key[8], idx[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = lane * EPL + i;
         const bool in = i < EPL && e < E;
         const float v = in ? row[e] : 0.0f;
         key[i] = in ? logit_key(v) : 0u;
+        idx[i] = (uint32_t)i;
         bad |= in && ((v != v) || (v == INFINITY));
     }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+#pragma unroll
+        for (int i = r & 1; i + 1 < 8; i += 2) {
+            const bool sw = key[i + 1] > key[i];
+            const uint32_t ka = key[i], kb = key[i + 1], ia = idx[i], ib = idx[i + 1];
+            key[i] = sw ? kb : ka;
+            key[i + 1] = sw ? ka : kb;
+            idx[i] = sw ? ib : ia;
+            idx[i + 1] = sw ? ia : ib;
+        }
+    }
+    uint32_t sidx = 0;  // sorted slots, 3 bits each, head in the low bits
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sidx |= idx[i] << (3 * i);
     int my_e = 0;
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
-        // best key and its slot, ties to the lower slot
-        uint32_t k2[4], k1[2];
-        int i2[4], i1[2];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const bool hi = key[2 * p + 1] > key[2 * p];
-            k2[p] = hi ? key[2 * p + 1] : key[2 * p];
-            i2[p] = 2 * p + (hi ? 1 : 0);
-        }
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            const bool hi = k2[2 * p + 1] > k2[2 * p];
-            k1[p] = hi ? k2[2 * p + 1] : k2[2 * p];
-            i1[p] = hi ? i2[2 * p + 1] : i2[2 * p];
-        }
-        const bool hi = k1[1] > k1[0];
-        const uint32_t bk = hi ? k1[1] : k1[0];
-        const int bi = hi ? i1[1] : i1[0];
-        const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
-        const int wl = __ffs(__ballot_sync(0xffffffffu, bk == gk)) - 1;
-        const int we = __shfl_sync(0xffffffffu, lane * EPL + bi, wl);
-        if (lane == wl) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i == bi) key[i] = 0u;
-        }
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, key[0]);
+        const int wl = __ffs(__ballot_sync(0xffffffffu, key[0] == gk)) - 1;
+        const int we = __shfl_sync(0xffffffffu, lane * EPL + (int)(sidx & 7u), wl);
         if (lane == j) my_e = we;
+        const bool win = lane == wl;  // pops its head
+#pragma unroll
+        for (int i = 0; i < 7; ++i) key[i] = win ? key[i + 1] : key[i];
+        key[7] = win ? 0u : key[7];
+        sidx = win ? (sidx >> 3) : sidx;
     }
     return my_e;
 }
@@ -618,6 +620,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         mbar_init(xbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         misc[M_FLAG] = 0;
+        misc[M_HFLAG] = 0;
         misc[M_ABORT] = 0;
         misc[M_TS] = 0;
     }
@@ -666,8 +669,27 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     // the ring is next written by the async proxy (the weight stream): order the reads before it
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     stage_x(misc + M_XEXP, misc + M_FLAG, xs, P.xs_stride, xraw, a.x, T, H, P.dv_xrow);  // ends with __syncthreads
-    if (route_mode) {
-        // grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}
+    // grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}.  Up to 32 slots
+    // one warp does it with shuffles and goes straight on to the scan below.
+    const bool warp_grouping = route_mode && nf <= 32;
+    if (warp_grouping) {
+        if (warp == 0) {
+            const int f = lane;
+            const int e = (f < nf) ? s_ids[f] : 0x7fffffff;
+            int pos = 0;
+#pragma unroll 4
+            for (int f2 = 0; f2 < nf; ++f2) {
+                const int e2 = __shfl_sync(0xffffffffu, e, f2);
+                pos += (e2 < e) || (e2 == e && f2 < f);
+            }
+            if (f < nf) {
+                s_plist[pos] = f;
+                s_ptok[pos] = fdiv(f, P.dv_k);
+                s_pexp[pos] = e;
+            }
+            __syncwarp();
+        }
+    } else if (route_mode) {
 #pragma unroll 1
         for (int f = tid; f < nf; f += dk::THREADS) {
             const int e = s_ids[f];
@@ -704,9 +726,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             s_pexp[p] = lo;
         }
     }
-    __syncthreads();
-    // every thread has read the x-staging flag: reset it for the h staging (published below)
-    if (tid == 32) misc[M_FLAG] = 0;
+    if (!warp_grouping) __syncthreads();
     // selected experts = segment starts of pexp (warp 0, ballot scan)
     if (warp == 0) {
         int run = 0;
@@ -911,7 +931,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
 
     // ---------------- phase 2: down projection over this CTA's output rows
     if (n_ot > 0)  // all h rows (permuted order), as each becomes available
-        stage_h(s_hexp, misc + M_FLAG, hs, P.hs_stride, hw, nf, I, P.dv_hrow, epoch, abort_flag);
+        stage_h(s_hexp, misc + M_HFLAG, hs, P.hs_stride, hw, nf, I, P.dv_hrow, epoch, abort_flag);
     tag_wait(&misc[M_TS], 1, abort_flag);
     {
         // chunks n_p1 .. n_chunks-1, round robin over the groups continuing phase 1's order;
@@ -926,10 +946,14 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         for (; n < n_chunks; n += dk::NG) {
             const int ot = o_beg + otl;
             const int u0 = jg * J, nj = min(J, U - u0);
+            // warps per expert tile: with one or two experts in the chunk the group's four warps
+            // split each tile's K-blocks, and their partials are summed through shared memory
+            const int wpe = (nj == 1) ? 4 : (nj == 2) ? 2 : 1;
             const int s = chunk_wait(full, misc + M_TAGS, n, P.dv_ns, abort_flag);
             const uint8_t* slot = ring + (size_t)s * P.stage_bytes;
+            float* rb = gred + buf * dk::WPG * 16 * TC;
 #pragma unroll 1
-            for (int jj = wig; jj < nj; jj += dk::WPG) {
+            for (int jj = wig / wpe; jj < nj; jj += dk::WPG / wpe) {
                 const int u = u0 + jj;
                 const int wi = s_uwi[u];
                 const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
@@ -939,8 +963,21 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                     const int nt = min(8, tu - c0);
                     const int col = min(g8, nt - 1);
                     float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (wi >= 0) dv = tile_partial(slot + jj * bytes2, KB2, 0, 1, hs + (pb + c0 + col) * P.hs_stride);
+                    if (wi >= 0)
+                        dv = tile_partial(slot + jj * bytes2, KB2, wig & (wpe - 1), wpe, hs + (pb + c0 + col) * P.hs_stride);
                     const float d[4] = {dv.x, dv.y, dv.z, dv.w};
+                    if (wpe > 1) {  // this warp's share of the K-blocks, summed below
+                        float* r = rb + wig * 16 * TC;
+                        if (2 * q4 < nt) {
+                            r[g8 * TC + c0 + 2 * q4] = d[0];
+                            r[(g8 + 8) * TC + c0 + 2 * q4] = d[2];
+                        }
+                        if (2 * q4 + 1 < nt) {
+                            r[g8 * TC + c0 + 2 * q4 + 1] = d[1];
+                            r[(g8 + 8) * TC + c0 + 2 * q4 + 1] = d[3];
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int cc = c0 + 2 * q4 + h2;  // column of d[h2] (row g8) and d[2 + h2] (row g8 + 8)
@@ -961,6 +998,29 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (wpe > 1) {
+                group_sync(gi);
+                // item idx of expert e2: row idx & 15, column idx >> 4
+#pragma unroll 1
+                for (int e2 = 0; e2 < nj; ++e2) {
+                    const int u = u0 + e2;
+                    const int wi = s_uwi[u];
+                    const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
+                    const float tsd = s_ts[4 * u + 2];
+#pragma unroll 1
+                    for (int idx = gtid; idx < 16 * tu; idx += dk::WPG * 32) {
+                        const int r = idx & 15, tt = idx >> 4;
+                        float ys = 0.0f;
+#pragma unroll 1
+                        for (int w = 0; w < wpe; ++w) ys += rb[((e2 * wpe + w) * 16 + r) * TC + tt];
+                        const int p = pb + tt;
+                        ys = (wi >= 0) ? ys * (tsd * pow2i(s_hexp[p])) : 0.0f;
+                        ybuf[(otl * nf + s_plist[p]) * 16 + r] = ys;
+                        if (a.y) a.y[(int64_t)p * H + ot * 16 + r] = ys;
+                    }
+                }
+                buf ^= 1;
+            }
             jg += dk::NG;
             while (jg >= n_jg) {
                 jg -= n_jg;
@@ -1059,7 +1119,7 @@ static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::s
     p.off_ulist = take((size_t)nf * 4);
     p.off_ubeg = take((size_t)(nf + 1) * 4);
     p.off_uwi = take((size_t)nf * 4);
-    p.off_misc = take((4 + dk::MAXT + dk::MAXNS + 1) * 4);
+    p.off_misc = take((4 + dk::MAXT + dk::MAXNS + 2) * 4);
     p.off_ts = take((size_t)nf * 16);
     p.xs_stride = H + dk::XPAD;
     p.hs_stride = I + dk::XPAD;
@@ -1085,7 +1145,10 @@ static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::s
     }
     p.nstages = (int)std::min<size_t>(dk::MAXNS, (dk::SMEM_BUDGET - off) / p.stage_bytes);
     p.smem = (int)(off + (size_t)p.nstages * p.stage_bytes);
+    // down tiles per stage: as many as a stage holds; for long down rows (8+ K-blocks) few enough
+    // that every group gets a chunk per output tile and splits its tiles' K-blocks
     p.J = std::max(1, std::min(p.stage_bytes / (9 * I), 16));
+    if (I / 128 >= 8) p.J = std::max(1, std::min(p.J, (nf + dk::NG - 1) / dk::NG));
     p.dv_ns = make_fastdiv((uint32_t)p.nstages);
     p.dv_tgu = make_fastdiv((uint32_t)(I / 8));
     p.dv_k = make_fastdiv((uint32_t)k);
