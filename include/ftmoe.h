@@ -267,13 +267,14 @@ FT_API size_t ft_moe_prefill_workspace_size(int T, int k, int E, int H, int I);
  *   additions not fixed: fp32 atomics).
  *   W (device) weights in FT_LAYOUT_UMMA_TILES, no slot table; H a multiple
  *          of 128, I a multiple of 128.
- *   x (device) bf16 [T][H]; offsets, perm (device) from ft_moe_permute;
- *   w (device) fp32 [T][k] routing weights; out (device) bf16 [T][H].
+ *   x (device) bf16 [T][H], 16-byte aligned; offsets, perm (device) from
+ *   ft_moe_permute; w (device) fp32 [T][k] routing weights; out (device) bf16
+ *   [T][H], 8-byte aligned.  A misaligned x or out is FT_ERR_INVALID_ARG.
  *   ws: ft_moe_prefill_workspace_size(T, k, E, H, I) bytes, 256-byte aligned
  *       (per-expert tile offsets, quantised x and h tiles, an fp32 output
  *       accumulator); no initial content needed.
- * Each expert's rows are padded to whole 128-row tiles; padding rows are zero
- * and ignored. */
+ * Each expert's rows are padded to whole 128-row tiles; the padding rows of a
+ * tile hold whatever the workspace held and never reach the output. */
 FT_API ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
                                                  const int32_t* offsets, const int32_t* perm, const float* w,
                                                  uint16_t* out, void* ws, size_t ws_bytes, ft_stream_t stream);

@@ -444,69 +444,6 @@ __device__ __noinline__ float4 tile_partial(const uint8_t* tile, int KB, int kb0
 
 // ---------------------------------------------------------------------------- routing
 
-// Order-preserving key of an fp32 logit: larger value -> larger key; -0 and +0
-// map to the same key; NaN to 1 (below every number); 0 is never produced.
-__device__ __forceinline__ uint32_t logit_key(float v) {
-    const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
-    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return (v != v) ? 1u : key;
-}
-
-// Top-k selection of one token's E logits by one warp.  Lane l holds experts
-// l*EPL .. l*EPL+EPL-1 (EPL = ceil(E/32)), so among equal keys the lowest lane,
-// and within it the lowest slot, is the lowest expert id.  Round j takes the
-// warp-wide maximum of the lanes' best keys (redux.sync) and the lowest lane
-// holding it.  `row` may point to shared or global memory.  Lane j < k gets
-// expert j.
-//
-// E <= 256: each lane sorts its (up to) eight keys once, descending, by a
-// stable odd-even transposition network (equal keys keep their slot order), so
-// a round reads only the head of every lane's list and the winner pops it:
-// the rounds' dependent chain is the warp reduction alone.
-__device__ __forceinline__ int select_topk8(const float* row, int E, int k, bool& bad) {
-    const int lane = threadIdx.x & 31;
-    const int EPL = (E + 31) >> 5;  // <= 8
-    uint32_t key[8], idx[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int e = lane * EPL + i;
-        const bool in = i < EPL && e < E;
-        const float v = in ? row[e] : 0.0f;
-        key[i] = in ? logit_key(v) : 0u;
-        idx[i] = (uint32_t)i;
-        bad |= in && ((v != v) || (v == INFINITY));
-    }
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-#pragma unroll
-        for (int i = r & 1; i + 1 < 8; i += 2) {
-            const bool sw = key[i + 1] > key[i];
-            const uint32_t ka = key[i], kb = key[i + 1], ia = idx[i], ib = idx[i + 1];
-            key[i] = sw ? kb : ka;
-            key[i + 1] = sw ? ka : kb;
-            idx[i] = sw ? ib : ia;
-            idx[i + 1] = sw ? ia : ib;
-        }
-    }
-    uint32_t sidx = 0;  // sorted slots, 3 bits each, head in the low bits
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sidx |= idx[i] << (3 * i);
-    int my_e = 0;
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-        const uint32_t gk = __reduce_max_sync(0xffffffffu, key[0]);
-        const int wl = __ffs(__ballot_sync(0xffffffffu, key[0] == gk)) - 1;
-        const int we = __shfl_sync(0xffffffffu, lane * EPL + (int)(sidx & 7u), wl);
-        if (lane == j) my_e = we;
-        const bool win = lane == wl;  // pops its head
-#pragma unroll
-        for (int i = 0; i < 7; ++i) key[i] = win ? key[i + 1] : key[i];
-        key[7] = win ? 0u : key[7];
-        sidx = win ? (sidx >> 3) : sidx;
-    }
-    return my_e;
-}
-
 // 256 < E <= 1024: a lane rescans its (up to 32) logits, skipping the slots in
 // `taken`.  Returns {expert of lane j < k, bad}.
 __device__ __noinline__ uint2 select_topk_wide(const float* row, int E, int k) {

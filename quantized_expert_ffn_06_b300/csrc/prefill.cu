@@ -33,13 +33,17 @@
 // tcgen05.cp .32x128b.warpx4 moves into TMEM (4 columns per 64 K).  A block is
 // one contiguous bulk copy.
 //
-// The GEMM kernel is persistent (one CTA per SM): warp 0 streams A and B
-// blocks into an 8-stage shared-memory ring (cp.async.bulk + mbarriers),
-// warp 1 allocates TMEM and one of its threads issues the MMAs (two per stage,
-// K = 64 each, scales copied to TMEM with tcgen05.cp) into one of two 128-column
-// accumulators, and warps 2-17 (four per TMEM lane quadrant, 32 columns each)
-// drain the other accumulator (tcgen05.ld) through the epilogue, so MMA and
-// epilogue overlap.  Every wait is bounded; on expiry
+// The GEMM kernel is persistent (one CTA per SM): warp 0 streams weight and
+// token blocks into a 3-stage shared-memory ring (cp.async.bulk + mbarriers;
+// four K blocks of each operand per copy, since a bulk copy costs about the
+// same whatever its size), warp 1 allocates TMEM and one of its threads issues
+// the MMAs (two per K block, K = 64 each, scales copied to TMEM with
+// tcgen05.cp) into one of two 128-column accumulators, and warps 2-17 (four per
+// TMEM lane quadrant, 32 columns each) drain the other accumulator (tcgen05.ld)
+// through the epilogue, so MMA and epilogue overlap.  The token tile is the
+// MMA's M side: each TMEM lane is one token and its columns are weight rows, so
+// the SwiGLU + NVFP4 quantisation of h and the weighted combine run without
+// leaving the thread.  Every wait is bounded; on expiry
 // the kernel sets FT_DEVERR_TIMEOUT and finishes, freeing its TMEM.
 #include "common.cuh"
 
@@ -50,14 +54,19 @@ namespace ft {
 
 namespace pf {
 constexpr int BLK = 9216;           // one 128 x 128 operand block
-constexpr int NS = 8;               // ring stages (A block + B block each)
-constexpr int STAGE = 2 * BLK;
+constexpr int KPS = 4;              // K blocks per ring stage: a bulk copy costs about the same whatever
+                                    // its size, so A and B each come in one copy of up to 4 blocks
+constexpr int NS = 3;               // ring stages (KPS A blocks + KPS B blocks each)
+constexpr int STAGE = 2 * KPS * BLK;
 constexpr int EPI_WARPS = 16;       // four per TMEM lane quadrant, each draining 32 of the 128 columns
 constexpr int THREADS = 32 * (2 + EPI_WARPS);  // warp 0 producer, warp 1 MMA, warps 2.. epilogue
 constexpr uint32_t TMEM_COLS = 512; // 2 x 128 accumulator columns + scale-factor columns
-constexpr uint32_t SF_COL0 = 256;   // 16 scale-factor columns per ring stage
+constexpr uint32_t SF_COL0 = 256;   // 16 scale-factor columns per K block of a ring stage
 constexpr unsigned long long WAIT_NS = 2000000000ull;
 constexpr size_t SMEM = (size_t)NS * STAGE + 1024;
+constexpr int RES_MAXKSN = 16;      // resident token tile: up to 16 K blocks (H or I up to 2048)
+constexpr int RES_MAXNS = 8;        // its weight ring: up to 8 stages of KPS blocks
+constexpr size_t SMEM_LIMIT = 227 * 1024 - 1024;  // dynamic shared memory, leaving room for the static part
 }  // namespace pf
 
 struct PfGemmArgs {
@@ -77,6 +86,7 @@ struct PfGemmArgs {
     const int2* rowmeta;     // [tiles*128] (token, routing weight bits) per padded row, token -1 for padding
     float* out32;            // [T][H]
     int H;
+    int nstages;             // ring stages (resident-token-tile kernel)
 };
 
 // ---------------------------------------------------------------------------- PTX helpers
@@ -230,129 +240,139 @@ __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restr
     }
 }
 
-// One warp per padded row q: the compact quantised row of its token copied into
-// the operand tiles, and the row's (token, routing weight) for the combine
-// (token -1 for padding rows, whose tile rows keep whatever they held: every
-// output column depends only on its own row, and padding columns are skipped).
+// One block per 128-row operand tile: the compact quantised rows of the tile's
+// tokens copied into the tile, and each row's (token, routing weight) for the
+// combine (token -1 for padding rows, whose tile rows keep whatever they held:
+// every output row depends only on its own tile row, and padding rows are
+// skipped).  The expert and the tokens are resolved once per tile; then every
+// thread copies 16-byte pieces, many in flight.
 __global__ void __launch_bounds__(256) k_pf_gather_x(const uint8_t* __restrict__ xc, int H, int k, int E,
                                                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
                                                      const float* __restrict__ w, const int32_t* __restrict__ tile_off,
-                                                     int max_rows, uint8_t* __restrict__ xq, int2* __restrict__ rowmeta) {
-    const int q = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (q >= max_rows || q >= 128 * __ldg(tile_off + E)) return;
-    const int e = pf_find_expert(tile_off, E, q >> 7);
-    const int local = q - 128 * __ldg(tile_off + e);
-    const int ne = __ldg(offsets + e + 1) - __ldg(offsets + e);
-    if (local >= ne) {
-        if (lane == 0) rowmeta[q] = make_int2(-1, 0);
-        return;
+                                                     uint8_t* __restrict__ xq, int2* __restrict__ rowmeta) {
+    __shared__ int s_tok[128];
+    __shared__ int s_toff[1025];
+    __shared__ int s_e;
+    const int rt = blockIdx.x, tid = threadIdx.x;
+    if (rt >= __ldg(tile_off + E)) return;
+    for (int i = tid; i <= E; i += blockDim.x) s_toff[i] = __ldg(tile_off + i);
+    __syncthreads();
+    if (tid == 0) {  // last expert with s_toff[e] <= rt
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_toff[mid] <= rt) lo = mid;
+            else hi = mid - 1;
+        }
+        s_e = lo;
     }
-    const int f = __ldg(perm + __ldg(offsets + e) + local);
-    const int t = f / k;
-    if (lane == 0) rowmeta[q] = make_int2(t, __float_as_int(__ldg(w + f)));
-    const uint8_t* row = xc + (int64_t)t * (H / 2 + H / 16);
-    const int KSN = H / 128, rt = q >> 7, r = q & 127;
-    // codes: 16-byte pieces (4 per 128-K block), then scale words (2 per block)
-    for (int i = lane; i < H / 32; i += 32) {
-        const int ks = i >> 2, piece = i & 3;
-        const uint4 v = *reinterpret_cast<const uint4*>(row + i * 16);
-        *reinterpret_cast<uint4*>(xq + ((int64_t)rt * KSN + ks) * pf::BLK + blk_code_off(r, piece * 16)) = v;
+    __syncthreads();
+    const int e = s_e;
+    if (tid < 128) {
+        const int local = (rt - s_toff[e]) * 128 + tid;
+        const int ne = __ldg(offsets + e + 1) - __ldg(offsets + e);
+        int t = -1;
+        float wt = 0.0f;
+        if (local < ne) {
+            const int f = __ldg(perm + __ldg(offsets + e) + local);
+            t = f / k;
+            wt = __ldg(w + f);
+        }
+        s_tok[tid] = t;
+        rowmeta[(int64_t)rt * 128 + tid] = make_int2(t, __float_as_int(wt));
     }
-    for (int i = lane; i < H / 64; i += 32) {
-        const int ks = i >> 1, half = i & 1;
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(row + H / 2 + i * 4);
-        *reinterpret_cast<uint32_t*>(xq + ((int64_t)rt * KSN + ks) * pf::BLK + blk_scale_off(r, half * 4)) = v;
+    __syncthreads();
+    const int KSN = H / 128, pieces = H / 32, words = H / 64;  // per row: 16-byte code pieces, 4-byte scale words
+    const int64_t rowb = H / 2 + H / 16;
+    uint8_t* tile = xq + (int64_t)rt * KSN * pf::BLK;
+    // codes: lanes 8a .. 8a+7 take eight consecutive rows of one 16-byte piece, i.e. one whole
+    // 128-byte line of the tile (index bits: row & 7, piece, row >> 3)
+#pragma unroll 4
+    for (int i = tid; i < 128 * pieces; i += blockDim.x) {
+        const int rest = i >> 3, pc = rest % pieces;
+        const int r = (rest / pieces) * 8 + (i & 7);
+        const int t = s_tok[r];
+        if (t < 0) continue;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xc + (int64_t)t * rowb) + pc);
+        *reinterpret_cast<uint4*>(tile + (pc >> 2) * pf::BLK + blk_code_off(r, (pc & 3) * 16)) = v;
+    }
+    // scale words: a warp covers rows (r & 7) + 32 (r >> 5), one 128-byte line (index bits:
+    // row & 7, row >> 5, word, (row >> 3) & 3)
+#pragma unroll 4
+    for (int i = tid; i < 128 * words; i += blockDim.x) {
+        const int rest = i >> 5, wd = rest % words;
+        const int r = (i & 7) + 32 * ((i >> 3) & 3) + 8 * (rest / words);
+        const int t = s_tok[r];
+        if (t < 0) continue;
+        const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(xc + (int64_t)t * rowb + H / 2) + wd);
+        *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK + blk_scale_off(r, (wd & 1) * 4)) = v;
     }
 }
 
-__global__ void __launch_bounds__(256) k_pf_out(const float* __restrict__ out32, int64_t n, uint16_t* __restrict__ out) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        out[i] = bf16_bits(out32[i]);
+__global__ void __launch_bounds__(256) k_pf_out(const float4* __restrict__ out32, int64_t n4, uint2* __restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = out32[i];
+        out[i] = make_uint2((uint32_t)bf16_bits(v.x) | ((uint32_t)bf16_bits(v.y) << 16),
+                            (uint32_t)bf16_bits(v.z) | ((uint32_t)bf16_bits(v.w) << 16));
+    }
 }
 
 // ---------------------------------------------------------------------------- epilogues
 
-// SwiGLU + h quantisation.  Thread of TMEM lane r (gate row r even, up row r odd
-// of the tile's 64 pairs) holds 32 token columns.  Pair p = r/2 is feature
-// m*64 + p of h; the 16 features of one quantisation block are the 32 lanes of
-// one warp.  The two lanes of a pair split the tokens: the even lane takes the
-// even tokens and the odd lane the odd ones, after one exchange, so every lane
-// computes distinct h values.
+// The MMA puts the token tile on the M side, so TMEM lane r of the accumulator is
+// token row r of the tile and its columns are the 128 weight rows of the m tile:
+// a thread that loads 32 columns holds 32 consecutive weight rows of one token.
+
+// SwiGLU + h quantisation.  Weight rows come as (gate, up) pairs, so the 32
+// columns c0 .. c0+31 of a thread are the 16 h features m*64 + c0/2 .. +15 of its
+// token: exactly one NVFP4 block, quantised without leaving the thread
+// (fp32, IEEE division, as the quantiser defines it).
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-__device__ __forceinline__ void epi_swiglu(const PfGemmArgs& a, const uint32_t (&v)[32], int m, int ntg, int c0, int qd,
-                                           int lane, float tsg, float tsu) {
-    const int f0 = m * 64 + 16 * qd;  // first feature of this warp's block
-    const int ks2 = f0 / 128, b0 = (f0 & 127) / 2, jblk = (f0 & 127) / 16;
-    uint8_t* blk_base = a.hq + (int64_t)ntg * a.KSN2 * pf::BLK + (int64_t)ks2 * pf::BLK;
-    const int par = lane & 1;  // 0: gate lane, computes even tokens; 1: up lane, odd tokens
-    // phase 1: h of token 2q+par for this lane's feature (the even lane sends g of token 2q+1,
-    // the odd lane sends u of token 2q)
+__device__ __forceinline__ void epi_swiglu(const PfGemmArgs& a, const uint32_t (&v)[32], int m, int ntg, int r, int c0,
+                                           float tsg, float tsu) {
     float hb[16];
+    float amax = 0.0f;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const float ve = __uint_as_float(v[2 * q]), vo = __uint_as_float(v[2 * q + 1]);
-        const float recv = __shfl_xor_sync(0xffffffffu, par ? ve : vo, 1);
-        const float g = (par ? recv : ve) * tsg, u = (par ? vo : recv) * tsu;
-        hb[q] = bf16_to_f32(bf16_bits(silu_fast(g) * u));
+    for (int i = 0; i < 16; ++i) {
+        const float g = __uint_as_float(v[2 * i]) * tsg, u = __uint_as_float(v[2 * i + 1]) * tsu;
+        hb[i] = bf16_to_f32(bf16_bits(silu_fast(g) * u));
+        amax = fmaxf(amax, fabsf(hb[i]));
     }
-    // phase 2: block amax over the 16 lanes of the same parity
-    float am[16];
+    const uint32_t sb = f32_to_e4m3_rn_sat(__fdiv_rn(amax, 6.0f));
+    const float eff = e4m3_to_f32(sb);
+    uint32_t w[2] = {0u, 0u};
+    if (eff != 0.0f) {
 #pragma unroll
-    for (int q = 0; q < 16; ++q) am[q] = fabsf(hb[q]);
-#pragma unroll
-    for (int o = 2; o < 32; o <<= 1)
-#pragma unroll
-        for (int q = 0; q < 16; ++q) am[q] = fmaxf(am[q], __shfl_xor_sync(0xffffffffu, am[q], o));
-    // phase 3: scale and code (fp32, IEEE division, as the quantiser defines them)
-    uint32_t sbv[16], word[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        sbv[q] = f32_to_e4m3_rn_sat(__fdiv_rn(am[q], 6.0f));
-        const float eff = e4m3_to_f32(sbv[q]);
-        word[q] = (eff == 0.0f) ? 0u : (f32x2_to_e2m1x2_rn_sat(__fdiv_rn(hb[q], eff), 0.0f) & 0xFu);
+        for (int i = 0; i < 8; ++i)
+            w[i >> 2] |= f32x2_to_e2m1x2_rn_sat(__fdiv_rn(hb[2 * i], eff), __fdiv_rn(hb[2 * i + 1], eff)) << (8 * (i & 3));
     }
-    // phase 4: bytes of features (2u, 2u+1) in lane 4u+par, then 8 bytes per token in lanes 0/1 and 16/17
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const uint32_t hi = __shfl_down_sync(0xffffffffu, word[q], 2);
-        word[q] = ((lane & 2) == 0) ? ((word[q] | (hi << 4)) << (8 * ((lane >> 2) & 3))) : 0u;
-    }
-#pragma unroll
-    for (int q = 0; q < 16; ++q) word[q] |= __shfl_xor_sync(0xffffffffu, word[q], 4);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) word[q] |= __shfl_xor_sync(0xffffffffu, word[q], 8);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const uint32_t w1 = __shfl_sync(0xffffffffu, word[q], 16 + par);
-        if (lane < 2) {
-            const int r = c0 + 2 * q + par;  // token row within the tile
-            *reinterpret_cast<uint2*>(blk_base + blk_code_off(r, b0)) = make_uint2(word[q], w1);
-            blk_base[blk_scale_off(r, jblk)] = (uint8_t)sbv[q];
-        }
-    }
+    const int f0 = m * 64 + c0 / 2;  // first feature: block f0 / 128 of the h row, bytes (f0 % 128) / 2 ..
+    uint8_t* blk = a.hq + ((int64_t)ntg * a.KSN2 + f0 / 128) * pf::BLK;
+    *reinterpret_cast<uint2*>(blk + blk_code_off(r, (f0 & 127) / 2)) = make_uint2(w[0], w[1]);
+    blk[blk_scale_off(r, (f0 & 127) / 16)] = (uint8_t)sb;
 }
 
-// Down projection + combine: out32[t][m*128 + r] += w * tsd * y for each real token
-// column (row table entry: token, routing weight; token -1 for padding).
-__device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t (&v)[32], int2 meta, int m, int qd,
-                                            int lane, float tsd) {
-    const int tj = meta.x;
-    const float wj = __int_as_float(meta.y) * tsd;
-    float* dst = a.out32 + m * 128 + 32 * qd + lane;
+// Down projection + combine: out32[t][m*128 + c0 .. +31] += w * tsd * y for the
+// thread's token row (row table entry: token, routing weight; token -1 for
+// padding), as eight 16-byte vector reductions.
+__device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t (&v)[32], int2 meta, int m, int c0,
+                                            float tsd) {
+    if (meta.x < 0) return;
+    const float wt = __int_as_float(meta.y) * tsd;
+    float* dst = a.out32 + (int64_t)meta.x * a.H + m * 128 + c0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int t = __shfl_sync(0xffffffffu, tj, j);
-        const float wt = __shfl_sync(0xffffffffu, wj, j);
-        if (t >= 0) atomicAdd(dst + (int64_t)t * a.H, __uint_as_float(v[j]) * wt);
-    }
+    for (int i = 0; i < 8; ++i)
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * i),
+                     "f"(__uint_as_float(v[4 * i]) * wt), "f"(__uint_as_float(v[4 * i + 1]) * wt),
+                     "f"(__uint_as_float(v[4 * i + 2]) * wt), "f"(__uint_as_float(v[4 * i + 3]) * wt)
+                     : "memory");
 }
 
 // ---------------------------------------------------------------------------- grouped GEMM
 
 template <int EPI>
-__global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) {
+__global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmArgs a) {
     extern __shared__ __align__(1024) uint8_t pf_smem[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_smem) + 1023) & ~(uintptr_t)1023);
     __shared__ __align__(8) unsigned long long full[pf::NS], empty[pf::NS], acc_full[2], acc_empty[2];
@@ -402,19 +422,21 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) 
                 item(i, e, m, ntg);
                 const uint8_t* ab = a.A + (int64_t)e * a.a_stride + (int64_t)m * a.KSN * pf::BLK;
                 const uint8_t* bb = a.B + (int64_t)ntg * a.KSN * pf::BLK;
-                for (int ks = 0; ks < a.KSN; ++ks, ++sc) {
+                // a tile's K blocks are contiguous: KPS of them (A, then B) per stage
+                for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
                     const int s = sc % pf::NS, use = sc / pf::NS;
                     if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag)) break;
                     uint8_t* dst = ring + (size_t)s * pf::STAGE;
+                    const uint32_t bytes = (uint32_t)(min(pf::KPS, a.KSN - ks) * pf::BLK);
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&full[s])),
-                                 "r"((uint32_t)pf::STAGE) : "memory");
+                                 "r"(2 * bytes) : "memory");
                     asm volatile(
                         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                            pf_su(dst)), "l"(ab + (int64_t)ks * pf::BLK), "r"((uint32_t)pf::BLK), "r"(pf_su(&full[s]))
+                            pf_su(dst)), "l"(ab + (int64_t)ks * pf::BLK), "r"(bytes), "r"(pf_su(&full[s]))
                         : "memory");
                     asm volatile(
                         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                            pf_su(dst + pf::BLK)), "l"(bb + (int64_t)ks * pf::BLK), "r"((uint32_t)pf::BLK), "r"(pf_su(&full[s]))
+                            pf_su(dst + pf::KPS * pf::BLK)), "l"(bb + (int64_t)ks * pf::BLK), "r"(bytes), "r"(pf_su(&full[s]))
                         : "memory");
                 }
             }
@@ -433,25 +455,29 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) 
                 if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t dcol = tbase + (uint32_t)(buf * 128);
-                for (int ks = 0; ks < a.KSN; ++ks, ++sc) {
+                for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
                     const int s = sc % pf::NS;
                     if (!pf_wait(&full[s], (sc / pf::NS) & 1, abort_flag)) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint8_t* sa = ring + (size_t)s * pf::STAGE;
-                    const uint8_t* sbp = sa + pf::BLK;
+                    const int nkb = min(pf::KPS, a.KSN - ks);
+                    for (int bi = 0; bi < nkb; ++bi) {
+                        const uint8_t* sa = ring + (size_t)s * pf::STAGE + bi * pf::BLK;
+                        const uint8_t* sbp = sa + pf::KPS * pf::BLK;
 #pragma unroll
-                    for (int kb = 0; kb < 2; ++kb) {
-                        const uint32_t tsfa = tbase + pf::SF_COL0 + (uint32_t)(s * 16 + kb * 8), tsfb = tsfa + 4;
-                        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsfa),
-                                     "l"(umma_desc(sa + 8192 + kb * 512, 0, 128)));
-                        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsfb),
-                                     "l"(umma_desc(sbp + 8192 + kb * 512, 0, 128)));
-                        const uint64_t da = umma_desc(sa + kb * 4096, 2048, 128), db = umma_desc(sbp + kb * 4096, 2048, 128);
-                        const uint32_t acc = (ks | kb) ? 1u : 0u;
-                        asm volatile(
-                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                                dcol), "l"(da), "l"(db), "r"(kIdesc), "r"(tsfa), "r"(tsfb), "r"(acc));
+                        for (int kb = 0; kb < 2; ++kb) {
+                            // M side: the token tile (ring B half); N side: the weight tile (A half)
+                            const uint32_t tsfa = tbase + pf::SF_COL0 + (uint32_t)((s * pf::KPS + bi) * 16 + kb * 8), tsfb = tsfa + 4;
+                            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsfa),
+                                         "l"(umma_desc(sbp + 8192 + kb * 512, 0, 128)));
+                            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsfb),
+                                         "l"(umma_desc(sa + 8192 + kb * 512, 0, 128)));
+                            const uint64_t da = umma_desc(sbp + kb * 4096, 2048, 128), db = umma_desc(sa + kb * 4096, 2048, 128);
+                            const uint32_t acc = (ks | bi | kb) ? 1u : 0u;
+                            asm volatile(
+                                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                                    dcol), "l"(da), "l"(db), "r"(kIdesc), "r"(tsfa), "r"(tsfb), "r"(acc));
+                        }
                     }
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                      pf_su(&empty[s])) : "memory");
@@ -461,8 +487,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) 
             }
         }
     } else {
-        // ---------------- epilogue warps 2..17: TMEM lane quadrant qd = warp % 4, 32 columns each
+        // ---------------- epilogue warps 2..17: TMEM lane quadrant qd = warp % 4 (token rows
+        // 32 qd .. +31), 32 columns (weight rows c0 .. +31) each
         const int qd = warp & 3, c0 = 32 * ((warp - 2) >> 2);
+        const int r = 32 * qd + lane;
         int it = 0;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
             const int buf = it & 1;
@@ -472,14 +500,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) 
             const float* ts = a.tscale + (int64_t)e * a.ts_stride;
             const float t0s = __ldg(ts + 0), t1s = __ldg(ts + 1), t2s = __ldg(ts + 2);
             int2 meta = make_int2(-1, 0);
-            if (EPI == 2) meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + c0 + lane);
+            if (EPI == 2) meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
             if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             {
                 uint32_t v[32];
                 tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
-                if (EPI == 1) epi_swiglu(a, v, m, ntg, c0, qd, lane, t0s, t1s);
-                else epi_combine(a, v, meta, m, qd, lane, t2s);
+                if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
+                else epi_combine(a, v, meta, m, c0, t2s);
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
@@ -495,6 +523,232 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm(const PfGemmArgs a) 
         if (it > 0)
             while (!pf_try_wait(&acc_full[(it - 1) & 1], ((it - 1) >> 1) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
             }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(pf::TMEM_COLS));
+    }
+}
+
+// Resident-token-tile variant (K <= 2048): a work item is (token tile, half of
+// the weight row tiles).  The token tile's K blocks are copied once into shared
+// memory and stay there (scale factors copied once into TMEM) while the item's
+// weight tiles stream through the ring, KPS blocks per stage: half as many bulk
+// copies per token tile as streaming both operands.
+__device__ __forceinline__ bool pf_res_item(const PfGemmArgs& a, int i, int& e, int& ntg, int& mlo, int& mhi) {
+    ntg = i >> 1;
+    const int mh = (a.MT + 1) >> 1;
+    mlo = (i & 1) ? mh : 0;
+    mhi = (i & 1) ? a.MT : mh;
+    if (mlo >= mhi) return false;
+    e = pf_find_expert(a.tile_off, a.E, ntg);
+    return true;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs a) {
+    extern __shared__ __align__(1024) uint8_t pf_smem[];
+    uint8_t* btile = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_smem) + 1023) & ~(uintptr_t)1023);
+    uint8_t* ring = btile + (size_t)a.KSN * pf::BLK;
+    __shared__ __align__(8) unsigned long long full[pf::RES_MAXNS], empty[pf::RES_MAXNS], acc_full[2], acc_empty[2], bfull,
+        bfree;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_s;
+    volatile int* abort_flag = &abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NSr = a.nstages;
+    // TMEM columns: accumulators [0, 256), token-tile scale factors (8 per K block), then the
+    // weight scale factors of the ring stages (8 per K block of a stage)
+    const uint32_t SFT0 = 256, SFW0 = 256 + 8 * (uint32_t)a.KSN;
+    if (tid == 0) {
+        for (int s = 0; s < NSr; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&full[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&empty[s])));
+        }
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&acc_full[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(pf_su(&acc_empty[b])), "n"(pf::EPI_WARPS));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfull)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfree)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_s = 0;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(pf_su(&tmem_base)),
+                     "n"(pf::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tbase = tmem_base;
+    const int n_items = 2 * __ldg(a.tile_off + a.E);
+    const uint32_t tile_bytes = (uint32_t)a.KSN * pf::BLK;
+    int bfree_commits = 0;  // MMA thread: token-tile releases committed
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            int sc = 0, bi = 0;
+            for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
+                int e, ntg, mlo, mhi;
+                if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
+                // the token tile, once the previous item's MMAs have read the last one
+                if (bi > 0 && !pf_wait(&bfree, (bi - 1) & 1, abort_flag)) break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&bfull)), "r"(tile_bytes)
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        pf_su(btile)), "l"(a.B + (int64_t)ntg * a.KSN * pf::BLK), "r"(tile_bytes), "r"(pf_su(&bfull))
+                    : "memory");
+                ++bi;
+                const uint8_t* ae = a.A + (int64_t)e * a.a_stride;
+                bool stop = false;
+                for (int m = mlo; m < mhi && !stop; ++m) {
+                    // warm L2 with the item's next weight tile, or with the next item's token tile,
+                    // while this one streams through the two or so stages shared memory leaves
+                    if (m + 1 < mhi) {
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ae + (int64_t)(m + 1) * a.KSN * pf::BLK),
+                                     "r"(tile_bytes) : "memory");
+                    } else if (i + (int)gridDim.x < n_items) {
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                         a.B + (int64_t)((i + (int)gridDim.x) >> 1) * a.KSN * pf::BLK),
+                                     "r"(tile_bytes) : "memory");
+                    }
+                    for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
+                        const int s = sc % NSr, use = sc / NSr;
+                        if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag)) {
+                            stop = true;
+                            break;
+                        }
+                        const uint32_t bytes = (uint32_t)(min(pf::KPS, a.KSN - ks) * pf::BLK);
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&full[s])),
+                                     "r"(bytes) : "memory");
+                        asm volatile(
+                            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                pf_su(ring + (size_t)s * pf::KPS * pf::BLK)),
+                            "l"(ae + ((int64_t)m * a.KSN + ks) * pf::BLK), "r"(bytes), "r"(pf_su(&full[s]))
+                            : "memory");
+                    }
+                }
+                if (stop) break;
+            }
+            // do not leave copies landing after exit: wait (bounded) for the last ring stages and
+            // the last token tile issued
+            const unsigned long long t0 = pf_gt();
+            for (int n = max(0, sc - NSr); n < sc; ++n)
+                while (!pf_try_wait(&full[n % NSr], (n / NSr) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
+                }
+            if (bi > 0)
+                while (!pf_try_wait(&bfull, (bi - 1) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: the token tile is the M side, the weight tile the N side
+        if (lane == 0) {
+            int sc = 0, it = 0, bi = 0;
+            bool stop = false;
+            for (int i = blockIdx.x; i < n_items && !stop && !*abort_flag; i += gridDim.x) {
+                int e, ntg, mlo, mhi;
+                if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
+                if (!pf_wait(&bfull, bi & 1, abort_flag)) break;
+                ++bi;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int ks = 0; ks < a.KSN; ++ks)
+#pragma unroll
+                    for (int kb = 0; kb < 2; ++kb)
+                        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(
+                                         tbase + SFT0 + (uint32_t)(ks * 8 + kb * 4)),
+                                     "l"(umma_desc(btile + (size_t)ks * pf::BLK + 8192 + kb * 512, 0, 128)));
+                for (int m = mlo; m < mhi && !stop; ++m, ++it) {
+                    const int buf = it & 1, useb = it >> 1;
+                    if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t dcol = tbase + (uint32_t)(buf * 128);
+                    for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
+                        const int s = sc % NSr;
+                        if (!pf_wait(&full[s], (sc / NSr) & 1, abort_flag)) {
+                            stop = true;
+                            break;
+                        }
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        const int nkb = min(pf::KPS, a.KSN - ks);
+                        for (int bq = 0; bq < nkb; ++bq) {
+                            const uint8_t* wb = ring + ((size_t)s * pf::KPS + bq) * pf::BLK;
+                            const uint8_t* tb = btile + (size_t)(ks + bq) * pf::BLK;
+#pragma unroll
+                            for (int kb = 0; kb < 2; ++kb) {
+                                const uint32_t sfw = tbase + SFW0 + (uint32_t)((s * pf::KPS + bq) * 8 + kb * 4);
+                                const uint32_t sft = tbase + SFT0 + (uint32_t)((ks + bq) * 8 + kb * 4);
+                                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfw),
+                                             "l"(umma_desc(wb + 8192 + kb * 512, 0, 128)));
+                                const uint64_t da = umma_desc(tb + kb * 4096, 2048, 128), db = umma_desc(wb + kb * 4096, 2048, 128);
+                                const uint32_t acc = (ks | bq | kb) ? 1u : 0u;
+                                asm volatile(
+                                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                                    "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                                        dcol), "l"(da), "l"(db), "r"(kIdesc), "r"(sft), "r"(sfw), "r"(acc));
+                            }
+                        }
+                        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                         pf_su(&empty[s])) : "memory");
+                    }
+                    if (stop) break;
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     pf_su(&acc_full[buf])) : "memory");
+                }
+                // the token tile may be replaced once this item's MMAs are done
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 pf_su(&bfree)) : "memory");
+                ++bfree_commits;
+            }
+        }
+    } else {
+        // ---------------- epilogue warps 2..17: TMEM lane quadrant qd = warp % 4 (token rows
+        // 32 qd .. +31), 32 columns (weight rows c0 .. +31) each
+        const int qd = warp & 3, c0 = 32 * ((warp - 2) >> 2);
+        const int r = 32 * qd + lane;
+        int it = 0;
+        bool stop = false;
+        for (int i = blockIdx.x; i < n_items && !stop; i += gridDim.x) {
+            int e, ntg, mlo, mhi;
+            if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
+            const float* ts = a.tscale + (int64_t)e * a.ts_stride;
+            const float t0s = __ldg(ts + 0), t1s = __ldg(ts + 1), t2s = __ldg(ts + 2);
+            int2 meta = make_int2(-1, 0);
+            if (EPI == 2) meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
+            for (int m = mlo; m < mhi; ++m, ++it) {
+                const int buf = it & 1;
+                if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
+                    if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
+                    else epi_combine(a, v, meta, m, c0, t2s);
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pf_su(&acc_empty[buf])) : "memory");
+            }
+        }
+    }
+    // all MMAs have completed once the epilogue has consumed every accumulator; on an abort
+    // wait (bounded) for the last commit before the TMEM is released
+    if (warp == 1 && lane == 0 && *abort_flag && bfree_commits > 0) {
+        // the last commit covers every MMA issued before it
+        const unsigned long long t0 = pf_gt();
+        while (!pf_try_wait(&bfree, (bfree_commits - 1) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
+        }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -573,6 +827,25 @@ static PfWs pf_ws_layout(int T, int k, int E, int H, int I) {
 
 ft_status validate_weights(const ft_moe_layer_weights* W, const char* fn);
 
+// Resident token tile when it fits with a ring of at least two stages (shared memory) and the
+// scale factors fit TMEM; otherwise both operands stream through the ring.
+template <int EPI>
+static void launch_pf_gemm(PfGemmArgs g, int G, cudaStream_t s) {
+    const size_t tile = (size_t)g.KSN * pf::BLK, stage = (size_t)pf::KPS * pf::BLK;
+    int ns = 0;
+    if (g.KSN <= pf::RES_MAXKSN && tile + 1024 < pf::SMEM_LIMIT) {
+        const int by_smem = (int)((pf::SMEM_LIMIT - 1024 - tile) / stage);
+        const int by_tmem = (int)((pf::TMEM_COLS - 256 - 8 * (uint32_t)g.KSN) / (8 * pf::KPS));
+        ns = std::min({by_smem, by_tmem, pf::RES_MAXNS});
+    }
+    if (ns >= 2) {
+        g.nstages = ns;
+        k_pf_gemm_res<EPI><<<G, pf::THREADS, tile + (size_t)ns * stage + 1024, s>>>(g);
+    } else {
+        k_pf_gemm_stream<EPI><<<G, pf::THREADS, pf::SMEM, s>>>(g);
+    }
+}
+
 }  // namespace ft
 
 using namespace ft;
@@ -613,6 +886,7 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     if (T == 0) return FT_OK;
     if (!x || !offsets || !perm || !w || !out) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
     if (!aligned(x, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": x needs 16-byte alignment");
+    if (!aligned(out, 8)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": out needs 8-byte alignment");
     const int E = W->E, H = W->H, I = W->I;
     const PfWs L = pf_ws_layout(T, k, E, H, I);
     if (!ws || ws_bytes < L.total || !aligned(ws, 256))
@@ -627,16 +901,16 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     cudaStream_t s = cu(stream);
     static std::once_flag once;
     std::call_once(once, [] {
-        cudaFuncSetAttribute(k_pf_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM);
-        cudaFuncSetAttribute(k_pf_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM);
+        cudaFuncSetAttribute(k_pf_gemm_stream<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM);
+        cudaFuncSetAttribute(k_pf_gemm_stream<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM);
+        cudaFuncSetAttribute(k_pf_gemm_res<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM_LIMIT);
+        cudaFuncSetAttribute(k_pf_gemm_res<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM_LIMIT);
     });
     cudaError_t e = cudaMemsetAsync(out32, 0, (size_t)T * H * 4, s);
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
     k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, tile_off);
-    const int max_rows = 128 * L.max_tiles;
     k_pf_quant_tokens<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(x, T, H, xc);
-    k_pf_gather_x<<<(unsigned)((max_rows + 7) / 8), 256, 0, s>>>(xc, H, k, E, offsets, perm, w, tile_off, max_rows, xq,
-                                                                   rowmeta);
+    k_pf_gather_x<<<(unsigned)L.max_tiles, 256, 0, s>>>(xc, H, k, E, offsets, perm, w, tile_off, xq, rowmeta);
     PfGemmArgs g{};
     g.tscale = W->tscale;
     g.ts_stride = W->tscale_stride;
@@ -655,16 +929,17 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     g.B = xq;
     g.MT = 2 * I / 128;
     g.KSN = H / 128;
-    k_pf_gemm<1><<<G, pf::THREADS, pf::SMEM, s>>>(g);
+    launch_pf_gemm<1>(g, G, s);
     // down + combine
     g.A = W->d_codes;
     g.a_stride = W->d_codes_stride;
     g.B = hq;
     g.MT = H / 128;
     g.KSN = I / 128;
-    k_pf_gemm<2><<<G, pf::THREADS, pf::SMEM, s>>>(g);
-    const int64_t n = (int64_t)T * H;
-    k_pf_out<<<(unsigned)std::min<int64_t>((n + 255) / 256, 148 * 32), 256, 0, s>>>(out32, n, out);
+    launch_pf_gemm<2>(g, G, s);
+    const int64_t n4 = (int64_t)T * H / 4;  // H is a multiple of 128
+    k_pf_out<<<(unsigned)std::min<int64_t>((n4 + 255) / 256, 148 * 16), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(out32), n4, reinterpret_cast<uint2*>(out));
     return check_launch(fn);
 }
 

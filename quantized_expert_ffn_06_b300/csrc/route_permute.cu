@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 namespace ft {
 
@@ -76,6 +77,34 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
     const float m = __shfl_sync(0xffffffffu, my_val, 0);
     float wj;
     if (m == -INFINITY) {
+        wj = 1.0f / (float)k;
+    } else {
+        const float ej = (lane < k) ? expf(my_val - m) : 0.0f;
+        const float s = warp_sum(ej);
+        wj = ej / s;
+    }
+    if (lane < k) {
+        ids[(int64_t)t * k + lane] = my_id;
+        w[(int64_t)t * k + lane] = wj;
+    }
+}
+
+// E <= 256: the selection of select_topk8 (each lane's eight keys sorted once,
+// then k rounds of one warp reduction over the lanes' heads); same experts, same
+// order and the same weights as k_route.
+__global__ void __launch_bounds__(256) k_route_sorted(const float* __restrict__ logits, int T, int E, int k,
+                                                      int32_t* __restrict__ ids, float* __restrict__ w) {
+    const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float* row = logits + (int64_t)t * E;
+    bool bad = false;
+    const int my_id = select_topk8(row, E, k, bad);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
+    const float my_val = (lane < k) ? __ldg(row + my_id) : -INFINITY;
+    const float m = __shfl_sync(0xffffffffu, my_val, 0);
+    float wj;
+    if (m == -INFINITY || m != m) {
         wj = 1.0f / (float)k;
     } else {
         const float ej = (lane < k) ? expf(my_val - m) : 0.0f;
@@ -202,10 +231,16 @@ __global__ void __launch_bounds__(1024) k_permute_scan(int32_t* __restrict__ chu
     int has = 0;
     if (tid < E) {
         int run = 0;
-        for (int c = 0; c < nchunks; ++c) {  // exclusive scan over chunks for this expert
-            const int v = chunk_cnt[(int64_t)c * E + tid];
-            chunk_cnt[(int64_t)c * E + tid] = run;
-            run += v;
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {  // exclusive scan over chunks for this expert
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = (c0 + u < nchunks) ? chunk_cnt[(int64_t)(c0 + u) * E + tid] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + u < nchunks) {
+                    chunk_cnt[(int64_t)(c0 + u) * E + tid] = run;
+                    run += v[u];
+                }
         }
         tot[tid] = run;
         has = run > 0;
@@ -215,7 +250,14 @@ __global__ void __launch_bounds__(1024) k_permute_scan(int32_t* __restrict__ chu
     block_exclusive_scan(tot, E, warp_tot);
     if (tid < E) {
         offsets[tid] = tot[tid];
-        for (int c = 0; c < nchunks; ++c) chunk_cnt[(int64_t)c * E + tid] += tot[tid];
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = (c0 + u < nchunks) ? chunk_cnt[(int64_t)(c0 + u) * E + tid] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + u < nchunks) chunk_cnt[(int64_t)(c0 + u) * E + tid] = v[u] + tot[tid];
+        }
     }
     if (tid == 0) offsets[E] = n;
     if (active) {
@@ -225,21 +267,38 @@ __global__ void __launch_bounds__(1024) k_permute_scan(int32_t* __restrict__ chu
     }
 }
 
+// Rank of a slot within its chunk: lanes of a warp holding the same expert are
+// ranked by __match_any_sync, and each warp's count per expert (leader lane) is
+// scanned over the chunk's 32 warps in shared memory ([32][E] ints, dynamic).
 __global__ void __launch_bounds__(1024) k_permute_place(const int32_t* __restrict__ ids, int n, int E,
                                                         const int32_t* __restrict__ chunk_base,
                                                         int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-    __shared__ int sid[kPermChunk];
-    const int tid = threadIdx.x;
+    extern __shared__ int wcnt[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
     const int64_t f = (int64_t)blockIdx.x * kPermChunk + tid;
     int e = -1;
     if (f < n) {
         e = ids[f];
         if (e < 0 || e >= E) e = -1;
     }
-    sid[tid] = e;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int lrank = __popc(peers & ((1u << lane) - 1u));
+    __syncthreads();
+    if (e >= 0 && lrank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int x = tid; x < E; x += blockDim.x) {  // exclusive scan over the warps
+        int run = 0;
+#pragma unroll 8
+        for (int w = 0; w < 32; ++w) {
+            const int v = wcnt[w * E + x];
+            wcnt[w * E + x] = run;
+            run += v;
+        }
+    }
     __syncthreads();
     if (e >= 0) {
-        const int p = chunk_base[(int64_t)blockIdx.x * E + e] + chunk_rank(sid, tid, e);
+        const int p = chunk_base[(int64_t)blockIdx.x * E + e] + wcnt[warp * E + e] + lrank;
         perm[p] = (int32_t)f;
         inv[f] = p;
     }
@@ -290,7 +349,7 @@ ft_status ft_moe_route(const float* logits, int T, int E, int k, int32_t* ids, f
     if (epl <= 1) k_route<1><<<grid, threads, 0, s>>>(logits, T, E, k, ids, w);
     else if (epl <= 2) k_route<2><<<grid, threads, 0, s>>>(logits, T, E, k, ids, w);
     else if (epl <= 4) k_route<4><<<grid, threads, 0, s>>>(logits, T, E, k, ids, w);
-    else if (epl <= 8) k_route<8><<<grid, threads, 0, s>>>(logits, T, E, k, ids, w);
+    else if (epl <= 8) k_route_sorted<<<grid, threads, 0, s>>>(logits, T, E, k, ids, w);
     else if (epl <= 16) k_route<16><<<grid, threads, 0, s>>>(logits, T, E, k, ids, w);
     else k_route<32><<<grid, threads, 0, s>>>(logits, T, E, k, ids, w);
     return check_launch("ft_moe_route");
@@ -325,7 +384,11 @@ ft_status ft_moe_permute(const int32_t* ids, int T, int E, int k, int32_t* offse
     int32_t* chunk_cnt = static_cast<int32_t*>(ws);
     k_permute_hist<<<nchunks, 1024, 0, s>>>(ids, n, E, chunk_cnt);
     k_permute_scan<<<1, 1024, 0, s>>>(chunk_cnt, nchunks, n, E, offsets, active);
-    k_permute_place<<<nchunks, 1024, 0, s>>>(ids, n, E, chunk_cnt, perm, inv);
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(k_permute_place, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4);
+    });
+    k_permute_place<<<nchunks, 1024, (size_t)32 * E * 4, s>>>(ids, n, E, chunk_cnt, perm, inv);
     return check_launch("ft_moe_permute");
 }
 

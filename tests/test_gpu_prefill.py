@@ -121,3 +121,13 @@ def test_umma_packing_places_every_byte_where_the_layout_says():
             ks, jj = divmod(j, 8)
             base = (rt * KSN + ks) * 9216
             assert blob[base + 8192 + (jj // 4) * 512 + (r % 32) * 16 + (r // 32) * 4 + jj % 4] == scales[n, j]
+
+
+def test_hidden_beyond_resident_token_tile_streams_both_operands():
+    """H = 2304 (18 K blocks of 128) is too long for the resident token tile, so the gate/up GEMM
+    streams both operands; the down GEMM (I = 128) keeps its token tile resident."""
+    cfg = W.scaled(W.CONFIGS["tiny"], H=2304, T=40)
+    lw = weights(cfg, 0, generated=False)
+    logits, x_bits = W.router_logits(cfg, 0, 3), W.activations_bf16(cfg, 0, 3)
+    mod, out = run(cfg, lw, logits, x_bits)
+    check(cfg, 0, mod, out, logits, x_bits)
