@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             const int u0 = jg * J, nj = min(J, U - u0);
             // warps per expert tile: with one or two experts in the chunk the group's four warps
             // split each tile's K-blocks, and their partials are summed through shared memory
-            const int wpe = (nj == 1) ? 4 : (nj == 2) ? 2 : 1;
+            const int wpe = (nj == 1) ? dk::WPG : (nj == 2) ? dk::WPG / 2 : (nj <= 4 && dk::WPG >= 8) ? dk::WPG / 4 : 1;
             const int s = chunk_wait(full, misc + M_TAGS, n, P.dv_ns, abort_flag);
             const uint8_t* slot = ring + (size_t)s * P.stage_bytes;
             float* rb = gred + buf * dk::WPG * 16 * TC;

@@ -138,6 +138,21 @@ __device__ __forceinline__ uint64_t umma_desc(const void* p, uint32_t lbo, uint3
 // Instruction descriptor: kind::mxf4nvf4, E2M1 x E2M1, UE4M3 scales, M = 128, N = 128, both K-major.
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 
+// A descriptor's address field counts 16-byte units, so a descriptor moves by adding the byte
+// offset / 16 (shared-memory addresses stay below 256 KB: no carry out of the field).
+constexpr uint64_t kDescBlk = 9216 / 16, kDescHalf = 4096 / 16, kDescSfHalf = 512 / 16;
+
+__device__ __forceinline__ void sf_copy(uint32_t tcol, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tcol), "l"(desc));
+}
+
+__device__ __forceinline__ void mma_fp4(uint32_t dcol, uint64_t da, uint64_t db, uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(dcol),
+        "l"(da), "l"(db), "r"(kIdesc), "r"(sfa), "r"(sfb), "r"(acc));
+}
+
 __device__ __forceinline__ int pf_find_expert(const int32_t* tile_off, int E, int v) {
     // largest e in [0, E) with tile_off[e] <= v
     int lo = 0, hi = E - 1;
@@ -651,18 +666,18 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
         if (lane == 0) {
             int sc = 0, it = 0, bi = 0;
             bool stop = false;
+            const uint64_t dW0 = umma_desc(ring, 2048, 128), sW0 = umma_desc(ring + 8192, 0, 128);
+            const uint64_t dT0 = umma_desc(btile, 2048, 128), sT0 = umma_desc(btile + 8192, 0, 128);
             for (int i = blockIdx.x; i < n_items && !stop && !*abort_flag; i += gridDim.x) {
                 int e, ntg, mlo, mhi;
                 if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
                 if (!pf_wait(&bfull, bi & 1, abort_flag)) break;
                 ++bi;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int ks = 0; ks < a.KSN; ++ks)
-#pragma unroll
-                    for (int kb = 0; kb < 2; ++kb)
-                        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(
-                                         tbase + SFT0 + (uint32_t)(ks * 8 + kb * 4)),
-                                     "l"(umma_desc(btile + (size_t)ks * pf::BLK + 8192 + kb * 512, 0, 128)));
+                for (int ks = 0; ks < a.KSN; ++ks) {
+                    sf_copy(tbase + SFT0 + (uint32_t)(ks * 8), sT0 + (uint64_t)ks * kDescBlk);
+                    sf_copy(tbase + SFT0 + (uint32_t)(ks * 8 + 4), sT0 + (uint64_t)ks * kDescBlk + kDescSfHalf);
+                }
                 for (int m = mlo; m < mhi && !stop; ++m, ++it) {
                     const int buf = it & 1, useb = it >> 1;
                     if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag)) {
@@ -678,24 +693,27 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                             break;
                         }
                         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        // A single thread issues every MMA, so its instruction count between MMAs
+                        // sets their rate: descriptors advance by constant offsets, the loops unroll,
+                        // and the stage's scale-factor copies go first.
                         const int nkb = min(pf::KPS, a.KSN - ks);
-                        for (int bq = 0; bq < nkb; ++bq) {
-                            const uint8_t* wb = ring + ((size_t)s * pf::KPS + bq) * pf::BLK;
-                            const uint8_t* tb = btile + (size_t)(ks + bq) * pf::BLK;
+                        const uint64_t dW = dW0 + (uint64_t)(s * pf::KPS) * kDescBlk, sW = sW0 + (uint64_t)(s * pf::KPS) * kDescBlk;
+                        const uint64_t dT = dT0 + (uint64_t)ks * kDescBlk;
+                        const uint32_t cW = tbase + SFW0 + (uint32_t)(s * pf::KPS * 8), cT = tbase + SFT0 + (uint32_t)(ks * 8);
 #pragma unroll
-                            for (int kb = 0; kb < 2; ++kb) {
-                                const uint32_t sfw = tbase + SFW0 + (uint32_t)((s * pf::KPS + bq) * 8 + kb * 4);
-                                const uint32_t sft = tbase + SFT0 + (uint32_t)((ks + bq) * 8 + kb * 4);
-                                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfw),
-                                             "l"(umma_desc(wb + 8192 + kb * 512, 0, 128)));
-                                const uint64_t da = umma_desc(tb + kb * 4096, 2048, 128), db = umma_desc(wb + kb * 4096, 2048, 128);
-                                const uint32_t acc = (ks | bq | kb) ? 1u : 0u;
-                                asm volatile(
-                                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                                    "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                                        dcol), "l"(da), "l"(db), "r"(kIdesc), "r"(sft), "r"(sfw), "r"(acc));
+                        for (int bq = 0; bq < pf::KPS; ++bq)
+                            if (bq < nkb) {
+                                sf_copy(cW + bq * 8, sW + bq * kDescBlk);
+                                sf_copy(cW + bq * 8 + 4, sW + bq * kDescBlk + kDescSfHalf);
                             }
-                        }
+#pragma unroll
+                        for (int bq = 0; bq < pf::KPS; ++bq)
+                            if (bq < nkb) {
+#pragma unroll
+                                for (int kb = 0; kb < 2; ++kb)
+                                    mma_fp4(dcol, dT + bq * kDescBlk + kb * kDescHalf, dW + bq * kDescBlk + kb * kDescHalf,
+                                            cT + bq * 8 + kb * 4, cW + bq * 8 + kb * 4, (ks | bq | kb) ? 1u : 0u);
+                            }
                         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                          pf_su(&empty[s])) : "memory");
                     }
