@@ -254,9 +254,12 @@ def run_gpu(args, ws, rank, local):
     L, S, T, H, E, k = cfg.layers, min(cfg.steps, args.distinct_steps), cfg.T, cfg.H, cfg.E, cfg.k
     if args.layers:
         L = args.layers
-    # the fused launch stages x and the h rows as f16 in shared memory (120 KB); larger shapes take the
+    # the fused layer step stages x and the h rows as f16 in shared memory (120 KB per launch) and runs a
+    # larger batch as launches over token chunks that fit; a single token that does not fit takes the
     # separate calls (route, permute, row-layout expert FFN, combine)
-    fused = T <= 16 and (T * (H + 32) + T * k * (cfg.I + 32)) * 2 <= 120 * 1024
+    fused = T <= 16 and ((H + 32) + k * (cfg.I + 32)) * 2 <= 120 * 1024
+    chunk = max([c for c in range(1, T + 1) if (c * (H + 32) + c * k * (cfg.I + 32)) * 2 <= 120 * 1024] or [1])
+    n_chunks = -(-T // chunk)  # launches per layer on the fused path
     layout = Q.FT_LAYOUT_DECODE_TILES if fused else Q.FT_LAYOUT_ROWS
 
     # ---- weights (device generator + device quantiser), all experts resident
@@ -279,7 +282,7 @@ def run_gpu(args, ws, rank, local):
         layer_mods = [FusedDecodeLayer(E, H, cfg.I, k, T, dev) for _ in range(L)]
     else:
         layer_mods = [MoEDecodeLayer(E, H, cfg.I, k, T, dev) for _ in range(L)]
-    launches_per_layer = 1 if fused else 5  # route, permute, gate/up, down, combine
+    launches_per_layer = n_chunks if fused else 5  # (route, permute, gate/up, down, combine)
     stream = torch.cuda.Stream(device=dev)
 
     def step_body(xs, ls, os_):
@@ -343,8 +346,10 @@ def run_gpu(args, ws, rank, local):
               for i in range(min(args.steps, S)) for l in range(L)]
     # algorithmic bytes of one layer launch: the selected experts' NVFP4 weights (three matrices at
     # 0.5625 B/param plus three fp32 tensor scales) plus logits, activations and output
-    bytes_per_launch = float(np.mean(unique)) * (cfg.expert_bytes + 12) + T * (E * 4 + H * 2 * 2)
-    avg_launch_s = (ms / 1e3) / (args.steps * L)
+    # (with several token chunks per layer, the layer's bytes and time are shared evenly by its launches)
+    bytes_per_launch = (float(np.mean(unique)) * (cfg.expert_bytes + 12) + T * (E * 4 + H * 2 * 2)) / (
+        n_chunks if fused else 1)
+    avg_launch_s = (ms / 1e3) / (args.steps * L * (n_chunks if fused else 1))
     peak, peak_kind = load_peaks()
     achieved = bytes_per_launch / avg_launch_s / 1e9
 
@@ -400,7 +405,10 @@ def run_gpu(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind,
-                     "kernel": ("k_moe_decode (ft_moe_layer_decode), one launch per layer" if fused else
+                     "kernel": (("k_moe_decode (ft_moe_layer_decode), one launch per layer" if n_chunks == 1 else
+                                 f"k_moe_decode (ft_moe_layer_decode), {n_chunks} launches per layer (token chunks "
+                                 f"of {chunk}); the layer's unique-expert bytes and time shared by its launches")
+                                if fused else
                                 "route + permute + k_decode_gateup + k_decode_down + combine per layer, timed together"),
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_launch_s * 1e6,
                      "traffic": profiled_traffic(cfg.name, src_hash) if fused else None, "source_hash": src_hash},

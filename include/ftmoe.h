@@ -210,7 +210,7 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
  * [P4 MoE core mechanism; P3 §2.1; P5 NVFP4]
  *   logits (device) fp32 [T][E]; x (device) bf16 [T][H], 16-byte aligned.
  *   out    (device) bf16 [T][H]: out[t] = bf16(sum_j w[t][j] * y_{t,j}), the
- *          sum over a token's experts taken in ascending expert id, fp32.
+ *          sum over a token's experts taken in slot order j, fp32.
  *   ids, w (device, optional, both or neither) [T][k]: the routing result.
  *   ws: ft_moe_layer_decode_workspace_size(T, k, H, I) bytes, 256-byte
  *       aligned, ZERO-FILLED before its first use.  Its first 256 bytes hold a
@@ -218,8 +218,11 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
  *       gate/up phase hands to the down phase; calls sharing a workspace must
  *       not overlap on the device.  After a FT_DEVERR_TIMEOUT zero it again.
  * 0 <= T <= 16, 1 <= k <= min(E, 32).  The activations are staged in shared
- * memory as f16: T*(H+32) + T*k*(I+32) halves must fit 120 KB, otherwise
- * FT_ERR_UNSUPPORTED is returned (use the separate calls with FT_LAYOUT_ROWS).
+ * memory as f16: T'*(H+32) + T'*k*(I+32) halves must fit 120 KB for a launch
+ * of T' tokens.  A larger batch runs as consecutive launches over the largest
+ * token chunks that fit (tokens are independent here, so the result is the
+ * same); FT_ERR_UNSUPPORTED only if a single token does not fit (then use the
+ * separate calls with FT_LAYOUT_ROWS).
  * The launch allows programmatic dependent launch: the kernel reads no input
  * before the preceding kernel in the stream has completed. */
 FT_API size_t ft_moe_layer_decode_workspace_size(int T, int k, int H, int I);

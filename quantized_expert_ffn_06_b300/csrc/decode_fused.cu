@@ -1262,18 +1262,32 @@ ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits
     const size_t need = fused_workspace_size(T, k, W->I);
     if (!ws || ws_bytes < need || !aligned(ws, 256))
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": workspace missing, too small or not 256-byte aligned");
-    DecodeArgs a{};
-    a.W = *W;
-    a.logits = logits;
-    a.x = x;
-    a.out = out;
-    a.ids_out = ids;
-    a.w_out = w;
-    a.bar = static_cast<unsigned int*>(ws);
-    a.hbuf = static_cast<char*>(ws) + 256;
-    a.T = T;
-    a.k = k;
-    return launch_decode(a, stream, fn);
+    // Tokens are independent in this step (each one's output depends only on its own routing),
+    // so a batch whose activations do not fit the shared-memory staging runs as consecutive
+    // launches over the largest token chunks that do, in order on the stream.
+    int Tc = T;
+    {
+        DecodePlan probe;
+        std::string why;
+        while (Tc > 0 && !plan_decode(Tc, k, W->H, W->I, sm_count(), probe, why)) --Tc;
+        if (Tc == 0) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
+    }
+    for (int t0 = 0; t0 < T; t0 += Tc) {
+        DecodeArgs a{};
+        a.W = *W;
+        a.logits = logits + (int64_t)t0 * W->E;
+        a.x = x + (int64_t)t0 * W->H;
+        a.out = out + (int64_t)t0 * W->H;
+        a.ids_out = ids ? ids + (int64_t)t0 * k : nullptr;
+        a.w_out = w ? w + (int64_t)t0 * k : nullptr;
+        a.bar = static_cast<unsigned int*>(ws);
+        a.hbuf = static_cast<char*>(ws) + 256;
+        a.T = std::min(Tc, T - t0);
+        a.k = k;
+        st = launch_decode(a, stream, fn);
+        if (st != FT_OK) return st;
+    }
+    return FT_OK;
 }
 
 }  // extern "C"
