@@ -301,26 +301,33 @@ __global__ void __launch_bounds__(256) k_pf_gather_x(const uint8_t* __restrict__
     const int64_t rowb = H / 2 + H / 16;
     uint8_t* tile = xq + (int64_t)rt * KSN * pf::BLK;
     // codes: lanes 8a .. 8a+7 take eight consecutive rows of one 16-byte piece, i.e. one whole
-    // 128-byte line of the tile (index bits: row & 7, piece, row >> 3)
+    // 128-byte line of the tile; thread t: row t & 7 of each 8-row group, pieces t >> 3, +32, ...
+    // (no runtime division: this copy is instruction-heavy enough for that to matter)
+    {
+        const int r_lo = tid & 7, pc0 = tid >> 3, pstep = blockDim.x >> 3;
 #pragma unroll 4
-    for (int i = tid; i < 128 * pieces; i += blockDim.x) {
-        const int rest = i >> 3, pc = rest % pieces;
-        const int r = (rest / pieces) * 8 + (i & 7);
-        const int t = s_tok[r];
-        if (t < 0) continue;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xc + (int64_t)t * rowb) + pc);
-        *reinterpret_cast<uint4*>(tile + (pc >> 2) * pf::BLK + blk_code_off(r, (pc & 3) * 16)) = v;
+        for (int rg = 0; rg < 16; ++rg) {
+            const int r = rg * 8 + r_lo;
+            const int t = s_tok[r];
+            if (t < 0) continue;
+            const uint4* src = reinterpret_cast<const uint4*>(xc + (int64_t)t * rowb);
+            for (int pc = pc0; pc < pieces; pc += pstep)
+                *reinterpret_cast<uint4*>(tile + (pc >> 2) * pf::BLK + blk_code_off(r, (pc & 3) * 16)) = __ldg(src + pc);
+        }
     }
-    // scale words: a warp covers rows (r & 7) + 32 (r >> 5), one 128-byte line (index bits:
-    // row & 7, row >> 5, word, (row >> 3) & 3)
-#pragma unroll 4
-    for (int i = tid; i < 128 * words; i += blockDim.x) {
-        const int rest = i >> 5, wd = rest % words;
-        const int r = (i & 7) + 32 * ((i >> 3) & 3) + 8 * (rest / words);
-        const int t = s_tok[r];
-        if (t < 0) continue;
-        const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(xc + (int64_t)t * rowb + H / 2) + wd);
-        *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK + blk_scale_off(r, (wd & 1) * 4)) = v;
+    // scale words: a warp covers rows (r & 7) + 32 (r >> 5), one 128-byte line; thread t: row
+    // (t & 7) + 32 ((t >> 3) & 3) + 8 rb, words t >> 5, +8, ...
+    {
+        const int r_base = (tid & 7) + 32 * ((tid >> 3) & 3), w0 = tid >> 5, wstep = blockDim.x >> 5;
+#pragma unroll
+        for (int rb = 0; rb < 4; ++rb) {
+            const int r = r_base + 8 * rb;
+            const int t = s_tok[r];
+            if (t < 0) continue;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(xc + (int64_t)t * rowb + H / 2);
+            for (int wd = w0; wd < words; wd += wstep)
+                *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK + blk_scale_off(r, (wd & 1) * 4)) = __ldg(src + wd);
+        }
     }
 }
 
@@ -518,15 +525,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
             if (EPI == 2) meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
             if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            {
-                uint32_t v[32];
-                tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
-                if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
-                else epi_combine(a, v, meta, m, c0, t2s);
-            }
+            // the accumulator is in registers once the load has completed: hand the TMEM columns back to
+            // the MMA before the epilogue's math and stores
+            uint32_t v[32];
+            tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pf_su(&acc_empty[buf])) : "memory");
+            if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
+            else epi_combine(a, v, meta, m, c0, t2s);
         }
     }
     // all MMAs have completed once the epilogue has consumed every accumulator; on an abort
@@ -748,15 +755,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
-                    if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
-                    else epi_combine(a, v, meta, m, c0, t2s);
-                }
+                // the accumulator is in registers once the load has completed: hand the TMEM columns back to
+                // the MMA before the epilogue's math and stores
+                uint32_t v[32];
+                tmem_ld32(tbase + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * 128 + c0), v);
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pf_su(&acc_empty[buf])) : "memory");
+                if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
+                else epi_combine(a, v, meta, m, c0, t2s);
             }
         }
     }
