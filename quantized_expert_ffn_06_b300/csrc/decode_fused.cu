@@ -13,13 +13,18 @@
 //    L*16 and 512 + L*16 (its mma A fragment for rows L/4 and L/4 + 8), then
 //    128 B of E4M3 scales, one 4-byte word per lane.  One tile is one bulk copy
 //    and every shared-memory read of it is conflict-free.
-//  * Prologue: each token's top-k is found by one warp (k rounds of a warp-wide
-//    integer max on order-preserving keys, ties to the lower expert id) while the
-//    other threads stage the activations as f16.  Every CTA does this
-//    redundantly, so the weight stream starts without any inter-CTA traffic.
+//  * Prologue: x and the router logits land in shared memory by one bulk copy
+//    each.  Each token's top-k is found by one warp: every lane sorts its
+//    (up to eight) keys once, then k rounds of a warp-wide integer max over the
+//    lanes' heads (order-preserving keys, ties to the lower expert id).  All
+//    threads stage the activations as f16, and up to 32 (token, slot) pairs are
+//    grouped by expert inside one warp.  Every CTA does this redundantly, so
+//    the weight stream starts without any inter-CTA traffic.
 //  * One producer warp issues every tile the CTA needs with cp.async.bulk into
 //    a ring of shared-memory stages guarded by mbarriers; the down-projection
-//    tiles are prefetched while the gate/up tiles are consumed.
+//    tiles are prefetched while the gate/up tiles are consumed.  Its other
+//    lanes fetch the experts' tensor scales into shared memory, and it
+//    triggers the dependent launch, off the consumers' path.
 //  * Sixteen consumer warps form four groups.  A group owns whole tiles: its
 //    four warps split a tile's K-blocks, decode each E2M1 pair exactly to f16
 //    (cvt.rn.f16x2.e2m1x2), multiply by the E4M3 block scale in f16 (exact: at
@@ -31,9 +36,16 @@
 //    down phase of every CTA waits (bounded) for exactly the words it reads, so
 //    no grid-wide barrier separates the phases.
 //    In the down phase each CTA owns a range of 16-row output tiles for all
-//    selected experts; a warp computes one expert's down tile over the full K,
-//    so no cross-warp reduction is needed, and the weighted sum over a token's
-//    k experts is taken in slot order j from shared memory.
+//    selected experts; a warp computes one expert's down tile (for rows of 8+
+//    K-blocks, one or two experts per chunk and their K-blocks split across
+//    the group's warps), and the weighted sum over a token's k experts is
+//    taken in slot order j from shared memory.
+//  * The control code runs once per launch, so its size and latency are on the
+//    critical path: divisions by launch-time constants are host-computed
+//    multiply-high divisors, slow paths are out of line, one-shot loops stay
+//    rolled.
+//  * A batch whose f16 staging does not fit one launch runs as launches over
+//    token chunks (ft_moe_layer_decode).
 //  * Grid = one CTA per SM, all co-resident, which those waits rely on.  Every
 //    wait is bounded by a %globaltimer budget; on expiry the kernel sets
 //    FT_DEVERR_TIMEOUT, stops waiting and finishes without trapping.
