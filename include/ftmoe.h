@@ -277,7 +277,10 @@ FT_API size_t ft_moe_prefill_workspace_size(int T, int k, int E, int H, int I);
  *       (per-expert tile offsets, quantised x and h tiles, an fp32 output
  *       accumulator); no initial content needed.
  * Each expert's rows are padded to whole 128-row tiles; the padding rows of a
- * tile hold whatever the workspace held and never reach the output. */
+ * tile hold whatever the workspace held and never reach the output.
+ * offsets that do not partition [0, T*k) in order (offsets[0] = 0, non-
+ * decreasing, offsets[E] = T*k) set FT_DEVERR_BAD_INDEX; no expert row is then
+ * computed and out is all zeros. */
 FT_API ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
                                                  const int32_t* offsets, const int32_t* perm, const float* w,
                                                  uint16_t* out, void* ws, size_t ws_bytes, ft_stream_t stream);

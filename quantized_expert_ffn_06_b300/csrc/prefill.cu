@@ -186,12 +186,22 @@ __host__ __device__ __forceinline__ int blk_scale_off(int r, int j) {
 
 // ---------------------------------------------------------------------------- plan and activation tiles
 
-__global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ tile_off) {
-    __shared__ int part[1024];
+// tile_off[e] = first tile of expert e (exclusive scan of its tile counts);
+// tinfo[tile] = {expert, first permuted row, real rows in the tile, 0}.
+// offsets must partition [0, P) in order; otherwise FT_DEVERR_BAD_INDEX is
+// raised and every tile count is zero, so the later kernels do nothing.
+__global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ offsets, int E, int P, int max_tiles,
+                                                  int32_t* __restrict__ tile_off, int4* __restrict__ tinfo) {
     __shared__ int wsum[33];
+    __shared__ int s_bad;
     const int tid = threadIdx.x;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
     // experts per thread: E <= 1024, so one each
-    const int n = (tid < E) ? (offsets[tid + 1] - offsets[tid]) : 0;
+    const int o0 = (tid < E) ? offsets[tid] : 0;
+    const int o1 = (tid < E) ? offsets[tid + 1] : 0;
+    if (tid < E && (o0 < 0 || o1 < o0 || o1 > P || (tid == 0 && o0 != 0) || (tid == E - 1 && o1 != P))) s_bad = 1;
+    const int n = max(o1 - o0, 0);
     const int nt = (n + 127) / 128;
     int incl = nt;
     const int lane = tid & 31, wid = tid >> 5;
@@ -213,46 +223,55 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ of
         if (lane == 31) wsum[32] = si;
     }
     __syncthreads();
-    part[tid] = wsum[wid] + incl - nt;
-    if (tid < E) tile_off[tid] = part[tid];
+    if (s_bad || wsum[32] > max_tiles) {
+        if (tid <= E) tile_off[tid] = 0;
+        if (tid == 0) raise_dev_error(FT_DEVERR_BAD_INDEX);
+        return;
+    }
+    const int first = wsum[wid] + incl - nt;
+    if (tid < E) tile_off[tid] = first;
     if (tid == 0) tile_off[E] = wsum[32];
+    for (int i = 0; i < nt; ++i) tinfo[first + i] = make_int4(tid, o0 + 128 * i, min(128, n - 128 * i), 0);
 }
 
-// One warp per token: x[t] quantised once (unit tensor scale) into a compact
-// row of H/2 code bytes followed by H/16 scale bytes.
+// x[t] quantised once (unit tensor scale) into a compact row of H/2 code bytes
+// followed by H/16 scale bytes.  A warp covers 1024 elements of one token, 32
+// per lane (two blocks of 16): the IEEE divisions of the quantiser make this
+// latency-bound, so it spreads over as many warps as the rows allow.
 __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restrict__ x, int T, int H,
                                                          uint8_t* __restrict__ xc) {
-    const int t = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int wpt = (H + 1023) / 1024;  // warps per token
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (t >= T) return;
+    if (gw >= (int64_t)T * wpt) return;
+    const int t = (int)(gw / wpt), sub = (int)(gw - (int64_t)t * wpt);
+    const int e0 = sub * 1024 + lane * 32;
+    if (e0 >= H) return;
     uint8_t* row = xc + (int64_t)t * (H / 2 + H / 16);
-    for (int e0 = lane * 64; e0 < H; e0 += 32 * 64) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H + e0);
-        uint32_t cw[8], sw = 0;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H + e0);
+    uint32_t cw[4], sw = 0;
 #pragma unroll
-        for (int bl = 0; bl < 4; ++bl) {
-            float v[16];
+    for (int bl = 0; bl < 2; ++bl) {
+        float v[16];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint4 u = __ldg(src + 2 * bl + hh);
-                const uint32_t words[4] = {u.x, u.y, u.z, u.w};
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint4 u = __ldg(src + 2 * bl + hh);
+            const uint32_t words[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[8 * hh + 2 * i] = __uint_as_float(words[i] << 16);
-                    v[8 * hh + 2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
-                }
+            for (int i = 0; i < 4; ++i) {
+                v[8 * hh + 2 * i] = __uint_as_float(words[i] << 16);
+                v[8 * hh + 2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
             }
-            uint2 c;
-            uint32_t sb;
-            quant_block16(v, 1.0f, c, sb);
-            cw[2 * bl] = c.x;
-            cw[2 * bl + 1] = c.y;
-            sw |= sb << (8 * bl);
         }
-        *reinterpret_cast<uint4*>(row + e0 / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        *reinterpret_cast<uint4*>(row + e0 / 2 + 16) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        *reinterpret_cast<uint32_t*>(row + H / 2 + e0 / 16) = sw;
+        uint2 c;
+        uint32_t sb;
+        quant_block16(v, 1.0f, c, sb);
+        cw[2 * bl] = c.x;
+        cw[2 * bl + 1] = c.y;
+        sw |= sb << (8 * bl);
     }
+    *reinterpret_cast<uint4*>(row + e0 / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    *reinterpret_cast<uint16_t*>(row + H / 2 + e0 / 16) = (uint16_t)sw;
 }
 
 // One block per 128-row operand tile: the compact quantised rows of the tile's
@@ -261,40 +280,24 @@ __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restr
 // every output row depends only on its own tile row, and padding rows are
 // skipped).  The expert and the tokens are resolved once per tile; then every
 // thread copies 16-byte pieces, many in flight.
-__global__ void __launch_bounds__(256) k_pf_gather_x(const uint8_t* __restrict__ xc, int H, int k, int E,
-                                                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
-                                                     const float* __restrict__ w, const int32_t* __restrict__ tile_off,
+__global__ void __launch_bounds__(256, 2) k_pf_gather_x(const uint8_t* __restrict__ xc, int H, int k, int E,
+                                                     const int32_t* __restrict__ perm, const float* __restrict__ w,
+                                                     const int32_t* __restrict__ tile_off, const int4* __restrict__ tinfo,
                                                      uint8_t* __restrict__ xq, int2* __restrict__ rowmeta) {
     __shared__ int s_tok[128];
-    __shared__ int s_toff[1025];
-    __shared__ int s_e;
     const int rt = blockIdx.x, tid = threadIdx.x;
-    if (rt >= __ldg(tile_off + E)) return;
-    for (int i = tid; i <= E; i += blockDim.x) s_toff[i] = __ldg(tile_off + i);
-    __syncthreads();
-    if (tid == 0) {  // last expert with s_toff[e] <= rt
-        int lo = 0, hi = E - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_toff[mid] <= rt) lo = mid;
-            else hi = mid - 1;
-        }
-        s_e = lo;
-    }
-    __syncthreads();
-    const int e = s_e;
+    const int ntiles = __ldg(tile_off + E);
+    const int4 ti = __ldg(tinfo + rt);  // beyond the used tiles it is never read past the check below
+    if (rt >= ntiles) return;
+    int t = -1;
+    float wt = 0.0f;
     if (tid < 128) {
-        const int local = (rt - s_toff[e]) * 128 + tid;
-        const int ne = __ldg(offsets + e + 1) - __ldg(offsets + e);
-        int t = -1;
-        float wt = 0.0f;
-        if (local < ne) {
-            const int f = __ldg(perm + __ldg(offsets + e) + local);
+        if (tid < ti.z) {
+            const int f = __ldg(perm + ti.y + tid);
             t = f / k;
-            wt = __ldg(w + f);
+            wt = __ldg(w + f);  // consumed only by the row table, written last
         }
         s_tok[tid] = t;
-        rowmeta[(int64_t)rt * 128 + tid] = make_int2(t, __float_as_int(wt));
     }
     __syncthreads();
     const int KSN = H / 128, pieces = H / 32, words = H / 64;  // per row: 16-byte code pieces, 4-byte scale words
@@ -302,33 +305,53 @@ __global__ void __launch_bounds__(256) k_pf_gather_x(const uint8_t* __restrict__
     uint8_t* tile = xq + (int64_t)rt * KSN * pf::BLK;
     // codes: lanes 8a .. 8a+7 take eight consecutive rows of one 16-byte piece, i.e. one whole
     // 128-byte line of the tile; thread t: row t & 7 of each 8-row group, pieces t >> 3, +32, ...
-    // (no runtime division: this copy is instruction-heavy enough for that to matter)
+    // All sixteen row groups of a piece are loaded before any is stored, so each thread keeps
+    // sixteen loads in flight (no runtime division either: this copy is instruction-heavy).
     {
         const int r_lo = tid & 7, pc0 = tid >> 3, pstep = blockDim.x >> 3;
-#pragma unroll 4
-        for (int rg = 0; rg < 16; ++rg) {
-            const int r = rg * 8 + r_lo;
-            const int t = s_tok[r];
-            if (t < 0) continue;
-            const uint4* src = reinterpret_cast<const uint4*>(xc + (int64_t)t * rowb);
-            for (int pc = pc0; pc < pieces; pc += pstep)
-                *reinterpret_cast<uint4*>(tile + (pc >> 2) * pf::BLK + blk_code_off(r, (pc & 3) * 16)) = __ldg(src + pc);
+        for (int pc = pc0; pc < pieces; pc += pstep) {
+            uint4 v[16];
+#pragma unroll
+            for (int rg = 0; rg < 16; ++rg) {
+                const int tk = s_tok[rg * 8 + r_lo];
+                if (tk >= 0) v[rg] = __ldg(reinterpret_cast<const uint4*>(xc + (int64_t)tk * rowb) + pc);
+            }
+            uint8_t* dst = tile + (pc >> 2) * pf::BLK + blk_code_off(r_lo, (pc & 3) * 16);
+#pragma unroll
+            for (int rg = 0; rg < 16; ++rg)
+                if (s_tok[rg * 8 + r_lo] >= 0) *reinterpret_cast<uint4*>(dst + rg * 128) = v[rg];
         }
     }
     // scale words: a warp covers rows (r & 7) + 32 (r >> 5), one 128-byte line; thread t: row
-    // (t & 7) + 32 ((t >> 3) & 3) + 8 rb, words t >> 5, +8, ...
+    // (t & 7) + 32 ((t >> 3) & 3) + 8 rb, words t >> 5, +8, ...; up to four words of each of the
+    // four rows are loaded before any is stored
     {
         const int r_base = (tid & 7) + 32 * ((tid >> 3) & 3), w0 = tid >> 5, wstep = blockDim.x >> 5;
+        const uint32_t* src[4];
 #pragma unroll
         for (int rb = 0; rb < 4; ++rb) {
-            const int r = r_base + 8 * rb;
-            const int t = s_tok[r];
-            if (t < 0) continue;
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(xc + (int64_t)t * rowb + H / 2);
-            for (int wd = w0; wd < words; wd += wstep)
-                *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK + blk_scale_off(r, (wd & 1) * 4)) = __ldg(src + wd);
+            const int tk = s_tok[r_base + 8 * rb];
+            src[rb] = tk < 0 ? nullptr : reinterpret_cast<const uint32_t*>(xc + (int64_t)tk * rowb + H / 2);
+        }
+        for (int wd0 = w0; wd0 < words; wd0 += 4 * wstep) {
+            uint32_t v[4][4];
+#pragma unroll
+            for (int rb = 0; rb < 4; ++rb)
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if (src[rb] != nullptr && wd0 + m * wstep < words) v[rb][m] = __ldg(src[rb] + wd0 + m * wstep);
+#pragma unroll
+            for (int rb = 0; rb < 4; ++rb)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int wd = wd0 + m * wstep;
+                    if (src[rb] != nullptr && wd < words)
+                        *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK +
+                                                     blk_scale_off(r_base + 8 * rb, (wd & 1) * 4)) = v[rb][m];
+                }
         }
     }
+    if (tid < 128) rowmeta[(int64_t)rt * 128 + tid] = make_int2(t, __float_as_int(wt));
 }
 
 __global__ void __launch_bounds__(256) k_pf_out(const float4* __restrict__ out32, int64_t n4, uint2* __restrict__ out) {
@@ -825,7 +848,7 @@ static int pf_sm_count() {
 static size_t a256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct PfWs {
-    size_t tile_off, xc, xq, hq, rowmeta, out32, total;
+    size_t tile_off, tinfo, xc, xq, hq, rowmeta, out32, total;
     int max_tiles;
 };
 
@@ -836,6 +859,8 @@ static PfWs pf_ws_layout(int T, int k, int E, int H, int I) {
     size_t off = 0;
     w.tile_off = off;
     off += a256((size_t)(E + 1) * 4);
+    w.tinfo = off;
+    off += a256((size_t)w.max_tiles * 16);
     w.xc = off;
     off += a256((size_t)T * (H / 2 + H / 16));
     w.xq = off;
@@ -909,6 +934,7 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     if (W->I % 128) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": I must be a multiple of 128");
     if (T < 0 || k <= 0 || k > W->E || k > 32) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need T >= 0, 1 <= k <= min(E, 32)");
     if (T == 0) return FT_OK;
+    if ((int64_t)T * k > INT32_MAX) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": T*k must fit in int32");
     if (!x || !offsets || !perm || !w || !out) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
     if (!aligned(x, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": x needs 16-byte alignment");
     if (!aligned(out, 8)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": out needs 8-byte alignment");
@@ -918,6 +944,7 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": workspace missing, too small or not 256-byte aligned");
     uint8_t* base = static_cast<uint8_t*>(ws);
     int32_t* tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
+    int4* tinfo = reinterpret_cast<int4*>(base + L.tinfo);
     uint8_t* xq = base + L.xq;
     uint8_t* xc = base + L.xc;
     int2* rowmeta = reinterpret_cast<int2*>(base + L.rowmeta);
@@ -933,9 +960,12 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     });
     cudaError_t e = cudaMemsetAsync(out32, 0, (size_t)T * H * 4, s);
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
-    k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, tile_off);
-    k_pf_quant_tokens<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(x, T, H, xc);
-    k_pf_gather_x<<<(unsigned)L.max_tiles, 256, 0, s>>>(xc, H, k, E, offsets, perm, w, tile_off, xq, rowmeta);
+    k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, (int)((int64_t)T * k), L.max_tiles, tile_off, tinfo);
+    {
+        const int64_t warps = (int64_t)T * ((H + 1023) / 1024);
+        k_pf_quant_tokens<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(x, T, H, xc);
+    }
+    k_pf_gather_x<<<(unsigned)L.max_tiles, 256, 0, s>>>(xc, H, k, E, perm, w, tile_off, tinfo, xq, rowmeta);
     PfGemmArgs g{};
     g.tscale = W->tscale;
     g.ts_stride = W->tscale_stride;

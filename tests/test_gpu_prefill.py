@@ -131,3 +131,28 @@ def test_hidden_beyond_resident_token_tile_streams_both_operands():
     logits, x_bits = W.router_logits(cfg, 0, 3), W.activations_bf16(cfg, 0, 3)
     mod, out = run(cfg, lw, logits, x_bits)
     check(cfg, 0, mod, out, logits, x_bits)
+
+
+@pytest.mark.parametrize("case", ["short_total", "decreasing", "negative_start"])
+def test_offsets_that_do_not_partition_the_rows_are_reported_and_add_nothing(case):
+    """offsets must split [0, T*k) into consecutive per-expert ranges; anything else is flagged on the
+    device and no expert row is computed, so no tile index can run past the workspace."""
+    cfg = W.CONFIGS["tiny"]
+    lw = weights(cfg, 0)
+    logits, x_bits = W.router_logits(cfg, 0, 3), W.activations_bf16(cfg, 0, 3)
+    mod, out = run(cfg, lw, logits, x_bits)
+    bad = mod.offsets.clone()
+    if case == "short_total":
+        bad[-1] -= 1
+    elif case == "decreasing":
+        bad[2] = int(bad[3].item()) + 1  # expert 2 would end before it starts
+    else:
+        bad[0] = -128
+    out.fill_(1.0)
+    Q.ft_moe_expert_ffn_nvfp4_prefill(lw, to_dev(x_bits.view(np.int16), torch.bfloat16), cfg.k, bad, mod.perm,
+                                      mod.w, out, mod.ws)
+    assert Q.ft_device_status() == Q.FT_DEVERR_BAD_INDEX
+    assert not out.float().abs().sum().item()
+    # the workspace stays usable: a valid call after the failed one is exact again
+    mod2, out2 = run(cfg, lw, logits, x_bits)
+    check(cfg, 0, mod2, out2, logits, x_bits)
