@@ -15,7 +15,7 @@
 //     tiles; tile_off[e] = first tile of expert e (exclusive scan).
 //  2. k_pf_quant_tokens + k_pf_gather_x: each token's x quantised once, then
 //     copied in permuted order into operand tiles, with a (token, weight) table
-//     of the padded rows.
+//     of the padded rows; the gather also zeroes the fp32 output accumulator.
 //  3. k_pf_gemm<1>: h = silu(Wg x) * (Wu x) per (expert, 128 gate/up rows,
 //     128 tokens) tile, rounded to bf16 and quantised into operand tiles.
 //  4. k_pf_gemm<2>: y = Wd h per (expert, 128 output rows, 128 tokens) tile;
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ of
 // x[t] quantised once (unit tensor scale) into a compact row of H/2 code bytes
 // followed by H/16 scale bytes.  A warp covers 1024 elements of one token, 32
 // per lane (two blocks of 16): the IEEE divisions of the quantiser make this
-// latency-bound, so it spreads over as many warps as the rows allow.
+// issue-bound, so it spreads over as many warps as the rows allow.
 __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restrict__ x, int T, int H,
                                                          uint8_t* __restrict__ xc) {
     const int wpt = (H + 1023) / 1024;  // warps per token
@@ -274,18 +274,29 @@ __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restr
     *reinterpret_cast<uint16_t*>(row + H / 2 + e0 / 16) = (uint16_t)sw;
 }
 
-// One block per 128-row operand tile: the compact quantised rows of the tile's
-// tokens copied into the tile, and each row's (token, routing weight) for the
-// combine (token -1 for padding rows, whose tile rows keep whatever they held:
-// every output row depends only on its own tile row, and padding rows are
-// skipped).  The expert and the tokens are resolved once per tile; then every
-// thread copies 16-byte pieces, many in flight.
+// Two blocks per 128-row operand tile, one per half of K: the compact quantised
+// rows of the tile's tokens copied into the tile, and each row's (token,
+// routing weight) for the combine (token -1 for padding rows, whose tile rows
+// keep whatever they held: every output row depends only on its own tile row,
+// and padding rows are skipped).  Each block resolves the tile's tokens, then
+// every thread copies 16-byte pieces, many in flight.  Every block (used tile
+// or not) first zeroes its share of the fp32 output accumulator (n4 float4s in
+// all), which the down GEMM's combine adds into: the stores overlap the
+// block's first dependent loads.
 __global__ void __launch_bounds__(256, 2) k_pf_gather_x(const uint8_t* __restrict__ xc, int H, int k, int E,
                                                      const int32_t* __restrict__ perm, const float* __restrict__ w,
                                                      const int32_t* __restrict__ tile_off, const int4* __restrict__ tinfo,
-                                                     uint8_t* __restrict__ xq, int2* __restrict__ rowmeta) {
+                                                     uint8_t* __restrict__ xq, int2* __restrict__ rowmeta,
+                                                     float4* __restrict__ out32, int64_t n4) {
     __shared__ int s_tok[128];
-    const int rt = blockIdx.x, tid = threadIdx.x;
+    {
+        const int64_t per = (n4 + gridDim.x - 1) / gridDim.x, z0 = (int64_t)blockIdx.x * per;
+        const int64_t z1 = min(n4, z0 + per);
+        for (int64_t i = z0 + threadIdx.x; i < z1; i += blockDim.x) out32[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    // two blocks per tile, each copying half of its K blocks (H is a multiple of 256, so the halves are whole
+    // K blocks); the first also writes the row table
+    const int rt = blockIdx.x >> 1, kp = blockIdx.x & 1, tid = threadIdx.x;
     const int ntiles = __ldg(tile_off + E);
     const int4 ti = __ldg(tinfo + rt);  // beyond the used tiles it is never read past the check below
     if (rt >= ntiles) return;
@@ -309,7 +320,8 @@ __global__ void __launch_bounds__(256, 2) k_pf_gather_x(const uint8_t* __restric
     // sixteen loads in flight (no runtime division either: this copy is instruction-heavy).
     {
         const int r_lo = tid & 7, pc0 = tid >> 3, pstep = blockDim.x >> 3;
-        for (int pc = pc0; pc < pieces; pc += pstep) {
+        const int pc_end = (kp + 1) * (pieces / 2);
+        for (int pc = kp * (pieces / 2) + pc0; pc < pc_end; pc += pstep) {
             uint4 v[16];
 #pragma unroll
             for (int rg = 0; rg < 16; ++rg) {
@@ -333,25 +345,26 @@ __global__ void __launch_bounds__(256, 2) k_pf_gather_x(const uint8_t* __restric
             const int tk = s_tok[r_base + 8 * rb];
             src[rb] = tk < 0 ? nullptr : reinterpret_cast<const uint32_t*>(xc + (int64_t)tk * rowb + H / 2);
         }
-        for (int wd0 = w0; wd0 < words; wd0 += 4 * wstep) {
+        const int wd_end = (kp + 1) * (words / 2);
+        for (int wd0 = kp * (words / 2) + w0; wd0 < wd_end; wd0 += 4 * wstep) {
             uint32_t v[4][4];
 #pragma unroll
             for (int rb = 0; rb < 4; ++rb)
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
-                    if (src[rb] != nullptr && wd0 + m * wstep < words) v[rb][m] = __ldg(src[rb] + wd0 + m * wstep);
+                    if (src[rb] != nullptr && wd0 + m * wstep < wd_end) v[rb][m] = __ldg(src[rb] + wd0 + m * wstep);
 #pragma unroll
             for (int rb = 0; rb < 4; ++rb)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int wd = wd0 + m * wstep;
-                    if (src[rb] != nullptr && wd < words)
+                    if (src[rb] != nullptr && wd < wd_end)
                         *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK +
                                                      blk_scale_off(r_base + 8 * rb, (wd & 1) * 4)) = v[rb][m];
                 }
         }
     }
-    if (tid < 128) rowmeta[(int64_t)rt * 128 + tid] = make_int2(t, __float_as_int(wt));
+    if (kp == 0 && tid < 128) rowmeta[(int64_t)rt * 128 + tid] = make_int2(t, __float_as_int(wt));
 }
 
 __global__ void __launch_bounds__(256) k_pf_out(const float4* __restrict__ out32, int64_t n4, uint2* __restrict__ out) {
@@ -958,14 +971,13 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
         cudaFuncSetAttribute(k_pf_gemm_res<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM_LIMIT);
         cudaFuncSetAttribute(k_pf_gemm_res<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM_LIMIT);
     });
-    cudaError_t e = cudaMemsetAsync(out32, 0, (size_t)T * H * 4, s);
-    if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
     k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, (int)((int64_t)T * k), L.max_tiles, tile_off, tinfo);
     {
         const int64_t warps = (int64_t)T * ((H + 1023) / 1024);
         k_pf_quant_tokens<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(x, T, H, xc);
     }
-    k_pf_gather_x<<<(unsigned)L.max_tiles, 256, 0, s>>>(xc, H, k, E, perm, w, tile_off, tinfo, xq, rowmeta);
+    k_pf_gather_x<<<(unsigned)(2 * L.max_tiles), 256, 0, s>>>(xc, H, k, E, perm, w, tile_off, tinfo, xq, rowmeta,
+                                                               reinterpret_cast<float4*>(out32), (int64_t)T * H / 4);
     PfGemmArgs g{};
     g.tscale = W->tscale;
     g.ts_stride = W->tscale_stride;
