@@ -418,6 +418,16 @@ def run_gpu(args, ws, rank, local):
     }
 
 
+def bench_config(args):
+    """The named workload; for a prefill workload ``--tokens`` sets the prompt length of a T-sweep point."""
+    cfg = W.CONFIGS[args.config]
+    if args.tokens:
+        if cfg.routing != "zipf":
+            raise SystemExit("--tokens applies to the prefill workload only")
+        cfg = W.scaled(cfg, T=args.tokens, name=f"{cfg.name}_t{args.tokens}")
+    return cfg
+
+
 def run_gpu_prefill(args, ws, rank, local):
     """Prefill layer step: T tokens through route -> permute -> tensor-core NVFP4 expert FFN + combine."""
     import torch
@@ -426,7 +436,7 @@ def run_gpu_prefill(args, ws, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = W.CONFIGS[args.config]
+    cfg = bench_config(args)
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     NW = 4  # weight sets rotated between steps: 4 x the layer's weights, far beyond L2
     S = min(args.distinct_steps, 4)
@@ -505,6 +515,8 @@ def run_gpu_prefill(args, ws, rank, local):
     hbm_peak, hbm_kind = load_peaks()
     bf16_peak, bf16_kind = load_bf16_peak()
     fp4_peak = bf16_peak * 6.0  # nominal dense FP4 : BF16 ratio of 13.5 : 2.25
+    ai = flops / bytes_ffn  # FLOP per algorithmic byte
+    attainable = min(fp4_peak, hbm_peak * ai / 1e3)  # TFLOP/s
     e2e = None
     if not args.no_e2e:
         x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -555,6 +567,9 @@ def run_gpu_prefill(args, ws, rank, local):
                      "kernel": "ft_moe_expert_ffn_nvfp4_prefill (plan, x quantisation, gate/up and down grouped "
                                "GEMMs, output), timed as one call",
                      "bytes_per_launch": bytes_ffn, "avg_launch_us": ffn_s * 1e6, "traffic": None},
+        "attainable": {"tflops": attainable, "frac": flops / ffn_s / 1e12 / attainable,
+                       "bound": "hbm" if hbm_peak * ai / 1e3 < fp4_peak else "tensor", "flop_per_byte": ai,
+                       "what": "the FFN call against min(FP4 peak, HBM peak x its arithmetic intensity)"},
         "tensor": {"achieved": flops / ffn_s / 1e12, "peak": fp4_peak, "unit": "TFLOP/s",
                    "frac": flops / ffn_s / 1e12 / fp4_peak,
                    "peak_kind": f"{bf16_kind} bf16 x 6 (nominal FP4:BF16 dense ratio)", "flops_per_launch": flops},
@@ -683,10 +698,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=48)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="prefill only: prompt tokens per step instead of the workload's 4096 (a labelled T-sweep point)")
     args = ap.parse_args()
 
     ws, rank, local = dist_env()
-    cfg = W.CONFIGS[args.config]
+    cfg = bench_config(args)
 
     if args.impl == "reference":
         if rank != 0:
