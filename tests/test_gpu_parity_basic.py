@@ -77,6 +77,46 @@ def test_weight_quantizer_random_bulk_bit_exact():
     assert np.array_equal(codes.cpu().numpy(), c_ref)
 
 
+def mixed_magnitude_blocks(rng, rows, K, lo=-14.0, hi=6.0):
+    """fp32 [rows, K]: N(0,1) values whose 16-element blocks are scaled by log-uniform magnitudes e^lo..e^hi, so
+    block scales land on zero, subnormal, normal and saturating E4M3 values against one tensor amax."""
+    mag = np.exp(rng.uniform(lo, hi, size=(rows, K // 16, 1))).astype(np.float32)
+    return (rng.standard_normal(size=(rows, K // 16, 16), dtype=np.float32) * mag).reshape(rows, K)
+
+
+def test_weight_quantizer_bit_exact_on_1e8_values():
+    """Six tensors of 2^24 values each (1.007e8 in all) quantised on the GPU and by the oracle, compared byte for
+    byte: tensor scale, every E4M3 block scale and every E2M1 code."""
+    rng = np.random.default_rng(20240601)
+    N, K = 8192, 2048
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((N, K // 16), dtype=torch.uint8, device=DEV)
+    ts = torch.empty(1, dtype=torch.float32, device=DEV)
+    for chunk in range(6):
+        w = mixed_magnitude_blocks(rng, N, K)
+        Q.ft_nvfp4_quantize_weight(to_dev(w), codes, scales, ts)
+        c_ref, s_ref, ts_ref = O.quantize_weight(w)
+        assert ts.item() == ts_ref, chunk
+        assert np.array_equal(scales.cpu().numpy(), s_ref), chunk
+        assert np.array_equal(codes.cpu().numpy(), c_ref), chunk
+
+
+def test_activation_quantizer_bit_exact_on_1e8_values():
+    """1.007e8 bf16 activations (six batches of 2^24, mixed block magnitudes) quantised with unit tensor scale on
+    the GPU and by the oracle, compared byte for byte."""
+    rng = np.random.default_rng(20240602)
+    T, K = 8192, 2048
+    for chunk in range(6):
+        f = mixed_magnitude_blocks(rng, T, K, lo=-12.0, hi=8.0)
+        u = f.view(np.uint32)
+        bits = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)  # fp32 -> bf16, nearest even
+        x = (bits.astype(np.uint32) << 16).view(np.float32)
+        codes, scales = Q.ft_nvfp4_quantize_act(to_dev(bits.view(np.int16), torch.bfloat16))
+        c_ref, s_ref = O.quantize_act(x)
+        assert np.array_equal(scales.cpu().numpy(), s_ref), chunk
+        assert np.array_equal(codes.cpu().numpy(), c_ref), chunk
+
+
 @pytest.mark.parametrize("T,K", [(4, 256), (64, 2048), (3, 512)])
 def test_activation_quantizer_bit_exact(T, K):
     bits = W.normal_bf16(W.x_stream(7, T, K), T * K).reshape(T, K)
