@@ -659,6 +659,24 @@ def run_gpu_cache(args, ws, rank, local):
     hits, misses, filled = h1 - h0, m1 - m0, b1 - b0
     step_s = ms / 1e3 / args.steps
     hbm_peak, hbm_kind = load_peaks()
+    # elastic resize at a safe point, after the timed stream: every layer shrinks to half its slots in a new pool
+    # (the most recently used half moves device to device), then grows back (all of them move again)
+    resize = {}
+    S0 = pool.S
+    for name, n in (("shrink", S0 // 2), ("grow", S0)):
+        moved = sum(q >= 0 for row in pool.cache.resize_plan(n) for q in row)
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        r0.record(stream)
+        pool.resize(n, stream=stream)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        t_s = r0.elapsed_time(r1) / 1e3
+        resize[name] = {"slots": f"{S0 if name == 'shrink' else S0 // 2} -> {n} per layer", "experts_moved": moved,
+                        "bytes_moved": moved * pool.expert_bytes, "ms": t_s * 1e3,
+                        "gbs_read_plus_write": 2 * moved * pool.expert_bytes / t_s / 1e9,
+                        "frac_of_hbm_copy": 2 * moved * pool.expert_bytes / t_s / 1e9 / hbm_peak}
+    assert Q.ft_device_status(stream) == 0
     # per-token bound: every layer must bring its misses over PCIe and stream its k experts from HBM
     miss_bytes_tok = filled / args.steps
     hbm_bytes_tok = L * k * pool.expert_bytes
@@ -675,7 +693,10 @@ def run_gpu_cache(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "cache": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                   "h2d_bytes_per_token": miss_bytes_tok, "h2d_gbs_achieved": filled / (ms / 1e3) / 1e9,
-                  "h2d_gbs_measured_peak": h2d_gbs},
+                  "h2d_gbs_measured_peak": h2d_gbs,
+                  "resize": dict(resize, what="ft_expert_cache_resize after the timed stream (device-to-device "
+                                              "moves + the publish of every layer's table), CUDA events on the "
+                                              "stream; not part of the tok/s")},
         "roofline": {"bound": "pcie+hbm", "achieved": 1.0 / step_s, "peak": 1.0 / bound_s, "unit": "tok/s",
                      "frac": bound_s / step_s, "peak_kind": f"measured pinned H2D {h2d_gbs:.1f} GB/s and {hbm_kind} HBM",
                      "kernel": "whole token (route, host lookup, fills, slot-table publish, fused layer kernel) x layers",

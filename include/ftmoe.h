@@ -335,9 +335,34 @@ FT_API ft_status ft_expert_cache_fill(ft_expert_cache* cache, int layer, int exp
 FT_API ft_status ft_expert_cache_publish(ft_expert_cache* cache, int layer, ft_stream_t stream);
 /* Counters since creation: hit and miss accesses, bytes enqueued by fills. */
 FT_API ft_status ft_expert_cache_stats(ft_expert_cache* cache, int64_t* hits, int64_t* misses, int64_t* bytes_filled);
-/* Test hook: the fill with 0-based index `fill_index` (counting every fill
- * call on this handle) returns FT_ERR_CUDA without enqueuing a copy; -1 turns
- * the hook off. */
+/* [P5 设计核心, third mechanism] Elastic resize at a safe point: the cache
+ * becomes new_S slots per layer in the pool new_slots (device, caller-owned,
+ * slot s of layer l at new_slots + (l*new_S + s)*new_slot_stride; alignment as
+ * in _create), rebuilt from the experts already in VRAM with no host reload.
+ * Policy (the pages give none): per layer, all resident experts are kept if
+ * they fit, else the new_S most recently used (lower old slot on equal
+ * stamps); kept experts take new slots 0.. in ascending old-slot order and keep
+ * their stamps; the others leave the cache.  Counters are unchanged.
+ * The moves run on `stream` (a copy kernel between disjoint pools, ordered
+ * cudaMemcpyAsync in place), followed by the publish of every layer's table
+ * on `stream`.  Safe point: every fill into the
+ * old pool and every kernel reading it must be ordered before `stream`; the
+ * old pool must stay allocated until `stream` passes this call.  new_slots may
+ * overlap the old pool only as a shrink in place (same base and stride,
+ * new_S <= S); any other overlap is FT_ERR_INVALID_ARG.  If a move cannot be
+ * enqueued the call returns FT_ERR_CUDA and the cache is empty with the new
+ * geometry (nothing published: publish each layer before its next use).
+ * A lookup after a shrink needs n <= new_S. */
+FT_API ft_status ft_expert_cache_resize(ft_expert_cache* cache, int new_S, void* new_slots, size_t new_slot_stride,
+                                        ft_stream_t stream);
+/* The plan ft_expert_cache_resize(new_S) would apply now, without applying it
+ * (pure host): moves (host) int32 [L][new_S], the old slot whose expert goes to
+ * each new slot, -1 for a free one. */
+FT_API ft_status ft_expert_cache_resize_plan(ft_expert_cache* cache, int new_S, int32_t* moves);
+/* Test hook: the slot copy with 0-based index `fill_index` (counting every
+ * fill call and every copy a resize enqueues on this handle: one per moved
+ * slot in place, one per launch of up to 256 moves between disjoint pools)
+ * returns FT_ERR_CUDA without enqueuing it; -1 turns the hook off. */
 FT_API ft_status ft_expert_cache_inject_fill_failure(ft_expert_cache* cache, int64_t fill_index);
 
 /* ------------------------------------------------------------------------ */

@@ -15,6 +15,12 @@ details, so this oracle states them:
   the slot with the oldest stamp among experts the current token does not
   select, the lower slot index winning a tie; the new expert's stamp is the
   current step.
+
+The same page (section 设计核心, third mechanism) resizes and rebuilds the cache
+at safe points from free VRAM without a reload.  Which experts survive is not
+said; this oracle reads it as: all resident experts when they fit, else the
+``slots`` most recently used ones (the lower old slot on equal stamps); they
+keep their stamps and take slots 0, 1, ... in the order of their old slots.
 """
 from __future__ import annotations
 
@@ -61,3 +67,18 @@ class LayerLRU:
             result[e] = s
             misses.append((e, s))
         return [result[e] for e in ids], misses
+
+    def resize(self, slots: int):
+        """Resize to ``slots`` slots; returns, for each new slot, the old slot whose expert moves there (-1: free)."""
+        if slots <= 0:
+            raise ValueError("slots must be positive")
+        resident = [q for q in range(self.slots) if self.expert_of[q] >= 0]
+        if len(resident) > slots:
+            newest_first = sorted(resident, key=lambda q: (-self.stamp[q], q))
+            resident = sorted(newest_first[:slots])
+        moves = resident + [-1] * (slots - len(resident))
+        self.expert_of = [self.expert_of[q] if q >= 0 else -1 for q in moves]
+        self.stamp = [self.stamp[q] if q >= 0 else -1 for q in moves]
+        self.slot_of = {e: s for s, e in enumerate(self.expert_of) if e >= 0}
+        self.slots = slots
+        return moves

@@ -88,6 +88,8 @@ _sig("ft_expert_cache_fill", [_vp, _i32, _i32, _i32, _vp, _vp])
 _sig("ft_expert_cache_publish", [_vp, _i32, _vp])
 _sig("ft_expert_cache_stats", [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64)])
 _sig("ft_expert_cache_inject_fill_failure", [_vp, _i64])
+_sig("ft_expert_cache_resize", [_vp, _i32, _vp, _sz, _vp])
+_sig("ft_expert_cache_resize_plan", [_vp, _i32, ctypes.POINTER(ctypes.c_int32)])
 
 EXPORTED = [n for n in dir(_lib) if n.startswith("ft_")]
 
@@ -322,6 +324,21 @@ class ExpertCacheHandle:
 
     def inject_fill_failure(self, fill_index: int):
         _check(_lib.ft_expert_cache_inject_fill_failure(self.h, fill_index))
+
+    def resize_plan(self, new_S: int):
+        """[[old slot or -1 for each new slot] for each layer] that resize(new_S) would apply now."""
+        moves = (ctypes.c_int32 * (self.L * new_S))()
+        _check(_lib.ft_expert_cache_resize_plan(self.h, new_S, moves))
+        return [[moves[l * new_S + i] for i in range(new_S)] for l in range(self.L)]
+
+    def resize(self, new_S: int, new_slots_ptr: int, new_slot_stride: int, stream=None):
+        """Rebuild the cache as new_S slots per layer in a caller-owned device pool (device-to-device moves and the
+        publish of every layer's table, on `stream`)."""
+        try:
+            _check(_lib.ft_expert_cache_resize(self.h, new_S, new_slots_ptr, new_slot_stride, _s(stream)))
+        finally:
+            # the handle has the new geometry whether or not every move was enqueued
+            self.S = new_S
 
 
 from .layer import FusedDecodeLayer, LayerWeights, MoEDecodeLayer  # noqa: E402,F401

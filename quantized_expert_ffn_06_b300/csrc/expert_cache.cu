@@ -16,6 +16,12 @@
 //    stamp among experts the current token does not select (lower slot wins a
 //    tie); the new expert's stamp is the current step.
 //
+// Elastic resize (same page, section 设计核心, third mechanism: the cache is
+// resized and rebuilt from free VRAM at safe points, with no restart and no
+// reload): the resident experts move device to device into the new pool (or
+// are compacted in place when it shrinks); the ones that no longer fit go,
+// least recently used first.
+//
 // Everything here is host bookkeeping plus cudaMemcpyAsync: the caller owns the
 // pinned host pool, the device slot pool and the device slot tables.
 #include "common.cuh"
@@ -41,7 +47,7 @@ struct ft_expert_cache {
     std::vector<int> ring_pos;         // [L]
     // statistics and the host-side fault hook
     int64_t hits = 0, misses = 0, fills = 0, bytes_filled = 0;
-    int64_t fail_at_fill = -1;  // the fill with this index (0-based) reports a failure instead of copying
+    int64_t fail_at_fill = -1;  // the slot copy (fill or resize move) with this 0-based index fails instead
     std::mutex mu;
 };
 
@@ -104,6 +110,71 @@ ft_status ensure_staging(ft_expert_cache* c, const char* fn) {
         e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
         if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
     }
+    return FT_OK;
+}
+
+// Plan of one layer for a resize to new_S slots: moves[i] = the old slot whose
+// expert goes to new slot i, or -1.  The occupied slots are always a prefix
+// (misses take the lowest free slot; evictions reuse the victim's slot).  When
+// they fit, all are kept; otherwise the new_S with the newest stamps (the lower
+// old slot on a tie).  The kept experts take new slots 0.. in ascending old-slot
+// order, which a compaction in place relies on.
+void plan_layer(const ft_expert_cache* c, int layer, int new_S, int32_t* moves) {
+    const auto& expert_of = c->expert_of[layer];
+    const auto& stamp = c->stamp[layer];
+    std::vector<int32_t> occ;
+    for (int q = 0; q < c->S; ++q)
+        if (expert_of[q] >= 0) occ.push_back(q);
+    if ((int)occ.size() > new_S) {
+        std::stable_sort(occ.begin(), occ.end(), [&](int32_t a, int32_t b) { return stamp[a] > stamp[b]; });
+        occ.resize(new_S);
+        std::sort(occ.begin(), occ.end());
+    }
+    for (int i = 0; i < new_S; ++i) moves[i] = i < (int)occ.size() ? occ[i] : -1;
+}
+
+// Device-to-device moves of whole slots between two disjoint pools, passed by
+// value (up to kMovesPerLaunch per launch): block (c, m) copies bytes
+// [c*kMoveChunk, min(bytes, (c+1)*kMoveChunk)) of move m, 16 bytes per thread
+// and step (slot starts are 256-byte aligned), the last bytes singly.
+constexpr int kMovesPerLaunch = 256;
+constexpr size_t kMoveChunk = 64 * 1024;
+struct SlotMoves {
+    int32_t src[kMovesPerLaunch];  // global slot index in the old pool (layer*S + slot)
+    int32_t dst[kMovesPerLaunch];  // global slot index in the new pool (layer*new_S + slot)
+};
+
+__global__ void __launch_bounds__(256) k_slot_moves(const uint8_t* __restrict__ old_base, size_t old_stride,
+                                                    uint8_t* __restrict__ new_base, size_t new_stride, size_t bytes,
+                                                    SlotMoves mv) {
+    const int m = blockIdx.y;
+    const size_t c0 = (size_t)blockIdx.x * kMoveChunk;
+    if (c0 >= bytes) return;
+    const size_t c1 = c0 + kMoveChunk < bytes ? c0 + kMoveChunk : bytes;
+    const uint8_t* src = old_base + (size_t)mv.src[m] * old_stride;
+    uint8_t* dst = new_base + (size_t)mv.dst[m] * new_stride;
+    const size_t v1 = c0 + ((c1 - c0) & ~(size_t)15);  // c0 is a multiple of 16
+    for (size_t o = c0 + 16 * (size_t)threadIdx.x; o < v1; o += 16 * (size_t)blockDim.x)
+        *reinterpret_cast<uint4*>(dst + o) = __ldg(reinterpret_cast<const uint4*>(src + o));
+    for (size_t o = v1 + threadIdx.x; o < c1; o += blockDim.x) dst[o] = src[o];
+}
+
+// Copy of layer `layer`'s expert -> slot table to the device, through the pinned ring (caller holds the lock).
+ft_status publish_locked(ft_expert_cache* c, int layer, cudaStream_t stream, const char* fn) {
+    ft_status st = ensure_staging(c, fn);
+    if (st != FT_OK) return st;
+    const int pos = c->ring_pos[layer];
+    c->ring_pos[layer] = (pos + 1) % c->kRing;
+    cudaEvent_t ev = c->ring_ev[(size_t)layer * c->kRing + pos];
+    // the staging entry may still feed a copy issued kRing publishes ago
+    cudaError_t e = cudaEventSynchronize(ev);
+    if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+    int32_t* stage = c->pinned + ((size_t)layer * c->kRing + pos) * c->E;
+    std::copy(c->slot_of[layer].begin(), c->slot_of[layer].end(), stage);
+    e = cudaMemcpyAsync(c->tables + (size_t)layer * c->E, stage, sizeof(int32_t) * c->E, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": cudaMemcpyAsync: " + cudaGetErrorString(e));
+    e = cudaEventRecord(ev, stream);
+    if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": cudaEventRecord: " + cudaGetErrorString(e));
     return FT_OK;
 }
 
@@ -205,21 +276,121 @@ ft_status ft_expert_cache_publish(ft_expert_cache* c, int layer, ft_stream_t str
     if (!c) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null cache");
     if (layer < 0 || layer >= c->L) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": layer out of range");
     std::lock_guard<std::mutex> lock(c->mu);
-    ft_status st = ensure_staging(c, fn);
-    if (st != FT_OK) return st;
-    const int pos = c->ring_pos[layer];
-    c->ring_pos[layer] = (pos + 1) % c->kRing;
-    cudaEvent_t ev = c->ring_ev[(size_t)layer * c->kRing + pos];
-    // the staging entry may still feed a copy issued kRing publishes ago
-    cudaError_t e = cudaEventSynchronize(ev);
-    if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
-    int32_t* stage = c->pinned + ((size_t)layer * c->kRing + pos) * c->E;
-    std::copy(c->slot_of[layer].begin(), c->slot_of[layer].end(), stage);
-    e = cudaMemcpyAsync(c->tables + (size_t)layer * c->E, stage, sizeof(int32_t) * c->E, cudaMemcpyHostToDevice,
-                        ft::cu(stream));
-    if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": cudaMemcpyAsync: " + cudaGetErrorString(e));
-    e = cudaEventRecord(ev, ft::cu(stream));
-    if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": cudaEventRecord: " + cudaGetErrorString(e));
+    return publish_locked(c, layer, ft::cu(stream), fn);
+}
+
+ft_status ft_expert_cache_resize_plan(ft_expert_cache* c, int new_S, int32_t* moves) {
+    const char* fn = "ft_expert_cache_resize_plan";
+    if (!c || !moves) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if (new_S <= 0 || new_S > c->E) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 1 <= new_S <= E");
+    std::lock_guard<std::mutex> lock(c->mu);
+    for (int l = 0; l < c->L; ++l) plan_layer(c, l, new_S, moves + (size_t)l * new_S);
+    return FT_OK;
+}
+
+ft_status ft_expert_cache_resize(ft_expert_cache* c, int new_S, void* new_slots, size_t new_slot_stride,
+                                 ft_stream_t stream) {
+    const char* fn = "ft_expert_cache_resize";
+    if (!c || !new_slots) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if (new_S <= 0 || new_S > c->E) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 1 <= new_S <= E");
+    if (new_slot_stride < c->expert_bytes || new_slot_stride % 256 || reinterpret_cast<uintptr_t>(new_slots) % 256)
+        return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) +
+                                                  ": new_slot_stride must be >= expert_bytes and both it and new_slots "
+                                                  "256-byte aligned");
+    std::lock_guard<std::mutex> lock(c->mu);
+    uint8_t* nb = static_cast<uint8_t*>(new_slots);
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(c->slots), o1 = o0 + (size_t)c->L * c->S * c->slot_stride;
+    const uintptr_t n0 = reinterpret_cast<uintptr_t>(nb), n1 = n0 + (size_t)c->L * new_S * new_slot_stride;
+    const bool overlap = n0 < o1 && o0 < n1;
+    const bool in_place = nb == c->slots && new_slot_stride == c->slot_stride && new_S <= c->S;
+    if (overlap && !in_place)
+        return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) +
+                                                  ": the new pool overlaps the old one (only a shrink in place, same "
+                                                  "base and stride, may)");
+    std::vector<int32_t> moves((size_t)c->L * new_S);
+    for (int l = 0; l < c->L; ++l) plan_layer(c, l, new_S, moves.data() + (size_t)l * new_S);
+    ft_status st = FT_OK;
+    std::string err;
+    if (in_place) {
+        // Moves in ascending (layer, new slot) order on one stream, one slot per copy: new index l*new_S + i is
+        // never above the source l*S + q (i <= q, new_S <= S) and sources only grow, so no copy overwrites a
+        // source still unread, and same-stride slots never partly overlap.
+        for (int l = 0; l < c->L && st == FT_OK; ++l)
+            for (int i = 0; i < new_S && st == FT_OK; ++i) {
+                const int q = moves[(size_t)l * new_S + i];
+                if (q < 0) continue;
+                const uint8_t* src = c->slots + ((size_t)l * c->S + q) * c->slot_stride;
+                uint8_t* dst = nb + ((size_t)l * new_S + i) * new_slot_stride;
+                if (src == dst) continue;
+                if (c->fills++ == c->fail_at_fill) {
+                    st = FT_ERR_CUDA;
+                    err = "injected copy failure";
+                    break;
+                }
+                const cudaError_t e =
+                    cudaMemcpyAsync(dst, src, c->expert_bytes, cudaMemcpyDeviceToDevice, ft::cu(stream));
+                if (e != cudaSuccess) {
+                    st = FT_ERR_CUDA;
+                    err = std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e);
+                }
+            }
+    } else {
+        // Disjoint pools: all moves are independent, so one copy kernel per kMovesPerLaunch of them (a
+        // cudaMemcpyAsync per expert pays a fixed cost of several microseconds, about what its bytes take).
+        SlotMoves mv;
+        int n = 0;
+        const unsigned chunks = (unsigned)((c->expert_bytes + kMoveChunk - 1) / kMoveChunk);
+        auto flush = [&]() {
+            if (n == 0) return;
+            if (c->fills++ == c->fail_at_fill) {
+                st = FT_ERR_CUDA;
+                err = "injected copy failure";
+                return;
+            }
+            k_slot_moves<<<dim3(chunks, (unsigned)n), 256, 0, ft::cu(stream)>>>(c->slots, c->slot_stride, nb,
+                                                                               new_slot_stride, c->expert_bytes, mv);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) {
+                st = FT_ERR_CUDA;
+                err = std::string("slot move kernel: ") + cudaGetErrorString(e);
+            }
+            n = 0;
+        };
+        for (int l = 0; l < c->L && st == FT_OK; ++l)
+            for (int i = 0; i < new_S && st == FT_OK; ++i) {
+                const int q = moves[(size_t)l * new_S + i];
+                if (q < 0) continue;
+                mv.src[n] = l * c->S + q;
+                mv.dst[n] = l * new_S + i;
+                if (++n == kMovesPerLaunch) flush();
+            }
+        if (st == FT_OK) flush();
+    }
+    // the new geometry in either case; after a failed move no slot is trusted and every access refills from host
+    for (int l = 0; l < c->L; ++l) {
+        std::vector<int32_t> eo(new_S, -1);
+        std::vector<int64_t> sp(new_S, -1);
+        if (st == FT_OK)
+            for (int i = 0; i < new_S; ++i) {
+                const int q = moves[(size_t)l * new_S + i];
+                if (q < 0) continue;
+                eo[i] = c->expert_of[l][q];
+                sp[i] = c->stamp[l][q];
+            }
+        std::fill(c->slot_of[l].begin(), c->slot_of[l].end(), -1);
+        for (int i = 0; i < new_S; ++i)
+            if (eo[i] >= 0) c->slot_of[l][eo[i]] = i;
+        c->expert_of[l].swap(eo);
+        c->stamp[l].swap(sp);
+    }
+    c->S = new_S;
+    c->slots = nb;
+    c->slot_stride = new_slot_stride;
+    if (st != FT_OK) return cache_fail(st, std::string(fn) + ": " + err + " (the cache is now empty)");
+    for (int l = 0; l < c->L; ++l) {
+        st = publish_locked(c, l, ft::cu(stream), fn);
+        if (st != FT_OK) return st;
+    }
     return FT_OK;
 }
 

@@ -218,6 +218,24 @@ class ExpertSlotPool:
     def layer_weights(self, layer: int) -> "SlotLayerWeights":
         return SlotLayerWeights(self, layer)
 
+    def resize(self, new_S: int, in_place: bool = False, stream=None) -> None:
+        """Elastic resize at a safe point: the cache becomes new_S slots per layer, rebuilt from the experts already
+        in VRAM (device-to-device; the least recently used leave when it shrinks).  A new pool is allocated unless
+        ``in_place`` (a shrink that compacts the current pool and frees nothing).  The caller orders every fill and
+        every kernel that reads the current pool before ``stream`` (default: the current stream)."""
+        stream = torch.cuda.current_stream(self.device) if stream is None else stream
+        if in_place:
+            if new_S > self.S:
+                raise ValueError("only a shrink can be done in place")
+            new_pool = self.slots
+        else:
+            new_pool = torch.empty(self.L * new_S * self.slot_stride, dtype=torch.uint8, device=self.device)
+        old_pool = self.slots
+        self.cache.resize(new_S, new_pool.data_ptr(), self.slot_stride, stream=stream)
+        self.S, self.slots = new_S, new_pool
+        if old_pool is not new_pool:
+            old_pool.record_stream(stream)  # kept alive until the moves on `stream` have read it
+
 
 class SlotLayerWeights:
     """Descriptor of one layer's cache slots for the FFN kernels (decode-tile layout)."""
@@ -225,9 +243,12 @@ class SlotLayerWeights:
     def __init__(self, pool: ExpertSlotPool, layer: int):
         self.pool, self.layer = pool, layer
         self.E, self.H, self.I = pool.E, pool.H, pool.I
-        self.n = pool.S
         self.layout = FT_LAYOUT_DECODE_TILES
         self.device = pool.device
+
+    @property
+    def n(self) -> int:  # the pool's current slot count (it changes on a resize)
+        return self.pool.S
 
     def desc(self) -> ft_moe_layer_weights:
         p = self.pool

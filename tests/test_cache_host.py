@@ -74,3 +74,56 @@ def test_injected_fill_failure_is_reported_without_touching_the_device():
     with pytest.raises(Q.FtError) as ei:
         c.fill(1, e, s, stream=0)   # the legacy default stream handle; no torch device lookup
     assert ei.value.status == Q.FT_ERR_CUDA and "injected" in str(ei.value)
+
+
+def test_resize_plan_matches_oracle_along_the_stream():
+    """The library's resize plan (pure host) against the oracle's, at several points of the cache stream and for
+    shrinking, equal and growing sizes, on three layers."""
+    cfg = W.scaled(W.CONFIGS["cache_stream"], steps=120)
+    L = 3
+    c = fake_cache(L, cfg.E, cfg.slots)
+    oracles = [LayerLRU(cfg.slots) for _ in range(L)]
+    sets = [W.cache_stream_sets(cfg, l, 120) for l in range(L)]
+    for s in range(120):
+        for l in range(L):
+            c.lookup(l, s, list(sets[l][s]))
+            oracles[l].access(s, list(sets[l][s]))
+        if s in (0, 3, 17, 60, 119):
+            for n in (8, 9, 20, 32, 40, 128):
+                want = []
+                for o in oracles:
+                    probe = LayerLRU(o.slots)
+                    probe.expert_of, probe.stamp, probe.slot_of = list(o.expert_of), list(o.stamp), dict(o.slot_of)
+                    want.append(probe.resize(n))
+                assert c.resize_plan(n) == want, (s, n)
+
+
+def test_resize_rejects_overlapping_pools_and_bad_sizes():
+    c = fake_cache(2, 16, 4)          # pool at 0x40000000, 2 layers x 4 slots x 4096 B
+    c.lookup(0, 0, [1, 2])
+    for args in ((8, 0x40000000 + 4096, 4096),   # overlaps and is not a shrink in place
+                 (8, 0x40000000, 4096),          # same base but growing
+                 (0, 0x50000000, 4096),          # no slots
+                 (17, 0x50000000, 4096),         # more slots than experts
+                 (4, 0x50000000, 1000)):         # stride below expert_bytes / unaligned
+        with pytest.raises(Q.FtError) as ei:
+            c.resize(*args, stream=0)
+        assert ei.value.status == Q.FT_ERR_INVALID_ARG, args
+    assert c.lookup(0, 1, [1, 2])[1] == []   # nothing changed: both still resident
+
+
+def test_injected_move_failure_empties_the_cache_with_the_new_geometry():
+    """A move that cannot be enqueued (host-side hook, before any CUDA call) leaves an empty cache of the new size,
+    so every access refills from host memory."""
+    c = fake_cache(2, 16, 4)
+    c.lookup(0, 0, [1, 2, 3])
+    c.lookup(1, 0, [4])
+    c.inject_fill_failure(0)
+    with pytest.raises(Q.FtError) as ei:
+        c.resize(2, 0x50000000, 4096, stream=0)   # a disjoint pool: every kept expert needs a move
+    assert ei.value.status == Q.FT_ERR_CUDA and "injected" in str(ei.value)
+    c.inject_fill_failure(-1)
+    assert c.lookup(0, 1, [2, 3]) == ([0, 1], [(2, 0), (3, 1)])
+    assert c.lookup(1, 1, [4])[1] == [(4, 0)]
+    with pytest.raises(Q.FtError):
+        c.lookup(0, 2, [5, 6, 7])             # n > the new slot count

@@ -117,3 +117,58 @@ def test_injected_fill_failure_leaves_the_device_usable(pool_and_resident):
     s.synchronize()
     assert Q.ft_device_status() == 0
     c.close()
+
+
+def test_elastic_resize_keeps_the_cached_stream_exact(pool_and_resident):
+    """The cached decode stream with three resizes at safe points: a shrink into a new pool, a growth into a new
+    pool, and a shrink compacted in place.  At each resize the plan equals the oracle's, every kept slot holds its
+    expert's bytes (moved device to device, not reloaded), the published tables map exactly the kept experts, and
+    the stream goes on with misses as the oracle predicts and outputs bit-equal to the resident weights."""
+    _, resident = pool_and_resident
+    cfg = CFG
+    pool = ExpertSlotPool(cfg.layers, cfg.E, cfg.H, cfg.I, cfg.slots, DEV)
+    for l in range(cfg.layers):
+        pool.load_layer(l, resident[l])
+    layers = [CachedDecodeLayer(pool, l, cfg.k, cfg.T) for l in range(cfg.layers)]
+    ref_mods = [FusedDecodeLayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV) for _ in range(cfg.layers)]
+    oracles = [LayerLRU(cfg.slots) for _ in range(cfg.layers)]
+    resizes = {6: (16, False), 12: (40, False), 18: (12, True)}
+    stream = torch.cuda.current_stream()
+    _, _, filled0 = pool.cache.stats()
+    for step in range(cfg.steps):
+        if step in resizes:
+            n, in_place = resizes[step]
+            torch.cuda.synchronize()   # safe point: fills and layer kernels are done
+            plan = pool.cache.resize_plan(n)
+            assert plan == [o.resize(n) for o in oracles], step
+            pool.resize(n, in_place=in_place, stream=stream)
+            torch.cuda.synchronize()
+            _, _, filled = pool.cache.stats()
+            assert filled == filled0   # no host bytes moved by a resize
+            tables = pool.tables.cpu().numpy()
+            for l, o in enumerate(oracles):
+                want_table = np.full(cfg.E, -1, np.int32)
+                for i, e in enumerate(o.expert_of):
+                    if e < 0:
+                        continue
+                    want_table[e] = i
+                    off = (l * n + i) * pool.slot_stride
+                    assert torch.equal(pool.slots[off:off + pool.expert_bytes].cpu(), pool.host_expert(l, e)), (step, l, i)
+                assert np.array_equal(tables[l], want_table), (step, l)
+        for l in range(cfg.layers):
+            logits_np = W.router_logits(cfg, l, step)
+            x_np = W.activations_bf16(cfg, l, step)
+            logits = torch.from_numpy(logits_np).to(DEV)
+            x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(DEV)
+            out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)
+            misses = layers[l](logits, x, out, step, stream=stream)
+            ref = torch.empty_like(out)
+            ref_mods[l](resident[l], logits, x, ref)
+            torch.cuda.synchronize()
+            assert Q.ft_device_status() == 0
+            ids = sorted(W.cache_stream_sets(cfg, l, step + 1)[step])
+            _, want_misses = oracles[l].access(step, ids)
+            assert misses == [tuple(m) for m in want_misses], (step, l)
+            assert torch.equal(out, ref), (step, l)
+        _, _, filled0 = pool.cache.stats()
+    assert pool.S == 12

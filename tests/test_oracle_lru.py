@@ -44,3 +44,47 @@ def test_invariants_on_cache_stream():
         hits += len(ids) - len(misses)
         prev = set(ids)
     assert hits > 0.5 * 8 * 300
+
+
+def test_resize_hand_worked():
+    """Worked by hand from the resize reading: keep the newest experts (lower old slot on equal stamps), in old-slot
+    order, with their stamps."""
+    c = LayerLRU(3)
+    c.access(0, [1, 2])    # 1 -> slot 0, 2 -> slot 1
+    c.access(1, [3])       # 3 -> slot 2
+    c.access(2, [1])       # hit: slot 0 stamp 2
+    c.access(3, [4, 2])    # 2 hit (stamp 3); 4 evicts expert 3 (slot 2, stamp 1)
+    assert c.expert_of == [1, 2, 4] and c.stamp == [2, 3, 3]
+    assert c.resize(2) == [1, 2]            # stamps 3, 3 beat 2; kept in old-slot order
+    assert c.expert_of == [2, 4] and c.stamp == [3, 3] and c.slot_of == {2: 0, 4: 1}
+    assert c.resize(4) == [0, 1, -1, -1]    # growing keeps everything in place
+    assert c.access(4, [7]) == ([2], [(7, 2)])   # the lowest free slot
+    assert c.resize(1) == [2]               # expert 7 (stamp 4) is the newest
+    assert c.expert_of == [7] and c.access(5, [7]) == ([0], [])
+
+
+def test_resize_ties_go_to_the_lower_old_slot():
+    c = LayerLRU(4)
+    c.access(0, [10, 11, 12, 13])   # one step: all four stamps equal
+    assert c.resize(2) == [0, 1] and c.expert_of == [10, 11]
+
+
+def test_resize_keeps_the_policy_on_a_long_stream():
+    """After any resize the survivors are exactly the most recently used residents, and the model keeps serving
+    accesses with the usual invariants (every id resident after its access, at most `slots` residents)."""
+    cfg = W.scaled(W.CONFIGS["cache_stream"], steps=240)
+    sets = W.cache_stream_sets(cfg, 1, 240)
+    c = LayerLRU(cfg.slots)
+    sizes = {40: 12, 80: 32, 120: 8, 160: 64, 200: 16}
+    for s, ids in enumerate(sets):
+        if s in sizes:
+            before = {c.expert_of[q]: c.stamp[q] for q in range(c.slots) if c.expert_of[q] >= 0}
+            n = sizes[s]
+            c.resize(n)
+            after = {e for e in c.expert_of if e >= 0}
+            assert len(after) == min(n, len(before))
+            if after:
+                assert min(before[e] for e in after) >= max((before[e] for e in before if e not in after), default=-1)
+        got, _ = c.access(s, list(ids))
+        assert all(c.expert_of[q] == e for q, e in zip(got, ids))
+        assert len(c.slot_of) <= c.slots
