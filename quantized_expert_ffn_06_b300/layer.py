@@ -130,6 +130,87 @@ class PrefillLayer:
         return out
 
 
+class StreamedPrefill:
+    """Prefill through L layers whose NVFP4 experts live in pinned host memory, double-buffered.
+
+    The experts of layer l+1 are copied host -> device on a side stream into one of two device buffers while layer
+    l computes from the other; events order each copy after the layer that last read its buffer, and each layer
+    after its copy.  Each expert is one contiguous block in the tensor-core tile layout,
+        [gate/up blocks: 2I*H*9/16 bytes][down blocks: H*I*9/16 bytes][tensor scales: 4 floats],
+    at a 256-byte stride, in the host pool and in a buffer alike, so a layer moves as one copy.
+    """
+
+    def __init__(self, L: int, E: int, H: int, I: int, k: int, T: int, device):
+        self.L, self.E, self.H, self.I, self.k, self.T = L, E, H, I, k, T
+        self.device = torch.device(device)
+        self.gu_bytes = 2 * I * H * 9 // 16
+        self.d_bytes = H * I * 9 // 16
+        self.expert_bytes = self.gu_bytes + self.d_bytes + 16
+        self.slot_stride = (self.expert_bytes + 255) // 256 * 256
+        self.layer_bytes = E * self.slot_stride
+        self.host = torch.empty(L * self.layer_bytes, dtype=torch.uint8, pin_memory=True)
+        self.bufs = [torch.empty(self.layer_bytes, dtype=torch.uint8, device=self.device) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device=self.device)
+        self.landed = [torch.cuda.Event() for _ in range(2)]  # the layer assigned to buffer b is on the device
+        self.freed = [torch.cuda.Event() for _ in range(2)]   # the layer that last read buffer b has finished
+        self.layer = PrefillLayer(E, H, I, k, T, self.device)
+
+    def load_layer(self, layer: int, lw: LayerWeights) -> None:
+        """Copy the E experts of a device LayerWeights (tensor-core tile layout) into the host pool."""
+        assert lw.layout == FT_LAYOUT_UMMA_TILES and lw.n >= self.E
+        g, d, eb = self.gu_bytes, self.d_bytes, self.expert_bytes
+        stage = torch.zeros((self.E, self.slot_stride), dtype=torch.uint8, device=lw.device)
+        stage[:, :g].copy_(lw.gu_codes[:self.E])
+        stage[:, g:g + d].copy_(lw.d_codes[:self.E])
+        stage[:, g + d:eb].copy_(lw.tscale[:self.E].view(torch.uint8))
+        off = layer * self.layer_bytes
+        self.host[off:off + self.layer_bytes].view(self.E, self.slot_stride).copy_(stage)  # device -> pinned
+        torch.cuda.synchronize(lw.device)
+
+    def buffer_weights(self, b: int) -> "_BufferWeights":
+        return _BufferWeights(self, b)
+
+    def _issue_copy(self, layer: int) -> None:
+        b = layer % 2
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.freed[b])
+            off = layer * self.layer_bytes
+            self.bufs[b].copy_(self.host[off:off + self.layer_bytes], non_blocking=True)
+            self.landed[b].record(self.copy_stream)
+
+    def __call__(self, logits, xs, outs, stream=None):
+        """Layer l reads logits[l] [T, E] fp32 and xs[l] [T, H] bf16 and writes outs[l] [T, H] bf16."""
+        stream = torch.cuda.current_stream(self.device) if stream is None else stream
+        self._issue_copy(0)
+        for l in range(self.L):
+            if l + 1 < self.L:
+                self._issue_copy(l + 1)  # overlaps this layer's compute
+            stream.wait_event(self.landed[l % 2])
+            self.layer(self.buffer_weights(l % 2), logits[l], xs[l], outs[l], stream=stream)
+            self.freed[l % 2].record(stream)
+        return outs
+
+
+class _BufferWeights:
+    """Descriptor of the experts in one StreamedPrefill buffer (tensor-core tile layout, no slot table)."""
+
+    def __init__(self, sp: StreamedPrefill, b: int):
+        self.sp, self.b = sp, b
+        self.E, self.H, self.I, self.n = sp.E, sp.H, sp.I, sp.E
+        self.layout = FT_LAYOUT_UMMA_TILES
+        self.device = sp.device
+
+    def desc(self) -> ft_moe_layer_weights:
+        sp = self.sp
+        d = ft_moe_layer_weights()
+        d.E, d.H, d.I, d.n_weights, d.layout = sp.E, sp.H, sp.I, sp.E, FT_LAYOUT_UMMA_TILES
+        base = sp.bufs[self.b].data_ptr()
+        d.gu_codes, d.gu_codes_stride = base, sp.slot_stride
+        d.d_codes, d.d_codes_stride = base + sp.gu_bytes, sp.slot_stride
+        d.tscale, d.tscale_stride = base + sp.gu_bytes + sp.d_bytes, sp.slot_stride // 4
+        return d
+
+
 class MoEDecodeLayer:
     """route -> permute -> decode expert FFN (+ combine) as separate C-ABI calls, buffers allocated once."""
 

@@ -156,3 +156,31 @@ def test_offsets_that_do_not_partition_the_rows_are_reported_and_add_nothing(cas
     # the workspace stays usable: a valid call after the failed one is exact again
     mod2, out2 = run(cfg, lw, logits, x_bits)
     check(cfg, 0, mod2, out2, logits, x_bits)
+
+
+def test_streamed_layers_equal_resident_weights():
+    """Three layers of a k = 2 prefill whose experts stream from pinned host memory through two device buffers,
+    called twice: every layer's output equals, bit for bit, the same call on resident weights (with k = 2 each
+    output element receives two fp32 additions onto zero, so their order cannot matter), and layer 0 also agrees
+    with the oracle."""
+    from quantized_expert_ffn_06_b300.layer import StreamedPrefill
+    cfg = W.scaled(W.CONFIGS["tiny"], T=200)
+    L = 3
+    lws = [weights(cfg, l) for l in range(L)]
+    sp = StreamedPrefill(L, cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV)
+    for l in range(L):
+        sp.load_layer(l, lws[l])
+    logits = [W.router_logits(cfg, l, 5) for l in range(L)]
+    xs = [W.activations_bf16(cfg, l, 5) for l in range(L)]
+    lg_d = [to_dev(a) for a in logits]
+    x_d = [to_dev(a.view(np.int16), torch.bfloat16) for a in xs]
+    for call in range(2):
+        outs = [torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+        sp(lg_d, x_d, outs)
+        torch.cuda.synchronize()
+        assert Q.ft_device_status() == 0
+        for l in range(L):
+            mod, ref = run(cfg, lws[l], logits[l], xs[l])
+            assert torch.equal(outs[l], ref), (call, l)
+            if l == 0 and call == 0:
+                check(cfg, 0, mod, outs[0], logits[0], xs[0])
