@@ -141,6 +141,23 @@ def dist_env():
     return ws, rank, local
 
 
+def init_dist(ws: int) -> None:
+    """One process per GPU: NCCL when CUDA is present, gloo otherwise (the host logic's CPU tests)."""
+    if ws > 1:
+        import torch
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The slowest rank's time: replicas run independent work, so the job takes as long as its slowest rank."""
+    if ws <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
 # --------------------------------------------------------------------------- oracle (CPU baseline)
 
 class OracleDecode:
@@ -332,10 +349,7 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.synchronize()
     barrier()
     ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks(ms, ws, dev)
     value = args.steps * T * ws / (ms / 1e3)
     assert Q.ft_device_status(stream) == 0
 
@@ -385,10 +399,7 @@ def run_gpu(args, ws, rank, local):
             e1.record(stream)
         e1.synchronize()
         ems = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = t.item()
+        ems = max_over_ranks(ems, ws, dev)
         e2e = {"value": args.steps * T * ws / (ems / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": L * T * (H * 2 + E * 4), "d2h_bytes_per_step": L * T * H * 2}
 
@@ -492,10 +503,7 @@ def run_gpu_prefill(args, ws, rank, local):
         ev1.synchronize()
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks(ms, ws, dev)
     assert Q.ft_device_status(stream) == 0
     step_s = ms / 1e3 / args.steps
     # the expert FFN call alone (its kernels: plan, x quantisation, two grouped GEMMs, output), live, same stream
@@ -652,10 +660,7 @@ def run_gpu_prefill_stream(args, ws, rank, local):
             e1.record(stream)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks(ms, ws, dev)
     assert Q.ft_device_status(stream) == 0
     step_s = ms / 1e3 / args.steps
     flops = 6.0 * H * I * T * k * L
@@ -758,10 +763,7 @@ def run_gpu_cache(args, ws, rank, local):
             e1.record(stream)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks(ms, ws, dev)
     assert Q.ft_device_status(stream) == 0
     h1, m1, b1 = pool.cache.stats()
     hits, misses, filled = h1 - h0, m1 - m0, b1 - b0
@@ -860,9 +862,7 @@ def main():
         print(json.dumps(line))
         return
 
-    if ws > 1:
-        import torch
-        torch.distributed.init_process_group("nccl")
+    init_dist(ws)
     if cfg.routing == "stream":
         res = run_gpu_cache(args, ws, rank, local)
         if rank == 0:
