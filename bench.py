@@ -238,6 +238,42 @@ def oracle_prefill_baseline(cfg, n_rows: int = 16):
                       f"of {n_rows} tokens (weight quantisation untimed)"}
 
 
+class OraclePrefill:
+    """The CPU oracle (A4 mode) on the prefill layer, a few tokens per step: the routing of all T tokens and the
+    quantisation of the experts a step needs happen untimed; each timed step runs route, permute, the fp64 expert
+    FFN and the combine for `rows` tokens."""
+
+    def __init__(self, cfg, rows: int = 2):
+        import oracle as O
+        self.O, self.cfg, self.rows = O, cfg, rows
+        self.logits = W.router_logits(cfg, 0, 0)
+        self.x_bits = W.activations_bf16(cfg, 0, 0)
+        self.ids, _ = O.route(self.logits, cfg.k)
+        self.q = {}
+
+    def _expert(self, e):
+        O = self.O
+
+        class _Deq:
+            def __init__(self, t):
+                self.Wg, self.Wu, self.Wd = (O.dequantize(*a) for a in t)
+
+        return _Deq(self.q[e])
+
+    def step(self, s: int) -> float:
+        T = self.cfg.T
+        rows = np.array([(s * self.rows + i) % T for i in range(self.rows)])
+        for e in sorted(set(self.ids[rows].ravel().tolist())):
+            if e not in self.q:
+                self.q[e] = [self.O.quantize_weight(W.weights_fp32(self.cfg, 0, e, p)) for p in range(3)]
+        t0 = time.perf_counter()
+        self.O.moe_layer(self.logits, self.x_bits, self.cfg.k, self._expert, self.O.MODE_A4, rows=rows)
+        return time.perf_counter() - t0
+
+    def threads(self) -> int:
+        return self.O.lib().ora_max_threads()
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def kernel_source_hash() -> str:
@@ -878,6 +914,27 @@ def main():
 
     if args.impl == "reference":
         if rank != 0:
+            return
+        if cfg.routing == "zipf":
+            # the prefill workload: the oracle's FLOP rate on a few tokens per step, in the GPU arm's unit
+            ref = OraclePrefill(cfg)
+            for s in range(args.warmup):
+                ref.step(10_000 + s)
+            secs = sum(ref.step(s) for s in range(args.steps))
+            flops = 6.0 * cfg.H * cfg.I * cfg.k * ref.rows * args.steps
+            val = flops / secs / 1e12
+            layer_ms = secs / (ref.rows * args.steps) * cfg.T * 1e3
+            line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": 1,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": layer_ms, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                    "data": "synthetic (seeded Philox4x32-10, Zipf(1.1) expert popularity)",
+                    "config": {"workload": cfg.name},
+                    "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": ref.threads(), "kind": "oracle",
+                                     "sample": f"each step: route and permute of all {cfg.T} tokens, then the fp64 "
+                                               f"A4-mode expert FFN and combine of {ref.rows} tokens (expert "
+                                               f"quantisation untimed); ms_per_step scales that to {cfg.T} tokens"},
+                    "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            print(json.dumps(line))
             return
         # the oracle as it stands on the host cores; one bench step = one routed expert of one token in
         # layer 0 (route + permute + that expert's dequantisation and FFN, scaled by k), so that a full

@@ -80,3 +80,12 @@ def test_reference_arm_under_two_ranks_prints_one_line_from_rank_0():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_on_the_prefill_workload_reports_the_gpu_arms_unit():
+    r = subprocess.run([sys.executable, "bench.py", "--config", "prefill_35b", "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["config"]["workload"] == "prefill_35b" and d["cpu_baseline"]["kind"] == "oracle"
