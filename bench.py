@@ -160,6 +160,36 @@ def max_over_ranks(ms: float, ws: int, device) -> float:
 
 # --------------------------------------------------------------------------- oracle (CPU baseline)
 
+def host_info() -> dict:
+    """The host the CPU oracle runs on: CPU model, logical CPUs, and the CPUs this process may use."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        affinity = os.cpu_count()
+    return {"cpu_model": model, "nproc": os.cpu_count(), "affinity": affinity}
+
+
+def single_thread_rate(step, n: int, units_per_step: float, first: int = 20_000) -> float:
+    """Units per second of `step` (returns its timed seconds) on one oracle thread over n steps."""
+    import oracle as O
+    threads = O.lib().ora_max_threads()
+    O.set_threads(1)
+    try:
+        secs = sum(step(first + s) for s in range(n))
+    finally:
+        O.set_threads(threads)
+    return units_per_step * n / secs
+
+
 class OracleDecode:
     """The CPU oracle on decode steps of one layer of the workload.
 
@@ -235,7 +265,7 @@ def oracle_prefill_baseline(cfg, n_rows: int = 16):
     return {"value": n_rows / secs, "unit": "tok/s", "tflops": 6.0 * cfg.H * cfg.I * cfg.k * n_rows / secs / 1e12,
             "cores": O.lib().ora_max_threads(), "kind": "oracle",
             "sample": f"route and permute of all {cfg.T} tokens, then fp64 dequantisation, A4-mode FFN and combine "
-                      f"of {n_rows} tokens (weight quantisation untimed)"}
+                      f"of {n_rows} tokens (weight quantisation untimed)", **host_info()}
 
 
 class OraclePrefill:
@@ -993,7 +1023,10 @@ def main():
             res["cpu_baseline"] = {"value": cfg.T / per_token, "unit": UNIT, "cores": ref.threads(), "kind": "oracle",
                                    "sample": f"{args.cpu_steps} single-token steps of layer 0 (route, permute, fp64 "
                                              f"dequantisation, FFN, combine), scaled to {cfg.layers} layers; "
-                                             f"weight generation and quantisation untimed"}
+                                             f"weight generation and quantisation untimed",
+                                   "single_thread": {"value": single_thread_rate(ref.step, 4, cfg.T / cfg.layers),
+                                                     "unit": UNIT, "sample": "4 such steps on one thread"},
+                                   **host_info()}
         print(json.dumps(res))
     if ws > 1:
         import torch
