@@ -349,9 +349,11 @@ FT_API ft_status ft_expert_cache_stats(ft_expert_cache* cache, int64_t* hits, in
  * old pool and every kernel reading it must be ordered before `stream`; the
  * old pool must stay allocated until `stream` passes this call.  new_slots may
  * overlap the old pool only as a shrink in place (same base and stride,
- * new_S <= S); any other overlap is FT_ERR_INVALID_ARG.  If a move cannot be
- * enqueued the call returns FT_ERR_CUDA and the cache is empty with the new
- * geometry (nothing published: publish each layer before its next use).
+ * new_S <= S); any other overlap is FT_ERR_INVALID_ARG.  FT_ERR_INVALID_ARG
+ * is returned before any change; every other error leaves the handle on the
+ * new pool: if a move cannot be enqueued (FT_ERR_CUDA) the cache is empty and
+ * nothing is published; if a table publish fails the moves stand.  Either way
+ * publish each layer before its next use.
  * A lookup after a shrink needs n <= new_S. */
 FT_API ft_status ft_expert_cache_resize(ft_expert_cache* cache, int new_S, void* new_slots, size_t new_slot_stride,
                                         ft_stream_t stream);

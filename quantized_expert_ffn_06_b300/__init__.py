@@ -334,11 +334,11 @@ class ExpertCacheHandle:
     def resize(self, new_S: int, new_slots_ptr: int, new_slot_stride: int, stream=None):
         """Rebuild the cache as new_S slots per layer in a caller-owned device pool (device-to-device moves and the
         publish of every layer's table, on `stream`)."""
-        try:
-            _check(_lib.ft_expert_cache_resize(self.h, new_S, new_slots_ptr, new_slot_stride, _s(stream)))
-        finally:
-            # the handle has the new geometry whether or not every move was enqueued
+        rc = _lib.ft_expert_cache_resize(self.h, new_S, new_slots_ptr, new_slot_stride, _s(stream))
+        if rc != FT_ERR_INVALID_ARG:
+            # only a rejected argument leaves the old geometry; any later failure leaves the handle on the new pool
             self.S = new_S
+        _check(rc)
 
 
 from .layer import FusedDecodeLayer, LayerWeights, MoEDecodeLayer  # noqa: E402,F401

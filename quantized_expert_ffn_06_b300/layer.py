@@ -311,8 +311,18 @@ class ExpertSlotPool:
             new_pool = self.slots
         else:
             new_pool = torch.empty(self.L * new_S * self.slot_stride, dtype=torch.uint8, device=self.device)
+        from . import FT_ERR_INVALID_ARG, FtError
         old_pool = self.slots
-        self.cache.resize(new_S, new_pool.data_ptr(), self.slot_stride, stream=stream)
+        try:
+            self.cache.resize(new_S, new_pool.data_ptr(), self.slot_stride, stream=stream)
+        except FtError as e:
+            if e.status == FT_ERR_INVALID_ARG:
+                raise  # rejected before any change: the cache still uses the current pool
+            self._adopt(new_S, new_pool, old_pool, stream)  # the handle is on the new pool either way
+            raise
+        self._adopt(new_S, new_pool, old_pool, stream)
+
+    def _adopt(self, new_S, new_pool, old_pool, stream) -> None:
         self.S, self.slots = new_S, new_pool
         if old_pool is not new_pool:
             old_pool.record_stream(stream)  # kept alive until the moves on `stream` have read it

@@ -109,7 +109,7 @@ def test_resize_rejects_overlapping_pools_and_bad_sizes():
         with pytest.raises(Q.FtError) as ei:
             c.resize(*args, stream=0)
         assert ei.value.status == Q.FT_ERR_INVALID_ARG, args
-    assert c.lookup(0, 1, [1, 2])[1] == []   # nothing changed: both still resident
+    assert c.S == 4 and c.lookup(0, 1, [1, 2])[1] == []   # nothing changed: both still resident
 
 
 def test_injected_move_failure_empties_the_cache_with_the_new_geometry():
@@ -122,6 +122,7 @@ def test_injected_move_failure_empties_the_cache_with_the_new_geometry():
     with pytest.raises(Q.FtError) as ei:
         c.resize(2, 0x50000000, 4096, stream=0)   # a disjoint pool: every kept expert needs a move
     assert ei.value.status == Q.FT_ERR_CUDA and "injected" in str(ei.value)
+    assert c.S == 2   # the handle is on the new pool
     c.inject_fill_failure(-1)
     assert c.lookup(0, 1, [2, 3]) == ([0, 1], [(2, 0), (3, 1)])
     assert c.lookup(1, 1, [4])[1] == [(4, 0)]
