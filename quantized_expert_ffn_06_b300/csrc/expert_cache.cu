@@ -108,7 +108,15 @@ ft_status ensure_staging(ft_expert_cache* c, const char* fn) {
     c->ring_ev.assign((size_t)c->L * c->kRing, nullptr);
     for (auto& ev : c->ring_ev) {
         e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-        if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+        if (e != cudaSuccess) {  // undo it all, so that the next publish tries again from scratch
+            ev = nullptr;
+            for (auto& made : c->ring_ev)
+                if (made) cudaEventDestroy(made);
+            c->ring_ev.clear();
+            cudaFreeHost(c->pinned);
+            c->pinned = nullptr;
+            return cache_fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+        }
     }
     return FT_OK;
 }
@@ -250,14 +258,11 @@ ft_status ft_expert_cache_fill(ft_expert_cache* c, int layer, int expert, int sl
                                ft_event_t done) {
     const char* fn = "ft_expert_cache_fill";
     if (!c) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null cache");
+    // the whole call holds the lock: a resize changes the pool, its slot count and its stride
+    std::lock_guard<std::mutex> lock(c->mu);
     if (layer < 0 || layer >= c->L || expert < 0 || expert >= c->E || slot < 0 || slot >= c->S)
         return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": layer, expert or slot out of range");
-    int64_t idx;
-    {
-        std::lock_guard<std::mutex> lock(c->mu);
-        idx = c->fills++;
-    }
-    if (idx == c->fail_at_fill) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": injected copy failure");
+    if (c->fills++ == c->fail_at_fill) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": injected copy failure");
     uint8_t* dst = c->slots + ((size_t)layer * c->S + slot) * c->slot_stride;
     cudaError_t e = cudaMemcpyAsync(dst, c->host[(size_t)layer * c->E + expert], c->expert_bytes, cudaMemcpyHostToDevice,
                                     ft::cu(copy_stream));
@@ -266,7 +271,6 @@ ft_status ft_expert_cache_fill(ft_expert_cache* c, int layer, int expert, int sl
         e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(done), ft::cu(copy_stream));
         if (e != cudaSuccess) return cache_fail(FT_ERR_CUDA, std::string(fn) + ": cudaEventRecord: " + cudaGetErrorString(e));
     }
-    std::lock_guard<std::mutex> lock(c->mu);
     c->bytes_filled += (int64_t)c->expert_bytes;
     return FT_OK;
 }
