@@ -287,7 +287,8 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, 
 
 /* [P4 MoE core mechanism] Routing-weighted combine:
  * out[t][n] = bf16( sum_{j<k} w[t][j] * y[inv[t*k+j]][n] ), fp32, j order.
- *   y (device) fp32 [T*k][H]; inv, w as above; out (device) bf16 [T][H]. */
+ *   y (device) fp32 [T*k][H]; inv, w as above; out (device) bf16 [T][H].
+ * An inv entry outside [0, T*k) sets FT_DEVERR_BAD_INDEX and adds nothing. */
 FT_API ft_status ft_moe_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H, uint16_t* out,
                          ft_stream_t stream);
 

@@ -312,13 +312,18 @@ __global__ void __launch_bounds__(1024) k_permute_place(const int32_t* __restric
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, const int32_t* __restrict__ inv,
                                                  const float* __restrict__ w, int T, int k, int H,
                                                  uint16_t* __restrict__ out) {
-    const int t = blockIdx.y;
-    const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    const int t = blockIdx.x;  // tokens on x: its limit is 2^31 - 1, y's only 65535
+    const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
     if (t >= T || n >= H) return;
+    const int64_t P = (int64_t)T * k;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
         const float wj = w[(int64_t)t * k + j];
         const int p = inv[(int64_t)t * k + j];
+        if (p < 0 || p >= P) {  // not a row of y: reported, contributes nothing
+            if (n == 0) raise_dev_error(FT_DEVERR_BAD_INDEX);
+            continue;
+        }
         const float4 v = *reinterpret_cast<const float4*>(y + (int64_t)p * H + n);
         acc.x = fmaf(wj, v.x, acc.x);
         acc.y = fmaf(wj, v.y, acc.y);
@@ -399,7 +404,7 @@ ft_status ft_moe_combine(const float* y, const int32_t* inv, const float* w, int
     if (T == 0) return FT_OK;
     if (!y || !inv || !w || !out) return fail(FT_ERR_INVALID_ARG, "ft_moe_combine: null pointer");
     if (!aligned(y, 16) || !aligned(out, 8)) return fail(FT_ERR_INVALID_ARG, "ft_moe_combine: misaligned y or out");
-    const dim3 grid((H / 4 + 255) / 256, T);
+    const dim3 grid(T, (H / 4 + 255) / 256);
     k_combine<<<grid, 256, 0, cu(stream)>>>(y, inv, w, T, k, H, out);
     return check_launch("ft_moe_combine");
 }

@@ -226,3 +226,28 @@ def test_combine_parity(T, k, H):
     assert np.all(np.abs(got - pre) <= bound)
     # and the result is one of the two bf16 neighbours of the exact sum
     assert np.mean(got == out_ref) > 0.99
+
+
+def test_combine_beyond_65535_tokens():
+    """Tokens ride on the grid's x dimension, so a batch of more than 65535 tokens combines like any other
+    (k = 1 with unit weights: each output is its y row rounded to bf16)."""
+    T, k, H = 70_000, 1, 8
+    rng = np.random.default_rng(7)
+    y = rng.normal(0, 1, size=(T * k, H)).astype(np.float32)
+    inv = rng.permutation(T * k).astype(np.int32)
+    w = np.ones((T, k), np.float32)
+    out_ref, _ = O.combine(y.astype(np.float64), inv, w.astype(np.float64), T, k)
+    out = Q.ft_moe_combine(to_dev(y), to_dev(inv), to_dev(w), T, k)
+    assert Q.ft_device_status() == 0
+    assert np.array_equal(out.float().cpu().numpy().astype(np.float64), out_ref)
+
+
+def test_combine_reports_an_inv_entry_outside_the_rows():
+    T, k, H = 4, 2, 256
+    y = np.ones((T * k, H), np.float32)
+    inv = np.arange(T * k, dtype=np.int32)
+    inv[3] = T * k            # token 1, slot 1: not a row of y
+    w = np.full((T, k), 0.5, np.float32)
+    out = Q.ft_moe_combine(to_dev(y), to_dev(inv), to_dev(w), T, k).float().cpu().numpy()
+    assert Q.ft_device_status() == Q.FT_DEVERR_BAD_INDEX
+    assert np.all(out[1] == 0.5) and np.all(out[[0, 2, 3]] == 1.0)
