@@ -48,7 +48,9 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
+            # FT_ORACLE_LIB: a library built from a deliberately altered copy of ftoracle.c, loaded by the
+            # mutation test to check that the pins catch the alteration
+            L = ctypes.CDLL(os.environ.get("FT_ORACLE_LIB") or build())
             vp, i64, i32, dbl, flt, u8 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
                                           ctypes.c_float, ctypes.c_uint8)
             L.ora_e2m1_value.argtypes, L.ora_e2m1_value.restype = [u8], dbl

@@ -94,6 +94,21 @@ def test_a4_mode_on_grid_exact_activations_matches_a16_through_gate_up():
     assert np.allclose(y4, indep_deq(hq_c, hq_s, 1.0) @ ex.Wd.T, rtol=1e-12, atol=1e-14)
 
 
+def test_a4_mode_quantises_x_before_gate_up():
+    """Off the grid: A4's h on x equals A16's h on x quantised per 16 with unit scale and decoded independently,
+    and differs from A16's h on x itself."""
+    cfg = W.CONFIGS["tiny"]
+    ex = make_expert(cfg, 0, 5)
+    x = W.bf16_bits_to_f32(W.activations_bf16(cfg, 0, 4)).astype(np.float64)
+    xc, xs = O.quantize_act(x.astype(np.float32))
+    xq = indep_deq(xc, xs, 1.0)
+    h4, _ = O.expert_ffn(ex.Wg, ex.Wu, ex.Wd, x, O.MODE_A4)
+    h16q, _ = O.expert_ffn(ex.Wg, ex.Wu, ex.Wd, xq, O.MODE_A16)
+    h16, _ = O.expert_ffn(ex.Wg, ex.Wu, ex.Wd, x, O.MODE_A16)
+    assert np.array_equal(h4, h16q)
+    assert not np.array_equal(h4, h16)
+
+
 def test_a4_vs_a16_deviation_is_small_on_gaussian_inputs():
     cfg = W.CONFIGS["tiny"]
     experts = {e: make_expert(cfg, 0, e) for e in range(cfg.E)}
