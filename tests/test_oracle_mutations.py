@@ -47,6 +47,17 @@ MUTATIONS = [
      "s += w[(int64_t)t * k + (k - 1 - j)] * y"),
     ("combined output not rounded", "out[(int64_t)t * H + n] = ora_bf16_round(s);", "out[(int64_t)t * H + n] = s;"),
     ("A4 mode skips the x quantisation", "deq_vec(qc, qs, H, xa);", "memcpy(xa, xr, sizeof(double) * (size_t)H);"),
+    ("negative zero kept", "if (c == 0) return 0;", "if (c == 0 && v >= 0.0f) return 0;"),
+    ("zero tensor keeps a zero scale", "if (st == 0.0f) st = 1.0f;", "if (st < 0.0f) st = 1.0f;"),
+    ("all -inf row weighted 0", "for (int j = 0; j < k; ++j) w[(int64_t)t * k + j] = 1.0 / k;",
+     "for (int j = 0; j < k; ++j) w[(int64_t)t * k + j] = 0.0;"),
+    ("offsets not shifted", "for (int64_t f = 0; f < n; ++f) offsets[ids[f] + 1] += 1;",
+     "for (int64_t f = 0; f < n; ++f) offsets[ids[f] + (ids[f] + 1 < E)] += 1;"),
+    ("combine ignores inv", "y[(int64_t)inv[(int64_t)t * k + j] * H + n]", "y[((int64_t)t * k + j) * H + n]"),
+    ("e4m3 NaN code read as a number", "if ((b & 0x7F) == 0x7F) return NAN;", "if (b == 0xFF) return NAN;"),
+    ("bf16 overflow kept finite", "if (fabs(r) >= 0x1.0p128) return v > 0 ? INFINITY : -INFINITY;",
+     "if (fabs(r) >= 0x1.0p129) return v > 0 ? INFINITY : -INFINITY;"),
+    ("e2m1 saturates to 4", "    int c = 7;\n    if (a < 6.0) {", "    int c = 6;\n    if (a < 6.0) {"),
 ]
 
 
