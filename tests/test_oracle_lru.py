@@ -88,3 +88,15 @@ def test_resize_keeps_the_policy_on_a_long_stream():
         got, _ = c.access(s, list(ids))
         assert all(c.expert_of[q] == e for q, e in zip(got, ids))
         assert len(c.slot_of) <= c.slots
+
+
+def test_resize_keeps_survivors_in_old_slot_order():
+    """Worked by hand: stamps [1, 2, 0] make slot 1 the newest and slot 0 the next; a resize to two slots keeps
+    both and places them in their old order (slot 0's expert first), not newest first."""
+    c = LayerLRU(3)
+    c.access(0, [10, 11, 12])   # 10, 11, 12 -> slots 0, 1, 2, stamps 0
+    c.access(1, [10])           # slot 0 stamp 1
+    c.access(2, [11])           # slot 1 stamp 2
+    assert c.stamp == [1, 2, 0]
+    assert c.resize(2) == [0, 1]
+    assert c.expert_of == [10, 11] and c.stamp == [1, 2]
