@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "MoE decode tok/s and % of HBM roofline; prefill NVFP4 TFLOP/s vs peak"
+HBM_NOMINAL_GBS = 7700.0  # B300 HBM3e, nominal; the fractions use the measured copy bandwidth, this is context
 UNIT = "tok/s"
 
 
@@ -475,7 +476,8 @@ def run_gpu(args, ws, rank, local):
                          (L * float(np.mean(unique)) * cfg.expert_bytes / 1e6),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind,
+                     "peak_kind": peak_kind, "nominal_peak": HBM_NOMINAL_GBS,
+                     "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
                      "kernel": (("k_moe_decode (ft_moe_layer_decode), one launch per layer" if n_chunks == 1 else
                                  f"k_moe_decode (ft_moe_layer_decode), {n_chunks} launches per layer (token chunks "
                                  f"of {chunk}); the layer's unique-expert bytes and time shared by its launches")
