@@ -263,10 +263,18 @@ def oracle_prefill_baseline(cfg, n_rows: int = 16):
     t0 = time.perf_counter()
     O.moe_layer(logits, x_bits, cfg.k, lambda e: _Deq(q[e]), O.MODE_A4, rows=np.array(rows))
     secs = time.perf_counter() - t0
+
+    def one_thread_step(s):  # the first two of those tokens again, on one oracle thread
+        t1 = time.perf_counter()
+        O.moe_layer(logits, x_bits, cfg.k, lambda e: _Deq(q[e]), O.MODE_A4, rows=np.array(rows[:2]))
+        return time.perf_counter() - t1
+
     return {"value": n_rows / secs, "unit": "tok/s", "tflops": 6.0 * cfg.H * cfg.I * cfg.k * n_rows / secs / 1e12,
             "cores": O.lib().ora_max_threads(), "kind": "oracle",
             "sample": f"route and permute of all {cfg.T} tokens, then fp64 dequantisation, A4-mode FFN and combine "
-                      f"of {n_rows} tokens (weight quantisation untimed)", **host_info()}
+                      f"of {n_rows} tokens (weight quantisation untimed)",
+            "single_thread": {"value": single_thread_rate(one_thread_step, 1, 2.0), "unit": "tok/s",
+                              "sample": "the same for 2 tokens on one thread"}, **host_info()}
 
 
 class OraclePrefill:
