@@ -55,13 +55,52 @@ def load_peaks():
 
 # --------------------------------------------------------------------------- clocks
 
+class _NvmlLib:
+    """The few NVML calls the clock sampler needs, straight from the driver's libnvidia-ml (when the pynvml module
+    is not installed).  Read-only: nothing here changes a setting of the GPU."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, pci_bus_id: str | None):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        rc = (self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) if pci_bus_id
+              else self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)))
+        if rc != 0:
+            raise RuntimeError(f"NVML device handle: error {rc}")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _clock(self, fn) -> int:
+        v = self.c.c_uint(0)
+        if fn(self.h, self.NVML_CLOCK_SM, self.c.byref(v)) != 0:
+            raise RuntimeError("NVML clock query failed")
+        return v.value
+
+    def sm_mhz(self) -> int:
+        return self._clock(self.lib.nvmlDeviceGetClockInfo)
+
+    def max_sm_mhz(self) -> int:
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def reasons(self) -> int:
+        v = self.c.c_ulonglong(0)
+        if self.reasons_fn(self.h, self.c.byref(v)) != 0:
+            raise RuntimeError("NVML clock-event reasons query failed")
+        return v.value
+
+
 class ClockSampler:
     """Samples SM clock and clock-event reasons while the timed region runs (NVML, else nvidia-smi)."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, pci_bus_id: str | None, period_s: float = 0.02):
+    def __init__(self, pci_bus_id: str | None, period_s: float = 0.002):
         self.samples, self.reasons, self.period = [], set(), period_s
         self.max_mhz, self.how, self.err = None, None, None
         self._stop = threading.Event()
@@ -76,25 +115,39 @@ class ClockSampler:
                       else pynvml.nvmlDeviceGetHandleByIndex(0))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.how = "nvml"
-        except Exception as e:  # fall back to polling nvidia-smi
+        except Exception as e:  # the driver's NVML library directly, else polling nvidia-smi
             self.err = f"{type(e).__name__}: {e}"
-            self.how = "nvidia-smi"
+            try:
+                self.nv = _NvmlLib(pci_bus_id)
+                self.h = None
+                self.max_mhz = self.nv.max_sm_mhz()
+                self.how = "nvml (libnvidia-ml)"
+            except Exception as e2:
+                self.err += f"; {type(e2).__name__}: {e2}"
+                self.how = "nvidia-smi"
 
     def _run_nvml(self):
         nv = self.nv
-        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        while not self._stop.is_set():
+        if isinstance(nv, _NvmlLib):
+            sm, reasons = nv.sm_mhz, nv.reasons
+        else:
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            sm = lambda: nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)  # noqa: E731
+            reasons = lambda: fn(self.h)  # noqa: E731
+        while True:
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                mask = fn(self.h)
+                self.samples.append(sm())
+                mask = reasons()
                 self.reasons |= {name for bit, name in self.REASONS.items() if mask & bit}
             except Exception as e:
                 self.err = f"{type(e).__name__}: {e}"
+            if self._stop.is_set():  # one sample after the timed region as well
+                break
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.how == "nvml":
+        if self.how.startswith("nvml"):
             self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
         else:
@@ -239,6 +292,59 @@ class OracleDecode:
         Wg, Wu, Wd = (O.dequantize(*a) for a in self.q[e])
         O.expert_ffn(Wg, Wu, Wd, x, O.MODE_A16)
         return t_route + (time.perf_counter() - t0) * cfg.k
+
+    def threads(self) -> int:
+        return self.O.lib().ora_max_threads()
+
+
+class OracleToken:
+    """The CPU oracle on whole decode steps: one token through every layer of the workload (route, permute,
+    fp64 dequantisation and FFN of its experts, combine), each layer with its own experts.
+
+    The experts a step needs are drawn and quantised by the oracle before the step (its inputs, untimed), on a
+    pool of host threads, and kept for later steps up to a bounded number of them."""
+
+    def __init__(self, cfg: W.MoEConfig, keep: int = 1536):
+        import concurrent.futures as cf
+
+        import oracle as O
+        self.O, self.cfg, self.keep = O, cfg, keep
+        self.q = {}
+        self.pool = cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+
+    def _quantised(self, layer: int, e: int):
+        O, cfg = self.O, self.cfg
+        return [O.quantize_weight(W.weights_fp32(cfg, layer, e, p)) for p in range(3)]
+
+    def prepare(self, s: int):
+        """Inputs of step s: logits and x of every layer, and the experts it routes to (quantised here)."""
+        O, cfg = self.O, self.cfg
+        inputs = []
+        need = []
+        for layer in range(cfg.layers):
+            logits = W.router_logits(cfg, layer, s)
+            x_bits = W.activations_bf16(cfg, layer, s)
+            ids, _ = O.route(logits, cfg.k)
+            inputs.append((logits, x_bits))
+            need += [(layer, int(e)) for e in sorted(set(ids.ravel().tolist())) if (layer, int(e)) not in self.q]
+        for key, qv in zip(need, self.pool.map(lambda le: self._quantised(*le), need)):
+            self.q[key] = qv
+        while len(self.q) > self.keep:
+            self.q.pop(next(iter(self.q)))
+        return inputs
+
+    def step(self, s: int) -> float:
+        O, cfg = self.O, self.cfg
+        inputs = self.prepare(s)
+
+        class _Deq:
+            def __init__(self, t):
+                self.Wg, self.Wu, self.Wd = (O.dequantize(*a) for a in t)
+
+        t0 = time.perf_counter()
+        for layer, (logits, x_bits) in enumerate(inputs):
+            O.moe_layer(logits, x_bits, cfg.k, lambda e, layer=layer: _Deq(self.q[(layer, e)]), O.MODE_A16)
+        return time.perf_counter() - t0
 
     def threads(self) -> int:
         return self.O.lib().ora_max_threads()
@@ -976,23 +1082,21 @@ def main():
                     "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
             print(json.dumps(line))
             return
-        # the oracle as it stands on the host cores; one bench step = one routed expert of one token in
-        # layer 0 (route + permute + that expert's dequantisation and FFN, scaled by k), so that a full
-        # token is k x layers of them
-        ref = OracleDecode(cfg)
+        # the oracle as it stands on the host cores, on whole steps: one token through all the layers
+        ref = OracleToken(cfg)
         for s in range(args.warmup):
-            ref.expert_step(10_000 + s)
-        secs = sum(ref.expert_step(s) for s in range(args.steps))
-        per_token = secs / args.steps * cfg.layers
+            ref.step(10_000 + s)
+        secs = sum(ref.step(s) for s in range(args.steps))
+        per_token = secs / args.steps
         val = cfg.T / per_token
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": per_token * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox4x32-10)",
                 "config": {"workload": cfg.name},
                 "cpu_baseline": {"value": val, "unit": UNIT, "cores": ref.threads(), "kind": "oracle",
-                                 "sample": f"each step: one routed expert of one token in layer 0 (route, permute, "
-                                           f"fp64 dequantisation and FFN of that expert x {cfg.k}), scaled to "
-                                           f"{cfg.layers} layers"},
+                                 "sample": f"each step: one token through all {cfg.layers} layers (route, permute, "
+                                           f"fp64 dequantisation and FFN of its {cfg.k} experts per layer, combine); "
+                                           f"drawing and quantising the experts untimed"},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return

@@ -85,6 +85,18 @@ FT_API const char* ft_last_error(void);
 /* Library ABI version, (major << 16) | minor. */
 FT_API int ft_version(void);
 
+/* Test hook for failure detection (off by default; affects launches made after
+ * the call, from any thread).  site FT_WAIT_SITE_DECODE_H makes the down phase
+ * of the fused decode step (ft_moe_layer_decode and the tiled
+ * ft_moe_expert_ffn_nvfp4_decode) wait for h words of a tag that no CTA
+ * writes, with every wait bounded by limit_ns (0 < limit_ns <= 2 s): the wait
+ * runs out, the kernel sets FT_DEVERR_TIMEOUT, finishes without trapping and
+ * its output is unspecified.  site FT_WAIT_SITE_NONE restores normal waits
+ * with the default 2 s bound (limit_ns ignored). */
+#define FT_WAIT_SITE_NONE 0
+#define FT_WAIT_SITE_DECODE_H 1
+FT_API ft_status ft_debug_inject_wait_expiry(int site, uint64_t limit_ns);
+
 /* Waits for `stream`, then reads and clears the current device's error word.
  * *err_word receives the FT_DEVERR_* bits; returns FT_ERR_DEVICE if any bit was
  * set, FT_ERR_CUDA if the stream reported a CUDA error, FT_OK otherwise. */
@@ -145,6 +157,48 @@ typedef struct ft_moe_layer_weights {
     const uint8_t* d_sf_tiled;
     int64_t d_sf_tiled_stride;
 } ft_moe_layer_weights;
+
+/* The layer weights handle: canonical NVFP4 expert matrices repacked, once,
+ * into the layouts the kernels read.  [P4 MoE core mechanism: each expert an
+ * independent FFN; P5 NVFP4 weights]
+ * One canonical matrix [N][K] (device memory, caller-owned): codes [N][K/2]
+ * with element 2j in the low nibble of byte j, row stride codes_ld bytes
+ * (16-byte aligned base, codes_ld a multiple of 16); E4M3 scales [N][K/16],
+ * row stride scales_ld bytes, one per 16 consecutive elements of a row; and a
+ * pointer to its fp32 tensor scale.  An expert is gate [I][H], up [I][H] and
+ * down [H][I]. */
+typedef struct ft_nvfp4_matrix {
+    const uint8_t* codes;
+    int64_t codes_ld;
+    const uint8_t* scales;
+    int64_t scales_ld;
+    const float* tensor_scale;
+} ft_nvfp4_matrix;
+typedef struct ft_nvfp4_expert_desc {
+    ft_nvfp4_matrix gate, up, down;
+} ft_nvfp4_expert_desc;
+#define FT_WEIGHTS_ROWS (1 << FT_LAYOUT_ROWS)
+#define FT_WEIGHTS_DECODE_TILES (1 << FT_LAYOUT_DECODE_TILES)
+#define FT_WEIGHTS_UMMA_TILES (1 << FT_LAYOUT_UMMA_TILES)
+typedef struct ft_moe_weights ft_moe_weights;
+/* experts (host) [E]: the canonical matrices of experts 0..E-1.  layout_flags: a
+ * non-empty set of FT_WEIGHTS_*.  The handle allocates device memory for the
+ * requested layouts (plus per-expert tensor scales {gate, up, down, 0}), copies
+ * and repacks the bytes on `stream` and returns once that work has finished, so
+ * the canonical matrices may be freed right after.  Repacking only moves bytes:
+ * kernels reading the handle compute on exactly the caller's codes and scales.
+ * Sizes: 1 <= E <= 1024, H a multiple of 256, I a multiple of 128.  Errors:
+ * FT_ERR_INVALID_ARG (checked before any CUDA call), FT_ERR_OOM (device
+ * allocation), FT_ERR_CUDA (a copy failed); *out is NULL on any error. */
+FT_API ft_status ft_moe_weights_create(const ft_nvfp4_expert_desc* experts, int E, int H, int I, int layout_flags,
+                                       ft_stream_t stream, ft_moe_weights** out);
+/* Fills *desc (host) with the descriptor of the handle's copy in `layout`
+ * (FT_LAYOUT_*), ready for the FFN and layer calls; FT_ERR_INVALID_ARG if the
+ * handle holds no copy in that layout.  The descriptor stays valid until
+ * ft_moe_weights_destroy. */
+FT_API ft_status ft_moe_weights_describe(const ft_moe_weights* w, int layout, ft_moe_layer_weights* desc);
+/* Frees the handle and its device memory (no kernel may still be reading it). */
+FT_API ft_status ft_moe_weights_destroy(ft_moe_weights* w);
 
 /* ------------------------------------------------------------------------ */
 /* Router                                                                     */
@@ -213,10 +267,12 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
  *          sum over a token's experts taken in slot order j, fp32.
  *   ids, w (device, optional, both or neither) [T][k]: the routing result.
  *   ws: ft_moe_layer_decode_workspace_size(T, k, H, I) bytes, 256-byte
- *       aligned, ZERO-FILLED before its first use.  Its first 256 bytes hold a
- *       call counter (each call adds one per CTA) that tags the h values the
- *       gate/up phase hands to the down phase; calls sharing a workspace must
- *       not overlap on the device.  After a FT_DEVERR_TIMEOUT zero it again.
+ *       aligned, ZERO-FILLED before its first use.  Its first 8 bytes hold a
+ *       64-bit call counter (each call adds one per CTA) from which the tag of
+ *       the h values the gate/up phase hands to the down phase is derived (a
+ *       32-bit tag that skips 0 and repeats only after 2^32 - 1 calls); calls
+ *       sharing a workspace must not overlap on the device.  A call whose wait
+ *       ran out (FT_DEVERR_TIMEOUT) leaves the workspace consistent.
  * 0 <= T <= 16, 1 <= k <= min(E, 32).  The activations are staged in shared
  * memory as f16: T'*(H+32) + T'*k*(I+32) halves must fit 120 KB for a launch
  * of T' tokens.  A larger batch runs as consecutive launches over the largest

@@ -24,6 +24,7 @@ FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_UNSUPPORTED, FT_ERR_TIMEOUT, FT_E
     FT_ERR_DEVICE = range(8)
 FT_LAYOUT_ROWS, FT_LAYOUT_DECODE_TILES, FT_LAYOUT_UMMA_TILES = 0, 1, 2
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX = 1, 2, 4, 8
+FT_WAIT_SITE_NONE, FT_WAIT_SITE_DECODE_H = 0, 1
 
 _vp, _i32, _i64, _u64, _sz, _dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t,
                                     ctypes.c_double)
@@ -46,6 +47,17 @@ class ft_moe_layer_weights(ctypes.Structure):
                 ("expert_to_slot", _vp),
                 ("gu_sf_tiled", _vp), ("gu_sf_tiled_stride", _i64),
                 ("d_sf_tiled", _vp), ("d_sf_tiled_stride", _i64)]
+
+
+class ft_nvfp4_matrix(ctypes.Structure):
+    _fields_ = [("codes", _vp), ("codes_ld", _i64), ("scales", _vp), ("scales_ld", _i64), ("tensor_scale", _vp)]
+
+
+class ft_nvfp4_expert_desc(ctypes.Structure):
+    _fields_ = [("gate", ft_nvfp4_matrix), ("up", ft_nvfp4_matrix), ("down", ft_nvfp4_matrix)]
+
+
+FT_WEIGHTS_ROWS, FT_WEIGHTS_DECODE_TILES, FT_WEIGHTS_UMMA_TILES = 1, 2, 4
 
 
 def _sig(name, args, res=ctypes.c_int):
@@ -74,6 +86,7 @@ _sig("ft_nvfp4_pack_tiles", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_moe_layer_decode_workspace_size", [_i32, _i32, _i32, _i32], _sz)
 _sig("ft_moe_layer_decode", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
                              _vp])
+_sig("ft_debug_inject_wait_expiry", [_i32, _u64])
 _sig("ft_moe_layer_decode_noalloc", [ctypes.POINTER(ft_moe_layer_weights), _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp])
 _sig("ft_nvfp4_pack_umma", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_moe_prefill_workspace_size", [_i32, _i32, _i32, _i32, _i32], _sz)
@@ -90,6 +103,11 @@ _sig("ft_expert_cache_stats", [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), 
 _sig("ft_expert_cache_inject_fill_failure", [_vp, _i64])
 _sig("ft_expert_cache_resize", [_vp, _i32, _vp, _sz, _vp])
 _sig("ft_expert_cache_resize_plan", [_vp, _i32, ctypes.POINTER(ctypes.c_int32)])
+
+_sig("ft_moe_weights_create", [ctypes.POINTER(ft_nvfp4_expert_desc), _i32, _i32, _i32, _i32, _vp,
+                               ctypes.POINTER(ctypes.c_void_p)])
+_sig("ft_moe_weights_describe", [_vp, _i32, ctypes.POINTER(ft_moe_layer_weights)])
+_sig("ft_moe_weights_destroy", [_vp])
 
 EXPORTED = [n for n in dir(_lib) if n.startswith("ft_")]
 
@@ -130,6 +148,11 @@ def _ws(nbytes: int, device) -> torch.Tensor | None:
 
 def ft_version() -> int:
     return _lib.ft_version()
+
+
+def ft_debug_inject_wait_expiry(site: int, limit_ns: int = 0) -> None:
+    """Test hook: make a device wait run out after limit_ns (site FT_WAIT_SITE_*); FT_WAIT_SITE_NONE turns it off."""
+    _check(_lib.ft_debug_inject_wait_expiry(int(site), int(limit_ns)))
 
 
 def ft_device_status(stream=None) -> int:
@@ -273,6 +296,42 @@ def ft_moe_expert_ffn_nvfp4_prefill(W, x: torch.Tensor, k: int, offsets, perm, w
     _check(_lib.ft_moe_expert_ffn_nvfp4_prefill(ctypes.byref(desc), _p(x), T, k, _p(offsets), _p(perm), _p(w), _p(out),
                                                 _p(ws), ws.numel() * ws.element_size(), _s(stream)))
     return out
+
+
+# --------------------------------------------------------------------------- layer weights handle
+
+class MoEWeightsHandle:
+    """Owns an ft_moe_weights handle: canonical NVFP4 experts repacked into the requested kernel layouts.
+
+    experts: E entries, each ((gate codes ptr, codes_ld, scales ptr, scales_ld, tensor-scale ptr), up, down) of device
+    pointers and row strides in bytes.  layout_flags: a set of FT_WEIGHTS_*.
+    """
+
+    def __init__(self, experts, H: int, I: int, layout_flags: int, stream=None):
+        E = len(experts)
+        arr = (ft_nvfp4_expert_desc * E)()
+        for e, mats in enumerate(experts):
+            for name, m in zip(("gate", "up", "down"), mats):
+                setattr(arr[e], name, ft_nvfp4_matrix(*m))
+        h = ctypes.c_void_p()
+        _check(_lib.ft_moe_weights_create(arr, E, H, I, layout_flags, _s(stream), ctypes.byref(h)))
+        self.h, self.E, self.H, self.I, self.flags = h, E, H, I, layout_flags
+
+    def describe(self, layout: int) -> ft_moe_layer_weights:
+        d = ft_moe_layer_weights()
+        _check(_lib.ft_moe_weights_describe(self.h, layout, ctypes.byref(d)))
+        return d
+
+    def close(self):
+        if self.h:
+            _lib.ft_moe_weights_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # --------------------------------------------------------------------------- expert-slot cache

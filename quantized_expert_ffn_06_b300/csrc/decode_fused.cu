@@ -1,82 +1,80 @@
-// decode_fused.cu -- one persistent launch per MoE layer for small token
-// counts (decode): router top-k, expert grouping, NVFP4 gate/up projection with
-// SwiGLU, down projection and routing-weighted combine.
+// decode_fused.cu -- one launch per MoE layer for small token counts (decode):
+// router top-k, grouping by expert, NVFP4 gate/up projection with SwiGLU, down
+// projection and the routing-weighted combine.
 //
 // The step follows the page "FreeToken：753B大模型塞进单卡的本地部署硬件账该怎么算"
 // (MoE core mechanism: linear + softmax router, top-K experts, weighted sum of
-// independent expert FFNs).  Decode is bound by streaming the selected experts'
-// weights from HBM, and at batch 1 a layer moves only ~14 MB (a few
-// microseconds), so the kernel is built around the latency of that stream:
+// independent expert FFNs).  At batch 1 a layer of the 35B-class shape moves
+// ~14 MB of expert weights, a few microseconds of HBM time, so the kernel is a
+// chain of latencies around that stream, and two costs dominate that chain
+// besides the stream itself: round trips to memory and instruction fetch (the
+// control code runs once per launch, so every instruction on the path is
+// fetched cold).  The kernel is built for both:
 //
-//  * Weights sit in HBM in 16-row tiles (ft_nvfp4_pack_tiles): per 128-element
-//    K-block 1 KB of codes in which lane L of a warp owns the 16-byte pieces at
-//    L*16 and 512 + L*16 (its mma A fragment for rows L/4 and L/4 + 8), then
-//    128 B of E4M3 scales, one 4-byte word per lane.  One tile is one bulk copy
-//    and every shared-memory read of it is conflict-free.
-//  * Prologue: x and the router logits land in shared memory by one bulk copy
-//    each.  Each token's top-k is found by one warp: every lane sorts its
-//    (up to eight) keys once, then k rounds of a warp-wide integer max over the
-//    lanes' heads (order-preserving keys, ties to the lower expert id).  All
-//    threads stage the activations as f16, and up to 32 (token, slot) pairs are
-//    grouped by expert inside one warp.  Every CTA does this redundantly, so
-//    the weight stream starts without any inter-CTA traffic.
-//  * One producer warp issues every tile the CTA needs with cp.async.bulk into
-//    a ring of shared-memory stages guarded by mbarriers; the down-projection
-//    tiles are prefetched while the gate/up tiles are consumed.  Its other
-//    lanes fetch the experts' tensor scales into shared memory, and it
-//    triggers the dependent launch, off the consumers' path.
-//  * Sixteen consumer warps form four groups.  A group owns whole tiles: its
-//    four warps split a tile's K-blocks, decode each E2M1 pair exactly to f16
-//    (cvt.rn.f16x2.e2m1x2), multiply by the E4M3 block scale in f16 (exact: at
-//    most 6 significant bits, magnitudes in [2^-10, 2688]) and feed mma.sync
-//    m16n8k16 with fp32 accumulation (tokens are the mma's N).  The tensor cores
-//    only take over the multiply-adds of this HBM-bound GEMV.  The group then
-//    reduces its four partial tiles and writes h = bf16(silu(g) * u).
-//  * The gate/up phase writes h as 64-bit words {bf16, bf16, call epoch}; the
-//    down phase of every CTA waits (bounded) for exactly the words it reads, so
-//    no grid-wide barrier separates the phases.
-//    In the down phase each CTA owns a range of 16-row output tiles for all
-//    selected experts; a warp computes one expert's down tile (for rows of 8+
-//    K-blocks, one or two experts per chunk and their K-blocks split across
-//    the group's warps), and the weighted sum over a token's k experts is
-//    taken in slot order j from shared memory.
-//  * The control code runs once per launch, so its size and latency are on the
-//    critical path: divisions by launch-time constants are host-computed
-//    multiply-high divisors, slow paths are out of line, one-shot loops stay
-//    rolled.
-//  * A batch whose f16 staging does not fit one launch runs as launches over
-//    token chunks (ft_moe_layer_decode).
-//  * Grid = one CTA per SM, all co-resident, which those waits rely on.  Every
-//    wait is bounded by a %globaltimer budget; on expiry the kernel sets
-//    FT_DEVERR_TIMEOUT, stops waiting and finishes without trapping.
-//  * The launch allows programmatic dependent launch: the kernel waits for its
-//    predecessor's results (griddepcontrol.wait) before reading any input, and
-//    lets its successor be scheduled once all of its own CTAs have started.
+//  * Code size.  Control loops stay rolled, divisions by per-launch constants
+//    are host-computed multiply-high divisors, and one out-of-line routine
+//    computes a K-block for both projections.
+//  * Inputs.  Right after the dependency wait every thread issues its async
+//    copies of the router logits and of x at once.
+//  * Router (every CTA, redundantly: no inter-CTA traffic before the weight
+//    stream).  Two levels, no serial rounds: each warp ranks a block of 32
+//    logits by 32 shuffles and keeps its k best as sorted candidates; then one
+//    thread per (candidate, block) counts by binary search how many of that
+//    block's candidates beat it, and the sum of those counts is the
+//    candidate's rank.  Keys order the fp32 logits exactly, equal logits going
+//    to the lower expert id.
+//  * Work split.  Phase 1 is the gate/up tiles of the selected experts, phase 2
+//    the down projection of 16-row output tiles over all selected experts.  A
+//    CTA's phase-1 share is balanced by bytes against its phase-2 share.
+//  * Weight stream.  Each warp copies its own K-blocks (1152 bytes each) from
+//    HBM into a shared-memory ring of R slots with per-lane async copies
+//    (cp.async, one commit group per K-block), so R K-blocks per warp are in
+//    flight; a lane reads back only the bytes it copied itself.  The ring runs
+//    straight on from the gate/up K-blocks into the down K-blocks, which thus
+//    land while the gate/up results are handed over.
+//  * Inner loop.  A code word is split into its four bytes in one move, each
+//    byte (two E2M1 codes) converts exactly to f16x2 (cvt.rn.f16x2.e2m1x2) and
+//    is multiplied by its E4M3 block scale in f16 (exact: at most 6 significant
+//    bits, magnitudes in [2^-10, 2688]); mma.sync m16n8k16 accumulates in fp32
+//    with tokens as N.  Warps that share a tile sum their partials in shared
+//    memory in a fixed order.
+//  * Hand-off.  h = bf16(silu(g) * u) goes to global memory as 64-bit words
+//    {bf16, bf16, call epoch}; phase 2 of every CTA waits (bounded) for exactly
+//    the words it reads, so no grid-wide barrier separates the phases.
+//  * Combine.  A token's k expert outputs are summed in slot order j in fp32
+//    from shared memory and rounded once to bf16.
+//  * Grid = one CTA per SM, all co-resident, which the hand-off relies on.
+//    Every wait is bounded by a %globaltimer budget; on expiry the kernel sets
+//    FT_DEVERR_TIMEOUT and finishes without trapping.  The launch allows
+//    programmatic dependent launch (griddepcontrol).
 #include "common.cuh"
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace ft {
 
 namespace dk {
-constexpr int NCW = 16;                  // consumer warps
-constexpr int NG = 4;                    // consumer groups
-constexpr int WPG = NCW / NG;            // warps per group
-constexpr int THREADS = 32 * (NCW + 1);  // + one producer warp
-constexpr int MAXT = 16;                 // tokens per launch
-constexpr int MAXK = 32;                 // experts per token
-constexpr int MAXNS = 16;                // ring stages
-constexpr int XPAD = 32;                 // halves of padding per staged f16 row (bank spread between rows)
+constexpr int NW = 16;                 // warps per CTA
+constexpr int LOG_NW = 4;
+constexpr int THREADS = 32 * NW;
+constexpr int MAXT = 16;               // tokens per launch
+constexpr int MAXK = 32;               // experts per token
+constexpr int ITEM = 1152;             // bytes of one K-block (128 elements) of a 16-row tile
+constexpr int XPAD = 32;               // halves of padding per staged f16 row
+constexpr int MAXSLOT = 2 * NW;        // partial-sum slots of a phase split across warps
 constexpr size_t SMEM_BUDGET = 227 * 1024;
-constexpr size_t XS_BUDGET = 120 * 1024;  // staged activations: x and h, separate buffers
-constexpr unsigned long long WAIT_NS = 2000000000ull;  // bound on any single wait
+constexpr unsigned long long WAIT_NS = 2000000000ull;  // default bound on any single wait
 }  // namespace dk
 
-// Division by a divisor fixed at launch: q = x / d as one multiply-high with
+// Test hooks (off by default): a shorter wait bound, and a wait made to expire.
+static std::atomic<unsigned long long> g_wait_ns{dk::WAIT_NS};
+static std::atomic<int> g_wait_site{FT_WAIT_SITE_NONE};
+
+// Division by a divisor fixed per launch: q = x / d as one multiply-high with
 // m = ceil(2^32 / d), exact whenever x * d < 2^32 (every use below stays far
-// inside that).  Runtime integer division is a long instruction sequence, and
-// this kernel's control code runs once per launch, so its size is its latency.
+// inside that).
 struct FastDiv {
     uint32_t d, m;  // m == 0 encodes d == 1
 };
@@ -88,30 +86,32 @@ static FastDiv make_fastdiv(uint32_t d) {
     return f;
 }
 
-__device__ __forceinline__ int fdiv(int x, const FastDiv& f) {
-    return f.m ? (int)__umulhi((uint32_t)x, f.m) : x;
-}
+__device__ __forceinline__ int fdiv(int x, const FastDiv& f) { return f.m ? (int)__umulhi((uint32_t)x, f.m) : x; }
 
-// Shared-memory plan, computed on the host (byte offsets into dynamic shared memory).
+// Shared-memory plan and per-launch constants, computed on the host.
 struct DecodePlan {
-    int nstages, stage_bytes;  // ring
-    int J;                     // down tiles (experts) per phase-2 stage
-    int tcol;                  // token columns of a partial tile (T)
-    int max_ot;                // phase-2 output tiles per CTA, at most
+    int ring;                  // K-block slots per warp (R)
     int xs_stride, hs_stride;  // halves per staged x / h row
-    int off_bars, off_ids, off_wts, off_plist, off_pexp, off_hexp, off_ulist, off_ubeg, off_uwi, off_misc;
-    int off_xs, off_hs, off_red, off_ybuf, off_ring, off_ptok, off_ts;
+    int tc;                    // token columns of a partial tile (T)
+    int nb, kk;                // router: 32-logit blocks per token, candidates per block (min(k, 32))
+    int max_ot;                // output tiles per CTA, at most
+    int off_misc, off_ids, off_wts, off_plist, off_ptok, off_pexp, off_hexp, off_ulist, off_ubeg, off_uwi, off_ts;
+    int off_rank, off_xs, off_big, off_xraw, off_cand, off_slot, off_wscr, off_ybuf, off_ring;
     int smem;
-    FastDiv dv_ns;    // ring stages
-    FastDiv dv_tgu;   // gate/up tiles per expert (2I/16)
     FastDiv dv_k;     // slots per token
     FastDiv dv_xrow;  // 16-byte pieces per x row (H/8)
     FastDiv dv_hrow;  // h words per row (I/2)
     FastDiv dv_g;     // CTAs in the grid
     FastDiv dv_t;     // tokens
-    FastDiv dv_j;     // down tiles per stage (J)
-    int logits_bulk;  // the logits are copied into the ring by one bulk copy
+    FastDiv dv_nb;    // router blocks per token
+    FastDiv dv_c;     // router candidates per token (nb * kk)
+    FastDiv dv_tgu;   // gate/up tiles per expert (I/8)
+    FastDiv dv_kb1;   // K-blocks per gate/up tile (H/128)
+    FastDiv dv_kb2;   // K-blocks per down tile (I/128)
+    unsigned long long dv_g64;  // ceil(2^64 / G): call number = mulhi(counter, dv_g64)
     float inv_k;      // 1/k, rounded to nearest (the weight of every slot of a -inf row)
+    unsigned long long wait_ns;  // bound on any single wait
+    int wait_site;               // FT_WAIT_SITE_DECODE_H: the h hand-off waits for an epoch nobody writes
 };
 
 struct DecodeArgs {
@@ -126,14 +126,13 @@ struct DecodeArgs {
     int32_t* ids_out;         // route mode, optional
     float* w_out;             // route mode, optional
     void* hbuf;               // [T*k][I/2] h words {bf16, bf16, epoch}, by permuted row
-    unsigned int* bar;        // call counter (monotonic, starts at 0): G per call
+    unsigned long long* bar;  // call counter (monotonic, starts at 0): one per CTA per call
     int T, k;
     DecodePlan P;
 };
 
-// misc ints in shared memory
-// (xexp: MAXT entries, tags: MAXNS; FLAG / HFLAG: x / h rows needed rescaling)
-enum { M_U = 0, M_FLAG = 1, M_ABORT = 2, M_EPOCH = 3, M_XEXP = 4, M_TAGS = 4 + 16, M_TS = 4 + 16 + 16, M_HFLAG = M_TS + 1 };
+// misc ints in shared memory (XEXP: pre-scale exponent of each staged x row)
+enum { M_U = 0, M_FLAG = 1, M_HFLAG = 2, M_ABORT = 3, M_EPOCH = 4, M_XEXP = 8, M_COUNT = 8 + dk::MAXT };
 
 // ---------------------------------------------------------------------------- PTX helpers
 
@@ -145,108 +144,67 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
-__device__ __forceinline__ void mbar_init(unsigned long long* b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Gives up a bounded wait: the first expiry in a CTA sets FT_DEVERR_TIMEOUT and
-// the CTA's abort flag; returns whether the wait may go on.
-__device__ __forceinline__ bool wait_budget_left(unsigned long long t0, volatile int* abort_flag) {
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > dk::WAIT_NS) {
-        *abort_flag = 1;
-        raise_dev_error(FT_DEVERR_TIMEOUT);
-        return false;
-    }
-    return true;
-}
-
-// Bounded wait on an mbarrier phase (slow path, out of line).  On expiry, or
-// if the CTA already gave up, returns false.
-__device__ __noinline__ bool mbar_wait_slow(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(b, parity))
-        if (!wait_budget_left(t0, abort_flag)) return false;
-    return true;
-}
-
-__device__ __forceinline__ bool mbar_wait(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
-    return mbar_try_wait(b, parity) || mbar_wait_slow(b, parity, abort_flag);
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* b) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(b))
-                 : "memory");
-}
-
-// Stage tags: the producer publishes, after arming a stage's full barrier for
-// chunk n, tag[stage] = n (release); a consumer of chunk n first waits for that
-// tag (acquire) and only then tests the barrier's phase parity.  Without the tag
-// a consumer group running ahead could test the parity of a use whose previous
-// use has not landed yet, and parity alone cannot tell the two apart.
-__device__ __forceinline__ void tag_publish(int* tag, int n) {
-    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tag)), "r"(n) : "memory");
-}
-__device__ __forceinline__ int tag_read(const int* tag) {
-    int v;
-    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(tag)) : "memory");
-    return v;
-}
-
-// Bounded wait for chunk n (stage n mod NS, use n / NS): its tag, then its
-// full-barrier phase.  Out of line: both consumer loops share one copy.
-// Bounded wait (slow path, out of line) for a shared-memory tag to read `want`.
-__device__ __noinline__ void tag_wait_slow(int* tag, int want, volatile int* abort_flag) {
-    const unsigned long long t0 = globaltimer();
-    while (tag_read(tag) != want)
-        if (!wait_budget_left(t0, abort_flag)) return;
-}
-
-__device__ __forceinline__ void tag_wait(int* tag, int want, volatile int* abort_flag) {
-    if (tag_read(tag) != want) tag_wait_slow(tag, want, abort_flag);
-}
-
-// Returns the stage; after an expired wait the CTA's abort flag is set and the
-// stage's contents are not to be trusted (the caller finishes without waiting).
-__device__ __noinline__ int chunk_wait(unsigned long long* full, int* tags, int n, FastDiv dv_ns, volatile int* abort_flag) {
-    const int q = fdiv(n, dv_ns), s = n - q * (int)dv_ns.d;
-    tag_wait(&tags[s], n, abort_flag);
-    mbar_wait(&full[s], q & 1, abort_flag);
-    return s;
-}
-
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(dk::NCW * 32) : "memory"); }
-__device__ __forceinline__ void group_sync(int gi) {
-    asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "n"(dk::WPG * 32) : "memory");
+// per-thread async copies global -> shared (cp.async): 16 bytes (L2 only) or 4 bytes
+__device__ __forceinline__ void cp16(void* s, const void* g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(s)), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp4(void* s, const void* g) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s)), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// wait until at most n of this thread's commit groups are pending (n clamped to [0, 15])
+__device__ __forceinline__ void cp_wait_upto(int n) {
+    switch (n <= 0 ? 0 : n >= 15 ? 15 : n) {
+        case 0: cp_wait<0>(); break;
+        case 1: cp_wait<1>(); break;
+        case 2: cp_wait<2>(); break;
+        case 3: cp_wait<3>(); break;
+        case 4: cp_wait<4>(); break;
+        case 5: cp_wait<5>(); break;
+        case 6: cp_wait<6>(); break;
+        case 7: cp_wait<7>(); break;
+        case 8: cp_wait<8>(); break;
+        case 9: cp_wait<9>(); break;
+        case 10: cp_wait<10>(); break;
+        case 11: cp_wait<11>(); break;
+        case 12: cp_wait<12>(); break;
+        case 13: cp_wait<13>(); break;
+        case 14: cp_wait<14>(); break;
+        default: cp_wait<15>(); break;
+    }
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
+}
+
+// The four bytes of a code word (eight E2M1 codes) as four f16x2 (exact).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&f)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+        : "r"(w));
+}
+
+// A lane's four E4M3 block scales (one word) as f16x2, each value in both halves (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2_bcast(uint32_t sc, uint32_t& s0, uint32_t& s1, uint32_t& s2,
+                                                      uint32_t& s3) {
+    const uint32_t lo = __byte_perm(sc, 0u, 0x1100), hi = __byte_perm(sc, 0u, 0x3322);
+    asm("{\n\t.reg .b16 a, b, c, d;\n\tmov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
+        : "=r"(s0), "=r"(s1), "=r"(s2), "=r"(s3)
+        : "r"(lo), "r"(hi));
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -257,8 +215,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-    return (i == 0) ? v.x : (i == 1) ? v.y : (i == 2) ? v.z : v.w;
+// h words: the gate/up phase writes h as 64-bit words {bf16 h[2j], bf16 h[2j+1],
+// uint32 epoch} (one single-copy-atomic store each), so the down phase can wait
+// for exactly the words it reads instead of for a grid-wide barrier.
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // ---------------------------------------------------------------------------- staged activation rows
@@ -285,256 +251,72 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& big) {
 
 // Rare path of the staging: rows holding a value of magnitude >= 60000 are
 // rescaled by a power of two so that they fit f16; exps[r] records it.  The
-// caller synchronises before and after.  Source: bf16 rows (x), or h words.
+// caller synchronises the CTA before and after.  Source: bf16 rows (x), or h words.
 __device__ __noinline__ void restage_scaled(int* exps, __half* dst, int stride, int n, int K, const uint16_t* xsrc,
-                                            const unsigned long long* hw, int ti, int nthr, bool cta_wide) {
+                                            const unsigned long long* hw) {
     auto val = [&](int r, int c) {
         if (xsrc) return bf16_to_f32(__ldcg(xsrc + (int64_t)r * K + c));
         const uint32_t w = (uint32_t)__ldcg(hw + (int64_t)r * (K / 2) + c / 2);
         return bf16_to_f32((uint16_t)((c & 1) ? (w >> 16) : (w & 0xFFFFu)));
     };
-    const int w = ti >> 5, lane = ti & 31, nw = nthr >> 5;
+    const int ti = threadIdx.x, w = ti >> 5, lane = ti & 31;
 #pragma unroll 1
-    for (int r = w; r < n; r += nw) {
+    for (int r = w; r < n; r += dk::NW) {
         float m = 0.0f;
 #pragma unroll 1
         for (int i = lane; i < K; i += 32) m = fmaxf(m, fabsf(val(r, i)));
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) exps[r] = (m >= 16384.0f) ? ilogbf(m) - 14 : 0;
     }
-    if (cta_wide) __syncthreads();
-    else consumer_sync();
+    __syncthreads();
 #pragma unroll 1
-    for (int idx = ti; idx < n * K; idx += nthr) {
+    for (int idx = ti; idx < n * K; idx += dk::THREADS) {
         const int r = idx / K, c = idx - r * K;
         dst[r * stride + staged_pos(c)] = __float2half_rn(val(r, c) * pow2i(-exps[r]));
     }
 }
 
-// Convert the n activation rows that landed as bf16 [n][K] in `raw` (shared
-// memory, by one bulk copy) to f16 in dst (row stride `stride` halves,
-// staged_pos order), with every thread of the CTA; `src` is the same rows in
-// global memory, read again only on the rare rescaling path.
-__device__ void stage_x(int* exps, volatile int* flag, __half* dst, int stride, const uint16_t* raw, const uint16_t* src,
-                        int n, int K, FastDiv dv_row) {
-    const int ti = threadIdx.x, nthr = blockDim.x;
-    const int per_row = K >> 3, total = n * per_row;
-    bool big = false;
-#pragma unroll 1
-    for (int idx = ti; idx < total; idx += nthr) {
-        const int r = fdiv(idx, dv_row), c = idx - r * per_row;
-        const uint4 v = *reinterpret_cast<const uint4*>(raw + (size_t)idx * 8);
-        const uint4 o = make_uint4(bf16x2_to_f16x2(v.x, big), bf16x2_to_f16x2(v.y, big), bf16x2_to_f16x2(v.z, big),
-                                   bf16x2_to_f16x2(v.w, big));
-        *reinterpret_cast<uint4*>(dst + r * stride + staged_pos(c * 8)) = o;
-    }
-    if (big) *flag = 1;
-    __syncthreads();
-    if (*flag) {
-        restage_scaled(exps, dst, stride, n, K, src, nullptr, ti, nthr, true);
-        __syncthreads();
-    }
-}
+// ---------------------------------------------------------------------------- one K-block of a 16-row tile
 
-// h words: the gate/up phase writes h as 64-bit words {bf16 h[2j], bf16 h[2j+1],
-// uint32 epoch} (one single-copy-atomic store each), so the down phase can wait
-// for exactly the words it reads instead of for a grid-wide barrier.
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Stage all n h rows (I values each, nw = I/2 words per row) as f16 into dst,
-// waiting (bounded) for each word to carry `epoch`; consumer threads only.
-// Returns false if a wait gave up.
-__device__ bool stage_h(int* exps, volatile int* flag, __half* dst, int stride, const unsigned long long* hw, int n, int I,
-                        FastDiv dv_row, unsigned int epoch, volatile int* abort_flag) {
-    const int ti = threadIdx.x, nthr = dk::NCW * 32;
-    const int nw = I / 2, total = n * nw;
-    constexpr int B = 8;  // 8-byte loads in flight per thread
-    bool big = false, ok = true;
-#pragma unroll 1
-    for (int base = ti; base < total; base += B * nthr) {
-        unsigned long long v[B];
-        uint32_t pending = 0;
-#pragma unroll
-        for (int u = 0; u < B; ++u) {
-            const int idx = base + u * nthr;
-            if (idx < total) {
-                v[u] = ld_relaxed_u64(hw + idx);
-                if ((uint32_t)(v[u] >> 32) != epoch) pending |= 1u << u;
-            }
-        }
-        if (pending) {
-            const unsigned long long t0 = globaltimer();
-            while (pending) {
-#pragma unroll
-                for (int u = 0; u < B; ++u)
-                    if (pending & (1u << u)) {
-                        v[u] = ld_relaxed_u64(hw + base + u * nthr);
-                        if ((uint32_t)(v[u] >> 32) == epoch) pending &= ~(1u << u);
-                    }
-                if (pending && !wait_budget_left(t0, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < B; ++u) {
-            const int idx = base + u * nthr;
-            if (idx < total) {
-                const int r = fdiv(idx, dv_row), c = idx - r * nw;
-                *reinterpret_cast<uint32_t*>(dst + r * stride + staged_pos(2 * c)) = bf16x2_to_f16x2((uint32_t)v[u], big);
-            }
-        }
-        if (!ok) break;
-    }
-    if (big) *flag = 1;
-    consumer_sync();
-    if (*flag) {
-        restage_scaled(exps, dst, stride, n, I, nullptr, hw, ti, nthr, false);
-        consumer_sync();
-    }
-    return ok;
-}
-
-// ---------------------------------------------------------------------------- tile math
-
-// Partial products of one 16-row tile over K-blocks kb0, kb0+kstep, ... (K =
-// 128*KB) against one staged f16 row per lane column (`xrow`, staged_pos
-// order): the mma accumulator (rows g, g+8; token columns 2q, 2q+1) as
-// {d0, d1, d2, d3}.  Out of line: one copy serves both phases.
-//
-// Lane L = 4g + q owns code bytes [16q, 16q+16) of rows g and g+8 in each
-// K-block, i.e. elements 32q .. 32q+31.  mma s (of 8 per K-block) takes
-// elements 32q + 4s .. +3 of them: the pair 4s, 4s+1 as the fragment's
-// k = 2q, 2q+1 and the pair 4s+2, 4s+3 as k = 2q+8, 2q+9.  The activations are
-// read at the same element positions, so the dot product is unchanged by this
-// K order.  Two accumulators shorten the dependent mma chain.
-__device__ __noinline__ float4 tile_partial(const uint8_t* tile, int KB, int kb0, int kstep, const __half* xrow) {
+// Partial products of one K-block (128 elements x 16 rows) held in shared
+// memory as laid out in HBM: lane L = 4g + q owns the code bytes [16q, 16q+16)
+// of rows g and g+8 (at L*16 and 512 + L*16) and the scale word of blocks 2q,
+// 2q+1 of both rows (at 1024 + L*4), i.e. elements 32q .. 32q+31.  x: the
+// lane's staged f16 row (its token column) at this K-block, + 8q halves.  mma s
+// (8 per K-block) takes elements 32q + 4s .. +3: the pair 4s, 4s+1 as the
+// fragment's k = 2q, 2q+1 and the pair 4s+2, 4s+3 as k = 2q+8, 2q+9; the
+// activations are read at the same element positions, so the dot product is
+// unchanged by this K order.  Returns the accumulator (rows g, g+8; columns
+// 2q, 2q+1) as {d0, d1, d2, d3}.  Out of line: one copy serves both phases.
+__device__ __noinline__ float4 kblock_partial(const uint8_t* item, const __half* x) {
     const int lane = threadIdx.x & 31;
-    const int q = lane & 3;
-    const uint8_t* scl = tile + KB * 1024;
+    uint32_t sg0, sg1, sh0, sh1;
+    e4m3x4_to_f16x2_bcast(*reinterpret_cast<const uint32_t*>(item + 1024 + lane * 4), sg0, sg1, sh0, sh1);
+    const uint32_t* c0 = reinterpret_cast<const uint32_t*>(item + lane * 16);
+    const uint32_t* c1 = reinterpret_cast<const uint32_t*>(item + 512 + lane * 16);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     float e[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int kb = kb0; kb < KB; kb += kstep) {
-        const uint4 c0 = *reinterpret_cast<const uint4*>(tile + kb * 1024 + lane * 16);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(tile + kb * 1024 + 512 + lane * 16);
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(scl + kb * 128 + lane * 4);
-        const uint32_t sg0 = e4m3_to_f16x2_bcast(sc & 0xFFu), sg1 = e4m3_to_f16x2_bcast((sc >> 8) & 0xFFu);
-        const uint32_t sh0 = e4m3_to_f16x2_bcast((sc >> 16) & 0xFFu), sh1 = e4m3_to_f16x2_bcast(sc >> 24);
-        const __half* xr = xrow + kb * 128 + q * 8;
-        uint4 xv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) xv[i] = *reinterpret_cast<const uint4*>(xr + 32 * i);
-        const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w};
-        const uint32_t cw1[4] = {c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint32_t sa = (s < 4) ? sg0 : sg1, sb = (s < 4) ? sh0 : sh1;
-            const uint32_t w0 = cw0[s >> 1], w1 = cw1[s >> 1];
-            const int sh = (s & 1) * 16;
-            const uint32_t a0 = hmul2(e2m1x2_to_f16x2((w0 >> sh) & 0xFFu), sa);
-            const uint32_t a2 = hmul2(e2m1x2_to_f16x2((w0 >> (sh + 8)) & 0xFFu), sa);
-            const uint32_t a1 = hmul2(e2m1x2_to_f16x2((w1 >> sh) & 0xFFu), sb);
-            const uint32_t a3 = hmul2(e2m1x2_to_f16x2((w1 >> (sh + 8)) & 0xFFu), sb);
-            const uint32_t b0 = word_of(xv[s >> 1], (2 * s) & 3);
-            const uint32_t b1 = word_of(xv[s >> 1], (2 * s + 1) & 3);
-            if (s & 1)
-                mma16816(e, a0, a1, a2, a3, b0, b1);
-            else
-                mma16816(d, a0, a1, a2, a3, b0, b1);
-        }
+#pragma unroll 2
+    for (int s2 = 0; s2 < 4; ++s2) {
+        uint32_t f0[4], f1[4];
+        e2m1x8_to_f16x2x4(c0[s2], f0);
+        e2m1x8_to_f16x2x4(c1[s2], f1);
+        const uint32_t sa = (s2 < 2) ? sg0 : sg1, sb = (s2 < 2) ? sh0 : sh1;
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + 32 * s2);
+        mma16816(d, hmul2(f0[0], sa), hmul2(f1[0], sb), hmul2(f0[1], sa), hmul2(f1[1], sb), xv.x, xv.y);
+        mma16816(e, hmul2(f0[2], sa), hmul2(f1[2], sb), hmul2(f0[3], sa), hmul2(f1[3], sb), xv.z, xv.w);
     }
     return make_float4(d[0] + e[0], d[1] + e[1], d[2] + e[2], d[3] + e[3]);
 }
 
-// ---------------------------------------------------------------------------- routing
-
-// 256 < E <= 1024: a lane rescans its (up to 32) logits, skipping the slots in
-// `taken`.  Returns {expert of lane j < k, bad}.
-__device__ __noinline__ uint2 select_topk_wide(const float* row, int E, int k) {
-    const int lane = threadIdx.x & 31;
-    const int EPL = (E + 31) >> 5;
-    const int n = max(0, min(EPL, E - lane * EPL));
-    const float* mine = row + lane * EPL;
-    uint32_t taken = 0, bad = 0;
-    int my_e = 0;
-    uint32_t bk = 0;
-    int bi = 0;
-    bool dirty = true;
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-        if (dirty) {
-            bk = 0;
-#pragma unroll 1
-            for (int i0 = 0; i0 < n; i0 += 4) {
-                float x[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) x[u] = (i0 + u < n) ? mine[i0 + u] : 0.0f;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = i0 + u;
-                    bad |= (i < n) && ((x[u] != x[u]) || (x[u] == INFINITY));
-                    const uint32_t key = (i < n && !((taken >> i) & 1u)) ? logit_key(x[u]) : 0u;
-                    if (key > bk) {
-                        bk = key;
-                        bi = i;
-                    }
-                }
-            }
-            dirty = false;
-        }
-        const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
-        const int wl = __ffs(__ballot_sync(0xffffffffu, bk == gk)) - 1;
-        const int we = __shfl_sync(0xffffffffu, lane * EPL + bi, wl);
-        if (lane == wl) {
-            taken |= 1u << bi;
-            dirty = true;
-        }
-        if (lane == j) my_e = we;
-    }
-    return make_uint2((uint32_t)my_e, bad);
-}
-
-// Router of one token by one warp: top-k selection, then the weights
-// exp(l_j - l_0) / sum over the k selected, with the same butterfly sum as
-// ft_moe_route (every weight inv_k = 1/k when the largest logit is -inf).
-__device__ __forceinline__ void route_token(const float* row, int E, int k, float inv_k, int& my_e, float& my_w, bool& bad) {
-    const int lane = threadIdx.x & 31;
-    bool b = false;
-    if (E <= 256) {
-        my_e = select_topk8(row, E, k, b);
-    } else {
-        const uint2 r = select_topk_wide(row, E, k);
-        my_e = (int)r.x;
-        b = r.y != 0u;
-    }
-    bad = __any_sync(0xffffffffu, b);
-    const float my_v = (lane < k) ? row[my_e] : -INFINITY;
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    if (m == -INFINITY || m != m) {
-        my_w = inv_k;
-    } else {
-        const float ej = (lane < k) ? expf(my_v - m) : 0.0f;
-        const float s = warp_sum(ej);
-        my_w = ej / s;
-    }
-}
-
 // ---------------------------------------------------------------------------- kernel
 
+template <int R>
 __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
     const DecodePlan& P = a.P;
-    unsigned long long* full = reinterpret_cast<unsigned long long*>(dsm + P.off_bars);
-    unsigned long long* empty = full + dk::MAXNS;
-    unsigned long long* xbar = full + 2 * dk::MAXNS;  // the bulk copy of x
+    int* misc = reinterpret_cast<int*>(dsm + P.off_misc);
+    volatile int* abort_flag = misc + M_ABORT;
     int* s_ids = reinterpret_cast<int*>(dsm + P.off_ids);      // [nf] expert of slot f (route mode)
     float* s_wts = reinterpret_cast<float*>(dsm + P.off_wts);  // [nf] weight of slot f
     int* s_plist = reinterpret_cast<int*>(dsm + P.off_plist);  // [nf] slot f of permuted row p
@@ -544,85 +326,144 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     int* s_ulist = reinterpret_cast<int*>(dsm + P.off_ulist);  // [nf] selected experts, ascending
     int* s_ubeg = reinterpret_cast<int*>(dsm + P.off_ubeg);    // [nf+1] permuted-row range of each
     int* s_uwi = reinterpret_cast<int*>(dsm + P.off_uwi);      // [nf] weight index (-1: invalid slot)
-    float* s_ts = reinterpret_cast<float*>(dsm + P.off_ts);   // [nf][4] tensor scales (gate, up, down) of each
-    int* misc = reinterpret_cast<int*>(dsm + P.off_misc);
-    volatile int* abort_flag = misc + M_ABORT;
-    __half* xs = reinterpret_cast<__half*>(dsm + P.off_xs);  // x rows (phase 1)
-    __half* hs = reinterpret_cast<__half*>(dsm + P.off_hs);  // h rows (phase 2); separate, so no CTA-wide sync between
-    float* red = reinterpret_cast<float*>(dsm + P.off_red);
-    float* ybuf = reinterpret_cast<float*>(dsm + P.off_ybuf);  // [max_ot][nf][16]
-    uint8_t* ring = dsm + P.off_ring;
+    float* s_ts = reinterpret_cast<float*>(dsm + P.off_ts);    // [nf][4] tensor scales (gate, up, down)
+    int* s_rank = reinterpret_cast<int*>(dsm + P.off_rank);    // [T][nb*kk] router candidate ranks
+    __half* xs = reinterpret_cast<__half*>(dsm + P.off_xs);    // x rows, f16, staged layout
+    float* lg = reinterpret_cast<float*>(dsm + P.off_big);     // raw logits [T][E] (router), then ...
+    __half* hs = reinterpret_cast<__half*>(dsm + P.off_big);   // ... h rows, f16, staged layout (phase 2)
+    uint16_t* xraw = reinterpret_cast<uint16_t*>(dsm + P.off_xraw);                       // x as loaded, bf16
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(dsm + P.off_cand);  // [T][nb][kk]
+    float* slots = reinterpret_cast<float*>(dsm + P.off_slot);  // [MAXSLOT][16][tc] partial tiles
+    float* wscr = reinterpret_cast<float*>(dsm + P.off_wscr);   // [NW][16][tc] a warp's finished tile
+    float* ybuf = reinterpret_cast<float*>(dsm + P.off_ybuf);   // [max_ot][nf][16] expert outputs
 
     const ft_moe_layer_weights& W = a.W;
     const int H = W.H, I = W.I, E = W.E, T = a.T, k = a.k;
     const int nf = T * k;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const int NS = P.nstages;
+    const int TC = P.tc;
+    const bool route_mode = a.logits != nullptr;
+    uint8_t* ring = dsm + P.off_ring + warp * (R * dk::ITEM);
 
-    if (tid == 0) {
-#pragma unroll 1
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], dk::WPG);
-        }
-        mbar_init(xbar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        misc[M_FLAG] = 0;
-        misc[M_HFLAG] = 0;
-        misc[M_ABORT] = 0;
-        misc[M_TS] = 0;
-    }
-    if (tid < dk::MAXT) misc[M_XEXP + tid] = 0;
-    if (tid < dk::MAXNS) misc[M_TAGS + tid] = -1;
+    if (tid < M_COUNT) misc[tid] = 0;
 #pragma unroll 1
     for (int i = tid; i < nf; i += dk::THREADS) s_hexp[i] = 0;
-    __syncthreads();
+    if (route_mode) {
+#pragma unroll 1
+        for (int i = tid; i < T * P.nb * P.kk; i += dk::THREADS) s_rank[i] = 0;
+    }
     // inputs (and the workspace) may be written by the preceding kernel in the stream
     griddep_wait();
-    // x lands as bf16 in the h staging area (unused until the down phase) by one bulk copy.
-    // This call's epoch: calls sharing a workspace each add G to its counter.  The producer
-    // lane takes it (off the router's path) and publishes it at the end of the prologue.
-    // The logits, where the plan allows, land the same way in the ring (unused until the weights
-    // stream); the router then reads them through a generic pointer either way.
-    const bool route_mode = a.logits != nullptr;
-    const uint16_t* xraw = reinterpret_cast<const uint16_t*>(hs);
-    const float* lsrc = P.logits_bulk ? reinterpret_cast<const float*>(ring) : a.logits;
-    unsigned int old_count = 0;
-    if (tid == dk::NCW * 32) {
-        const uint32_t xbytes = (uint32_t)(T * H * 2), lbytes = route_mode && P.logits_bulk ? (uint32_t)(T * E * 4) : 0u;
-        mbar_arrive_expect_tx(xbar, xbytes + lbytes);
-        bulk_g2s(hs, a.x, xbytes, xbar);
-        if (lbytes) bulk_g2s(ring, a.logits, lbytes, xbar);
-        old_count = atomicAdd(a.bar, 1u);
+    griddep_launch_dependents();
+    unsigned long long old_count = 0;
+    if (tid == 0) old_count = atomicAdd(a.bar, 1ull);
+
+    // ---------------- inputs: every thread issues its async copies at once
+    {
+        const int nx = T * (H >> 3);  // 16-byte pieces of x
+        const int nl = route_mode ? T * E : 0;
+#pragma unroll 1
+        for (int i = tid; i < nl; i += dk::THREADS) cp4(lg + i, a.logits + i);
+#pragma unroll 1
+        for (int i = tid; i < nx; i += dk::THREADS) cp16(xraw + i * 8, a.x + i * 8);
+        cp_commit();
+        cp_wait<0>();
+        __syncthreads();
+        bool big = false;
+#pragma unroll 1
+        for (int i = tid; i < nx; i += dk::THREADS) {
+            const int r = fdiv(i, P.dv_xrow), cp = i - r * (H >> 3);
+            const uint4 v = *reinterpret_cast<const uint4*>(xraw + i * 8);
+            const uint4 o = make_uint4(bf16x2_to_f16x2(v.x, big), bf16x2_to_f16x2(v.y, big), bf16x2_to_f16x2(v.z, big),
+                                       bf16x2_to_f16x2(v.w, big));
+            *reinterpret_cast<uint4*>(xs + r * P.xs_stride + staged_pos(cp * 8)) = o;
+        }
+        if (big) misc[M_FLAG] = 1;
     }
 
-    // ---------------- prologue: warps < T route their token once the inputs have landed, then all
-    // threads stage x
-    mbar_wait(xbar, 0, abort_flag);
-    if (route_mode && warp < T) {
-        int my_e = 0;
-        float my_w = 0.0f;
+    // ---------------- router: top-k of every token (route mode)
+    if (route_mode) {
+        const int nb = P.nb, kk = P.kk, C = nb * kk;
+        // level 1: rank within each block of 32 logits; the kk best become sorted candidates.
+        // Key = (order-preserving key of the fp32 logit, then ~expert): larger is better, and
+        // equal logits rank the lower expert id first.
         bool bad = false;
-        route_token(lsrc + warp * E, E, k, P.inv_k, my_e, my_w, bad);
-        if (bad && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
-        if (lane < k) {
-            s_ids[warp * k + lane] = my_e;
-            s_wts[warp * k + lane] = my_w;
-            if (c == 0 && a.ids_out) {
-                a.ids_out[warp * k + lane] = my_e;
-                a.w_out[warp * k + lane] = my_w;
+#pragma unroll 1
+        for (int b = warp; b < T * nb; b += dk::NW) {
+            const int t = fdiv(b, P.dv_nb), bb = b - t * nb;
+            const int e = bb * 32 + lane;
+            const float v = (e < E) ? lg[t * E + e] : 0.0f;
+            const uint32_t key = (e < E) ? logit_key(v) : 0u;
+            bad |= (e < E) && ((v != v) || (v == INFINITY));
+            int rank = 0;
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+                rank += (kj > key) || (kj == key && j < lane);
+            }
+            if (rank < kk)
+                cand[b * kk + rank] = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
+        __syncthreads();
+        // level 2: rank of a candidate = sum over the token's blocks of the number of that
+        // block's candidates that beat it (binary search in the sorted list)
+#pragma unroll 1
+        for (int i = tid; i < T * C * nb; i += dk::THREADS) {
+            const int tc = fdiv(i, P.dv_nb), L = i - tc * nb;
+            const int t = fdiv(tc, P.dv_c);
+            const unsigned long long key = cand[tc];
+            const unsigned long long* list = cand + t * C + L * kk;
+            int lo = 0, hi = kk;
+#pragma unroll 1
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (list[mid] > key) lo = mid + 1;
+                else hi = mid;
+            }
+            if (lo) atomicAdd(&s_rank[tc], lo);
+        }
+        __syncthreads();
+        // the k best of token t, in order, by warp t mod NW; then their weights exp(l_j - l_0) / sum
+        // over the k selected (the router's arithmetic)
+#pragma unroll 1
+        for (int t = warp; t < T; t += dk::NW) {
+#pragma unroll 1
+            for (int i = lane; i < C; i += 32) {
+                const int r = s_rank[t * C + i];
+                if (r < k) s_ids[t * k + r] = (int)(0xFFFFFFFFu - (uint32_t)cand[t * C + i]);
+            }
+            __syncwarp();
+            const int e = (lane < k) ? s_ids[t * k + lane] : 0;
+            const float v = (lane < k) ? lg[t * E + e] : -INFINITY;
+            const float m = __shfl_sync(0xffffffffu, v, 0);
+            float w;
+            if (m == -INFINITY || m != m) {
+                w = P.inv_k;
+            } else {
+                const float ej = (lane < k) ? expf(v - m) : 0.0f;
+                const float s = warp_sum(ej);
+                w = ej / s;
+            }
+            if (lane < k) {
+                s_wts[t * k + lane] = w;
+                if (c == 0 && a.ids_out) {
+                    a.ids_out[t * k + lane] = e;
+                    a.w_out[t * k + lane] = w;
+                }
             }
         }
     }
-    // the ring is next written by the async proxy (the weight stream): order the reads before it
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    stage_x(misc + M_XEXP, misc + M_FLAG, xs, P.xs_stride, xraw, a.x, T, H, P.dv_xrow);  // ends with __syncthreads
-    // grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}.  Up to 32 slots
-    // one warp does it with shuffles and goes straight on to the scan below.
-    const bool warp_grouping = route_mode && nf <= 32;
-    if (warp_grouping) {
-        if (warp == 0) {
+    __syncthreads();
+    if (misc[M_FLAG]) {  // rare: x rows with values beyond the f16 range
+        restage_scaled(misc + M_XEXP, xs, P.xs_stride, T, H, a.x, nullptr);
+        __syncthreads();
+    }
+
+    // ---------------- grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}
+    if (route_mode && nf <= 32) {
+        if (warp == 0) {  // one warp, shuffles
             const int f = lane;
             const int e = (f < nf) ? s_ids[f] : 0x7fffffff;
             int pos = 0;
@@ -636,7 +477,6 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 s_ptok[pos] = fdiv(f, P.dv_k);
                 s_pexp[pos] = e;
             }
-            __syncwarp();
         }
     } else if (route_mode) {
 #pragma unroll 1
@@ -665,6 +505,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             s_wts[p] = a.w_in ? a.w_in[p] : 0.0f;  // indexed by slot f: w_in is [T][k]
             // expert owning row p: last e with offsets[e] <= p
             int lo = 0, hi = E - 1;
+#pragma unroll 1
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (__ldg(a.offsets + mid) <= p) lo = mid;
@@ -675,7 +516,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             s_pexp[p] = lo;
         }
     }
-    if (!warp_grouping) __syncthreads();
+    __syncthreads();
     // selected experts = segment starts of pexp (warp 0, ballot scan)
     if (warp == 0) {
         int run = 0;
@@ -686,18 +527,26 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             const uint32_t b = __ballot_sync(0xffffffffu, start);
             if (start) {
                 const int u = run + __popc(b & ((1u << lane) - 1u));
+                const int wi = weight_index(W, s_pexp[p]);
                 s_ulist[u] = s_pexp[p];
                 s_ubeg[u] = p;
-                s_uwi[u] = weight_index(W, s_pexp[p]);
+                s_uwi[u] = wi;
             }
             run += __popc(b);
         }
         if (lane == 0) {
             misc[M_U] = run;
             s_ubeg[run] = nf;
+            // this call's epoch: calls sharing a workspace each add G to its 64-bit counter; the
+            // tag runs through 1 .. 2^32-1 (never 0, the value of a zeroed word):
+            // (call mod (2^32 - 1)) + 1, with call = counter / G and 2^32 = 1 mod (2^32 - 1)
+            const unsigned long long call = __umul64hi(old_count, P.dv_g64);
+            unsigned long long f = (call >> 32) + (call & 0xFFFFFFFFull);
+            f = (f >> 32) + (f & 0xFFFFFFFFull);
+            if (f >= 0xFFFFFFFFull) f -= 0xFFFFFFFFull;
+            misc[M_EPOCH] = (int)(uint32_t)(f + 1ull);
         }
     }
-    if (tid == dk::NCW * 32) misc[M_EPOCH] = (int)(old_count / (unsigned)G + 1u);
     __syncthreads();
     const int U = misc[M_U];
     const unsigned int epoch = (unsigned int)misc[M_EPOCH];
@@ -705,284 +554,355 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     // ---------------- work split
     const int tiles_gu = I >> 3;  // 16-row tiles of an expert's [2I][H] gate/up matrix
     const int KB1 = H >> 7, KB2 = I >> 7;
-    const int bytes1 = 9 * H, bytes2 = 9 * I;  // one 16-row tile of [.][H] or [.][I]
-    const int n1 = U * tiles_gu;                // <= 512 * 2048
-    const int p1_beg = (int)((unsigned)(n1 * c) / (unsigned)G), p1_end = (int)((unsigned)(n1 * (c + 1)) / (unsigned)G);
+    const int n1 = U * tiles_gu;
     const int n2 = H >> 4;
     const int o_beg = fdiv(n2 * c, P.dv_g), o_end = fdiv(n2 * (c + 1), P.dv_g);
-    const int J = P.J;
-    const int n_p1 = p1_end - p1_beg;
+    const float inv_u = 1.0f / (float)max(U, 1);
+    // r / U for 0 <= r < 2^20: float estimate, corrected by one step
+    auto div_u = [&](int r) {
+        int q = (int)((float)r * inv_u);
+        const int rem = r - q * U;
+        q += (rem >= U) - (rem < 0);
+        return q;
+    };
+    int p1_beg, p1_end;
+    {
+        // phase-1 share balanced by bytes against the phase-2 share: CTA c's boundary is
+        // proportional to c * tgt - (bytes of the down tiles of CTAs < c), in units of 9 bytes.
+        // Float rounding can move a boundary by a tile; both neighbours compute a boundary from
+        // the same expression, so the tiles still partition (at worst a tile is done twice).
+        const float b1 = (float)H, b2 = (float)I * (float)U;
+        float tgt = ((float)n1 * b1 + (float)n2 * b2) / (float)G;
+        tgt = fmaxf(tgt, (float)((n2 + G - 1) / G) * b2);
+        const float scale = (float)n1 / ((float)G * tgt - (float)n2 * b2);
+        p1_beg = c == 0 ? 0 : min(n1, __float2int_rn(((float)c * tgt - (float)o_beg * b2) * scale));
+        p1_end = c == G - 1 ? n1 : min(n1, __float2int_rn(((float)(c + 1) * tgt - (float)o_end * b2) * scale));
+        p1_end = max(p1_end, p1_beg);
+    }
+    const int n_t1 = p1_end - p1_beg;
     const int n_ot = o_end - o_beg;
-    const int n_jg = fdiv(U + J - 1, P.dv_j);  // expert groups per output tile
-    const int n_chunks = n_p1 + n_ot * n_jg;
+    const int nr2 = n_ot * U;  // phase-2 runs (output tile, expert), run r = otl * U + u
+    // this warp's K-block ranges: split evenly (runs shared by neighbouring warps), or whole runs
+    // per warp when a phase has more runs than warps
+    const bool split1 = n_t1 <= dk::NW, split2 = nr2 <= dk::NW;
+    const int ni1 = n_t1 * KB1, ni2 = nr2 * KB2;
+    int ib1, ie1, ib2, ie2;
+    if (split1) {
+        ib1 = (warp * ni1) >> dk::LOG_NW;
+        ie1 = ((warp + 1) * ni1) >> dk::LOG_NW;
+    } else {
+        ib1 = ((warp * n_t1) >> dk::LOG_NW) * KB1;
+        ie1 = (((warp + 1) * n_t1) >> dk::LOG_NW) * KB1;
+    }
+    if (split2) {
+        ib2 = (warp * ni2) >> dk::LOG_NW;
+        ie2 = ((warp + 1) * ni2) >> dk::LOG_NW;
+    } else {
+        ib2 = ((warp * nr2) >> dk::LOG_NW) * KB2;
+        ie2 = (((warp + 1) * nr2) >> dk::LOG_NW) * KB2;
+    }
+    const int cnt1 = ie1 - ib1, cnt = cnt1 + (ie2 - ib2);  // this warp's K-blocks, phase 1 then 2
 
-    if (warp == dk::NCW) {
-        // ---------------- producer: stream tiles into the ring
-        if (lane == 0) {
-            int n = 0, s = 0, use = 0;  // chunk, its stage and the stage's use
-            int u = 0, lt = 0;          // gate/up chunk: expert and tile within it
-            if (n_p1 > 0) {
-                u = fdiv(p1_beg, P.dv_tgu);
-                lt = p1_beg - u * tiles_gu;
-            }
-            int otl = 0, jg = 0;  // down chunk: output tile and expert group
-#pragma unroll 1
-            for (; n < n_chunks; ++n) {
-                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag)) break;
-                uint8_t* dst = ring + (size_t)s * P.stage_bytes;
-                if (n < n_p1) {
-                    const int wi = s_uwi[u];
-                    if (wi < 0) {
-                        mbar_arrive(&full[s]);
-                    } else {
-                        mbar_arrive_expect_tx(&full[s], (uint32_t)bytes1);
-                        bulk_g2s(dst, W.gu_codes + (int64_t)wi * W.gu_codes_stride + (int64_t)lt * bytes1,
-                                 (uint32_t)bytes1, &full[s]);
-                    }
-                    if (++lt == tiles_gu) {
-                        lt = 0;
-                        ++u;
-                    }
-                } else {
-                    const int ot = o_beg + otl;
-                    const int u0 = jg * J, nj = min(J, U - u0);
-                    uint32_t tx = 0;
-#pragma unroll 1
-                    for (int jj = 0; jj < nj; ++jj) tx += (s_uwi[u0 + jj] >= 0) ? (uint32_t)bytes2 : 0u;
-                    mbar_arrive_expect_tx(&full[s], tx);
-#pragma unroll 1
-                    for (int jj = 0; jj < nj; ++jj) {
-                        const int wi = s_uwi[u0 + jj];
-                        if (wi >= 0)
-                            bulk_g2s(dst + jj * bytes2, W.d_codes + (int64_t)wi * W.d_codes_stride + (int64_t)ot * bytes2,
-                                     (uint32_t)bytes2, &full[s]);
-                    }
-                    if (++jg == n_jg) {
-                        jg = 0;
-                        ++otl;
-                    }
-                }
-                tag_publish(&misc[M_TAGS + s], n);
-                if (++s == NS) {
-                    s = 0;
-                    ++use;
-                }
-            }
-            // Once every CTA of this grid has started (the call counter reaches epoch * G), the
-            // next kernel in the stream may be scheduled: it cannot take an SM one of ours still
-            // needs, and it waits for our completion itself before reading anything.
-            {
-                const unsigned long long t0 = globaltimer();
-                unsigned int v;
-                do {
-                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.bar) : "memory");
-                } while ((int)(v - epoch * (unsigned)G) < 0 && globaltimer() - t0 < 100000ull);
-                if ((int)(v - epoch * (unsigned)G) >= 0) griddep_launch_dependents();
-            }
-            // the CTA must not exit with copies still landing in its shared memory: wait
-            // (bounded, even after an abort) for the last use of every stage issued
-            const unsigned long long t0 = globaltimer();
-            int q = max(0, n - NS);
-            const int uq = fdiv(q, P.dv_ns);
-            int sq = q - uq * NS, pq = uq & 1;
-#pragma unroll 1
-            for (; q < n; ++q) {
-                while (!mbar_try_wait(&full[sq], pq) && globaltimer() - t0 < dk::WAIT_NS) {
-                }
-                if (++sq == NS) {
-                    sq = 0;
-                    pq ^= 1;
-                }
-            }
+    // ---------------- weight stream: per-lane async copies into this warp's ring.  The issue
+    // cursor walks this warp's K-blocks: within a run (a tile, or an (output tile, expert) pair)
+    // consecutive K-blocks are 1024 code bytes and 128 scale bytes apart.
+    int is_n = 0, is_left = 0, is_ph = 1, is_run = 0, is_kb0 = 0;
+    const uint8_t* is_cb = nullptr;  // codes of the next K-block (nullptr: expert without weights)
+    const uint8_t* is_sb = nullptr;  // its scales
+    // first K-block `kb` of run `run` of phase `ph` (run: local tile, or local (output tile, expert))
+    auto open_run = [&](int ph, int run, int kb, int left) {
+        is_ph = ph;
+        is_run = run;
+        is_left = left;
+        int wi, KB;
+        const uint8_t* base;
+        if (ph == 1) {
+            const int t = p1_beg + run;
+            const int u = fdiv(t, P.dv_tgu);
+            wi = s_uwi[u];
+            KB = KB1;
+            base = W.gu_codes + (int64_t)max(wi, 0) * W.gu_codes_stride + (int64_t)(t - u * tiles_gu) * (9 * H);
         } else {
-            // lanes 1..31: the tensor scales (gate, up, down) of the selected experts into shared
-            // memory, published once all are there
-#pragma unroll 1
-            for (int u = lane - 1; u < U; u += 31) {
-                const int wi = s_uwi[u];
-                const float* ts = W.tscale + (int64_t)(wi >= 0 ? wi : 0) * W.tscale_stride;
-                const float t0 = ts[0], t1 = ts[1], t2 = ts[2];
-                s_ts[4 * u + 0] = (wi >= 0) ? t0 : 0.0f;
-                s_ts[4 * u + 1] = (wi >= 0) ? t1 : 0.0f;
-                s_ts[4 * u + 2] = (wi >= 0) ? t2 : 0.0f;
-            }
-            __syncwarp(0xfffffffeu);
-            if (lane == 1) tag_publish(&misc[M_TS], 1);
+            const int otl = div_u(run), u = run - otl * U;
+            wi = s_uwi[u];
+            KB = KB2;
+            base = W.d_codes + (int64_t)max(wi, 0) * W.d_codes_stride + (int64_t)(o_beg + otl) * (9 * I);
         }
-        return;
+        is_cb = (wi >= 0) ? base + kb * 1024 : nullptr;
+        is_sb = base + KB * 1024 + kb * 128;
+    };
+    auto issue = [&]() {
+        if (is_n < cnt) {
+            if (is_n == cnt1) {  // this warp's first down K-block
+                const int r = ib2 / KB2, kb = ib2 - r * KB2;
+                open_run(2, r, kb, KB2 - kb);
+            } else if (is_left == 0) {  // next run of the same phase
+                open_run(is_ph, is_run + 1, 0, is_ph == 1 ? KB1 : KB2);
+            }
+            uint8_t* slot = ring + (is_n & (R - 1)) * dk::ITEM;
+            if (is_cb) {
+                cp16(slot + lane * 16, is_cb + lane * 16);
+                cp16(slot + 512 + lane * 16, is_cb + 512 + lane * 16);
+                cp4(slot + 1024 + lane * 4, is_sb + lane * 4);
+            } else {  // no weights behind this expert: zeros
+                *reinterpret_cast<uint4*>(slot + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(slot + 512 + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint32_t*>(slot + 1024 + lane * 4) = 0u;
+            }
+            if (is_cb) is_cb += 1024;
+            is_sb += 128;
+            --is_left;
+            ++is_n;
+            cp_commit();  // one group per K-block: the waits count groups
+        }
+    };
+    if (cnt1 > 0) {
+        const int tl = ib1 / KB1, kb = ib1 - tl * KB1;
+        open_run(1, tl, kb, KB1 - kb);
+    }
+    // the gate/up K-blocks go first; the down K-blocks follow as the ring frees up, the rest of them
+    // once this warp's gate/up K-blocks are all consumed (they land during the hand-off)
+#pragma unroll 1
+    for (int j = 0; j < min(R, cnt1 > 0 ? cnt1 : cnt); ++j) issue();
+    // tensor scales of the selected experts, read once the weights are on their way
+#pragma unroll 1
+    for (int u = tid; u < U; u += dk::THREADS) {
+        const int wi = s_uwi[u];
+        const float* ts = W.tscale + (int64_t)(wi >= 0 ? wi : 0) * W.tscale_stride;
+        s_ts[4 * u + 0] = (wi >= 0) ? __ldg(ts + 0) : 0.0f;
+        s_ts[4 * u + 1] = (wi >= 0) ? __ldg(ts + 1) : 0.0f;
+        s_ts[4 * u + 2] = (wi >= 0) ? __ldg(ts + 2) : 0.0f;
     }
 
-    // ---------------- consumers (warps 0 .. NCW-1), phase 1: gate/up tiles -> h words
-    const int gi = warp / dk::WPG, wig = warp % dk::WPG, gtid = tid % (dk::WPG * 32);
     const int g8 = lane >> 2, q4 = lane & 3;
-    const int TC = P.tcol;
-    const int hw_row = I / 2;  // h words per permuted row
+    const int hw_row = I >> 1;  // h words per permuted row
     unsigned long long* hw = reinterpret_cast<unsigned long long*>(a.hbuf);
-    float* gred = red + gi * 2 * dk::WPG * 16 * TC;  // this group's two partial buffers [WPG][16][TC]
-    int buf = 0;
-#pragma unroll 1
-    for (int n = gi; n < n_p1; n += dk::NG) {
-        const int t = p1_beg + n;
+
+    // partial tiles [16][TC]: this lane's accumulator (rows g8, g8+8; columns cg*8 + 2q4, +1)
+    auto store_acc = [&](float* dst, int cg, const float4& v, int tu) {
+        const int col = cg * 8 + 2 * q4;
+        if (col < tu) {
+            dst[g8 * TC + col] = v.x;
+            dst[(g8 + 8) * TC + col] = v.z;
+        }
+        if (col + 1 < tu) {
+            dst[g8 * TC + col + 1] = v.y;
+            dst[(g8 + 8) * TC + col + 1] = v.w;
+        }
+    };
+    // tensor scale j of expert index u: from shared memory once a CTA barrier has passed since it
+    // was stored (split phases), else from global memory
+    auto tscale = [&](int u, int j, bool shared) {
+        if (shared) return s_ts[4 * u + j];
+        const int wi = s_uwi[u];
+        return (wi >= 0) ? __ldg(W.tscale + (int64_t)wi * W.tscale_stride + j) : 0.0f;
+    };
+    // is warp w without K-blocks in a split phase of ni K-blocks?
+    auto empty_warp = [&](int w, int ni) { return ni && ((w * ni) >> dk::LOG_NW) == (((w + 1) * ni) >> dk::LOG_NW); };
+    // phase-1 epilogue of tile t (global index) from the partial tiles at tile + w*16*TC, w in
+    // [wlo, whi] (skipping warps without K-blocks of a split phase of ni K-blocks; ni = 0: none):
+    // h of the tile's 8 (gate, up) row pairs for its tu tokens, as h words; items (token, pair)
+    auto finish1 = [&](int t, const float* tile, int wlo, int whi, int ni, bool shared) {
         const int u = fdiv(t, P.dv_tgu), lt = t - u * tiles_gu;
         const int wi = s_uwi[u];
         const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
-        const int s = chunk_wait(full, misc + M_TAGS, n, P.dv_ns, abort_flag);
-        const uint8_t* tile = ring + (size_t)s * P.stage_bytes;
-        float* rb = gred + buf * dk::WPG * 16 * TC;
+        const float tsg = tscale(u, 0, shared), tsu = tscale(u, 1, shared);
+        // lane 8*tt' + pr handles pair pr of token tt; the 32 lanes cover 4 tokens per pass
 #pragma unroll 1
-        for (int c0 = 0; c0 < tu; c0 += 8) {
-            const int nt = min(8, tu - c0);
-            const int col = min(g8, nt - 1);
-            const int xr = s_ptok[pb + c0 + col];  // token of this lane's column
-            float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (wi >= 0) dv = tile_partial(tile, KB1, wig, dk::WPG, xs + xr * P.xs_stride);
-            const float d[4] = {dv.x, dv.y, dv.z, dv.w};
-            float* r = rb + wig * 16 * TC;
-            if (2 * q4 < nt) {
-                r[g8 * TC + c0 + 2 * q4] = d[0];
-                r[(g8 + 8) * TC + c0 + 2 * q4] = d[2];
-            }
-            if (2 * q4 + 1 < nt) {
-                r[g8 * TC + c0 + 2 * q4 + 1] = d[1];
-                r[(g8 + 8) * TC + c0 + 2 * q4 + 1] = d[3];
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        group_sync(gi);
-        // h = silu(g) * u for the tile's 8 (gate, up) row pairs: word j holds pairs 2j, 2j+1
-        tag_wait(&misc[M_TS], 1, abort_flag);
-        const float tsg = s_ts[4 * u + 0], tsu = s_ts[4 * u + 1];
+        for (int idx0 = 0; idx0 < 8 * tu; idx0 += 32) {
+            const int idx = idx0 + lane;
+            const int pr = idx & 7, tt = idx >> 3;
+            float hv = 0.0f;
+            if (idx < 8 * tu) {
+                float gs = 0.0f, us = 0.0f;
 #pragma unroll 1
-        for (int idx = gtid; idx < 4 * tu; idx += dk::WPG * 32) {
-            const int j = idx & 3, tt = idx >> 2;
-            float hv[2] = {0.0f, 0.0f};
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int p = 2 * j + h2;
-                float gs = 0.f, us = 0.f;
-#pragma unroll
-                for (int w = 0; w < dk::WPG; ++w) {
-                    gs += rb[(w * 16 + 2 * p) * TC + tt];
-                    us += rb[(w * 16 + 2 * p + 1) * TC + tt];
+                for (int w = wlo; w <= whi; ++w) {
+                    if (empty_warp(w, ni)) continue;
+                    const float* s = tile + w * 16 * TC;
+                    gs += s[(2 * pr) * TC + tt];
+                    us += s[(2 * pr + 1) * TC + tt];
                 }
                 if (wi >= 0) {
                     const float sc = pow2i(misc[M_XEXP + s_ptok[pb + tt]]);
-                    hv[h2] = silu_f32(gs * tsg * sc) * (us * tsu * sc);
+                    hv = silu_f32(gs * tsg * sc) * (us * tsu * sc);
                 }
             }
-            const unsigned long long word = (unsigned long long)bf16_bits(hv[0]) |
-                                            ((unsigned long long)bf16_bits(hv[1]) << 16) | ((unsigned long long)epoch << 32);
-            st_relaxed_u64(hw + (int64_t)(pb + tt) * hw_row + lt * 4 + j, word);
+            // lanes of pairs 2j, 2j+1 are neighbours: the even one stores the word
+            const uint32_t hb = bf16_bits(hv);
+            const uint32_t hb1 = __shfl_down_sync(0xffffffffu, hb, 1);
+            if (idx < 8 * tu && !(pr & 1))
+                st_relaxed_u64(hw + (int64_t)(pb + tt) * hw_row + lt * 4 + (pr >> 1),
+                               (unsigned long long)(hb | (hb1 << 16)) | ((unsigned long long)epoch << 32));
         }
-        buf ^= 1;
+    };
+    // phase-2 epilogue of run r (local index: output tile r / U, expert r % U)
+    auto finish2 = [&](int r, const float* tile, int wlo, int whi, int ni, bool shared) {
+        const int otl = div_u(r), u = r - otl * U;
+        const int wi = s_uwi[u];
+        const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
+        const float tsd = tscale(u, 2, shared);
+#pragma unroll 1
+        for (int idx = lane; idx < 16 * tu; idx += 32) {
+            const int row = idx & 15, tt = idx >> 4;
+            float ys = 0.0f;
+#pragma unroll 1
+            for (int w = wlo; w <= whi; ++w)
+                if (!empty_warp(w, ni)) ys += tile[w * 16 * TC + row * TC + tt];
+            const int p = pb + tt;
+            ys = (wi >= 0) ? ys * (tsd * pow2i(s_hexp[p])) : 0.0f;
+            ybuf[(otl * nf + s_plist[p]) * 16 + row] = ys;
+            if (a.y) a.y[(int64_t)p * H + (o_beg + otl) * 16 + row] = ys;
+        }
+    };
+    // warps whose K-block range of a split phase covers run r (KB K-blocks per run, ni in all):
+    // warp(i) = floor(((i + 1) * NW - 1) / ni) covers K-block i
+    auto cover = [&](int r, int KB, int ni, int& wlo, int& whi) {
+        wlo = ((r * KB + 1) * dk::NW - 1) / ni;
+        whi = (((r + 1) * KB) * dk::NW - 1) / ni;
+    };
+
+    // this warp's K-blocks [ib, ie) of a phase (KB per run), consumed in ring order n0, n0+1, ...:
+    // runs in turn, each accumulated in registers, then flushed into its slot (split phase) or
+    // finished in the warp (whole runs)
+    auto run_phase = [&](int ph, int n0, int ib, int ie, int KB, bool split) {
+        int n = n0;
+#pragma unroll 1
+        for (int i = ib; i < ie;) {
+            const int run = fdiv(i, ph == 1 ? P.dv_kb1 : P.dv_kb2);
+            const int kb0 = i - run * KB, kb1 = min(KB, kb0 + (ie - i));
+            int pb, tu;
+            const __half* r0;
+            const __half* r1;
+            if (ph == 1) {
+                const int u = fdiv(p1_beg + run, P.dv_tgu);
+                pb = s_ubeg[u];
+                tu = s_ubeg[u + 1] - pb;
+                r0 = xs + s_ptok[pb + min(g8, tu - 1)] * P.xs_stride + q4 * 8;
+                r1 = xs + s_ptok[pb + min(8 + g8, tu - 1)] * P.xs_stride + q4 * 8;
+            } else {
+                const int u = run - div_u(run) * U;
+                pb = s_ubeg[u];
+                tu = s_ubeg[u + 1] - pb;
+                r0 = hs + (pb + min(g8, tu - 1)) * P.hs_stride + q4 * 8;
+                r1 = hs + (pb + min(8 + g8, tu - 1)) * P.hs_stride + q4 * 8;
+            }
+            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+#pragma unroll 1
+            for (int kb = kb0; kb < kb1; ++kb, ++n) {
+                cp_wait_upto(is_n - n - 1);  // K-block n of this lane has landed
+                const uint8_t* slot = ring + (n & (R - 1)) * dk::ITEM;
+                const float4 v = kblock_partial(slot, r0 + kb * 128);
+                acc0.x += v.x, acc0.y += v.y, acc0.z += v.z, acc0.w += v.w;
+                if (tu > 8) {
+                    const float4 v1 = kblock_partial(slot, r1 + kb * 128);
+                    acc1.x += v1.x, acc1.y += v1.y, acc1.z += v1.z, acc1.w += v1.w;
+                }
+                issue();  // into the slot just read (this lane's own bytes)
+            }
+            float* dst = split ? slots + (run + warp) * 16 * TC : wscr + warp * 16 * TC;
+            store_acc(dst, 0, acc0, tu);
+            if (tu > 8) store_acc(dst, 1, acc1, tu);
+            if (!split) {
+                __syncwarp();
+                if (ph == 1) finish1(p1_beg + run, dst, 0, 0, 0, false);
+                else finish2(run, dst, 0, 0, 0, false);
+                __syncwarp();
+            }
+            i += kb1 - kb0;
+        }
+    };
+
+    // ---------------- phase 1: gate/up K-blocks -> partial tiles -> h words
+    run_phase(1, 0, ib1, ie1, KB1, split1);
+#pragma unroll 1
+    while (is_n < min(cnt, cnt1 + R)) issue();  // the ring full of down K-blocks before the hand-off
+    if (split1) {
+        __syncthreads();
+        // tiles shared by warps: sum the slots in warp order
+#pragma unroll 1
+        for (int tl = warp; tl < n_t1; tl += dk::NW) {
+            int wlo, whi;
+            cover(tl, KB1, ni1, wlo, whi);
+            finish1(p1_beg + tl, slots + tl * 16 * TC, wlo, whi, ni1, true);
+        }
+    }
+    if (n_ot == 0) {
+        cp_wait<0>();  // no copy may land after the CTA exits
+        return;
     }
 
-    // ---------------- phase 2: down projection over this CTA's output rows
-    if (n_ot > 0)  // all h rows (permuted order), as each becomes available
-        stage_h(s_hexp, misc + M_HFLAG, hs, P.hs_stride, hw, nf, I, P.dv_hrow, epoch, abort_flag);
-    tag_wait(&misc[M_TS], 1, abort_flag);
+    // ---------------- phase 2: all h rows (permuted order) staged as f16, as each becomes available
     {
-        // chunks n_p1 .. n_chunks-1, round robin over the groups continuing phase 1's order;
-        // chunk n_p1 + m is (output tile m / n_jg, expert group m mod n_jg)
-        int n = n_p1 + ((gi - n_p1) % dk::NG + dk::NG) % dk::NG;
-        int otl = 0, jg = n - n_p1;
-        while (n_jg > 0 && jg >= n_jg) {
-            jg -= n_jg;
-            ++otl;
-        }
+        const unsigned int want = (P.wait_site == FT_WAIT_SITE_DECODE_H) ? (epoch ^ 0x80000000u) : epoch;
+        const int total = nf * hw_row;
+        bool big = false;
+        // B loads in flight per thread; words whose tag is not there yet are read again, all
+        // together, until they are (bounded)
+        constexpr int B = 4;
 #pragma unroll 1
-        for (; n < n_chunks; n += dk::NG) {
-            const int ot = o_beg + otl;
-            const int u0 = jg * J, nj = min(J, U - u0);
-            // warps per expert tile: with one or two experts in the chunk the group's four warps
-            // split each tile's K-blocks, and their partials are summed through shared memory
-            const int wpe = (nj == 1) ? dk::WPG : (nj == 2) ? dk::WPG / 2 : (nj <= 4 && dk::WPG >= 8) ? dk::WPG / 4 : 1;
-            const int s = chunk_wait(full, misc + M_TAGS, n, P.dv_ns, abort_flag);
-            const uint8_t* slot = ring + (size_t)s * P.stage_bytes;
-            float* rb = gred + buf * dk::WPG * 16 * TC;
+        for (int base = tid; base < total; base += B * dk::THREADS) {
+            unsigned long long v[B];
+            uint32_t pending = 0;
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                const int idx = base + u * dk::THREADS;
+                if (idx < total) {
+                    v[u] = ld_relaxed_u64(hw + idx);
+                    pending |= ((uint32_t)(v[u] >> 32) != want) << u;
+                }
+            }
+            if (pending) {
+                const unsigned long long t0 = globaltimer();
 #pragma unroll 1
-            for (int jj = wig / wpe; jj < nj; jj += dk::WPG / wpe) {
-                const int u = u0 + jj;
-                const int wi = s_uwi[u];
-                const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
-                const float tsd = s_ts[4 * u + 2];
-#pragma unroll 1
-                for (int c0 = 0; c0 < tu; c0 += 8) {
-                    const int nt = min(8, tu - c0);
-                    const int col = min(g8, nt - 1);
-                    float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (wi >= 0)
-                        dv = tile_partial(slot + jj * bytes2, KB2, wig & (wpe - 1), wpe, hs + (pb + c0 + col) * P.hs_stride);
-                    const float d[4] = {dv.x, dv.y, dv.z, dv.w};
-                    if (wpe > 1) {  // this warp's share of the K-blocks, summed below
-                        float* r = rb + wig * 16 * TC;
-                        if (2 * q4 < nt) {
-                            r[g8 * TC + c0 + 2 * q4] = d[0];
-                            r[(g8 + 8) * TC + c0 + 2 * q4] = d[2];
-                        }
-                        if (2 * q4 + 1 < nt) {
-                            r[g8 * TC + c0 + 2 * q4 + 1] = d[1];
-                            r[(g8 + 8) * TC + c0 + 2 * q4 + 1] = d[3];
-                        }
-                        continue;
+                while (pending) {
+                    if (*abort_flag) break;
+                    if (globaltimer() - t0 > P.wait_ns) {
+                        *abort_flag = 1;
+                        raise_dev_error(FT_DEVERR_TIMEOUT);
+                        break;
                     }
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int cc = c0 + 2 * q4 + h2;  // column of d[h2] (row g8) and d[2 + h2] (row g8 + 8)
-                        if (2 * q4 + h2 < nt) {
-                            const int p = pb + cc;
-                            const float sc = (wi >= 0) ? tsd * pow2i(s_hexp[p]) : 0.0f;
-                            const int f = s_plist[p];
-                            const float y0 = d[h2] * sc, y1 = d[2 + h2] * sc;
-                            ybuf[(otl * nf + f) * 16 + g8] = y0;
-                            ybuf[(otl * nf + f) * 16 + g8 + 8] = y1;
-                            if (a.y) {
-                                a.y[(int64_t)p * H + ot * 16 + g8] = y0;
-                                a.y[(int64_t)p * H + ot * 16 + g8 + 8] = y1;
-                            }
-                        }
-                    }
+                    for (int u = 0; u < B; ++u)
+                        if (pending & (1u << u)) v[u] = ld_relaxed_u64(hw + base + u * dk::THREADS);
+#pragma unroll
+                    for (int u = 0; u < B; ++u)
+                        if ((pending & (1u << u)) && (uint32_t)(v[u] >> 32) == want) pending &= ~(1u << u);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            if (wpe > 1) {
-                group_sync(gi);
-                // item idx of expert e2: row idx & 15, column idx >> 4
-#pragma unroll 1
-                for (int e2 = 0; e2 < nj; ++e2) {
-                    const int u = u0 + e2;
-                    const int wi = s_uwi[u];
-                    const int pb = s_ubeg[u], tu = s_ubeg[u + 1] - pb;
-                    const float tsd = s_ts[4 * u + 2];
-#pragma unroll 1
-                    for (int idx = gtid; idx < 16 * tu; idx += dk::WPG * 32) {
-                        const int r = idx & 15, tt = idx >> 4;
-                        float ys = 0.0f;
-#pragma unroll 1
-                        for (int w = 0; w < wpe; ++w) ys += rb[((e2 * wpe + w) * 16 + r) * TC + tt];
-                        const int p = pb + tt;
-                        ys = (wi >= 0) ? ys * (tsd * pow2i(s_hexp[p])) : 0.0f;
-                        ybuf[(otl * nf + s_plist[p]) * 16 + r] = ys;
-                        if (a.y) a.y[(int64_t)p * H + ot * 16 + r] = ys;
-                    }
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                const int idx = base + u * dk::THREADS;
+                if (idx < total) {
+                    const int r = fdiv(idx, P.dv_hrow), cc = idx - r * hw_row;
+                    *reinterpret_cast<uint32_t*>(hs + r * P.hs_stride + staged_pos(2 * cc)) =
+                        bf16x2_to_f16x2((uint32_t)v[u], big);
                 }
-                buf ^= 1;
-            }
-            jg += dk::NG;
-            while (jg >= n_jg) {
-                jg -= n_jg;
-                ++otl;
             }
         }
+        if (big) misc[M_HFLAG] = 1;
+        __syncthreads();
+        if (misc[M_HFLAG]) {
+            restage_scaled(s_hexp, hs, P.hs_stride, nf, I, nullptr, hw);
+            __syncthreads();
+        }
     }
-    consumer_sync();
+    run_phase(2, cnt1, ib2, ie2, KB2, split2);
+    cp_wait<0>();
+    __syncthreads();
+    if (split2) {
+#pragma unroll 1
+        for (int r = warp; r < nr2; r += dk::NW) {
+            int wlo, whi;
+            cover(r, KB2, ni2, wlo, whi);
+            finish2(r, slots + r * 16 * TC, wlo, whi, ni2, true);
+        }
+        __syncthreads();
+    }
     // combine: out[t][row] = bf16(sum_j w[t][j] * y[t*k + j][row]) in slot order j;
     // item i = (otl * T + tok) * 16 + row
     if (a.out) {
 #pragma unroll 1
-        for (int i = tid; i < n_ot * 16 * T; i += dk::NCW * 32) {
+        for (int i = tid; i < n_ot * 16 * T; i += dk::THREADS) {
             const int q = i >> 4, r = i & 15;
             const int otl = fdiv(q, P.dv_t), tok = q - otl * T;
             float acc = 0.0f;
@@ -1047,10 +967,11 @@ static int sm_count() {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Shared memory: barriers and routing tables, staged activations (x in phase
-// 1, h in phase 2, same area), the groups' partial tiles, the per-slot down
-// outputs, and the ring (one 16-row tile of the wider matrix per stage).
-static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::string& why) {
+// Shared memory: routing and grouping tables, staged x, one area that holds the
+// raw inputs and the router's candidates and later the staged h rows, the
+// partial-tile slots, the warps' scratch tiles, the per-slot down outputs and
+// the warps' K-block rings (R slots each: 16, else 8, 4 or 2, whichever fits).
+static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mode, DecodePlan& p, std::string& why) {
     const int nf = T * k;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -1058,7 +979,10 @@ static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::s
         off = align_up(off + bytes, 128);
         return (int)o;
     };
-    p.off_bars = take((2 * dk::MAXNS + 1) * 8);
+    p.nb = (E + 31) / 32;
+    p.kk = std::min(k, 32);
+    const int C = p.nb * p.kk;
+    p.off_misc = take(M_COUNT * 4);
     p.off_ids = take((size_t)nf * 4);
     p.off_wts = take((size_t)nf * 4);
     p.off_plist = take((size_t)nf * 4);
@@ -1068,62 +992,89 @@ static bool plan_decode(int T, int k, int H, int I, int G, DecodePlan& p, std::s
     p.off_ulist = take((size_t)nf * 4);
     p.off_ubeg = take((size_t)(nf + 1) * 4);
     p.off_uwi = take((size_t)nf * 4);
-    p.off_misc = take((4 + dk::MAXT + dk::MAXNS + 2) * 4);
     p.off_ts = take((size_t)nf * 16);
+    p.off_rank = take(route_mode ? (size_t)T * C * 4 : 4);
     p.xs_stride = H + dk::XPAD;
     p.hs_stride = I + dk::XPAD;
-    // the h staging area first receives x as bf16 [T][H] (the prologue's bulk copy)
-    const size_t xs = (size_t)T * p.xs_stride * 2, hs = std::max((size_t)nf * p.hs_stride * 2, (size_t)T * H * 2);
-    if (xs + hs > dk::XS_BUDGET) {
-        why = "activations of " + std::to_string(T) + " tokens and their " + std::to_string(nf) +
-              " expert rows do not fit the fused kernel's staging area";
-        return false;
-    }
-    p.off_xs = take(xs);
-    p.off_hs = take(hs);
-    p.tcol = T;
-    p.off_red = take((size_t)dk::NG * 2 * dk::WPG * 16 * T * 4);
+    p.off_xs = take((size_t)T * p.xs_stride * 2);
+    const size_t lg_bytes = route_mode ? align_up((size_t)T * E * 4, 16) : 0;
+    const size_t xraw_bytes = align_up((size_t)T * H * 2, 16);
+    const size_t cand_bytes = route_mode ? (size_t)T * C * 8 : 0;
+    const size_t big = std::max((size_t)nf * p.hs_stride * 2, lg_bytes + xraw_bytes + cand_bytes);
+    p.off_big = take(big);
+    p.off_xraw = p.off_big + (int)lg_bytes;
+    p.off_cand = p.off_xraw + (int)xraw_bytes;
+    p.tc = T;
+    p.off_slot = take((size_t)dk::MAXSLOT * 16 * T * 4);
+    p.off_wscr = take((size_t)dk::NW * 16 * T * 4);
     const int n2 = H / 16;
     p.max_ot = (n2 + G - 1) / G;
     p.off_ybuf = take((size_t)p.max_ot * nf * 16 * 4);
-    p.stage_bytes = (int)align_up((size_t)9 * std::max(H, I), 128);
     p.off_ring = (int)off;
-    if (off + 2 * (size_t)p.stage_bytes > dk::SMEM_BUDGET) {
-        why = "layer too large for the fused kernel's shared memory";
+    p.ring = 0;
+    for (int r : {16, 8, 4, 2})
+        if (off + (size_t)dk::NW * r * dk::ITEM <= dk::SMEM_BUDGET) {
+            p.ring = r;
+            break;
+        }
+    if (!p.ring) {
+        why = "activations of " + std::to_string(T) + " tokens and their " + std::to_string(nf) +
+              " expert rows do not fit the fused kernel's shared memory";
         return false;
     }
-    p.nstages = (int)std::min<size_t>(dk::MAXNS, (dk::SMEM_BUDGET - off) / p.stage_bytes);
-    p.smem = (int)(off + (size_t)p.nstages * p.stage_bytes);
-    // down tiles per stage: as many as a stage holds; for long down rows (8+ K-blocks) few enough
-    // that every group gets a chunk per output tile and splits its tiles' K-blocks
-    p.J = std::max(1, std::min(p.stage_bytes / (9 * I), 16));
-    if (I / 128 >= 8) p.J = std::max(1, std::min(p.J, (nf + dk::NG - 1) / dk::NG));
-    p.dv_ns = make_fastdiv((uint32_t)p.nstages);
-    p.dv_tgu = make_fastdiv((uint32_t)(I / 8));
+    p.smem = (int)(off + (size_t)dk::NW * p.ring * dk::ITEM);
     p.dv_k = make_fastdiv((uint32_t)k);
     p.dv_xrow = make_fastdiv((uint32_t)(H / 8));
     p.dv_hrow = make_fastdiv((uint32_t)(I / 2));
     p.dv_g = make_fastdiv((uint32_t)G);
     p.dv_t = make_fastdiv((uint32_t)T);
-    p.dv_j = make_fastdiv((uint32_t)p.J);
+    p.dv_nb = make_fastdiv((uint32_t)p.nb);
+    p.dv_c = make_fastdiv((uint32_t)C);
+    p.dv_tgu = make_fastdiv((uint32_t)(I / 8));
+    p.dv_kb1 = make_fastdiv((uint32_t)(H / 128));
+    p.dv_kb2 = make_fastdiv((uint32_t)(I / 128));
+    // ceil(2^64 / G): mulhi(x, m) = floor(x / G) for every x below 2^64 / G (the error of m, under G,
+    // times x stays under 2^64)
+    p.dv_g64 = (G <= 1) ? ~0ull : (~0ull / (unsigned long long)G) + 1ull;
     p.inv_k = 1.0f / (float)k;
+    p.wait_ns = g_wait_ns.load();
+    p.wait_site = g_wait_site.load();
     return true;
 }
 
-static ft_status launch_decode(const DecodeArgs& args0, ft_stream_t stream, const char* fn) {
-    const ft_moe_layer_weights& W = args0.W;
+// The kernels' shared-memory limit, set once per device before the first launch there.
+static ft_status decode_attributes(const char* fn) {
+    static std::mutex mu;
+    static bool done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fail(FT_ERR_CUDA, std::string(fn) + ": no current device");
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return FT_OK;
+    const cudaError_t errs[4] = {
+        cudaFuncSetAttribute(k_moe_decode<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET),
+        cudaFuncSetAttribute(k_moe_decode<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET),
+        cudaFuncSetAttribute(k_moe_decode<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET),
+        cudaFuncSetAttribute(k_moe_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET)};
+    for (cudaError_t e : errs)
+        if (e != cudaSuccess) {
+            cudaGetLastError();  // not sticky: leave no error behind for the launch check
+            return fail(FT_ERR_CUDA, std::string(fn) + ": setting the shared-memory limit: " + cudaGetErrorString(e));
+        }
+    done[dev] = true;
+    return FT_OK;
+}
+
+static ft_status launch_decode(DecodeArgs a, ft_stream_t stream, const char* fn) {
+    const ft_moe_layer_weights& W = a.W;
     const int G = sm_count();
-    DecodeArgs a = args0;
     std::string why;
-    if (!plan_decode(a.T, a.k, W.H, W.I, G, a.P, why)) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
-    // the router's logits come in by one bulk copy when their address and size allow it
-    const size_t lbytes = (size_t)a.T * W.E * 4;
-    a.P.logits_bulk = a.logits && aligned(a.logits, 16) && lbytes % 16 == 0 &&
-                      lbytes <= (size_t)a.P.nstages * a.P.stage_bytes;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaFuncSetAttribute(k_moe_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET);
-    });
+    if (!plan_decode(a.T, a.k, W.E, W.H, W.I, G, a.logits != nullptr, a.P, why))
+        return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
+    ft_status st = decode_attributes(fn);
+    if (st != FT_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(dk::THREADS);
@@ -1134,7 +1085,11 @@ static ft_status launch_decode(const DecodeArgs& args0, ft_stream_t stream, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_moe_decode, a);
+    cudaError_t e;
+    if (a.P.ring == 16) e = cudaLaunchKernelEx(&cfg, k_moe_decode<16>, a);
+    else if (a.P.ring == 8) e = cudaLaunchKernelEx(&cfg, k_moe_decode<8>, a);
+    else if (a.P.ring == 4) e = cudaLaunchKernelEx(&cfg, k_moe_decode<4>, a);
+    else e = cudaLaunchKernelEx(&cfg, k_moe_decode<2>, a);
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
     return check_launch(fn);
 }
@@ -1165,11 +1120,29 @@ ft_status decode_tiles_grouped(const ft_moe_layer_weights* W, const uint16_t* x,
     a.x = x;
     a.out = out;
     a.y = y;
-    a.bar = static_cast<unsigned int*>(ws);
+    a.bar = static_cast<unsigned long long*>(ws);
     a.hbuf = static_cast<char*>(ws) + 256;
     a.T = T;
     a.k = k;
     return launch_decode(a, stream, fn);
+}
+
+// Argument checks of the fused decode step (shared by both entry points).
+static ft_status check_layer_decode_args(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x, int T,
+                                         int k, uint16_t* out, int32_t* ids, float* w, const char* fn) {
+    ft_status st = validate_weights(W, fn);
+    if (st != FT_OK) return st;
+    if (W->layout != FT_LAYOUT_DECODE_TILES)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights must use FT_LAYOUT_DECODE_TILES");
+    if (T < 0 || T > dk::MAXT || k <= 0 || k > W->E || k > dk::MAXK)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 0 <= T <= 16 and 1 <= k <= min(E, 32)");
+    if (T == 0) return FT_OK;
+    if (!logits || !x || !out) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if ((ids == nullptr) != (w == nullptr))
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": give both ids and w or neither");
+    if (!aligned(x, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": x needs 16-byte alignment");
+    if (!aligned(logits, 4)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": logits need 4-byte alignment");
+    return FT_OK;
 }
 
 }  // namespace ft
@@ -1189,6 +1162,16 @@ ft_status ft_nvfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 64);
     k_pack_tiles<<<(unsigned)blocks, 256, 0, cu(stream)>>>(codes, codes_ld, scales, scales_ld, N, K, tiles);
     return check_launch("ft_nvfp4_pack_tiles");
+}
+
+ft_status ft_debug_inject_wait_expiry(int site, uint64_t limit_ns) {
+    if (site != FT_WAIT_SITE_NONE && site != FT_WAIT_SITE_DECODE_H)
+        return fail(FT_ERR_INVALID_ARG, "ft_debug_inject_wait_expiry: unknown wait site");
+    if (site != FT_WAIT_SITE_NONE && (limit_ns == 0 || limit_ns > dk::WAIT_NS))
+        return fail(FT_ERR_INVALID_ARG, "ft_debug_inject_wait_expiry: need 0 < limit_ns <= 2 s");
+    g_wait_ns.store(site == FT_WAIT_SITE_NONE ? dk::WAIT_NS : limit_ns);
+    g_wait_site.store(site);
+    return FT_OK;
 }
 
 }  // extern "C"
@@ -1232,11 +1215,9 @@ extern "C" {
 ft_status ft_moe_layer_decode_noalloc(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x, int T,
                                       int k, uint16_t* out, int32_t* ids, float* w, ft_stream_t stream) {
     const char* fn = "ft_moe_layer_decode_noalloc";
-    ft_status st = validate_weights(W, fn);
-    if (st != FT_OK) return st;
-    if (T < 0 || T > dk::MAXT || k <= 0 || k > W->E || k > dk::MAXK)
-        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 0 <= T <= 16 and 1 <= k <= min(E, 32)");
-    if (T == 0) return FT_OK;
+    // every argument check comes before any CUDA call
+    ft_status st = check_layer_decode_args(W, logits, x, T, k, out, ids, w, fn);
+    if (st != FT_OK || T == 0) return st;
     const size_t need = fused_workspace_size(T, k, W->I);
     if (need > kNoAllocScratchBytes)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": T*k*I = " + std::to_string((size_t)T * k * W->I) +
@@ -1260,17 +1241,8 @@ size_t ft_moe_layer_decode_workspace_size(int T, int k, int H, int I) {
 ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x, int T, int k,
                               uint16_t* out, int32_t* ids, float* w, void* ws, size_t ws_bytes, ft_stream_t stream) {
     const char* fn = "ft_moe_layer_decode";
-    ft_status st = validate_weights(W, fn);
-    if (st != FT_OK) return st;
-    if (W->layout != FT_LAYOUT_DECODE_TILES)
-        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights must use FT_LAYOUT_DECODE_TILES");
-    if (T < 0 || T > dk::MAXT || k <= 0 || k > W->E || k > dk::MAXK)
-        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 0 <= T <= 16 and 1 <= k <= min(E, 32)");
-    if (T == 0) return FT_OK;
-    if (!logits || !x || !out) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
-    if ((ids == nullptr) != (w == nullptr))
-        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": give both ids and w or neither");
-    if (!aligned(x, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": x needs 16-byte alignment");
+    ft_status st = check_layer_decode_args(W, logits, x, T, k, out, ids, w, fn);
+    if (st != FT_OK || T == 0) return st;
     const size_t need = fused_workspace_size(T, k, W->I);
     if (!ws || ws_bytes < need || !aligned(ws, 256))
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": workspace missing, too small or not 256-byte aligned");
@@ -1281,7 +1253,7 @@ ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits
     {
         DecodePlan probe;
         std::string why;
-        while (Tc > 0 && !plan_decode(Tc, k, W->H, W->I, sm_count(), probe, why)) --Tc;
+        while (Tc > 0 && !plan_decode(Tc, k, W->E, W->H, W->I, sm_count(), true, probe, why)) --Tc;
         if (Tc == 0) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
     }
     for (int t0 = 0; t0 < T; t0 += Tc) {
@@ -1292,7 +1264,7 @@ ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits
         a.out = out + (int64_t)t0 * W->H;
         a.ids_out = ids ? ids + (int64_t)t0 * k : nullptr;
         a.w_out = w ? w + (int64_t)t0 * k : nullptr;
-        a.bar = static_cast<unsigned int*>(ws);
+        a.bar = static_cast<unsigned long long*>(ws);
         a.hbuf = static_cast<char*>(ws) + 256;
         a.T = std::min(Tc, T - t0);
         a.k = k;

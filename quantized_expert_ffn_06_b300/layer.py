@@ -5,6 +5,8 @@ buffers allocated once.
 """
 from __future__ import annotations
 
+import time
+
 import torch
 
 from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_ROWS, FT_LAYOUT_UMMA_TILES, ft_gen_normal_f32,
@@ -14,6 +16,16 @@ from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_ROWS, FT_LAYOUT_UMMA_TILES, ft_
                ft_nvfp4_pack_umma, ft_nvfp4_quantize_weight)
 
 PROJ_GATE, PROJ_UP, PROJ_DOWN = 0, 1, 2
+
+
+def wait_event(event, timeout_s: float, what: str) -> None:
+    """Host wait for a CUDA event (anything with query()), bounded: raises FtError(FT_ERR_TIMEOUT) once timeout_s
+    seconds have passed without the event completing, instead of blocking for ever."""
+    from . import FT_ERR_TIMEOUT, FtError
+    deadline = time.monotonic() + timeout_s
+    while not event.query():
+        if time.monotonic() > deadline:
+            raise FtError(FT_ERR_TIMEOUT, f"{what}: not complete after {timeout_s} s")
 
 
 class LayerWeights:
@@ -104,6 +116,70 @@ class LayerWeights:
             for proj in (PROJ_GATE, PROJ_UP, PROJ_DOWN):
                 ft_gen_normal_f32(seed, stream_of(e, proj), H * I, sigma, tmp[proj], stream=stream)
             self.set_expert(e, tmp[0].view(I, H), tmp[1].view(I, H), tmp[2].view(H, I), stream=stream)
+
+
+class MoEWeights:
+    """The layer weights handle (ft_moe_weights_create) over canonical NVFP4 experts held by a row-layout
+    LayerWeights: each expert's gate, up and down matrices are described in place (gate and up are the even and odd
+    rows of the interleaved [2I][H] matrix) and repacked by the library into the requested layouts.
+    view(layout) gives the descriptor object the layer calls take."""
+
+    def __init__(self, canonical: LayerWeights, layout_flags: int, stream=None):
+        from . import MoEWeightsHandle
+        assert canonical.layout == FT_LAYOUT_ROWS
+        c = canonical
+        H, I = c.H, c.I
+        experts = []
+        for e in range(c.n):
+            guc, gus, dc, ds = (t[e].data_ptr() for t in (c.gu_codes, c.gu_scales, c.d_codes, c.d_scales))
+            ts = c.tscale[e].data_ptr()
+            experts.append(((guc, H, gus, H // 8, ts), (guc + H // 2, H, gus + H // 16, H // 8, ts + 4),
+                            (dc, I // 2, ds, I // 16, ts + 8)))
+        self.handle = MoEWeightsHandle(experts, H, I, layout_flags, stream=stream)
+        self.E, self.H, self.I, self.device = c.n, H, I, c.device
+
+    def view(self, layout: int) -> "_HandleView":
+        return _HandleView(self, layout)
+
+
+class _DeviceBytes:
+    """A library-owned device range presented to torch (zero copy, through the CUDA array interface)."""
+
+    def __init__(self, ptr: int, nbytes: int):
+        self.__cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False), "version": 3}
+
+
+def _rows_view(ptr: int, n: int, row_bytes: int, stride: int, device) -> torch.Tensor:
+    flat = torch.as_tensor(_DeviceBytes(ptr, (n - 1) * stride + row_bytes), device=device)
+    return flat.as_strided((n, row_bytes), (stride, 1))
+
+
+class _HandleView:
+    """Descriptor of one layout held by a MoEWeights handle, with torch views of its bytes (per expert:
+    gu_codes, d_codes, and for the row layout gu_scales, d_scales; tscale [E, 4])."""
+
+    def __init__(self, w: MoEWeights, layout: int):
+        self.w, self.layout = w, layout
+        self.E, self.H, self.I, self.n, self.device = w.E, w.H, w.I, w.E, w.device
+        self.expert_to_slot = None
+        d = w.handle.describe(layout)
+        E, H, I, dev = w.E, w.H, w.I, w.device
+        if layout == FT_LAYOUT_ROWS:
+            self.gu_codes = _rows_view(d.gu_codes, E, 2 * I * H // 2, d.gu_codes_stride, dev).view(E, 2 * I, H // 2)
+            self.d_codes = _rows_view(d.d_codes, E, H * I // 2, d.d_codes_stride, dev).view(E, H, I // 2)
+            self.gu_scales = _rows_view(d.gu_scales, E, 2 * I * H // 16, d.gu_scales_stride, dev).view(E, 2 * I, H // 16)
+            self.d_scales = _rows_view(d.d_scales, E, H * I // 16, d.d_scales_stride, dev).view(E, H, I // 16)
+        else:
+            self.gu_codes = _rows_view(d.gu_codes, E, 2 * I * H * 9 // 16, d.gu_codes_stride, dev)
+            self.d_codes = _rows_view(d.d_codes, E, H * I * 9 // 16, d.d_codes_stride, dev)
+            self.gu_scales = self.d_scales = None
+        self.tscale = _rows_view(d.tscale, E, 16, 16, dev).view(torch.float32)
+
+    def desc(self) -> ft_moe_layer_weights:
+        d = self.w.handle.describe(self.layout)
+        if self.expert_to_slot is not None:
+            d.expert_to_slot = self.expert_to_slot.data_ptr()
+        return d
 
 
 class PrefillLayer:
@@ -360,8 +436,9 @@ class CachedDecodeLayer:
     slot table -> the fused layer kernel (which routes again, identically, and reads weights through the table).
     """
 
-    def __init__(self, pool: ExpertSlotPool, layer: int, k: int, T: int, copy_stream=None):
+    def __init__(self, pool: ExpertSlotPool, layer: int, k: int, T: int, copy_stream=None, timeout_s: float = 2.0):
         self.pool, self.layer, self.k, self.T = pool, layer, k, T
+        self.timeout_s = timeout_s
         dev = pool.device
         self.weights = pool.layer_weights(layer)
         self.ids = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -378,7 +455,7 @@ class CachedDecodeLayer:
         with torch.cuda.stream(stream):
             self.ids_host.copy_(self.ids, non_blocking=True)
             self.routed.record(stream)
-        self.routed.synchronize()
+        wait_event(self.routed, self.timeout_s, f"layer {self.layer}: routing result")
         needed = sorted(set(int(e) for e in self.ids_host.view(-1).tolist()))
         _, misses = self.pool.cache.lookup(self.layer, step, needed)
         for e, s in misses:

@@ -41,3 +41,32 @@ def oracle_expert(cfg: W.MoEConfig, layer: int, e: int) -> O.QuantizedExpert:
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return W.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def oracle_expert_from_rows(rows, e: int) -> O.QuantizedExpert:
+    """Expert e as the oracle reads it: the device's own row-layout NVFP4 bytes (gate and up are the even and odd
+    rows of the interleaved gate/up matrix) and tensor scales, copied to the host."""
+    gc = rows.gu_codes[e].cpu().numpy()
+    gs = rows.gu_scales[e].cpu().numpy()
+    dc = rows.d_codes[e].cpu().numpy()
+    ds = rows.d_scales[e].cpu().numpy()
+    ts = rows.tscale[e].cpu().numpy()
+    return O.QuantizedExpert((np.ascontiguousarray(gc[0::2]), np.ascontiguousarray(gs[0::2]), float(ts[0])),
+                             (np.ascontiguousarray(gc[1::2]), np.ascontiguousarray(gs[1::2]), float(ts[1])),
+                             (dc, ds, float(ts[2])))
+
+
+class OracleExperts:
+    """expert(e) for O.moe_layer from device row-layout bytes; kept in memory only for small experts."""
+
+    def __init__(self, rows, cache: bool | None = None):
+        self.rows = rows
+        self.cache = (rows.H * rows.I <= 65536) if cache is None else cache
+        self.memo = {}
+
+    def __call__(self, e: int) -> O.QuantizedExpert:
+        if not self.cache:
+            return oracle_expert_from_rows(self.rows, e)
+        if e not in self.memo:
+            self.memo[e] = oracle_expert_from_rows(self.rows, e)
+        return self.memo[e]

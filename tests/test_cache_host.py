@@ -128,3 +128,38 @@ def test_injected_move_failure_empties_the_cache_with_the_new_geometry():
     assert c.lookup(1, 1, [4])[1] == [(4, 0)]
     with pytest.raises(Q.FtError):
         c.lookup(0, 2, [5, 6, 7])             # n > the new slot count
+
+
+class _NeverReady:
+    def __init__(self):
+        self.queries = 0
+
+    def query(self):
+        self.queries += 1
+        return False
+
+
+class _ReadyAfter:
+    def __init__(self, n):
+        self.n = n
+
+    def query(self):
+        self.n -= 1
+        return self.n < 0
+
+
+def test_bounded_host_wait_gives_up_with_a_timeout_status():
+    """The cached decode step waits for its routing result on the host; an event that never completes ends that
+    wait with FT_ERR_TIMEOUT after the limit instead of blocking (a stand-in event, no GPU involved)."""
+    import time
+
+    import quantized_expert_ffn_06_b300 as Q
+    from quantized_expert_ffn_06_b300.layer import wait_event
+    ev = _NeverReady()
+    t0 = time.monotonic()
+    with pytest.raises(Q.FtError) as ei:
+        wait_event(ev, 0.05, "routing result")
+    assert ei.value.status == Q.FT_ERR_TIMEOUT
+    assert 0.05 <= time.monotonic() - t0 < 1.0
+    assert ev.queries > 1
+    wait_event(_ReadyAfter(3), 1.0, "routing result")   # completes before the limit: returns

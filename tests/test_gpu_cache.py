@@ -1,11 +1,11 @@
 """GPU tests of the expert-slot cache: fills, the cached decode stream, and fill failures.
 
-The decode stream uses the cache workload's routing (E = 128, k = 8, 32 slots,
-60 % of each token's experts shared with the previous token) on a reduced
-expert shape so that the pinned host pool stays small.  Every layer output
-read through the cache slots must equal, bit for bit, the output of the same
-kernel on the resident weights (same bytes, same arithmetic, only the weight
-index differs), and the first step is checked against the oracle as well.
+The decode stream uses the cache workload's routing (E = 128, k = 8, 32 slots, 60 % of each token's experts shared
+with the previous token), once on a reduced expert shape (hidden 512, intermediate 256; also through three elastic
+resizes) and once at the workload's own shape (hidden 4096, intermediate 1536).  Every layer output read through
+the cache slots must equal, bit for bit, the output of the same kernel on the resident weights (same bytes, same
+arithmetic, only the weight index differs), and outputs are checked against the oracle, which reads the device's
+own canonical NVFP4 bytes.
 """
 import numpy as np
 import pytest
@@ -13,7 +13,7 @@ import torch
 
 import oracle as O
 import workloads as W
-from helpers import assert_layer_close, oracle_expert
+from helpers import OracleExperts, assert_layer_close
 from oracle.lru import LayerLRU
 
 pytestmark = pytest.mark.gpu
@@ -22,28 +22,70 @@ DEV = "cuda:0"
 if torch.cuda.is_available():
     import quantized_expert_ffn_06_b300 as Q
     from quantized_expert_ffn_06_b300.layer import (CachedDecodeLayer, ExpertSlotPool, FusedDecodeLayer,
-                                                     LayerWeights)
+                                                     LayerWeights, MoEWeights)
 
 CFG = W.scaled(W.CONFIGS["cache_stream"], H=512, I=256, layers=2, steps=24)
 
 
-def resident_weights(cfg, layer):
-    lw = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_DECODE_TILES)
-    lw.fill_synthetic(lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
-    return lw
+class Resident:
+    """One layer's experts resident on the device: canonical row-layout NVFP4 bytes drawn and quantised there, the
+    handle's decode-tile copy of them (w, what the pool is loaded from and the resident kernel reads), and the
+    oracle's experts read from the canonical bytes."""
+
+    def __init__(self, cfg, layer):
+        canon = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_ROWS)
+        canon.fill_synthetic(lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
+        self.canon = canon
+        self.handle = MoEWeights(canon, Q.FT_WEIGHTS_DECODE_TILES)
+        self.w = self.handle.view(Q.FT_LAYOUT_DECODE_TILES)
+        self.oracle = OracleExperts(canon)
+
+
+def make_pool(cfg):
+    pool = ExpertSlotPool(cfg.layers, cfg.E, cfg.H, cfg.I, cfg.slots, DEV)
+    resident = []
+    for l in range(cfg.layers):
+        r = Resident(cfg, l)
+        pool.load_layer(l, r.w)
+        resident.append(r)
+    torch.cuda.synchronize()
+    return pool, resident
 
 
 @pytest.fixture(scope="module")
 def pool_and_resident():
-    cfg = CFG
-    pool = ExpertSlotPool(cfg.layers, cfg.E, cfg.H, cfg.I, cfg.slots, DEV)
-    resident = []
-    for l in range(cfg.layers):
-        lw = resident_weights(cfg, l)
-        pool.load_layer(l, lw)
-        resident.append(lw)
-    torch.cuda.synchronize()
-    return pool, resident
+    return make_pool(CFG)
+
+
+def run_stream(cfg, pool, resident, oracle_steps):
+    """The cached decode stream over cfg.steps tokens and cfg.layers layers: misses as the oracle LRU predicts,
+    outputs bit-equal to the resident weights, and equal to the oracle within the tolerance at oracle_steps."""
+    layers = [CachedDecodeLayer(pool, l, cfg.k, cfg.T) for l in range(cfg.layers)]
+    ref_mods = [FusedDecodeLayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV) for _ in range(cfg.layers)]
+    oracles = [LayerLRU(cfg.slots) for _ in range(cfg.layers)]
+    want_miss_total = 0
+    stream = torch.cuda.current_stream()
+    for step in range(cfg.steps):
+        for l in range(cfg.layers):
+            logits_np = W.router_logits(cfg, l, step)
+            x_np = W.activations_bf16(cfg, l, step)
+            logits = torch.from_numpy(logits_np).to(DEV)
+            x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(DEV)
+            out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)
+            misses = layers[l](logits, x, out, step, stream=stream)
+            ref = torch.empty_like(out)
+            ref_mods[l](resident[l].w, logits, x, ref)
+            torch.cuda.synchronize()
+            assert Q.ft_device_status() == 0
+            ids = sorted(W.cache_stream_sets(cfg, l, step + 1)[step])
+            _, want_misses = oracles[l].access(step, ids)
+            assert misses == [tuple(m) for m in want_misses], (step, l)
+            want_miss_total += len(want_misses)
+            assert torch.equal(out, ref), (step, l)
+            if step in oracle_steps:
+                r = O.moe_layer(logits_np, x_np, cfg.k, resident[l].oracle, O.MODE_A16)
+                assert_layer_close(out.float().cpu().numpy(), r["out"], f"cached layer {l} step {step}")
+    return want_miss_total
 
 
 def test_fill_copies_the_host_block_into_the_slot(pool_and_resident):
@@ -68,36 +110,24 @@ def test_fill_copies_the_host_block_into_the_slot(pool_and_resident):
 
 def test_cached_decode_stream_equals_resident_weights(pool_and_resident):
     pool, resident = pool_and_resident
-    cfg = CFG
-    layers = [CachedDecodeLayer(pool, l, cfg.k, cfg.T) for l in range(cfg.layers)]
-    ref_mods = [FusedDecodeLayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV) for _ in range(cfg.layers)]
-    oracles = [LayerLRU(cfg.slots) for _ in range(cfg.layers)]
-    want_miss_total = 0
-    stream = torch.cuda.current_stream()
-    for step in range(cfg.steps):
-        for l in range(cfg.layers):
-            logits_np = W.router_logits(cfg, l, step)
-            x_np = W.activations_bf16(cfg, l, step)
-            logits = torch.from_numpy(logits_np).to(DEV)
-            x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(DEV)
-            out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)
-            misses = layers[l](logits, x, out, step, stream=stream)
-            ref = torch.empty_like(out)
-            ref_mods[l](resident[l], logits, x, ref)
-            torch.cuda.synchronize()
-            assert Q.ft_device_status() == 0
-            ids = sorted(W.cache_stream_sets(cfg, l, step + 1)[step])
-            _, want_misses = oracles[l].access(step, ids)
-            assert misses == [tuple(m) for m in want_misses], (step, l)
-            want_miss_total += len(want_misses)
-            assert torch.equal(out, ref), (step, l)
-            if step == 0:
-                r = O.moe_layer(logits_np, x_np, cfg.k, lambda e: oracle_expert(cfg, l, e), O.MODE_A16)
-                assert_layer_close(out.float().cpu().numpy(), r["out"], f"cached layer {l}")
+    want_miss_total = run_stream(CFG, pool, resident, oracle_steps=(0, 11, 23))
     hits, miss, filled = pool.cache.stats()
     assert miss == want_miss_total
     assert filled == miss * pool.expert_bytes
     assert hits > miss   # 60 % sharing between consecutive tokens
+
+
+def test_cached_decode_stream_at_the_workload_shape():
+    """Hidden 4096, intermediate 1536, 128 experts, top-8, 32 VRAM slots per layer, experts from a pinned host
+    pool (two layers, 16 tokens): misses as the oracle LRU predicts, every output bit-equal to the resident
+    weights, and against the oracle on the first, a middle and the last token."""
+    cfg = W.scaled(W.CONFIGS["cache_stream"], layers=2, steps=16)
+    assert (cfg.H, cfg.I, cfg.E, cfg.k, cfg.slots) == (4096, 1536, 128, 8, 32)
+    pool, resident = make_pool(cfg)
+    want_miss_total = run_stream(cfg, pool, resident, oracle_steps=(0, 7, 15))
+    hits, miss, filled = pool.cache.stats()
+    assert miss == want_miss_total and filled == miss * pool.expert_bytes
+    assert hits > miss
 
 
 def test_injected_fill_failure_leaves_the_device_usable(pool_and_resident):
@@ -128,7 +158,7 @@ def test_elastic_resize_keeps_the_cached_stream_exact(pool_and_resident):
     cfg = CFG
     pool = ExpertSlotPool(cfg.layers, cfg.E, cfg.H, cfg.I, cfg.slots, DEV)
     for l in range(cfg.layers):
-        pool.load_layer(l, resident[l])
+        pool.load_layer(l, resident[l].w)
     layers = [CachedDecodeLayer(pool, l, cfg.k, cfg.T) for l in range(cfg.layers)]
     ref_mods = [FusedDecodeLayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV) for _ in range(cfg.layers)]
     oracles = [LayerLRU(cfg.slots) for _ in range(cfg.layers)]
@@ -163,7 +193,7 @@ def test_elastic_resize_keeps_the_cached_stream_exact(pool_and_resident):
             out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)
             misses = layers[l](logits, x, out, step, stream=stream)
             ref = torch.empty_like(out)
-            ref_mods[l](resident[l], logits, x, ref)
+            ref_mods[l](resident[l].w, logits, x, ref)
             torch.cuda.synchronize()
             assert Q.ft_device_status() == 0
             ids = sorted(W.cache_stream_sets(cfg, l, step + 1)[step])

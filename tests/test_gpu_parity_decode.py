@@ -1,9 +1,9 @@
 """GPU parity of the decode layer step (route -> permute -> NVFP4 expert FFN -> combine).
 
-The device quantises fp32 weights drawn by its own generator (or uploaded from
-the host generator for the tiny layer); the oracle quantises the host
-generator's weights itself.  ids, offsets, perm and inv are compared bit for
-bit; outputs within relative L2 5e-3 and max |err| 2e-2 * RMS.
+The weights are drawn and quantised on the device (or, for the small layers, uploaded from the host generator and
+quantised there) into canonical row-layout NVFP4 bytes; the layer weights handle (ft_moe_weights_create) repacks
+those bytes into the kernel layouts, and the oracle reads the very same canonical bytes, copied to the host.  ids,
+offsets, perm and inv are compared bit for bit; outputs within relative L2 5e-3 and max |err| 2e-2 * RMS.
 
 Three paths are checked:
   rows  -- route / permute / expert FFN / combine as separate calls, row-major weights
@@ -16,13 +16,13 @@ import torch
 
 import oracle as O
 import workloads as W
-from helpers import assert_layer_close, oracle_expert
+from helpers import OracleExperts, assert_layer_close, oracle_expert
 
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import quantized_expert_ffn_06_b300 as Q
-    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights, MoEDecodeLayer
+    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights, MoEDecodeLayer, MoEWeights
 DEV = "cuda:0"
 PATHS = ["rows", "tiles", "fused"]
 
@@ -38,8 +38,25 @@ def to_dev(a, dtype=None):
     return t.to(DEV)
 
 
+class DeviceLayer:
+    """Canonical row-layout NVFP4 weights of one layer on the device, and the handle's kernel layouts of them."""
+
+    def __init__(self, cfg, layer, from_host=False):
+        self.canon = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_ROWS)
+        if from_host:
+            for e in range(cfg.E):
+                self.canon.set_expert(e, *(to_dev(W.weights_fp32(cfg, layer, e, p)) for p in range(3)))
+        else:
+            self.canon.fill_synthetic(lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
+        self.handle = MoEWeights(self.canon, Q.FT_WEIGHTS_ROWS | Q.FT_WEIGHTS_DECODE_TILES)
+        self.oracle = OracleExperts(self.canon)
+
+    def view(self, path):
+        return self.handle.view(layout_of(path))
+
+
 def device_weights_from_host(cfg, layer, experts=None, layout=0):
-    """Upload the host generator's fp32 weights and quantise them on the device."""
+    """Upload the host generator's fp32 weights and quantise them on the device (one layout, no handle)."""
     lw = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=layout)
     for e in (range(cfg.E) if experts is None else experts):
         lw.set_expert(e, *(to_dev(W.weights_fp32(cfg, layer, e, p)) for p in range(3)))
@@ -70,8 +87,9 @@ def run_layer(cfg, lw, layer, step, T=None, want_y=False, path="rows"):
     return logits, x_bits, mod, out, y
 
 
-def oracle_layer(cfg, layer, logits, x_bits, rows=None):
-    return O.moe_layer(logits, x_bits, cfg.k, lambda e: oracle_expert(cfg, layer, e), O.MODE_A16, rows=rows)
+def oracle_layer(cfg, dl, logits, x_bits, rows=None):
+    """The oracle on the device's own bytes (dl: a DeviceLayer)."""
+    return O.moe_layer(logits, x_bits, cfg.k, dl.oracle, O.MODE_A16, rows=rows)
 
 
 def check_routing(mod, ref):
@@ -87,9 +105,9 @@ def check_routing(mod, ref):
 @pytest.mark.parametrize("path", PATHS)
 def test_tiny_layer_every_output(path):
     cfg = W.CONFIGS["tiny"]
-    lw = device_weights_from_host(cfg, 0, layout=layout_of(path))
-    logits, x_bits, mod, out, y = run_layer(cfg, lw, 0, 0, want_y=True, path=path)
-    ref = oracle_layer(cfg, 0, logits, x_bits)
+    dl = DeviceLayer(cfg, 0, from_host=True)
+    logits, x_bits, mod, out, y = run_layer(cfg, dl.view(path), 0, 0, want_y=True, path=path)
+    ref = oracle_layer(cfg, dl, logits, x_bits)
     check_routing(mod, ref)
     assert_layer_close(out.float().cpu().numpy(), ref["out"], "tiny out")
     if y is not None:
@@ -142,37 +160,48 @@ def test_tile_packing_is_a_permutation_of_row_bytes():
             assert tb[base + KB * 1024 + kb * 128 + (g * 4 + q) * 4 + 2 * h + bb] == scales[n, blk]
 
 
+@pytest.fixture(scope="module")
+def layers35():
+    cfg = W.CONFIGS["decode_35b"]
+    return {layer: DeviceLayer(cfg, layer) for layer in (0, 7, 47)}
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("layer,step", [(0, 0), (7, 3), (47, 255)])
-def test_decode_35b_layer(layer, step, path):
+def test_decode_35b_layer(layers35, layer, step, path):
     cfg = W.CONFIGS["decode_35b"]
-    lw = device_weights_generated(cfg, layer, layout=layout_of(path))
-    logits, x_bits, mod, out, _ = run_layer(cfg, lw, layer, step, path=path)
-    ref = oracle_layer(cfg, layer, logits, x_bits)
+    dl = layers35[layer]
+    logits, x_bits, mod, out, _ = run_layer(cfg, dl.view(path), layer, step, path=path)
+    ref = oracle_layer(cfg, dl, logits, x_bits)
     check_routing(mod, ref)
     assert_layer_close(out.float().cpu().numpy(), ref["out"], f"35B layer {layer} step {step}")
 
 
+@pytest.fixture(scope="module")
+def layer753():
+    return DeviceLayer(W.CONFIGS["decode_753b_b1"], 3)
+
+
 @pytest.mark.parametrize("path", PATHS)
-def test_decode_753b_batch1_layer(path):
+def test_decode_753b_batch1_layer(layer753, path):
     cfg = W.CONFIGS["decode_753b_b1"]
-    lw = device_weights_generated(cfg, 3, layout=layout_of(path))
-    logits, x_bits, mod, out, _ = run_layer(cfg, lw, 3, 11, path=path)
-    ref = oracle_layer(cfg, 3, logits, x_bits)
+    logits, x_bits, mod, out, _ = run_layer(cfg, layer753.view(path), 3, 11, path=path)
+    ref = oracle_layer(cfg, layer753, logits, x_bits)
     check_routing(mod, ref)
     assert_layer_close(out.float().cpu().numpy(), ref["out"], "753B b1")
 
 
 @pytest.mark.parametrize("path", ["rows", "fused"])
-def test_decode_753b_batch16_sampled_tokens(path):
-    """Batch 16 of hidden 6144: the fused step runs as launches over token chunks that fit its staging."""
+def test_decode_753b_batch16_every_token(layer753, path):
+    """Batch 16 of hidden 6144, all 16 tokens against the oracle: the fused step runs as launches over token
+    chunks that fit its shared memory."""
     cfg = W.CONFIGS["decode_753b_b16"]
-    lw = device_weights_generated(cfg, 1, layout=layout_of(path))
-    logits, x_bits, mod, out, _ = run_layer(cfg, lw, 1, 2, path=path)
-    rows = [0, 9, 15]
-    ref = oracle_layer(cfg, 1, logits, x_bits, rows=rows)
-    assert np.array_equal(mod.ids.cpu().numpy(), ref["ids"])
-    assert_layer_close(out.float().cpu().numpy()[rows], ref["out"], f"753B b16 sampled ({path})")
+    logits, x_bits, mod, out, _ = run_layer(cfg, layer753.view(path), 3, 2, path=path)
+    ref = oracle_layer(cfg, layer753, logits, x_bits)
+    check_routing(mod, ref)
+    got = out.float().cpu().numpy()
+    for t in range(cfg.T):
+        assert_layer_close(got[t:t + 1], ref["out"][t:t + 1], f"753B b16 token {t} ({path})")
 
 
 def test_fused_token_chunks_agree_with_single_token_launches():
@@ -212,9 +241,9 @@ def test_tiled_grouped_kernel_reports_unsupported_staging_size():
 def test_ragged_token_counts_and_single_expert_segments(path, T):
     """T tokens over 8 experts with k = 2: segments of uneven length, several token groups."""
     cfg = W.scaled(W.CONFIGS["tiny"], T=T)
-    lw = device_weights_from_host(cfg, 0, layout=layout_of(path))
-    logits, x_bits, mod, out, _ = run_layer(cfg, lw, 0, 4, path=path)
-    ref = oracle_layer(cfg, 0, logits, x_bits)
+    dl = DeviceLayer(cfg, 0, from_host=True)
+    logits, x_bits, mod, out, _ = run_layer(cfg, dl.view(path), 0, 4, path=path)
+    ref = oracle_layer(cfg, dl, logits, x_bits)
     check_routing(mod, ref)
     assert_layer_close(out.float().cpu().numpy(), ref["out"], "ragged")
 
@@ -302,17 +331,18 @@ def fused_run(cfg, lw, logits_dev, x_bits):
 @pytest.mark.parametrize("E,k,T", [(8, 2, 4), (10, 3, 3), (512, 8, 3)])
 @pytest.mark.parametrize("offset", [0, 1])
 def test_fused_router_on_wide_odd_and_unaligned_logits(E, k, T, offset):
-    """E = 512 takes more than eight logits per lane; T*E*4 not a multiple of 16 bytes, or logits
-    not 16-byte aligned (offset 1), make the router read global memory instead of a staged copy."""
+    """E = 512 spans 16 router blocks of 32 logits; E = 10 leaves most of a block empty; logits at a 4-byte offset
+    (offset 1) are not 16-byte aligned."""
     cfg = W.scaled(W.CONFIGS["tiny"], E=E, k=k, T=T)
-    lw = device_weights_generated(cfg, 0, layout=Q.FT_LAYOUT_DECODE_TILES)
+    dl = DeviceLayer(cfg, 0)
+    lw = dl.view("fused")
     logits = W.router_logits(cfg, 0, 1)
     x_bits = W.activations_bf16(cfg, 0, 1)
     buf = torch.zeros(T * E + 4, dtype=torch.float32, device=DEV)
     lg = buf[offset:offset + T * E].view(T, E)
     lg.copy_(to_dev(logits))
     mod, out = fused_run(cfg, lw, lg, x_bits)
-    ref = oracle_layer(cfg, 0, logits, x_bits)
+    ref = oracle_layer(cfg, dl, logits, x_bits)
     check_routing(mod, ref)
     assert_layer_close(out.float().cpu().numpy(), ref["out"], f"E={E} offset={offset}")
 
@@ -320,7 +350,8 @@ def test_fused_router_on_wide_odd_and_unaligned_logits(E, k, T, offset):
 def test_fused_router_ties_and_infinities():
     """Equal logits go to the lower expert id; a row of -inf gives every slot weight 1/k."""
     cfg = W.scaled(W.CONFIGS["tiny"], E=16, k=3)
-    lw = device_weights_generated(cfg, 0, layout=Q.FT_LAYOUT_DECODE_TILES)
+    dl = DeviceLayer(cfg, 0)
+    lw = dl.view("fused")
     logits = np.zeros((4, 16), np.float32)
     logits[1, [9, 3, 12]] = 2.0
     logits[2] = -np.inf
@@ -328,7 +359,7 @@ def test_fused_router_ties_and_infinities():
     logits[3, [5, 7]] = [0.0, -0.0]
     x_bits = W.activations_bf16(cfg, 0, 3)
     mod, out = fused_run(cfg, lw, to_dev(logits), x_bits)
-    ref = oracle_layer(cfg, 0, logits, x_bits)
+    ref = oracle_layer(cfg, dl, logits, x_bits)
     check_routing(mod, ref)
     assert_layer_close(out.float().cpu().numpy(), ref["out"], "ties")
 
@@ -337,13 +368,14 @@ def test_fused_activations_beyond_f16_range_are_rescaled():
     """A token row scaled by 2^20 overflows f16 staging: x and its h rows take the exact
     power-of-two rescaling path.  Each token row is checked on its own scale."""
     cfg = W.CONFIGS["tiny"]
-    lw = device_weights_from_host(cfg, 0, layout=Q.FT_LAYOUT_DECODE_TILES)
+    dl = DeviceLayer(cfg, 0, from_host=True)
+    lw = dl.view("fused")
     logits = W.router_logits(cfg, 0, 2)
     x32 = W.bf16_bits_to_f32(W.activations_bf16(cfg, 0, 2)).copy()
     x32[1] *= 2.0 ** 20
     x_bits = (x32.view(np.uint32) >> 16).astype(np.uint16)   # exact: only exponents changed
     mod, out = fused_run(cfg, lw, to_dev(logits), x_bits)
-    ref = oracle_layer(cfg, 0, logits, x_bits)
+    ref = oracle_layer(cfg, dl, logits, x_bits)
     check_routing(mod, ref)
     got = out.float().cpu().numpy()
     for t in range(cfg.T):

@@ -11,14 +11,14 @@ import torch
 
 import oracle as O
 import workloads as W
-from helpers import assert_layer_close, oracle_expert
+from helpers import OracleExperts, assert_layer_close
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 if torch.cuda.is_available():
     import quantized_expert_ffn_06_b300 as Q
-    from quantized_expert_ffn_06_b300.layer import LayerWeights, PrefillLayer
+    from quantized_expert_ffn_06_b300.layer import LayerWeights, MoEWeights, PrefillLayer
 
 
 def to_dev(a, dtype=None):
@@ -28,31 +28,44 @@ def to_dev(a, dtype=None):
     return t.to(DEV)
 
 
+class DeviceLayer:
+    """Canonical row-layout NVFP4 weights of one layer on the device (drawn and quantised there, or uploaded from the
+    host generator and quantised there), the handle's tensor-core layout of them (w), and the oracle's experts read
+    from the same canonical bytes."""
+
+    def __init__(self, cfg, layer, generated=True):
+        self.canon = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_ROWS)
+        if generated:
+            self.canon.fill_synthetic(lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
+        else:
+            for e in range(cfg.E):
+                self.canon.set_expert(e, *(to_dev(W.weights_fp32(cfg, layer, e, p)) for p in range(3)))
+        self.handle = MoEWeights(self.canon, Q.FT_WEIGHTS_UMMA_TILES)
+        self.w = self.handle.view(Q.FT_LAYOUT_UMMA_TILES)
+        self.oracle = OracleExperts(self.canon)
+
+
 def weights(cfg, layer, generated=True):
-    lw = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_UMMA_TILES)
-    if generated:
-        lw.fill_synthetic(lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p), sigma=cfg.w_sigma)
-    else:
-        for e in range(cfg.E):
-            lw.set_expert(e, *(to_dev(W.weights_fp32(cfg, layer, e, p)) for p in range(3)))
-    return lw
+    return DeviceLayer(cfg, layer, generated)
 
 
 def run(cfg, lw, logits, x_bits):
     T = logits.shape[0]
     mod = PrefillLayer(cfg.E, cfg.H, cfg.I, cfg.k, T, DEV)
     out = torch.empty((T, cfg.H), dtype=torch.bfloat16, device=DEV)
-    mod(lw, to_dev(logits), to_dev(x_bits.view(np.int16), torch.bfloat16), out)
+    w = lw.w if isinstance(lw, DeviceLayer) else lw
+    mod(w, to_dev(logits), to_dev(x_bits.view(np.int16), torch.bfloat16), out)
     torch.cuda.synchronize()
     assert Q.ft_device_status() == 0
     return mod, out
 
 
-def check(cfg, layer, mod, out, logits, x_bits, rows=None):
-    ref = O.moe_layer(logits, x_bits, cfg.k, lambda e: oracle_expert(cfg, layer, e), O.MODE_A4, rows=rows)
+def check(cfg, dl, mod, out, logits, x_bits, rows=None):
+    ref = O.moe_layer(logits, x_bits, cfg.k, dl.oracle, O.MODE_A4, rows=rows)
     assert np.array_equal(mod.ids.cpu().numpy(), ref["ids"])
     assert np.array_equal(mod.offsets.cpu().numpy(), ref["offsets"])
     assert np.array_equal(mod.perm.cpu().numpy(), ref["perm"])
+    assert np.array_equal(mod.inv.cpu().numpy(), ref["inv"])
     got = out.float().cpu().numpy()
     if rows is not None:
         got = got[rows]
@@ -64,7 +77,7 @@ def test_tiny_layer_every_output():
     lw = weights(cfg, 0, generated=False)
     logits, x_bits = W.router_logits(cfg, 0, 0), W.activations_bf16(cfg, 0, 0)
     mod, out = run(cfg, lw, logits, x_bits)
-    check(cfg, 0, mod, out, logits, x_bits)
+    check(cfg, lw, mod, out, logits, x_bits)
 
 
 @pytest.mark.parametrize("T", [1, 13, 37, 200])
@@ -73,7 +86,7 @@ def test_ragged_token_counts(T):
     lw = weights(cfg, 0, generated=False)
     logits, x_bits = W.router_logits(cfg, 0, 1), W.activations_bf16(cfg, 0, 1)
     mod, out = run(cfg, lw, logits, x_bits)
-    check(cfg, 0, mod, out, logits, x_bits)
+    check(cfg, lw, mod, out, logits, x_bits)
 
 
 def test_one_expert_spanning_several_tiles():
@@ -85,18 +98,44 @@ def test_one_expert_spanning_several_tiles():
     x_bits = W.activations_bf16(cfg, 0, 2)
     mod, out = run(cfg, lw, logits, x_bits)
     assert (mod.ids.cpu().numpy() == 5).all()
-    check(cfg, 0, mod, out, logits, x_bits)
+    check(cfg, lw, mod, out, logits, x_bits)
 
 
-def test_prefill_35b_zipf_sampled_tokens():
+def boundary_tokens(offsets, perm, k, heavy=10, extra=256, seed=0):
+    """Tokens whose expert rows include every expert's first and last permuted row and every row of the last
+    (partial) 128-row tile of the `heavy` experts with the most rows, plus a seeded sample up to `extra` more."""
+    offsets = np.asarray(offsets)
+    perm = np.asarray(perm)
+    rows = set()
+    counts = np.diff(offsets)
+    for e in np.nonzero(counts)[0]:
+        rows.add(int(offsets[e]))
+        rows.add(int(offsets[e + 1]) - 1)
+    for e in np.argsort(-counts, kind="stable")[:heavy]:
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        last_tile = lo + 128 * ((hi - lo - 1) // 128)
+        rows.update(range(last_tile, hi))
+    toks = set(int(perm[p]) // k for p in rows)
+    T = len(perm) // k
+    rng = np.random.default_rng(seed)
+    toks.update(int(t) for t in rng.choice(T, size=min(extra, T), replace=False))
+    return sorted(toks)
+
+
+def test_prefill_35b_zipf_boundary_tokens():
+    """4096 tokens with Zipf(1.1) expert popularity.  Checked against the oracle: every token owning some
+    expert's first or last permuted row, every token in the last partial 128-row tile of the ten heaviest
+    experts, and 256 more drawn at random (several hundred tokens, every expert's tile boundaries)."""
     cfg = W.CONFIGS["prefill_35b"]
     lw = weights(cfg, 0)
     logits, x_bits = W.router_logits(cfg, 0, 0), W.activations_bf16(cfg, 0, 0)
     mod, out = run(cfg, lw, logits, x_bits)
-    counts = np.diff(mod.offsets.cpu().numpy())
+    offsets = mod.offsets.cpu().numpy()
+    counts = np.diff(offsets)
     assert counts.max() > 1000 and counts.min() < 100   # skewed groups, as Zipf(1.1) popularity gives
-    rows = [0, 1, 777, 2048, 4095]
-    check(cfg, 0, mod, out, logits, x_bits, rows=rows)
+    rows = boundary_tokens(offsets, mod.perm.cpu().numpy(), cfg.k)
+    assert len(rows) >= 256
+    check(cfg, lw, mod, out, logits, x_bits, rows=rows)
 
 
 def test_umma_packing_places_every_byte_where_the_layout_says():
@@ -130,7 +169,7 @@ def test_hidden_beyond_resident_token_tile_streams_both_operands():
     lw = weights(cfg, 0, generated=False)
     logits, x_bits = W.router_logits(cfg, 0, 3), W.activations_bf16(cfg, 0, 3)
     mod, out = run(cfg, lw, logits, x_bits)
-    check(cfg, 0, mod, out, logits, x_bits)
+    check(cfg, lw, mod, out, logits, x_bits)
 
 
 @pytest.mark.parametrize("case", ["short_total", "decreasing", "negative_start"])
@@ -149,13 +188,13 @@ def test_offsets_that_do_not_partition_the_rows_are_reported_and_add_nothing(cas
     else:
         bad[0] = -128
     out.fill_(1.0)
-    Q.ft_moe_expert_ffn_nvfp4_prefill(lw, to_dev(x_bits.view(np.int16), torch.bfloat16), cfg.k, bad, mod.perm,
+    Q.ft_moe_expert_ffn_nvfp4_prefill(lw.w, to_dev(x_bits.view(np.int16), torch.bfloat16), cfg.k, bad, mod.perm,
                                       mod.w, out, mod.ws)
     assert Q.ft_device_status() == Q.FT_DEVERR_BAD_INDEX
     assert not out.float().abs().sum().item()
     # the workspace stays usable: a valid call after the failed one is exact again
     mod2, out2 = run(cfg, lw, logits, x_bits)
-    check(cfg, 0, mod2, out2, logits, x_bits)
+    check(cfg, lw, mod2, out2, logits, x_bits)
 
 
 def test_streamed_layers_equal_resident_weights():
@@ -169,7 +208,7 @@ def test_streamed_layers_equal_resident_weights():
     lws = [weights(cfg, l) for l in range(L)]
     sp = StreamedPrefill(L, cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV)
     for l in range(L):
-        sp.load_layer(l, lws[l])
+        sp.load_layer(l, lws[l].w)
     logits = [W.router_logits(cfg, l, 5) for l in range(L)]
     xs = [W.activations_bf16(cfg, l, 5) for l in range(L)]
     lg_d = [to_dev(a) for a in logits]
@@ -183,4 +222,4 @@ def test_streamed_layers_equal_resident_weights():
             mod, ref = run(cfg, lws[l], logits[l], xs[l])
             assert torch.equal(outs[l], ref), (call, l)
             if l == 0 and call == 0:
-                check(cfg, 0, mod, outs[0], logits[0], xs[0])
+                check(cfg, lws[0], mod, outs[0], logits[0], xs[0])
