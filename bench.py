@@ -943,7 +943,8 @@ def run_gpu_cache(args, ws, rank, local):
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     copy_stream = torch.cuda.Stream(device=dev)
     stream = torch.cuda.Stream(device=dev)
-    layers = [CachedDecodeLayer(pool, l, k, T, copy_stream=copy_stream) for l in range(L)]
+    P = args.prefetch
+    layers = [CachedDecodeLayer(pool, l, k, T, copy_stream=copy_stream, prefetch=P) for l in range(L)]
     # pinned host -> device copy bandwidth on this machine (the bound of the misses)
     probe_h = torch.empty(512 << 20, dtype=torch.uint8, pin_memory=True)
     probe_d = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -967,6 +968,7 @@ def run_gpu_cache(args, ws, rank, local):
             token(s)
     torch.cuda.synchronize()
     h0, m0, b0 = pool.cache.stats()
+    pf0, pu0 = pool.cache.prefetch_stats()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(dev)
     bus = None
@@ -987,6 +989,8 @@ def run_gpu_cache(args, ws, rank, local):
     assert Q.ft_device_status(stream) == 0
     h1, m1, b1 = pool.cache.stats()
     hits, misses, filled = h1 - h0, m1 - m0, b1 - b0
+    pf1, pu1 = pool.cache.prefetch_stats()
+    prefetched, used = pf1 - pf0, pu1 - pu0
     step_s = ms / 1e3 / args.steps
     hbm_peak, hbm_kind = load_peaks()
     # elastic resize at a safe point, after the timed stream: every layer shrinks to half its slots in a new pool
@@ -1018,12 +1022,19 @@ def run_gpu_cache(args, ws, rank, local):
         "data": "synthetic (seeded Philox4x32-10; Zipf(1.1) popularity, 60 % of experts shared between tokens)",
         "config": {"workload": f"{cfg.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, intermediate {I}, "
                                f"batch {T}, VRAM LRU cache of {cfg.slots} slots per layer over a "
-                               f"{L * E * pool.slot_stride / 1e9:.1f} GB pinned host pool",
+                               f"{L * E * pool.slot_stride / 1e9:.1f} GB pinned host pool"
+                               + (f", router-driven prefetch of the next {P} ranks" if P else ""),
                    "global_batch": T * ws, "l2": "inputs larger than L2: misses come from host memory",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "cache": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                   "h2d_bytes_per_token": miss_bytes_tok, "h2d_gbs_achieved": filled / (ms / 1e3) / 1e9,
                   "h2d_gbs_measured_peak": h2d_gbs,
+                  "prefetch": {"next_ranks": P, "prefetched": prefetched, "used": used,
+                               "accuracy": used / prefetched if prefetched else None,
+                               "demand_misses_per_token": misses / args.steps,
+                               "what": "the router's next P ranks of each token installed for the next token and "
+                                       "copied behind its misses on the copy stream; accuracy = installed experts a "
+                                       "later lookup found / installed"},
                   "resize": dict(resize, what="ft_expert_cache_resize after the timed stream (device-to-device "
                                               "moves + the publish of every layer's table), CUDA events on the "
                                               "stream; not part of the tok/s")},
@@ -1046,6 +1057,8 @@ def main():
     ap.add_argument("--config", default="decode_35b")
     ap.add_argument("--distinct-steps", type=int, default=256)
     ap.add_argument("--layers", type=int, default=0, help="(debug) fewer layers; the result is then not the workload")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="cache stream: install the router's next P ranked experts of each token for the next one")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=48)

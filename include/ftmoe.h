@@ -324,21 +324,26 @@ FT_API size_t ft_moe_prefill_workspace_size(int T, int k, int E, int H, int I);
  *   g = Wg q(x_t), u = Wu q(x_t), h = bf16(silu(g) * u), y_p = Wd q(h),
  *   out[t] = bf16( sum_j w[t][j] * y_{inv[t*k+j]} ), fp32 (order of the
  *   additions not fixed: fp32 atomics).
- *   W (device) weights in FT_LAYOUT_UMMA_TILES, no slot table; H a multiple
- *          of 128, I a multiple of 128.
+ *   W (device) weights in FT_LAYOUT_UMMA_TILES; H a multiple of 128, I a
+ *          multiple of 128.  With a slot table (expert_to_slot), an expert
+ *          with rows whose slot is outside [0, n_weights) sets
+ *          FT_DEVERR_BAD_INDEX and its rows contribute nothing.
  *   x (device) bf16 [T][H], 16-byte aligned; offsets, perm (device) from
- *   ft_moe_permute; w (device) fp32 [T][k] routing weights; out (device) bf16
- *   [T][H], 8-byte aligned.  A misaligned x or out is FT_ERR_INVALID_ARG.
+ *   ft_moe_permute; w (device) fp32 [T][k] routing weights (needed with out).
+ *   y (device, optional) fp32 [T*k][H], 16-byte aligned: y_p of every permuted
+ *          row p (tensor scale applied, no routing weight).
+ *   out (device, optional) bf16 [T][H], 8-byte aligned: the combine.  At least
+ *          one of y, out.  A misaligned x, y or out is FT_ERR_INVALID_ARG.
  *   ws: ft_moe_prefill_workspace_size(T, k, E, H, I) bytes, 256-byte aligned
  *       (per-expert tile offsets, quantised x and h tiles, an fp32 output
  *       accumulator); no initial content needed.
  * Each expert's rows are padded to whole 128-row tiles; the padding rows of a
- * tile hold whatever the workspace held and never reach the output.
+ * tile hold whatever the workspace held and never reach the outputs.
  * offsets that do not partition [0, T*k) in order (offsets[0] = 0, non-
  * decreasing, offsets[E] = T*k) set FT_DEVERR_BAD_INDEX; no expert row is then
  * computed and out is all zeros. */
 FT_API ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
-                                                 const int32_t* offsets, const int32_t* perm, const float* w,
+                                                 const int32_t* offsets, const int32_t* perm, const float* w, float* y,
                                                  uint16_t* out, void* ws, size_t ws_bytes, ft_stream_t stream);
 
 /* [P4 MoE core mechanism] Routing-weighted combine:
@@ -390,6 +395,24 @@ FT_API ft_status ft_expert_cache_fill(ft_expert_cache* cache, int layer, int exp
  * tables + layer*E (from a pinned ring of 4 staging copies per layer; a ring
  * entry still in flight is waited for on the host). */
 FT_API ft_status ft_expert_cache_publish(ft_expert_cache* cache, int layer, ft_stream_t stream);
+/* [P4 bandwidth-aware storage: experts predicted from the gate outputs are
+ * fetched ahead, asynchronously, so the transfer overlaps the computation]
+ * Installs the predicted experts ids (host, n <= E; repeats ignored) of layer
+ * `layer` ahead of the token that will use them.  Policy (the pages give
+ * none): ids are visited in ascending order; one already resident is left as
+ * it is (a prediction is not a use); otherwise it takes the lowest free slot,
+ * else the slot with the oldest stamp older than `step` (lower slot on a tie)
+ * whose expert is not among `ids`, so neither a predicted expert nor one
+ * stamped `step` -- the current token's, which a kernel may still be reading --
+ * is displaced; when no slot qualifies the id is skipped.  An installed expert gets stamp step - 1.  fill_experts /
+ * fill_slots (host, room for n) receive the copies the caller must enqueue
+ * (ft_expert_cache_fill) before a layer reads them, ascending expert id;
+ * *n_fill their count.  Pure host bookkeeping. */
+FT_API ft_status ft_expert_cache_prefetch(ft_expert_cache* cache, int layer, int64_t step, const int32_t* ids, int n,
+                                          int32_t* fill_experts, int32_t* fill_slots, int* n_fill);
+/* Experts installed by prefetches since creation, and how many of those a later
+ * lookup used before they left the cache. */
+FT_API ft_status ft_expert_cache_prefetch_stats(ft_expert_cache* cache, int64_t* prefetched, int64_t* used);
 /* Counters since creation: hit and miss accesses, bytes enqueued by fills. */
 FT_API ft_status ft_expert_cache_stats(ft_expert_cache* cache, int64_t* hits, int64_t* misses, int64_t* bytes_filled);
 /* [P5 设计核心, third mechanism] Elastic resize at a safe point: the cache

@@ -91,7 +91,7 @@ _sig("ft_moe_layer_decode_noalloc", [ctypes.POINTER(ft_moe_layer_weights), _vp, 
 _sig("ft_nvfp4_pack_umma", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_moe_prefill_workspace_size", [_i32, _i32, _i32, _i32, _i32], _sz)
 _sig("ft_moe_expert_ffn_nvfp4_prefill", [ctypes.POINTER(ft_moe_layer_weights), _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
-                                         _sz, _vp])
+                                         _vp, _sz, _vp])
 _sig("ft_expert_cache_create", [_i32, _i32, _i32, _sz, ctypes.POINTER(ctypes.c_void_p), _vp, _sz, _vp,
                                 ctypes.POINTER(ctypes.c_void_p)])
 _sig("ft_expert_cache_destroy", [_vp])
@@ -101,6 +101,9 @@ _sig("ft_expert_cache_fill", [_vp, _i32, _i32, _i32, _vp, _vp])
 _sig("ft_expert_cache_publish", [_vp, _i32, _vp])
 _sig("ft_expert_cache_stats", [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64)])
 _sig("ft_expert_cache_inject_fill_failure", [_vp, _i64])
+_sig("ft_expert_cache_prefetch", [_vp, _i32, _i64, ctypes.POINTER(ctypes.c_int32), _i32, ctypes.POINTER(ctypes.c_int32),
+                                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(_i32)])
+_sig("ft_expert_cache_prefetch_stats", [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64)])
 _sig("ft_expert_cache_resize", [_vp, _i32, _vp, _sz, _vp])
 _sig("ft_expert_cache_resize_plan", [_vp, _i32, ctypes.POINTER(ctypes.c_int32)])
 
@@ -288,13 +291,14 @@ def ft_moe_prefill_workspace_size(T: int, k: int, E: int, H: int, I: int) -> int
     return _lib.ft_moe_prefill_workspace_size(T, k, E, H, I)
 
 
-def ft_moe_expert_ffn_nvfp4_prefill(W, x: torch.Tensor, k: int, offsets, perm, w, out, ws, stream=None):
-    """Prefill expert FFN + combine on the FP4 tensor cores (weights in FT_LAYOUT_UMMA_TILES)."""
+def ft_moe_expert_ffn_nvfp4_prefill(W, x: torch.Tensor, k: int, offsets, perm, w, out, ws, stream=None, y=None):
+    """Prefill expert FFN on the FP4 tensor cores (weights in FT_LAYOUT_UMMA_TILES): the combine into out (bf16
+    [T, H]) and/or the per-row expert outputs into y (fp32 [T*k, H]); either may be None, not both."""
     _req(x, torch.bfloat16, "x")
     T = x.shape[0]
     desc = W.desc()
-    _check(_lib.ft_moe_expert_ffn_nvfp4_prefill(ctypes.byref(desc), _p(x), T, k, _p(offsets), _p(perm), _p(w), _p(out),
-                                                _p(ws), ws.numel() * ws.element_size(), _s(stream)))
+    _check(_lib.ft_moe_expert_ffn_nvfp4_prefill(ctypes.byref(desc), _p(x), T, k, _p(offsets), _p(perm), _p(w), _p(y),
+                                                _p(out), _p(ws), ws.numel() * ws.element_size(), _s(stream)))
     return out
 
 
@@ -380,6 +384,23 @@ class ExpertCacheHandle:
         h, m, b = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
         _check(_lib.ft_expert_cache_stats(self.h, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b)))
         return h.value, m.value, b.value
+
+    def prefetch(self, layer: int, step: int, ids):
+        """Install predicted experts (host ints) ahead of the token that uses them; returns the [(expert, slot)] fills
+        the caller must enqueue."""
+        n = len(ids)
+        c_ids = (ctypes.c_int32 * max(n, 1))(*ids)
+        fe = (ctypes.c_int32 * max(n, 1))()
+        fs = (ctypes.c_int32 * max(n, 1))()
+        nf = ctypes.c_int(0)
+        _check(_lib.ft_expert_cache_prefetch(self.h, layer, step, c_ids, n, fe, fs, ctypes.byref(nf)))
+        return [(fe[i], fs[i]) for i in range(nf.value)]
+
+    def prefetch_stats(self):
+        """(experts installed by prefetches, of which a later lookup used)."""
+        p, u = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.ft_expert_cache_prefetch_stats(self.h, ctypes.byref(p), ctypes.byref(u)))
+        return p.value, u.value
 
     def inject_fill_failure(self, fill_index: int):
         _check(_lib.ft_expert_cache_inject_fill_failure(self.h, fill_index))

@@ -112,6 +112,7 @@ struct DecodePlan {
     float inv_k;      // 1/k, rounded to nearest (the weight of every slot of a -inf row)
     unsigned long long wait_ns;  // bound on any single wait
     int wait_site;               // FT_WAIT_SITE_DECODE_H: the h hand-off waits for an epoch nobody writes
+    int logits_bulk;             // the logits come in by one bulk copy (16-byte aligned, size a multiple of 16)
 };
 
 struct DecodeArgs {
@@ -132,7 +133,7 @@ struct DecodeArgs {
 };
 
 // misc ints in shared memory (XEXP: pre-scale exponent of each staged x row)
-enum { M_U = 0, M_FLAG = 1, M_HFLAG = 2, M_ABORT = 3, M_EPOCH = 4, M_XEXP = 8, M_COUNT = 8 + dk::MAXT };
+enum { M_U = 0, M_FLAG = 1, M_HFLAG = 2, M_ABORT = 3, M_EPOCH = 4, M_XEXP = 8, M_BAR = 8 + dk::MAXT, M_COUNT = M_BAR + 2 };
 
 // ---------------------------------------------------------------------------- PTX helpers
 
@@ -346,30 +347,65 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const bool route_mode = a.logits != nullptr;
     uint8_t* ring = dsm + P.off_ring + warp * (R * dk::ITEM);
 
-    if (tid < M_COUNT) misc[tid] = 0;
+    unsigned long long* ibar = reinterpret_cast<unsigned long long*>(misc + M_BAR);  // the inputs' bulk copies
+    if (tid < M_BAR) misc[tid] = 0;
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(ibar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
 #pragma unroll 1
     for (int i = tid; i < nf; i += dk::THREADS) s_hexp[i] = 0;
     if (route_mode) {
 #pragma unroll 1
         for (int i = tid; i < T * P.nb * P.kk; i += dk::THREADS) s_rank[i] = 0;
     }
+    __syncthreads();
     // inputs (and the workspace) may be written by the preceding kernel in the stream
     griddep_wait();
     griddep_launch_dependents();
     unsigned long long old_count = 0;
-    if (tid == 0) old_count = atomicAdd(a.bar, 1ull);
 
-    // ---------------- inputs: every thread issues its async copies at once
+    // ---------------- inputs: x (and the logits, when aligned) by one bulk copy each
     {
         const int nx = T * (H >> 3);  // 16-byte pieces of x
-        const int nl = route_mode ? T * E : 0;
+        const bool lbulk = route_mode && P.logits_bulk;
+        if (tid == 0) {
+            const uint32_t xbytes = (uint32_t)(T * H * 2), lbytes = lbulk ? (uint32_t)(T * E * 4) : 0u;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(ibar)),
+                         "r"(xbytes + lbytes) : "memory");
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             smem_u32(xraw)), "l"(a.x), "r"(xbytes), "r"(smem_u32(ibar)) : "memory");
+            if (lbulk)
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                 smem_u32(lg)), "l"(a.logits), "r"(lbytes), "r"(smem_u32(ibar)) : "memory");
+            old_count = atomicAdd(a.bar, 1ull);
+        }
+        if (route_mode && !lbulk) {  // unaligned logits: 4-byte async copies
+            const int nl = T * E;
 #pragma unroll 1
-        for (int i = tid; i < nl; i += dk::THREADS) cp4(lg + i, a.logits + i);
+            for (int i = tid; i < nl; i += dk::THREADS) cp4(lg + i, a.logits + i);
+            cp_commit();
+            cp_wait<0>();
+        }
+        {  // bounded wait for the bulk copies
+            uint32_t ok = 0;
+            const unsigned long long t0 = globaltimer();
 #pragma unroll 1
-        for (int i = tid; i < nx; i += dk::THREADS) cp16(xraw + i * 8, a.x + i * 8);
-        cp_commit();
-        cp_wait<0>();
-        __syncthreads();
+            while (true) {
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                    : "=r"(ok)
+                    : "r"(smem_u32(ibar))
+                    : "memory");
+                if (ok || *abort_flag) break;
+                if (globaltimer() - t0 > P.wait_ns) {
+                    *abort_flag = 1;
+                    raise_dev_error(FT_DEVERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        if (route_mode && !lbulk) __syncthreads();
         bool big = false;
 #pragma unroll 1
         for (int i = tid; i < nx; i += dk::THREADS) {
@@ -407,61 +443,64 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
         __syncthreads();
-        // level 2: rank of a candidate = sum over the token's blocks of the number of that
-        // block's candidates that beat it (binary search in the sorted list)
+        if (C <= 64) {
+            // level 2 over the whole CTA: eight consecutive lanes per candidate, each comparing it with an
+            // eighth of the token's C candidates; the eight counts summed by shuffles give its rank (keys
+            // are distinct, so the ranks are too)
+            const int per = (C + 7) >> 3;
 #pragma unroll 1
-        for (int i = tid; i < T * C * nb; i += dk::THREADS) {
-            const int tc = fdiv(i, P.dv_nb), L = i - tc * nb;
-            const int t = fdiv(tc, P.dv_c);
-            const unsigned long long key = cand[tc];
-            const unsigned long long* list = cand + t * C + L * kk;
-            int lo = 0, hi = kk;
-#pragma unroll 1
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (list[mid] > key) lo = mid + 1;
-                else hi = mid;
+            for (int base = 0; base < T * C * 8; base += dk::THREADS) {
+                const int idx = base + tid;
+                const bool in = idx < T * C * 8;
+                const int tc = idx >> 3, part = idx & 7;
+                const int t = in ? fdiv(tc, P.dv_c) : 0;
+                const unsigned long long* ct = cand + t * C;
+                const unsigned long long key = in ? cand[tc] : 0ull;
+                int r = 0;
+                const int j0 = part * per, j1 = min(C, j0 + per);
+#pragma unroll 4
+                for (int j = j0; j < j1; ++j) r += ct[j] > key;
+                r += __shfl_xor_sync(0xffffffffu, r, 1);
+                r += __shfl_xor_sync(0xffffffffu, r, 2);
+                r += __shfl_xor_sync(0xffffffffu, r, 4);
+                if (in && part == 0 && r < k) s_ids[t * k + r] = (int)(0xFFFFFFFFu - (uint32_t)key);
             }
-            if (lo) atomicAdd(&s_rank[tc], lo);
-        }
-        __syncthreads();
-        // the k best of token t, in order, by warp t mod NW; then their weights exp(l_j - l_0) / sum
-        // over the k selected (the router's arithmetic)
+            __syncthreads();
+        } else {
+            // level 2: rank of a candidate = sum over the token's blocks of the number of that
+            // block's candidates that beat it (binary search in the sorted list)
 #pragma unroll 1
-        for (int t = warp; t < T; t += dk::NW) {
+            for (int i = tid; i < T * C * nb; i += dk::THREADS) {
+                const int tc = fdiv(i, P.dv_nb), L = i - tc * nb;
+                const int t = fdiv(tc, P.dv_c);
+                const unsigned long long key = cand[tc];
+                const unsigned long long* list = cand + t * C + L * kk;
+                int lo = 0, hi = kk;
 #pragma unroll 1
-            for (int i = lane; i < C; i += 32) {
-                const int r = s_rank[t * C + i];
-                if (r < k) s_ids[t * k + r] = (int)(0xFFFFFFFFu - (uint32_t)cand[t * C + i]);
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (list[mid] > key) lo = mid + 1;
+                    else hi = mid;
+                }
+                if (lo) atomicAdd(&s_rank[tc], lo);
             }
-            __syncwarp();
-            const int e = (lane < k) ? s_ids[t * k + lane] : 0;
-            const float v = (lane < k) ? lg[t * E + e] : -INFINITY;
-            const float m = __shfl_sync(0xffffffffu, v, 0);
-            float w;
-            if (m == -INFINITY || m != m) {
-                w = P.inv_k;
-            } else {
-                const float ej = (lane < k) ? expf(v - m) : 0.0f;
-                const float s = warp_sum(ej);
-                w = ej / s;
-            }
-            if (lane < k) {
-                s_wts[t * k + lane] = w;
-                if (c == 0 && a.ids_out) {
-                    a.ids_out[t * k + lane] = e;
-                    a.w_out[t * k + lane] = w;
+            __syncthreads();
+            // the k best of token t, in order, by warp t mod NW
+#pragma unroll 1
+            for (int t = warp; t < T; t += dk::NW) {
+#pragma unroll 1
+                for (int i = lane; i < C; i += 32) {
+                    const int r = s_rank[t * C + i];
+                    if (r < k) s_ids[t * k + r] = (int)(0xFFFFFFFFu - (uint32_t)cand[t * C + i]);
                 }
             }
+            __syncthreads();
         }
     }
-    __syncthreads();
-    if (misc[M_FLAG]) {  // rare: x rows with values beyond the f16 range
-        restage_scaled(misc + M_XEXP, xs, P.xs_stride, T, H, a.x, nullptr);
-        __syncthreads();
-    }
 
-    // ---------------- grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e}
+    // ---------------- grouping: permuted row of slot f = #{f2 : e2 < e} + #{f2 < f : e2 == e} (every
+    // token's ids are in: the router ends with a CTA barrier)
+    if (!route_mode) __syncthreads();
     if (route_mode && nf <= 32) {
         if (warp == 0) {  // one warp, shuffles
             const int f = lane;
@@ -477,6 +516,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 s_ptok[pos] = fdiv(f, P.dv_k);
                 s_pexp[pos] = e;
             }
+            __syncwarp();
         }
     } else if (route_mode) {
 #pragma unroll 1
@@ -516,7 +556,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             s_pexp[p] = lo;
         }
     }
-    __syncthreads();
+    if (!(route_mode && nf <= 32)) __syncthreads();
     // selected experts = segment starts of pexp (warp 0, ballot scan)
     if (warp == 0) {
         int run = 0;
@@ -548,6 +588,10 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         }
     }
     __syncthreads();
+    if (misc[M_FLAG]) {  // rare: x rows with values beyond the f16 range
+        restage_scaled(misc + M_XEXP, xs, P.xs_stride, T, H, a.x, nullptr);
+        __syncthreads();
+    }
     const int U = misc[M_U];
     const unsigned int epoch = (unsigned int)misc[M_EPOCH];
 
@@ -557,7 +601,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const int n1 = U * tiles_gu;
     const int n2 = H >> 4;
     const int o_beg = fdiv(n2 * c, P.dv_g), o_end = fdiv(n2 * (c + 1), P.dv_g);
-    const float inv_u = 1.0f / (float)max(U, 1);
+    const float inv_u = __fdividef(1.0f, (float)max(U, 1));
     // r / U for 0 <= r < 2^20: float estimate, corrected by one step
     auto div_u = [&](int r) {
         int q = (int)((float)r * inv_u);
@@ -572,9 +616,9 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         // Float rounding can move a boundary by a tile; both neighbours compute a boundary from
         // the same expression, so the tiles still partition (at worst a tile is done twice).
         const float b1 = (float)H, b2 = (float)I * (float)U;
-        float tgt = ((float)n1 * b1 + (float)n2 * b2) / (float)G;
-        tgt = fmaxf(tgt, (float)((n2 + G - 1) / G) * b2);
-        const float scale = (float)n1 / ((float)G * tgt - (float)n2 * b2);
+        float tgt = __fdividef((float)n1 * b1 + (float)n2 * b2, (float)G);
+        tgt = fmaxf(tgt, (float)P.max_ot * b2);
+        const float scale = __fdividef((float)n1, (float)G * tgt - (float)n2 * b2);
         p1_beg = c == 0 ? 0 : min(n1, __float2int_rn(((float)c * tgt - (float)o_beg * b2) * scale));
         p1_end = c == G - 1 ? n1 : min(n1, __float2int_rn(((float)(c + 1) * tgt - (float)o_end * b2) * scale));
         p1_end = max(p1_end, p1_beg);
@@ -664,7 +708,31 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     // once this warp's gate/up K-blocks are all consumed (they land during the hand-off)
 #pragma unroll 1
     for (int j = 0; j < min(R, cnt1 > 0 ? cnt1 : cnt); ++j) issue();
-    // tensor scales of the selected experts, read once the weights are on their way
+    // with the weights on their way: the routing weights exp(l_j - l_0) / sum over the k selected (the
+    // router's arithmetic), token t by warp t mod NW, and the tensor scales of the selected experts
+    if (route_mode) {
+#pragma unroll 1
+        for (int t = warp; t < T; t += dk::NW) {
+            const int e = (lane < k) ? s_ids[t * k + lane] : 0;
+            const float v = (lane < k) ? lg[t * E + e] : -INFINITY;
+            const float m = __shfl_sync(0xffffffffu, v, 0);
+            float w;
+            if (m == -INFINITY || m != m) {
+                w = P.inv_k;
+            } else {
+                const float ej = (lane < k) ? expf(v - m) : 0.0f;
+                const float s = warp_sum(ej);
+                w = ej / s;
+            }
+            if (lane < k) {
+                s_wts[t * k + lane] = w;
+                if (c == 0 && a.ids_out) {
+                    a.ids_out[t * k + lane] = e;
+                    a.w_out[t * k + lane] = w;
+                }
+            }
+        }
+    }
 #pragma unroll 1
     for (int u = tid; u < U; u += dk::THREADS) {
         const int wi = s_uwi[u];
@@ -831,7 +899,9 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         return;
     }
 
-    // ---------------- phase 2: all h rows (permuted order) staged as f16, as each becomes available
+    // ---------------- phase 2: all h rows (permuted order) staged as f16, as each becomes available (over
+    // the raw logits: every warp has read them by the barrier)
+    if (!split1) __syncthreads();
     {
         const unsigned int want = (P.wait_site == FT_WAIT_SITE_DECODE_H) ? (epoch ^ 0x80000000u) : epoch;
         const int total = nf * hw_row;
@@ -1039,6 +1109,7 @@ static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mod
     p.inv_k = 1.0f / (float)k;
     p.wait_ns = g_wait_ns.load();
     p.wait_site = g_wait_site.load();
+    p.logits_bulk = 0;
     return true;
 }
 
@@ -1073,6 +1144,7 @@ static ft_status launch_decode(DecodeArgs a, ft_stream_t stream, const char* fn)
     std::string why;
     if (!plan_decode(a.T, a.k, W.E, W.H, W.I, G, a.logits != nullptr, a.P, why))
         return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
+    a.P.logits_bulk = a.logits && aligned(a.logits, 16) && ((size_t)a.T * W.E * 4) % 16 == 0;
     ft_status st = decode_attributes(fn);
     if (st != FT_OK) return st;
     cudaLaunchConfig_t cfg = {};

@@ -40,6 +40,7 @@ struct ft_expert_cache {
     std::vector<std::vector<int32_t>> expert_of;  // [L][S] slot -> expert (-1 free)
     std::vector<std::vector<int64_t>> stamp;      // [L][S] step of last use
     std::vector<std::vector<int32_t>> slot_of;    // [L][E] expert -> slot (-1 absent)
+    std::vector<std::vector<uint8_t>> fetched;    // [L][S] put there by a prefetch and not used since
     // pinned staging of the published tables: a ring per layer, each entry guarded by an event
     static constexpr int kRing = 4;
     int32_t* pinned = nullptr;  // [L][kRing][E]
@@ -47,6 +48,7 @@ struct ft_expert_cache {
     std::vector<int> ring_pos;         // [L]
     // statistics and the host-side fault hook
     int64_t hits = 0, misses = 0, fills = 0, bytes_filled = 0;
+    int64_t prefetched = 0, prefetch_used = 0;  // experts installed by a prefetch; of those, later used
     int64_t fail_at_fill = -1;  // the slot copy (fill or resize move) with this 0-based index fails instead
     std::mutex mu;
 };
@@ -85,6 +87,7 @@ ft_status ft_expert_cache_create(int L, int E, int S, size_t expert_bytes, const
     c->expert_of.assign(L, std::vector<int32_t>(S, -1));
     c->stamp.assign(L, std::vector<int64_t>(S, -1));
     c->slot_of.assign(L, std::vector<int32_t>(E, -1));
+    c->fetched.assign(L, std::vector<uint8_t>(S, 0));
     c->ring_pos.assign(L, 0);
     *out = c;
     return FT_OK;
@@ -220,11 +223,16 @@ ft_status ft_expert_cache_lookup(ft_expert_cache* c, int layer, int64_t step, co
     auto& stamp = c->stamp[layer];
     auto& slot_of = c->slot_of[layer];
     int nm = 0;
+    auto& fetched = c->fetched[layer];
     for (int e : order) {
         int s = slot_of[e];
         if (s >= 0) {
             stamp[s] = step;
             ++c->hits;
+            if (fetched[s]) {
+                fetched[s] = 0;
+                ++c->prefetch_used;
+            }
             continue;
         }
         s = -1;
@@ -244,6 +252,7 @@ ft_status ft_expert_cache_lookup(ft_expert_cache* c, int layer, int64_t step, co
         expert_of[s] = e;
         stamp[s] = step;
         slot_of[e] = s;
+        fetched[s] = 0;
         miss_experts[nm] = e;
         miss_slots[nm] = s;
         ++nm;
@@ -251,6 +260,62 @@ ft_status ft_expert_cache_lookup(ft_expert_cache* c, int layer, int64_t step, co
     }
     for (int i = 0; i < n; ++i) slots_out[i] = slot_of[ids[i]];
     *n_miss = nm;
+    return FT_OK;
+}
+
+ft_status ft_expert_cache_prefetch(ft_expert_cache* c, int layer, int64_t step, const int32_t* ids, int n,
+                                   int32_t* fill_experts, int32_t* fill_slots, int* n_fill) {
+    const char* fn = "ft_expert_cache_prefetch";
+    if (!c || (n > 0 && (!ids || !fill_experts || !fill_slots)) || !n_fill)
+        return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if (layer < 0 || layer >= c->L || n < 0 || n > c->E)
+        return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 0 <= layer < L and 0 <= n <= E");
+    for (int i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= c->E) return cache_fail(FT_ERR_INVALID_ARG, std::string(fn) + ": expert id out of range");
+    std::lock_guard<std::mutex> lock(c->mu);
+    std::vector<int32_t> order(ids, ids + n);
+    std::sort(order.begin(), order.end());
+    order.erase(std::unique(order.begin(), order.end()), order.end());
+    auto& expert_of = c->expert_of[layer];
+    auto& stamp = c->stamp[layer];
+    auto& slot_of = c->slot_of[layer];
+    auto& fetched = c->fetched[layer];
+    int nf = 0;
+    for (int e : order) {
+        if (slot_of[e] >= 0) continue;  // resident: left as it is (a prediction is not a use)
+        int s = -1;
+        for (int q = 0; q < c->S; ++q)
+            if (expert_of[q] < 0) {
+                s = q;
+                break;
+            }
+        if (s < 0) {  // the oldest stamp before `step` (lower slot on a tie) among experts not predicted now;
+                      // this step's experts stay
+            for (int q = 0; q < c->S; ++q)
+                if (stamp[q] < step && !std::binary_search(order.begin(), order.end(), expert_of[q]) &&
+                    (s < 0 || stamp[q] < stamp[s]))
+                    s = q;
+            if (s < 0) continue;
+            slot_of[expert_of[s]] = -1;
+        }
+        expert_of[s] = e;
+        stamp[s] = step - 1;
+        slot_of[e] = s;
+        fetched[s] = 1;
+        fill_experts[nf] = e;
+        fill_slots[nf] = s;
+        ++nf;
+        ++c->prefetched;
+    }
+    *n_fill = nf;
+    return FT_OK;
+}
+
+ft_status ft_expert_cache_prefetch_stats(ft_expert_cache* c, int64_t* prefetched, int64_t* used) {
+    if (!c || !prefetched || !used) return cache_fail(FT_ERR_INVALID_ARG, "ft_expert_cache_prefetch_stats: null pointer");
+    std::lock_guard<std::mutex> lock(c->mu);
+    *prefetched = c->prefetched;
+    *used = c->prefetch_used;
     return FT_OK;
 }
 
@@ -374,18 +439,21 @@ ft_status ft_expert_cache_resize(ft_expert_cache* c, int new_S, void* new_slots,
     for (int l = 0; l < c->L; ++l) {
         std::vector<int32_t> eo(new_S, -1);
         std::vector<int64_t> sp(new_S, -1);
+        std::vector<uint8_t> fe(new_S, 0);
         if (st == FT_OK)
             for (int i = 0; i < new_S; ++i) {
                 const int q = moves[(size_t)l * new_S + i];
                 if (q < 0) continue;
                 eo[i] = c->expert_of[l][q];
                 sp[i] = c->stamp[l][q];
+                fe[i] = c->fetched[l][q];
             }
         std::fill(c->slot_of[l].begin(), c->slot_of[l].end(), -1);
         for (int i = 0; i < new_S; ++i)
             if (eo[i] >= 0) c->slot_of[l][eo[i]] = i;
         c->expert_of[l].swap(eo);
         c->stamp[l].swap(sp);
+        c->fetched[l].swap(fe);
     }
     c->S = new_S;
     c->slots = nb;

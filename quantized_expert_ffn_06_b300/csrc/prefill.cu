@@ -84,10 +84,16 @@ struct PfGemmArgs {
     int KSN2;
     // combine epilogue
     const int2* rowmeta;     // [tiles*128] (token, routing weight bits) per padded row, token -1 for padding
-    float* out32;            // [T][H]
+    float* out32;            // [T][H], or nullptr: no combine
     int H;
     int nstages;             // ring stages (resident-token-tile kernel)
+    const int32_t* e2s;      // optional expert -> weight index (slot table); validated by the plan
+    const int4* tinfo;       // [tiles] {expert, first permuted row, real rows, 0}
+    float* y;                // optional [T*k][H] fp32 per-row expert outputs (tensor scale applied, no routing weight)
 };
+
+// weight index of expert e (identity without a slot table; the plan has checked every expert with rows)
+__device__ __forceinline__ int64_t pf_widx(const PfGemmArgs& a, int e) { return a.e2s ? (int64_t)__ldg(a.e2s + e) : e; }
 
 // ---------------------------------------------------------------------------- PTX helpers
 
@@ -187,10 +193,13 @@ __host__ __device__ __forceinline__ int blk_scale_off(int r, int j) {
 // ---------------------------------------------------------------------------- plan and activation tiles
 
 // tile_off[e] = first tile of expert e (exclusive scan of its tile counts);
-// tinfo[tile] = {expert, first permuted row, real rows in the tile, 0}.
+// tinfo[tile] = {expert, first permuted row, real rows in the tile, 0}.  With a
+// slot table, an expert with rows whose slot is out of [0, n_weights) raises
+// FT_DEVERR_BAD_INDEX and gets no tiles.
 // offsets must partition [0, P) in order; otherwise FT_DEVERR_BAD_INDEX is
 // raised and every tile count is zero, so the later kernels do nothing.
 __global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ offsets, int E, int P, int max_tiles,
+                                                  const int32_t* __restrict__ e2s, int n_weights,
                                                   int32_t* __restrict__ tile_off, int4* __restrict__ tinfo) {
     __shared__ int wsum[33];
     __shared__ int s_bad;
@@ -201,7 +210,14 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ of
     const int o0 = (tid < E) ? offsets[tid] : 0;
     const int o1 = (tid < E) ? offsets[tid + 1] : 0;
     if (tid < E && (o0 < 0 || o1 < o0 || o1 > P || (tid == 0 && o0 != 0) || (tid == E - 1 && o1 != P))) s_bad = 1;
-    const int n = max(o1 - o0, 0);
+    int n = max(o1 - o0, 0);
+    if (e2s && n > 0) {  // an expert whose slot is invalid gets no tiles: its rows contribute nothing
+        const int sl = e2s[tid];
+        if (sl < 0 || sl >= n_weights) {
+            raise_dev_error(FT_DEVERR_BAD_INDEX);
+            n = 0;
+        }
+    }
     const int nt = (n + 127) / 128;
     int incl = nt;
     const int lane = tid & 31, wid = tid >> 5;
@@ -414,9 +430,18 @@ __device__ __forceinline__ void epi_swiglu(const PfGemmArgs& a, const uint32_t (
 // Down projection + combine: out32[t][m*128 + c0 .. +31] += w * tsd * y for the
 // thread's token row (row table entry: token, routing weight; token -1 for
 // padding), as eight 16-byte vector reductions.
-__device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t (&v)[32], int2 meta, int m, int c0,
-                                            float tsd) {
+// With a y output, the row's y = tsd * acc (no routing weight) also goes to y[prow][...].
+__device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t (&v)[32], int2 meta, int prow, int m,
+                                            int c0, float tsd) {
     if (meta.x < 0) return;
+    if (a.y) {
+        float4* yd = reinterpret_cast<float4*>(a.y + (int64_t)prow * a.H + m * 128 + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            yd[i] = make_float4(__uint_as_float(v[4 * i]) * tsd, __uint_as_float(v[4 * i + 1]) * tsd,
+                                __uint_as_float(v[4 * i + 2]) * tsd, __uint_as_float(v[4 * i + 3]) * tsd);
+    }
+    if (!a.out32) return;
     const float wt = __int_as_float(meta.y) * tsd;
     float* dst = a.out32 + (int64_t)meta.x * a.H + m * 128 + c0;
 #pragma unroll
@@ -478,7 +503,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
             for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
                 int e, m, ntg;
                 item(i, e, m, ntg);
-                const uint8_t* ab = a.A + (int64_t)e * a.a_stride + (int64_t)m * a.KSN * pf::BLK;
+                const uint8_t* ab = a.A + pf_widx(a, e) * a.a_stride + (int64_t)m * a.KSN * pf::BLK;
                 const uint8_t* bb = a.B + (int64_t)ntg * a.KSN * pf::BLK;
                 // a tile's K blocks are contiguous: KPS of them (A, then B) per stage
                 for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
@@ -555,10 +580,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
             // everything that does not depend on the accumulator is loaded before waiting for it
             int e, m, ntg;
             item(i, e, m, ntg);
-            const float* ts = a.tscale + (int64_t)e * a.ts_stride;
+            const float* ts = a.tscale + pf_widx(a, e) * a.ts_stride;
             const float t0s = __ldg(ts + 0), t1s = __ldg(ts + 1), t2s = __ldg(ts + 2);
             int2 meta = make_int2(-1, 0);
-            if (EPI == 2) meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
+            int prow = -1;  // permuted row of this token row of the tile (y output)
+            if (EPI == 2) {
+                meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
+                if (a.y) prow = __ldg(a.tinfo + ntg).y + r;
+            }
             if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // the accumulator is in registers once the load has completed: hand the TMEM columns back to
@@ -569,7 +598,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pf_su(&acc_empty[buf])) : "memory");
             if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
-            else epi_combine(a, v, meta, m, c0, t2s);
+            else epi_combine(a, v, meta, prow, m, c0, t2s);
         }
     }
     // all MMAs have completed once the epilogue has consumed every accumulator; on an abort
@@ -663,7 +692,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                         pf_su(btile)), "l"(a.B + (int64_t)ntg * a.KSN * pf::BLK), "r"(tile_bytes), "r"(pf_su(&bfull))
                     : "memory");
                 ++bi;
-                const uint8_t* ae = a.A + (int64_t)e * a.a_stride;
+                const uint8_t* ae = a.A + pf_widx(a, e) * a.a_stride;
                 bool stop = false;
                 for (int m = mlo; m < mhi && !stop; ++m) {
                     // warm L2 with the item's next weight tile, or with the next item's token tile,
@@ -780,10 +809,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
         for (int i = blockIdx.x; i < n_items && !stop; i += gridDim.x) {
             int e, ntg, mlo, mhi;
             if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
-            const float* ts = a.tscale + (int64_t)e * a.ts_stride;
+            const float* ts = a.tscale + pf_widx(a, e) * a.ts_stride;
             const float t0s = __ldg(ts + 0), t1s = __ldg(ts + 1), t2s = __ldg(ts + 2);
             int2 meta = make_int2(-1, 0);
-            if (EPI == 2) meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
+            int prow = -1;  // permuted row of this token row of the tile (y output)
+            if (EPI == 2) {
+                meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
+                if (a.y) prow = __ldg(a.tinfo + ntg).y + r;
+            }
             for (int m = mlo; m < mhi; ++m, ++it) {
                 const int buf = it & 1;
                 if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) {
@@ -799,7 +832,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                 __syncwarp();
                 if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pf_su(&acc_empty[buf])) : "memory");
                 if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
-                else epi_combine(a, v, meta, m, c0, t2s);
+                else epi_combine(a, v, meta, prow, m, c0, t2s);
             }
         }
     }
@@ -934,23 +967,24 @@ size_t ft_moe_prefill_workspace_size(int T, int k, int E, int H, int I) {
 }
 
 ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const uint16_t* x, int T, int k,
-                                          const int32_t* offsets, const int32_t* perm, const float* w, uint16_t* out,
-                                          void* ws, size_t ws_bytes, ft_stream_t stream) {
+                                          const int32_t* offsets, const int32_t* perm, const float* w, float* y,
+                                          uint16_t* out, void* ws, size_t ws_bytes, ft_stream_t stream) {
     const char* fn = "ft_moe_expert_ffn_nvfp4_prefill";
     ft_status st = validate_weights(W, fn);
     if (st != FT_OK) return st;
     if (W->layout != FT_LAYOUT_UMMA_TILES)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights must use FT_LAYOUT_UMMA_TILES");
-    if (W->expert_to_slot) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": slot tables are not supported");
     if (W->H % 128 || W->I % 64 || (2 * W->I) % 128)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need H a multiple of 128 and I of 64");
     if (W->I % 128) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": I must be a multiple of 128");
     if (T < 0 || k <= 0 || k > W->E || k > 32) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need T >= 0, 1 <= k <= min(E, 32)");
     if (T == 0) return FT_OK;
     if ((int64_t)T * k > INT32_MAX) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": T*k must fit in int32");
-    if (!x || !offsets || !perm || !w || !out) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if (!x || !offsets || !perm || (out && !w)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if (!y && !out) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need y or out");
     if (!aligned(x, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": x needs 16-byte alignment");
-    if (!aligned(out, 8)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": out needs 8-byte alignment");
+    if (out && !aligned(out, 8)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": out needs 8-byte alignment");
+    if (y && !aligned(y, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": y needs 16-byte alignment");
     const int E = W->E, H = W->H, I = W->I;
     const PfWs L = pf_ws_layout(T, k, E, H, I);
     if (!ws || ws_bytes < L.total || !aligned(ws, 256))
@@ -971,7 +1005,8 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
         cudaFuncSetAttribute(k_pf_gemm_res<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM_LIMIT);
         cudaFuncSetAttribute(k_pf_gemm_res<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pf::SMEM_LIMIT);
     });
-    k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, (int)((int64_t)T * k), L.max_tiles, tile_off, tinfo);
+    k_pf_plan<<<1, 1024, 0, s>>>(offsets, E, (int)((int64_t)T * k), L.max_tiles, W->expert_to_slot, W->n_weights,
+                                  tile_off, tinfo);
     {
         const int64_t warps = (int64_t)T * ((H + 1023) / 1024);
         k_pf_quant_tokens<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(x, T, H, xc);
@@ -987,8 +1022,11 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     g.hq = hq;
     g.KSN2 = I / 128;
     g.rowmeta = rowmeta;
-    g.out32 = out32;
+    g.out32 = out ? out32 : nullptr;
     g.H = H;
+    g.e2s = W->expert_to_slot;
+    g.tinfo = tinfo;
+    g.y = y;
     const int G = pf_sm_count();
     // gate/up + SwiGLU
     g.A = W->gu_codes;
@@ -1004,6 +1042,7 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     g.MT = H / 128;
     g.KSN = I / 128;
     launch_pf_gemm<2>(g, G, s);
+    if (!out) return check_launch(fn);
     const int64_t n4 = (int64_t)T * H / 4;  // H is a multiple of 128
     k_pf_out<<<(unsigned)std::min<int64_t>((n4 + 255) / 256, 148 * 16), 256, 0, s>>>(
         reinterpret_cast<const float4*>(out32), n4, reinterpret_cast<uint2*>(out));

@@ -434,16 +434,22 @@ class CachedDecodeLayer:
 
     route (device) -> expert ids to the host -> LRU lookup -> fills of the misses on the copy stream -> publish the
     slot table -> the fused layer kernel (which routes again, identically, and reads weights through the table).
-    """
 
-    def __init__(self, pool: ExpertSlotPool, layer: int, k: int, T: int, copy_stream=None, timeout_s: float = 2.0):
+    With prefetch = P > 0 the router also ranks the next P experts of the token, and those are installed in the
+    cache for the next token and copied on the copy stream behind this token's fills, overlapping later layers'
+    compute (router-driven prefetch; ft_expert_cache_prefetch)."""
+
+    def __init__(self, pool: ExpertSlotPool, layer: int, k: int, T: int, copy_stream=None, timeout_s: float = 2.0,
+                 prefetch: int = 0):
         self.pool, self.layer, self.k, self.T = pool, layer, k, T
         self.timeout_s = timeout_s
+        self.prefetch = prefetch
         dev = pool.device
         self.weights = pool.layer_weights(layer)
-        self.ids = torch.empty((T, k), dtype=torch.int32, device=dev)
-        self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
-        self.ids_host = torch.empty((T, k), dtype=torch.int32).pin_memory()
+        kr = k + prefetch  # the router ranks k + P experts; the first k are the token's (same order, same ties)
+        self.ids = torch.empty((T, kr), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, kr), dtype=torch.float32, device=dev)
+        self.ids_host = torch.empty((T, kr), dtype=torch.int32).pin_memory()
         self.fused = FusedDecodeLayer(pool.E, pool.H, pool.I, k, T, dev)
         self.copy_stream = copy_stream if copy_stream is not None else torch.cuda.Stream(device=dev)
         self.filled = torch.cuda.Event()
@@ -451,12 +457,13 @@ class CachedDecodeLayer:
 
     def __call__(self, logits: torch.Tensor, x: torch.Tensor, out: torch.Tensor, step: int, stream=None):
         stream = torch.cuda.current_stream(self.pool.device) if stream is None else stream
-        ft_moe_route(logits, self.k, self.ids, self.w, stream=stream)
+        ft_moe_route(logits, self.k + self.prefetch, self.ids, self.w, stream=stream)
         with torch.cuda.stream(stream):
             self.ids_host.copy_(self.ids, non_blocking=True)
             self.routed.record(stream)
         wait_event(self.routed, self.timeout_s, f"layer {self.layer}: routing result")
-        needed = sorted(set(int(e) for e in self.ids_host.view(-1).tolist()))
+        ranked = self.ids_host.tolist()
+        needed = sorted(set(int(e) for row in ranked for e in row[:self.k]))
         _, misses = self.pool.cache.lookup(self.layer, step, needed)
         for e, s in misses:
             self.pool.cache.fill(self.layer, e, s, stream=self.copy_stream)
@@ -464,4 +471,11 @@ class CachedDecodeLayer:
         self.pool.cache.publish(self.layer, stream=stream)
         stream.wait_event(self.filled)
         self.fused(self.weights, logits, x, out, routing=False, stream=stream)
+        if self.prefetch:
+            # the next-ranked experts, for the next token: copied behind this token's fills, which the next step's
+            # kernel waits for (same copy stream), while this and later layers compute
+            predicted = sorted(set(int(e) for row in ranked for e in row[self.k:]) - set(needed))
+            self.prefetched = self.pool.cache.prefetch(self.layer, step, predicted)
+            for e, s in self.prefetched:
+                self.pool.cache.fill(self.layer, e, s, stream=self.copy_stream)
         return misses

@@ -90,14 +90,14 @@ def test_prefill_argument_checks():
     W = weights(layout=Q.FT_LAYOUT_UMMA_TILES)
     ws = L.ft_moe_prefill_workspace_size(64, 2, W.E, W.H, W.I)
 
-    def call(Wd=W, x=P, T=64, k=2, offsets=P, perm=P, w=P, out=P, wsp=P, ws_bytes=ws):
-        return L.ft_moe_expert_ffn_nvfp4_prefill(ctypes.byref(Wd), x, T, k, offsets, perm, w, out, wsp, ws_bytes,
+    def call(Wd=W, x=P, T=64, k=2, offsets=P, perm=P, w=P, y=NULL, out=P, wsp=P, ws_bytes=ws):
+        return L.ft_moe_expert_ffn_nvfp4_prefill(ctypes.byref(Wd), x, T, k, offsets, perm, w, y, out, wsp, ws_bytes,
                                                  NULL)
 
     status(call(Wd=weights(layout=Q.FT_LAYOUT_DECODE_TILES)), Q.FT_ERR_INVALID_ARG)
-    status(call(Wd=weights(layout=Q.FT_LAYOUT_UMMA_TILES, slot_table=True)), Q.FT_ERR_UNSUPPORTED)
     for bad in (dict(T=-1), dict(k=0), dict(k=9), dict(k=2, T=1 << 30), dict(x=NULL), dict(offsets=NULL),
-                dict(x=MIS), dict(out=P + 4), dict(wsp=NULL), dict(ws_bytes=ws - 1), dict(wsp=P + 16)):
+                dict(x=MIS), dict(out=P + 4), dict(wsp=NULL), dict(ws_bytes=ws - 1), dict(wsp=P + 16),
+                dict(out=NULL), dict(y=P + 8), dict(w=NULL)):
         status(call(**bad), Q.FT_ERR_INVALID_ARG)
     status(call(T=0), Q.FT_OK)
 
@@ -116,3 +116,23 @@ def test_quantiser_argument_checks():
     status(L.ft_nvfp4_quantize_weight(NULL, 16, 256, P, 128, P, 16, P, P, need, NULL), Q.FT_ERR_INVALID_ARG)
     status(L.ft_nvfp4_quantize_weight(P, 16, 256, P, 127, P, 16, P, P, need, NULL), Q.FT_ERR_INVALID_ARG)  # ld < K/2
     status(L.ft_nvfp4_quantize_act(P, 4, 250, P, P, NULL), Q.FT_ERR_INVALID_ARG)
+
+
+def test_no_alloc_decode_argument_checks_come_before_any_cuda_call():
+    """The entry point without a workspace rejects bad arguments before it looks up its scratch (a CUDA call)."""
+    W = weights()
+
+    def call(**over):
+        a = dict(dict(logits=P, x=P, T=4, k=2, out=P, ids=NULL, w=NULL), **over)
+        return L.ft_moe_layer_decode_noalloc(ctypes.byref(a.pop("W", W)), a["logits"], a["x"], a["T"], a["k"], a["out"],
+                                             a["ids"], a["w"], NULL)
+
+    status(L.ft_moe_layer_decode_noalloc(None, P, P, 4, 2, P, NULL, NULL, NULL), Q.FT_ERR_INVALID_ARG)
+    status(call(W=weights(layout=Q.FT_LAYOUT_UMMA_TILES)), Q.FT_ERR_INVALID_ARG)
+    for bad in (dict(T=-1), dict(T=17), dict(k=0), dict(k=9), dict(logits=NULL), dict(x=NULL), dict(out=NULL),
+                dict(ids=P), dict(w=P), dict(x=MIS), dict(logits=MIS)):
+        status(call(**bad), Q.FT_ERR_INVALID_ARG)
+    # T*k*I beyond the built-in scratch
+    status(call(W=weights(E=64, I=1024), T=16, k=32), Q.FT_ERR_INVALID_ARG)
+    assert b"scratch" in L.ft_last_error()
+    status(call(T=0), Q.FT_OK)

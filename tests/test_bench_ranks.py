@@ -71,7 +71,7 @@ def test_reference_arm_under_two_ranks_prints_one_line_from_rank_0():
     port = free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port),
-           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1"]
+           "bench.py", "--impl", "reference", "--config", "tiny", "--gpus", "2", "--steps", "2", "--warmup", "1"]
     env = dict(os.environ, OMP_NUM_THREADS="2")
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-3000:]

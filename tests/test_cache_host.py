@@ -163,3 +163,35 @@ def test_bounded_host_wait_gives_up_with_a_timeout_status():
     assert 0.05 <= time.monotonic() - t0 < 1.0
     assert ev.queries > 1
     wait_event(_ReadyAfter(3), 1.0, "routing result")   # completes before the limit: returns
+
+
+def test_prefetch_matches_oracle_along_the_stream():
+    """Lookup + prefetch of a noisy predictor (the next token's experts, some replaced by random ids) through the
+    library against the oracle, on two layers: the same fills, the same slots for every token, the same stats."""
+    import numpy as np
+    cfg = W.scaled(W.CONFIGS["cache_stream"], steps=150)
+    L = 2
+    c = fake_cache(L, cfg.E, cfg.slots)
+    oracles = [LayerLRU(cfg.slots) for _ in range(L)]
+    sets = [W.cache_stream_sets(cfg, 10 + l, 150) for l in range(L)]
+    rng = np.random.default_rng(5)
+    for s in range(150):
+        for l in range(L):
+            got = c.lookup(l, s, list(sets[l][s]))
+            want = oracles[l].access(s, list(sets[l][s]))
+            assert got[0] == want[0] and got[1] == [tuple(m) for m in want[1]], (s, l)
+            if s + 1 < 150:
+                pred = [int(e) for e in sets[l][s + 1]]
+                pred = [e if rng.random() < 0.8 else int(rng.integers(cfg.E)) for e in pred] + [pred[0]]  # a repeat
+                assert c.prefetch(l, s, pred) == [tuple(f) for f in oracles[l].prefetch(s, pred)], (s, l)
+    assert c.prefetch_stats() == (sum(o.prefetched for o in oracles), sum(o.prefetch_used for o in oracles))
+    assert c.prefetch_stats()[1] > 0
+
+
+def test_prefetch_rejects_bad_ids():
+    c = fake_cache(1, 16, 3)
+    for ids in ([16], [-1]):
+        with pytest.raises(Q.FtError) as ei:
+            c.prefetch(0, 0, ids)
+        assert ei.value.status == Q.FT_ERR_INVALID_ARG
+    assert c.prefetch(0, 0, []) == []

@@ -57,10 +57,11 @@ def pool_and_resident():
     return make_pool(CFG)
 
 
-def run_stream(cfg, pool, resident, oracle_steps):
-    """The cached decode stream over cfg.steps tokens and cfg.layers layers: misses as the oracle LRU predicts,
-    outputs bit-equal to the resident weights, and equal to the oracle within the tolerance at oracle_steps."""
-    layers = [CachedDecodeLayer(pool, l, cfg.k, cfg.T) for l in range(cfg.layers)]
+def run_stream(cfg, pool, resident, oracle_steps, prefetch=0):
+    """The cached decode stream over cfg.steps tokens and cfg.layers layers: misses (and, with prefetch = P, the
+    prefetch fills of the router's next P ranks) as the oracle LRU predicts, outputs bit-equal to the resident
+    weights, and equal to the oracle within the tolerance at oracle_steps."""
+    layers = [CachedDecodeLayer(pool, l, cfg.k, cfg.T, prefetch=prefetch) for l in range(cfg.layers)]
     ref_mods = [FusedDecodeLayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV) for _ in range(cfg.layers)]
     oracles = [LayerLRU(cfg.slots) for _ in range(cfg.layers)]
     want_miss_total = 0
@@ -81,11 +82,16 @@ def run_stream(cfg, pool, resident, oracle_steps):
             _, want_misses = oracles[l].access(step, ids)
             assert misses == [tuple(m) for m in want_misses], (step, l)
             want_miss_total += len(want_misses)
+            if prefetch:
+                ranked = [int(e) for e in O.route(logits_np, cfg.k + prefetch)[0][0]]
+                assert sorted(ranked[:cfg.k]) == ids
+                want_fills = oracles[l].prefetch(step, sorted(set(ranked[cfg.k:]) - set(ids)))
+                assert layers[l].prefetched == [tuple(f) for f in want_fills], (step, l)
             assert torch.equal(out, ref), (step, l)
             if step in oracle_steps:
                 r = O.moe_layer(logits_np, x_np, cfg.k, resident[l].oracle, O.MODE_A16)
                 assert_layer_close(out.float().cpu().numpy(), r["out"], f"cached layer {l} step {step}")
-    return want_miss_total
+    return want_miss_total, oracles
 
 
 def test_fill_copies_the_host_block_into_the_slot(pool_and_resident):
@@ -110,7 +116,7 @@ def test_fill_copies_the_host_block_into_the_slot(pool_and_resident):
 
 def test_cached_decode_stream_equals_resident_weights(pool_and_resident):
     pool, resident = pool_and_resident
-    want_miss_total = run_stream(CFG, pool, resident, oracle_steps=(0, 11, 23))
+    want_miss_total, _ = run_stream(CFG, pool, resident, oracle_steps=(0, 11, 23))
     hits, miss, filled = pool.cache.stats()
     assert miss == want_miss_total
     assert filled == miss * pool.expert_bytes
@@ -124,10 +130,26 @@ def test_cached_decode_stream_at_the_workload_shape():
     cfg = W.scaled(W.CONFIGS["cache_stream"], layers=2, steps=16)
     assert (cfg.H, cfg.I, cfg.E, cfg.k, cfg.slots) == (4096, 1536, 128, 8, 32)
     pool, resident = make_pool(cfg)
-    want_miss_total = run_stream(cfg, pool, resident, oracle_steps=(0, 7, 15))
+    want_miss_total, _ = run_stream(cfg, pool, resident, oracle_steps=(0, 7, 15))
     hits, miss, filled = pool.cache.stats()
     assert miss == want_miss_total and filled == miss * pool.expert_bytes
     assert hits > miss
+
+
+def test_cached_decode_stream_with_router_driven_prefetch():
+    """Prefetch of the router's next 4 ranks after each token: the prefetch fills (copied on the copy stream behind
+    the token's misses while later layers compute) and the demand misses follow the oracle LRU with its prefetch
+    reading, the outputs stay bit-equal to the resident weights, and the library's prefetch counters equal the
+    oracle's."""
+    cfg = CFG
+    pool, resident = make_pool(cfg)
+    want_miss_total, oracles = run_stream(cfg, pool, resident, oracle_steps=(0, 23), prefetch=4)
+    hits, miss, filled = pool.cache.stats()
+    prefetched, used = pool.cache.prefetch_stats()
+    assert miss == want_miss_total
+    assert prefetched == sum(o.prefetched for o in oracles) > 0
+    assert used == sum(o.prefetch_used for o in oracles)
+    assert filled == (miss + prefetched) * pool.expert_bytes
 
 
 def test_injected_fill_failure_leaves_the_device_usable(pool_and_resident):

@@ -223,3 +223,49 @@ def test_streamed_layers_equal_resident_weights():
             assert torch.equal(outs[l], ref), (call, l)
             if l == 0 and call == 0:
                 check(cfg, lws[0], mod, outs[0], logits[0], xs[0])
+
+
+def test_per_row_outputs_and_slot_table():
+    """The per-row expert outputs y (fp32, no routing weight) against the oracle's y; the same call through a slot
+    table that stores expert e at slot perm[e] gives bit-identical outputs (k = 2: two fp32 additions onto zero per
+    output element, so their order cannot matter); an expert mapped to an invalid slot is flagged and contributes
+    nothing (the oracle with that expert's weights all zero)."""
+    cfg = W.scaled(W.CONFIGS["tiny"], T=200)
+    dl = weights(cfg, 0)
+    logits, x_bits = W.router_logits(cfg, 0, 6), W.activations_bf16(cfg, 0, 6)
+    mod, out = run(cfg, dl, logits, x_bits)
+    x_dev = to_dev(x_bits.view(np.int16), torch.bfloat16)
+    y = torch.full((cfg.T * cfg.k, cfg.H), float("nan"), dtype=torch.float32, device=DEV)
+    Q.ft_moe_expert_ffn_nvfp4_prefill(dl.w, x_dev, cfg.k, mod.offsets, mod.perm, mod.w, None, mod.ws, y=y)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    ref = O.moe_layer(logits, x_bits, cfg.k, dl.oracle, O.MODE_A4)
+    assert_layer_close(y.cpu().numpy(), ref["y"], "prefill y")
+
+    slots = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, n_weights=cfg.E, layout=Q.FT_LAYOUT_UMMA_TILES)
+    perm = np.random.default_rng(5).permutation(cfg.E)
+    for e in range(cfg.E):
+        s = int(perm[e])
+        slots.gu_codes[s].copy_(dl.w.gu_codes[e])
+        slots.d_codes[s].copy_(dl.w.d_codes[e])
+        slots.tscale[s].copy_(dl.w.tscale[e])
+    slots.expert_to_slot = to_dev(perm.astype(np.int32))
+    out_s = torch.empty_like(out)
+    Q.ft_moe_expert_ffn_nvfp4_prefill(slots, x_dev, cfg.k, mod.offsets, mod.perm, mod.w, out_s, mod.ws)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    assert torch.equal(out_s, out)
+
+    counts = np.diff(mod.offsets.cpu().numpy())
+    bad = int(np.argmax(counts))   # an expert with rows
+    table = perm.astype(np.int32).copy()
+    table[bad] = -1
+    slots.expert_to_slot = to_dev(table)
+    Q.ft_moe_expert_ffn_nvfp4_prefill(slots, x_dev, cfg.k, mod.offsets, mod.perm, mod.w, out_s, mod.ws)
+    assert Q.ft_device_status() == Q.FT_DEVERR_BAD_INDEX
+    H, I = cfg.H, cfg.I
+    zero = O.QuantizedExpert((np.zeros((I, H // 2), np.uint8), np.zeros((I, H // 16), np.uint8), 1.0),
+                             (np.zeros((I, H // 2), np.uint8), np.zeros((I, H // 16), np.uint8), 1.0),
+                             (np.zeros((H, I // 2), np.uint8), np.zeros((H, I // 16), np.uint8), 1.0))
+    ref_bad = O.moe_layer(logits, x_bits, cfg.k, lambda e: zero if e == bad else dl.oracle(e), O.MODE_A4)
+    assert_layer_close(out_s.float().cpu().numpy(), ref_bad["out"], "prefill without the unmapped expert")

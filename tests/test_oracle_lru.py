@@ -100,3 +100,56 @@ def test_resize_keeps_survivors_in_old_slot_order():
     assert c.stamp == [1, 2, 0]
     assert c.resize(2) == [0, 1]
     assert c.expert_of == [10, 11] and c.stamp == [1, 2]
+
+
+def test_prefetch_hand_worked():
+    """Worked by hand from the prefetch reading.  Two slots: the second prediction may not displace the first one
+    (both stamped step - 1 = 0 like the residents), and a resident expert is left with its own stamp."""
+    c = LayerLRU(2)
+    c.access(0, [1, 2])                          # 1 -> slot 0, 2 -> slot 1, stamps 0
+    assert c.prefetch(1, [7, 5, 5]) == [(5, 0), (7, 1)]   # ascending, repeats ignored
+    assert c.expert_of == [5, 7] and c.stamp == [0, 0] and c.fetched == [True, True]
+    assert c.prefetch(1, [5]) == [] and c.stamp == [0, 0]  # resident: no fill, no restamp
+    assert c.access(1, [7]) == ([1], []) and c.prefetch_used == 1 and c.prefetched == 2
+    assert c.fetched == [True, False]
+    assert c.access(2, [5, 9]) == ([0, 1], [(9, 1)]) and c.prefetch_used == 2
+
+
+def test_prefetch_keeps_the_current_steps_experts():
+    """Worked by hand: slot 0 holds expert 3, used at step 1; a prefetch at step 1 takes slot 1 (stamp 0) and then
+    finds no slot for the second prediction."""
+    c = LayerLRU(2)
+    c.access(0, [1, 2])
+    c.access(1, [3])                             # evicts expert 1 (slot 0); 3 stamped 1
+    assert c.prefetch(1, [4, 5]) == [(4, 1)]     # 5 finds no slot older than step 1 that this call did not fill
+    assert c.expert_of == [3, 4] and c.stamp == [1, 0]
+    assert c.prefetch(2, [6]) == [(6, 1)]        # at step 2 both are older; stamp 0 < 1 picks slot 1
+
+
+def test_perfect_prediction_leaves_no_miss_on_the_stream():
+    """With the next token's experts predicted exactly, every access after the first is a hit: the k current experts
+    stay (stamp == step) and the other slots - at least k of them - take the new ones (slots >= 2k)."""
+    cfg = W.scaled(W.CONFIGS["cache_stream"], steps=200)
+    sets = W.cache_stream_sets(cfg, 2, 200)
+    assert cfg.slots >= 2 * cfg.k
+    c = LayerLRU(cfg.slots)
+    for s, ids in enumerate(sets):
+        _, misses = c.access(s, list(ids))
+        assert s == 0 or misses == []
+        if s + 1 < len(sets):
+            before = {c.expert_of[q] for q in range(c.slots)}
+            fills = c.prefetch(s, list(sets[s + 1]))
+            assert {e for e, _ in fills} == set(sets[s + 1]) - before
+            assert all(c.expert_of[q] in ids for q in range(c.slots) if c.stamp[q] == s)
+            assert set(ids) <= set(c.slot_of)
+    assert 0 < c.prefetch_used == c.prefetched   # every exact prediction is used by the next token
+
+
+def test_prefetch_keeps_a_predicted_resident():
+    """Worked by hand: expert 1 (slot 0, stamp 0) is predicted again with expert 9; 9 must take slot 1 (stamp 0,
+    tie broken to the lower slot would otherwise pick slot 0)."""
+    c = LayerLRU(3)
+    c.access(0, [1, 2])
+    c.access(1, [3])                             # 3 -> slot 2, stamp 1
+    assert c.prefetch(1, [1, 9]) == [(9, 1)]     # slot 0 holds a predicted expert, slot 2 is this step's
+    assert c.expert_of == [1, 9, 3] and c.stamp == [0, 0, 1] and c.fetched == [False, True, False]

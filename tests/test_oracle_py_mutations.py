@@ -14,11 +14,22 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 LRU_MUTATIONS = [
-    ("evicts the newest", "key=lambda q: (self.stamp[q], q)", "key=lambda q: (-self.stamp[q], q)"),
-    ("eviction ties to the higher slot", "key=lambda q: (self.stamp[q], q)", "key=lambda q: (self.stamp[q], -q)"),
-    ("takes the highest free slot", "s = free[0]", "s = free[-1]"),
-    ("hit keeps the old stamp", "                self.stamp[s] = step\n                result[e] = s",
-     "                result[e] = s"),
+    ("evicts the newest", "s = min(cands, key=lambda q: (self.stamp[q], q))",
+     "s = min(cands, key=lambda q: (-self.stamp[q], q))"),
+    ("eviction ties to the higher slot", "s = min(cands, key=lambda q: (self.stamp[q], q))",
+     "s = min(cands, key=lambda q: (self.stamp[q], -q))"),
+    ("takes the highest free slot", "            if free:\n                s = free[0]\n            else:\n                cands",
+     "            if free:\n                s = free[-1]\n            else:\n                cands"),
+    ("hit keeps the old stamp", "                self.stamp[s] = step\n                if self.fetched[s]:",
+     "                if self.fetched[s]:"),
+    ("prefetch may displace this step's experts", "if self.stamp[s] < step and self.expert_of[s] not in want]",
+     "if self.expert_of[s] not in want]"),
+    ("prefetch displaces predicted experts", "if self.stamp[s] < step and self.expert_of[s] not in want]",
+     "if self.stamp[s] < step]"),
+    ("prefetch stamps like a use", "self.stamp[s] = step - 1", "self.stamp[s] = step"),
+    ("prefetch refreshes resident experts", "            if e in self.slot_of:\n                continue",
+     "            if e in self.slot_of:\n                self.stamp[self.slot_of[e]] = step\n                continue"),
+    ("used predictions not counted", "self.prefetch_used += 1", "pass"),
     ("ids visited in the given order", "for e in sorted(ids):", "for e in ids:"),
     ("may evict the token's own experts", "if self.expert_of[s] not in current]", "]"),
     ("resize keeps the oldest", "key=lambda q: (-self.stamp[q], q)", "key=lambda q: (self.stamp[q], q)"),
