@@ -459,6 +459,14 @@ def run_gpu(args, ws, rank, local):
     chunk = max([c for c in range(1, T + 1) if (c * (H + 32) + c * k * (cfg.I + 32)) * 2 <= 120 * 1024] or [1])
     n_chunks = -(-T // chunk)  # launches per layer on the fused path
     layout = Q.FT_LAYOUT_DECODE_TILES if fused else Q.FT_LAYOUT_ROWS
+    mx = args.weights == "mxfp4"
+    if mx:
+        if not fused:
+            raise SystemExit("MXFP4 weights run on the fused decode step only")
+        layout = Q.FT_LAYOUT_MXFP4_DECODE_TILES
+    # bytes of one expert's three matrices: NVFP4 0.5 B per code + 1 B per 16 + three fp32 tensor scales,
+    # MXFP4 0.5 B per code + 1 B per 32
+    expert_bytes = 3 * H * cfg.I * 17 // 32 if mx else cfg.expert_bytes + 12
 
     # ---- weights (device generator + device quantiser), all experts resident
     weights = []
@@ -539,10 +547,10 @@ def run_gpu(args, ws, rank, local):
     # the gap to the next launch is included
     unique = [len(set(np.argsort(-lg_host[i % S][l], axis=1, kind="stable")[:, :k].ravel().tolist()))
               for i in range(min(args.steps, S)) for l in range(L)]
-    # algorithmic bytes of one layer launch: the selected experts' NVFP4 weights (three matrices at
-    # 0.5625 B/param plus three fp32 tensor scales) plus logits, activations and output
+    # algorithmic bytes of one layer launch: the selected experts' weights (three matrices at 0.5625 B/param
+    # plus three fp32 tensor scales for NVFP4, 0.53125 B/param for MXFP4) plus logits, activations and output
     # (with several token chunks per layer, the layer's bytes and time are shared evenly by its launches)
-    bytes_per_launch = (float(np.mean(unique)) * (cfg.expert_bytes + 12) + T * (E * 4 + H * 2 * 2)) / (
+    bytes_per_launch = (float(np.mean(unique)) * expert_bytes + T * (E * 4 + H * 2 * 2)) / (
         n_chunks if fused else 1)
     avg_launch_s = (ms / 1e3) / (args.steps * L * (n_chunks if fused else 1))
     peak, peak_kind = load_peaks()
@@ -579,15 +587,17 @@ def run_gpu(args, ws, rank, local):
                "h2d_bytes_per_step": L * T * (H * 2 + E * 4), "d2h_bytes_per_step": L * T * H * 2}
 
     src_hash = kernel_source_hash()
+    wfmt = "MXFP4 (E2M1 + UE8M0/32)" if mx else "NVFP4 (E2M1 + E4M3/16 + fp32 tensor scale)"
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4 weights x bf16 activations, fp32 accumulate", "data": "synthetic (seeded Philox4x32-10)",
+        "dtype": f"{args.weights} weights x bf16 activations, fp32 accumulate",
+        "data": "synthetic (seeded Philox4x32-10)",
         "config": {"workload": f"{cfg.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, intermediate {cfg.I}, "
-                               f"batch {T}, NVFP4 (E2M1 + E4M3/16 + fp32 tensor scale), all experts resident",
+                               f"batch {T}, {wfmt}, all experts resident",
                    "global_batch": T * ws, "distinct_steps": S,
                    "l2": "inputs larger than L2: each step streams ~%.0f MB of expert weights" %
-                         (L * float(np.mean(unique)) * cfg.expert_bytes / 1e6),
+                         (L * float(np.mean(unique)) * expert_bytes / 1e6),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "nominal_peak": HBM_NOMINAL_GBS,
@@ -598,7 +608,8 @@ def run_gpu(args, ws, rank, local):
                                 if fused else
                                 "route + permute + k_decode_gateup + k_decode_down + combine per layer, timed together"),
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_launch_s * 1e6,
-                     "traffic": profiled_traffic(cfg.name, src_hash) if fused else None, "source_hash": src_hash},
+                     "traffic": profiled_traffic(cfg.name + ("_mxfp4" if mx else ""), src_hash) if fused else None,
+                     "source_hash": src_hash},
         "e2e": e2e,
         "gpu_launches": L * args.steps * launches_per_layer,
         "clocks": clk.report(),
@@ -944,7 +955,8 @@ def run_gpu_cache(args, ws, rank, local):
     copy_stream = torch.cuda.Stream(device=dev)
     stream = torch.cuda.Stream(device=dev)
     P = args.prefetch
-    layers = [CachedDecodeLayer(pool, l, k, T, copy_stream=copy_stream, prefetch=P) for l in range(L)]
+    layers = [CachedDecodeLayer(pool, l, k, T, copy_stream=copy_stream,
+                                prefetch=P if args.prefetch_source == "router" else 0) for l in range(L)]
     # pinned host -> device copy bandwidth on this machine (the bound of the misses)
     probe_h = torch.empty(512 << 20, dtype=torch.uint8, pin_memory=True)
     probe_d = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -959,9 +971,15 @@ def run_gpu_cache(args, ws, rank, local):
     h2d_gbs = 4 * (512 << 20) / (p0.elapsed_time(p1) / 1e3) / 1e9
     del probe_h, probe_d
 
+    # predictions: the router's next P ranks (the mechanism), or the next token's own experts (an exact
+    # predictor: the bound on what prefetching can save on this stream)
+    exact = args.prefetch_source == "next"
+    nxt = [W.cache_stream_sets(cfg, l, rank_off + n_steps + 1)[rank_off:] for l in range(L)] if exact else None
+
     def token(s):
         for l in range(L):
-            layers[l](lg_dev[l, s][None, :], x_dev[s % NX, l], out, rank_off + s, stream=stream)
+            layers[l](lg_dev[l, s][None, :], x_dev[s % NX, l], out, rank_off + s, stream=stream,
+                      predicted=nxt[l][s + 1] if exact else None)
 
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
@@ -1023,18 +1041,20 @@ def run_gpu_cache(args, ws, rank, local):
         "config": {"workload": f"{cfg.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, intermediate {I}, "
                                f"batch {T}, VRAM LRU cache of {cfg.slots} slots per layer over a "
                                f"{L * E * pool.slot_stride / 1e9:.1f} GB pinned host pool"
-                               + (f", router-driven prefetch of the next {P} ranks" if P else ""),
+                               + (f", router-driven prefetch of the next {P} ranks" if P and not exact else "")
+                               + (", prefetch of the next token's experts (exact predictor)" if exact else ""),
                    "global_batch": T * ws, "l2": "inputs larger than L2: misses come from host memory",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "cache": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                   "h2d_bytes_per_token": miss_bytes_tok, "h2d_gbs_achieved": filled / (ms / 1e3) / 1e9,
                   "h2d_gbs_measured_peak": h2d_gbs,
-                  "prefetch": {"next_ranks": P, "prefetched": prefetched, "used": used,
+                  "prefetch": {"next_ranks": P, "source": args.prefetch_source, "prefetched": prefetched, "used": used,
                                "accuracy": used / prefetched if prefetched else None,
                                "demand_misses_per_token": misses / args.steps,
-                               "what": "the router's next P ranks of each token installed for the next token and "
-                                       "copied behind its misses on the copy stream; accuracy = installed experts a "
-                                       "later lookup found / installed"},
+                               "what": "predicted experts (source router: the router's next P ranks of each token; "
+                                       "source next: the next token's own experts, an exact predictor) installed "
+                                       "for the next token and copied behind its misses on the copy stream; "
+                                       "accuracy = installed experts a later lookup found / installed"},
                   "resize": dict(resize, what="ft_expert_cache_resize after the timed stream (device-to-device "
                                               "moves + the publish of every layer's table), CUDA events on the "
                                               "stream; not part of the tok/s")},
@@ -1057,6 +1077,10 @@ def main():
     ap.add_argument("--config", default="decode_35b")
     ap.add_argument("--distinct-steps", type=int, default=256)
     ap.add_argument("--layers", type=int, default=0, help="(debug) fewer layers; the result is then not the workload")
+    ap.add_argument("--prefetch-source", default="router", choices=["router", "next"],
+                    help="cache stream: predictions from the router's ranks, or the next token's experts (exact)")
+    ap.add_argument("--weights", default="nvfp4", choices=["nvfp4", "mxfp4"],
+                    help="decode configs: expert weight format of the fused layer step")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="cache stream: install the router's next P ranked experts of each token for the next one")
     ap.add_argument("--no-e2e", action="store_true")

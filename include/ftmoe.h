@@ -110,6 +110,8 @@ FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
 #define FT_LAYOUT_ROWS 0         /* row-major codes [N][K/2] + row-major scales [N][K/16] */
 #define FT_LAYOUT_DECODE_TILES 1 /* 16-row tiles for the decode kernels, see ft_nvfp4_pack_tiles() */
 #define FT_LAYOUT_UMMA_TILES 2   /* 128x128 blocks for the tensor-core prefill, see ft_nvfp4_pack_umma() */
+#define FT_LAYOUT_MXFP4_ROWS 3   /* MXFP4: row-major codes [N][K/2] + row-major UE8M0 scales [N][K/32] */
+#define FT_LAYOUT_MXFP4_DECODE_TILES 4 /* MXFP4 16-row tiles for the fused decode, see ft_mxfp4_pack_tiles() */
 
 /* Expert weights of one layer in device memory.  For weight index w (the
  * expert id, or its cache slot when expert_to_slot is given):
@@ -128,8 +130,14 @@ FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
  *   gate/up  gu_codes + w*gu_codes_stride : the [2I][H] matrix above packed by
  *            ft_nvfp4_pack_tiles() (2I*H*9/16 bytes)
  *   down     d_codes  + w*d_codes_stride  : the [H][I] matrix packed likewise
- *  both layouts
+ *  layout FT_LAYOUT_MXFP4_ROWS: as FT_LAYOUT_ROWS with UE8M0 scales, one per 32
+ *            elements: gu_scales [2I][H/32], d_scales [H][I/32]; no tensor scale
+ *  layout FT_LAYOUT_MXFP4_DECODE_TILES (codes and scales together): the same
+ *            matrices packed by ft_mxfp4_pack_tiles() (2I*H*17/32 and H*I*17/32
+ *            bytes); no tensor scale
+ *  NVFP4 layouts
  *   tensor scales  tscale + w*tscale_stride : float {gate, up, down}
+ *   (MXFP4 layouts have none: tscale may be NULL and is not read)
  *   gu_sf_tiled / d_sf_tiled (optional, prefill only): scales rearranged for the
  *            block-scaled tensor cores, strides gu_sf_tiled_stride / d_sf_tiled_stride.
  * Strides are in bytes (tscale_stride in floats).  Every base address and
@@ -257,11 +265,17 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
                                          const int32_t* inv, const float* w, float* y, uint16_t* out, void* ws,
                                          size_t ws_bytes, ft_stream_t stream);
 
-/* Fused decode layer step for up to 16 tokens, weights in FT_LAYOUT_DECODE_TILES:
+/* Fused decode layer step for up to 16 tokens, weights in FT_LAYOUT_DECODE_TILES
+ * (NVFP4) or FT_LAYOUT_MXFP4_DECODE_TILES (MXFP4):
  * router top-k (same selection and weights as ft_moe_route), grouping by
- * expert (same order as ft_moe_permute), the NVFP4 SwiGLU expert FFN and the
- * weighted combine, in one launch of one CTA per SM.
- * [P4 MoE core mechanism; P3 §2.1; P5 NVFP4]
+ * expert (same order as ft_moe_permute), the SwiGLU expert FFN on the 4-bit
+ * weights and the weighted combine, in one launch of one CTA per SM.
+ * [P4 MoE core mechanism; P3 §2.1; P5 NVFP4, and MXFP4 in its limits]
+ * MXFP4: per 128-element K-block, each 16-row tile row takes the largest of
+ * its four block exponents r; the codes are scaled by 2^(x - r) in f16 before
+ * the tensor-core product and the fp32 partial by 2^r after it -- exact unless
+ * a block is more than 2^22 below the largest of its row's K-block, whose bits
+ * below f16's subnormal range are then lost.
  *   logits (device) fp32 [T][E]; x (device) bf16 [T][H], 16-byte aligned.
  *   out    (device) bf16 [T][H]: out[t] = bf16(sum_j w[t][j] * y_{t,j}), the
  *          sum over a token's experts taken in slot order j, fp32.
@@ -496,6 +510,30 @@ FT_API ft_status ft_nvfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, con
  * 128.  All pointers (device). */
 FT_API ft_status ft_nvfp4_pack_umma(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
                                     int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
+
+/* MXFP4 weight quantiser [P5 limits: MXFP4 among the weight formats; the OCP
+ * Microscaling v1.0 format]: fp32 w [N][K] (device, row-major, 16-byte
+ * aligned) -> E2M1 codes [N][K/2] (element 2j in the low nibble of byte j; row
+ * stride codes_ld, a multiple of 16, >= K/2) and UE8M0 scales [N][K/32] (row
+ * stride scales_ld >= K/32).  Per 32-element block: X = floor(log2(amax)) - 2
+ * clamped to [-127, 127] (-127 for an all-zero block), scale byte X + 127,
+ * code = E2M1 round-to-nearest-even of v / 2^X saturating at 6, -0 stored as
+ * +0.  NaN or inf inputs set FT_DEVERR_BAD_SCALE.  K a multiple of 32.  No
+ * workspace; asynchronous on `stream`. */
+FT_API ft_status ft_mxfp4_quantize_weight(const float* w, int64_t N, int64_t K, uint8_t* codes, int64_t codes_ld,
+                                          uint8_t* scales, int64_t scales_ld, ft_stream_t stream);
+
+/* Packs a row-major MXFP4 matrix [N][K] (codes [N][K/2] at byte stride
+ * codes_ld, scales [N][K/32] at stride scales_ld) into
+ * FT_LAYOUT_MXFP4_DECODE_TILES: N/16 tiles of 16*K*17/32 bytes.  Within a
+ * tile, per 128-element K-block kb: the 1024 code bytes exactly as
+ * ft_nvfp4_pack_tiles() places them; then, after all code blocks, 64 scale
+ * bytes per K-block: the scale of block 4kb+q of row 8h+g at
+ * (K/128)*1024 + kb*64 + (g*4+q)*2 + h.  Warp lane L = 4g+q thus holds the
+ * codes of exactly one block of rows g and g+8 and reads their two scale bytes
+ * at L*2.  N a multiple of 16, K a multiple of 128.  All pointers (device). */
+FT_API ft_status ft_mxfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
+                                     int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
 
 /* Synthetic weights: out[j] = (float)(sigma * Z_{first+j}) where Z is the
  * Box-Muller normal of Philox4x32-10 block (first+j)/2 with counter

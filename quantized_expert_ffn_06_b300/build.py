@@ -15,7 +15,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libftmoe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "route_permute.cu", "quant.cu", "decode.cu", "decode_fused.cu", "expert_cache.cu", "prefill.cu", "weights.cu"]
+SOURCES = ["api.cu", "route_permute.cu", "quant.cu", "decode.cu", "decode_fused.cu", "expert_cache.cu", "prefill.cu", "weights.cu", "mx.cu"]
 HOST_SOURCES = []
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

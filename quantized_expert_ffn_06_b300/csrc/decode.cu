@@ -245,8 +245,9 @@ ft_status validate_weights(const ft_moe_layer_weights* W, const char* fn) {
     if (!W) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights descriptor is null");
     if (W->E <= 0 || W->E > 1024 || W->H <= 0 || W->H % 256 || W->I <= 0 || W->I % 128 || W->n_weights <= 0)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 1 <= E <= 1024, H a multiple of 256, I a multiple of 128");
-    const bool rows = W->layout == FT_LAYOUT_ROWS;
-    if (!W->gu_codes || !W->d_codes || !W->tscale || (rows && (!W->gu_scales || !W->d_scales)))
+    const bool rows = W->layout == FT_LAYOUT_ROWS || W->layout == FT_LAYOUT_MXFP4_ROWS;
+    const bool mx = W->layout == FT_LAYOUT_MXFP4_ROWS || W->layout == FT_LAYOUT_MXFP4_DECODE_TILES;  // no tensor scale
+    if (!W->gu_codes || !W->d_codes || (!mx && !W->tscale) || (rows && (!W->gu_scales || !W->d_scales)))
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null weight pointer");
     if (!W->expert_to_slot && W->n_weights < W->E)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": n_weights < E without a slot table");
@@ -255,7 +256,7 @@ ft_status validate_weights(const ft_moe_layer_weights* W, const char* fn) {
         if (p && !aligned(p, 16)) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weight pointers need 16-byte alignment");
     if (W->gu_codes_stride % 16 || W->gu_scales_stride % 16 || W->d_codes_stride % 16 || W->d_scales_stride % 16)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weight strides need to be multiples of 16 bytes");
-    if (W->tscale_stride < 3) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": tscale_stride < 3");
+    if (!mx && W->tscale_stride < 3) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": tscale_stride < 3");
     return FT_OK;
 }
 

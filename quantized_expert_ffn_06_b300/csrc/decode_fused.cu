@@ -113,6 +113,9 @@ struct DecodePlan {
     unsigned long long wait_ns;  // bound on any single wait
     int wait_site;               // FT_WAIT_SITE_DECODE_H: the h hand-off waits for an epoch nobody writes
     int logits_bulk;             // the logits come in by one bulk copy (16-byte aligned, size a multiple of 16)
+    int solo;                    // one routed token of at most 256 logits: one warp routes it, and the work split
+                                 // (U = k distinct experts) is made before the inputs arrive
+    int mx;                      // MXFP4 weights (FT_LAYOUT_MXFP4_DECODE_TILES): 1088-byte K-blocks, no tensor scale
 };
 
 struct DecodeArgs {
@@ -310,6 +313,47 @@ __device__ __noinline__ float4 kblock_partial(const uint8_t* item, const __half*
     return make_float4(d[0] + e[0], d[1] + e[1], d[2] + e[2], d[3] + e[3]);
 }
 
+// 2^d (d <= 0) as f16 in both halves: exact down to 2^-24 (subnormals), 0 below.
+__device__ __forceinline__ uint32_t pow2_f16x2(int d) {
+    const uint32_t b = (d >= -14) ? (uint32_t)(d + 15) << 10 : (d >= -24) ? 1u << (d + 24) : 0u;
+    return b | (b << 16);
+}
+// The power of two a UE8M0 byte stands for, 2^(s - 127), as an fp32 (s = 0: the subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t s) {
+    return s ? __uint_as_float(s << 23) : __uint_as_float(1u << 22);
+}
+
+// The MXFP4 form of kblock_partial: item = 1024 code bytes as above, then the
+// UE8M0 scale bytes of rows g and g+8 for lane L = 4g + q at 1024 + 2L (lane
+// L's 32 elements of a row are exactly one MX block).  Row g's reference
+// exponent r is the largest of its four blocks (lanes 4g .. 4g+3); the codes
+// are scaled by 2^(x - r) in f16 (exact unless x - r < -22), the fp32 partial
+// by 2^(r - 127).
+__device__ __noinline__ float4 kblock_partial_mx(const uint8_t* item, const __half* x) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t sp = *reinterpret_cast<const uint16_t*>(item + 1024 + lane * 2);
+    const uint32_t own = (sp & 0xFFu) | ((sp >> 8) << 16);  // {row g, row g+8} as 16-bit halves
+    uint32_t ref = __vmaxu2(own, __shfl_xor_sync(0xffffffffu, own, 1));
+    ref = __vmaxu2(ref, __shfl_xor_sync(0xffffffffu, ref, 2));
+    const int rg = (int)(ref & 0xFFFFu), rh = (int)(ref >> 16);
+    const uint32_t sa = pow2_f16x2((int)(own & 0xFFFFu) - rg), sb = pow2_f16x2((int)(own >> 16) - rh);
+    const uint32_t* c0 = reinterpret_cast<const uint32_t*>(item + lane * 16);
+    const uint32_t* c1 = reinterpret_cast<const uint32_t*>(item + 512 + lane * 16);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int s2 = 0; s2 < 4; ++s2) {
+        uint32_t f0[4], f1[4];
+        e2m1x8_to_f16x2x4(c0[s2], f0);
+        e2m1x8_to_f16x2x4(c1[s2], f1);
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + 32 * s2);
+        mma16816(d, hmul2(f0[0], sa), hmul2(f1[0], sb), hmul2(f0[1], sa), hmul2(f1[1], sb), xv.x, xv.y);
+        mma16816(e, hmul2(f0[2], sa), hmul2(f1[2], sb), hmul2(f0[3], sa), hmul2(f1[3], sb), xv.z, xv.w);
+    }
+    const float fg = ue8m0_to_f32((uint32_t)rg), fh = ue8m0_to_f32((uint32_t)rh);
+    return make_float4((d[0] + e[0]) * fg, (d[1] + e[1]) * fg, (d[2] + e[2]) * fh, (d[3] + e[3]) * fh);
+}
+
 // ---------------------------------------------------------------------------- kernel
 
 template <int R>
@@ -347,6 +391,67 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const bool route_mode = a.logits != nullptr;
     uint8_t* ring = dsm + P.off_ring + warp * (R * dk::ITEM);
 
+    // ---------------- work split over U selected experts: CTA c takes phase-1 tiles [p1_beg, p1_end) and
+    // output tiles [o_beg, o_end); its warps split the K-blocks of each phase.  With one routed token U = k
+    // is known before the inputs arrive, and the split is made there.
+    const int tiles_gu = I >> 3;  // 16-row tiles of an expert's [2I][H] gate/up matrix
+    const int KB1 = H >> 7, KB2 = I >> 7;
+    const int n2 = H >> 4;
+    const int o_beg = fdiv(n2 * c, P.dv_g), o_end = fdiv(n2 * (c + 1), P.dv_g);
+    const int n_ot = o_end - o_beg;
+    int U = 0, n1 = 0, p1_beg = 0, p1_end = 0, n_t1 = 0, nr2 = 0, ni1 = 0, ni2 = 0;
+    int ib1 = 0, ie1 = 0, ib2 = 0, ie2 = 0, cnt1 = 0, cnt = 0;
+    bool split1 = false, split2 = false;
+    float inv_u = 1.0f;
+    // r / U for 0 <= r < 2^20: float estimate, corrected by one step
+    auto div_u = [&](int r) {
+        int q = (int)((float)r * inv_u);
+        const int rem = r - q * U;
+        q += (rem >= U) - (rem < 0);
+        return q;
+    };
+    auto work_split = [&](int u_count) {
+        U = u_count;
+        n1 = U * tiles_gu;
+        inv_u = __fdividef(1.0f, (float)max(U, 1));
+        // phase-1 share balanced by bytes against the phase-2 share: CTA c's boundary is
+        // proportional to c * tgt - (bytes of the down tiles of CTAs < c), in units of 9 bytes.
+        // Float rounding can move a boundary by a tile; both neighbours compute a boundary from
+        // the same expression, so the tiles still partition (at worst a tile is done twice).
+        const float b1 = (float)H, b2 = (float)I * (float)U;
+        float tgt = __fdividef((float)n1 * b1 + (float)n2 * b2, (float)G);
+        tgt = fmaxf(tgt, (float)P.max_ot * b2);
+        const float scale = __fdividef((float)n1, (float)G * tgt - (float)n2 * b2);
+        p1_beg = c == 0 ? 0 : min(n1, __float2int_rn(((float)c * tgt - (float)o_beg * b2) * scale));
+        p1_end = c == G - 1 ? n1 : min(n1, __float2int_rn(((float)(c + 1) * tgt - (float)o_end * b2) * scale));
+        p1_end = max(p1_end, p1_beg);
+        n_t1 = p1_end - p1_beg;
+        nr2 = n_ot * U;  // phase-2 runs (output tile, expert), run r = otl * U + u
+        // this warp's K-block ranges: split evenly (runs shared by neighbouring warps), or whole runs
+        // per warp when a phase has more runs than warps
+        split1 = n_t1 <= dk::NW;
+        split2 = nr2 <= dk::NW;
+        ni1 = n_t1 * KB1;
+        ni2 = nr2 * KB2;
+        if (split1) {
+            ib1 = (warp * ni1) >> dk::LOG_NW;
+            ie1 = ((warp + 1) * ni1) >> dk::LOG_NW;
+        } else {
+            ib1 = ((warp * n_t1) >> dk::LOG_NW) * KB1;
+            ie1 = (((warp + 1) * n_t1) >> dk::LOG_NW) * KB1;
+        }
+        if (split2) {
+            ib2 = (warp * ni2) >> dk::LOG_NW;
+            ie2 = ((warp + 1) * ni2) >> dk::LOG_NW;
+        } else {
+            ib2 = ((warp * nr2) >> dk::LOG_NW) * KB2;
+            ie2 = (((warp + 1) * nr2) >> dk::LOG_NW) * KB2;
+        }
+        cnt1 = ie1 - ib1;
+        cnt = cnt1 + (ie2 - ib2);  // this warp's K-blocks, phase 1 then 2
+    };
+    if (P.solo) work_split(k);
+
     unsigned long long* ibar = reinterpret_cast<unsigned long long*>(misc + M_BAR);  // the inputs' bulk copies
     if (tid < M_BAR) misc[tid] = 0;
     if (tid == 0) {
@@ -355,7 +460,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     }
 #pragma unroll 1
     for (int i = tid; i < nf; i += dk::THREADS) s_hexp[i] = 0;
-    if (route_mode) {
+    if (route_mode && !P.solo) {
 #pragma unroll 1
         for (int i = tid; i < T * P.nb * P.kk; i += dk::THREADS) s_rank[i] = 0;
     }
@@ -364,6 +469,16 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     griddep_wait();
     griddep_launch_dependents();
     unsigned long long old_count = 0;
+    // this call's epoch (thread 0, which drew old_count): calls sharing a workspace each add G to its 64-bit
+    // counter; the tag runs through 1 .. 2^32-1 (never 0, the value of a zeroed word):
+    // (call mod (2^32 - 1)) + 1, with call = counter / G and 2^32 = 1 mod (2^32 - 1)
+    auto set_epoch = [&]() {
+        const unsigned long long call = __umul64hi(old_count, P.dv_g64);
+        unsigned long long f = (call >> 32) + (call & 0xFFFFFFFFull);
+        f = (f >> 32) + (f & 0xFFFFFFFFull);
+        if (f >= 0xFFFFFFFFull) f -= 0xFFFFFFFFull;
+        misc[M_EPOCH] = (int)(uint32_t)(f + 1ull);
+    };
 
     // ---------------- inputs: x (and the logits, when aligned) by one bulk copy each
     {
@@ -407,8 +522,9 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         }
         if (route_mode && !lbulk) __syncthreads();
         bool big = false;
+        const int st0 = P.solo ? 32 : 0;  // one routed token: warp 0 routes while the other warps stage x
 #pragma unroll 1
-        for (int i = tid; i < nx; i += dk::THREADS) {
+        for (int i = tid - st0; i >= 0 && i < nx; i += dk::THREADS - st0) {
             const int r = fdiv(i, P.dv_xrow), cp = i - r * (H >> 3);
             const uint4 v = *reinterpret_cast<const uint4*>(xraw + i * 8);
             const uint4 o = make_uint4(bf16x2_to_f16x2(v.x, big), bf16x2_to_f16x2(v.y, big), bf16x2_to_f16x2(v.z, big),
@@ -418,6 +534,34 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         if (big) misc[M_FLAG] = 1;
     }
 
+    if (P.solo) {
+        if (warp == 0) {
+            // one routed token: warp 0 takes its top k (one warp reduction per rank), orders the k distinct
+            // experts by id (permuted row = rank of the id among them) and writes the selected-expert list
+            bool bad = false;
+            const int e = select_topk8(lg, E, k, bad);  // lane j < k: expert of rank j
+            if (__any_sync(0xffffffffu, bad) && lane == 0) raise_dev_error(FT_DEVERR_NAN_LOGIT);
+            const int ej = (lane < k) ? e : 0x7fffffff;
+            int pos = 0;
+#pragma unroll 4
+            for (int i = 0; i < k; ++i) pos += __shfl_sync(0xffffffffu, ej, i) < ej;
+            if (lane < k) {
+                const int wi = weight_index(W, e);
+                s_ids[lane] = e;
+                s_plist[pos] = lane;
+                s_ptok[pos] = 0;
+                s_pexp[pos] = e;
+                s_ulist[pos] = e;
+                s_ubeg[pos] = pos;
+                s_uwi[pos] = wi;
+            }
+            if (lane == 0) {
+                misc[M_U] = k;
+                s_ubeg[k] = k;
+                set_epoch();
+            }
+        }
+    } else {
     // ---------------- router: top-k of every token (route mode)
     if (route_mode) {
         const int nb = P.nb, kk = P.kk, C = nb * kk;
@@ -577,80 +721,27 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         if (lane == 0) {
             misc[M_U] = run;
             s_ubeg[run] = nf;
-            // this call's epoch: calls sharing a workspace each add G to its 64-bit counter; the
-            // tag runs through 1 .. 2^32-1 (never 0, the value of a zeroed word):
-            // (call mod (2^32 - 1)) + 1, with call = counter / G and 2^32 = 1 mod (2^32 - 1)
-            const unsigned long long call = __umul64hi(old_count, P.dv_g64);
-            unsigned long long f = (call >> 32) + (call & 0xFFFFFFFFull);
-            f = (f >> 32) + (f & 0xFFFFFFFFull);
-            if (f >= 0xFFFFFFFFull) f -= 0xFFFFFFFFull;
-            misc[M_EPOCH] = (int)(uint32_t)(f + 1ull);
+            set_epoch();
         }
     }
+    }  // general routing and grouping
     __syncthreads();
     if (misc[M_FLAG]) {  // rare: x rows with values beyond the f16 range
         restage_scaled(misc + M_XEXP, xs, P.xs_stride, T, H, a.x, nullptr);
         __syncthreads();
     }
-    const int U = misc[M_U];
+    if (!P.solo) work_split(misc[M_U]);
     const unsigned int epoch = (unsigned int)misc[M_EPOCH];
 
-    // ---------------- work split
-    const int tiles_gu = I >> 3;  // 16-row tiles of an expert's [2I][H] gate/up matrix
-    const int KB1 = H >> 7, KB2 = I >> 7;
-    const int n1 = U * tiles_gu;
-    const int n2 = H >> 4;
-    const int o_beg = fdiv(n2 * c, P.dv_g), o_end = fdiv(n2 * (c + 1), P.dv_g);
-    const float inv_u = __fdividef(1.0f, (float)max(U, 1));
-    // r / U for 0 <= r < 2^20: float estimate, corrected by one step
-    auto div_u = [&](int r) {
-        int q = (int)((float)r * inv_u);
-        const int rem = r - q * U;
-        q += (rem >= U) - (rem < 0);
-        return q;
-    };
-    int p1_beg, p1_end;
-    {
-        // phase-1 share balanced by bytes against the phase-2 share: CTA c's boundary is
-        // proportional to c * tgt - (bytes of the down tiles of CTAs < c), in units of 9 bytes.
-        // Float rounding can move a boundary by a tile; both neighbours compute a boundary from
-        // the same expression, so the tiles still partition (at worst a tile is done twice).
-        const float b1 = (float)H, b2 = (float)I * (float)U;
-        float tgt = __fdividef((float)n1 * b1 + (float)n2 * b2, (float)G);
-        tgt = fmaxf(tgt, (float)P.max_ot * b2);
-        const float scale = __fdividef((float)n1, (float)G * tgt - (float)n2 * b2);
-        p1_beg = c == 0 ? 0 : min(n1, __float2int_rn(((float)c * tgt - (float)o_beg * b2) * scale));
-        p1_end = c == G - 1 ? n1 : min(n1, __float2int_rn(((float)(c + 1) * tgt - (float)o_end * b2) * scale));
-        p1_end = max(p1_end, p1_beg);
-    }
-    const int n_t1 = p1_end - p1_beg;
-    const int n_ot = o_end - o_beg;
-    const int nr2 = n_ot * U;  // phase-2 runs (output tile, expert), run r = otl * U + u
-    // this warp's K-block ranges: split evenly (runs shared by neighbouring warps), or whole runs
-    // per warp when a phase has more runs than warps
-    const bool split1 = n_t1 <= dk::NW, split2 = nr2 <= dk::NW;
-    const int ni1 = n_t1 * KB1, ni2 = nr2 * KB2;
-    int ib1, ie1, ib2, ie2;
-    if (split1) {
-        ib1 = (warp * ni1) >> dk::LOG_NW;
-        ie1 = ((warp + 1) * ni1) >> dk::LOG_NW;
-    } else {
-        ib1 = ((warp * n_t1) >> dk::LOG_NW) * KB1;
-        ie1 = (((warp + 1) * n_t1) >> dk::LOG_NW) * KB1;
-    }
-    if (split2) {
-        ib2 = (warp * ni2) >> dk::LOG_NW;
-        ie2 = ((warp + 1) * ni2) >> dk::LOG_NW;
-    } else {
-        ib2 = ((warp * nr2) >> dk::LOG_NW) * KB2;
-        ie2 = (((warp + 1) * nr2) >> dk::LOG_NW) * KB2;
-    }
-    const int cnt1 = ie1 - ib1, cnt = cnt1 + (ie2 - ib2);  // this warp's K-blocks, phase 1 then 2
 
     // ---------------- weight stream: per-lane async copies into this warp's ring.  The issue
     // cursor walks this warp's K-blocks: within a run (a tile, or an (output tile, expert) pair)
     // consecutive K-blocks are 1024 code bytes and 128 scale bytes apart.
     int is_n = 0, is_left = 0, is_ph = 1, is_run = 0, is_kb0 = 0;
+    // bytes of a 16-row tile (gate/up, down) and of a K-block's scales: NVFP4 1152-byte K-blocks (128
+    // scale bytes), MXFP4 1088-byte ones (64)
+    const int tile_b1 = P.mx ? (17 * H) >> 1 : 9 * H, tile_b2 = P.mx ? (17 * I) >> 1 : 9 * I;
+    const int sc_kb = P.mx ? 64 : 128;
     const uint8_t* is_cb = nullptr;  // codes of the next K-block (nullptr: expert without weights)
     const uint8_t* is_sb = nullptr;  // its scales
     // first K-block `kb` of run `run` of phase `ph` (run: local tile, or local (output tile, expert))
@@ -665,15 +756,15 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             const int u = fdiv(t, P.dv_tgu);
             wi = s_uwi[u];
             KB = KB1;
-            base = W.gu_codes + (int64_t)max(wi, 0) * W.gu_codes_stride + (int64_t)(t - u * tiles_gu) * (9 * H);
+            base = W.gu_codes + (int64_t)max(wi, 0) * W.gu_codes_stride + (int64_t)(t - u * tiles_gu) * tile_b1;
         } else {
             const int otl = div_u(run), u = run - otl * U;
             wi = s_uwi[u];
             KB = KB2;
-            base = W.d_codes + (int64_t)max(wi, 0) * W.d_codes_stride + (int64_t)(o_beg + otl) * (9 * I);
+            base = W.d_codes + (int64_t)max(wi, 0) * W.d_codes_stride + (int64_t)(o_beg + otl) * tile_b2;
         }
         is_cb = (wi >= 0) ? base + kb * 1024 : nullptr;
-        is_sb = base + KB * 1024 + kb * 128;
+        is_sb = base + KB * 1024 + kb * sc_kb;
     };
     auto issue = [&]() {
         if (is_n < cnt) {
@@ -684,17 +775,18 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 open_run(is_ph, is_run + 1, 0, is_ph == 1 ? KB1 : KB2);
             }
             uint8_t* slot = ring + (is_n & (R - 1)) * dk::ITEM;
+            const bool sc = lane * 4 < sc_kb;  // lanes holding a scale word of this K-block
             if (is_cb) {
                 cp16(slot + lane * 16, is_cb + lane * 16);
                 cp16(slot + 512 + lane * 16, is_cb + 512 + lane * 16);
-                cp4(slot + 1024 + lane * 4, is_sb + lane * 4);
+                if (sc) cp4(slot + 1024 + lane * 4, is_sb + lane * 4);
             } else {  // no weights behind this expert: zeros
                 *reinterpret_cast<uint4*>(slot + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(slot + 512 + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint32_t*>(slot + 1024 + lane * 4) = 0u;
+                if (sc) *reinterpret_cast<uint32_t*>(slot + 1024 + lane * 4) = 0u;
             }
             if (is_cb) is_cb += 1024;
-            is_sb += 128;
+            is_sb += sc_kb;
             --is_left;
             ++is_n;
             cp_commit();  // one group per K-block: the waits count groups
@@ -736,10 +828,10 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
 #pragma unroll 1
     for (int u = tid; u < U; u += dk::THREADS) {
         const int wi = s_uwi[u];
-        const float* ts = W.tscale + (int64_t)(wi >= 0 ? wi : 0) * W.tscale_stride;
-        s_ts[4 * u + 0] = (wi >= 0) ? __ldg(ts + 0) : 0.0f;
-        s_ts[4 * u + 1] = (wi >= 0) ? __ldg(ts + 1) : 0.0f;
-        s_ts[4 * u + 2] = (wi >= 0) ? __ldg(ts + 2) : 0.0f;
+        const float* ts = P.mx ? nullptr : W.tscale + (int64_t)(wi >= 0 ? wi : 0) * W.tscale_stride;
+        s_ts[4 * u + 0] = (wi >= 0) ? (P.mx ? 1.0f : __ldg(ts + 0)) : 0.0f;
+        s_ts[4 * u + 1] = (wi >= 0) ? (P.mx ? 1.0f : __ldg(ts + 1)) : 0.0f;
+        s_ts[4 * u + 2] = (wi >= 0) ? (P.mx ? 1.0f : __ldg(ts + 2)) : 0.0f;
     }
 
     const int g8 = lane >> 2, q4 = lane & 3;
@@ -763,7 +855,8 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     auto tscale = [&](int u, int j, bool shared) {
         if (shared) return s_ts[4 * u + j];
         const int wi = s_uwi[u];
-        return (wi >= 0) ? __ldg(W.tscale + (int64_t)wi * W.tscale_stride + j) : 0.0f;
+        if (wi < 0) return 0.0f;
+        return P.mx ? 1.0f : __ldg(W.tscale + (int64_t)wi * W.tscale_stride + j);
     };
     // is warp w without K-blocks in a split phase of ni K-blocks?
     auto empty_warp = [&](int w, int ni) { return ni && ((w * ni) >> dk::LOG_NW) == (((w + 1) * ni) >> dk::LOG_NW); };
@@ -859,10 +952,11 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             for (int kb = kb0; kb < kb1; ++kb, ++n) {
                 cp_wait_upto(is_n - n - 1);  // K-block n of this lane has landed
                 const uint8_t* slot = ring + (n & (R - 1)) * dk::ITEM;
-                const float4 v = kblock_partial(slot, r0 + kb * 128);
+                const float4 v = P.mx ? kblock_partial_mx(slot, r0 + kb * 128) : kblock_partial(slot, r0 + kb * 128);
                 acc0.x += v.x, acc0.y += v.y, acc0.z += v.z, acc0.w += v.w;
                 if (tu > 8) {
-                    const float4 v1 = kblock_partial(slot, r1 + kb * 128);
+                    const float4 v1 =
+                        P.mx ? kblock_partial_mx(slot, r1 + kb * 128) : kblock_partial(slot, r1 + kb * 128);
                     acc1.x += v1.x, acc1.y += v1.y, acc1.z += v1.z, acc1.w += v1.w;
                 }
                 issue();  // into the slot just read (this lane's own bytes)
@@ -1110,6 +1204,8 @@ static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mod
     p.wait_ns = g_wait_ns.load();
     p.wait_site = g_wait_site.load();
     p.logits_bulk = 0;
+    p.solo = (route_mode && T == 1 && E <= 256) ? 1 : 0;
+    p.mx = 0;
     return true;
 }
 
@@ -1145,6 +1241,7 @@ static ft_status launch_decode(DecodeArgs a, ft_stream_t stream, const char* fn)
     if (!plan_decode(a.T, a.k, W.E, W.H, W.I, G, a.logits != nullptr, a.P, why))
         return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
     a.P.logits_bulk = a.logits && aligned(a.logits, 16) && ((size_t)a.T * W.E * 4) % 16 == 0;
+    a.P.mx = W.layout == FT_LAYOUT_MXFP4_DECODE_TILES;
     ft_status st = decode_attributes(fn);
     if (st != FT_OK) return st;
     cudaLaunchConfig_t cfg = {};
@@ -1204,8 +1301,9 @@ static ft_status check_layer_decode_args(const ft_moe_layer_weights* W, const fl
                                          int k, uint16_t* out, int32_t* ids, float* w, const char* fn) {
     ft_status st = validate_weights(W, fn);
     if (st != FT_OK) return st;
-    if (W->layout != FT_LAYOUT_DECODE_TILES)
-        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights must use FT_LAYOUT_DECODE_TILES");
+    if (W->layout != FT_LAYOUT_DECODE_TILES && W->layout != FT_LAYOUT_MXFP4_DECODE_TILES)
+        return fail(FT_ERR_INVALID_ARG,
+                    std::string(fn) + ": weights must use FT_LAYOUT_DECODE_TILES or FT_LAYOUT_MXFP4_DECODE_TILES");
     if (T < 0 || T > dk::MAXT || k <= 0 || k > W->E || k > dk::MAXK)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 0 <= T <= 16 and 1 <= k <= min(E, 32)");
     if (T == 0) return FT_OK;

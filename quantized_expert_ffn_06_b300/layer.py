@@ -9,7 +9,8 @@ import time
 
 import torch
 
-from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_ROWS, FT_LAYOUT_UMMA_TILES, ft_gen_normal_f32,
+from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_MXFP4_DECODE_TILES, FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_ROWS,
+               FT_LAYOUT_UMMA_TILES, ft_gen_normal_f32, ft_mxfp4_pack_tiles, ft_mxfp4_quantize_weight,
                ft_moe_decode_workspace_size, ft_moe_expert_ffn_nvfp4_decode, ft_moe_expert_ffn_nvfp4_prefill,
                ft_moe_layer_decode, ft_moe_layer_decode_workspace_size, ft_moe_layer_weights, ft_moe_permute,
                ft_moe_permute_workspace_size, ft_moe_prefill_workspace_size, ft_moe_route, ft_nvfp4_pack_tiles,
@@ -36,6 +37,9 @@ class LayerWeights:
     layout TILES:  gu_codes [n, 2I*H*9/16], d_codes [n, H*I*9/16] (16-row tiles, see ft_nvfp4_pack_tiles)
     layout UMMA:   the same sizes in 128x128 blocks for the tensor-core prefill (see ft_nvfp4_pack_umma)
     tscale [n, 4] fp32 (gate, up, down, pad)
+    MXFP4 layouts (UE8M0 scales per 32, no tensor scale):
+    layout MXFP4_ROWS:  as ROWS with gu_scales [n, 2I, H/32], d_scales [n, H, I/32]
+    layout MXFP4_TILES: gu_codes [n, 2I*H*17/32], d_codes [n, H*I*17/32] (see ft_mxfp4_pack_tiles)
     """
 
     def __init__(self, E: int, H: int, I: int, device, n_weights: int | None = None, layout: int = FT_LAYOUT_ROWS):
@@ -44,11 +48,17 @@ class LayerWeights:
         self.layout = layout
         self.device = torch.device(device)
         u8 = torch.uint8
-        if layout == FT_LAYOUT_ROWS:
+        self.mx = layout in (FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP4_DECODE_TILES)
+        self.sblock = 32 if self.mx else 16  # elements per scale
+        if layout in (FT_LAYOUT_ROWS, FT_LAYOUT_MXFP4_ROWS):
             self.gu_codes = torch.empty((self.n, 2 * I, H // 2), dtype=u8, device=device)
-            self.gu_scales = torch.empty((self.n, 2 * I, H // 16), dtype=u8, device=device)
+            self.gu_scales = torch.empty((self.n, 2 * I, H // self.sblock), dtype=u8, device=device)
             self.d_codes = torch.empty((self.n, H, I // 2), dtype=u8, device=device)
-            self.d_scales = torch.empty((self.n, H, I // 16), dtype=u8, device=device)
+            self.d_scales = torch.empty((self.n, H, I // self.sblock), dtype=u8, device=device)
+        elif layout == FT_LAYOUT_MXFP4_DECODE_TILES:
+            self.gu_codes = torch.empty((self.n, 2 * I * H * 17 // 32), dtype=u8, device=device)
+            self.d_codes = torch.empty((self.n, H * I * 17 // 32), dtype=u8, device=device)
+            self.gu_scales = self.d_scales = None
         else:
             self.gu_codes = torch.empty((self.n, 2 * I * H * 9 // 16), dtype=u8, device=device)
             self.d_codes = torch.empty((self.n, H * I * 9 // 16), dtype=u8, device=device)
@@ -68,29 +78,41 @@ class LayerWeights:
         d.E, d.H, d.I, d.n_weights, d.layout = self.E, self.H, self.I, self.n, self.layout
         d.gu_codes, d.gu_codes_stride = self.gu_codes.data_ptr(), self.gu_codes.stride(0)
         d.d_codes, d.d_codes_stride = self.d_codes.data_ptr(), self.d_codes.stride(0)
-        if self.layout == FT_LAYOUT_ROWS:
+        if self.gu_scales is not None:
             d.gu_scales, d.gu_scales_stride = self.gu_scales.data_ptr(), self.gu_scales.stride(0)
             d.d_scales, d.d_scales_stride = self.d_scales.data_ptr(), self.d_scales.stride(0)
-        d.tscale, d.tscale_stride = self.tscale.data_ptr(), self.tscale.stride(0)
+        if not self.mx:  # MXFP4 has no tensor scale: the descriptor carries none
+            d.tscale, d.tscale_stride = self.tscale.data_ptr(), self.tscale.stride(0)
         d.expert_to_slot = None if self.expert_to_slot is None else self.expert_to_slot.data_ptr()
         return d
 
     def _rows_target(self, wi: int):
         """Row-major destination for expert wi: the weights themselves (ROWS) or a staging copy (TILES)."""
-        if self.layout == FT_LAYOUT_ROWS:
+        if self.layout in (FT_LAYOUT_ROWS, FT_LAYOUT_MXFP4_ROWS):
             return self.gu_codes[wi], self.gu_scales[wi], self.d_codes[wi], self.d_scales[wi]
         if self._tmp is None:
-            H, I, u8, dev = self.H, self.I, torch.uint8, self.device
+            H, I, u8, dev, sb = self.H, self.I, torch.uint8, self.device, self.sblock
             self._tmp = (torch.empty((2 * I, H // 2), dtype=u8, device=dev),
-                         torch.empty((2 * I, H // 16), dtype=u8, device=dev),
+                         torch.empty((2 * I, H // sb), dtype=u8, device=dev),
                          torch.empty((H, I // 2), dtype=u8, device=dev),
-                         torch.empty((H, I // 16), dtype=u8, device=dev))
+                         torch.empty((H, I // sb), dtype=u8, device=dev))
         return self._tmp
 
     def set_expert(self, wi: int, wg: torch.Tensor, wu: torch.Tensor, wd: torch.Tensor, stream=None) -> None:
         """Quantise fp32 gate [I,H], up [I,H], down [H,I] into weight index wi."""
         H, I = self.H, self.I
         guc, gus, dc, ds = self._rows_target(wi)
+        if self.mx:
+            for proj, w in ((PROJ_GATE, wg), (PROJ_UP, wu)):
+                assert tuple(w.shape) == (I, H)
+                ft_mxfp4_quantize_weight(w, guc.data_ptr() + proj * (H // 2), gus.data_ptr() + proj * (H // 32),
+                                         codes_ld=H, scales_ld=H // 16, stream=stream)
+            assert tuple(wd.shape) == (H, I)
+            ft_mxfp4_quantize_weight(wd, dc, ds, stream=stream)
+            if self.layout == FT_LAYOUT_MXFP4_DECODE_TILES:
+                ft_mxfp4_pack_tiles(guc, H // 2, gus, H // 32, 2 * I, H, self.gu_codes[wi], stream=stream)
+                ft_mxfp4_pack_tiles(dc, I // 2, ds, I // 32, H, I, self.d_codes[wi], stream=stream)
+            return
         for proj, w in ((PROJ_GATE, wg), (PROJ_UP, wu)):
             assert tuple(w.shape) == (I, H)
             ft_nvfp4_quantize_weight(w, guc.data_ptr() + proj * (H // 2), gus.data_ptr() + proj * (H // 16),
@@ -455,7 +477,10 @@ class CachedDecodeLayer:
         self.filled = torch.cuda.Event()
         self.routed = torch.cuda.Event()
 
-    def __call__(self, logits: torch.Tensor, x: torch.Tensor, out: torch.Tensor, step: int, stream=None):
+    def __call__(self, logits: torch.Tensor, x: torch.Tensor, out: torch.Tensor, step: int, stream=None,
+                 predicted=None):
+        """One token's layer step; returns the (expert, slot) misses filled for it.  `predicted` (host ints,
+        optional) replaces the router's next P ranks as the experts installed for the next token."""
         stream = torch.cuda.current_stream(self.pool.device) if stream is None else stream
         ft_moe_route(logits, self.k + self.prefetch, self.ids, self.w, stream=stream)
         with torch.cuda.stream(stream):
@@ -471,10 +496,12 @@ class CachedDecodeLayer:
         self.pool.cache.publish(self.layer, stream=stream)
         stream.wait_event(self.filled)
         self.fused(self.weights, logits, x, out, routing=False, stream=stream)
-        if self.prefetch:
+        if self.prefetch or predicted is not None:
             # the next-ranked experts, for the next token: copied behind this token's fills, which the next step's
             # kernel waits for (same copy stream), while this and later layers compute
-            predicted = sorted(set(int(e) for row in ranked for e in row[self.k:]) - set(needed))
+            if predicted is None:
+                predicted = set(int(e) for row in ranked for e in row[self.k:])
+            predicted = sorted(set(int(e) for e in predicted) - set(needed))
             self.prefetched = self.pool.cache.prefetch(self.layer, step, predicted)
             for e, s in self.prefetched:
                 self.pool.cache.fill(self.layer, e, s, stream=self.copy_stream)

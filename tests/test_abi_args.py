@@ -136,3 +136,32 @@ def test_no_alloc_decode_argument_checks_come_before_any_cuda_call():
     status(call(W=weights(E=64, I=1024), T=16, k=32), Q.FT_ERR_INVALID_ARG)
     assert b"scratch" in L.ft_last_error()
     status(call(T=0), Q.FT_OK)
+
+
+def test_mxfp4_argument_checks():
+    q = L.ft_mxfp4_quantize_weight
+    status(q(P, 16, 250, P, 128, P, 8, NULL), Q.FT_ERR_INVALID_ARG)       # K not a multiple of 32
+    status(q(NULL, 16, 256, P, 128, P, 8, NULL), Q.FT_ERR_INVALID_ARG)
+    status(q(P, 16, 256, P, 120, P, 8, NULL), Q.FT_ERR_INVALID_ARG)       # codes_ld < K/2
+    status(q(P, 16, 256, P, 136, P, 7, NULL), Q.FT_ERR_INVALID_ARG)       # scales_ld < K/32 (and ld not x16)
+    status(q(P, 16, 256, MIS, 128, P, 8, NULL), Q.FT_ERR_INVALID_ARG)     # misaligned codes
+    pk = L.ft_mxfp4_pack_tiles
+    status(pk(P, 128, P, 8, 15, 256, P, NULL), Q.FT_ERR_INVALID_ARG)     # N not a multiple of 16
+    status(pk(P, 128, P, 8, 16, 200, P, NULL), Q.FT_ERR_INVALID_ARG)     # K not a multiple of 128
+    status(pk(P, 128, P, 4, 16, 256, P, NULL), Q.FT_ERR_INVALID_ARG)     # scales_ld < K/32
+    status(pk(NULL, 128, P, 8, 16, 256, P, NULL), Q.FT_ERR_INVALID_ARG)
+
+
+def test_layer_decode_takes_mxfp4_tiles_without_tensor_scales():
+    """MXFP4 tiles are accepted with no tensor-scale pointer (T = 0: checks only, nothing launched); MXFP4 rows are
+    not a layout of the fused step, and NVFP4 tiles still need their tensor scales."""
+    W = weights(layout=Q.FT_LAYOUT_MXFP4_DECODE_TILES)
+    W.tscale, W.tscale_stride = None, 0
+    ws = L.ft_moe_layer_decode_workspace_size(4, 2, W.H, W.I)
+    status(L.ft_moe_layer_decode(ctypes.byref(W), P, P, 0, 2, P, NULL, NULL, P, ws, NULL), Q.FT_OK)
+    status(L.ft_moe_layer_decode(ctypes.byref(W), P, P, 4, 2, NULL, NULL, NULL, P, ws, NULL), Q.FT_ERR_INVALID_ARG)
+    R = weights(layout=Q.FT_LAYOUT_MXFP4_ROWS)
+    status(L.ft_moe_layer_decode(ctypes.byref(R), P, P, 0, 2, P, NULL, NULL, P, ws, NULL), Q.FT_ERR_INVALID_ARG)
+    N = weights()
+    N.tscale = None
+    status(L.ft_moe_layer_decode(ctypes.byref(N), P, P, 0, 2, P, NULL, NULL, P, ws, NULL), Q.FT_ERR_INVALID_ARG)
