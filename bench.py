@@ -1084,6 +1084,8 @@ def main():
     ap.add_argument("--prefetch", type=int, default=0,
                     help="cache stream: install the router's next P ranked experts of each token for the next one")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode_35b: skip the prefill measurement reported beside the decode line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=48)
     ap.add_argument("--stream-layers", type=int, default=0,
@@ -1166,6 +1168,16 @@ def main():
             torch.distributed.destroy_process_group()
         return
     res = run_gpu(args, ws, rank, local)
+    if args.config == "decode_35b" and not args.no_prefill:
+        # the same layer shape's 4096-token prefill (grouped FP4 tensor-core GEMMs), measured in the same run
+        # after the decode and reported beside it: its own workload, unit and roofline
+        import argparse as _ap
+        pa = _ap.Namespace(**vars(args))
+        pa.config, pa.steps, pa.warmup, pa.tokens = "prefill_35b", 20, 5, 0
+        pres = run_gpu_prefill(pa, ws, rank, local)
+        res["prefill"] = {key: pres[key] for key in ("metric", "value", "unit", "ms_per_step", "steps", "warmup",
+                                                     "dtype", "config", "roofline", "e2e", "gpu_launches", "clocks")
+                          if key in pres}
     if rank == 0:
         if not args.no_cpu_baseline:
             ref = OracleDecode(cfg)

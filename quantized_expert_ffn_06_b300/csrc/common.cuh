@@ -122,28 +122,23 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
     return (v != v) ? 1u : key;
 }
 
-// Top-k selection of one token's E logits by one warp.  Lane l holds experts
-// l*EPL .. l*EPL+EPL-1 (EPL = ceil(E/32)), so among equal keys the lowest lane,
-// and within it the lowest slot, is the lowest expert id.  Round j takes the
-// warp-wide maximum of the lanes' best keys (redux.sync) and the lowest lane
-// holding it.  `row` may point to shared or global memory.  Lane j < k gets
-// expert j.
-//
-// E <= 256: each lane sorts its (up to) eight keys once, descending, by a
-// stable odd-even transposition network (equal keys keep their slot order), so
-// a round reads only the head of every lane's list and the winner pops it:
-// the rounds' dependent chain is the warp reduction alone.
+// Top-k selection of one token's E logits by one warp (E <= 256, k <= 32).
+// Lane l holds experts l, l+32, ..., l+224 (consecutive lanes, consecutive
+// addresses) and sorts its keys once, descending, by a stable odd-even
+// transposition network (equal keys keep ascending expert order).  Round j
+// takes the warp-wide maximum of the lanes' head keys and, among the lanes
+// holding it, the lowest expert id (two redux.sync); that lane pops its head.
+// `row` may point to shared or global memory.  Lane j < k gets expert j.
 __device__ __forceinline__ int select_topk8(const float* row, int E, int k, bool& bad) {
     const int lane = threadIdx.x & 31;
-    const int EPL = (E + 31) >> 5;  // <= 8
-    uint32_t key[8], idx[8];
+    uint32_t key[8], ex[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int e = lane * EPL + i;
-        const bool in = i < EPL && e < E;
+        const int e = lane + 32 * i;
+        const bool in = e < E;
         const float v = in ? row[e] : 0.0f;
         key[i] = in ? logit_key(v) : 0u;
-        idx[i] = (uint32_t)i;
+        ex[i] = (uint32_t)e;
         bad |= in && ((v != v) || (v == INFINITY));
     }
 #pragma unroll
@@ -151,28 +146,26 @@ __device__ __forceinline__ int select_topk8(const float* row, int E, int k, bool
 #pragma unroll
         for (int i = r & 1; i + 1 < 8; i += 2) {
             const bool sw = key[i + 1] > key[i];
-            const uint32_t ka = key[i], kb = key[i + 1], ia = idx[i], ib = idx[i + 1];
+            const uint32_t ka = key[i], kb = key[i + 1], ea = ex[i], eb = ex[i + 1];
             key[i] = sw ? kb : ka;
             key[i + 1] = sw ? ka : kb;
-            idx[i] = sw ? ib : ia;
-            idx[i + 1] = sw ? ia : ib;
+            ex[i] = sw ? eb : ea;
+            ex[i + 1] = sw ? ea : eb;
         }
     }
-    uint32_t sidx = 0;  // sorted slots, 3 bits each, head in the low bits
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sidx |= idx[i] << (3 * i);
     int my_e = 0;
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
         const uint32_t gk = __reduce_max_sync(0xffffffffu, key[0]);
-        const int wl = __ffs(__ballot_sync(0xffffffffu, key[0] == gk)) - 1;
-        const int we = __shfl_sync(0xffffffffu, lane * EPL + (int)(sidx & 7u), wl);
-        if (lane == j) my_e = we;
-        const bool win = lane == wl;  // pops its head
+        const uint32_t we = __reduce_min_sync(0xffffffffu, key[0] == gk ? ex[0] : 0xFFFFFFFFu);
+        if (lane == j) my_e = (int)we;
+        const bool win = ex[0] == we;  // expert ids are distinct: exactly one lane pops
 #pragma unroll
-        for (int i = 0; i < 7; ++i) key[i] = win ? key[i + 1] : key[i];
+        for (int i = 0; i < 7; ++i) {
+            key[i] = win ? key[i + 1] : key[i];
+            ex[i] = win ? ex[i + 1] : ex[i];
+        }
         key[7] = win ? 0u : key[7];
-        sidx = win ? (sidx >> 3) : sidx;
     }
     return my_e;
 }

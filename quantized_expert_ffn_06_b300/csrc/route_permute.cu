@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
 }
 
 // E <= 256: the selection of select_topk8 (each lane's eight keys sorted once,
-// then k rounds of one warp reduction over the lanes' heads); same experts, same
+// then k rounds of two warp reductions over the lanes' heads); same experts, same
 // order and the same weights as k_route.
 __global__ void __launch_bounds__(256) k_route_sorted(const float* __restrict__ logits, int T, int E, int k,
                                                       int32_t* __restrict__ ids, float* __restrict__ w) {
