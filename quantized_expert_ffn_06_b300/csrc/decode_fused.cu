@@ -296,11 +296,13 @@ __device__ __noinline__ float4 kblock_partial(const uint8_t* item, const __half*
     const int lane = threadIdx.x & 31;
     uint32_t sg0, sg1, sh0, sh1;
     e4m3x4_to_f16x2_bcast(*reinterpret_cast<const uint32_t*>(item + 1024 + lane * 4), sg0, sg1, sh0, sh1);
-    const uint32_t* c0 = reinterpret_cast<const uint32_t*>(item + lane * 16);
-    const uint32_t* c1 = reinterpret_cast<const uint32_t*>(item + 512 + lane * 16);
+    // the lane's 16 code bytes of each row in one 16-byte load each, the loop fully unrolled
+    const uint4 w0 = *reinterpret_cast<const uint4*>(item + lane * 16);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(item + 512 + lane * 16);
+    const uint32_t c0[4] = {w0.x, w0.y, w0.z, w0.w}, c1[4] = {w1.x, w1.y, w1.z, w1.w};
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
+#pragma unroll
     for (int s2 = 0; s2 < 4; ++s2) {
         uint32_t f0[4], f1[4];
         e2m1x8_to_f16x2x4(c0[s2], f0);
@@ -337,11 +339,12 @@ __device__ __noinline__ float4 kblock_partial_mx(const uint8_t* item, const __ha
     ref = __vmaxu2(ref, __shfl_xor_sync(0xffffffffu, ref, 2));
     const int rg = (int)(ref & 0xFFFFu), rh = (int)(ref >> 16);
     const uint32_t sa = pow2_f16x2((int)(own & 0xFFFFu) - rg), sb = pow2_f16x2((int)(own >> 16) - rh);
-    const uint32_t* c0 = reinterpret_cast<const uint32_t*>(item + lane * 16);
-    const uint32_t* c1 = reinterpret_cast<const uint32_t*>(item + 512 + lane * 16);
+    const uint4 w0 = *reinterpret_cast<const uint4*>(item + lane * 16);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(item + 512 + lane * 16);
+    const uint32_t c0[4] = {w0.x, w0.y, w0.z, w0.w}, c1[4] = {w1.x, w1.y, w1.z, w1.w};
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
+#pragma unroll
     for (int s2 = 0; s2 < 4; ++s2) {
         uint32_t f0[4], f1[4];
         e2m1x8_to_f16x2x4(c0[s2], f0);

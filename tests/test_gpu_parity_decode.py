@@ -364,15 +364,17 @@ def test_fused_router_ties_and_infinities():
     assert_layer_close(out.float().cpu().numpy(), ref["out"], "ties")
 
 
-def test_fused_activations_beyond_f16_range_are_rescaled():
+@pytest.mark.parametrize("T,big_row", [(4, 1), (1, 0)])
+def test_fused_activations_beyond_f16_range_are_rescaled(T, big_row):
     """A token row scaled by 2^20 overflows f16 staging: x and its h rows take the exact
-    power-of-two rescaling path.  Each token row is checked on its own scale."""
-    cfg = W.CONFIGS["tiny"]
+    power-of-two rescaling path (one token: the one-warp router and per-warp h slices; four tokens: the
+    general router).  Each token row is checked on its own scale."""
+    cfg = W.scaled(W.CONFIGS["tiny"], T=T)
     dl = DeviceLayer(cfg, 0, from_host=True)
     lw = dl.view("fused")
     logits = W.router_logits(cfg, 0, 2)
     x32 = W.bf16_bits_to_f32(W.activations_bf16(cfg, 0, 2)).copy()
-    x32[1] *= 2.0 ** 20
+    x32[big_row] *= 2.0 ** 20
     x_bits = (x32.view(np.uint32) >> 16).astype(np.uint16)   # exact: only exponents changed
     mod, out = fused_run(cfg, lw, to_dev(logits), x_bits)
     ref = oracle_layer(cfg, dl, logits, x_bits)
