@@ -421,24 +421,28 @@ class OraclePrefill:
 
 # --------------------------------------------------------------------------- GPU arm
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=("decode_fused.cu", "common.cuh")) -> str:
     h = hashlib.sha256()
-    for f in ("decode_fused.cu", "common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "quantized_expert_ffn_06_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, src_hash: str):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary, if still current."""
-    p = os.path.join(ROOT, "profiles", f"k_moe_decode_{workload}.json")
+PREFILL_SOURCES = ("prefill.cu", "route_permute.cu", "common.cuh")
+
+
+def profiled_traffic(workload: str, src_hash: str, kernel: str = "k_moe_decode", key: str = "dram_bytes_per_launch"):
+    """DRAM bytes per launch (or per call) of the measured kernel(s) from the committed ncu summary, if the
+    source it was taken on is still the current one."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     if d.get("source_hash") != src_hash:
         return None
-    return d.get("dram_bytes_per_launch")
+    return d.get(key)
 
 
 def run_gpu(args, ws, rank, local):
@@ -811,7 +815,11 @@ def run_gpu_prefill(args, ws, rank, local):
                      "frac": bytes_ffn / ffn_s / 1e9 / hbm_peak, "peak_kind": hbm_kind,
                      "kernel": "ft_moe_expert_ffn_nvfp4_prefill (plan, x quantisation, gate/up and down grouped "
                                "GEMMs, output), timed as one call",
-                     "bytes_per_launch": bytes_ffn, "avg_launch_us": ffn_s * 1e6, "traffic": None},
+                     "bytes_per_launch": bytes_ffn, "avg_launch_us": ffn_s * 1e6,
+                     "traffic": profiled_traffic(cfg.name, kernel_source_hash(PREFILL_SOURCES), "k_pf_ffn",
+                                                 "dram_bytes_per_call"),
+                     "traffic_what": "DRAM bytes read + written by the FFN call's kernels (plan, x quantisation, "
+                                     "gather, both GEMMs, output), from the committed ncu launch list"},
         "attainable": {"tflops": attainable, "frac": flops / ffn_s / 1e12 / attainable,
                        "bound": "hbm" if hbm_peak * ai / 1e3 < fp4_peak else "tensor", "flop_per_byte": ai,
                        "what": "the FFN call against min(FP4 peak, HBM peak x its arithmetic intensity)"},
@@ -987,6 +995,8 @@ def run_gpu_cache(args, ws, rank, local):
     torch.cuda.synchronize()
     h0, m0, b0 = pool.cache.stats()
     pf0, pu0 = pool.cache.prefetch_stats()
+    for lay in layers:
+        lay.host_wait_s = lay.host_cache_s = lay.host_call_s = 0.0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(dev)
     bus = None
@@ -1048,6 +1058,14 @@ def run_gpu_cache(args, ws, rank, local):
         "cache": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                   "h2d_bytes_per_token": miss_bytes_tok, "h2d_gbs_achieved": filled / (ms / 1e3) / 1e9,
                   "h2d_gbs_measured_peak": h2d_gbs,
+                  "host_ms_per_token": {
+                      "routing_wait": sum(lay.host_wait_s for lay in layers) * 1e3 / args.steps,
+                      "cache_logic": sum(lay.host_cache_s for lay in layers) * 1e3 / args.steps,
+                      "enqueue": sum(lay.host_call_s for lay in layers) * 1e3 / args.steps,
+                      "what": "host wall time per token, all layers: waiting for each layer's routing result (the "
+                              "device work queued before it: the previous layers' kernels and copies), the cache's "
+                              "host logic (lookup, fill and prefetch enqueues, publish), and the route/kernel "
+                              "launches"},
                   "prefetch": {"next_ranks": P, "source": args.prefetch_source, "prefetched": prefetched, "used": used,
                                "accuracy": used / prefetched if prefetched else None,
                                "demand_misses_per_token": misses / args.steps,

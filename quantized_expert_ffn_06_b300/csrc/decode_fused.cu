@@ -63,7 +63,8 @@ constexpr int MAXT = 16;               // tokens per launch
 constexpr int MAXK = 32;               // experts per token
 constexpr int ITEM = 1152;             // bytes of one K-block (128 elements) of a 16-row tile
 constexpr int XPAD = 32;               // halves of padding per staged f16 row
-constexpr int MAXSLOT = 2 * NW;        // partial-sum slots of a phase split across warps
+constexpr int MINSLOT = 2 * NW;        // partial-sum slots of a phase split across warps: at least,
+constexpr int MAXSLOT = 4 * NW;        // and at most (one- and two-token launches)
 constexpr size_t SMEM_BUDGET = 227 * 1024;
 constexpr unsigned long long WAIT_NS = 2000000000ull;  // default bound on any single wait
 }  // namespace dk
@@ -116,6 +117,7 @@ struct DecodePlan {
     int solo;                    // one routed token of at most 256 logits: one warp routes it, and the work split
                                  // (U = k distinct experts) is made before the inputs arrive
     int mx;                      // MXFP4 weights (FT_LAYOUT_MXFP4_DECODE_TILES): 1088-byte K-blocks, no tensor scale
+    int nslot;                   // partial-tile slots (a phase of n runs is split over the warps if n + NW <= nslot)
 };
 
 struct DecodeArgs {
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     __half* hs = reinterpret_cast<__half*>(dsm + P.off_big);   // ... h rows, f16, staged layout (phase 2)
     uint16_t* xraw = reinterpret_cast<uint16_t*>(dsm + P.off_xraw);                       // x as loaded, bf16
     unsigned long long* cand = reinterpret_cast<unsigned long long*>(dsm + P.off_cand);  // [T][nb][kk]
-    float* slots = reinterpret_cast<float*>(dsm + P.off_slot);  // [MAXSLOT][16][tc] partial tiles
+    float* slots = reinterpret_cast<float*>(dsm + P.off_slot);  // [nslot][16][tc] partial tiles
     float* wscr = reinterpret_cast<float*>(dsm + P.off_wscr);   // [NW][16][tc] a warp's finished tile
     float* ybuf = reinterpret_cast<float*>(dsm + P.off_ybuf);   // [max_ot][nf][16] expert outputs
 
@@ -430,10 +432,10 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         p1_end = max(p1_end, p1_beg);
         n_t1 = p1_end - p1_beg;
         nr2 = n_ot * U;  // phase-2 runs (output tile, expert), run r = otl * U + u
-        // this warp's K-block ranges: split evenly (runs shared by neighbouring warps), or whole runs
-        // per warp when a phase has more runs than warps
-        split1 = n_t1 <= dk::NW;
-        split2 = nr2 <= dk::NW;
+        // this warp's K-block ranges: split evenly (runs shared by neighbouring warps; run r of warp w
+        // sums into slot r + w), or whole runs per warp when the slots cannot hold a split
+        split1 = n_t1 + dk::NW <= P.nslot;
+        split2 = nr2 + dk::NW <= P.nslot;
         ni1 = n_t1 * KB1;
         ni2 = nr2 * KB2;
         if (split1) {
@@ -1172,7 +1174,14 @@ static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mod
     p.off_xraw = p.off_big + (int)lg_bytes;
     p.off_cand = p.off_xraw + (int)xraw_bytes;
     p.tc = T;
-    p.off_slot = take((size_t)dk::MAXSLOT * 16 * T * 4);
+    {
+        // enough slots for a split of either phase when the CTA's share allows it: at most
+        // ceil(n1 / G) + 2 gate/up tiles (float rounding of the byte balance) and max_ot * U runs
+        const int umax = std::min(E, nf);
+        const int t1max = (umax * (I / 8) + G - 1) / G + 2, r2max = ((H / 16 + G - 1) / G) * umax;
+        p.nslot = std::max(dk::MINSLOT, std::min(T <= 2 ? dk::MAXSLOT : dk::MINSLOT, dk::NW + std::max(t1max, r2max)));
+    }
+    p.off_slot = take((size_t)p.nslot * 16 * T * 4);
     p.off_wscr = take((size_t)dk::NW * 16 * T * 4);
     const int n2 = H / 16;
     p.max_ot = (n2 + G - 1) / G;

@@ -476,17 +476,23 @@ class CachedDecodeLayer:
         self.copy_stream = copy_stream if copy_stream is not None else torch.cuda.Stream(device=dev)
         self.filled = torch.cuda.Event()
         self.routed = torch.cuda.Event()
+        # host seconds spent, summed over calls: waiting for the routing result, in the cache's host logic
+        # (lookup, fill and prefetch enqueues, publish), and enqueueing the rest
+        self.host_wait_s = self.host_cache_s = self.host_call_s = 0.0
 
     def __call__(self, logits: torch.Tensor, x: torch.Tensor, out: torch.Tensor, step: int, stream=None,
                  predicted=None):
         """One token's layer step; returns the (expert, slot) misses filled for it.  `predicted` (host ints,
         optional) replaces the router's next P ranks as the experts installed for the next token."""
         stream = torch.cuda.current_stream(self.pool.device) if stream is None else stream
+        t0 = time.perf_counter()
         ft_moe_route(logits, self.k + self.prefetch, self.ids, self.w, stream=stream)
         with torch.cuda.stream(stream):
             self.ids_host.copy_(self.ids, non_blocking=True)
             self.routed.record(stream)
+        t1 = time.perf_counter()
         wait_event(self.routed, self.timeout_s, f"layer {self.layer}: routing result")
+        t2 = time.perf_counter()
         ranked = self.ids_host.tolist()
         needed = sorted(set(int(e) for row in ranked for e in row[:self.k]))
         _, misses = self.pool.cache.lookup(self.layer, step, needed)
@@ -495,7 +501,9 @@ class CachedDecodeLayer:
         self.filled.record(self.copy_stream)
         self.pool.cache.publish(self.layer, stream=stream)
         stream.wait_event(self.filled)
+        t3 = time.perf_counter()
         self.fused(self.weights, logits, x, out, routing=False, stream=stream)
+        t4 = time.perf_counter()
         if self.prefetch or predicted is not None:
             # the next-ranked experts, for the next token: copied behind this token's fills, which the next step's
             # kernel waits for (same copy stream), while this and later layers compute
@@ -505,4 +513,8 @@ class CachedDecodeLayer:
             self.prefetched = self.pool.cache.prefetch(self.layer, step, predicted)
             for e, s in self.prefetched:
                 self.pool.cache.fill(self.layer, e, s, stream=self.copy_stream)
+        t5 = time.perf_counter()
+        self.host_wait_s += t2 - t1
+        self.host_cache_s += (t3 - t2) + (t5 - t4)
+        self.host_call_s += (t1 - t0) + (t4 - t3)
         return misses
