@@ -29,8 +29,12 @@ def layer_and_inputs(cfg):
     return lw, logits, x
 
 
-def test_expired_wait_reports_timeout_and_the_next_call_is_exact():
-    cfg = W.CONFIGS["decode_35b"]
+@pytest.mark.parametrize("shape", ["decode_35b", "hidden_4096"])
+def test_expired_wait_reports_timeout_and_the_next_call_is_exact(shape):
+    """On the 35B layer shape and on hidden 4096 / intermediate 1536 (several tiles per warp, the down phase
+    split across warps)."""
+    cfg = (W.CONFIGS["decode_35b"] if shape == "decode_35b" else
+           W.scaled(W.CONFIGS["cache_stream"], routing="normal", T=1))
     lw, logits, x = layer_and_inputs(cfg)
     mod = FusedDecodeLayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV)
     clean = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)

@@ -173,3 +173,12 @@ def test_mx_tiles_equal_repacked_rows():
         dc, ds = unpack_mx_tiles(tiles.d_codes[e].cpu().numpy(), H, I)
         assert np.array_equal(gc, rows.gu_codes[e].cpu().numpy()) and np.array_equal(gs, rows.gu_scales[e].cpu().numpy())
         assert np.array_equal(dc, rows.d_codes[e].cpu().numpy()) and np.array_equal(ds, rows.d_scales[e].cpu().numpy())
+
+
+def test_fused_decode_mxfp4_large_shape():
+    """Hidden 4096, intermediate 1536, 128 experts, top-8 (the cache workload's layer shape, K-blocks of several
+    tiles per warp and a down phase split across warps), one token at two steps."""
+    cfg = W.scaled(W.CONFIGS["cache_stream"], routing="normal", T=1)
+    rows, tiles = mx_layer(cfg, 0)
+    for step in range(2):
+        check_fused(cfg, rows, tiles, 0, step, 1)
