@@ -418,10 +418,14 @@ FT_API ft_status ft_expert_cache_publish(ft_expert_cache* cache, int layer, ft_s
  * else the slot with the oldest stamp older than `step` (lower slot on a tie)
  * whose expert is not among `ids`, so neither a predicted expert nor one
  * stamped `step` -- the current token's, which a kernel may still be reading --
- * is displaced; when no slot qualifies the id is skipped.  An installed expert gets stamp step - 1.  fill_experts /
- * fill_slots (host, room for n) receive the copies the caller must enqueue
- * (ft_expert_cache_fill) before a layer reads them, ascending expert id;
- * *n_fill their count.  Pure host bookkeeping. */
+ * is displaced; when no slot qualifies the id is skipped.  An installed
+ * expert gets stamp step - 1.  fill_experts / fill_slots (host, room for n)
+ * receive the copies the caller must enqueue (ft_expert_cache_fill) before a
+ * layer reads them, ascending expert id; *n_fill their count.  The caller
+ * orders those copies after every kernel that may still read a displaced slot
+ * (experts stamped below `step`: earlier tokens' layer kernels), e.g. by
+ * enqueueing them on a copy stream only once this layer's previous kernel has
+ * completed.  Pure host bookkeeping. */
 FT_API ft_status ft_expert_cache_prefetch(ft_expert_cache* cache, int layer, int64_t step, const int32_t* ids, int n,
                                           int32_t* fill_experts, int32_t* fill_slots, int* n_fill);
 /* Experts installed by prefetches since creation, and how many of those a later

@@ -161,6 +161,13 @@ __device__ __forceinline__ void cp4(void* s, const void* g) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s)), "l"(g) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// the same copies to a shared-memory address given as such
+__device__ __forceinline__ void cp16s(uint32_t s, const void* g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp4s(uint32_t s, const void* g) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(g) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
@@ -747,8 +754,11 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     // scale bytes), MXFP4 1088-byte ones (64)
     const int tile_b1 = P.mx ? (17 * H) >> 1 : 9 * H, tile_b2 = P.mx ? (17 * I) >> 1 : 9 * I;
     const int sc_kb = P.mx ? 64 : 128;
-    const uint8_t* is_cb = nullptr;  // codes of the next K-block (nullptr: expert without weights)
-    const uint8_t* is_sb = nullptr;  // its scales
+    const uint8_t* is_cb = nullptr;  // this lane's codes of the next K-block (nullptr: expert without weights)
+    const uint8_t* is_sb = nullptr;  // this lane's scale word of it
+    // shared address of this lane's code piece in ring slot 0; its scale word is sc_off further
+    const uint32_t ring_l = smem_u32(ring) + lane * 16;
+    const int sc_off = 1024 - lane * 12;
     // first K-block `kb` of run `run` of phase `ph` (run: local tile, or local (output tile, expert))
     auto open_run = [&](int ph, int run, int kb, int left) {
         is_ph = ph;
@@ -768,29 +778,32 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             KB = KB2;
             base = W.d_codes + (int64_t)max(wi, 0) * W.d_codes_stride + (int64_t)(o_beg + otl) * tile_b2;
         }
-        is_cb = (wi >= 0) ? base + kb * 1024 : nullptr;
-        is_sb = base + KB * 1024 + kb * sc_kb;
+        is_cb = (wi >= 0) ? base + kb * 1024 + lane * 16 : nullptr;  // this lane's first code byte
+        is_sb = base + KB * 1024 + kb * sc_kb + lane * 4;               // and scale word
     };
+    const bool sc_lane = lane * 4 < sc_kb;  // lanes holding a scale word of a K-block
     auto issue = [&]() {
         if (is_n < cnt) {
-            if (is_n == cnt1) {  // this warp's first down K-block
-                const int r = ib2 / KB2, kb = ib2 - r * KB2;
-                open_run(2, r, kb, KB2 - kb);
-            } else if (is_left == 0) {  // next run of the same phase
-                open_run(is_ph, is_run + 1, 0, is_ph == 1 ? KB1 : KB2);
+            if (is_left == 0 || is_n == cnt1) {
+                if (is_n == cnt1) {  // this warp's first down K-block
+                    const int r = ib2 / KB2, kb = ib2 - r * KB2;
+                    open_run(2, r, kb, KB2 - kb);
+                } else {  // next run of the same phase
+                    open_run(is_ph, is_run + 1, 0, is_ph == 1 ? KB1 : KB2);
+                }
             }
-            uint8_t* slot = ring + (is_n & (R - 1)) * dk::ITEM;
-            const bool sc = lane * 4 < sc_kb;  // lanes holding a scale word of this K-block
+            const uint32_t d = ring_l + (uint32_t)((is_n & (R - 1)) * dk::ITEM);
             if (is_cb) {
-                cp16(slot + lane * 16, is_cb + lane * 16);
-                cp16(slot + 512 + lane * 16, is_cb + 512 + lane * 16);
-                if (sc) cp4(slot + 1024 + lane * 4, is_sb + lane * 4);
+                cp16s(d, is_cb);
+                cp16s(d + 512, is_cb + 512);
+                if (sc_lane) cp4s(d + sc_off, is_sb);
+                is_cb += 1024;
             } else {  // no weights behind this expert: zeros
+                uint8_t* slot = ring + (is_n & (R - 1)) * dk::ITEM;
                 *reinterpret_cast<uint4*>(slot + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(slot + 512 + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
-                if (sc) *reinterpret_cast<uint32_t*>(slot + 1024 + lane * 4) = 0u;
+                if (sc_lane) *reinterpret_cast<uint32_t*>(slot + 1024 + lane * 4) = 0u;
             }
-            if (is_cb) is_cb += 1024;
             is_sb += sc_kb;
             --is_left;
             ++is_n;
@@ -955,7 +968,9 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll 1
             for (int kb = kb0; kb < kb1; ++kb, ++n) {
-                cp_wait_upto(is_n - n - 1);  // K-block n of this lane has landed
+                // K-block n of this lane has landed: R - 1 younger groups in flight in the steady state
+                if (is_n - n - 1 >= R - 1) cp_wait<R - 1>();
+                else cp_wait_upto(is_n - n - 1);
                 const uint8_t* slot = ring + (n & (R - 1)) * dk::ITEM;
                 const float4 v = P.mx ? kblock_partial_mx(slot, r0 + kb * 128) : kblock_partial(slot, r0 + kb * 128);
                 acc0.x += v.x, acc0.y += v.y, acc0.z += v.z, acc0.w += v.w;
