@@ -195,3 +195,23 @@ def test_prefetch_rejects_bad_ids():
             c.prefetch(0, 0, ids)
         assert ei.value.status == Q.FT_ERR_INVALID_ARG
     assert c.prefetch(0, 0, []) == []
+
+
+def test_resize_plan_after_prefetches_matches_oracle():
+    """Prefetched experts carry stamp step - 1, which decides who survives a resize: the library's plan against the
+    oracle's along a stream with a prefetch after every token (the next token's experts plus one wrong guess)."""
+    cfg = W.scaled(W.CONFIGS["cache_stream"], steps=60)
+    c = fake_cache(1, cfg.E, cfg.slots)
+    o = LayerLRU(cfg.slots)
+    sets = W.cache_stream_sets(cfg, 3, 61)
+    for s in range(60):
+        c.lookup(0, s, list(sets[s]))
+        o.access(s, list(sets[s]))
+        pred = [int(e) for e in sets[s + 1]] + [(s * 37) % cfg.E]
+        assert c.prefetch(0, s, pred) == [tuple(f) for f in o.prefetch(s, pred)], s
+        if s in (5, 30, 59):
+            for n in (8, 16, 31, 64):
+                probe = LayerLRU(o.slots)
+                probe.expert_of, probe.stamp, probe.slot_of = list(o.expert_of), list(o.stamp), dict(o.slot_of)
+                probe.fetched = list(o.fetched)
+                assert c.resize_plan(n) == [probe.resize(n)], (s, n)
