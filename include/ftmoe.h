@@ -294,7 +294,10 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
  * same); FT_ERR_UNSUPPORTED only if a single token does not fit (then use the
  * separate calls with FT_LAYOUT_ROWS).
  * The launch allows programmatic dependent launch: the kernel reads no input
- * before the preceding kernel in the stream has completed. */
+ * before the preceding kernel in the stream has completed.  Its grid is one CTA
+ * per SM and the phases hand over through global memory, so every CTA must be
+ * able to run at once: a kernel on another stream holding SMs for longer than
+ * the wait bound (2 s) makes the call report FT_DEVERR_TIMEOUT. */
 FT_API size_t ft_moe_layer_decode_workspace_size(int T, int k, int H, int I);
 FT_API ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits, const uint16_t* x, int T,
                                      int k, uint16_t* out, int32_t* ids, float* w, void* ws, size_t ws_bytes,

@@ -14,15 +14,17 @@
 //  * Code size.  Control loops stay rolled, divisions by per-launch constants
 //    are host-computed multiply-high divisors, and one out-of-line routine
 //    computes a K-block for both projections.
-//  * Inputs.  Right after the dependency wait every thread issues its async
-//    copies of the router logits and of x at once.
+//  * Inputs.  Right after the dependency wait one thread issues one bulk copy of
+//    x and one of the router logits on an mbarrier.
 //  * Router (every CTA, redundantly: no inter-CTA traffic before the weight
-//    stream).  Two levels, no serial rounds: each warp ranks a block of 32
-//    logits by 32 shuffles and keeps its k best as sorted candidates; then one
-//    thread per (candidate, block) counts by binary search how many of that
-//    block's candidates beat it, and the sum of those counts is the
-//    candidate's rank.  Keys order the fp32 logits exactly, equal logits going
-//    to the lower expert id.
+//    stream).  One token of at most 256 logits: warp 0 keeps each lane's eight
+//    keys sorted and takes each rank with two warp reductions (the largest key,
+//    then the lowest expert holding it) while the other warps stage x, and the
+//    work split, a function of k alone, is made before the inputs arrive.
+//    Several tokens: each warp ranks a block of 32 logits by 32 shuffles and
+//    keeps its k best as sorted candidates, then eight lanes per candidate count
+//    the candidates that beat it.  Keys order the fp32 logits exactly, equal
+//    logits going to the lower expert id.
 //  * Work split.  Phase 1 is the gate/up tiles of the selected experts, phase 2
 //    the down projection of 16-row output tiles over all selected experts.  A
 //    CTA's phase-1 share is balanced by bytes against its phase-2 share.
@@ -43,10 +45,15 @@
 //    the words it reads, so no grid-wide barrier separates the phases.
 //  * Combine.  A token's k expert outputs are summed in slot order j in fp32
 //    from shared memory and rounded once to bf16.
-//  * Grid = one CTA per SM, all co-resident, which the hand-off relies on.
-//    Every wait is bounded by a %globaltimer budget; on expiry the kernel sets
-//    FT_DEVERR_TIMEOUT and finishes without trapping.  The launch allows
-//    programmatic dependent launch (griddepcontrol).
+//  * MXFP4 weights run through the same kernel with 1088-byte K-blocks (UE8M0
+//    scales: a per-row reference exponent, the residual in f16, 2^r on the fp32
+//    partial).
+//  * Grid = one CTA per SM (its shared memory admits one), all co-resident,
+//    which the hand-off relies on: while another kernel holds SMs, resident CTAs
+//    wait for the h of CTAs not yet started.  Every wait is bounded by a
+//    %globaltimer budget; on expiry the kernel sets FT_DEVERR_TIMEOUT and
+//    finishes without trapping.  The launch allows programmatic dependent
+//    launch (griddepcontrol).
 #include "common.cuh"
 
 #include <algorithm>
