@@ -463,14 +463,14 @@ def run_gpu(args, ws, rank, local):
     chunk = max([c for c in range(1, T + 1) if (c * (H + 32) + c * k * (cfg.I + 32)) * 2 <= 120 * 1024] or [1])
     n_chunks = -(-T // chunk)  # launches per layer on the fused path
     layout = Q.FT_LAYOUT_DECODE_TILES if fused else Q.FT_LAYOUT_ROWS
-    mx = args.weights == "mxfp4"
+    mx = args.weights in ("mxfp4", "mxfp8")
     if mx:
         if not fused:
-            raise SystemExit("MXFP4 weights run on the fused decode step only")
-        layout = Q.FT_LAYOUT_MXFP4_DECODE_TILES
+            raise SystemExit("MX weights run on the fused decode step only")
+        layout = Q.FT_LAYOUT_MXFP4_DECODE_TILES if args.weights == "mxfp4" else Q.FT_LAYOUT_MXFP8_DECODE_TILES
     # bytes of one expert's three matrices: NVFP4 0.5 B per code + 1 B per 16 + three fp32 tensor scales,
-    # MXFP4 0.5 B per code + 1 B per 32
-    expert_bytes = 3 * H * cfg.I * 17 // 32 if mx else cfg.expert_bytes + 12
+    # MXFP4 0.5 B per code + 1 B per 32, MXFP8 1 B per code + 1 B per 32
+    expert_bytes = (3 * H * cfg.I * (17 if args.weights == "mxfp4" else 33) // 32 if mx else cfg.expert_bytes + 12)
 
     # ---- weights (device generator + device quantiser), all experts resident
     weights = []
@@ -591,7 +591,8 @@ def run_gpu(args, ws, rank, local):
                "h2d_bytes_per_step": L * T * (H * 2 + E * 4), "d2h_bytes_per_step": L * T * H * 2}
 
     src_hash = kernel_source_hash()
-    wfmt = "MXFP4 (E2M1 + UE8M0/32)" if mx else "NVFP4 (E2M1 + E4M3/16 + fp32 tensor scale)"
+    wfmt = {"mxfp4": "MXFP4 (E2M1 + UE8M0/32)", "mxfp8": "MXFP8 (E4M3 + UE8M0/32)"}.get(
+        args.weights, "NVFP4 (E2M1 + E4M3/16 + fp32 tensor scale)")
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -612,7 +613,7 @@ def run_gpu(args, ws, rank, local):
                                 if fused else
                                 "route + permute + k_decode_gateup + k_decode_down + combine per layer, timed together"),
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_launch_s * 1e6,
-                     "traffic": profiled_traffic(cfg.name + ("_mxfp4" if mx else ""), src_hash) if fused else None,
+                     "traffic": profiled_traffic(cfg.name + ("_" + args.weights if mx else ""), src_hash) if fused else None,
                      "source_hash": src_hash},
         "e2e": e2e,
         "gpu_launches": L * args.steps * launches_per_layer,
@@ -1097,7 +1098,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="(debug) fewer layers; the result is then not the workload")
     ap.add_argument("--prefetch-source", default="router", choices=["router", "next"],
                     help="cache stream: predictions from the router's ranks, or the next token's experts (exact)")
-    ap.add_argument("--weights", default="nvfp4", choices=["nvfp4", "mxfp4"],
+    ap.add_argument("--weights", default="nvfp4", choices=["nvfp4", "mxfp4", "mxfp8"],
                     help="decode configs: expert weight format of the fused layer step")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="cache stream: install the router's next P ranked experts of each token for the next one")

@@ -112,6 +112,8 @@ FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
 #define FT_LAYOUT_UMMA_TILES 2   /* 128x128 blocks for the tensor-core prefill, see ft_nvfp4_pack_umma() */
 #define FT_LAYOUT_MXFP4_ROWS 3   /* MXFP4: row-major codes [N][K/2] + row-major UE8M0 scales [N][K/32] */
 #define FT_LAYOUT_MXFP4_DECODE_TILES 4 /* MXFP4 16-row tiles for the fused decode, see ft_mxfp4_pack_tiles() */
+#define FT_LAYOUT_MXFP8_ROWS 5   /* MXFP8: row-major E4M3 codes [N][K] + row-major UE8M0 scales [N][K/32] */
+#define FT_LAYOUT_MXFP8_DECODE_TILES 6 /* MXFP8 16-row tiles for the fused decode, see ft_mxfp8_pack_tiles() */
 
 /* Expert weights of one layer in device memory.  For weight index w (the
  * expert id, or its cache slot when expert_to_slot is given):
@@ -135,9 +137,12 @@ FT_API ft_status ft_device_status(ft_stream_t stream, uint32_t* err_word);
  *  layout FT_LAYOUT_MXFP4_DECODE_TILES (codes and scales together): the same
  *            matrices packed by ft_mxfp4_pack_tiles() (2I*H*17/32 and H*I*17/32
  *            bytes); no tensor scale
+ *  layout FT_LAYOUT_MXFP8_ROWS / FT_LAYOUT_MXFP8_DECODE_TILES: as the MXFP4 ones
+ *            with one E4M3 byte per element (codes [N][K]; tiles of 2I*H*33/32
+ *            and H*I*33/32 bytes, see ft_mxfp8_pack_tiles()); no tensor scale
  *  NVFP4 layouts
  *   tensor scales  tscale + w*tscale_stride : float {gate, up, down}
- *   (MXFP4 layouts have none: tscale may be NULL and is not read)
+ *   (MX layouts have none: tscale may be NULL and is not read)
  *   gu_sf_tiled / d_sf_tiled (optional, prefill only): scales rearranged for the
  *            block-scaled tensor cores, strides gu_sf_tiled_stride / d_sf_tiled_stride.
  * Strides are in bytes (tscale_stride in floats).  Every base address and
@@ -266,7 +271,9 @@ FT_API ft_status ft_moe_expert_ffn_nvfp4_decode(const ft_moe_layer_weights* W, c
                                          size_t ws_bytes, ft_stream_t stream);
 
 /* Fused decode layer step for up to 16 tokens, weights in FT_LAYOUT_DECODE_TILES
- * (NVFP4) or FT_LAYOUT_MXFP4_DECODE_TILES (MXFP4):
+ * (NVFP4), FT_LAYOUT_MXFP4_DECODE_TILES (MXFP4) or FT_LAYOUT_MXFP8_DECODE_TILES
+ * (MXFP8, the same scale handling; exact unless a block is more than 2^15
+ * below the largest of its row's K-block):
  * router top-k (same selection and weights as ft_moe_route), grouping by
  * expert (same order as ft_moe_permute), the SwiGLU expert FFN on the 4-bit
  * weights and the weighted combine, in one launch of one CTA per SM.
@@ -540,6 +547,25 @@ FT_API ft_status ft_mxfp4_quantize_weight(const float* w, int64_t N, int64_t K, 
  * codes of exactly one block of rows g and g+8 and reads their two scale bytes
  * at L*2.  N a multiple of 16, K a multiple of 128.  All pointers (device). */
 FT_API ft_status ft_mxfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
+                                     int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
+
+/* MXFP8 weight quantiser [P5 limits: FP8 among the weight formats; the OCP
+ * Microscaling v1.0 MXFP8 format]: as ft_mxfp4_quantize_weight with E4M3
+ * elements: X = floor(log2(amax)) - 8 clamped to [-127, 127], code = E4M3
+ * round-to-nearest-even of v / 2^X saturating at 448 (sign in bit 7, -0 stored
+ * as +0), one byte per element: codes [N][K] at row stride codes_ld (a
+ * multiple of 16, >= K). */
+FT_API ft_status ft_mxfp8_quantize_weight(const float* w, int64_t N, int64_t K, uint8_t* codes, int64_t codes_ld,
+                                          uint8_t* scales, int64_t scales_ld, ft_stream_t stream);
+
+/* Packs a row-major MXFP8 matrix [N][K] (codes [N][K], scales [N][K/32]) into
+ * FT_LAYOUT_MXFP8_DECODE_TILES: N/16 tiles of 16*K*33/32 bytes.  Within a tile,
+ * per 128-element K-block kb: 2048 code bytes, the 32 bytes of elements
+ * 32q .. 32q+31 of row 8h+g at kb*2048 + h*1024 + (g*4+q)*32; after all code
+ * blocks, 64 scale bytes per K-block placed as in ft_mxfp4_pack_tiles()
+ * ((K/128)*2048 + kb*64 + (g*4+q)*2 + h).  N a multiple of 16, K of 128.
+ * All pointers (device). */
+FT_API ft_status ft_mxfp8_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
                                      int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
 
 /* Synthetic weights: out[j] = (float)(sigma * Z_{first+j}) where Z is the

@@ -24,6 +24,7 @@ FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_UNSUPPORTED, FT_ERR_TIMEOUT, FT_E
     FT_ERR_DEVICE = range(8)
 FT_LAYOUT_ROWS, FT_LAYOUT_DECODE_TILES, FT_LAYOUT_UMMA_TILES = 0, 1, 2
 FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP4_DECODE_TILES = 3, 4
+FT_LAYOUT_MXFP8_ROWS, FT_LAYOUT_MXFP8_DECODE_TILES = 5, 6
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX = 1, 2, 4, 8
 FT_WAIT_SITE_NONE, FT_WAIT_SITE_DECODE_H = 0, 1
 
@@ -92,6 +93,8 @@ _sig("ft_moe_layer_decode_noalloc", [ctypes.POINTER(ft_moe_layer_weights), _vp, 
 _sig("ft_nvfp4_pack_umma", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_mxfp4_quantize_weight", [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp])
 _sig("ft_mxfp4_pack_tiles", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
+_sig("ft_mxfp8_quantize_weight", [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp])
+_sig("ft_mxfp8_pack_tiles", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_moe_prefill_workspace_size", [_i32, _i32, _i32, _i32, _i32], _sz)
 _sig("ft_moe_expert_ffn_nvfp4_prefill", [ctypes.POINTER(ft_moe_layer_weights), _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                          _vp, _sz, _vp])
@@ -274,6 +277,20 @@ def ft_mxfp4_quantize_weight(w: torch.Tensor, codes, scales, codes_ld: int | Non
 
 def ft_mxfp4_pack_tiles(codes, codes_ld: int, scales, scales_ld: int, N: int, K: int, tiles, stream=None):
     _check(_lib.ft_mxfp4_pack_tiles(_p(codes), codes_ld, _p(scales), scales_ld, N, K, _p(tiles), _s(stream)))
+
+
+def ft_mxfp8_quantize_weight(w: torch.Tensor, codes, scales, codes_ld: int | None = None, scales_ld: int | None = None,
+                             stream=None):
+    """MXFP8 codes [N][K] (E4M3) and UE8M0 scales [N][K/32] of an fp32 [N][K] matrix (device)."""
+    _req(w, torch.float32, "w")
+    N, K = w.shape
+    codes_ld = K if codes_ld is None else codes_ld
+    scales_ld = K // 32 if scales_ld is None else scales_ld
+    _check(_lib.ft_mxfp8_quantize_weight(_p(w), N, K, _p(codes), codes_ld, _p(scales), scales_ld, _s(stream)))
+
+
+def ft_mxfp8_pack_tiles(codes, codes_ld: int, scales, scales_ld: int, N: int, K: int, tiles, stream=None):
+    _check(_lib.ft_mxfp8_pack_tiles(_p(codes), codes_ld, _p(scales), scales_ld, N, K, _p(tiles), _s(stream)))
 
 
 def ft_moe_layer_decode_workspace_size(T: int, k: int, H: int, I: int) -> int:

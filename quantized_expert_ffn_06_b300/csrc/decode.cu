@@ -245,8 +245,8 @@ ft_status validate_weights(const ft_moe_layer_weights* W, const char* fn) {
     if (!W) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights descriptor is null");
     if (W->E <= 0 || W->E > 1024 || W->H <= 0 || W->H % 256 || W->I <= 0 || W->I % 128 || W->n_weights <= 0)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 1 <= E <= 1024, H a multiple of 256, I a multiple of 128");
-    const bool rows = W->layout == FT_LAYOUT_ROWS || W->layout == FT_LAYOUT_MXFP4_ROWS;
-    const bool mx = W->layout == FT_LAYOUT_MXFP4_ROWS || W->layout == FT_LAYOUT_MXFP4_DECODE_TILES;  // no tensor scale
+    const bool rows = W->layout == FT_LAYOUT_ROWS || W->layout == FT_LAYOUT_MXFP4_ROWS || W->layout == FT_LAYOUT_MXFP8_ROWS;
+    const bool mx = W->layout >= FT_LAYOUT_MXFP4_ROWS && W->layout <= FT_LAYOUT_MXFP8_DECODE_TILES;  // no tensor scale
     if (!W->gu_codes || !W->d_codes || (!mx && !W->tscale) || (rows && (!W->gu_scales || !W->d_scales)))
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null weight pointer");
     if (!W->expert_to_slot && W->n_weights < W->E)

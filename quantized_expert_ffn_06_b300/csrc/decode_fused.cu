@@ -68,7 +68,8 @@ constexpr int LOG_NW = 4;
 constexpr int THREADS = 32 * NW;
 constexpr int MAXT = 16;               // tokens per launch
 constexpr int MAXK = 32;               // experts per token
-constexpr int ITEM = 1152;             // bytes of one K-block (128 elements) of a 16-row tile
+constexpr int ITEM = 1152;             // bytes of one K-block (128 elements) of a 16-row tile: NVFP4 (MXFP4: 1088)
+constexpr int ITEM8 = 2112;            // MXFP8: 2048 code bytes + 64 scale bytes
 constexpr int XPAD = 32;               // halves of padding per staged f16 row
 constexpr int MINSLOT = 2 * NW;        // partial-sum slots of a phase split across warps: at least,
 constexpr int MAXSLOT = 4 * NW;        // and at most (one- and two-token launches)
@@ -123,7 +124,8 @@ struct DecodePlan {
     int logits_bulk;             // the logits come in by one bulk copy (16-byte aligned, size a multiple of 16)
     int solo;                    // one routed token of at most 256 logits: one warp routes it, and the work split
                                  // (U = k distinct experts) is made before the inputs arrive
-    int mx;                      // MXFP4 weights (FT_LAYOUT_MXFP4_DECODE_TILES): 1088-byte K-blocks, no tensor scale
+    int mx;                      // 0 NVFP4; 1 MXFP4 (1088-byte K-blocks), 2 MXFP8 (2112-byte K-blocks): no tensor scale
+    int item;                    // bytes of a ring slot (one K-block of the format, rounded up to ITEM)
     int nslot;                   // partial-tile slots (a phase of n runs is split over the warps if n + NW <= nslot)
 };
 
@@ -225,6 +227,13 @@ __device__ __forceinline__ void e4m3x4_to_f16x2_bcast(uint32_t sc, uint32_t& s0,
         "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
         : "=r"(s0), "=r"(s1), "=r"(s2), "=r"(s3)
         : "r"(lo), "r"(hi));
+}
+
+// Four E4M3 bytes (one word, byte 0 first) as two f16x2: bytes 0, 1 and bytes 2, 3 (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -373,6 +382,43 @@ __device__ __noinline__ float4 kblock_partial_mx(const uint8_t* item, const __ha
     return make_float4((d[0] + e[0]) * fg, (d[1] + e[1]) * fg, (d[2] + e[2]) * fh, (d[3] + e[3]) * fh);
 }
 
+// The MXFP8 form: item = 2048 code bytes (one E4M3 byte per element; lane L =
+// 4g + q owns the 32 bytes of row g at L*32 and of row g+8 at 1024 + L*32, i.e.
+// elements 32q .. 32q+31, exactly one MX block of each row), then the UE8M0
+// pairs at 2048 + 2L.  E4M3 converts exactly to f16; the scales are applied as
+// for MXFP4 (exact unless a block is more than 2^15 below the largest of its
+// row's K-block).
+__device__ __noinline__ float4 kblock_partial_mx8(const uint8_t* item, const __half* x) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t sp = *reinterpret_cast<const uint16_t*>(item + 2048 + lane * 2);
+    const uint32_t own = (sp & 0xFFu) | ((sp >> 8) << 16);
+    uint32_t ref = __vmaxu2(own, __shfl_xor_sync(0xffffffffu, own, 1));
+    ref = __vmaxu2(ref, __shfl_xor_sync(0xffffffffu, ref, 2));
+    const int rg = (int)(ref & 0xFFFFu), rh = (int)(ref >> 16);
+    const uint32_t sa = pow2_f16x2((int)(own & 0xFFFFu) - rg), sb = pow2_f16x2((int)(own >> 16) - rh);
+    const uint4 g0 = *reinterpret_cast<const uint4*>(item + lane * 32);
+    const uint4 g1 = *reinterpret_cast<const uint4*>(item + lane * 32 + 16);
+    const uint4 h0 = *reinterpret_cast<const uint4*>(item + 1024 + lane * 32);
+    const uint4 h1 = *reinterpret_cast<const uint4*>(item + 1024 + lane * 32 + 16);
+    const uint32_t c0[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t c1[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+        uint32_t f0[4], f1[4];
+        e4m3x4_to_f16x2x2(c0[2 * s2], f0[0], f0[1]);
+        e4m3x4_to_f16x2x2(c0[2 * s2 + 1], f0[2], f0[3]);
+        e4m3x4_to_f16x2x2(c1[2 * s2], f1[0], f1[1]);
+        e4m3x4_to_f16x2x2(c1[2 * s2 + 1], f1[2], f1[3]);
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + 32 * s2);
+        mma16816(d, hmul2(f0[0], sa), hmul2(f1[0], sb), hmul2(f0[1], sa), hmul2(f1[1], sb), xv.x, xv.y);
+        mma16816(e, hmul2(f0[2], sa), hmul2(f1[2], sb), hmul2(f0[3], sa), hmul2(f1[3], sb), xv.z, xv.w);
+    }
+    const float fg = ue8m0_to_f32((uint32_t)rg), fh = ue8m0_to_f32((uint32_t)rh);
+    return make_float4((d[0] + e[0]) * fg, (d[1] + e[1]) * fg, (d[2] + e[2]) * fh, (d[3] + e[3]) * fh);
+}
+
 // ---------------------------------------------------------------------------- kernel
 
 template <int R>
@@ -408,7 +454,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const int G = gridDim.x, c = blockIdx.x;
     const int TC = P.tc;
     const bool route_mode = a.logits != nullptr;
-    uint8_t* ring = dsm + P.off_ring + warp * (R * dk::ITEM);
+    uint8_t* ring = dsm + P.off_ring + warp * (R * P.item);
 
     // ---------------- work split over U selected experts: CTA c takes phase-1 tiles [p1_beg, p1_end) and
     // output tiles [o_beg, o_end); its warps split the K-blocks of each phase.  With one routed token U = k
@@ -759,13 +805,17 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     int is_n = 0, is_left = 0, is_ph = 1, is_run = 0, is_kb0 = 0;
     // bytes of a 16-row tile (gate/up, down) and of a K-block's scales: NVFP4 1152-byte K-blocks (128
     // scale bytes), MXFP4 1088-byte ones (64)
-    const int tile_b1 = P.mx ? (17 * H) >> 1 : 9 * H, tile_b2 = P.mx ? (17 * I) >> 1 : 9 * I;
+    // MXFP8: 2112-byte K-blocks (2048 code bytes)
+    const int cb_kb = P.mx == 2 ? 2048 : 1024;  // code bytes of a K-block
+    const int tile_b1 = P.mx == 2 ? (33 * H) >> 1 : P.mx ? (17 * H) >> 1 : 9 * H;
+    const int tile_b2 = P.mx == 2 ? (33 * I) >> 1 : P.mx ? (17 * I) >> 1 : 9 * I;
     const int sc_kb = P.mx ? 64 : 128;
     const uint8_t* is_cb = nullptr;  // this lane's codes of the next K-block (nullptr: expert without weights)
     const uint8_t* is_sb = nullptr;  // this lane's scale word of it
-    // shared address of this lane's code piece in ring slot 0; its scale word is sc_off further
-    const uint32_t ring_l = smem_u32(ring) + lane * 16;
-    const int sc_off = 1024 - lane * 12;
+    // shared address of this lane's code piece in ring slot 0 (16 bytes per lane and half tile; MXFP8: 32);
+    // its scale word is sc_off further
+    const uint32_t ring_l = smem_u32(ring) + lane * (cb_kb >> 6);
+    const int sc_off = cb_kb + lane * 4 - lane * (cb_kb >> 6);
     // first K-block `kb` of run `run` of phase `ph` (run: local tile, or local (output tile, expert))
     auto open_run = [&](int ph, int run, int kb, int left) {
         is_ph = ph;
@@ -785,8 +835,8 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
             KB = KB2;
             base = W.d_codes + (int64_t)max(wi, 0) * W.d_codes_stride + (int64_t)(o_beg + otl) * tile_b2;
         }
-        is_cb = (wi >= 0) ? base + kb * 1024 + lane * 16 : nullptr;  // this lane's first code byte
-        is_sb = base + KB * 1024 + kb * sc_kb + lane * 4;               // and scale word
+        is_cb = (wi >= 0) ? base + kb * cb_kb + lane * (cb_kb >> 6) : nullptr;  // this lane's first code byte
+        is_sb = base + KB * cb_kb + kb * sc_kb + lane * 4;                        // and scale word
     };
     const bool sc_lane = lane * 4 < sc_kb;  // lanes holding a scale word of a K-block
     auto issue = [&]() {
@@ -799,17 +849,24 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                     open_run(is_ph, is_run + 1, 0, is_ph == 1 ? KB1 : KB2);
                 }
             }
-            const uint32_t d = ring_l + (uint32_t)((is_n & (R - 1)) * dk::ITEM);
+            const uint32_t d = ring_l + (uint32_t)((is_n & (R - 1)) * P.item);
             if (is_cb) {
-                cp16s(d, is_cb);
-                cp16s(d + 512, is_cb + 512);
+                if (P.mx == 2) {  // 32 code bytes per lane and half tile
+                    cp16s(d, is_cb);
+                    cp16s(d + 16, is_cb + 16);
+                    cp16s(d + 1024, is_cb + 1024);
+                    cp16s(d + 1040, is_cb + 1040);
+                } else {
+                    cp16s(d, is_cb);
+                    cp16s(d + 512, is_cb + 512);
+                }
                 if (sc_lane) cp4s(d + sc_off, is_sb);
-                is_cb += 1024;
+                is_cb += cb_kb;
             } else {  // no weights behind this expert: zeros
-                uint8_t* slot = ring + (is_n & (R - 1)) * dk::ITEM;
-                *reinterpret_cast<uint4*>(slot + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(slot + 512 + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
-                if (sc_lane) *reinterpret_cast<uint32_t*>(slot + 1024 + lane * 4) = 0u;
+                uint8_t* slot = ring + (is_n & (R - 1)) * P.item;
+#pragma unroll 1
+                for (int o = lane * 16; o < cb_kb; o += 512) *reinterpret_cast<uint4*>(slot + o) = make_uint4(0u, 0u, 0u, 0u);
+                if (sc_lane) *reinterpret_cast<uint32_t*>(slot + cb_kb + lane * 4) = 0u;
             }
             is_sb += sc_kb;
             --is_left;
@@ -978,12 +1035,15 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 // K-block n of this lane has landed: R - 1 younger groups in flight in the steady state
                 if (is_n - n - 1 >= R - 1) cp_wait<R - 1>();
                 else cp_wait_upto(is_n - n - 1);
-                const uint8_t* slot = ring + (n & (R - 1)) * dk::ITEM;
-                const float4 v = P.mx ? kblock_partial_mx(slot, r0 + kb * 128) : kblock_partial(slot, r0 + kb * 128);
+                const uint8_t* slot = ring + (n & (R - 1)) * P.item;
+                const float4 v = P.mx == 2 ? kblock_partial_mx8(slot, r0 + kb * 128)
+                                 : P.mx  ? kblock_partial_mx(slot, r0 + kb * 128)
+                                         : kblock_partial(slot, r0 + kb * 128);
                 acc0.x += v.x, acc0.y += v.y, acc0.z += v.z, acc0.w += v.w;
                 if (tu > 8) {
-                    const float4 v1 =
-                        P.mx ? kblock_partial_mx(slot, r1 + kb * 128) : kblock_partial(slot, r1 + kb * 128);
+                    const float4 v1 = P.mx == 2 ? kblock_partial_mx8(slot, r1 + kb * 128)
+                                      : P.mx  ? kblock_partial_mx(slot, r1 + kb * 128)
+                                              : kblock_partial(slot, r1 + kb * 128);
                     acc1.x += v1.x, acc1.y += v1.y, acc1.z += v1.z, acc1.w += v1.w;
                 }
                 issue();  // into the slot just read (this lane's own bytes)
@@ -1162,7 +1222,10 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // raw inputs and the router's candidates and later the staged h rows, the
 // partial-tile slots, the warps' scratch tiles, the per-slot down outputs and
 // the warps' K-block rings (R slots each: 16, else 8, 4 or 2, whichever fits).
-static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mode, DecodePlan& p, std::string& why) {
+static int item_bytes(int layout) { return layout == FT_LAYOUT_MXFP8_DECODE_TILES ? dk::ITEM8 : dk::ITEM; }
+
+static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mode, int item, DecodePlan& p,
+                        std::string& why) {
     const int nf = T * k;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -1211,7 +1274,7 @@ static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mod
     p.off_ring = (int)off;
     p.ring = 0;
     for (int r : {16, 8, 4, 2})
-        if (off + (size_t)dk::NW * r * dk::ITEM <= dk::SMEM_BUDGET) {
+        if (off + (size_t)dk::NW * r * item <= dk::SMEM_BUDGET) {
             p.ring = r;
             break;
         }
@@ -1220,7 +1283,8 @@ static bool plan_decode(int T, int k, int E, int H, int I, int G, bool route_mod
               " expert rows do not fit the fused kernel's shared memory";
         return false;
     }
-    p.smem = (int)(off + (size_t)dk::NW * p.ring * dk::ITEM);
+    p.smem = (int)(off + (size_t)dk::NW * p.ring * item);
+    p.item = item;
     p.dv_k = make_fastdiv((uint32_t)k);
     p.dv_xrow = make_fastdiv((uint32_t)(H / 8));
     p.dv_hrow = make_fastdiv((uint32_t)(I / 2));
@@ -1272,10 +1336,10 @@ static ft_status launch_decode(DecodeArgs a, ft_stream_t stream, const char* fn)
     const ft_moe_layer_weights& W = a.W;
     const int G = sm_count();
     std::string why;
-    if (!plan_decode(a.T, a.k, W.E, W.H, W.I, G, a.logits != nullptr, a.P, why))
+    if (!plan_decode(a.T, a.k, W.E, W.H, W.I, G, a.logits != nullptr, item_bytes(W.layout), a.P, why))
         return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
     a.P.logits_bulk = a.logits && aligned(a.logits, 16) && ((size_t)a.T * W.E * 4) % 16 == 0;
-    a.P.mx = W.layout == FT_LAYOUT_MXFP4_DECODE_TILES;
+    a.P.mx = W.layout == FT_LAYOUT_MXFP4_DECODE_TILES ? 1 : W.layout == FT_LAYOUT_MXFP8_DECODE_TILES ? 2 : 0;
     ft_status st = decode_attributes(fn);
     if (st != FT_OK) return st;
     cudaLaunchConfig_t cfg = {};
@@ -1335,9 +1399,9 @@ static ft_status check_layer_decode_args(const ft_moe_layer_weights* W, const fl
                                          int k, uint16_t* out, int32_t* ids, float* w, const char* fn) {
     ft_status st = validate_weights(W, fn);
     if (st != FT_OK) return st;
-    if (W->layout != FT_LAYOUT_DECODE_TILES && W->layout != FT_LAYOUT_MXFP4_DECODE_TILES)
-        return fail(FT_ERR_INVALID_ARG,
-                    std::string(fn) + ": weights must use FT_LAYOUT_DECODE_TILES or FT_LAYOUT_MXFP4_DECODE_TILES");
+    if (W->layout != FT_LAYOUT_DECODE_TILES && W->layout != FT_LAYOUT_MXFP4_DECODE_TILES &&
+        W->layout != FT_LAYOUT_MXFP8_DECODE_TILES)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": weights must use FT_LAYOUT_DECODE_TILES or an MX tile layout");
     if (T < 0 || T > dk::MAXT || k <= 0 || k > W->E || k > dk::MAXK)
         return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 0 <= T <= 16 and 1 <= k <= min(E, 32)");
     if (T == 0) return FT_OK;
@@ -1457,7 +1521,8 @@ ft_status ft_moe_layer_decode(const ft_moe_layer_weights* W, const float* logits
     {
         DecodePlan probe;
         std::string why;
-        while (Tc > 0 && !plan_decode(Tc, k, W->E, W->H, W->I, sm_count(), true, probe, why)) --Tc;
+        while (Tc > 0 && !plan_decode(Tc, k, W->E, W->H, W->I, sm_count(), true, item_bytes(W->layout), probe, why))
+            --Tc;
         if (Tc == 0) return fail(FT_ERR_UNSUPPORTED, std::string(fn) + ": " + why);
     }
     for (int t0 = 0; t0 < T; t0 += Tc) {

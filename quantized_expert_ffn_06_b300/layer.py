@@ -9,8 +9,9 @@ import time
 
 import torch
 
-from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_MXFP4_DECODE_TILES, FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_ROWS,
-               FT_LAYOUT_UMMA_TILES, ft_gen_normal_f32, ft_mxfp4_pack_tiles, ft_mxfp4_quantize_weight,
+from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_MXFP4_DECODE_TILES, FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP8_DECODE_TILES,
+               FT_LAYOUT_MXFP8_ROWS, FT_LAYOUT_ROWS, FT_LAYOUT_UMMA_TILES, ft_gen_normal_f32, ft_mxfp4_pack_tiles,
+               ft_mxfp4_quantize_weight, ft_mxfp8_pack_tiles, ft_mxfp8_quantize_weight,
                ft_moe_decode_workspace_size, ft_moe_expert_ffn_nvfp4_decode, ft_moe_expert_ffn_nvfp4_prefill,
                ft_moe_layer_decode, ft_moe_layer_decode_workspace_size, ft_moe_layer_weights, ft_moe_permute,
                ft_moe_permute_workspace_size, ft_moe_prefill_workspace_size, ft_moe_route, ft_nvfp4_pack_tiles,
@@ -40,6 +41,8 @@ class LayerWeights:
     MXFP4 layouts (UE8M0 scales per 32, no tensor scale):
     layout MXFP4_ROWS:  as ROWS with gu_scales [n, 2I, H/32], d_scales [n, H, I/32]
     layout MXFP4_TILES: gu_codes [n, 2I*H*17/32], d_codes [n, H*I*17/32] (see ft_mxfp4_pack_tiles)
+    layout MXFP8_ROWS:  codes of one byte per element: gu_codes [n, 2I, H], d_codes [n, H, I]; scales as MXFP4
+    layout MXFP8_TILES: gu_codes [n, 2I*H*33/32], d_codes [n, H*I*33/32] (see ft_mxfp8_pack_tiles)
     """
 
     def __init__(self, E: int, H: int, I: int, device, n_weights: int | None = None, layout: int = FT_LAYOUT_ROWS):
@@ -48,16 +51,19 @@ class LayerWeights:
         self.layout = layout
         self.device = torch.device(device)
         u8 = torch.uint8
-        self.mx = layout in (FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP4_DECODE_TILES)
+        self.mx8 = layout in (FT_LAYOUT_MXFP8_ROWS, FT_LAYOUT_MXFP8_DECODE_TILES)
+        self.mx = self.mx8 or layout in (FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP4_DECODE_TILES)
         self.sblock = 32 if self.mx else 16  # elements per scale
-        if layout in (FT_LAYOUT_ROWS, FT_LAYOUT_MXFP4_ROWS):
-            self.gu_codes = torch.empty((self.n, 2 * I, H // 2), dtype=u8, device=device)
+        self.cpe = 1 if self.mx8 else 2      # code elements per byte
+        if layout in (FT_LAYOUT_ROWS, FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP8_ROWS):
+            self.gu_codes = torch.empty((self.n, 2 * I, H // self.cpe), dtype=u8, device=device)
             self.gu_scales = torch.empty((self.n, 2 * I, H // self.sblock), dtype=u8, device=device)
-            self.d_codes = torch.empty((self.n, H, I // 2), dtype=u8, device=device)
+            self.d_codes = torch.empty((self.n, H, I // self.cpe), dtype=u8, device=device)
             self.d_scales = torch.empty((self.n, H, I // self.sblock), dtype=u8, device=device)
-        elif layout == FT_LAYOUT_MXFP4_DECODE_TILES:
-            self.gu_codes = torch.empty((self.n, 2 * I * H * 17 // 32), dtype=u8, device=device)
-            self.d_codes = torch.empty((self.n, H * I * 17 // 32), dtype=u8, device=device)
+        elif layout in (FT_LAYOUT_MXFP4_DECODE_TILES, FT_LAYOUT_MXFP8_DECODE_TILES):
+            num = 33 if self.mx8 else 17
+            self.gu_codes = torch.empty((self.n, 2 * I * H * num // 32), dtype=u8, device=device)
+            self.d_codes = torch.empty((self.n, H * I * num // 32), dtype=u8, device=device)
             self.gu_scales = self.d_scales = None
         else:
             self.gu_codes = torch.empty((self.n, 2 * I * H * 9 // 16), dtype=u8, device=device)
@@ -88,13 +94,13 @@ class LayerWeights:
 
     def _rows_target(self, wi: int):
         """Row-major destination for expert wi: the weights themselves (ROWS) or a staging copy (TILES)."""
-        if self.layout in (FT_LAYOUT_ROWS, FT_LAYOUT_MXFP4_ROWS):
+        if self.layout in (FT_LAYOUT_ROWS, FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP8_ROWS):
             return self.gu_codes[wi], self.gu_scales[wi], self.d_codes[wi], self.d_scales[wi]
         if self._tmp is None:
-            H, I, u8, dev, sb = self.H, self.I, torch.uint8, self.device, self.sblock
-            self._tmp = (torch.empty((2 * I, H // 2), dtype=u8, device=dev),
+            H, I, u8, dev, sb, c = self.H, self.I, torch.uint8, self.device, self.sblock, self.cpe
+            self._tmp = (torch.empty((2 * I, H // c), dtype=u8, device=dev),
                          torch.empty((2 * I, H // sb), dtype=u8, device=dev),
-                         torch.empty((H, I // 2), dtype=u8, device=dev),
+                         torch.empty((H, I // c), dtype=u8, device=dev),
                          torch.empty((H, I // sb), dtype=u8, device=dev))
         return self._tmp
 
@@ -103,15 +109,17 @@ class LayerWeights:
         H, I = self.H, self.I
         guc, gus, dc, ds = self._rows_target(wi)
         if self.mx:
+            quant, pack, c = ((ft_mxfp8_quantize_weight, ft_mxfp8_pack_tiles, 1) if self.mx8 else
+                              (ft_mxfp4_quantize_weight, ft_mxfp4_pack_tiles, 2))
             for proj, w in ((PROJ_GATE, wg), (PROJ_UP, wu)):
                 assert tuple(w.shape) == (I, H)
-                ft_mxfp4_quantize_weight(w, guc.data_ptr() + proj * (H // 2), gus.data_ptr() + proj * (H // 32),
-                                         codes_ld=H, scales_ld=H // 16, stream=stream)
+                quant(w, guc.data_ptr() + proj * (H // c), gus.data_ptr() + proj * (H // 32),
+                      codes_ld=2 * H // c, scales_ld=H // 16, stream=stream)
             assert tuple(wd.shape) == (H, I)
-            ft_mxfp4_quantize_weight(wd, dc, ds, stream=stream)
-            if self.layout == FT_LAYOUT_MXFP4_DECODE_TILES:
-                ft_mxfp4_pack_tiles(guc, H // 2, gus, H // 32, 2 * I, H, self.gu_codes[wi], stream=stream)
-                ft_mxfp4_pack_tiles(dc, I // 2, ds, I // 32, H, I, self.d_codes[wi], stream=stream)
+            quant(wd, dc, ds, stream=stream)
+            if self.layout in (FT_LAYOUT_MXFP4_DECODE_TILES, FT_LAYOUT_MXFP8_DECODE_TILES):
+                pack(guc, H // c, gus, H // 32, 2 * I, H, self.gu_codes[wi], stream=stream)
+                pack(dc, I // c, ds, I // 32, H, I, self.d_codes[wi], stream=stream)
             return
         for proj, w in ((PROJ_GATE, wg), (PROJ_UP, wu)):
             assert tuple(w.shape) == (I, H)

@@ -165,3 +165,17 @@ def test_layer_decode_takes_mxfp4_tiles_without_tensor_scales():
     N = weights()
     N.tscale = None
     status(L.ft_moe_layer_decode(ctypes.byref(N), P, P, 0, 2, P, NULL, NULL, P, ws, NULL), Q.FT_ERR_INVALID_ARG)
+
+
+def test_mxfp8_argument_checks():
+    q = L.ft_mxfp8_quantize_weight
+    status(q(P, 16, 250, P, 256, P, 8, NULL), Q.FT_ERR_INVALID_ARG)       # K not a multiple of 32
+    status(q(P, 16, 256, P, 240, P, 8, NULL), Q.FT_ERR_INVALID_ARG)       # codes_ld < K
+    status(q(P, 16, 256, MIS, 256, P, 8, NULL), Q.FT_ERR_INVALID_ARG)     # misaligned codes
+    pk = L.ft_mxfp8_pack_tiles
+    status(pk(P, 256, P, 8, 15, 256, P, NULL), Q.FT_ERR_INVALID_ARG)     # N not a multiple of 16
+    status(pk(P, 128, P, 8, 16, 256, P, NULL), Q.FT_ERR_INVALID_ARG)     # codes_ld < K
+    W = weights(layout=Q.FT_LAYOUT_MXFP8_DECODE_TILES)
+    W.tscale, W.tscale_stride = None, 0
+    ws = L.ft_moe_layer_decode_workspace_size(4, 2, W.H, W.I)
+    status(L.ft_moe_layer_decode(ctypes.byref(W), P, P, 0, 2, P, NULL, NULL, P, ws, NULL), Q.FT_OK)

@@ -1,7 +1,7 @@
-"""GPU tests of the MXFP4 expert weights: the quantiser and the tile packing bit for bit against the oracle's
-statement of the format (oracle/mx.py) and of the layout, and the fused decode layer step on MXFP4 tiles against the
-oracle layer reading the device's own row-layout MXFP4 bytes (relative L2 5e-3, max |err| 2e-2 * RMS), on the
-one-token path (routing by one warp) and the multi-token path.
+"""GPU tests of the MX expert weights (MXFP4 and MXFP8): the quantisers and the tile packings bit for bit against the
+oracle's statement of the formats (oracle/mx.py) and of the layouts, and the fused decode layer step on MX tiles
+against the oracle layer reading the device's own row-layout MX bytes (relative L2 5e-3, max |err| 2e-2 * RMS), on
+the one-token path (routing by one warp) and the multi-token path.
 """
 import numpy as np
 import pytest
@@ -20,11 +20,15 @@ if torch.cuda.is_available():
     from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights
 
 
-def quantize_on_device(w: np.ndarray):
+FMTS = ["mxfp4", "mxfp8"]
+
+
+def quantize_on_device(w: np.ndarray, fmt: str = "mxfp4"):
     N, K = w.shape
-    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=DEV)
+    codes = torch.empty((N, K // 2 if fmt == "mxfp4" else K), dtype=torch.uint8, device=DEV)
     scales = torch.empty((N, K // 32), dtype=torch.uint8, device=DEV)
-    Q.ft_mxfp4_quantize_weight(torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(DEV), codes, scales)
+    quant = Q.ft_mxfp4_quantize_weight if fmt == "mxfp4" else Q.ft_mxfp8_quantize_weight
+    quant(torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(DEV), codes, scales)
     torch.cuda.synchronize()
     assert Q.ft_device_status() == 0
     return codes.cpu().numpy(), scales.cpu().numpy()
@@ -53,8 +57,9 @@ def special_matrix(rng):
     return w
 
 
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("which", ["normal", "special", "wide"])
-def test_quantiser_bit_exact_against_oracle(which):
+def test_quantiser_bit_exact_against_oracle(which, fmt):
     rng = np.random.default_rng({"normal": 0, "special": 1, "wide": 2}[which])
     if which == "normal":
         w = rng.normal(0, 0.02, (512, 2048)).astype(np.float32)
@@ -62,38 +67,48 @@ def test_quantiser_bit_exact_against_oracle(which):
         w = special_matrix(rng)
     else:  # magnitudes over the whole fp32 range, one decade per block
         w = (rng.normal(0, 1, (256, 1024)) * 10.0 ** rng.integers(-40, 37, (256, 32)).repeat(32, axis=1)).astype(np.float32)
-    codes, scales = quantize_on_device(w)
-    want_c, want_s = MX.quantize(w, "mxfp4")
+    if fmt == "mxfp8" and which == "special":   # E4M3 ties and saturation at its own grid
+        w[4, :32] = np.float32(256.0 + 16.0) * np.sign(w[4, :32])   # halfway between 256 and 288
+        w[4, 31] = 416.0                                            # amax 416: X = 0; 416 = 448 - 32 exact
+        w[5, 0] = 470.0                                             # above 448 * 2^X: saturates
+    codes, scales = quantize_on_device(w, fmt)
+    want_c, want_s = MX.quantize(w, fmt)
     assert np.array_equal(scales, want_s)
     assert np.array_equal(codes, want_c)
 
 
-def unpack_mx_tiles(tiles: np.ndarray, N: int, K: int):
-    """Rows-layout codes and scales read back from MXFP4 decode tiles by the layout statement of
-    ft_mxfp4_pack_tiles: codes of row 8h+g, bytes 16q..16q+15 of K-block kb, at kb*1024 + h*512 + (g*4+q)*16; the
-    scale of block 4kb+q of row 8h+g at (K/128)*1024 + kb*64 + (g*4+q)*2 + h."""
+def unpack_mx_tiles(tiles: np.ndarray, N: int, K: int, fmt: str = "mxfp4"):
+    """Rows-layout codes and scales read back from MX decode tiles by the layout statements of ft_mxfp4_pack_tiles
+    and ft_mxfp8_pack_tiles: with P code bytes per lane and half tile (16 for MXFP4, 32 for MXFP8) and C = 32 P
+    code bytes per half tile, the codes of row 8h+g, bytes Pq..Pq+P-1 of K-block kb, at kb*2C + h*C + (g*4+q)*P;
+    the scale of block 4kb+q of row 8h+g at (K/128)*2C + kb*64 + (g*4+q)*2 + h."""
     KB = K // 128
-    t = tiles.reshape(N // 16, KB * 1088)
-    codes = np.empty((N, K // 2), np.uint8)
+    P = 16 if fmt == "mxfp4" else 32
+    C = 32 * P
+    t = tiles.reshape(N // 16, KB * (2 * C + 64))
+    codes = np.empty((N, KB * 4 * P), np.uint8)
     scales = np.empty((N, K // 32), np.uint8)
     for kb in range(KB):
         for h in range(2):
             for g in range(8):
                 for q in range(4):
-                    off = kb * 1024 + h * 512 + (g * 4 + q) * 16
-                    codes[8 * h + g::16, kb * 64 + 16 * q:kb * 64 + 16 * q + 16] = t[:, off:off + 16]
-                    scales[8 * h + g::16, kb * 4 + q] = t[:, KB * 1024 + kb * 64 + (g * 4 + q) * 2 + h]
+                    off = kb * 2 * C + h * C + (g * 4 + q) * P
+                    codes[8 * h + g::16, kb * 4 * P + P * q:kb * 4 * P + P * q + P] = t[:, off:off + P]
+                    scales[8 * h + g::16, kb * 4 + q] = t[:, KB * 2 * C + kb * 64 + (g * 4 + q) * 2 + h]
     return codes, scales
 
 
-def test_pack_tiles_places_every_byte():
+@pytest.mark.parametrize("fmt", FMTS)
+def test_pack_tiles_places_every_byte(fmt):
     rng = np.random.default_rng(3)
     N, K = 48, 384
-    codes = torch.from_numpy(rng.integers(0, 256, (N, K // 2), dtype=np.uint8)).to(DEV)
+    cb = K // 2 if fmt == "mxfp4" else K
+    codes = torch.from_numpy(rng.integers(0, 256, (N, cb), dtype=np.uint8)).to(DEV)
     scales = torch.from_numpy(rng.integers(0, 255, (N, K // 32), dtype=np.uint8)).to(DEV)
-    tiles = torch.empty(N * K * 17 // 32, dtype=torch.uint8, device=DEV)
-    Q.ft_mxfp4_pack_tiles(codes, K // 2, scales, K // 32, N, K, tiles)
-    got_c, got_s = unpack_mx_tiles(tiles.cpu().numpy(), N, K)
+    tiles = torch.empty(N * K * (17 if fmt == "mxfp4" else 33) // 32, dtype=torch.uint8, device=DEV)
+    pack = Q.ft_mxfp4_pack_tiles if fmt == "mxfp4" else Q.ft_mxfp8_pack_tiles
+    pack(codes, cb, scales, K // 32, N, K, tiles)
+    got_c, got_s = unpack_mx_tiles(tiles.cpu().numpy(), N, K, fmt)
     assert np.array_equal(got_c, codes.cpu().numpy())
     assert np.array_equal(got_s, scales.cpu().numpy())
 
@@ -102,11 +117,11 @@ class MxOracleExperts:
     """expert(e) for O.moe_layer: the device's row-layout MXFP4 bytes (gate and up are the even and odd rows of the
     interleaved gate/up matrix), dequantised by the oracle."""
 
-    def __init__(self, rows):
-        self.rows = rows
+    def __init__(self, rows, fmt="mxfp4"):
+        self.rows, self.fmt = rows, fmt
 
     def __call__(self, e):
-        r = self.rows
+        r, f = self.rows, self.fmt
         gc, gs = r.gu_codes[e].cpu().numpy(), r.gu_scales[e].cpu().numpy()
         dc, ds = r.d_codes[e].cpu().numpy(), r.d_scales[e].cpu().numpy()
 
@@ -114,24 +129,26 @@ class MxOracleExperts:
             pass
 
         ex = Ex()
-        ex.Wg = MX.dequantize(gc[0::2], gs[0::2], "mxfp4")
-        ex.Wu = MX.dequantize(gc[1::2], gs[1::2], "mxfp4")
-        ex.Wd = MX.dequantize(dc, ds, "mxfp4")
+        ex.Wg = MX.dequantize(gc[0::2], gs[0::2], f)
+        ex.Wu = MX.dequantize(gc[1::2], gs[1::2], f)
+        ex.Wd = MX.dequantize(dc, ds, f)
         return ex
 
 
-def mx_layer(cfg, layer):
+def mx_layer(cfg, layer, fmt="mxfp4"):
     """The same fp32 draws quantised twice on the device: row layout (what the oracle reads) and decode tiles."""
     stream_of = lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p)  # noqa: E731
-    rows = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_MXFP4_ROWS)
+    lr, lt = ((Q.FT_LAYOUT_MXFP4_ROWS, Q.FT_LAYOUT_MXFP4_DECODE_TILES) if fmt == "mxfp4" else
+              (Q.FT_LAYOUT_MXFP8_ROWS, Q.FT_LAYOUT_MXFP8_DECODE_TILES))
+    rows = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=lr)
     rows.fill_synthetic(stream_of, sigma=cfg.w_sigma)
-    tiles = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_MXFP4_DECODE_TILES)
+    tiles = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=lt)
     tiles.fill_synthetic(stream_of, sigma=cfg.w_sigma)
     torch.cuda.synchronize()
     return rows, tiles
 
 
-def check_fused(cfg, rows, tiles, layer, step, T):
+def check_fused(cfg, rows, tiles, layer, step, T, fmt="mxfp4"):
     logits = W.router_logits(cfg, layer, step, T=T)
     x_bits = W.activations_bf16(cfg, layer, step, T=T)
     out = torch.empty((T, cfg.H), dtype=torch.bfloat16, device=DEV)
@@ -140,45 +157,49 @@ def check_fused(cfg, rows, tiles, layer, step, T):
         torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).to(DEV), out)
     torch.cuda.synchronize()
     assert Q.ft_device_status() == 0
-    r = O.moe_layer(logits, x_bits, cfg.k, MxOracleExperts(rows), O.MODE_A16)
+    r = O.moe_layer(logits, x_bits, cfg.k, MxOracleExperts(rows, fmt), O.MODE_A16)
     assert np.array_equal(mod.ids.cpu().numpy(), r["ids"])
-    assert_layer_close(out.float().cpu().numpy(), r["out"], f"mxfp4 layer {layer} step {step} T={T}")
+    assert_layer_close(out.float().cpu().numpy(), r["out"], f"{fmt} layer {layer} step {step} T={T}")
 
 
-def test_fused_decode_mxfp4_tiny():
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fused_decode_mx_tiny(fmt):
     cfg = W.CONFIGS["tiny"]
-    rows, tiles = mx_layer(cfg, 0)
+    rows, tiles = mx_layer(cfg, 0, fmt)
     for T in (1, 4):
-        check_fused(cfg, rows, tiles, 0, 0, T)
+        check_fused(cfg, rows, tiles, 0, 0, T, fmt)
 
 
-def test_fused_decode_mxfp4_35b_shape():
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fused_decode_mx_35b_shape(fmt):
     """Hidden 2048, 256 experts, top-8, intermediate 512: one token (one-warp routing) at several steps, and 16
     tokens (the multi-token path)."""
     cfg = W.CONFIGS["decode_35b"]
-    rows, tiles = mx_layer(cfg, 0)
+    rows, tiles = mx_layer(cfg, 0, fmt)
     for step in range(3):
-        check_fused(cfg, rows, tiles, 0, step, 1)
-    check_fused(cfg, rows, tiles, 0, 5, 16)
+        check_fused(cfg, rows, tiles, 0, step, 1, fmt)
+    check_fused(cfg, rows, tiles, 0, 5, 16, fmt)
 
 
-def test_mx_tiles_equal_repacked_rows():
-    """The decode tiles drawn directly equal the row-layout bytes packed by ft_mxfp4_pack_tiles (the quantiser is
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mx_tiles_equal_repacked_rows(fmt):
+    """The decode tiles drawn directly equal the row-layout bytes packed by the pack call (the quantiser is
     deterministic), so the oracle's bytes are the kernel's bytes."""
     cfg = W.scaled(W.CONFIGS["tiny"], E=3)
-    rows, tiles = mx_layer(cfg, 1)
+    rows, tiles = mx_layer(cfg, 1, fmt)
     H, I = cfg.H, cfg.I
     for e in range(cfg.E):
-        gc, gs = unpack_mx_tiles(tiles.gu_codes[e].cpu().numpy(), 2 * I, H)
-        dc, ds = unpack_mx_tiles(tiles.d_codes[e].cpu().numpy(), H, I)
+        gc, gs = unpack_mx_tiles(tiles.gu_codes[e].cpu().numpy(), 2 * I, H, fmt)
+        dc, ds = unpack_mx_tiles(tiles.d_codes[e].cpu().numpy(), H, I, fmt)
         assert np.array_equal(gc, rows.gu_codes[e].cpu().numpy()) and np.array_equal(gs, rows.gu_scales[e].cpu().numpy())
         assert np.array_equal(dc, rows.d_codes[e].cpu().numpy()) and np.array_equal(ds, rows.d_scales[e].cpu().numpy())
 
 
-def test_fused_decode_mxfp4_large_shape():
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fused_decode_mx_large_shape(fmt):
     """Hidden 4096, intermediate 1536, 128 experts, top-8 (the cache workload's layer shape, K-blocks of several
     tiles per warp and a down phase split across warps), one token at two steps."""
     cfg = W.scaled(W.CONFIGS["cache_stream"], routing="normal", T=1)
-    rows, tiles = mx_layer(cfg, 0)
+    rows, tiles = mx_layer(cfg, 0, fmt)
     for step in range(2):
-        check_fused(cfg, rows, tiles, 0, step, 1)
+        check_fused(cfg, rows, tiles, 0, step, 1, fmt)
