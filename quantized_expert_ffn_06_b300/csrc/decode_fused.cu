@@ -421,8 +421,10 @@ __device__ __noinline__ float4 kblock_partial_mx8(const uint8_t* item, const __h
 
 // ---------------------------------------------------------------------------- kernel
 
-template <int R>
+// FMT: 0 NVFP4, 1 MXFP4, 2 MXFP8 (a template parameter: each format's kernel carries only its own code)
+template <int R, int FMT>
 __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs a) {
+    constexpr int ITEMB = FMT == 2 ? dk::ITEM8 : dk::ITEM;  // bytes of a ring slot
     extern __shared__ __align__(128) uint8_t dsm[];
     const DecodePlan& P = a.P;
     int* misc = reinterpret_cast<int*>(dsm + P.off_misc);
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     const int G = gridDim.x, c = blockIdx.x;
     const int TC = P.tc;
     const bool route_mode = a.logits != nullptr;
-    uint8_t* ring = dsm + P.off_ring + warp * (R * P.item);
+    uint8_t* ring = dsm + P.off_ring + warp * (R * ITEMB);
 
     // ---------------- work split over U selected experts: CTA c takes phase-1 tiles [p1_beg, p1_end) and
     // output tiles [o_beg, o_end); its warps split the K-blocks of each phase.  With one routed token U = k
@@ -806,10 +808,10 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
     // bytes of a 16-row tile (gate/up, down) and of a K-block's scales: NVFP4 1152-byte K-blocks (128
     // scale bytes), MXFP4 1088-byte ones (64)
     // MXFP8: 2112-byte K-blocks (2048 code bytes)
-    const int cb_kb = P.mx == 2 ? 2048 : 1024;  // code bytes of a K-block
-    const int tile_b1 = P.mx == 2 ? (33 * H) >> 1 : P.mx ? (17 * H) >> 1 : 9 * H;
-    const int tile_b2 = P.mx == 2 ? (33 * I) >> 1 : P.mx ? (17 * I) >> 1 : 9 * I;
-    const int sc_kb = P.mx ? 64 : 128;
+    constexpr int cb_kb = FMT == 2 ? 2048 : 1024;  // code bytes of a K-block
+    const int tile_b1 = FMT == 2 ? (33 * H) >> 1 : FMT ? (17 * H) >> 1 : 9 * H;
+    const int tile_b2 = FMT == 2 ? (33 * I) >> 1 : FMT ? (17 * I) >> 1 : 9 * I;
+    constexpr int sc_kb = FMT ? 64 : 128;
     const uint8_t* is_cb = nullptr;  // this lane's codes of the next K-block (nullptr: expert without weights)
     const uint8_t* is_sb = nullptr;  // this lane's scale word of it
     // shared address of this lane's code piece in ring slot 0 (16 bytes per lane and half tile; MXFP8: 32);
@@ -849,9 +851,9 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                     open_run(is_ph, is_run + 1, 0, is_ph == 1 ? KB1 : KB2);
                 }
             }
-            const uint32_t d = ring_l + (uint32_t)((is_n & (R - 1)) * P.item);
+            const uint32_t d = ring_l + (uint32_t)((is_n & (R - 1)) * ITEMB);
             if (is_cb) {
-                if (P.mx == 2) {  // 32 code bytes per lane and half tile
+                if (FMT == 2) {  // 32 code bytes per lane and half tile
                     cp16s(d, is_cb);
                     cp16s(d + 16, is_cb + 16);
                     cp16s(d + 1024, is_cb + 1024);
@@ -863,7 +865,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 if (sc_lane) cp4s(d + sc_off, is_sb);
                 is_cb += cb_kb;
             } else {  // no weights behind this expert: zeros
-                uint8_t* slot = ring + (is_n & (R - 1)) * P.item;
+                uint8_t* slot = ring + (is_n & (R - 1)) * ITEMB;
 #pragma unroll 1
                 for (int o = lane * 16; o < cb_kb; o += 512) *reinterpret_cast<uint4*>(slot + o) = make_uint4(0u, 0u, 0u, 0u);
                 if (sc_lane) *reinterpret_cast<uint32_t*>(slot + cb_kb + lane * 4) = 0u;
@@ -910,10 +912,10 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
 #pragma unroll 1
     for (int u = tid; u < U; u += dk::THREADS) {
         const int wi = s_uwi[u];
-        const float* ts = P.mx ? nullptr : W.tscale + (int64_t)(wi >= 0 ? wi : 0) * W.tscale_stride;
-        s_ts[4 * u + 0] = (wi >= 0) ? (P.mx ? 1.0f : __ldg(ts + 0)) : 0.0f;
-        s_ts[4 * u + 1] = (wi >= 0) ? (P.mx ? 1.0f : __ldg(ts + 1)) : 0.0f;
-        s_ts[4 * u + 2] = (wi >= 0) ? (P.mx ? 1.0f : __ldg(ts + 2)) : 0.0f;
+        const float* ts = FMT ? nullptr : W.tscale + (int64_t)(wi >= 0 ? wi : 0) * W.tscale_stride;
+        s_ts[4 * u + 0] = (wi >= 0) ? (FMT ? 1.0f : __ldg(ts + 0)) : 0.0f;
+        s_ts[4 * u + 1] = (wi >= 0) ? (FMT ? 1.0f : __ldg(ts + 1)) : 0.0f;
+        s_ts[4 * u + 2] = (wi >= 0) ? (FMT ? 1.0f : __ldg(ts + 2)) : 0.0f;
     }
 
     const int g8 = lane >> 2, q4 = lane & 3;
@@ -938,7 +940,7 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
         if (shared) return s_ts[4 * u + j];
         const int wi = s_uwi[u];
         if (wi < 0) return 0.0f;
-        return P.mx ? 1.0f : __ldg(W.tscale + (int64_t)wi * W.tscale_stride + j);
+        return FMT ? 1.0f : __ldg(W.tscale + (int64_t)wi * W.tscale_stride + j);
     };
     // is warp w without K-blocks in a split phase of ni K-blocks?
     auto empty_warp = [&](int w, int ni) { return ni && ((w * ni) >> dk::LOG_NW) == (((w + 1) * ni) >> dk::LOG_NW); };
@@ -1035,15 +1037,15 @@ __global__ void __launch_bounds__(dk::THREADS, 1) k_moe_decode(const DecodeArgs 
                 // K-block n of this lane has landed: R - 1 younger groups in flight in the steady state
                 if (is_n - n - 1 >= R - 1) cp_wait<R - 1>();
                 else cp_wait_upto(is_n - n - 1);
-                const uint8_t* slot = ring + (n & (R - 1)) * P.item;
-                const float4 v = P.mx == 2 ? kblock_partial_mx8(slot, r0 + kb * 128)
-                                 : P.mx  ? kblock_partial_mx(slot, r0 + kb * 128)
-                                         : kblock_partial(slot, r0 + kb * 128);
+                const uint8_t* slot = ring + (n & (R - 1)) * ITEMB;
+                const float4 v = FMT == 2 ? kblock_partial_mx8(slot, r0 + kb * 128)
+                                 : FMT    ? kblock_partial_mx(slot, r0 + kb * 128)
+                                          : kblock_partial(slot, r0 + kb * 128);
                 acc0.x += v.x, acc0.y += v.y, acc0.z += v.z, acc0.w += v.w;
                 if (tu > 8) {
-                    const float4 v1 = P.mx == 2 ? kblock_partial_mx8(slot, r1 + kb * 128)
-                                      : P.mx  ? kblock_partial_mx(slot, r1 + kb * 128)
-                                              : kblock_partial(slot, r1 + kb * 128);
+                    const float4 v1 = FMT == 2 ? kblock_partial_mx8(slot, r1 + kb * 128)
+                                      : FMT    ? kblock_partial_mx(slot, r1 + kb * 128)
+                                               : kblock_partial(slot, r1 + kb * 128);
                     acc1.x += v1.x, acc1.y += v1.y, acc1.z += v1.z, acc1.w += v1.w;
                 }
                 issue();  // into the slot just read (this lane's own bytes)
@@ -1318,11 +1320,14 @@ static ft_status decode_attributes(const char* fn) {
     }
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return FT_OK;
-    const cudaError_t errs[4] = {
-        cudaFuncSetAttribute(k_moe_decode<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET),
-        cudaFuncSetAttribute(k_moe_decode<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET),
-        cudaFuncSetAttribute(k_moe_decode<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET),
-        cudaFuncSetAttribute(k_moe_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dk::SMEM_BUDGET)};
+    const int lim = (int)dk::SMEM_BUDGET;
+    const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    const cudaError_t errs[10] = {
+        cudaFuncSetAttribute(k_moe_decode<16, 0>, attr, lim), cudaFuncSetAttribute(k_moe_decode<8, 0>, attr, lim),
+        cudaFuncSetAttribute(k_moe_decode<4, 0>, attr, lim),  cudaFuncSetAttribute(k_moe_decode<2, 0>, attr, lim),
+        cudaFuncSetAttribute(k_moe_decode<16, 1>, attr, lim), cudaFuncSetAttribute(k_moe_decode<8, 1>, attr, lim),
+        cudaFuncSetAttribute(k_moe_decode<4, 1>, attr, lim),  cudaFuncSetAttribute(k_moe_decode<2, 1>, attr, lim),
+        cudaFuncSetAttribute(k_moe_decode<4, 2>, attr, lim),  cudaFuncSetAttribute(k_moe_decode<2, 2>, attr, lim)};
     for (cudaError_t e : errs)
         if (e != cudaSuccess) {
             cudaGetLastError();  // not sticky: leave no error behind for the launch check
@@ -1353,10 +1358,15 @@ static ft_status launch_decode(DecodeArgs a, ft_stream_t stream, const char* fn)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (a.P.ring == 16) e = cudaLaunchKernelEx(&cfg, k_moe_decode<16>, a);
-    else if (a.P.ring == 8) e = cudaLaunchKernelEx(&cfg, k_moe_decode<8>, a);
-    else if (a.P.ring == 4) e = cudaLaunchKernelEx(&cfg, k_moe_decode<4>, a);
-    else e = cudaLaunchKernelEx(&cfg, k_moe_decode<2>, a);
+    // (an MXFP8 ring of 2112-byte slots holds at most 4 per warp in the shared-memory budget)
+    const int R = a.P.ring, F = a.P.mx;
+    if (F == 2) e = cudaLaunchKernelEx(&cfg, R >= 4 ? k_moe_decode<4, 2> : k_moe_decode<2, 2>, a);
+    else if (F == 1)
+        e = cudaLaunchKernelEx(&cfg, R == 16 ? k_moe_decode<16, 1> : R == 8 ? k_moe_decode<8, 1> :
+                                     R == 4 ? k_moe_decode<4, 1> : k_moe_decode<2, 1>, a);
+    else
+        e = cudaLaunchKernelEx(&cfg, R == 16 ? k_moe_decode<16, 0> : R == 8 ? k_moe_decode<8, 0> :
+                                     R == 4 ? k_moe_decode<4, 0> : k_moe_decode<2, 0>, a);
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
     return check_launch(fn);
 }
