@@ -90,6 +90,7 @@ struct PfGemmArgs {
     const int32_t* e2s;      // optional expert -> weight index (slot table); validated by the plan
     const int4* tinfo;       // [tiles] {expert, first permuted row, real rows, 0}
     float* y;                // optional [T*k][H] fp32 per-row expert outputs (tensor scale applied, no routing weight)
+    int cstage;              // resident kernel, down GEMM: 1 = the combine goes through a shared-memory transpose
 };
 
 // weight index of expert e (identity without a slot table; the plan has checked every expert with rows)
@@ -452,6 +453,43 @@ __device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t 
                      : "memory");
 }
 
+// The same combine with coalesced reductions.  A thread holds 32 columns of one token row, so the warp's direct
+// reductions touch 32 rows with 16 bytes each.  Here the warp's 32 rows x 32 columns, already scaled by each
+// row's w * tsd, pass through a per-warp shared-memory block (32 rows, row stride CST_LD floats) in two halves of
+// 16 columns; read back with four lanes per row, each reduction instruction covers 64 contiguous bytes of eight
+// output rows.  Row stride 20 floats: both the row-wise writes and the column-wise reads take the minimum of four
+// shared-memory wavefronts per 512 bytes.
+namespace pf {
+constexpr int CST_LD = 20;
+constexpr size_t CST_BYTES = (size_t)EPI_WARPS * 32 * CST_LD * 4;  // 40 KB for the 16 epilogue warps
+}  // namespace pf
+
+__device__ __forceinline__ void epi_combine_staged(const PfGemmArgs& a, const uint32_t (&v)[32], int2 meta, int m,
+                                                   int c0, float tsd, float* st, int lane) {
+    const float wt = meta.x < 0 ? 0.0f : __int_as_float(meta.y) * tsd;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(st + lane * pf::CST_LD + 4 * q) =
+                make_float4(__uint_as_float(v[16 * hh + 4 * q]) * wt, __uint_as_float(v[16 * hh + 4 * q + 1]) * wt,
+                            __uint_as_float(v[16 * hh + 4 * q + 2]) * wt, __uint_as_float(v[16 * hh + 4 * q + 3]) * wt);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 8 * i + (lane >> 2), cq = lane & 3;
+            const int tok = __shfl_sync(0xffffffffu, meta.x, row);
+            const float4 val = *reinterpret_cast<const float4*>(st + row * pf::CST_LD + 4 * cq);
+            if (tok >= 0)
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                                 a.out32 + (int64_t)tok * a.H + m * 128 + c0 + 16 * hh + 4 * cq),
+                             "f"(val.x), "f"(val.y), "f"(val.z), "f"(val.w)
+                             : "memory");
+        }
+        __syncwarp();
+    }
+}
+
 // ---------------------------------------------------------------------------- grouped GEMM
 
 template <int EPI>
@@ -639,6 +677,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
     extern __shared__ __align__(1024) uint8_t pf_smem[];
     uint8_t* btile = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_smem) + 1023) & ~(uintptr_t)1023);
     uint8_t* ring = btile + (size_t)a.KSN * pf::BLK;
+    float* cst = reinterpret_cast<float*>(ring + (size_t)a.nstages * pf::KPS * pf::BLK);  // combine staging (cstage)
     __shared__ __align__(8) unsigned long long full[pf::RES_MAXNS], empty[pf::RES_MAXNS], acc_full[2], acc_empty[2], bfull,
         bfree;
     __shared__ uint32_t tmem_base;
@@ -832,7 +871,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                 __syncwarp();
                 if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pf_su(&acc_empty[buf])) : "memory");
                 if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
-                else epi_combine(a, v, meta, prow, m, c0, t2s);
+                else {
+                    if (a.y) epi_combine(a, v, meta, prow, m, c0, t2s);  // y rows (and the combine, unstaged)
+                    else if (a.cstage) epi_combine_staged(a, v, meta, m, c0, t2s, cst + (warp - 2) * 32 * pf::CST_LD, lane);
+                    else epi_combine(a, v, meta, prow, m, c0, t2s);
+                }
             }
         }
     }
@@ -929,15 +972,23 @@ template <int EPI>
 static void launch_pf_gemm(PfGemmArgs g, int G, cudaStream_t s) {
     const size_t tile = (size_t)g.KSN * pf::BLK, stage = (size_t)pf::KPS * pf::BLK;
     int ns = 0;
+    size_t extra = 0;
+    g.cstage = 0;
     if (g.KSN <= pf::RES_MAXKSN && tile + 1024 < pf::SMEM_LIMIT) {
-        const int by_smem = (int)((pf::SMEM_LIMIT - 1024 - tile) / stage);
         const int by_tmem = (int)((pf::TMEM_COLS - 256 - 8 * (uint32_t)g.KSN) / (8 * pf::KPS));
+        // the down GEMM's combine (without y rows) goes through shared memory when two stages still fit beside it
+        if (EPI == 2 && g.out32 && !g.y && tile + 2 * stage + pf::CST_BYTES + 1024 <= pf::SMEM_LIMIT) {
+            g.cstage = 1;
+            extra = pf::CST_BYTES;
+        }
+        const int by_smem = (int)((pf::SMEM_LIMIT - 1024 - tile - extra) / stage);
         ns = std::min({by_smem, by_tmem, pf::RES_MAXNS});
     }
     if (ns >= 2) {
         g.nstages = ns;
-        k_pf_gemm_res<EPI><<<G, pf::THREADS, tile + (size_t)ns * stage + 1024, s>>>(g);
+        k_pf_gemm_res<EPI><<<G, pf::THREADS, tile + (size_t)ns * stage + extra + 1024, s>>>(g);
     } else {
+        g.cstage = 0;
         k_pf_gemm_stream<EPI><<<G, pf::THREADS, pf::SMEM, s>>>(g);
     }
 }

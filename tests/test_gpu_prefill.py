@@ -101,6 +101,17 @@ def test_one_expert_spanning_several_tiles():
     check(cfg, lw, mod, out, logits, x_bits)
 
 
+@pytest.mark.parametrize("I", [1536, 2048])
+def test_wide_intermediate(I):
+    """Intermediate 1536 (the down GEMM's token tile leaves room for two ring stages and the combine's
+    shared-memory transpose) and 2048 (it does not: the combine reduces straight from the thread's row)."""
+    cfg = W.scaled(W.CONFIGS["tiny"], I=I, E=4, T=200)
+    lw = weights(cfg, 0)
+    logits, x_bits = W.router_logits(cfg, 0, 3), W.activations_bf16(cfg, 0, 3)
+    mod, out = run(cfg, lw, logits, x_bits)
+    check(cfg, lw, mod, out, logits, x_bits)
+
+
 def boundary_tokens(offsets, perm, k, heavy=10, extra=256, seed=0):
     """Tokens whose expert rows include every expert's first and last permuted row and every row of the last
     (partial) 128-row tile of the `heavy` experts with the most rows, plus a seeded sample up to `extra` more."""
