@@ -90,7 +90,8 @@ struct PfGemmArgs {
     const int32_t* e2s;      // optional expert -> weight index (slot table); validated by the plan
     const int4* tinfo;       // [tiles] {expert, first permuted row, real rows, 0}
     float* y;                // optional [T*k][H] fp32 per-row expert outputs (tensor scale applied, no routing weight)
-    int cstage;              // resident kernel, down GEMM: 1 = the combine goes through a shared-memory transpose
+    int cstage;              // resident kernel, down GEMM: 32 or 16 = the combine goes through a shared-memory
+                             // transpose, that many columns per pass; 0 = reductions straight from the thread's row
 };
 
 // weight index of expert e (identity without a slot table; the plan has checked every expert with rows)
@@ -455,34 +456,39 @@ __device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t 
 
 // The same combine with coalesced reductions.  A thread holds 32 columns of one token row, so the warp's direct
 // reductions touch 32 rows with 16 bytes each.  Here the warp's 32 rows x 32 columns, already scaled by each
-// row's w * tsd, pass through a per-warp shared-memory block (32 rows, row stride CST_LD floats) in two halves of
-// 16 columns; read back with four lanes per row, each reduction instruction covers 64 contiguous bytes of eight
-// output rows.  Row stride 20 floats: both the row-wise writes and the column-wise reads take the minimum of four
-// shared-memory wavefronts per 512 bytes.
+// row's w * tsd, pass through a per-warp shared-memory block (32 rows, row stride LD floats) in 32 / CW passes of
+// CW columns; read back with CW / 4 lanes per row, each reduction instruction covers 4 CW contiguous bytes of
+// 128 / CW output rows (whole 128-byte lines for CW = 32).  Row strides 36 (CW = 32) and 20 (CW = 16) floats:
+// both the row-wise writes and the column-wise reads take the minimum of four shared-memory wavefronts per
+// 512 bytes.
 namespace pf {
-constexpr int CST_LD = 20;
-constexpr size_t CST_BYTES = (size_t)EPI_WARPS * 32 * CST_LD * 4;  // 40 KB for the 16 epilogue warps
+template <int CW>
+constexpr int cst_ld() { return CW == 32 ? 36 : 20; }
+template <int CW>
+constexpr size_t cst_bytes() { return (size_t)EPI_WARPS * 32 * cst_ld<CW>() * 4; }  // 72 KB (CW 32), 40 KB (CW 16)
 }  // namespace pf
 
+template <int CW>
 __device__ __forceinline__ void epi_combine_staged(const PfGemmArgs& a, const uint32_t (&v)[32], int2 meta, int m,
                                                    int c0, float tsd, float* st, int lane) {
+    constexpr int LD = pf::cst_ld<CW>(), LPR = CW / 4, RPI = 32 / LPR;  // lanes per row, rows per instruction
     const float wt = meta.x < 0 ? 0.0f : __int_as_float(meta.y) * tsd;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    for (int hh = 0; hh < 32 / CW; ++hh) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(st + lane * pf::CST_LD + 4 * q) =
-                make_float4(__uint_as_float(v[16 * hh + 4 * q]) * wt, __uint_as_float(v[16 * hh + 4 * q + 1]) * wt,
-                            __uint_as_float(v[16 * hh + 4 * q + 2]) * wt, __uint_as_float(v[16 * hh + 4 * q + 3]) * wt);
+        for (int q = 0; q < CW / 4; ++q)
+            *reinterpret_cast<float4*>(st + lane * LD + 4 * q) =
+                make_float4(__uint_as_float(v[CW * hh + 4 * q]) * wt, __uint_as_float(v[CW * hh + 4 * q + 1]) * wt,
+                            __uint_as_float(v[CW * hh + 4 * q + 2]) * wt, __uint_as_float(v[CW * hh + 4 * q + 3]) * wt);
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = 8 * i + (lane >> 2), cq = lane & 3;
+        for (int i = 0; i < 32 / RPI; ++i) {
+            const int row = RPI * i + lane / LPR, cq = lane % LPR;
             const int tok = __shfl_sync(0xffffffffu, meta.x, row);
-            const float4 val = *reinterpret_cast<const float4*>(st + row * pf::CST_LD + 4 * cq);
+            const float4 val = *reinterpret_cast<const float4*>(st + row * LD + 4 * cq);
             if (tok >= 0)
                 asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
-                                 a.out32 + (int64_t)tok * a.H + m * 128 + c0 + 16 * hh + 4 * cq),
+                                 a.out32 + (int64_t)tok * a.H + m * 128 + c0 + CW * hh + 4 * cq),
                              "f"(val.x), "f"(val.y), "f"(val.z), "f"(val.w)
                              : "memory");
         }
@@ -873,7 +879,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                 if (EPI == 1) epi_swiglu(a, v, m, ntg, r, c0, t0s, t1s);
                 else {
                     if (a.y) epi_combine(a, v, meta, prow, m, c0, t2s);  // y rows (and the combine, unstaged)
-                    else if (a.cstage) epi_combine_staged(a, v, meta, m, c0, t2s, cst + (warp - 2) * 32 * pf::CST_LD, lane);
+                    else if (a.cstage == 32)
+                        epi_combine_staged<32>(a, v, meta, m, c0, t2s, cst + (warp - 2) * 32 * pf::cst_ld<32>(), lane);
+                    else if (a.cstage == 16)
+                        epi_combine_staged<16>(a, v, meta, m, c0, t2s, cst + (warp - 2) * 32 * pf::cst_ld<16>(), lane);
                     else epi_combine(a, v, meta, prow, m, c0, t2s);
                 }
             }
@@ -977,9 +986,15 @@ static void launch_pf_gemm(PfGemmArgs g, int G, cudaStream_t s) {
     if (g.KSN <= pf::RES_MAXKSN && tile + 1024 < pf::SMEM_LIMIT) {
         const int by_tmem = (int)((pf::TMEM_COLS - 256 - 8 * (uint32_t)g.KSN) / (8 * pf::KPS));
         // the down GEMM's combine (without y rows) goes through shared memory when two stages still fit beside it
-        if (EPI == 2 && g.out32 && !g.y && tile + 2 * stage + pf::CST_BYTES + 1024 <= pf::SMEM_LIMIT) {
-            g.cstage = 1;
-            extra = pf::CST_BYTES;
+        if (EPI == 2 && g.out32 && !g.y) {
+            for (int cw : {32, 16}) {
+                const size_t b = cw == 32 ? pf::cst_bytes<32>() : pf::cst_bytes<16>();
+                if (tile + 2 * stage + b + 1024 <= pf::SMEM_LIMIT) {
+                    g.cstage = cw;
+                    extra = b;
+                    break;
+                }
+            }
         }
         const int by_smem = (int)((pf::SMEM_LIMIT - 1024 - tile - extra) / stage);
         ns = std::min({by_smem, by_tmem, pf::RES_MAXNS});

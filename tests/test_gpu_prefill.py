@@ -104,7 +104,8 @@ def test_one_expert_spanning_several_tiles():
 @pytest.mark.parametrize("I", [1536, 2048])
 def test_wide_intermediate(I):
     """Intermediate 1536 (the down GEMM's token tile leaves room for two ring stages and the combine's
-    shared-memory transpose) and 2048 (it does not: the combine reduces straight from the thread's row)."""
+    shared-memory transpose in 16-column passes; the other shapes here take 32-column passes) and 2048 (no room:
+    the combine reduces straight from the thread's row)."""
     cfg = W.scaled(W.CONFIGS["tiny"], I=I, E=4, T=200)
     lw = weights(cfg, 0)
     logits, x_bits = W.router_logits(cfg, 0, 3), W.activations_bf16(cfg, 0, 3)
