@@ -90,6 +90,7 @@ struct PfGemmArgs {
     const int32_t* e2s;      // optional expert -> weight index (slot table); validated by the plan
     const int4* tinfo;       // [tiles] {expert, first permuted row, real rows, 0}
     float* y;                // optional [T*k][H] fp32 per-row expert outputs (tensor scale applied, no routing weight)
+    int parts;               // resident kernel: work items per token tile, each a contiguous part of the weight tiles
     int cstage;              // resident kernel, down GEMM: 32 or 16 = the combine goes through a shared-memory
                              // transpose, that many columns per pass; 0 = reductions straight from the thread's row
 };
@@ -159,17 +160,6 @@ __device__ __forceinline__ void mma_fp4(uint32_t dcol, uint64_t da, uint64_t db,
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(dcol),
         "l"(da), "l"(db), "r"(kIdesc), "r"(sfa), "r"(sfb), "r"(acc));
-}
-
-__device__ __forceinline__ int pf_find_expert(const int32_t* tile_off, int E, int v) {
-    // largest e in [0, E) with tile_off[e] <= v
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(tile_off + mid) <= v) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -301,7 +291,7 @@ __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restr
 // or not) first zeroes its share of the fp32 output accumulator (n4 float4s in
 // all), which the down GEMM's combine adds into: the stores overlap the
 // block's first dependent loads.
-__global__ void __launch_bounds__(256, 2) k_pf_gather_x(const uint8_t* __restrict__ xc, int H, int k, int E,
+__global__ void __launch_bounds__(256, 4) k_pf_gather_x(const uint8_t* __restrict__ xc, int H, int k, int E,
                                                      const int32_t* __restrict__ perm, const float* __restrict__ w,
                                                      const int32_t* __restrict__ tile_off, const int4* __restrict__ tinfo,
                                                      uint8_t* __restrict__ xq, int2* __restrict__ rowmeta,
@@ -334,22 +324,27 @@ __global__ void __launch_bounds__(256, 2) k_pf_gather_x(const uint8_t* __restric
     uint8_t* tile = xq + (int64_t)rt * KSN * pf::BLK;
     // codes: lanes 8a .. 8a+7 take eight consecutive rows of one 16-byte piece, i.e. one whole
     // 128-byte line of the tile; thread t: row t & 7 of each 8-row group, pieces t >> 3, +32, ...
-    // All sixteen row groups of a piece are loaded before any is stored, so each thread keeps
-    // sixteen loads in flight (no runtime division either: this copy is instruction-heavy).
+    // Eight row groups of a piece are loaded before any is stored, so each thread keeps eight loads
+    // in flight with few enough registers for four blocks per SM (no runtime division either: this
+    // copy is instruction-heavy).
     {
         const int r_lo = tid & 7, pc0 = tid >> 3, pstep = blockDim.x >> 3;
         const int pc_end = (kp + 1) * (pieces / 2);
         for (int pc = kp * (pieces / 2) + pc0; pc < pc_end; pc += pstep) {
-            uint4 v[16];
-#pragma unroll
-            for (int rg = 0; rg < 16; ++rg) {
-                const int tk = s_tok[rg * 8 + r_lo];
-                if (tk >= 0) v[rg] = __ldg(reinterpret_cast<const uint4*>(xc + (int64_t)tk * rowb) + pc);
-            }
             uint8_t* dst = tile + (pc >> 2) * pf::BLK + blk_code_off(r_lo, (pc & 3) * 16);
 #pragma unroll
-            for (int rg = 0; rg < 16; ++rg)
-                if (s_tok[rg * 8 + r_lo] >= 0) *reinterpret_cast<uint4*>(dst + rg * 128) = v[rg];
+            for (int h8 = 0; h8 < 2; ++h8) {
+                uint4 v[8];
+#pragma unroll
+                for (int rg = 0; rg < 8; ++rg) {
+                    const int tk = s_tok[(8 * h8 + rg) * 8 + r_lo];
+                    if (tk >= 0) v[rg] = __ldg(reinterpret_cast<const uint4*>(xc + (int64_t)tk * rowb) + pc);
+                }
+#pragma unroll
+                for (int rg = 0; rg < 8; ++rg)
+                    if (s_tok[(8 * h8 + rg) * 8 + r_lo] >= 0)
+                        *reinterpret_cast<uint4*>(dst + (8 * h8 + rg) * 128) = v[rg];
+            }
         }
     }
     // scale words: a warp covers rows (r & 7) + 32 (r >> 5), one 128-byte line; thread t: row
@@ -463,9 +458,9 @@ __device__ __forceinline__ void epi_combine(const PfGemmArgs& a, const uint32_t 
 // 512 bytes.
 namespace pf {
 template <int CW>
-constexpr int cst_ld() { return CW == 32 ? 36 : 20; }
+__host__ __device__ constexpr int cst_ld() { return CW == 32 ? 36 : 20; }
 template <int CW>
-constexpr size_t cst_bytes() { return (size_t)EPI_WARPS * 32 * cst_ld<CW>() * 4; }  // 72 KB (CW 32), 40 KB (CW 16)
+__host__ __device__ constexpr size_t cst_bytes() { return (size_t)EPI_WARPS * 32 * cst_ld<CW>() * 4; }  // 72 KB (CW 32), 40 KB (CW 16)
 }  // namespace pf
 
 template <int CW>
@@ -533,7 +528,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
     // decode item i -> (expert, m tile, global token tile)
     auto item = [&](int i, int& e, int& m, int& ntg) {
         const int v = i / a.MT;
-        e = pf_find_expert(a.tile_off, a.E, v);
+        e = __ldg(a.tinfo + v).x;
         const int t0 = __ldg(a.tile_off + e), nt = __ldg(a.tile_off + e + 1) - t0;
         const int local = i - a.MT * t0;
         m = local / nt;
@@ -663,19 +658,19 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
     }
 }
 
-// Resident-token-tile variant (K <= 2048): a work item is (token tile, half of
-// the weight row tiles).  The token tile's K blocks are copied once into shared
+// Resident-token-tile variant (K <= 2048): a work item is (token tile, a part of
+// the weight row tiles: all of them for gate/up, half for down).  The token tile's K blocks are copied once into shared
 // memory and stay there (scale factors copied once into TMEM) while the item's
 // weight tiles stream through the ring, KPS blocks per stage: half as many bulk
 // copies per token tile as streaming both operands.
-__device__ __forceinline__ bool pf_res_item(const PfGemmArgs& a, int i, int& e, int& ntg, int& mlo, int& mhi) {
-    ntg = i >> 1;
-    const int mh = (a.MT + 1) >> 1;
-    mlo = (i & 1) ? mh : 0;
-    mhi = (i & 1) ? a.MT : mh;
-    if (mlo >= mhi) return false;
-    e = pf_find_expert(a.tile_off, a.E, ntg);
-    return true;
+// The item's token tile and weight-tile range; its expert (tinfo[ntg].x) is loaded only by the roles that need it,
+// so the MMA issuer's per-item work has no global load.
+__device__ __forceinline__ bool pf_res_item(const PfGemmArgs& a, int i, int& ntg, int& mlo, int& mhi) {
+    ntg = i / a.parts;
+    const int part = i - ntg * a.parts, per = (a.MT + a.parts - 1) / a.parts;
+    mlo = part * per;
+    mhi = min(a.MT, mlo + per);
+    return mlo < mhi;
 }
 
 template <int EPI>
@@ -717,7 +712,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tbase = tmem_base;
-    const int n_items = 2 * __ldg(a.tile_off + a.E);
+    const int n_items = a.parts * __ldg(a.tile_off + a.E);
     const uint32_t tile_bytes = (uint32_t)a.KSN * pf::BLK;
     int bfree_commits = 0;  // MMA thread: token-tile releases committed
 
@@ -726,8 +721,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
         if (lane == 0) {
             int sc = 0, bi = 0;
             for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-                int e, ntg, mlo, mhi;
-                if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
+                int ntg, mlo, mhi;
+                if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
                 // the token tile, once the previous item's MMAs have read the last one
                 if (bi > 0 && !pf_wait(&bfree, (bi - 1) & 1, abort_flag)) break;
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&bfull)), "r"(tile_bytes)
@@ -737,7 +732,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                         pf_su(btile)), "l"(a.B + (int64_t)ntg * a.KSN * pf::BLK), "r"(tile_bytes), "r"(pf_su(&bfull))
                     : "memory");
                 ++bi;
-                const uint8_t* ae = a.A + pf_widx(a, e) * a.a_stride;
+                const uint8_t* ae = a.A + pf_widx(a, __ldg(a.tinfo + ntg).x) * a.a_stride;
                 bool stop = false;
                 for (int m = mlo; m < mhi && !stop; ++m) {
                     // warm L2 with the item's next weight tile, or with the next item's token tile,
@@ -747,7 +742,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                                      "r"(tile_bytes) : "memory");
                     } else if (i + (int)gridDim.x < n_items) {
                         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                                         a.B + (int64_t)((i + (int)gridDim.x) >> 1) * a.KSN * pf::BLK),
+                                         a.B + (int64_t)((i + (int)gridDim.x) / a.parts) * a.KSN * pf::BLK),
                                      "r"(tile_bytes) : "memory");
                     }
                     for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
@@ -786,8 +781,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
             const uint64_t dW0 = umma_desc(ring, 2048, 128), sW0 = umma_desc(ring + 8192, 0, 128);
             const uint64_t dT0 = umma_desc(btile, 2048, 128), sT0 = umma_desc(btile + 8192, 0, 128);
             for (int i = blockIdx.x; i < n_items && !stop && !*abort_flag; i += gridDim.x) {
-                int e, ntg, mlo, mhi;
-                if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
+                int ntg, mlo, mhi;
+                if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
                 if (!pf_wait(&bfull, bi & 1, abort_flag)) break;
                 ++bi;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -852,9 +847,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
         int it = 0;
         bool stop = false;
         for (int i = blockIdx.x; i < n_items && !stop; i += gridDim.x) {
-            int e, ntg, mlo, mhi;
-            if (!pf_res_item(a, i, e, ntg, mlo, mhi)) continue;
-            const float* ts = a.tscale + pf_widx(a, e) * a.ts_stride;
+            int ntg, mlo, mhi;
+            if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
+            const float* ts = a.tscale + pf_widx(a, __ldg(a.tinfo + ntg).x) * a.ts_stride;
             const float t0s = __ldg(ts + 0), t1s = __ldg(ts + 1), t2s = __ldg(ts + 2);
             int2 meta = make_int2(-1, 0);
             int prow = -1;  // permuted row of this token row of the tile (y output)
@@ -1001,6 +996,7 @@ static void launch_pf_gemm(PfGemmArgs g, int G, cudaStream_t s) {
     }
     if (ns >= 2) {
         g.nstages = ns;
+        g.parts = EPI == 1 ? 1 : 2;  // measured: whole token tiles for gate/up (one token-tile load each), halves for down
         k_pf_gemm_res<EPI><<<G, pf::THREADS, tile + (size_t)ns * stage + extra + 1024, s>>>(g);
     } else {
         g.cstage = 0;

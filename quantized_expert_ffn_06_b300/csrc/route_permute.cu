@@ -222,25 +222,25 @@ __global__ void __launch_bounds__(1024) k_permute_hist(const int32_t* __restrict
     for (int e = tid; e < E; e += blockDim.x) chunk_cnt[(int64_t)blockIdx.x * E + e] = cnt[e];
 }
 
+// One thread per expert: its chunk counts are loaded 32 at a time (independent loads, one round trip per 32
+// chunks) and summed; after the block scan of the totals, the per-chunk bases are written once (from registers
+// when there are at most 32 chunks, else from a second pass of loads).
 __global__ void __launch_bounds__(1024) k_permute_scan(int32_t* __restrict__ chunk_cnt, int nchunks, int n, int E,
                                                        int32_t* __restrict__ offsets, int32_t* __restrict__ active) {
+    constexpr int G = 32;
     __shared__ int tot[1024];
     __shared__ int flag[1024];
     __shared__ int warp_tot[33];
     const int tid = threadIdx.x;
     int has = 0;
+    int v[G];
     if (tid < E) {
         int run = 0;
-        for (int c0 = 0; c0 < nchunks; c0 += 8) {  // exclusive scan over chunks for this expert
-            int v[8];
+        for (int c0 = 0; c0 < nchunks; c0 += G) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = (c0 + u < nchunks) ? chunk_cnt[(int64_t)(c0 + u) * E + tid] : 0;
+            for (int u = 0; u < G; ++u) v[u] = (c0 + u < nchunks) ? chunk_cnt[(int64_t)(c0 + u) * E + tid] : 0;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (c0 + u < nchunks) {
-                    chunk_cnt[(int64_t)(c0 + u) * E + tid] = run;
-                    run += v[u];
-                }
+            for (int u = 0; u < G; ++u) run += v[u];
         }
         tot[tid] = run;
         has = run > 0;
@@ -249,14 +249,26 @@ __global__ void __launch_bounds__(1024) k_permute_scan(int32_t* __restrict__ chu
     __syncthreads();
     block_exclusive_scan(tot, E, warp_tot);
     if (tid < E) {
-        offsets[tid] = tot[tid];
-        for (int c0 = 0; c0 < nchunks; c0 += 8) {
-            int v[8];
+        int base = tot[tid];
+        offsets[tid] = base;
+        if (nchunks <= G) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = (c0 + u < nchunks) ? chunk_cnt[(int64_t)(c0 + u) * E + tid] : 0;
+            for (int u = 0; u < G; ++u)
+                if (u < nchunks) {
+                    chunk_cnt[(int64_t)u * E + tid] = base;
+                    base += v[u];
+                }
+        } else {
+            for (int c0 = 0; c0 < nchunks; c0 += G) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (c0 + u < nchunks) chunk_cnt[(int64_t)(c0 + u) * E + tid] = v[u] + tot[tid];
+                for (int u = 0; u < G; ++u) v[u] = (c0 + u < nchunks) ? chunk_cnt[(int64_t)(c0 + u) * E + tid] : 0;
+#pragma unroll
+                for (int u = 0; u < G; ++u)
+                    if (c0 + u < nchunks) {
+                        chunk_cnt[(int64_t)(c0 + u) * E + tid] = base;
+                        base += v[u];
+                    }
+            }
         }
     }
     if (tid == 0) offsets[E] = n;

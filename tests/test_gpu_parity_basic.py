@@ -187,7 +187,7 @@ def test_route_argument_errors():
 # ---------------------------------------------------------------- permutation
 
 @pytest.mark.parametrize("T,E,k", [(4, 8, 2), (1, 256, 8), (16, 256, 8), (128, 256, 8), (4096, 256, 8), (3000, 64, 6),
-                                   (1, 1024, 32)])
+                                   (1, 1024, 32), (8192, 256, 8), (5000, 64, 7)])
 def test_permute_bit_exact(T, E, k):
     cfg = W.scaled(W.CONFIGS["prefill_35b"], T=T, E=E)
     logits = W.router_logits(cfg, 0, 0) if E == 256 else W.normal_f32(W.logit_stream(8, E, T), T * E).reshape(T, E)
