@@ -319,62 +319,66 @@ __global__ void __launch_bounds__(256, 4) k_pf_gather_x(const uint8_t* __restric
         s_tok[tid] = t;
     }
     __syncthreads();
-    const int KSN = H / 128, pieces = H / 32, words = H / 64;  // per row: 16-byte code pieces, 4-byte scale words
+    const int KSN = H / 128, pieces = H / 32;  // per row: 16-byte code pieces
     const int64_t rowb = H / 2 + H / 16;
     uint8_t* tile = xq + (int64_t)rt * KSN * pf::BLK;
     // codes: lanes 8a .. 8a+7 take eight consecutive rows of one 16-byte piece, i.e. one whole
-    // 128-byte line of the tile; thread t: row t & 7 of each 8-row group, pieces t >> 3, +32, ...
-    // Eight row groups of a piece are loaded before any is stored, so each thread keeps eight loads
-    // in flight with few enough registers for four blocks per SM (no runtime division either: this
-    // copy is instruction-heavy).
+    // 128-byte line of the tile; thread t: row t & 7 of the eight row groups 8 ((t >> 3) & 1) .., and
+    // a pair of adjacent pieces (one 32-byte sector of the source row, so the second load is served
+    // by L1 and L2 sees one request per sector), pairs t >> 4, +16, ...  Four row groups are loaded
+    // before any is stored (eight loads in flight, few enough registers for four blocks per SM; no
+    // runtime division either: this copy is instruction-heavy).
     {
-        const int r_lo = tid & 7, pc0 = tid >> 3, pstep = blockDim.x >> 3;
-        const int pc_end = (kp + 1) * (pieces / 2);
-        for (int pc = kp * (pieces / 2) + pc0; pc < pc_end; pc += pstep) {
+        const int r_lo = tid & 7, rgh = (tid >> 3) & 1, npair = H / 128;  // pairs of pieces in this half
+        for (int pp = tid >> 4; pp < npair; pp += blockDim.x >> 4) {
+            const int pc = kp * (pieces / 2) + 2 * pp;  // even: both pieces lie in one K block
             uint8_t* dst = tile + (pc >> 2) * pf::BLK + blk_code_off(r_lo, (pc & 3) * 16);
 #pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                uint4 v[8];
+            for (int hb = 0; hb < 2; ++hb) {
+                uint4 v0[4], v1[4];
 #pragma unroll
-                for (int rg = 0; rg < 8; ++rg) {
-                    const int tk = s_tok[(8 * h8 + rg) * 8 + r_lo];
-                    if (tk >= 0) v[rg] = __ldg(reinterpret_cast<const uint4*>(xc + (int64_t)tk * rowb) + pc);
+                for (int j = 0; j < 4; ++j) {
+                    const int tk = s_tok[(rgh * 8 + hb * 4 + j) * 8 + r_lo];
+                    if (tk >= 0) {
+                        const uint4* src = reinterpret_cast<const uint4*>(xc + (int64_t)tk * rowb) + pc;
+                        v0[j] = __ldg(src);
+                        v1[j] = __ldg(src + 1);
+                    }
                 }
 #pragma unroll
-                for (int rg = 0; rg < 8; ++rg)
-                    if (s_tok[(8 * h8 + rg) * 8 + r_lo] >= 0)
-                        *reinterpret_cast<uint4*>(dst + (8 * h8 + rg) * 128) = v[rg];
+                for (int j = 0; j < 4; ++j) {
+                    const int rg = rgh * 8 + hb * 4 + j;
+                    if (s_tok[rg * 8 + r_lo] >= 0) {
+                        *reinterpret_cast<uint4*>(dst + rg * 128) = v0[j];
+                        *reinterpret_cast<uint4*>(dst + rg * 128 + 2048) = v1[j];
+                    }
+                }
             }
         }
     }
-    // scale words: a warp covers rows (r & 7) + 32 (r >> 5), one 128-byte line; thread t: row
-    // (t & 7) + 32 ((t >> 3) & 3) + 8 rb, words t >> 5, +8, ...; up to four words of each of the
-    // four rows are loaded before any is stored
+    // scale words: two threads per row (t >> 1), each loading its half of this half-row's H / 128
+    // words as 16-byte pieces (4-byte words when H / 256 is not a multiple of four) and storing
+    // every word where the tile layout puts it
     {
-        const int r_base = (tid & 7) + 32 * ((tid >> 3) & 3), w0 = tid >> 5, wstep = blockDim.x >> 5;
-        const uint32_t* src[4];
+        const int r = tid >> 1, tk = s_tok[r], wpt = H / 256, w0 = kp * (H / 128) + (tid & 1) * wpt;
+        if (tk >= 0) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(xc + (int64_t)tk * rowb + H / 2) + w0;
+            if ((wpt & 3) == 0) {
+                for (int c = 0; c < wpt; c += 4) {
+                    const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + c));
+                    const uint32_t ww[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int rb = 0; rb < 4; ++rb) {
-            const int tk = s_tok[r_base + 8 * rb];
-            src[rb] = tk < 0 ? nullptr : reinterpret_cast<const uint32_t*>(xc + (int64_t)tk * rowb + H / 2);
-        }
-        const int wd_end = (kp + 1) * (words / 2);
-        for (int wd0 = kp * (words / 2) + w0; wd0 < wd_end; wd0 += 4 * wstep) {
-            uint32_t v[4][4];
-#pragma unroll
-            for (int rb = 0; rb < 4; ++rb)
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    if (src[rb] != nullptr && wd0 + m * wstep < wd_end) v[rb][m] = __ldg(src[rb] + wd0 + m * wstep);
-#pragma unroll
-            for (int rb = 0; rb < 4; ++rb)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int wd = wd0 + m * wstep;
-                    if (src[rb] != nullptr && wd < wd_end)
-                        *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK +
-                                                     blk_scale_off(r_base + 8 * rb, (wd & 1) * 4)) = v[rb][m];
+                    for (int u = 0; u < 4; ++u) {
+                        const int wd = w0 + c + u;
+                        *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK + blk_scale_off(r, (wd & 1) * 4)) = ww[u];
+                    }
                 }
+            } else {
+                for (int c = 0; c < wpt; ++c) {
+                    const int wd = w0 + c;
+                    *reinterpret_cast<uint32_t*>(tile + (wd >> 1) * pf::BLK + blk_scale_off(r, (wd & 1) * 4)) = __ldg(src + c);
+                }
+            }
         }
     }
     if (kp == 0 && tid < 128) rowmeta[(int64_t)rt * 128 + tid] = make_int2(t, __float_as_int(wt));
