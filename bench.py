@@ -696,9 +696,12 @@ def run_gpu_prefill(args, ws, rank, local):
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     NW = 4  # weight sets rotated between steps: 4 x the layer's weights, far beyond L2
     S = min(args.distinct_steps, 4)
+    if args.weights == "mxfp8":
+        raise SystemExit("the tensor-core prefill takes NVFP4 or MXFP4 weights")
+    mx4 = args.weights == "mxfp4"  # MXFP4 re-encoded exactly into the FP4 tensor-core tiles
     weights = []
     for l in range(NW):
-        lw = LayerWeights(E, H, I, dev, layout=Q.FT_LAYOUT_UMMA_TILES)
+        lw = LayerWeights(E, H, I, dev, layout=Q.FT_LAYOUT_UMMA_TILES, source=args.weights)
         lw.fill_synthetic(lambda e, p, l=l: W.w_stream(cfg.weight_cfg, l, e, p), sigma=cfg.w_sigma)
         weights.append(lw)
     step0 = rank * S
@@ -803,11 +806,14 @@ def run_gpu_prefill(args, ws, rank, local):
     return {
         "metric": METRIC, "value": flops * ws / step_s / 1e12, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "nvfp4 x nvfp4 (E2M1, UE4M3 per 16), fp32 accumulate",
+        "vs_baseline": None,
+        "dtype": ("mxfp4 weights (UE8M0 per 32, re-encoded exactly as power-of-two UE4M3 per 16) x nvfp4 activations, "
+                  "fp32 accumulate" if mx4 else "nvfp4 x nvfp4 (E2M1, UE4M3 per 16), fp32 accumulate"),
         "data": "synthetic (seeded Philox4x32-10, Zipf(1.1) expert popularity)",
         "tok_per_s": T * ws / step_s,
         "config": {"workload": f"{cfg.name}: one MoE layer, hidden {H}, {E} experts, top-{k}, intermediate {I}, "
-                               f"{T} prompt tokens, NVFP4 weights and activations",
+                               f"{T} prompt tokens, " + ("MXFP4 weights, NVFP4 activations" if mx4 else
+                                                         "NVFP4 weights and activations"),
                    "global_batch": T * ws,
                    "l2": f"inputs larger than L2: {NW} weight sets of {touched * cfg.expert_bytes / 1e6:.0f} MB "
                          f"rotated between steps",
@@ -817,8 +823,8 @@ def run_gpu_prefill(args, ws, rank, local):
                      "kernel": "ft_moe_expert_ffn_nvfp4_prefill (plan, x quantisation, gate/up and down grouped "
                                "GEMMs, output), timed as one call",
                      "bytes_per_launch": bytes_ffn, "avg_launch_us": ffn_s * 1e6,
-                     "traffic": profiled_traffic(cfg.name, kernel_source_hash(PREFILL_SOURCES), "k_pf_ffn",
-                                                 "dram_bytes_per_call"),
+                     "traffic": profiled_traffic(cfg.name + ("_mxfp4" if mx4 else ""),
+                                                 kernel_source_hash(PREFILL_SOURCES), "k_pf_ffn", "dram_bytes_per_call"),
                      "traffic_what": "DRAM bytes read + written by the FFN call's kernels (plan, x quantisation, "
                                      "gather, both GEMMs, output), from the committed ncu launch list"},
         "attainable": {"tflops": attainable, "frac": flops / ffn_s / 1e12 / attainable,
@@ -844,6 +850,8 @@ def run_gpu_prefill_stream(args, ws, rank, local):
     dev = torch.device("cuda", local)
     cfg = bench_config(args)
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    if args.weights != "nvfp4":
+        raise SystemExit("--stream-layers streams NVFP4 layers")
     L = args.stream_layers
     sp = StreamedPrefill(L, E, H, I, k, T, dev)
     scratch = LayerWeights(E, H, I, dev, layout=Q.FT_LAYOUT_UMMA_TILES)
@@ -1099,7 +1107,7 @@ def main():
     ap.add_argument("--prefetch-source", default="router", choices=["router", "next"],
                     help="cache stream: predictions from the router's ranks, or the next token's experts (exact)")
     ap.add_argument("--weights", default="nvfp4", choices=["nvfp4", "mxfp4", "mxfp8"],
-                    help="decode configs: expert weight format of the fused layer step")
+                    help="expert weight format: decode configs (fused layer step) and the prefill workload (nvfp4, mxfp4)")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="cache stream: install the router's next P ranked experts of each token for the next one")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1187,7 +1195,7 @@ def main():
             torch.distributed.destroy_process_group()
         return
     res = run_gpu(args, ws, rank, local)
-    if args.config == "decode_35b" and not args.no_prefill:
+    if args.config == "decode_35b" and not args.no_prefill and args.weights != "mxfp8":  # no MXFP8 prefill path
         # the same layer shape's 4096-token prefill (grouped FP4 tensor-core GEMMs), measured in the same run
         # after the decode and reported beside it: its own workload, unit and roofline
         import argparse as _ap

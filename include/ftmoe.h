@@ -77,6 +77,7 @@ typedef enum ft_status {
 #define FT_DEVERR_BAD_SCALE 0x2u     /* an E4M3 scale byte was NaN or had its sign bit set */
 #define FT_DEVERR_TIMEOUT 0x4u       /* a bounded device wait gave up */
 #define FT_DEVERR_BAD_INDEX 0x8u     /* an expert id / slot / offset was out of range */
+#define FT_DEVERR_RANGE 0x10u        /* a value had no exact encoding in the target format (ft_mxfp4_pack_umma) */
 
 FT_API const char* ft_status_string(ft_status s);
 /* Message for the last failure on this thread ("" if none).  The pointer stays
@@ -548,6 +549,27 @@ FT_API ft_status ft_mxfp4_quantize_weight(const float* w, int64_t N, int64_t K, 
  * at L*2.  N a multiple of 16, K a multiple of 128.  All pointers (device). */
 FT_API ft_status ft_mxfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
                                      int64_t N, int64_t K, uint8_t* tiles, ft_stream_t stream);
+
+/* MXFP4 weights for the tensor-core prefill [P5 limits: MXFP4 among the
+ * weight formats]: packs a row-major MXFP4 matrix [N][K] (codes [N][K/2] at
+ * byte stride codes_ld, UE8M0 scales [N][K/32] at stride scales_ld) into
+ * FT_LAYOUT_UMMA_TILES, the layout of ft_nvfp4_pack_umma(), and writes the
+ * matrix's fp32 tensor scale to tscale[0 .. ts_count-1] (device).  The E2M1
+ * codes are copied unchanged; the scale 2^(s-127) of each 32-element block
+ * becomes the E4M3 scale 2^(s-s0) of both of its 16-element halves, with
+ * s0 = (largest s over blocks holding a non-zero code) - 8 and tensor scale
+ * 2^(s0-127).  Powers of two from 2^-9 to 2^8 are exact E4M3 values, so every
+ * product code x scale x tensor scale equals the MX one exactly when the
+ * matrix's non-zero blocks span at most 17 octaves (s >= largest s - 17).  A
+ * block beyond that sets FT_DEVERR_RANGE (its scale is written as 0); a scale
+ * byte of 255 (NaN) sets FT_DEVERR_BAD_SCALE.  Blocks whose codes are all
+ * zero get scale 0.  With no non-zero block the tensor scale is 1.  Three
+ * launches on `stream`; tscale[0] serves as their scratch word until the
+ * last.  N and K multiples of 128, 1 <= ts_count <= 4; codes and tiles
+ * 16-byte aligned, codes_ld a multiple of 16, tscale 4-byte aligned. */
+FT_API ft_status ft_mxfp4_pack_umma(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
+                                    int64_t N, int64_t K, uint8_t* tiles, float* tscale, int ts_count,
+                                    ft_stream_t stream);
 
 /* MXFP8 weight quantiser [P5 limits: FP8 among the weight formats; the OCP
  * Microscaling v1.0 MXFP8 format]: as ft_mxfp4_quantize_weight with E4M3

@@ -25,7 +25,7 @@ FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_UNSUPPORTED, FT_ERR_TIMEOUT, FT_E
 FT_LAYOUT_ROWS, FT_LAYOUT_DECODE_TILES, FT_LAYOUT_UMMA_TILES = 0, 1, 2
 FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP4_DECODE_TILES = 3, 4
 FT_LAYOUT_MXFP8_ROWS, FT_LAYOUT_MXFP8_DECODE_TILES = 5, 6
-FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX = 1, 2, 4, 8
+FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX, FT_DEVERR_RANGE = 1, 2, 4, 8, 16
 FT_WAIT_SITE_NONE, FT_WAIT_SITE_DECODE_H = 0, 1
 
 _vp, _i32, _i64, _u64, _sz, _dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t,
@@ -93,6 +93,7 @@ _sig("ft_moe_layer_decode_noalloc", [ctypes.POINTER(ft_moe_layer_weights), _vp, 
 _sig("ft_nvfp4_pack_umma", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_mxfp4_quantize_weight", [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp])
 _sig("ft_mxfp4_pack_tiles", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
+_sig("ft_mxfp4_pack_umma", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _i32, _vp])
 _sig("ft_mxfp8_quantize_weight", [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp])
 _sig("ft_mxfp8_pack_tiles", [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("ft_moe_prefill_workspace_size", [_i32, _i32, _i32, _i32, _i32], _sz)
@@ -277,6 +278,13 @@ def ft_mxfp4_quantize_weight(w: torch.Tensor, codes, scales, codes_ld: int | Non
 
 def ft_mxfp4_pack_tiles(codes, codes_ld: int, scales, scales_ld: int, N: int, K: int, tiles, stream=None):
     _check(_lib.ft_mxfp4_pack_tiles(_p(codes), codes_ld, _p(scales), scales_ld, N, K, _p(tiles), _s(stream)))
+
+
+def ft_mxfp4_pack_umma(codes, codes_ld: int, scales, scales_ld: int, N: int, K: int, tiles, tscale, ts_count: int = 1,
+                       stream=None):
+    """MXFP4 matrix [N][K] -> FT_LAYOUT_UMMA_TILES plus its fp32 tensor scale in tscale[0:ts_count] (device)."""
+    _check(_lib.ft_mxfp4_pack_umma(_p(codes), codes_ld, _p(scales), scales_ld, N, K, _p(tiles), _p(tscale), ts_count,
+                                   _s(stream)))
 
 
 def ft_mxfp8_quantize_weight(w: torch.Tensor, codes, scales, codes_ld: int | None = None, scales_ld: int | None = None,

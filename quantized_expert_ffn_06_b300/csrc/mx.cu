@@ -1,5 +1,6 @@
-// mx.cu -- MX expert weights (MXFP4 and MXFP8): the block quantisers and the
-// packing into the decode kernel's 16-row tiles.
+// mx.cu -- MX expert weights (MXFP4 and MXFP8): the block quantisers, the
+// packing into the decode kernel's 16-row tiles, and the exact re-encoding of
+// MXFP4 into the FP4 tensor-core tiles of the prefill.
 //
 // The page "8GB 笔记本 39.3 tok/s、单卡跑 753B：FreeToken 把 frontier MoE 拉回本地"
 // (section 局限) lists MXFP4 beside NVFP4 and FP8 as the weight formats the
@@ -179,6 +180,81 @@ __global__ void __launch_bounds__(256) k_mx_pack_tiles(const uint8_t* __restrict
     }
 }
 
+// ---------------------------------------------------------------------------- MXFP4 -> FP4 tensor-core tiles
+
+// The UMMA tile layout (the one ft_nvfp4_pack_umma writes): [R][K] in blocks of 128 rows x 128 K, 9216 bytes,
+// block (rt, ks) at (rt*(K/128) + ks)*9216; code byte b (0..63) of row r at (b/16)*2048 + (r/8)*128 + (r%8)*16 +
+// b%16, E4M3 scale j (0..7, one per 16 elements) of row r at 8192 + (j/4)*512 + (r%32)*16 + (r/32)*4 + j%4.
+__device__ __forceinline__ int mxu_code_off(int r, int b) { return (b >> 4) * 2048 + (r >> 3) * 128 + (r & 7) * 16 + (b & 15); }
+__device__ __forceinline__ int mxu_scale_off(int r, int j) { return 8192 + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3); }
+
+// A 32-element block holds a non-zero code when some nibble has a non-zero magnitude (E2M1 +-0 are 0x0 / 0x8).
+__device__ __forceinline__ bool mx4_block_nonzero(uint4 c) { return ((c.x | c.y | c.z | c.w) & 0x77777777u) != 0u; }
+
+// Pass 1, one thread per block: the largest scale byte over blocks with a non-zero code, into *smax (int, -1
+// initially).
+__global__ void __launch_bounds__(256) k_mx_umma_smax(const uint8_t* __restrict__ codes, int64_t codes_ld,
+                                                      const uint8_t* __restrict__ scales, int64_t scales_ld,
+                                                      int64_t N, int64_t K, int* __restrict__ smax) {
+    const int64_t nb = K / 32, i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int v = -1;
+    if (i < N * nb) {
+        const int64_t r = i / nb, b = i - r * nb;
+        const uint4 c = *reinterpret_cast<const uint4*>(codes + r * codes_ld + b * 16);
+        if (mx4_block_nonzero(c)) v = scales[r * scales_ld + b];
+    }
+    v = __reduce_max_sync(0xffffffffu, v);
+    if ((threadIdx.x & 31) == 0 && v >= 0) atomicMax(smax, v);
+}
+
+// E4M3 byte of 2^d, -9 <= d <= 8: normals (d >= -6) have exponent field d + 7 and no mantissa; 2^-7 .. 2^-9 are
+// the subnormals m * 2^-9 with m = 4, 2, 1.
+__device__ __forceinline__ uint32_t e4m3_pow2(int d) { return d >= -6 ? (uint32_t)(d + 7) << 3 : 1u << (d + 9); }
+
+// Pass 2, as the NVFP4 packing: per row and 128-K block, four 16-byte code pieces and one group of 8 scales.
+__global__ void __launch_bounds__(256) k_mx_pack_umma(const uint8_t* __restrict__ codes, int64_t codes_ld,
+                                                      const uint8_t* __restrict__ scales, int64_t scales_ld,
+                                                      int64_t N, int64_t K, const int* __restrict__ smax,
+                                                      uint8_t* __restrict__ out) {
+    const int64_t KSN = K / 128, per_row = 5, total = N * KSN * per_row;
+    const int s0 = __ldg(smax) - 8;
+    bool range = false, nan = false;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / (KSN * per_row), rem = i - row * (KSN * per_row), ks = rem / per_row;
+        const int piece = (int)(rem - ks * per_row), r = (int)(row % 128);
+        uint8_t* blk = out + ((row / 128) * KSN + ks) * 9216;
+        const uint8_t* crow = codes + row * codes_ld + ks * 64;
+        if (piece < 4) {
+            *reinterpret_cast<uint4*>(blk + mxu_code_off(r, piece * 16)) =
+                *reinterpret_cast<const uint4*>(crow + piece * 16);
+        } else {
+            for (int q = 0; q < 4; ++q) {  // the four MX blocks of this 128-K block
+                const uint32_t sb = scales[row * scales_ld + ks * 4 + q];
+                const bool nz = mx4_block_nonzero(*reinterpret_cast<const uint4*>(crow + q * 16));
+                uint32_t e = 0;
+                if (sb == 255u) {
+                    nan = true;
+                } else if (nz) {
+                    const int d = (int)sb - s0;
+                    if (d < -9) range = true;
+                    else e = e4m3_pow2(d);
+                }
+                blk[mxu_scale_off(r, 2 * q)] = (uint8_t)e;
+                blk[mxu_scale_off(r, 2 * q + 1)] = (uint8_t)e;
+            }
+        }
+    }
+    if (range) raise_dev_error(FT_DEVERR_RANGE);
+    if (nan) raise_dev_error(FT_DEVERR_BAD_SCALE);
+}
+
+// Pass 3: the tensor scale 2^(s0 - 127) (1 when no block is non-zero) replaces the scratch word.
+__global__ void k_mx_umma_tscale(float* tscale, int n) {
+    const int sm = *reinterpret_cast<const int*>(tscale);
+    const float t = sm < 0 ? 1.0f : ldexpf(1.0f, sm - 8 - 127);
+    for (int i = 0; i < n; ++i) tscale[i] = t;
+}
+
 }  // namespace ft
 
 using namespace ft;
@@ -212,6 +288,29 @@ ft_status ft_mxfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint
     const int64_t total = (N / 16) * (K / 128) * 96;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 148 * 32);
     k_mx_pack_tiles<<<(unsigned)blocks, 256, 0, cu(stream)>>>(codes, codes_ld, scales, scales_ld, N, K, tiles);
+    return check_launch(fn);
+}
+
+ft_status ft_mxfp4_pack_umma(const uint8_t* codes, int64_t codes_ld, const uint8_t* scales, int64_t scales_ld,
+                             int64_t N, int64_t K, uint8_t* tiles, float* tscale, int ts_count, ft_stream_t stream) {
+    const char* fn = "ft_mxfp4_pack_umma";
+    if (N <= 0 || K <= 0 || N % 128 || K % 128)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need N and K multiples of 128");
+    if (ts_count < 1 || ts_count > 4) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": need 1 <= ts_count <= 4");
+    if (!codes || !scales || !tiles || !tscale) return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+    if (!aligned(codes, 16) || codes_ld % 16 || !aligned(tiles, 16) || !aligned(tscale, 4) || codes_ld < K / 2 ||
+        scales_ld < K / 32)
+        return fail(FT_ERR_INVALID_ARG, std::string(fn) + ": codes/tiles need 16-byte alignment and row strides");
+    cudaStream_t s = cu(stream);
+    int* smax = reinterpret_cast<int*>(tscale);
+    if (cudaMemsetAsync(smax, 0xFF, sizeof(int), s) != cudaSuccess)
+        return fail(FT_ERR_CUDA, std::string(fn) + ": memset failed");
+    const int64_t nblk = N * (K / 32);
+    k_mx_umma_smax<<<(unsigned)((nblk + 255) / 256), 256, 0, s>>>(codes, codes_ld, scales, scales_ld, N, K, smax);
+    const int64_t total = N * (K / 128) * 5;
+    k_mx_pack_umma<<<(unsigned)std::min<int64_t>((total + 255) / 256, 148 * 64), 256, 0, s>>>(
+        codes, codes_ld, scales, scales_ld, N, K, smax, tiles);
+    k_mx_umma_tscale<<<1, 1, 0, s>>>(tscale, ts_count);
     return check_launch(fn);
 }
 

@@ -11,7 +11,7 @@ import torch
 
 from . import (FT_LAYOUT_DECODE_TILES, FT_LAYOUT_MXFP4_DECODE_TILES, FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP8_DECODE_TILES,
                FT_LAYOUT_MXFP8_ROWS, FT_LAYOUT_ROWS, FT_LAYOUT_UMMA_TILES, ft_gen_normal_f32, ft_mxfp4_pack_tiles,
-               ft_mxfp4_quantize_weight, ft_mxfp8_pack_tiles, ft_mxfp8_quantize_weight,
+               ft_mxfp4_pack_umma, ft_mxfp4_quantize_weight, ft_mxfp8_pack_tiles, ft_mxfp8_quantize_weight,
                ft_moe_decode_workspace_size, ft_moe_expert_ffn_nvfp4_decode, ft_moe_expert_ffn_nvfp4_prefill,
                ft_moe_layer_decode, ft_moe_layer_decode_workspace_size, ft_moe_layer_weights, ft_moe_permute,
                ft_moe_permute_workspace_size, ft_moe_prefill_workspace_size, ft_moe_route, ft_nvfp4_pack_tiles,
@@ -38,6 +38,8 @@ class LayerWeights:
     layout TILES:  gu_codes [n, 2I*H*9/16], d_codes [n, H*I*9/16] (16-row tiles, see ft_nvfp4_pack_tiles)
     layout UMMA:   the same sizes in 128x128 blocks for the tensor-core prefill (see ft_nvfp4_pack_umma)
     tscale [n, 4] fp32 (gate, up, down, pad)
+    layout UMMA with source="mxfp4": MXFP4 weights re-encoded exactly into the UMMA tiles (E4M3 power-of-two
+                   block scales and a power-of-two tensor scale per matrix, see ft_mxfp4_pack_umma)
     MXFP4 layouts (UE8M0 scales per 32, no tensor scale):
     layout MXFP4_ROWS:  as ROWS with gu_scales [n, 2I, H/32], d_scales [n, H, I/32]
     layout MXFP4_TILES: gu_codes [n, 2I*H*17/32], d_codes [n, H*I*17/32] (see ft_mxfp4_pack_tiles)
@@ -45,7 +47,10 @@ class LayerWeights:
     layout MXFP8_TILES: gu_codes [n, 2I*H*33/32], d_codes [n, H*I*33/32] (see ft_mxfp8_pack_tiles)
     """
 
-    def __init__(self, E: int, H: int, I: int, device, n_weights: int | None = None, layout: int = FT_LAYOUT_ROWS):
+    def __init__(self, E: int, H: int, I: int, device, n_weights: int | None = None, layout: int = FT_LAYOUT_ROWS,
+                 source: str = "nvfp4"):
+        assert source in ("nvfp4", "mxfp4") and (source == "nvfp4" or layout == FT_LAYOUT_UMMA_TILES)
+        self.mx_src = source == "mxfp4"
         self.E, self.H, self.I = E, H, I
         self.n = E if n_weights is None else n_weights
         self.layout = layout
@@ -53,7 +58,7 @@ class LayerWeights:
         u8 = torch.uint8
         self.mx8 = layout in (FT_LAYOUT_MXFP8_ROWS, FT_LAYOUT_MXFP8_DECODE_TILES)
         self.mx = self.mx8 or layout in (FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP4_DECODE_TILES)
-        self.sblock = 32 if self.mx else 16  # elements per scale
+        self.sblock = 32 if self.mx or self.mx_src else 16  # elements per scale (of the row-layout staging)
         self.cpe = 1 if self.mx8 else 2      # code elements per byte
         if layout in (FT_LAYOUT_ROWS, FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP8_ROWS):
             self.gu_codes = torch.empty((self.n, 2 * I, H // self.cpe), dtype=u8, device=device)
@@ -108,6 +113,17 @@ class LayerWeights:
         """Quantise fp32 gate [I,H], up [I,H], down [H,I] into weight index wi."""
         H, I = self.H, self.I
         guc, gus, dc, ds = self._rows_target(wi)
+        if self.mx_src:  # MXFP4 rows, then re-encoded into the tensor-core tiles with a tensor scale per matrix
+            for proj, w in ((PROJ_GATE, wg), (PROJ_UP, wu)):
+                assert tuple(w.shape) == (I, H)
+                ft_mxfp4_quantize_weight(w, guc.data_ptr() + proj * (H // 2), gus.data_ptr() + proj * (H // 32),
+                                         codes_ld=H, scales_ld=H // 16, stream=stream)
+            assert tuple(wd.shape) == (H, I)
+            ft_mxfp4_quantize_weight(wd, dc, ds, stream=stream)
+            ft_mxfp4_pack_umma(guc, H // 2, gus, H // 32, 2 * I, H, self.gu_codes[wi], self.tscale[wi, 0:2], 2,
+                               stream=stream)
+            ft_mxfp4_pack_umma(dc, I // 2, ds, I // 32, H, I, self.d_codes[wi], self.tscale[wi, 2:3], 1, stream=stream)
+            return
         if self.mx:
             quant, pack, c = ((ft_mxfp8_quantize_weight, ft_mxfp8_pack_tiles, 1) if self.mx8 else
                               (ft_mxfp4_quantize_weight, ft_mxfp4_pack_tiles, 2))

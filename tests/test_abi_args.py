@@ -152,6 +152,19 @@ def test_mxfp4_argument_checks():
     status(pk(NULL, 128, P, 8, 16, 256, P, NULL), Q.FT_ERR_INVALID_ARG)
 
 
+def test_mxfp4_umma_pack_arguments():
+    """The MXFP4 -> tensor-core tile packing rejects bad sizes, counts, pointers and alignment before any CUDA call."""
+    pu = L.ft_mxfp4_pack_umma
+    status(pu(P, 128, P, 8, 100, 256, P, P, 1, NULL), Q.FT_ERR_INVALID_ARG)   # N not a multiple of 128
+    status(pu(P, 128, P, 8, 128, 200, P, P, 1, NULL), Q.FT_ERR_INVALID_ARG)   # K not a multiple of 128
+    status(pu(P, 128, P, 8, 128, 256, P, P, 0, NULL), Q.FT_ERR_INVALID_ARG)   # ts_count < 1
+    status(pu(P, 128, P, 8, 128, 256, P, P, 5, NULL), Q.FT_ERR_INVALID_ARG)   # ts_count > 4
+    status(pu(P, 128, P, 8, 128, 256, P, NULL, 1, NULL), Q.FT_ERR_INVALID_ARG)  # no tensor-scale pointer
+    status(pu(P, 96, P, 8, 128, 256, P, P, 1, NULL), Q.FT_ERR_INVALID_ARG)    # codes_ld < K/2
+    status(pu(P, 128, P, 4, 128, 256, P, P, 1, NULL), Q.FT_ERR_INVALID_ARG)   # scales_ld < K/32
+    status(pu(MIS, 128, P, 8, 128, 256, P, P, 1, NULL), Q.FT_ERR_INVALID_ARG)  # misaligned codes
+
+
 def test_layer_decode_takes_mxfp4_tiles_without_tensor_scales():
     """MXFP4 tiles are accepted with no tensor-scale pointer (T = 0: checks only, nothing launched); MXFP4 rows are
     not a layout of the fused step, and NVFP4 tiles still need their tensor scales."""

@@ -1,7 +1,9 @@
 """GPU tests of the MX expert weights (MXFP4 and MXFP8): the quantisers and the tile packings bit for bit against the
 oracle's statement of the formats (oracle/mx.py) and of the layouts, and the fused decode layer step on MX tiles
 against the oracle layer reading the device's own row-layout MX bytes (relative L2 5e-3, max |err| 2e-2 * RMS), on
-the one-token path (routing by one warp) and the multi-token path.
+the one-token path (routing by one warp) and the multi-token path.  MXFP4 weights on the tensor-core prefill: the
+re-encoded tiles dequantise (by the oracle's NVFP4 reading) to exactly the MX values, and the prefill layer matches
+the oracle's A4-mode layer on the MX bytes.
 """
 import numpy as np
 import pytest
@@ -17,7 +19,7 @@ DEV = "cuda:0"
 
 if torch.cuda.is_available():
     import quantized_expert_ffn_06_b300 as Q
-    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights
+    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights, PrefillLayer
 
 
 FMTS = ["mxfp4", "mxfp8"]
@@ -203,3 +205,100 @@ def test_fused_decode_mx_large_shape(fmt):
     rows, tiles = mx_layer(cfg, 0, fmt)
     for step in range(2):
         check_fused(cfg, rows, tiles, 0, step, 1, fmt)
+
+
+# ---------------------------------------------------------------- MXFP4 on the tensor-core prefill
+
+def unpack_umma(blob: np.ndarray, N: int, K: int):
+    """Row-major NVFP4 codes [N][K/2] and E4M3 scales [N][K/16] read back from FT_LAYOUT_UMMA_TILES (code byte b of
+    row r of a 128 x 128 block at (b/16)*2048 + (r/8)*128 + (r%8)*16 + b%16, scale j at 8192 + (j/4)*512 +
+    (r%32)*16 + (r/32)*4 + j%4)."""
+    KSN = K // 128
+    t = blob.reshape(N // 128, KSN, 9216)
+    c = t[:, :, :8192].reshape(N // 128, KSN, 4, 16, 8, 16).transpose(0, 3, 4, 1, 2, 5).reshape(N, K // 2)
+    s = t[:, :, 8192:].reshape(N // 128, KSN, 2, 32, 4, 4).transpose(0, 4, 3, 1, 2, 5).reshape(N, K // 16)
+    return c, s
+
+
+def mx_umma_layer(cfg, layer):
+    """The same fp32 draws as MXFP4 rows (what the oracle reads) and as tensor-core tiles re-encoded from MXFP4."""
+    stream_of = lambda e, p: W.w_stream(cfg.weight_cfg, layer, e, p)  # noqa: E731
+    rows = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_MXFP4_ROWS)
+    rows.fill_synthetic(stream_of, sigma=cfg.w_sigma)
+    umma = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_UMMA_TILES, source="mxfp4")
+    umma.fill_synthetic(stream_of, sigma=cfg.w_sigma)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    return rows, umma
+
+
+def test_mxfp4_umma_tiles_dequantise_to_the_mx_values():
+    """Every expert's gate/up and down tiles: the codes are the MX codes, and E4M3 scale x tensor scale reproduces
+    each block's 2^(s-127) exactly (two independent oracle dequantisers agree bit for bit)."""
+    cfg = W.scaled(W.CONFIGS["tiny"], E=3)
+    rows, umma = mx_umma_layer(cfg, 2)
+    H, I = cfg.H, cfg.I
+    ts = umma.tscale.cpu().numpy()
+    for e in range(cfg.E):
+        for blob, codes, scales, N, K, t in ((umma.gu_codes[e], rows.gu_codes[e], rows.gu_scales[e], 2 * I, H, ts[e, 0]),
+                                             (umma.d_codes[e], rows.d_codes[e], rows.d_scales[e], H, I, ts[e, 2])):
+            c, s = unpack_umma(blob.cpu().numpy(), N, K)
+            mc, ms = codes.cpu().numpy(), scales.cpu().numpy()
+            assert np.array_equal(c, mc)
+            got = O.dequantize(c, s, float(t))
+            want = MX.dequantize(mc, ms, "mxfp4")
+            assert np.array_equal(got, want)
+        assert ts[e, 0] == ts[e, 1]
+
+
+@pytest.mark.parametrize("spread", [17, 18])
+def test_mxfp4_umma_exponent_span(spread):
+    """Non-zero blocks 17 octaves below the largest are still exact; 18 set FT_DEVERR_RANGE.  All-zero blocks (any
+    scale byte) get scale 0 and do not count."""
+    rng = np.random.default_rng(spread)
+    N, K = 128, 256
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scales = rng.integers(124, 130, (N, K // 32), dtype=np.uint8)
+    scales[0, 0] = 140                 # the largest: s0 = 132, tensor scale 2^5
+    scales[5, 3] = 140 - spread        # 2^-9 (the smallest E4M3 power of two) or beyond
+    codes[5, 48:64] = 0x31             # that block holds non-zero codes
+    codes[9, 16:32] = 0x80            # an all-zero block (signed zeros) with an out-of-span scale
+    scales[9, 1] = 3
+    tiles = torch.empty(N * K * 9 // 16, dtype=torch.uint8, device=DEV)
+    ts = torch.zeros(1, dtype=torch.float32, device=DEV)
+    assert Q.ft_device_status() == 0
+    Q.ft_mxfp4_pack_umma(torch.from_numpy(codes).to(DEV), K // 2, torch.from_numpy(scales).to(DEV), K // 32, N, K,
+                         tiles, ts, 1)
+    torch.cuda.synchronize()
+    st = Q.ft_device_status()
+    if spread == 17:
+        assert st == 0
+        c, s = unpack_umma(tiles.cpu().numpy(), N, K)
+        assert np.array_equal(O.dequantize(c, s, float(ts.item())), MX.dequantize(codes, scales, "mxfp4"))
+        assert s[9, 2] == 0 and s[9, 3] == 0
+    else:
+        assert st == Q.FT_DEVERR_RANGE
+
+
+def run_prefill(cfg, umma, logits, x_bits):
+    T = logits.shape[0]
+    mod = PrefillLayer(cfg.E, cfg.H, cfg.I, cfg.k, T, DEV)
+    out = torch.empty((T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    mod(umma, torch.from_numpy(logits).to(DEV),
+        torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).to(DEV), out)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    return mod, out
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 200), ("prefill_35b", 384)])
+def test_prefill_on_mxfp4_weights_matches_oracle(name, T):
+    """The tensor-core prefill on MXFP4 weights (tiny layer, every output; 35B layer shape, 384 tokens) against the
+    oracle's A4-mode layer on the MX-dequantised row bytes."""
+    cfg = W.scaled(W.CONFIGS[name], T=T)
+    rows, umma = mx_umma_layer(cfg, 0)
+    logits, x_bits = W.router_logits(cfg, 0, 4), W.activations_bf16(cfg, 0, 4)
+    mod, out = run_prefill(cfg, umma, logits, x_bits)
+    r = O.moe_layer(logits, x_bits, cfg.k, MxOracleExperts(rows), O.MODE_A4)
+    assert np.array_equal(mod.ids.cpu().numpy(), r["ids"])
+    assert_layer_close(out.float().cpu().numpy(), r["out"], f"mxfp4 prefill {name} T={T}")
