@@ -90,12 +90,17 @@ FT_API int ft_version(void);
  * the call, from any thread).  site FT_WAIT_SITE_DECODE_H makes the down phase
  * of the fused decode step (ft_moe_layer_decode and the tiled
  * ft_moe_expert_ffn_nvfp4_decode) wait for h words of a tag that no CTA
- * writes, with every wait bounded by limit_ns (0 < limit_ns <= 2 s): the wait
- * runs out, the kernel sets FT_DEVERR_TIMEOUT, finishes without trapping and
- * its output is unspecified.  site FT_WAIT_SITE_NONE restores normal waits
- * with the default 2 s bound (limit_ns ignored). */
+ * writes; site FT_WAIT_SITE_PREFILL_TOKEN makes the MMA issuer of the
+ * tensor-core prefill's gate/up GEMM (ft_moe_expert_ffn_nvfp4_prefill, token
+ * tiles resident) wait on a barrier that nothing completes before its first
+ * token-tile part.  Every wait of the affected kernel is then bounded by
+ * limit_ns (0 < limit_ns <= 2 s): the wait runs out, the kernel sets
+ * FT_DEVERR_TIMEOUT, finishes without trapping and its output is unspecified.
+ * site FT_WAIT_SITE_NONE restores normal waits with the default 2 s bound
+ * (limit_ns ignored). */
 #define FT_WAIT_SITE_NONE 0
 #define FT_WAIT_SITE_DECODE_H 1
+#define FT_WAIT_SITE_PREFILL_TOKEN 2
 FT_API ft_status ft_debug_inject_wait_expiry(int site, uint64_t limit_ns);
 
 /* Waits for `stream`, then reads and clears the current device's error word.

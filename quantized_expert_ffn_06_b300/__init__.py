@@ -26,7 +26,7 @@ FT_LAYOUT_ROWS, FT_LAYOUT_DECODE_TILES, FT_LAYOUT_UMMA_TILES = 0, 1, 2
 FT_LAYOUT_MXFP4_ROWS, FT_LAYOUT_MXFP4_DECODE_TILES = 3, 4
 FT_LAYOUT_MXFP8_ROWS, FT_LAYOUT_MXFP8_DECODE_TILES = 5, 6
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_SCALE, FT_DEVERR_TIMEOUT, FT_DEVERR_BAD_INDEX, FT_DEVERR_RANGE = 1, 2, 4, 8, 16
-FT_WAIT_SITE_NONE, FT_WAIT_SITE_DECODE_H = 0, 1
+FT_WAIT_SITE_NONE, FT_WAIT_SITE_DECODE_H, FT_WAIT_SITE_PREFILL_TOKEN = 0, 1, 2
 
 _vp, _i32, _i64, _u64, _sz, _dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t,
                                     ctypes.c_double)

@@ -170,6 +170,11 @@ __device__ __forceinline__ int select_topk8(const float* row, int E, int k, bool
     return my_e;
 }
 
+// Wait-expiry test hook (ft_debug_inject_wait_expiry): the bound on any single wait and the site made to expire,
+// read by the host code of each kernel at launch.
+unsigned long long wait_hook_ns();
+int wait_hook_site();
+
 // weight index of an expert (identity, or through a slot table)
 __device__ __forceinline__ int weight_index(const ft_moe_layer_weights& W, int e) {
     if (W.expert_to_slot == nullptr) return e;

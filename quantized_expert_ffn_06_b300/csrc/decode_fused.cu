@@ -80,6 +80,8 @@ constexpr unsigned long long WAIT_NS = 2000000000ull;  // default bound on any s
 // Test hooks (off by default): a shorter wait bound, and a wait made to expire.
 static std::atomic<unsigned long long> g_wait_ns{dk::WAIT_NS};
 static std::atomic<int> g_wait_site{FT_WAIT_SITE_NONE};
+unsigned long long wait_hook_ns() { return g_wait_ns.load(); }
+int wait_hook_site() { return g_wait_site.load(); }
 
 // Division by a divisor fixed per launch: q = x / d as one multiply-high with
 // m = ceil(2^32 / d), exact whenever x * d < 2^32 (every use below stays far
@@ -1443,7 +1445,7 @@ ft_status ft_nvfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, const uint
 }
 
 ft_status ft_debug_inject_wait_expiry(int site, uint64_t limit_ns) {
-    if (site != FT_WAIT_SITE_NONE && site != FT_WAIT_SITE_DECODE_H)
+    if (site != FT_WAIT_SITE_NONE && site != FT_WAIT_SITE_DECODE_H && site != FT_WAIT_SITE_PREFILL_TOKEN)
         return fail(FT_ERR_INVALID_ARG, "ft_debug_inject_wait_expiry: unknown wait site");
     if (site != FT_WAIT_SITE_NONE && (limit_ns == 0 || limit_ns > dk::WAIT_NS))
         return fail(FT_ERR_INVALID_ARG, "ft_debug_inject_wait_expiry: need 0 < limit_ns <= 2 s");

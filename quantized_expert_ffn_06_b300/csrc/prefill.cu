@@ -91,6 +91,8 @@ struct PfGemmArgs {
     const int4* tinfo;       // [tiles] {expert, first permuted row, real rows, 0}
     float* y;                // optional [T*k][H] fp32 per-row expert outputs (tensor scale applied, no routing weight)
     int parts;               // resident kernel: work items per token tile, each a contiguous part of the weight tiles
+    unsigned long long wait_ns;  // bound on any single wait (2 s; shorter under the wait-expiry test hook)
+    int wait_site;           // FT_WAIT_SITE_PREFILL_TOKEN: the gate/up MMA issuer waits on a barrier nothing completes
     int cstage;              // resident kernel, down GEMM: 32 or 16 = the combine goes through a shared-memory
                              // transpose, that many columns per pass; 0 = reductions straight from the thread's row
 };
@@ -120,12 +122,13 @@ __device__ __forceinline__ bool pf_try_wait(unsigned long long* b, uint32_t pari
     return ok != 0;
 }
 
-__device__ __forceinline__ bool pf_wait(unsigned long long* b, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool pf_wait(unsigned long long* b, uint32_t parity, volatile int* abort_flag,
+                                        unsigned long long limit_ns) {
     if (pf_try_wait(b, parity)) return true;
     const unsigned long long t0 = pf_gt();
     while (!pf_try_wait(b, parity)) {
         if (*abort_flag) return false;
-        if (pf_gt() - t0 > pf::WAIT_NS) {
+        if (pf_gt() - t0 > limit_ns) {
             *abort_flag = 1;
             raise_dev_error(FT_DEVERR_TIMEOUT);
             return false;
@@ -551,7 +554,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
                 // a tile's K blocks are contiguous: KPS of them (A, then B) per stage
                 for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
                     const int s = sc % pf::NS, use = sc / pf::NS;
-                    if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag)) break;
+                    if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag, a.wait_ns)) break;
                     uint8_t* dst = ring + (size_t)s * pf::STAGE;
                     const uint32_t bytes = (uint32_t)(min(pf::KPS, a.KSN - ks) * pf::BLK);
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&full[s])),
@@ -578,12 +581,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
             int sc = 0, it = 0;
             for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x, ++it) {
                 const int buf = it & 1, useb = it >> 1;
-                if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag)) break;
+                if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag, a.wait_ns)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t dcol = tbase + (uint32_t)(buf * 128);
                 for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
                     const int s = sc % pf::NS;
-                    if (!pf_wait(&full[s], (sc / pf::NS) & 1, abort_flag)) break;
+                    if (!pf_wait(&full[s], (sc / pf::NS) & 1, abort_flag, a.wait_ns)) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const int nkb = min(pf::KPS, a.KSN - ks);
                     for (int bi = 0; bi < nkb; ++bi) {
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_stream(const PfGemmA
                 meta = __ldg(a.rowmeta + (int64_t)ntg * 128 + r);
                 if (a.y) prow = __ldg(a.tinfo + ntg).y + r;
             }
-            if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
+            if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, a.wait_ns)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // the accumulator is in registers once the load has completed: hand the TMEM columns back to
             // the MMA before the epilogue's math and stores
@@ -684,7 +687,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
     uint8_t* ring = btile + (size_t)a.KSN * pf::BLK;
     float* cst = reinterpret_cast<float*>(ring + (size_t)a.nstages * pf::KPS * pf::BLK);  // combine staging (cstage)
     __shared__ __align__(8) unsigned long long full[pf::RES_MAXNS], empty[pf::RES_MAXNS], acc_full[2], acc_empty[2], bfull,
-        bfree;
+        bfree, never;  // never: the wait-expiry test hook's barrier, which nothing completes
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
     volatile int* abort_flag = &abort_s;
@@ -704,6 +707,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfull)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfree)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&never)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_s = 0;
     }
@@ -728,7 +732,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                 int ntg, mlo, mhi;
                 if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
                 // the token tile, once the previous item's MMAs have read the last one
-                if (bi > 0 && !pf_wait(&bfree, (bi - 1) & 1, abort_flag)) break;
+                if (bi > 0 && !pf_wait(&bfree, (bi - 1) & 1, abort_flag, a.wait_ns)) break;
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&bfull)), "r"(tile_bytes)
                              : "memory");
                 asm volatile(
@@ -751,7 +755,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                     }
                     for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
                         const int s = sc % NSr, use = sc / NSr;
-                        if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag)) {
+                        if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag, a.wait_ns)) {
                             stop = true;
                             break;
                         }
@@ -787,7 +791,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
             for (int i = blockIdx.x; i < n_items && !stop && !*abort_flag; i += gridDim.x) {
                 int ntg, mlo, mhi;
                 if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
-                if (!pf_wait(&bfull, bi & 1, abort_flag)) break;
+                // under the wait-expiry test hook the gate/up GEMM first waits on a barrier that nothing
+                // completes: the bound runs out and every role winds down
+                if (EPI == 1 && a.wait_site == FT_WAIT_SITE_PREFILL_TOKEN && !pf_wait(&never, 0, abort_flag, a.wait_ns))
+                    break;
+                if (!pf_wait(&bfull, bi & 1, abort_flag, a.wait_ns)) break;
                 ++bi;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 for (int ks = 0; ks < a.KSN; ++ks) {
@@ -796,7 +804,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                 }
                 for (int m = mlo; m < mhi && !stop; ++m, ++it) {
                     const int buf = it & 1, useb = it >> 1;
-                    if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag)) {
+                    if (useb > 0 && !pf_wait(&acc_empty[buf], (useb - 1) & 1, abort_flag, a.wait_ns)) {
                         stop = true;
                         break;
                     }
@@ -804,7 +812,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                     const uint32_t dcol = tbase + (uint32_t)(buf * 128);
                     for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
                         const int s = sc % NSr;
-                        if (!pf_wait(&full[s], (sc / NSr) & 1, abort_flag)) {
+                        if (!pf_wait(&full[s], (sc / NSr) & 1, abort_flag, a.wait_ns)) {
                             stop = true;
                             break;
                         }
@@ -863,7 +871,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
             }
             for (int m = mlo; m < mhi; ++m, ++it) {
                 const int buf = it & 1;
-                if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) {
+                if (!pf_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, a.wait_ns)) {
                     stop = true;
                     break;
                 }
@@ -1093,6 +1101,8 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     g.e2s = W->expert_to_slot;
     g.tinfo = tinfo;
     g.y = y;
+    g.wait_ns = wait_hook_ns();
+    g.wait_site = wait_hook_site();
     const int G = pf_sm_count();
     // gate/up + SwiGLU
     g.A = W->gu_codes;

@@ -2,7 +2,9 @@
 
 A bounded device wait runs out when it waits for h words of a tag no CTA writes (the library's test hook, with a
 1 ms limit): the kernel must return on its own, report FT_DEVERR_TIMEOUT through the device error word, and leave the
-workspace usable, so that the next call is bit-equal to a clean one.  The workspace's 64-bit call counter is also
+workspace usable, so that the next call is bit-equal to a clean one.  The same for the tensor-core prefill, whose
+gate/up MMA issuer is made to wait on a barrier nothing completes: the next call matches a clean one (its fp32
+reductions have no fixed order, so within the layer tolerance rather than bit for bit).  The workspace's 64-bit call counter is also
 started just before its tag wraps (2^32 - 1 tags, never 0): the calls across the wrap must equal a clean call.
 """
 import time
@@ -12,13 +14,14 @@ import pytest
 import torch
 
 import workloads as W
+from helpers import assert_layer_close
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 if torch.cuda.is_available():
     import quantized_expert_ffn_06_b300 as Q
-    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights
+    from quantized_expert_ffn_06_b300.layer import FusedDecodeLayer, LayerWeights, PrefillLayer
 
 
 def layer_and_inputs(cfg):
@@ -57,6 +60,38 @@ def test_expired_wait_reports_timeout_and_the_next_call_is_exact(shape):
     torch.cuda.synchronize()
     assert Q.ft_device_status() == 0
     assert torch.equal(again, clean)
+
+
+def test_prefill_expired_wait_reports_timeout_and_the_next_call_is_clean():
+    """The 35B layer shape with 512 prompt tokens: the gate/up GEMM's MMA issuer gives up after 1 ms, every role of
+    the kernel winds down (no trap, TMEM freed), the down GEMM and the output conversion still run, and the next
+    call without the hook equals a clean call."""
+    cfg = W.scaled(W.CONFIGS["prefill_35b"], T=512)
+    lw = LayerWeights(cfg.E, cfg.H, cfg.I, DEV, layout=Q.FT_LAYOUT_UMMA_TILES)
+    lw.fill_synthetic(lambda e, p: W.w_stream(cfg.weight_cfg, 0, e, p), sigma=cfg.w_sigma)
+    logits = torch.from_numpy(W.router_logits(cfg, 0, 0)).to(DEV)
+    x = torch.from_numpy(W.activations_bf16(cfg, 0, 0).view(np.int16)).view(torch.bfloat16).to(DEV)
+    mod = PrefillLayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.T, DEV)
+    clean = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    mod(lw, logits, x, clean)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    out = torch.empty_like(clean)
+    Q.ft_debug_inject_wait_expiry(Q.FT_WAIT_SITE_PREFILL_TOKEN, 1_000_000)  # 1 ms
+    try:
+        t0 = time.perf_counter()
+        mod(lw, logits, x, out)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+    finally:
+        Q.ft_debug_inject_wait_expiry(Q.FT_WAIT_SITE_NONE)
+    assert Q.ft_device_status() & Q.FT_DEVERR_TIMEOUT
+    assert elapsed < 0.5, elapsed
+    again = torch.empty_like(clean)
+    mod(lw, logits, x, again)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == 0
+    assert_layer_close(again.float().cpu().numpy(), clean.float().cpu().numpy().astype(np.float64), "prefill after expiry")
 
 
 def test_wait_hook_rejects_bad_arguments():
