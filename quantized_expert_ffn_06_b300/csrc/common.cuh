@@ -94,6 +94,39 @@ __device__ __forceinline__ void quant_block16(const float (&v)[16], float st, ui
     codes.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
 }
 
+// The same block quantiser for bf16-valued inputs with unit tensor scale (activations, and h after its bf16
+// rounding), with one reciprocal per block instead of a division per element.  With v of at most 8 significant
+// bits and eff an E4M3 value (at most 4), v / eff is either exactly a midpoint of the E2M1 grid (0.25, 0.75, 1.25,
+// 1.75, 2.5, 3.5, 5) or at least 2^-17 away from every midpoint.  q = v * (1/eff) rounded, followed by one residual
+// correction q + (v - q * eff) / eff evaluated with fused multiply-adds (the reciprocal-refinement step of
+// Markstein's division), lands within a few fp32 units of v / eff, so on the same side of every midpoint, and at
+// an exact midpoint on the midpoint itself.  The E2M1 conversion then rounds it exactly as it rounds the
+// correctly rounded quotient.  Finite inputs only.
+__device__ __forceinline__ void quant_block16_bf16(const float (&v)[16], uint2& codes, uint32_t& sb) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    sb = f32_to_e4m3_rn_sat(__fdiv_rn(amax, 6.0f));
+    const float eff = e4m3_to_f32(sb);
+    uint32_t b[8];
+    if (eff == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = 0u;
+    } else {
+        const float inv = __frcp_rn(eff);
+        float q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float q0 = __fmul_rn(v[i], inv);
+            q[i] = __fmaf_rn(__fmaf_rn(-q0, eff, v[i]), inv, q0);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = f32x2_to_e2m1x2_rn_sat(q[2 * i], q[2 * i + 1]);
+    }
+    codes.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+    codes.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+}
+
 // acc += a(f16) * b(f16), fp32 accumulate.
 __device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float acc) {
     float d;

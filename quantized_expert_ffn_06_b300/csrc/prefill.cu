@@ -247,8 +247,7 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const int32_t* __restrict__ of
 
 // x[t] quantised once (unit tensor scale) into a compact row of H/2 code bytes
 // followed by H/16 scale bytes.  A warp covers 1024 elements of one token, 32
-// per lane (two blocks of 16): the IEEE divisions of the quantiser make this
-// issue-bound, so it spreads over as many warps as the rows allow.
+// per lane (two blocks of 16), spread over as many warps as the rows allow.
 __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restrict__ x, int T, int H,
                                                          uint8_t* __restrict__ xc) {
     const int wpt = (H + 1023) / 1024;  // warps per token
@@ -276,7 +275,7 @@ __global__ void __launch_bounds__(256) k_pf_quant_tokens(const uint16_t* __restr
         }
         uint2 c;
         uint32_t sb;
-        quant_block16(v, 1.0f, c, sb);
+        quant_block16_bf16(v, c, sb);
         cw[2 * bl] = c.x;
         cw[2 * bl + 1] = c.y;
         sw |= sb << (8 * bl);
@@ -403,28 +402,22 @@ __global__ void __launch_bounds__(256) k_pf_out(const float4* __restrict__ out32
 
 // SwiGLU + h quantisation.  Weight rows come as (gate, up) pairs, so the 32
 // columns c0 .. c0+31 of a thread are the 16 h features m*64 + c0/2 .. +15 of its
-// token: exactly one NVFP4 block, quantised without leaving the thread
-// (fp32, IEEE division, as the quantiser defines it).
+// token: exactly one NVFP4 block, quantised without leaving the thread (the
+// quantiser's codes with one reciprocal per block: quant_block16_bf16).
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ void epi_swiglu(const PfGemmArgs& a, const uint32_t (&v)[32], int m, int ntg, int r, int c0,
                                            float tsg, float tsu) {
     float hb[16];
-    float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float g = __uint_as_float(v[2 * i]) * tsg, u = __uint_as_float(v[2 * i + 1]) * tsu;
         hb[i] = bf16_to_f32(bf16_bits(silu_fast(g) * u));
-        amax = fmaxf(amax, fabsf(hb[i]));
     }
-    const uint32_t sb = f32_to_e4m3_rn_sat(__fdiv_rn(amax, 6.0f));
-    const float eff = e4m3_to_f32(sb);
-    uint32_t w[2] = {0u, 0u};
-    if (eff != 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i >> 2] |= f32x2_to_e2m1x2_rn_sat(__fdiv_rn(hb[2 * i], eff), __fdiv_rn(hb[2 * i + 1], eff)) << (8 * (i & 3));
-    }
+    uint2 cw;
+    uint32_t sb;
+    quant_block16_bf16(hb, cw, sb);  // hb is bf16-valued, unit tensor scale
+    const uint32_t w[2] = {cw.x, cw.y};
     const int f0 = m * 64 + c0 / 2;  // first feature: block f0 / 128 of the h row, bytes (f0 % 128) / 2 ..
     uint8_t* blk = a.hq + ((int64_t)ntg * a.KSN2 + f0 / 128) * pf::BLK;
     *reinterpret_cast<uint2*>(blk + blk_code_off(r, (f0 & 127) / 2)) = make_uint2(w[0], w[1]);

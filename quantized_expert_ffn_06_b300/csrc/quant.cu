@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) k_quant_act(const uint16_t* __restrict__ 
     }
     uint2 c;
     uint32_t sb;
-    quant_block16(v, 1.0f, c, sb);
+    quant_block16_bf16(v, c, sb);  // bf16 inputs, unit tensor scale
     *reinterpret_cast<uint2*>(codes + t * (K / 2) + b * 8) = c;
     scales[t * nb + b] = (uint8_t)sb;
 }

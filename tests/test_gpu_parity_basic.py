@@ -117,6 +117,37 @@ def test_activation_quantizer_bit_exact_on_1e8_values():
         assert np.array_equal(codes.cpu().numpy(), c_ref), chunk
 
 
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_activation_quantizer_ties_and_neighbours():
+    """Blocks whose values sit exactly on the E2M1 midpoints times the block's scale (ties), and one bf16 step
+    either side of them, with power-of-two and other E4M3 scales and both signs: the device encoder (exact
+    comparisons with midpoint x scale) against the oracle's division and round-to-nearest-even, byte for byte."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    blocks = []
+    for k in range(-10, 9):
+        for f in (1.0, 1.125, 1.5, 1.875):
+            eff = f * 2.0 ** k
+            on = np.concatenate([mids, -mids]) * eff                        # 14 ties
+            for shift in (0, 1, -1):  # on the midpoint, one bf16 step away from / toward zero (sign-magnitude bits)
+                b = f32_to_bf16_bits(on.astype(np.float32)).astype(np.int32) + shift
+                vals = ((b.astype(np.uint32) & 0xFFFF) << 16).view(np.float32)
+                blk = np.concatenate([[6.0 * eff, 0.0], vals]).astype(np.float32)   # amax 6 * eff: scale eff
+                blocks.append(blk)
+    x = np.stack(blocks)                                                    # [n, 16]
+    n = (len(x) + 15) // 16 * 16
+    x = np.concatenate([x, np.zeros((n - len(x), 16), np.float32)]).reshape(n // 16, 256)
+    bits = f32_to_bf16_bits(x)
+    x = (bits.astype(np.uint32) << 16).view(np.float32)
+    codes, scales = Q.ft_nvfp4_quantize_act(to_dev(bits.view(np.int16), torch.bfloat16))
+    c_ref, s_ref = O.quantize_act(x)
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+
+
 @pytest.mark.parametrize("T,K", [(4, 256), (64, 2048), (3, 512)])
 def test_activation_quantizer_bit_exact(T, K):
     bits = W.normal_bf16(W.x_stream(7, T, K), T * K).reshape(T, K)
