@@ -316,6 +316,75 @@ __global__ void __launch_bounds__(1024) k_permute_place(const int32_t* __restric
     }
 }
 
+// The scan and the placement in one kernel, for at most 32 chunks: every block reads all the chunk counts
+// (one independent load per chunk and expert thread), forms the expert totals and its own chunk's bases, scans the
+// totals over the experts, and places its chunk as k_permute_place does.  Block 0 also writes offsets and the
+// active list.  The same arithmetic as k_permute_scan followed by k_permute_place, without the launch between.
+constexpr int kPermFusedMaxChunks = 32;
+
+__global__ void __launch_bounds__(1024) k_permute_scan_place(const int32_t* __restrict__ ids, int n, int E,
+                                                             const int32_t* __restrict__ chunk_cnt, int nchunks,
+                                                             int32_t* __restrict__ offsets,
+                                                             int32_t* __restrict__ active, int32_t* __restrict__ perm,
+                                                             int32_t* __restrict__ inv) {
+    extern __shared__ int wcnt[];
+    __shared__ int tot[1024];
+    __shared__ int flag[1024];
+    __shared__ int cbase[1024];
+    __shared__ int warp_tot[33];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
+    int base = 0, total = 0;
+    if (tid < E) {
+#pragma unroll
+        for (int c = 0; c < kPermFusedMaxChunks; ++c)
+            if (c < nchunks) {
+                const int v = __ldg(chunk_cnt + (int64_t)c * E + tid);
+                total += v;
+                if (c < b) base += v;
+            }
+        tot[tid] = total;
+        flag[tid] = total > 0;
+    }
+    for (int i = tid; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+    const int64_t f = (int64_t)b * kPermChunk + tid;
+    int e = -1;
+    if (f < n) {
+        e = ids[f];
+        if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int lrank = __popc(peers & ((1u << lane) - 1u));
+    __syncthreads();
+    block_exclusive_scan(tot, E, warp_tot);  // tot[e] <- first permuted row of expert e
+    if (tid < E) cbase[tid] = tot[tid] + base;
+    if (b == 0) {
+        if (tid < E) offsets[tid] = tot[tid];
+        if (tid == 0) offsets[E] = n;
+        if (active) {
+            const int nact = block_exclusive_scan(flag, E, warp_tot);
+            if (tid < E && total > 0) active[1 + flag[tid]] = tid;
+            if (tid == 0) active[0] = nact;
+        }
+    }
+    if (e >= 0 && lrank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int x = tid; x < E; x += blockDim.x) {  // exclusive scan over the warps
+        int run = 0;
+#pragma unroll 8
+        for (int w = 0; w < 32; ++w) {
+            const int v = wcnt[w * E + x];
+            wcnt[w * E + x] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    if (e >= 0) {
+        const int p = cbase[e] + wcnt[warp * E + e] + lrank;
+        perm[p] = (int32_t)f;
+        inv[f] = p;
+    }
+}
+
 // ----------------------------------------------------------------------------
 // combine
 // ----------------------------------------------------------------------------
@@ -400,12 +469,18 @@ ft_status ft_moe_permute(const int32_t* ids, int T, int E, int k, int32_t* offse
     const int nchunks = (n + kPermChunk - 1) / kPermChunk;
     int32_t* chunk_cnt = static_cast<int32_t*>(ws);
     k_permute_hist<<<nchunks, 1024, 0, s>>>(ids, n, E, chunk_cnt);
-    k_permute_scan<<<1, 1024, 0, s>>>(chunk_cnt, nchunks, n, E, offsets, active);
     static std::once_flag once;
     std::call_once(once, [] {
         cudaFuncSetAttribute(k_permute_place, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4);
+        cudaFuncSetAttribute(k_permute_scan_place, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4);
     });
-    k_permute_place<<<nchunks, 1024, (size_t)32 * E * 4, s>>>(ids, n, E, chunk_cnt, perm, inv);
+    if (nchunks <= kPermFusedMaxChunks) {
+        k_permute_scan_place<<<nchunks, 1024, (size_t)32 * E * 4, s>>>(ids, n, E, chunk_cnt, nchunks, offsets, active,
+                                                                       perm, inv);
+    } else {
+        k_permute_scan<<<1, 1024, 0, s>>>(chunk_cnt, nchunks, n, E, offsets, active);
+        k_permute_place<<<nchunks, 1024, (size_t)32 * E * 4, s>>>(ids, n, E, chunk_cnt, perm, inv);
+    }
     return check_launch("ft_moe_permute");
 }
 
