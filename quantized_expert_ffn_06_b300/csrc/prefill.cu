@@ -386,11 +386,24 @@ __global__ void __launch_bounds__(256, 4) k_pf_gather_x(const uint8_t* __restric
     if (kp == 0 && tid < 128) rowmeta[(int64_t)rt * 128 + tid] = make_int2(t, __float_as_int(wt));
 }
 
+// Each warp converts segments of 4 x 32 float4s (four coalesced loads in flight per lane, then four stores).
 __global__ void __launch_bounds__(256) k_pf_out(const float4* __restrict__ out32, int64_t n4, uint2* __restrict__ out) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-        const float4 v = out32[i];
-        out[i] = make_uint2((uint32_t)bf16_bits(v.x) | ((uint32_t)bf16_bits(v.y) << 16),
-                            (uint32_t)bf16_bits(v.z) | ((uint32_t)bf16_bits(v.w) << 16));
+    const int lane = threadIdx.x & 31;
+    const int64_t nseg = (n4 + 127) / 128, wstep = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t sg = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; sg < nseg; sg += wstep) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t i = sg * 128 + j * 32 + lane;
+            if (i < n4) v[j] = out32[i];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t i = sg * 128 + j * 32 + lane;
+            if (i < n4)
+                out[i] = make_uint2((uint32_t)bf16_bits(v[j].x) | ((uint32_t)bf16_bits(v[j].y) << 16),
+                                    (uint32_t)bf16_bits(v[j].z) | ((uint32_t)bf16_bits(v[j].w) << 16));
+        }
     }
 }
 
@@ -1113,7 +1126,7 @@ ft_status ft_moe_expert_ffn_nvfp4_prefill(const ft_moe_layer_weights* W, const u
     launch_pf_gemm<2>(g, G, s);
     if (!out) return check_launch(fn);
     const int64_t n4 = (int64_t)T * H / 4;  // H is a multiple of 128
-    k_pf_out<<<(unsigned)std::min<int64_t>((n4 + 255) / 256, 148 * 16), 256, 0, s>>>(
+    k_pf_out<<<(unsigned)std::min<int64_t>((n4 + 1023) / 1024, 148 * 8), 256, 0, s>>>(
         reinterpret_cast<const float4*>(out32), n4, reinterpret_cast<uint2*>(out));
     return check_launch(fn);
 }
