@@ -734,6 +734,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
         // ---------------- producer
         if (lane == 0) {
             int sc = 0, bi = 0;
+            int ps = 0, puse = 0;  // ring slot of stage sc and how many times it was filled before (sc % NSr, sc / NSr)
             for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
                 int ntg, mlo, mhi;
                 if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
@@ -760,7 +761,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                                      "r"(tile_bytes) : "memory");
                     }
                     for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
-                        const int s = sc % NSr, use = sc / NSr;
+                        const int s = ps, use = puse;
                         if (use > 0 && !pf_wait(&empty[s], (use - 1) & 1, abort_flag, a.wait_ns)) {
                             stop = true;
                             break;
@@ -773,6 +774,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                                 pf_su(ring + (size_t)s * pf::KPS * pf::BLK)),
                             "l"(ae + ((int64_t)m * a.KSN + ks) * pf::BLK), "r"(bytes), "r"(pf_su(&full[s]))
                             : "memory");
+                        if (++ps == NSr) {
+                            ps = 0;
+                            ++puse;
+                        }
                     }
                 }
                 if (stop) break;
@@ -791,6 +796,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
         // ---------------- MMA issuer: the token tile is the M side, the weight tile the N side
         if (lane == 0) {
             int sc = 0, it = 0, bi = 0;
+            int ms = 0;
+            uint32_t mph = 0;  // ring slot and phase parity of stage sc (sc % NSr, (sc / NSr) & 1)
             bool stop = false;
             const uint64_t dW0 = umma_desc(ring, 2048, 128), sW0 = umma_desc(ring + 8192, 0, 128);
             const uint64_t dT0 = umma_desc(btile, 2048, 128), sT0 = umma_desc(btile + 8192, 0, 128);
@@ -817,8 +824,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t dcol = tbase + (uint32_t)(buf * 128);
                     for (int ks = 0; ks < a.KSN; ks += pf::KPS, ++sc) {
-                        const int s = sc % NSr;
-                        if (!pf_wait(&full[s], (sc / NSr) & 1, abort_flag, a.wait_ns)) {
+                        const int s = ms;
+                        if (!pf_wait(&full[s], mph, abort_flag, a.wait_ns)) {
                             stop = true;
                             break;
                         }
@@ -830,22 +837,41 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                         const uint64_t dW = dW0 + (uint64_t)(s * pf::KPS) * kDescBlk, sW = sW0 + (uint64_t)(s * pf::KPS) * kDescBlk;
                         const uint64_t dT = dT0 + (uint64_t)ks * kDescBlk;
                         const uint32_t cW = tbase + SFW0 + (uint32_t)(s * pf::KPS * 8), cT = tbase + SFT0 + (uint32_t)(ks * 8);
+                        if (nkb == pf::KPS) {  // a full stage: no per-block predicates
 #pragma unroll
-                        for (int bq = 0; bq < pf::KPS; ++bq)
-                            if (bq < nkb) {
+                            for (int bq = 0; bq < pf::KPS; ++bq) {
                                 sf_copy(cW + bq * 8, sW + bq * kDescBlk);
                                 sf_copy(cW + bq * 8 + 4, sW + bq * kDescBlk + kDescSfHalf);
                             }
 #pragma unroll
-                        for (int bq = 0; bq < pf::KPS; ++bq)
-                            if (bq < nkb) {
+                            for (int bq = 0; bq < pf::KPS; ++bq)
 #pragma unroll
                                 for (int kb = 0; kb < 2; ++kb)
                                     mma_fp4(dcol, dT + bq * kDescBlk + kb * kDescHalf, dW + bq * kDescBlk + kb * kDescHalf,
                                             cT + bq * 8 + kb * 4, cW + bq * 8 + kb * 4, (ks | bq | kb) ? 1u : 0u);
-                            }
+                        } else {
+#pragma unroll
+                            for (int bq = 0; bq < pf::KPS; ++bq)
+                                if (bq < nkb) {
+                                    sf_copy(cW + bq * 8, sW + bq * kDescBlk);
+                                    sf_copy(cW + bq * 8 + 4, sW + bq * kDescBlk + kDescSfHalf);
+                                }
+#pragma unroll
+                            for (int bq = 0; bq < pf::KPS; ++bq)
+                                if (bq < nkb) {
+#pragma unroll
+                                    for (int kb = 0; kb < 2; ++kb)
+                                        mma_fp4(dcol, dT + bq * kDescBlk + kb * kDescHalf,
+                                                dW + bq * kDescBlk + kb * kDescHalf, cT + bq * 8 + kb * 4,
+                                                cW + bq * 8 + kb * 4, (ks | bq | kb) ? 1u : 0u);
+                                }
+                        }
                         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                          pf_su(&empty[s])) : "memory");
+                        if (++ms == NSr) {
+                            ms = 0;
+                            mph ^= 1u;
+                        }
                     }
                     if (stop) break;
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
