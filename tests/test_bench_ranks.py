@@ -89,3 +89,33 @@ def test_reference_arm_on_the_prefill_workload_reports_the_gpu_arms_unit():
     d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["config"]["workload"] == "prefill_35b" and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_keeps_each_steps_experts_when_its_store_is_full():
+    """The oracle's store of quantised experts is bounded: evicting the least recently used never drops an expert
+    the current step routes to, over more steps than the store holds."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    cfg = W.scaled(W.CONFIGS["tiny"], layers=3)
+    ref = bench.OracleToken(cfg, keep=2)
+    for s in range(6):
+        assert ref.step(s) >= 0.0
+        assert len(ref.q) <= max(2, cfg.layers * min(cfg.E, cfg.T * cfg.k))
+
+
+def test_reference_arm_stops_at_its_time_budget(monkeypatch):
+    """Asked for more steps than fit the budget, the reference arm times whole steps until the budget is spent and
+    reports how many it timed and how many were asked."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "REF_BUDGET_S", 0.0)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--config", "tiny", "--steps", "50",
+                                      "--warmup", "0"])
+    import contextlib
+    import io
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        bench.main()
+    d = json.loads([ln for ln in out.getvalue().splitlines() if ln.startswith("{")][-1])
+    assert d["steps"] == 1 and d["steps_requested"] == 50 and d["value"] > 0
