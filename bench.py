@@ -297,7 +297,7 @@ class OracleDecode:
         return self.O.lib().ora_max_threads()
 
 
-REF_BUDGET_S = 180.0  # reference arm: timed oracle seconds after which no further whole step starts
+REF_BUDGET_S = 60.0  # reference arm: timed oracle seconds after which no further whole step starts
 
 
 class OracleToken:
