@@ -124,3 +124,17 @@ def test_byte_layout():
     w8[0, :3] = [1.0, -1.0, 256.0]         # amax 256 -> X = 0
     c8, s8 = mx.quantize(w8, "mxfp8")
     assert s8.tolist() == [[127]] and c8[0, :3].tolist() == [0x38, 0xB8, 0x78]
+
+
+def test_e4m3_holds_exactly_the_powers_of_two_the_mxfp4_reencoding_uses():
+    """The MXFP4 tensor-core packing writes each block scale 2^(s - s0) as an E4M3 byte: (d + 7) << 3 for
+    d = -6 .. 8 and 1 << (d + 9) for the subnormals d = -9 .. -7.  Those bytes decode (the oracle's E4M3 table) to
+    exactly 2^d, and no E4M3 value is a power of two outside -9 .. 8: the 18 exponents s0 - 9 .. s0 + 8, a span
+    of 17 octaves."""
+    import oracle as O
+    for d in range(-9, 9):
+        b = (d + 7) << 3 if d >= -6 else 1 << (d + 9)
+        assert O.e4m3_value(b) == 2.0 ** d, d
+    vals = [O.e4m3_value(b) for b in range(0x7F)]            # every finite non-negative E4M3 value
+    pow2 = sorted({math.log2(v) for v in vals if v > 0 and math.log2(v).is_integer()})
+    assert pow2 == list(range(-9, 9))
