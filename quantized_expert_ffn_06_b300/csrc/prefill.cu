@@ -16,11 +16,12 @@
 //  2. k_pf_quant_tokens + k_pf_gather_x: each token's x quantised once, then
 //     copied in permuted order into operand tiles, with a (token, weight) table
 //     of the padded rows; the gather also zeroes the fp32 output accumulator.
-//  3. k_pf_gemm<1>: h = silu(Wg x) * (Wu x) per (expert, 128 gate/up rows,
+//  3. k_pf_gemm_res<1>: h = silu(Wg x) * (Wu x) per (expert, 128 gate/up rows,
 //     128 tokens) tile, rounded to bf16 and quantised into operand tiles.
-//  4. k_pf_gemm<2>: y = Wd h per (expert, 128 output rows, 128 tokens) tile;
-//     the epilogue adds w[t][j] * y into an fp32 accumulator of the output
-//     (red.global.add), i.e. the routing-weighted combine.
+//  4. k_pf_gemm_res<2>: y = Wd h per (expert, 128 output rows, 128 tokens)
+//     tile; the epilogue adds w[t][j] * y into an fp32 accumulator of the
+//     output (red.global.add, whole 128-byte lines through a shared-memory
+//     transpose), i.e. the routing-weighted combine.
 //  5. k_pf_out: the accumulator rounded to bf16.
 //
 // Operand tiles ("UMMA tiles"): an [R][K] NVFP4 matrix (R a multiple of 128,
@@ -33,10 +34,12 @@
 // tcgen05.cp .32x128b.warpx4 moves into TMEM (4 columns per 64 K).  A block is
 // one contiguous bulk copy.
 //
-// The GEMM kernel is persistent (one CTA per SM): warp 0 streams weight and
-// token blocks into a 3-stage shared-memory ring (cp.async.bulk + mbarriers;
-// four K blocks of each operand per copy, since a bulk copy costs about the
-// same whatever its size), warp 1 allocates TMEM and one of its threads issues
+// The GEMM kernels are persistent (one CTA per SM).  In k_pf_gemm_res (K up to
+// 2048) the token tile stays resident in shared memory while warp 0 streams the
+// weight blocks through a ring of bulk copies (cp.async.bulk + mbarriers; four
+// K blocks per copy, since a bulk copy costs about the same whatever its size);
+// k_pf_gemm_stream (longer K) streams both operands through a 3-stage ring.
+// Warp 1 allocates TMEM and one of its threads issues
 // the MMAs (two per K block, K = 64 each, scales copied to TMEM with
 // tcgen05.cp) into one of two 128-column accumulators, and warps 2-17 (four per
 // TMEM lane quadrant, 32 columns each) drain the other accumulator (tcgen05.ld)
