@@ -567,7 +567,8 @@ FT_API ft_status ft_mxfp4_pack_tiles(const uint8_t* codes, int64_t codes_ld, con
  * product code x scale x tensor scale equals the MX one exactly when the
  * matrix's non-zero blocks span at most 17 octaves (s >= largest s - 17).  A
  * block beyond that sets FT_DEVERR_RANGE (its scale is written as 0); a scale
- * byte of 255 (NaN) sets FT_DEVERR_BAD_SCALE.  Blocks whose codes are all
+ * byte of 255 (NaN) sets FT_DEVERR_BAD_SCALE, is written as 0 and does not
+ * count in s0.  Blocks whose codes are all
  * zero get scale 0.  With no non-zero block the tensor scale is 1.  Three
  * launches on `stream`; tscale[0] serves as their scratch word until the
  * last.  N and K multiples of 128, 1 <= ts_count <= 4; codes and tiles

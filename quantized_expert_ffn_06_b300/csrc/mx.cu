@@ -192,7 +192,7 @@ __device__ __forceinline__ int mxu_scale_off(int r, int j) { return 8192 + (j >>
 __device__ __forceinline__ bool mx4_block_nonzero(uint4 c) { return ((c.x | c.y | c.z | c.w) & 0x77777777u) != 0u; }
 
 // Pass 1, one thread per block: the largest scale byte over blocks with a non-zero code, into *smax (int, -1
-// initially).
+// initially).  A NaN scale byte (255) does not count: pass 2 reports it and the other blocks keep their span.
 __global__ void __launch_bounds__(256) k_mx_umma_smax(const uint8_t* __restrict__ codes, int64_t codes_ld,
                                                       const uint8_t* __restrict__ scales, int64_t scales_ld,
                                                       int64_t N, int64_t K, int* __restrict__ smax) {
@@ -201,7 +201,8 @@ __global__ void __launch_bounds__(256) k_mx_umma_smax(const uint8_t* __restrict_
     if (i < N * nb) {
         const int64_t r = i / nb, b = i - r * nb;
         const uint4 c = *reinterpret_cast<const uint4*>(codes + r * codes_ld + b * 16);
-        if (mx4_block_nonzero(c)) v = scales[r * scales_ld + b];
+        const int sb = scales[r * scales_ld + b];
+        if (sb != 255 && mx4_block_nonzero(c)) v = sb;
     }
     v = __reduce_max_sync(0xffffffffu, v);
     if ((threadIdx.x & 31) == 0 && v >= 0) atomicMax(smax, v);

@@ -280,6 +280,22 @@ def test_mxfp4_umma_exponent_span(spread):
         assert st == Q.FT_DEVERR_RANGE
 
 
+def test_mxfp4_umma_nan_scale_is_reported():
+    """A UE8M0 scale byte of 255 (NaN) sets FT_DEVERR_BAD_SCALE; the packing still finishes."""
+    rng = np.random.default_rng(5)
+    N, K = 128, 128
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scales = np.full((N, K // 32), 127, np.uint8)
+    scales[7, 2] = 255
+    tiles = torch.empty(N * K * 9 // 16, dtype=torch.uint8, device=DEV)
+    ts = torch.zeros(1, dtype=torch.float32, device=DEV)
+    assert Q.ft_device_status() == 0
+    Q.ft_mxfp4_pack_umma(torch.from_numpy(codes).to(DEV), K // 2, torch.from_numpy(scales).to(DEV), K // 32, N, K,
+                         tiles, ts, 1)
+    torch.cuda.synchronize()
+    assert Q.ft_device_status() == Q.FT_DEVERR_BAD_SCALE
+
+
 def run_prefill(cfg, umma, logits, x_bits):
     T = logits.shape[0]
     mod = PrefillLayer(cfg.E, cfg.H, cfg.I, cfg.k, T, DEV)
