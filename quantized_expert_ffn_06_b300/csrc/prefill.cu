@@ -90,6 +90,7 @@ struct PfGemmArgs {
     float* out32;            // [T][H], or nullptr: no combine
     int H;
     int nstages;             // ring stages (resident-token-tile kernel)
+    int tbufs;               // resident kernel: token-tile buffers (2: the next item's tile loads during this one)
     const int32_t* e2s;      // optional expert -> weight index (slot table); validated by the plan
     const int4* tinfo;       // [tiles] {expert, first permuted row, real rows, 0}
     float* y;                // optional [T*k][H] fp32 per-row expert outputs (tensor scale applied, no routing weight)
@@ -693,18 +694,19 @@ template <int EPI>
 __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs a) {
     extern __shared__ __align__(1024) uint8_t pf_smem[];
     uint8_t* btile = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pf_smem) + 1023) & ~(uintptr_t)1023);
-    uint8_t* ring = btile + (size_t)a.KSN * pf::BLK;
+    uint8_t* ring = btile + (size_t)a.tbufs * a.KSN * pf::BLK;  // after the token-tile buffer(s)
     float* cst = reinterpret_cast<float*>(ring + (size_t)a.nstages * pf::KPS * pf::BLK);  // combine staging (cstage)
-    __shared__ __align__(8) unsigned long long full[pf::RES_MAXNS], empty[pf::RES_MAXNS], acc_full[2], acc_empty[2], bfull,
-        bfree, never;  // never: the wait-expiry test hook's barrier, which nothing completes
+    __shared__ __align__(8) unsigned long long full[pf::RES_MAXNS], empty[pf::RES_MAXNS], acc_full[2], acc_empty[2],
+        bfull[2], bfree[2], never;  // per token-tile buffer; never: the wait-expiry test hook's barrier
     __shared__ uint32_t tmem_base;
     __shared__ int abort_s;
     volatile int* abort_flag = &abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NSr = a.nstages;
-    // TMEM columns: accumulators [0, 256), token-tile scale factors (8 per K block), then the
+    // TMEM columns: accumulators [0, 256), token-tile scale factors (8 per K block, per buffer), then the
     // weight scale factors of the ring stages (8 per K block of a stage)
-    const uint32_t SFT0 = 256, SFW0 = 256 + 8 * (uint32_t)a.KSN;
+    const int TB = a.tbufs;
+    const uint32_t SFT0 = 256, SFW0 = 256 + 8 * (uint32_t)(a.KSN * TB);
     if (tid == 0) {
         for (int s = 0; s < NSr; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&full[s])));
@@ -714,8 +716,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&acc_full[b])));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(pf_su(&acc_empty[b])), "n"(pf::EPI_WARPS));
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfull)));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfree)));
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfull[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&bfree[b])));
+        }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(pf_su(&never)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_s = 0;
@@ -741,13 +745,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
             for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
                 int ntg, mlo, mhi;
                 if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
-                // the token tile, once the previous item's MMAs have read the last one
-                if (bi > 0 && !pf_wait(&bfree, (bi - 1) & 1, abort_flag, a.wait_ns)) break;
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&bfull)), "r"(tile_bytes)
-                             : "memory");
+                // the token tile into buffer bi % TB, once the MMAs of the item that last used that buffer are done
+                const int tb = bi % TB, tuse = bi / TB;
+                if (tuse > 0 && !pf_wait(&bfree[tb], (tuse - 1) & 1, abort_flag, a.wait_ns)) break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(pf_su(&bfull[tb])),
+                             "r"(tile_bytes) : "memory");
                 asm volatile(
                     "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                        pf_su(btile)), "l"(a.B + (int64_t)ntg * a.KSN * pf::BLK), "r"(tile_bytes), "r"(pf_su(&bfull))
+                        pf_su(btile + (size_t)tb * tile_bytes)), "l"(a.B + (int64_t)ntg * a.KSN * pf::BLK), "r"(tile_bytes),
+                    "r"(pf_su(&bfull[tb]))
                     : "memory");
                 ++bi;
                 const uint8_t* ae = a.A + pf_widx(a, __ldg(a.tinfo + ntg).x) * a.a_stride;
@@ -791,8 +797,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
             for (int n = max(0, sc - NSr); n < sc; ++n)
                 while (!pf_try_wait(&full[n % NSr], (n / NSr) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
                 }
-            if (bi > 0)
-                while (!pf_try_wait(&bfull, (bi - 1) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
+            for (int n = max(0, bi - TB); n < bi; ++n)  // the last token tile of each buffer
+                while (!pf_try_wait(&bfull[n % TB], (n / TB) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
                 }
         }
     } else if (warp == 1) {
@@ -803,7 +809,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
             uint32_t mph = 0;  // ring slot and phase parity of stage sc (sc % NSr, (sc / NSr) & 1)
             bool stop = false;
             const uint64_t dW0 = umma_desc(ring, 2048, 128), sW0 = umma_desc(ring + 8192, 0, 128);
-            const uint64_t dT0 = umma_desc(btile, 2048, 128), sT0 = umma_desc(btile + 8192, 0, 128);
+            const uint64_t dTb = umma_desc(btile, 2048, 128), sTb = umma_desc(btile + 8192, 0, 128);
             for (int i = blockIdx.x; i < n_items && !stop && !*abort_flag; i += gridDim.x) {
                 int ntg, mlo, mhi;
                 if (!pf_res_item(a, i, ntg, mlo, mhi)) continue;
@@ -811,12 +817,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                 // completes: the bound runs out and every role winds down
                 if (EPI == 1 && a.wait_site == FT_WAIT_SITE_PREFILL_TOKEN && !pf_wait(&never, 0, abort_flag, a.wait_ns))
                     break;
-                if (!pf_wait(&bfull, bi & 1, abort_flag, a.wait_ns)) break;
+                const int tb = bi % TB;
+                if (!pf_wait(&bfull[tb], (bi / TB) & 1, abort_flag, a.wait_ns)) break;
+                const uint64_t dT0 = dTb + (uint64_t)tb * (tile_bytes >> 4), sT0 = sTb + (uint64_t)tb * (tile_bytes >> 4);
+                const uint32_t SFTb = SFT0 + (uint32_t)(tb * 8 * a.KSN);
                 ++bi;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 for (int ks = 0; ks < a.KSN; ++ks) {
-                    sf_copy(tbase + SFT0 + (uint32_t)(ks * 8), sT0 + (uint64_t)ks * kDescBlk);
-                    sf_copy(tbase + SFT0 + (uint32_t)(ks * 8 + 4), sT0 + (uint64_t)ks * kDescBlk + kDescSfHalf);
+                    sf_copy(tbase + SFTb + (uint32_t)(ks * 8), sT0 + (uint64_t)ks * kDescBlk);
+                    sf_copy(tbase + SFTb + (uint32_t)(ks * 8 + 4), sT0 + (uint64_t)ks * kDescBlk + kDescSfHalf);
                 }
                 for (int m = mlo; m < mhi && !stop; ++m, ++it) {
                     const int buf = it & 1, useb = it >> 1;
@@ -839,7 +848,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                         const int nkb = min(pf::KPS, a.KSN - ks);
                         const uint64_t dW = dW0 + (uint64_t)(s * pf::KPS) * kDescBlk, sW = sW0 + (uint64_t)(s * pf::KPS) * kDescBlk;
                         const uint64_t dT = dT0 + (uint64_t)ks * kDescBlk;
-                        const uint32_t cW = tbase + SFW0 + (uint32_t)(s * pf::KPS * 8), cT = tbase + SFT0 + (uint32_t)(ks * 8);
+                        const uint32_t cW = tbase + SFW0 + (uint32_t)(s * pf::KPS * 8), cT = tbase + SFTb + (uint32_t)(ks * 8);
                         if (nkb == pf::KPS) {  // a full stage: no per-block predicates
 #pragma unroll
                             for (int bq = 0; bq < pf::KPS; ++bq) {
@@ -882,7 +891,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
                 }
                 // the token tile may be replaced once this item's MMAs are done
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 pf_su(&bfree)) : "memory");
+                                 pf_su(&bfree[tb])) : "memory");
                 ++bfree_commits;
             }
         }
@@ -933,9 +942,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1) k_pf_gemm_res(const PfGemmArgs
     // all MMAs have completed once the epilogue has consumed every accumulator; on an abort
     // wait (bounded) for the last commit before the TMEM is released
     if (warp == 1 && lane == 0 && *abort_flag && bfree_commits > 0) {
+        const int lb = (bfree_commits - 1) % TB;
         // the last commit covers every MMA issued before it
         const unsigned long long t0 = pf_gt();
-        while (!pf_try_wait(&bfree, (bfree_commits - 1) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
+        while (!pf_try_wait(&bfree[lb], ((bfree_commits - 1) / TB) & 1) && pf_gt() - t0 < pf::WAIT_NS) {
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1025,8 +1035,8 @@ static void launch_pf_gemm(PfGemmArgs g, int G, cudaStream_t s) {
     int ns = 0;
     size_t extra = 0;
     g.cstage = 0;
+    g.tbufs = 1;
     if (g.KSN <= pf::RES_MAXKSN && tile + 1024 < pf::SMEM_LIMIT) {
-        const int by_tmem = (int)((pf::TMEM_COLS - 256 - 8 * (uint32_t)g.KSN) / (8 * pf::KPS));
         // the down GEMM's combine (without y rows) goes through shared memory when two stages still fit beside it
         if (EPI == 2 && g.out32 && !g.y) {
             for (int cw : {32, 16}) {
@@ -1038,13 +1048,19 @@ static void launch_pf_gemm(PfGemmArgs g, int G, cudaStream_t s) {
                 }
             }
         }
-        const int by_smem = (int)((pf::SMEM_LIMIT - 1024 - tile - extra) / stage);
+        // a second token-tile buffer when two stages still fit beside it: the next item's tile loads while this
+        // item's MMAs run
+        if (EPI == 2 && 2 * tile + 2 * stage + extra + 1024 <= pf::SMEM_LIMIT &&
+            256 + 16 * (uint32_t)g.KSN + 2 * 8 * pf::KPS <= pf::TMEM_COLS)
+            g.tbufs = 2;
+        const int by_tmem = (int)((pf::TMEM_COLS - 256 - 8 * (uint32_t)(g.KSN * g.tbufs)) / (8 * pf::KPS));
+        const int by_smem = (int)((pf::SMEM_LIMIT - 1024 - tile * g.tbufs - extra) / stage);
         ns = std::min({by_smem, by_tmem, pf::RES_MAXNS});
     }
     if (ns >= 2) {
         g.nstages = ns;
         g.parts = EPI == 1 ? 1 : 2;  // measured: whole token tiles for gate/up (one token-tile load each), halves for down
-        k_pf_gemm_res<EPI><<<G, pf::THREADS, tile + (size_t)ns * stage + extra + 1024, s>>>(g);
+        k_pf_gemm_res<EPI><<<G, pf::THREADS, tile * g.tbufs + (size_t)ns * stage + extra + 1024, s>>>(g);
     } else {
         g.cstage = 0;
         k_pf_gemm_stream<EPI><<<G, pf::THREADS, pf::SMEM, s>>>(g);
